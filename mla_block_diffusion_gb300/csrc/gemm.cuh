@@ -1,0 +1,320 @@
+// Skinny-M weight-streaming GEMM on the 5th-generation tensor core.
+//
+//   y[m, n] = sum_k W[n, k] * x[m, k]      (W bf16 [N, K] row-major, x bf16 [M, K], M = 7 * batch)
+//
+// Every linear map of the drafter has M = 7 * batch rows against a weight
+// matrix of millions of entries, so the weights are read exactly once and the
+// kernel is bound by HBM. The product is computed "swapped": the weight tile is
+// the A operand (128 output channels x 64 k, M = 128 of tcgen05.mma) and the few
+// activation rows are the B operand (N = BN, a multiple of 16). The accumulator
+// lives in TMEM (two buffers of BN fp32 columns).
+//
+// Roles (one CTA per SM, 6 warps):
+//   warp 0    TMA producer: streams W tiles (evict-first) and x tiles into a
+//             ring of shared-memory stages, completing on "full" mbarriers;
+//   warp 1    MMA issuer: one thread issues 4 x tcgen05.mma (K = 16 each) per
+//             stage and frees the stage with tcgen05.commit on "empty";
+//   warps 2-5 epilogue: tcgen05.ld the accumulator (TMEM lane = output channel),
+//             apply the output functor or write a split partial.
+//
+// Work split (stream-K): the (tile, k-block) units are divided into equal
+// contiguous ranges, one per CTA, so every SM streams the same number of
+// weight bytes. A tile covered by one CTA is finished directly from TMEM. A
+// tile split across CTAs is finished by whichever contributor arrives last
+// (atomic counter, no waiting): it sums the partials of all contributors in
+// increasing CTA order, so the result does not depend on arrival order.
+#pragma once
+
+#include "common.cuh"
+
+namespace ds {
+
+enum GemmEpi { EPI_STORE = 0, EPI_ADD = 1, EPI_SWIGLU = 2 };
+
+struct GemmParams {
+    int n_out;          // output channels
+    int K;              // reduction length
+    int M;              // valid activation rows (<= BN)
+    int KB;             // k-blocks of 64
+    int tiles;          // output tiles (128 channels, or 64 when paired)
+    long long units;    // tiles * KB
+    int grid;           // CTAs
+    int paired;         // SwiGLU: A rows 0-63 from gate, 64-127 from up
+    int epi;            // GemmEpi
+    float *out_f32;     // [M, ldo]
+    __nv_bfloat16 *out_bf16;
+    int ldo;
+    float *partials;    // [2 * grid][128][BN]
+    int *counters;      // [tiles], zero between launches
+    int *err;
+};
+
+constexpr int kGemmMaxSmem = 232448;
+
+template <int BN>
+struct GemmCfg {
+    static constexpr int kABytes = 128 * 128;  // 128 rows x 64 bf16
+    static constexpr int kBBytes = BN * 128;   // BN rows x 64 bf16
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kXchgFloats = 64 * 17;
+    static constexpr int kFixed = 1024 + kXchgFloats * 4 + 512;
+    static constexpr int kStagesFit = (kGemmMaxSmem - kFixed) / kStageBytes;
+    static constexpr int kStages = kStagesFit > 12 ? 12 : kStagesFit;
+    static constexpr int kSmemBytes = kFixed + kStages * kStageBytes;
+    static constexpr int kTmemCols = (2 * BN <= 32)    ? 32
+                                     : (2 * BN <= 64)  ? 64
+                                     : (2 * BN <= 128) ? 128
+                                     : (2 * BN <= 256) ? 256
+                                                       : 512;
+    static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "tcgen05 M=128 needs N in 16..256, step 16");
+    static_assert(kStages >= 3, "pipeline too shallow");
+};
+
+__host__ __device__ inline long long gemm_unit_begin(int c, long long units, int grid) {
+    return (long long)c * units / grid;
+}
+
+// CTA whose unit range contains unit u (ranges are non-empty: grid <= units).
+__device__ inline int gemm_cta_of_unit(long long u, long long units, int grid) {
+    int c = (int)((u * grid) / units);
+    if (c >= grid) c = grid - 1;
+    while (c + 1 < grid && gemm_unit_begin(c + 1, units, grid) <= u) ++c;
+    while (c > 0 && gemm_unit_begin(c, units, grid) > u) --c;
+    return c;
+}
+
+__device__ inline float silu_f(float g) { return g / (1.0f + __expf(-g)); }
+
+__device__ inline void gemm_store(const GemmParams &p, int n, int m, float v) {
+    float *dst = p.out_f32 + (size_t)m * p.ldo + n;
+    if (p.epi == EPI_ADD)
+        *dst += v;
+    else
+        *dst = v;
+}
+
+__device__ inline void gemm_store_swiglu(const GemmParams &p, int n, int m, float g, float u) {
+    p.out_bf16[(size_t)m * p.ldo + n] = __float2bfloat16(silu_f(g) * u);
+}
+
+template <int BN>
+__global__ void __launch_bounds__(192, 1)
+    gemm_swapab_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
+                       const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+    using C = GemmCfg<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t *sA = smem;
+    uint8_t *sB = smem + C::kStages * C::kABytes;
+    float *xchg = (float *)(sB + C::kStages * C::kBBytes);
+    uint64_t *full = (uint64_t *)(xchg + C::kXchgFloats);
+    uint64_t *empty = full + C::kStages;
+    uint64_t *tfull = empty + C::kStages;  // [2]
+    uint64_t *tempty = tfull + 2;          // [2]
+    uint64_t *done = tempty + 2;           // [1]
+    __shared__ uint32_t s_tmem;
+    __shared__ volatile int s_abort;
+    __shared__ int s_last;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int cta = blockIdx.x;
+    const long long u0 = gemm_unit_begin(cta, p.units, p.grid);
+    const long long u1 = gemm_unit_begin(cta + 1, p.units, p.grid);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], 128);
+        }
+        mbar_init(done, 1);
+        s_abort = 0;
+        fence_mbar_init();
+    }
+    if (threadIdx.x == 32) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmA2);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) tmem_alloc(&s_tmem, C::kTmemCols);
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+
+    // producer bookkeeping for the drain after an abort
+    uint32_t armed = 0, armed_par = 0;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_first();
+            long long it = 0;
+            for (long long u = u0; u < u1; ++u, ++it) {
+                const int s = (int)(it % C::kStages);
+                const uint32_t round = (uint32_t)(it / C::kStages);
+                if (!mbar_wait_bounded(&empty[s], (round & 1u) ^ 1u, &s_abort)) break;
+                const int tile = (int)(u / p.KB), kb = (int)(u % p.KB);
+                mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+                armed |= 1u << s;
+                armed_par = (armed_par & ~(1u << s)) | ((round & 1u) << s);
+                uint8_t *a = sA + s * C::kABytes;
+                if (p.paired) {
+                    tma_load_2d_hint(a, &tmA, kb * 64, tile * 64, &full[s], pol);
+                    tma_load_2d_hint(a + 8192, &tmA2, kb * 64, tile * 64, &full[s], pol);
+                } else {
+                    tma_load_2d_hint(a, &tmA, kb * 64, tile * 128, &full[s], pol);
+                    tma_load_2d_hint(a + 8192, &tmA, kb * 64, tile * 128 + 64, &full[s], pol);
+                }
+                tma_load_2d(sB + s * C::kBBytes, &tmB, kb * 64, 0, &full[s]);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(128, BN);
+            long long it = 0, u = u0;
+            int seg = 0;
+            bool ok = true;
+            while (u < u1 && ok) {
+                const int tile = (int)(u / p.KB);
+                const long long seg_end = min(u1, (long long)(tile + 1) * p.KB);
+                const int a = seg & 1;
+                if (!mbar_wait_bounded(&tempty[a], (((uint32_t)seg >> 1) & 1u) ^ 1u, &s_abort)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)(a * BN);
+                bool first = true;
+                for (; u < seg_end; ++u, ++it) {
+                    const int s = (int)(it % C::kStages);
+                    const uint32_t round = (uint32_t)(it / C::kStages);
+                    if (!mbar_wait_bounded(&full[s], round & 1u, &s_abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ad = sdesc_k_sw128(smem_u32(sA + s * C::kABytes));
+                    const uint64_t bd = sdesc_k_sw128(smem_u32(sB + s * C::kBBytes));
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_bf16(d, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), idesc,
+                                 (first && k == 0) ? 0u : 1u);
+                    first = false;
+                    mma_commit(&empty[s]);
+                }
+                if (!ok) break;
+                mma_commit(&tfull[a]);
+                ++seg;
+            }
+            // every MMA this thread issued has completed once "done" flips
+            mma_commit(done);
+            mbar_drain(done, 0);
+        }
+    } else {
+        // epilogue: warps 2..5, TMEM lane quadrant = warp % 4
+        const int q = warp & 3;
+        const int row = q * 32 + lane;
+        const int et = threadIdx.x - 64;
+        const int nch = p.paired ? 64 : 128;
+        int seg = 0;
+        long long u = u0;
+        while (u < u1) {
+            const int tile = (int)(u / p.KB);
+            const long long tbeg = (long long)tile * p.KB, tend = tbeg + p.KB;
+            const long long seg_end = min(u1, tend);
+            const bool whole = (u == tbeg) && (seg_end == tend);
+            const int a = seg & 1;
+            const bool got = mbar_wait_bounded(&tfull[a], ((uint32_t)seg >> 1) & 1u, &s_abort);
+            if (!named_bar_and(2, 128, got)) break;  // uniform exit keeps the named barriers matched
+            tc_fence_after();
+            const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * BN);
+            const int slot = (tile == (int)(u0 / p.KB)) ? 2 * cta : 2 * cta + 1;
+            for (int c0 = 0; c0 < BN; c0 += 16) {
+                float v[16];
+                tmem_ld16(taddr + (uint32_t)c0, v);
+                if (whole) {
+                    if (p.paired) {
+                        if (q >= 2) {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) xchg[(row - 64) * 17 + j] = v[j];
+                        }
+                        named_bar_sync(1, 128);
+                        const int n = tile * 64 + row;
+                        if (q < 2 && n < p.n_out) {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j)
+                                if (c0 + j < p.M) gemm_store_swiglu(p, n, c0 + j, v[j], xchg[row * 17 + j]);
+                        }
+                        named_bar_sync(1, 128);
+                    } else {
+                        const int n = tile * 128 + row;
+                        if (n < p.n_out) {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j)
+                                if (c0 + j < p.M) gemm_store(p, n, c0 + j, v[j]);
+                        }
+                    }
+                } else {
+                    float4 *dst = (float4 *)(p.partials + ((size_t)slot * 128 + row) * BN + c0);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&tempty[a]);
+            if (!whole) {
+                __threadfence();
+                named_bar_sync(1, 128);
+                const int c_lo = gemm_cta_of_unit(tbeg, p.units, p.grid);
+                const int c_hi = gemm_cta_of_unit(tend - 1, p.units, p.grid);
+                if (et == 0) {
+                    const int old = atomicAdd(&p.counters[tile], 1);
+                    s_last = (old == c_hi - c_lo);
+                    if (s_last) p.counters[tile] = 0;
+                }
+                named_bar_sync(1, 128);
+                if (s_last) {
+                    __threadfence();
+                    const int n = tile * nch + et;
+                    if (et < nch && n < p.n_out) {
+                        for (int m = 0; m < p.M; ++m) {
+                            float s1 = 0.f, s2 = 0.f;
+                            for (int cc = c_lo; cc <= c_hi; ++cc) {
+                                const int first_t = (int)(gemm_unit_begin(cc, p.units, p.grid) / p.KB);
+                                const int sl = (tile == first_t) ? 2 * cc : 2 * cc + 1;
+                                const float *src = p.partials + (size_t)sl * 128 * BN;
+                                s1 += __ldcg(src + (size_t)et * BN + m);
+                                if (p.paired) s2 += __ldcg(src + (size_t)(et + 64) * BN + m);
+                            }
+                            if (p.paired)
+                                gemm_store_swiglu(p, n, m, s1, s2);
+                            else
+                                gemm_store(p, n, m, s1);
+                        }
+                    }
+                }
+            }
+            u = seg_end;
+            ++seg;
+        }
+    }
+    __syncthreads();
+    if (s_abort) {
+        if (threadIdx.x == 0) set_error(p.err, DSPARK_ERR_TIMEOUT);
+        if (warp == 0 && lane == 0) {
+            for (int s = 0; s < C::kStages; ++s)
+                if (armed & (1u << s)) mbar_drain(&full[s], (armed_par >> s) & 1u);
+        }
+        __syncthreads();
+    }
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+}  // namespace ds

@@ -1,0 +1,93 @@
+// Internal declarations shared by the translation units of libdspark.
+#pragma once
+
+#include "common.cuh"
+
+namespace ds {
+
+// Per-pair RoPE angular frequencies (YaRN-adjusted when enabled), fp64.
+struct RopeTable {
+    double inv_freq[64];
+};
+
+struct AttnParams {
+    const __nv_bfloat16 *qt;        // [bs, R, DQK] absorbed, roped queries
+    int R;                          // block * n_heads rows per sequence
+    const __nv_bfloat16 *pool;      // [n_pages, page, DQK]
+    int n_pages, page;
+    const int32_t *page_table;      // [bs, max_pages]
+    int max_pages;
+    const int32_t *ctx_len;         // [bs]
+    int max_ctx;
+    const __nv_bfloat16 *blk_kv;    // [bs * block, DQK]
+    int block;
+    int splits, tok_per_split;      // KV split plan (tok_per_split a multiple of 64)
+    float scale_log2;               // softmax scale * log2(e)
+    float *o_lat;                   // [bs, R, DV]
+    float *part_o;                  // [bs, splits, R, DV]
+    float *part_ml;                 // [bs, splits, R, 2]
+    int *err;
+};
+
+cudaError_t launch_rmsnorm(const float *x, int ldx, const float *g, int H, float eps, __nv_bfloat16 *y, int ldy,
+                           float *y32, int ldy32, int M, int *err, cudaStream_t st);
+cudaError_t launch_latent(const float *qkv, int ld, int q_lora, int kv_lora, int d_rope, const float *g_q,
+                          const float *g_kv, float eps, const int32_t *ctx_len, int block, int max_ctx,
+                          const RopeTable &rt, __nv_bfloat16 *cq, __nv_bfloat16 *blk_kv, int M, int *err,
+                          cudaStream_t st);
+cudaError_t launch_q_absorb(const float *q, int M, int n_h, int d_nope, int d_rope, int kv_lora, int d_v,
+                            const __nv_bfloat16 *w_kvb, const int32_t *ctx_len, int block, int max_ctx,
+                            const RopeTable &rt, __nv_bfloat16 *qt, cudaStream_t st);
+cudaError_t launch_v_absorb(const float *o_lat, int M, int n_h, int d_nope, int d_v, int kv_lora,
+                            const __nv_bfloat16 *w_kvb, __nv_bfloat16 *out, cudaStream_t st);
+bool attention_supported(int dqk, int dv);
+cudaError_t launch_attention(const AttnParams &p, int bs, int dqk, int dv, cudaStream_t st);
+cudaError_t launch_confidence(const float *h_out, int H, const float *w, float bias, float *conf, int M,
+                              cudaStream_t st);
+
+// Grid-barrier words inside the workspace (zero before the first launch).
+struct SampleCtl {
+    unsigned int bar_count;
+    unsigned int bar_gen;
+};
+
+struct RolloutParams {
+    const float *z;                 // [bs, B, V]
+    const int32_t *anchor;          // [bs]
+    const __nv_bfloat16 *w1;        // [V, r]
+    const __nv_bfloat16 *w2;        // [r, V]
+    int32_t *tokens;                // [bs, B]
+    float *ell;                     // [bs, B, V]
+    int bs, B, V, r;
+    int draft_mode;
+    float T, top_p;
+    unsigned long long seed;
+    unsigned int step;
+    unsigned long long *scratch;    // zeroed by the kernel itself at start
+    SampleCtl *ctl;
+    int *err;
+};
+
+struct VerifyParams {
+    const float *P;                 // [bs, B + 1, V] target logits
+    const float *ell;               // [bs, B, V]
+    const int32_t *tokens;          // [bs, B]
+    int32_t *accept_len;            // [bs]
+    int32_t *out_tokens;            // [bs, B + 1]
+    int bs, B, V;
+    int verify_mode, draft_greedy;
+    float T, top_p;
+    unsigned long long seed;
+    unsigned int step;
+    unsigned long long *scratch;    // greedy: zero between launches; probabilistic: zeroed at start
+    SampleCtl *ctl;
+    int *err;
+};
+
+size_t rollout_scratch_words(int bs, int B, int grid);
+size_t verify_scratch_words(int bs, int B, int grid);
+cudaError_t launch_rollout(RolloutParams p, int grid, cudaStream_t st);
+cudaError_t launch_verify(VerifyParams p, int grid, cudaStream_t st);
+int sampling_max_grid(int num_sms);
+
+}  // namespace ds

@@ -1,0 +1,539 @@
+// Per-layer kernels of the DSpark draft pass other than the weight GEMMs:
+// RMSNorm, latent norms + RoPE, k_b / v_b absorption, paged latent-KV MLA
+// attention (split over the KV sequence, fixed-order combine), confidence.
+//
+// Model cards: 5 dense block-diffusion layers with non-causal attention over a
+// 7-token block, MLA with a 576-element latent per token shared with the target
+// ("Kimi-K3-DSpark-NVFP4", Original model card / Model Overview); MLA tensors
+// q_a, kv_a_mqa, k_b, v_b and split RoPE dims ("kimi-k3-dspark-gguf", Runtime
+// status); kv_b absorbed, norms high precision ("Kimi-K3-DSpark-NVFP4", What is
+// quantized to what).
+#include "internal.h"
+
+namespace ds {
+
+__device__ float block_sum(float v, float *red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+    v = warp_sum(v);
+    __syncthreads();
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    float r = (threadIdx.x < nw) ? red[threadIdx.x] : 0.f;
+    if (warp == 0) r = warp_sum(r);
+    if (threadIdx.x == 0) red[32] = r;
+    __syncthreads();
+    return red[32];
+}
+
+// ---------------------------------------------------------------------------
+// RMSNorm: y = x / sqrt(mean(x^2) + eps) * g, written as bf16 (GEMM operand)
+// and optionally fp32. One CTA per row; H a multiple of 4.
+// ---------------------------------------------------------------------------
+__global__ void rmsnorm_kernel(const float *__restrict__ x, int ldx, const float *__restrict__ g, int H, float eps,
+                               __nv_bfloat16 *__restrict__ y, int ldy, float *__restrict__ y32, int ldy32, int *err) {
+    __shared__ float red[33];
+    const int m = blockIdx.x;
+    const float4 *xr = (const float4 *)(x + (size_t)m * ldx);
+    float ss = 0.f;
+    for (int i = threadIdx.x; i < H / 4; i += blockDim.x) {
+        float4 v = xr[i];
+        ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+    }
+    ss = block_sum(ss, red);
+    if (!isfinite(ss) && threadIdx.x == 0) set_error(err, DSPARK_ERR_BAD_INPUT);
+    const float r = rsqrtf(ss / (float)H + eps);
+    const float4 *g4 = (const float4 *)g;
+    for (int i = threadIdx.x; i < H / 4; i += blockDim.x) {
+        float4 v = xr[i], gg = g4[i];
+        float4 o = make_float4(v.x * r * gg.x, v.y * r * gg.y, v.z * r * gg.z, v.w * r * gg.w);
+        __nv_bfloat162 *yb = (__nv_bfloat162 *)(y + (size_t)m * ldy + 4 * i);
+        yb[0] = __floats2bfloat162_rn(o.x, o.y);
+        yb[1] = __floats2bfloat162_rn(o.z, o.w);
+        if (y32) ((float4 *)(y32 + (size_t)m * ldy32))[i] = o;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Latent norms and RoPE of the fused q_a || kv_a output (one CTA per row):
+//   c_q = RMSNorm(qa) * g_q -> bf16 (operand of q_b)
+//   c_kv = RMSNorm(kv[:kv_lora]) * g_kv, k_r = RoPE(kv[kv_lora:], ctx_len + i)
+//   -> the block's own latent KV entries [c_kv || k_r] bf16.
+// Angles are formed in fp64 (positions reach ~10^5).
+// ---------------------------------------------------------------------------
+__global__ void latent_kernel(const float *__restrict__ qkv, int ld, int q_lora, int kv_lora, int d_rope,
+                              const float *__restrict__ g_q, const float *__restrict__ g_kv, float eps,
+                              const int32_t *__restrict__ ctx_len, int block, int max_ctx, RopeTable rt,
+                              __nv_bfloat16 *__restrict__ cq, __nv_bfloat16 *__restrict__ blk_kv, int *err) {
+    __shared__ float red[33];
+    const int m = blockIdx.x;
+    const int b = m / block, i = m % block;
+    const float *row = qkv + (size_t)m * ld;
+    float sq = 0.f, sk = 0.f;
+    for (int j = threadIdx.x; j < q_lora; j += blockDim.x) sq += row[j] * row[j];
+    for (int j = threadIdx.x; j < kv_lora; j += blockDim.x) sk += row[q_lora + j] * row[q_lora + j];
+    sq = block_sum(sq, red);
+    sk = block_sum(sk, red);
+    if ((!isfinite(sq) || !isfinite(sk)) && threadIdx.x == 0) set_error(err, DSPARK_ERR_BAD_INPUT);
+    const float rq = rsqrtf(sq / (float)q_lora + eps), rk = rsqrtf(sk / (float)kv_lora + eps);
+    for (int j = threadIdx.x; j < q_lora; j += blockDim.x)
+        cq[(size_t)m * q_lora + j] = __float2bfloat16(row[j] * rq * g_q[j]);
+    const int kvd = kv_lora + d_rope;
+    for (int j = threadIdx.x; j < kv_lora; j += blockDim.x)
+        blk_kv[(size_t)m * kvd + j] = __float2bfloat16(row[q_lora + j] * rk * g_kv[j]);
+    int c = ctx_len[b];
+    if (c < 0 || c > max_ctx) {
+        if (threadIdx.x == 0) set_error(err, DSPARK_ERR_OOB);
+        c = 0;
+    }
+    const double pos = (double)(c + i);
+    for (int p = threadIdx.x; p < d_rope / 2; p += blockDim.x) {
+        double s, co;
+        sincos(pos * rt.inv_freq[p], &s, &co);
+        const float fs = (float)s, fc = (float)co;
+        const float x0 = row[q_lora + kv_lora + 2 * p], x1 = row[q_lora + kv_lora + 2 * p + 1];
+        blk_kv[(size_t)m * kvd + kv_lora + 2 * p] = __float2bfloat16(x0 * fc - x1 * fs);
+        blk_kv[(size_t)m * kvd + kv_lora + 2 * p + 1] = __float2bfloat16(x0 * fs + x1 * fc);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// q absorption: Q_h = [W_kb,h^T q_nope,h || RoPE(q_rope,h)] per row and head,
+// bf16 [M, n_h, kv_lora + d_rope]. Grid (n_h, ceil(M / 16)); each thread owns
+// two latent columns and accumulates 16 rows over d_nope in fp32.
+// ---------------------------------------------------------------------------
+constexpr int kAbsorbRows = 16;
+
+__global__ void q_absorb_kernel(const float *__restrict__ q, int M, int n_h, int d_nope, int d_rope, int kv_lora,
+                                int d_v, const __nv_bfloat16 *__restrict__ w_kvb, const int32_t *__restrict__ ctx_len,
+                                int block, int max_ctx, RopeTable rt, __nv_bfloat16 *__restrict__ qt) {
+    extern __shared__ float sq[];  // [kAbsorbRows][d_nope]
+    const int h = blockIdx.x, m0 = blockIdx.y * kAbsorbRows;
+    const int qhd = d_nope + d_rope, kvd = kv_lora + d_rope;
+    for (int idx = threadIdx.x; idx < kAbsorbRows * d_nope; idx += blockDim.x) {
+        const int mm = idx / d_nope, d = idx % d_nope, m = m0 + mm;
+        sq[idx] = (m < M) ? q[((size_t)m * n_h + h) * qhd + d] : 0.f;
+    }
+    __syncthreads();
+    const __nv_bfloat16 *W = w_kvb + (size_t)h * (d_nope + d_v) * kv_lora;
+    for (int c = 2 * threadIdx.x; c < kv_lora; c += 2 * blockDim.x) {
+        float a0[kAbsorbRows], a1[kAbsorbRows];
+#pragma unroll
+        for (int mm = 0; mm < kAbsorbRows; ++mm) a0[mm] = a1[mm] = 0.f;
+        for (int d = 0; d < d_nope; ++d) {
+            const float2 w = __bfloat1622float2(*(const __nv_bfloat162 *)(W + (size_t)d * kv_lora + c));
+#pragma unroll
+            for (int mm = 0; mm < kAbsorbRows; ++mm) {
+                const float s = sq[mm * d_nope + d];
+                a0[mm] = fmaf(w.x, s, a0[mm]);
+                a1[mm] = fmaf(w.y, s, a1[mm]);
+            }
+        }
+#pragma unroll
+        for (int mm = 0; mm < kAbsorbRows; ++mm) {
+            const int m = m0 + mm;
+            if (m < M)
+                *(__nv_bfloat162 *)(qt + ((size_t)m * n_h + h) * kvd + c) = __floats2bfloat162_rn(a0[mm], a1[mm]);
+        }
+    }
+    const int np = d_rope / 2;
+    for (int idx = threadIdx.x; idx < kAbsorbRows * np; idx += blockDim.x) {
+        const int mm = idx / np, p = idx % np, m = m0 + mm;
+        if (m >= M) continue;
+        int c = ctx_len[m / block];
+        if (c < 0 || c > max_ctx) c = 0;
+        double s, co;
+        sincos((double)(c + m % block) * rt.inv_freq[p], &s, &co);
+        const float fs = (float)s, fc = (float)co;
+        const float *src = q + ((size_t)m * n_h + h) * qhd + d_nope;
+        const float x0 = src[2 * p], x1 = src[2 * p + 1];
+        __nv_bfloat16 *dst = qt + ((size_t)m * n_h + h) * kvd + kv_lora;
+        dst[2 * p] = __float2bfloat16(x0 * fc - x1 * fs);
+        dst[2 * p + 1] = __float2bfloat16(x0 * fs + x1 * fc);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// v absorption: o_h = W_vb,h o_lat,h -> bf16 [M, n_h * d_v] (operand of o_proj).
+// Grid (n_h, ceil(M / 16)); a warp per output channel e, lanes over the latent.
+// ---------------------------------------------------------------------------
+__global__ void v_absorb_kernel(const float *__restrict__ o_lat, int M, int n_h, int d_nope, int d_v, int kv_lora,
+                                const __nv_bfloat16 *__restrict__ w_kvb, __nv_bfloat16 *__restrict__ out) {
+    extern __shared__ float so[];  // [kAbsorbRows][kv_lora]
+    const int h = blockIdx.x, m0 = blockIdx.y * kAbsorbRows;
+    for (int idx = threadIdx.x; idx < kAbsorbRows * kv_lora; idx += blockDim.x) {
+        const int mm = idx / kv_lora, c = idx % kv_lora, m = m0 + mm;
+        so[idx] = (m < M) ? o_lat[((size_t)m * n_h + h) * kv_lora + c] : 0.f;
+    }
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    for (int e = warp; e < d_v; e += nw) {
+        const __nv_bfloat16 *W = w_kvb + ((size_t)h * (d_nope + d_v) + d_nope + e) * kv_lora;
+        float acc[kAbsorbRows];
+#pragma unroll
+        for (int mm = 0; mm < kAbsorbRows; ++mm) acc[mm] = 0.f;
+        for (int c = 2 * lane; c < kv_lora; c += 64) {
+            const float2 w = __bfloat1622float2(*(const __nv_bfloat162 *)(W + c));
+#pragma unroll
+            for (int mm = 0; mm < kAbsorbRows; ++mm)
+                acc[mm] = fmaf(w.x, so[mm * kv_lora + c], fmaf(w.y, so[mm * kv_lora + c + 1], acc[mm]));
+        }
+#pragma unroll
+        for (int mm = 0; mm < kAbsorbRows; ++mm) {
+            const float v = warp_sum(acc[mm]);
+            const int m = m0 + mm;
+            if (lane == 0 && m < M) out[(size_t)m * n_h * d_v + (size_t)h * d_v + e] = __float2bfloat16(v);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// MLA attention over the paged latent cache plus the block's own latents.
+//
+// All block * n_h query rows of a sequence share one latent key/value per token
+// (K_j = [c_kv,j || k_r,j], V_j = c_kv,j), so every row of a CTA attends to the
+// same 64-token chunks. A CTA owns 64 query rows and one contiguous range of
+// tokens (split of the KV sequence); 8 warps: warp w computes the scores of
+// rows 16*(w%4).. for the full key width and the output columns of half (w/4)
+// of the latent. Scores and P.V use mma.sync m16n8k16 (bf16 in, fp32
+// accumulate); the softmax is the online (running max) form in base 2.
+// Tokens: j < ctx from the page pool, ctx <= j < ctx + block from the block
+// latents; non-causal, so nothing is masked except past the range end.
+// ---------------------------------------------------------------------------
+DS_DEVINL void cp_async16(void *smem, const void *gmem, int src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem)), "l"(gmem), "r"(src_bytes)
+                 : "memory");
+}
+DS_DEVINL void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+DS_DEVINL void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+DS_DEVINL void ldsm_x4(uint32_t (&r)[4], const void *p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(smem_u32(p)));
+}
+DS_DEVINL void ldsm_x4_t(uint32_t (&r)[4], const void *p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(smem_u32(p)));
+}
+DS_DEVINL void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, "
+        "%2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+DS_DEVINL uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *(uint32_t *)&v;
+}
+
+template <int DQK, int DV>
+struct AttnCfg {
+    static constexpr int kRows = 64;
+    static constexpr int kTok = 64;
+    static constexpr int kPitch = DQK + 8;  // bf16 per smem row: +16 B keeps ldmatrix conflict-free
+    static constexpr int kQBytes = kRows * kPitch * 2;
+    static constexpr int kKVBytes = kTok * kPitch * 2;
+    static constexpr int kSmem = kQBytes + 2 * kKVBytes;
+    static constexpr int kNT = DV / 2 / 8;   // O n8-tiles per warp
+    static constexpr int kChunks = DQK / 8;  // 16-byte pieces per row
+    static_assert(DQK % 16 == 0 && DV % 32 == 0 && DV <= DQK, "latent dims");
+};
+
+template <int DQK, int DV>
+__global__ void __launch_bounds__(256, 1) mla_attention_kernel(const AttnParams p) {
+    using C = AttnCfg<DQK, DV>;
+    extern __shared__ __align__(16) uint8_t smem[];
+    __nv_bfloat16 *sQ = (__nv_bfloat16 *)smem;
+    __nv_bfloat16 *sKV = (__nv_bfloat16 *)(smem + C::kQBytes);
+
+    const int b = blockIdx.z, split = blockIdx.y, r0 = blockIdx.x * C::kRows;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int ctx = p.ctx_len[b];
+    if (ctx < 0 || ctx > p.max_ctx) {
+        if (threadIdx.x == 0) set_error(p.err, DSPARK_ERR_OOB);
+        ctx = 0;
+    }
+    const int ntok = ctx + p.block;
+    const int j_begin = split * p.tok_per_split;
+    const int j_end = min(ntok, j_begin + p.tok_per_split);
+    const int nchunks = j_end > j_begin ? (j_end - j_begin + C::kTok - 1) / C::kTok : 0;
+
+    const __nv_bfloat16 *qbase = p.qt + (size_t)b * p.R * DQK;
+    for (int idx = threadIdx.x; idx < C::kRows * C::kChunks; idx += blockDim.x) {
+        const int rr = idx / C::kChunks, ch = idx % C::kChunks, r = r0 + rr;
+        const bool ok = r < p.R;
+        cp_async16(sQ + rr * C::kPitch + ch * 8, qbase + (size_t)(ok ? r : 0) * DQK + ch * 8, ok ? 16 : 0);
+    }
+    auto load_chunk = [&](int ci, int buf) {
+        __nv_bfloat16 *dst = sKV + buf * (C::kKVBytes / 2);
+        const int j0 = j_begin + ci * C::kTok;
+        for (int idx = threadIdx.x; idx < C::kTok * C::kChunks; idx += blockDim.x) {
+            const int t = idx / C::kChunks, ch = idx % C::kChunks, j = j0 + t;
+            const __nv_bfloat16 *src = p.blk_kv;
+            int bytes = 0;
+            if (j < j_end) {
+                if (j < ctx) {
+                    const int pg = p.page_table[(size_t)b * p.max_pages + j / p.page];
+                    if (pg >= 0 && pg < p.n_pages) {
+                        src = p.pool + ((size_t)pg * p.page + (j % p.page)) * DQK + ch * 8;
+                        bytes = 16;
+                    } else if (ch == 0) {
+                        set_error(p.err, DSPARK_ERR_OOB);
+                    }
+                } else {
+                    src = p.blk_kv + ((size_t)b * p.block + (j - ctx)) * DQK + ch * 8;
+                    bytes = 16;
+                }
+            }
+            cp_async16(dst + t * C::kPitch + ch * 8, src, bytes);
+        }
+    };
+    if (nchunks > 0) load_chunk(0, 0);
+    cp_async_commit();
+
+    const int rg = warp & 3, vh = warp >> 2;
+    const int g = lane >> 2, tq = lane & 3;
+    float o[C::kNT][4];
+#pragma unroll
+    for (int i = 0; i < C::kNT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
+
+    for (int ci = 0; ci < nchunks; ++ci) {
+        if (ci + 1 < nchunks) load_chunk(ci + 1, (ci + 1) & 1);
+        cp_async_commit();
+        cp_async_wait<1>();
+        __syncthreads();
+        const __nv_bfloat16 *kv = sKV + (ci & 1) * (C::kKVBytes / 2);
+        float s[8][4];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
+#pragma unroll 4
+        for (int kk = 0; kk < DQK / 16; ++kk) {
+            uint32_t a[4];
+            ldsm_x4(a, sQ + (rg * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * C::kPitch + kk * 16 + (lane >> 4) * 8);
+#pragma unroll
+            for (int np = 0; np < 4; ++np) {
+                uint32_t bb[4];
+                ldsm_x4(bb, kv + (np * 16 + (lane & 7) + ((lane >> 4) << 3)) * C::kPitch + kk * 16 +
+                                ((lane >> 3) & 1) * 8);
+                mma16816(s[2 * np], a, bb[0], bb[1]);
+                mma16816(s[2 * np + 1], a, bb[2], bb[3]);
+            }
+        }
+        const int j0 = j_begin + ci * C::kTok;
+        float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int j = j0 + nt * 8 + 2 * tq + (e & 1);
+                s[nt][e] = (j < j_end) ? s[nt][e] * p.scale_log2 : -INFINITY;
+                mx[e >> 1] = fmaxf(mx[e >> 1], s[nt][e]);
+            }
+        }
+        float corr[2], base[2];
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+            mx[h2] = fmaxf(mx[h2], __shfl_xor_sync(0xffffffffu, mx[h2], 1));
+            mx[h2] = fmaxf(mx[h2], __shfl_xor_sync(0xffffffffu, mx[h2], 2));
+            const float mn = fmaxf(mrow[h2], mx[h2]);
+            base[h2] = (mn == -INFINITY) ? 0.f : mn;
+            corr[h2] = exp2f(mrow[h2] - base[h2]);
+            mrow[h2] = mn;
+        }
+        float ls[2] = {0.f, 0.f};
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                s[nt][e] = exp2f(s[nt][e] - base[e >> 1]);
+                ls[e >> 1] += s[nt][e];
+            }
+        }
+        lrow[0] = lrow[0] * corr[0] + ls[0];
+        lrow[1] = lrow[1] * corr[1] + ls[1];
+#pragma unroll
+        for (int nt = 0; nt < C::kNT; ++nt) {
+            o[nt][0] *= corr[0];
+            o[nt][1] *= corr[0];
+            o[nt][2] *= corr[1];
+            o[nt][3] *= corr[1];
+        }
+#pragma unroll
+        for (int kt = 0; kt < 4; ++kt) {
+            uint32_t pa[4];
+            pa[0] = pack_bf16(s[2 * kt][0], s[2 * kt][1]);
+            pa[1] = pack_bf16(s[2 * kt][2], s[2 * kt][3]);
+            pa[2] = pack_bf16(s[2 * kt + 1][0], s[2 * kt + 1][1]);
+            pa[3] = pack_bf16(s[2 * kt + 1][2], s[2 * kt + 1][3]);
+#pragma unroll
+            for (int ntp = 0; ntp < C::kNT / 2; ++ntp) {
+                uint32_t vb[4];
+                ldsm_x4_t(vb, kv + (kt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * C::kPitch + vh * (DV / 2) +
+                                  ntp * 16 + (lane >> 4) * 8);
+                mma16816(o[2 * ntp], pa, vb[0], vb[1]);
+                mma16816(o[2 * ntp + 1], pa, vb[2], vb[3]);
+            }
+        }
+        __syncthreads();
+    }
+    cp_async_wait<0>();
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2) {
+        lrow[h2] += __shfl_xor_sync(0xffffffffu, lrow[h2], 1);
+        lrow[h2] += __shfl_xor_sync(0xffffffffu, lrow[h2], 2);
+    }
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2) {
+        const int r = r0 + rg * 16 + g + 8 * h2;
+        if (r >= p.R) continue;
+        if (p.splits == 1) {
+            const float inv = lrow[h2] > 0.f ? 1.f / lrow[h2] : 0.f;
+            float *dst = p.o_lat + ((size_t)b * p.R + r) * DV + vh * (DV / 2);
+#pragma unroll
+            for (int nt = 0; nt < C::kNT; ++nt)
+                *(float2 *)(dst + nt * 8 + 2 * tq) = make_float2(o[nt][2 * h2] * inv, o[nt][2 * h2 + 1] * inv);
+        } else {
+            const size_t pr = ((size_t)b * p.splits + split) * p.R + r;
+            float *dst = p.part_o + pr * DV + vh * (DV / 2);
+#pragma unroll
+            for (int nt = 0; nt < C::kNT; ++nt)
+                *(float2 *)(dst + nt * 8 + 2 * tq) = make_float2(o[nt][2 * h2], o[nt][2 * h2 + 1]);
+            if (vh == 0 && tq == 0) *(float2 *)(p.part_ml + pr * 2) = make_float2(mrow[h2], lrow[h2]);
+        }
+    }
+}
+
+// Fixed-order merge of the split partials: o = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s.
+__global__ void attn_combine_kernel(const float *__restrict__ part_o, const float *__restrict__ part_ml, int splits,
+                                    int R, int DV, float *__restrict__ o_lat) {
+    const int r = blockIdx.x, b = blockIdx.y;
+    const size_t base = (size_t)b * splits * R + r;
+    float M = -INFINITY;
+    for (int s = 0; s < splits; ++s) {
+        const float ls = part_ml[(base + (size_t)s * R) * 2 + 1];
+        if (ls > 0.f) M = fmaxf(M, part_ml[(base + (size_t)s * R) * 2]);
+    }
+    float den = 0.f;
+    for (int s = 0; s < splits; ++s) {
+        const float ms = part_ml[(base + (size_t)s * R) * 2], ls = part_ml[(base + (size_t)s * R) * 2 + 1];
+        if (ls > 0.f) den += exp2f(ms - M) * ls;
+    }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    for (int c = threadIdx.x * 4; c < DV; c += blockDim.x * 4) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int s = 0; s < splits; ++s) {
+            const float ms = part_ml[(base + (size_t)s * R) * 2], ls = part_ml[(base + (size_t)s * R) * 2 + 1];
+            if (!(ls > 0.f)) continue;
+            const float w = exp2f(ms - M);
+            const float4 v = *(const float4 *)(part_o + (base + (size_t)s * R) * DV + c);
+            acc.x += w * v.x;
+            acc.y += w * v.y;
+            acc.z += w * v.z;
+            acc.w += w * v.w;
+        }
+        *(float4 *)(o_lat + ((size_t)b * R + r) * DV + c) =
+            make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    }
+}
+
+// Confidence head: c = sigmoid(w . h_out + b) per block row.
+__global__ void confidence_kernel(const float *__restrict__ h_out, int H, const float *__restrict__ w, float bias,
+                                  float *__restrict__ conf) {
+    __shared__ float red[33];
+    const int m = blockIdx.x;
+    float acc = 0.f;
+    for (int i = threadIdx.x; i < H; i += blockDim.x) acc = fmaf(w[i], h_out[(size_t)m * H + i], acc);
+    acc = block_sum(acc, red);
+    if (threadIdx.x == 0) conf[m] = 1.f / (1.f + expf(-(acc + bias)));
+}
+
+// ---------------------------------------------------------------------------
+// Host-side launch wrappers
+// ---------------------------------------------------------------------------
+cudaError_t launch_rmsnorm(const float *x, int ldx, const float *g, int H, float eps, __nv_bfloat16 *y, int ldy,
+                           float *y32, int ldy32, int M, int *err, cudaStream_t st) {
+    rmsnorm_kernel<<<M, 256, 0, st>>>(x, ldx, g, H, eps, y, ldy, y32, ldy32, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_latent(const float *qkv, int ld, int q_lora, int kv_lora, int d_rope, const float *g_q,
+                          const float *g_kv, float eps, const int32_t *ctx_len, int block, int max_ctx,
+                          const RopeTable &rt, __nv_bfloat16 *cq, __nv_bfloat16 *blk_kv, int M, int *err,
+                          cudaStream_t st) {
+    latent_kernel<<<M, 256, 0, st>>>(qkv, ld, q_lora, kv_lora, d_rope, g_q, g_kv, eps, ctx_len, block, max_ctx, rt, cq,
+                                     blk_kv, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_q_absorb(const float *q, int M, int n_h, int d_nope, int d_rope, int kv_lora, int d_v,
+                            const __nv_bfloat16 *w_kvb, const int32_t *ctx_len, int block, int max_ctx,
+                            const RopeTable &rt, __nv_bfloat16 *qt, cudaStream_t st) {
+    dim3 grid(n_h, (M + kAbsorbRows - 1) / kAbsorbRows);
+    int threads = kv_lora / 2;
+    if (threads > 256) threads = 256;
+    if (threads < 32) threads = 32;
+    const size_t smem = (size_t)kAbsorbRows * d_nope * sizeof(float);
+    q_absorb_kernel<<<grid, threads, smem, st>>>(q, M, n_h, d_nope, d_rope, kv_lora, d_v, w_kvb, ctx_len, block,
+                                                 max_ctx, rt, qt);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_v_absorb(const float *o_lat, int M, int n_h, int d_nope, int d_v, int kv_lora,
+                            const __nv_bfloat16 *w_kvb, __nv_bfloat16 *out, cudaStream_t st) {
+    dim3 grid(n_h, (M + kAbsorbRows - 1) / kAbsorbRows);
+    const size_t smem = (size_t)kAbsorbRows * kv_lora * sizeof(float);
+    v_absorb_kernel<<<grid, 256, smem, st>>>(o_lat, M, n_h, d_nope, d_v, kv_lora, w_kvb, out);
+    return cudaGetLastError();
+}
+
+template <int DQK, int DV>
+static cudaError_t launch_attn_t(const AttnParams &p, int bs, int qtiles, cudaStream_t st) {
+    using C = AttnCfg<DQK, DV>;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(mla_attention_kernel<DQK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::kSmem);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    dim3 grid(qtiles, p.splits, bs);
+    mla_attention_kernel<DQK, DV><<<grid, 256, C::kSmem, st>>>(p);
+    return cudaGetLastError();
+}
+
+bool attention_supported(int dqk, int dv) {
+    return (dqk == 576 && dv == 512) || (dqk == 80 && dv == 64) || (dqk == 160 && dv == 128) ||
+           (dqk == 288 && dv == 256);
+}
+
+cudaError_t launch_attention(const AttnParams &p, int bs, int dqk, int dv, cudaStream_t st) {
+    const int qtiles = (p.R + 63) / 64;
+    cudaError_t e;
+    if (dqk == 576 && dv == 512)
+        e = launch_attn_t<576, 512>(p, bs, qtiles, st);
+    else if (dqk == 80 && dv == 64)
+        e = launch_attn_t<80, 64>(p, bs, qtiles, st);
+    else if (dqk == 160 && dv == 128)
+        e = launch_attn_t<160, 128>(p, bs, qtiles, st);
+    else if (dqk == 288 && dv == 256)
+        e = launch_attn_t<288, 256>(p, bs, qtiles, st);
+    else
+        return cudaErrorInvalidValue;
+    if (e != cudaSuccess || p.splits == 1) return e;
+    attn_combine_kernel<<<dim3(p.R, bs), 128, 0, st>>>(p.part_o, p.part_ml, p.splits, p.R, dv, p.o_lat);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_confidence(const float *h_out, int H, const float *w, float bias, float *conf, int M,
+                              cudaStream_t st) {
+    confidence_kernel<<<M, 256, 0, st>>>(h_out, H, w, bias, conf);
+    return cudaGetLastError();
+}
+
+}  // namespace ds

@@ -1,0 +1,736 @@
+// Markov rollout and lossless verification for the DSpark step.
+//
+// Model cards: a low-rank sequential Markov head drafts the 7 tokens of a
+// block ("Kimi-K3-DSpark-NVFP4", Original model card / Model Overview; Markov
+// rank 256, "Kimi K3 DSpark Q8_0 GGUF", Architecture metadata); the target
+// verifies them in one pass and the output distribution equals the target's
+// ("kimi-k3-dspark-gguf", intro); greedy or probabilistic draft sampling and
+// an argmax match at temperature 0 ("Kimi-K3-DSpark-NVFP4", Sampling options).
+//
+// Every decision is made in exact integers on 2^32-scaled weights so that it
+// is reproducible bit for bit: for a logit row l at temperature T,
+//   y_v = l_v / T, m = max y, E_v = floor(2^32 * exp^(y_v - m)),
+// where exp^ is this library's own fp32 exp (Cody-Waite reduction by ln 2 with
+// a 16-bit head, the degree-7 Taylor polynomial in Horner form with fused
+// multiply-adds, then scaling by 2^n). The top-p nucleus is the shortest run of
+// keys (E_v << 18 | (2^18 - 1 - v)) in descending order whose weight reaches
+// tau = max(1, floor(S * P32 / 2^32)); it is found here by an 8-bit radix
+// select over the grid. Draws use 24-bit uniforms from Philox4x32-10 (Salmon et
+// al., SC'11) keyed by the seed with counter (step, seq, pos, purpose) and pick
+// the smallest id whose running weight (ascending ids) exceeds
+// floor(total * W / 2^24).
+//
+// The rollout and the probabilistic verify run cooperatively (all CTAs
+// resident) and synchronise through a bounded grid barrier in the workspace.
+#include "internal.h"
+
+namespace ds {
+
+constexpr int kSampThreads = 512;
+constexpr int kRowsPerGroup = 8;    // rows whose histograms share one pass
+constexpr int kRadixPasses = 7;     // keys < 2^51, digits at bits 48, 40, ..., 0
+constexpr int kMaxSampBs = 32;
+
+// ---------------------------------------------------------------------------
+// Counter-based uniforms: Philox4x32-10, first output word.
+// ---------------------------------------------------------------------------
+DS_DEVINL uint32_t philox_word(unsigned long long seed, uint32_t seq, uint32_t step, uint32_t pos, uint32_t purpose) {
+    uint32_t c0 = step, c1 = seq, c2 = pos, c3 = purpose;
+    uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
+#pragma unroll
+    for (int round = 0; round < 10; ++round) {
+        if (round) {
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
+        }
+        const uint32_t lo0 = 0xD2511F53u * c0, hi0 = __umulhi(0xD2511F53u, c0);
+        const uint32_t lo1 = 0xCD9E8D57u * c2, hi1 = __umulhi(0xCD9E8D57u, c2);
+        const uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+        c0 = n0;
+        c1 = lo1;
+        c2 = n2;
+        c3 = lo0;
+    }
+    return c0;
+}
+
+// ---------------------------------------------------------------------------
+// Own fp32 exp for x <= 0 (every step one IEEE operation).
+// ---------------------------------------------------------------------------
+DS_DEVINL float exp_hat(float x) {
+    if (!(x >= -23.0f)) return 0.0f;
+    const float n = rintf(__fmul_rn(x, 1.44269502162933349609375f));
+    float r = __fmaf_rn(-n, 0.693145751953125f, x);
+    r = __fmaf_rn(-n, 1.428606765330187045037746429443359375e-06f, r);
+    float p = 1.98412701138295233249664306640625e-04f;
+    p = __fmaf_rn(p, r, 1.388888922519981861114501953125e-03f);
+    p = __fmaf_rn(p, r, 8.333333767950534820556640625e-03f);
+    p = __fmaf_rn(p, r, 4.16666679084300994873046875e-02f);
+    p = __fmaf_rn(p, r, 1.66666671633720397949218750e-01f);
+    p = __fmaf_rn(p, r, 0.5f);
+    p = __fmaf_rn(p, r, 1.0f);
+    p = __fmaf_rn(p, r, 1.0f);
+    return __fmul_rn(p, __int_as_float(((int)n + 127) << 23));
+}
+
+DS_DEVINL unsigned long long weight_of(float l, float T, float m) {
+    const float y = __fdiv_rn(l, T);
+    const float e = exp_hat(__fsub_rn(y, m));
+    return (unsigned long long)__fmul_rn(e, 4294967296.0f);
+}
+
+DS_DEVINL unsigned long long key_of(unsigned long long E, int v) {
+    return (E << 18) | (unsigned long long)((1u << 18) - 1u - (uint32_t)v);
+}
+
+// Order-preserving map of fp32 to uint32 (NaN excluded by the callers).
+DS_DEVINL uint32_t f2ord(float f) {
+    const uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+DS_DEVINL float ord2f(uint32_t o) { return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o); }
+
+// Greedy key: larger value first, lower id on ties (-0 counts as +0).
+DS_DEVINL unsigned long long argmax_key(float l, int v) {
+    if (l == 0.0f) l = 0.0f;
+    return ((unsigned long long)f2ord(l) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)v);
+}
+DS_DEVINL int argmax_token(unsigned long long key) { return (int)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull)); }
+
+DS_DEVINL unsigned long long top_p_q32(float top_p) {
+    if (!(top_p > 0.0f)) return 0ull;
+    if (top_p >= 1.0f) return 1ull << 32;
+    return (unsigned long long)((double)top_p * 4294967296.0);
+}
+
+// ---------------------------------------------------------------------------
+// Block reductions
+// ---------------------------------------------------------------------------
+DS_DEVINL unsigned long long warp_max_u64(unsigned long long v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long w = __shfl_xor_sync(0xffffffffu, v, o);
+        v = w > v ? w : v;
+    }
+    return v;
+}
+DS_DEVINL unsigned long long warp_sum_u64(unsigned long long v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ unsigned long long block_max_u64(unsigned long long v, unsigned long long *red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    v = warp_max_u64(v);
+    __syncthreads();
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    unsigned long long r = (threadIdx.x < (blockDim.x >> 5)) ? red[threadIdx.x] : 0ull;
+    if (warp == 0) r = warp_max_u64(r);
+    if (threadIdx.x == 0) red[32] = r;
+    __syncthreads();
+    return red[32];
+}
+__device__ unsigned long long block_sum_u64(unsigned long long v, unsigned long long *red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    v = warp_sum_u64(v);
+    __syncthreads();
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    unsigned long long r = (threadIdx.x < (blockDim.x >> 5)) ? red[threadIdx.x] : 0ull;
+    if (warp == 0) r = warp_sum_u64(r);
+    if (threadIdx.x == 0) red[32] = r;
+    __syncthreads();
+    return red[32];
+}
+
+// ---------------------------------------------------------------------------
+// Bounded grid barrier (all CTAs resident: cooperative launch). On expiry the
+// error word gets DSPARK_ERR_TIMEOUT and every later barrier returns false.
+// ---------------------------------------------------------------------------
+__device__ bool grid_barrier(SampleCtl *ctl, volatile int *s_fail, int *err) {
+    __syncthreads();
+    if (threadIdx.x == 0 && !*s_fail) {
+        volatile unsigned int *genp = &ctl->bar_gen;
+        const unsigned int gen = *genp;
+        __threadfence();
+        const unsigned int arrived = atomicAdd(&ctl->bar_count, 1u) + 1u;
+        if (arrived == gridDim.x) {
+            atomicExch(&ctl->bar_count, 0u);
+            __threadfence();
+            atomicAdd(&ctl->bar_gen, 1u);
+        } else {
+            const unsigned long long t0 = globaltimer();
+            while (*genp == gen) {
+                if (globaltimer() - t0 > kWaitLimitNs) {
+                    set_error(err, DSPARK_ERR_TIMEOUT);
+                    *s_fail = 1;
+                    break;
+                }
+                __nanosleep(64);
+            }
+        }
+        __threadfence();
+    }
+    __syncthreads();
+    return !*s_fail;
+}
+
+// Pair slice [lo, hi) of this CTA over npairs pairs of vocabulary ids.
+DS_DEVINL void pair_slice(int npairs, int &lo, int &hi) {
+    lo = (int)((long long)blockIdx.x * npairs / gridDim.x);
+    hi = (int)((long long)(blockIdx.x + 1) * npairs / gridDim.x);
+}
+
+// ---------------------------------------------------------------------------
+// Exact nucleus of up to kRowsPerGroup rows by radix select over the grid.
+// Row r has logits rowp[r] (V entries) and its max ymax[r] of l / T known.
+// Produces kstar[r], Sn[r] in the shared memory of every CTA (identical).
+// ---------------------------------------------------------------------------
+struct NucleusSmem {
+    unsigned long long hist[kRowsPerGroup][256];
+    unsigned long long prefix[kRowsPerGroup];
+    unsigned long long above[kRowsPerGroup];
+    unsigned long long tau[kRowsPerGroup];
+    unsigned long long kstar[kRowsPerGroup];
+    unsigned long long Sn[kRowsPerGroup];
+    unsigned long long last_bin[kRowsPerGroup];
+    float ymax[kRowsPerGroup];
+    unsigned long long red[33];
+};
+
+struct DrawSmem {
+    unsigned long long lo[kSampThreads], hi[kSampThreads];
+    unsigned long long tot[4];
+};
+
+// gS: [nrows] global sums; gH: [kRadixPasses][nrows][256] global histograms (zero on entry).
+__device__ bool group_nucleus(const float *const *rowp, int nrows, int V, float T, float top_p, NucleusSmem &sm,
+                              unsigned long long *gS, unsigned long long *gH, SampleCtl *ctl, volatile int *s_fail,
+                              int *err) {
+    int lo, hi;
+    pair_slice(V / 2, lo, hi);
+    for (int r = 0; r < nrows; ++r) {
+        unsigned long long s = 0;
+        for (int pp = lo + threadIdx.x; pp < hi; pp += blockDim.x) {
+            const float2 l = *(const float2 *)(rowp[r] + 2 * pp);
+            s += weight_of(l.x, T, sm.ymax[r]) + weight_of(l.y, T, sm.ymax[r]);
+        }
+        s = block_sum_u64(s, sm.red);
+        if (threadIdx.x == 0 && s) atomicAdd(&gS[r], s);
+    }
+    if (!grid_barrier(ctl, s_fail, err)) return false;
+    const unsigned long long P32 = top_p_q32(top_p);
+    if (threadIdx.x < nrows) {
+        const unsigned long long S = ldcg_u64(&gS[threadIdx.x]);
+        const unsigned long long tau = (unsigned long long)(((unsigned __int128)S * P32) >> 32);
+        sm.tau[threadIdx.x] = tau < 1 ? 1 : tau;
+        sm.prefix[threadIdx.x] = 0;
+        sm.above[threadIdx.x] = 0;
+    }
+    __syncthreads();
+    for (int pass = 0; pass < kRadixPasses; ++pass) {
+        const int shift = 48 - 8 * pass;
+        for (int i = threadIdx.x; i < nrows * 256; i += blockDim.x) (&sm.hist[0][0])[i] = 0;
+        __syncthreads();
+        for (int r = 0; r < nrows; ++r) {
+            const unsigned long long want = sm.prefix[r] >> (shift + 8);
+            for (int pp = lo + threadIdx.x; pp < hi; pp += blockDim.x) {
+                const float2 l = *(const float2 *)(rowp[r] + 2 * pp);
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int v = 2 * pp + e;
+                    const unsigned long long E = weight_of(e ? l.y : l.x, T, sm.ymax[r]);
+                    const unsigned long long key = key_of(E, v);
+                    if (E && (key >> (shift + 8)) == want) atomicAdd(&sm.hist[r][(key >> shift) & 255], E);
+                }
+            }
+        }
+        __syncthreads();
+        unsigned long long *gp = gH + (size_t)pass * nrows * 256;
+        for (int i = threadIdx.x; i < nrows * 256; i += blockDim.x) {
+            const unsigned long long h = (&sm.hist[0][0])[i];
+            if (h) atomicAdd(&gp[i], h);
+        }
+        if (!grid_barrier(ctl, s_fail, err)) return false;
+        // every CTA resolves the digit the same way: the largest bin whose
+        // suffix weight (including itself) reaches tau
+        if (threadIdx.x < nrows) {
+            const int r = threadIdx.x;
+            const unsigned long long *hr = gp + (size_t)r * 256;
+            unsigned long long cum = sm.above[r];
+            int d = 255;
+            for (; d > 0; --d) {
+                const unsigned long long h = ldcg_u64(&hr[d]);
+                if (cum + h >= sm.tau[r]) break;
+                cum += h;
+            }
+            sm.prefix[r] |= (unsigned long long)d << shift;
+            sm.last_bin[r] = ldcg_u64(&hr[d]);
+            sm.above[r] = cum;
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x < nrows) {
+        sm.kstar[threadIdx.x] = sm.prefix[threadIdx.x];
+        sm.Sn[threadIdx.x] = sm.above[threadIdx.x] + sm.last_bin[threadIdx.x];
+    }
+    __syncthreads();
+    return true;
+}
+
+// Row maxima of y = l / T for a group of rows -> sm.ymax (one grid barrier).
+__device__ bool group_max(const float *const *rowp, int nrows, int V, float T, NucleusSmem &sm, unsigned long long *gM,
+                          SampleCtl *ctl, volatile int *s_fail, int *err) {
+    int lo, hi;
+    pair_slice(V / 2, lo, hi);
+    for (int r = 0; r < nrows; ++r) {
+        unsigned long long mx = 0;
+        bool bad = false;
+        for (int pp = lo + threadIdx.x; pp < hi; pp += blockDim.x) {
+            const float2 l = *(const float2 *)(rowp[r] + 2 * pp);
+            const float y0 = __fdiv_rn(l.x, T), y1 = __fdiv_rn(l.y, T);
+            if (!isfinite(y0) || !isfinite(y1)) bad = true;
+            const unsigned long long a = f2ord(y0), b = f2ord(y1);
+            mx = max(mx, max(a, b));
+        }
+        if (bad) set_error(err, DSPARK_ERR_BAD_INPUT);
+        mx = block_max_u64(mx, sm.red);
+        if (threadIdx.x == 0) atomicMax(&gM[r], mx);
+    }
+    if (!grid_barrier(ctl, s_fail, err)) return false;
+    if (threadIdx.x < nrows) sm.ymax[threadIdx.x] = ord2f((uint32_t)ldcg_u64(&gM[threadIdx.x]));
+    __syncthreads();
+    return true;
+}
+
+// Weighted draw over vocabulary ids in ascending order: the smallest v whose
+// running weight exceeds floor(total * W / 2^24), total = sum of weight(v).
+// gParts holds [gridDim.x][2] words (overwritten). The CTA holding the target
+// writes the token to *out.
+template <class WF>
+__device__ bool grid_draw(WF weight, int V, uint32_t W24, unsigned long long *gParts, int32_t *out, DrawSmem &ds_,
+                          SampleCtl *ctl, volatile int *s_fail, int *err) {
+    int lo, hi;
+    pair_slice(V / 2, lo, hi);
+    const int n = hi - lo;
+    const int per = (n + blockDim.x - 1) / blockDim.x;  // contiguous pairs per thread
+    const int t0 = lo + threadIdx.x * per, t1 = min(hi, t0 + per);
+    unsigned __int128 mine = 0;
+    for (int pp = t0; pp < t1; ++pp) mine += weight(2 * pp) + weight(2 * pp + 1);
+    ds_.lo[threadIdx.x] = (unsigned long long)mine;
+    ds_.hi[threadIdx.x] = (unsigned long long)(mine >> 64);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned __int128 acc = 0;
+        for (int t = 0; t < (int)blockDim.x; ++t) {
+            acc += ((unsigned __int128)ds_.hi[t] << 64) | ds_.lo[t];
+            ds_.lo[t] = (unsigned long long)acc;
+            ds_.hi[t] = (unsigned long long)(acc >> 64);
+        }
+        gParts[2 * blockIdx.x] = ds_.lo[blockDim.x - 1];
+        gParts[2 * blockIdx.x + 1] = ds_.hi[blockDim.x - 1];
+    }
+    if (!grid_barrier(ctl, s_fail, err)) return false;
+    if (threadIdx.x == 0) {
+        unsigned __int128 before = 0, total = 0;
+        for (int c = 0; c < (int)gridDim.x; ++c) {
+            const unsigned __int128 pc = ((unsigned __int128)ldcg_u64(&gParts[2 * c + 1]) << 64) | ldcg_u64(&gParts[2 * c]);
+            if (c < (int)blockIdx.x) before += pc;
+            total += pc;
+        }
+        ds_.tot[0] = (unsigned long long)before;
+        ds_.tot[1] = (unsigned long long)(before >> 64);
+        ds_.tot[2] = (unsigned long long)total;
+        ds_.tot[3] = (unsigned long long)(total >> 64);
+    }
+    __syncthreads();
+    const unsigned __int128 before = ((unsigned __int128)ds_.tot[1] << 64) | ds_.tot[0];
+    const unsigned __int128 total = ((unsigned __int128)ds_.tot[3] << 64) | ds_.tot[2];
+    const unsigned __int128 target = (total * (unsigned __int128)(W24 & 0xFFFFFFu)) >> 24;
+    const unsigned __int128 incl = before + (((unsigned __int128)ds_.hi[threadIdx.x] << 64) | ds_.lo[threadIdx.x]);
+    const unsigned __int128 excl = incl - mine;
+    if (t0 < t1 && excl <= target && target < incl) {
+        unsigned __int128 cum = excl;
+        for (int v = 2 * t0; v < 2 * t1; ++v) {
+            cum += weight(v);
+            if (cum > target) {
+                *out = v;
+                break;
+            }
+        }
+    }
+    return true;
+}
+
+// ---------------------------------------------------------------------------
+// Markov rollout
+// ---------------------------------------------------------------------------
+constexpr int kRollChunk = 8;  // sequences per pass over w2
+
+// scratch layout (words):
+//   amax [B][bs] | S [B][bs] | hist [B][bs][passes][256] | parts [B][bs][grid][2] | pick [B][bs]
+struct RollLayout {
+    size_t amax, S, hist, parts, pick, total;
+    __host__ __device__ RollLayout(int bs, int B, int grid) {
+        amax = 0;
+        S = amax + (size_t)B * bs;
+        hist = S + (size_t)B * bs;
+        parts = hist + (size_t)B * bs * kRadixPasses * 256;
+        pick = parts + (size_t)B * bs * grid * 2;
+        total = pick + (size_t)B * bs;
+    }
+};
+
+size_t rollout_scratch_words(int bs, int B, int grid) { return RollLayout(bs, B, grid).total; }
+
+__global__ void __launch_bounds__(kSampThreads, 1) rollout_kernel(RolloutParams p) {
+    __shared__ NucleusSmem sm;
+    __shared__ DrawSmem dsm;
+    __shared__ float s_w1[kRollChunk][256];
+    __shared__ int s_prev[kMaxSampBs];
+    __shared__ volatile int s_fail;
+    __shared__ const float *s_rows[kRowsPerGroup];
+    const RollLayout L(p.bs, p.B, gridDim.x);
+    unsigned long long *sc = p.scratch;
+    const int V = p.V, r = p.r;
+    if (threadIdx.x == 0) s_fail = 0;
+    for (size_t w = (size_t)blockIdx.x * blockDim.x + threadIdx.x; w < L.total; w += (size_t)gridDim.x * blockDim.x)
+        sc[w] = 0;
+    for (int b = threadIdx.x; b < p.bs; b += blockDim.x) {
+        int a = p.anchor[b];
+        if (a < 0 || a >= V) {
+            set_error(p.err, DSPARK_ERR_OOB);
+            a = 0;
+        }
+        s_prev[b] = a;
+    }
+    __threadfence();
+    if (!grid_barrier(p.ctl, &s_fail, p.err)) return;
+    int lo, hi;
+    pair_slice(V / 2, lo, hi);
+    const __nv_bfloat162 *w2 = (const __nv_bfloat162 *)p.w2;
+
+    for (int i = 0; i < p.B; ++i) {
+        // ell_i = z_i + fp32 FMA chain of w1[t_{i-1}] against w2 (k in order)
+        for (int b0 = 0; b0 < p.bs; b0 += kRollChunk) {
+            const int nb = min(kRollChunk, p.bs - b0);
+            for (int idx = threadIdx.x; idx < kRollChunk * r; idx += blockDim.x) {
+                const int bb = idx / r, k = idx % r;
+                s_w1[bb][k] = bb < nb ? __bfloat162float(p.w1[(size_t)s_prev[b0 + bb] * r + k]) : 0.f;
+            }
+            __syncthreads();
+            unsigned long long best[kRollChunk];
+#pragma unroll
+            for (int bb = 0; bb < kRollChunk; ++bb) best[bb] = 0;
+            bool bad = false;
+            for (int pp = lo + threadIdx.x; pp < hi; pp += blockDim.x) {
+                float a0[kRollChunk], a1[kRollChunk];
+#pragma unroll
+                for (int bb = 0; bb < kRollChunk; ++bb) a0[bb] = a1[bb] = 0.f;
+                for (int k = 0; k < r; ++k) {
+                    const float2 w = __bfloat1622float2(w2[((size_t)k * V) / 2 + pp]);
+#pragma unroll
+                    for (int bb = 0; bb < kRollChunk; ++bb) {
+                        a0[bb] = __fmaf_rn(s_w1[bb][k], w.x, a0[bb]);
+                        a1[bb] = __fmaf_rn(s_w1[bb][k], w.y, a1[bb]);
+                    }
+                }
+#pragma unroll
+                for (int bb = 0; bb < kRollChunk; ++bb) {
+                    if (bb < nb) {
+                        const int b = b0 + bb;
+                        const size_t off = ((size_t)b * p.B + i) * V + 2 * pp;
+                        const float2 z = *(const float2 *)(p.z + off);
+                        const float l0 = __fadd_rn(z.x, a0[bb]), l1 = __fadd_rn(z.y, a1[bb]);
+                        *(float2 *)(p.ell + off) = make_float2(l0, l1);
+                        if (!isfinite(l0) || !isfinite(l1)) bad = true;
+                        unsigned long long k0, k1;
+                        if (p.draft_mode == DSPARK_GREEDY) {
+                            k0 = argmax_key(l0, 2 * pp);
+                            k1 = argmax_key(l1, 2 * pp + 1);
+                        } else {
+                            k0 = f2ord(__fdiv_rn(l0, p.T));
+                            k1 = f2ord(__fdiv_rn(l1, p.T));
+                        }
+                        best[bb] = max(best[bb], max(k0, k1));
+                    }
+                }
+            }
+            if (bad) set_error(p.err, DSPARK_ERR_BAD_INPUT);
+            for (int bb = 0; bb < nb; ++bb) {
+                const unsigned long long m = block_max_u64(best[bb], sm.red);
+                if (threadIdx.x == 0) atomicMax(&sc[L.amax + (size_t)i * p.bs + b0 + bb], m);
+            }
+            __syncthreads();
+        }
+        if (!grid_barrier(p.ctl, &s_fail, p.err)) return;
+        if (p.draft_mode == DSPARK_GREEDY) {
+            for (int b = threadIdx.x; b < p.bs; b += blockDim.x) {
+                const int t = argmax_token(ldcg_u64(&sc[L.amax + (size_t)i * p.bs + b]));
+                s_prev[b] = t;
+                if (blockIdx.x == 0) p.tokens[b * p.B + i] = t;
+            }
+            __syncthreads();
+            continue;
+        }
+        // probabilistic: nucleus of ell_i / T per sequence, then a draw
+        for (int g0 = 0; g0 < p.bs; g0 += kRowsPerGroup) {
+            const int nr = min(kRowsPerGroup, p.bs - g0);
+            if (threadIdx.x < nr) {
+                s_rows[threadIdx.x] = p.ell + ((size_t)(g0 + threadIdx.x) * p.B + i) * V;
+                sm.ymax[threadIdx.x] = ord2f((uint32_t)ldcg_u64(&sc[L.amax + (size_t)i * p.bs + g0 + threadIdx.x]));
+            }
+            __syncthreads();
+            if (!group_nucleus(s_rows, nr, V, p.T, p.top_p, sm, sc + L.S + (size_t)i * p.bs + g0,
+                               sc + L.hist + ((size_t)i * p.bs + g0) * kRadixPasses * 256, p.ctl, &s_fail, p.err))
+                return;
+            for (int rr = 0; rr < nr; ++rr) {
+                const int b = g0 + rr;
+                const float *row = s_rows[rr];
+                const unsigned long long kstar = sm.kstar[rr];
+                const float ym = sm.ymax[rr], T = p.T;
+                auto wf = [&](int v) -> unsigned __int128 {
+                    const unsigned long long E = weight_of(row[v], T, ym);
+                    return key_of(E, v) >= kstar ? (unsigned __int128)E : (unsigned __int128)0;
+                };
+                const uint32_t W = philox_word(p.seed, (uint32_t)b, p.step, (uint32_t)i, 1u) >> 8;
+                int32_t *pick = (int32_t *)&sc[L.pick + (size_t)i * p.bs + b];
+                if (!grid_draw(wf, V, W, sc + L.parts + ((size_t)i * p.bs + b) * gridDim.x * 2, pick, dsm, p.ctl,
+                               &s_fail, p.err))
+                    return;
+            }
+        }
+        if (!grid_barrier(p.ctl, &s_fail, p.err)) return;
+        for (int b = threadIdx.x; b < p.bs; b += blockDim.x) {
+            const int t = (int)(uint32_t)ldcg_u64(&sc[L.pick + (size_t)i * p.bs + b]);
+            s_prev[b] = t;
+            if (blockIdx.x == 0) p.tokens[b * p.B + i] = t;
+        }
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Verification
+// ---------------------------------------------------------------------------
+// Greedy: row argmax keys (zero between launches) then a finalize kernel that
+// also returns the keys to zero.
+__global__ void verify_argmax_kernel(const float *__restrict__ P, int rows, int V, unsigned long long *keys, int *err) {
+    __shared__ unsigned long long red[33];
+    const int row = blockIdx.y;
+    const int nslices = gridDim.x;
+    const int npairs = V / 2;
+    const int lo = (int)((long long)blockIdx.x * npairs / nslices);
+    const int hi = (int)((long long)(blockIdx.x + 1) * npairs / nslices);
+    unsigned long long best = 0;
+    bool bad = false;
+    const float *pr = P + (size_t)row * V;
+    for (int pp = lo + threadIdx.x; pp < hi; pp += blockDim.x) {
+        const float2 l = *(const float2 *)(pr + 2 * pp);
+        if (!isfinite(l.x) || !isfinite(l.y)) bad = true;
+        best = max(best, max(argmax_key(l.x, 2 * pp), argmax_key(l.y, 2 * pp + 1)));
+    }
+    if (bad) set_error(err, DSPARK_ERR_BAD_INPUT);
+    best = block_max_u64(best, red);
+    if (threadIdx.x == 0) atomicMax(&keys[row], best);
+}
+
+__global__ void verify_greedy_finalize(const int32_t *__restrict__ tokens, int bs, int B, int V,
+                                       unsigned long long *keys, int32_t *accept_len, int32_t *out_tokens, int *err) {
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= bs) return;
+    unsigned long long *k = keys + (size_t)b * (B + 1);
+    int a = 0;
+    for (; a < B; ++a) {
+        const int t = tokens[b * B + a];
+        if (t < 0 || t >= V) {
+            set_error(err, DSPARK_ERR_OOB);
+            break;
+        }
+        if (argmax_token(k[a]) != t) break;
+        out_tokens[b * (B + 1) + a] = t;
+    }
+    out_tokens[b * (B + 1) + a] = argmax_token(k[a]);
+    for (int j = a + 1; j <= B; ++j) out_tokens[b * (B + 1) + j] = -1;
+    accept_len[b] = a;
+    for (int j = 0; j <= B; ++j) k[j] = 0;
+}
+
+// Probabilistic (cooperative). scratch layout (words), R rows per sequence:
+// p rows 0..B, then (unless the draft was greedy) q rows 0..B-1:
+//   gM [bs*R] | gS [bs*R] | gH [groups][passes][kRowsPerGroup][256] | stats [bs*R][2] | parts [bs][grid][2]
+struct VerLayout {
+    size_t gM, gS, gH, stats, parts, total;
+    int R, nrows, groups;
+    __host__ __device__ VerLayout(int bs, int B, int grid, int draft_greedy) {
+        R = draft_greedy ? B + 1 : 2 * B + 1;
+        nrows = bs * R;
+        groups = (nrows + kRowsPerGroup - 1) / kRowsPerGroup;
+        gM = 0;
+        gS = gM + nrows;
+        gH = gS + nrows;
+        stats = gH + (size_t)groups * kRadixPasses * kRowsPerGroup * 256;
+        parts = stats + (size_t)nrows * 2;
+        total = parts + (size_t)bs * grid * 2;
+    }
+};
+
+size_t verify_scratch_words(int bs, int B, int grid) { return VerLayout(bs, B, grid, 0).total; }
+
+DS_DEVINL const float *ver_row(const VerifyParams &p, int gr) {
+    const int R = p.draft_greedy ? p.B + 1 : 2 * p.B + 1, b = gr / R, j = gr % R;
+    if (j <= p.B) return p.P + ((size_t)b * (p.B + 1) + j) * p.V;
+    return p.ell + ((size_t)b * p.B + (j - p.B - 1)) * p.V;
+}
+
+__global__ void __launch_bounds__(kSampThreads, 1) verify_prob_kernel(VerifyParams p) {
+    __shared__ NucleusSmem sm;
+    __shared__ DrawSmem dsm;
+    __shared__ volatile int s_fail;
+    __shared__ const float *s_rows[kRowsPerGroup];
+    __shared__ int s_acc[kMaxSampBs];
+    __shared__ int s_kind[kMaxSampBs];  // 0: residual draw at position s_acc, 1: bonus draw
+    const VerLayout L(p.bs, p.B, gridDim.x, p.draft_greedy);
+    unsigned long long *sc = p.scratch;
+    const int V = p.V;
+    if (threadIdx.x == 0) s_fail = 0;
+    for (size_t w = (size_t)blockIdx.x * blockDim.x + threadIdx.x; w < L.total; w += (size_t)gridDim.x * blockDim.x)
+        sc[w] = 0;
+    __threadfence();
+    if (!grid_barrier(p.ctl, &s_fail, p.err)) return;
+    for (int g = 0; g < L.groups; ++g) {
+        const int r0 = g * kRowsPerGroup, nr = min(kRowsPerGroup, L.nrows - r0);
+        if (threadIdx.x < nr) s_rows[threadIdx.x] = ver_row(p, r0 + threadIdx.x);
+        __syncthreads();
+        if (!group_max(s_rows, nr, V, p.T, sm, sc + L.gM + r0, p.ctl, &s_fail, p.err)) return;
+        if (!group_nucleus(s_rows, nr, V, p.T, p.top_p, sm, sc + L.gS + r0,
+                           sc + L.gH + (size_t)g * kRadixPasses * kRowsPerGroup * 256, p.ctl, &s_fail, p.err))
+            return;
+        if (blockIdx.x == 0 && threadIdx.x < nr) {
+            sc[L.stats + (size_t)(r0 + threadIdx.x) * 2] = sm.kstar[threadIdx.x];
+            sc[L.stats + (size_t)(r0 + threadIdx.x) * 2 + 1] = sm.Sn[threadIdx.x];
+        }
+        __syncthreads();
+    }
+    if (!grid_barrier(p.ctl, &s_fail, p.err)) return;
+    // accept chain per sequence (computed identically by every CTA)
+    for (int b = threadIdx.x; b < p.bs; b += blockDim.x) {
+        const int R = L.R;
+        int a = 0, kind = 1;
+        for (; a < p.B; ++a) {
+            int t = p.tokens[b * p.B + a];
+            if (t < 0 || t >= V) {
+                set_error(p.err, DSPARK_ERR_OOB);
+                t = 0;
+            }
+            const int rp = b * R + a, rq = b * R + p.B + 1 + a;
+            const float mp = ord2f((uint32_t)ldcg_u64(&sc[L.gM + rp]));
+            const unsigned long long ksp = ldcg_u64(&sc[L.stats + 2 * rp]), Sp = ldcg_u64(&sc[L.stats + 2 * rp + 1]);
+            const unsigned long long Ept = weight_of(p.P[((size_t)b * (p.B + 1) + a) * V + t], p.T, mp);
+            const unsigned long long ep = key_of(Ept, t) >= ksp ? Ept : 0ull;
+            unsigned long long eq, Sq;
+            if (p.draft_greedy) {
+                eq = 1;
+                Sq = 1;
+            } else {
+                const float mq = ord2f((uint32_t)ldcg_u64(&sc[L.gM + rq]));
+                const unsigned long long ksq = ldcg_u64(&sc[L.stats + 2 * rq]);
+                Sq = ldcg_u64(&sc[L.stats + 2 * rq + 1]);
+                const unsigned long long Eqt = weight_of(p.ell[((size_t)b * p.B + a) * V + t], p.T, mq);
+                eq = key_of(Eqt, t) >= ksq ? Eqt : 0ull;
+            }
+            const uint32_t U = philox_word(p.seed, (uint32_t)b, p.step, (uint32_t)a, 2u);
+            const unsigned __int128 lhs = (unsigned __int128)U * eq * Sp;
+            const unsigned __int128 rhs = ((unsigned __int128)ep << 32) * Sq;
+            if (!(lhs < rhs)) {
+                kind = 0;
+                break;
+            }
+            if (blockIdx.x == 0) p.out_tokens[b * (p.B + 1) + a] = t;
+        }
+        s_acc[b] = a;
+        s_kind[b] = kind;
+        if (blockIdx.x == 0) {
+            p.accept_len[b] = a;
+            for (int j = a + 1; j <= p.B; ++j) p.out_tokens[b * (p.B + 1) + j] = -1;
+        }
+    }
+    __syncthreads();
+    // one draw per sequence: the residual at the first reject, or the bonus
+    for (int b = 0; b < p.bs; ++b) {
+        const int a = s_acc[b], kind = s_kind[b], R = L.R;
+        const int prow_i = kind ? p.B : a;
+        const int rp = b * R + prow_i;
+        const float *prow = p.P + ((size_t)b * (p.B + 1) + prow_i) * V;
+        const float mp = ord2f((uint32_t)ldcg_u64(&sc[L.gM + rp]));
+        const unsigned long long ksp = ldcg_u64(&sc[L.stats + 2 * rp]), Sp = ldcg_u64(&sc[L.stats + 2 * rp + 1]);
+        const float T = p.T;
+        int32_t *dst = p.out_tokens + b * (p.B + 1) + a;
+        unsigned long long *parts = sc + L.parts + (size_t)b * gridDim.x * 2;
+        if (kind) {
+            const uint32_t W = philox_word(p.seed, (uint32_t)b, p.step, (uint32_t)p.B, 4u) >> 8;
+            auto wf = [&](int v) -> unsigned __int128 {
+                const unsigned long long E = weight_of(prow[v], T, mp);
+                return key_of(E, v) >= ksp ? (unsigned __int128)E : (unsigned __int128)0;
+            };
+            if (!grid_draw(wf, V, W, parts, dst, dsm, p.ctl, &s_fail, p.err)) return;
+        } else {
+            const uint32_t W = philox_word(p.seed, (uint32_t)b, p.step, (uint32_t)a, 3u) >> 8;
+            const int t = min(max(p.tokens[b * p.B + a], 0), V - 1);
+            const int rq = b * R + p.B + 1 + a;
+            const float *qrow = p.ell + ((size_t)b * p.B + a) * V;
+            const bool dg = p.draft_greedy != 0;
+            const float mq = dg ? 0.f : ord2f((uint32_t)ldcg_u64(&sc[L.gM + rq]));
+            const unsigned long long ksq = dg ? 0ull : ldcg_u64(&sc[L.stats + 2 * rq]);
+            const unsigned long long Sq = dg ? 1ull : ldcg_u64(&sc[L.stats + 2 * rq + 1]);
+            auto wf = [&](int v) -> unsigned __int128 {
+                const unsigned long long Ep = weight_of(prow[v], T, mp);
+                const unsigned long long ep = key_of(Ep, v) >= ksp ? Ep : 0ull;
+                unsigned long long eq;
+                if (dg) {
+                    eq = (v == t) ? 1ull : 0ull;
+                } else {
+                    const unsigned long long Eq = weight_of(qrow[v], T, mq);
+                    eq = key_of(Eq, v) >= ksq ? Eq : 0ull;
+                }
+                const unsigned __int128 x = (unsigned __int128)ep * Sq, y = (unsigned __int128)eq * Sp;
+                return x > y ? x - y : (unsigned __int128)0;
+            };
+            if (!grid_draw(wf, V, W, parts, dst, dsm, p.ctl, &s_fail, p.err)) return;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host launchers
+// ---------------------------------------------------------------------------
+int sampling_max_grid(int num_sms) {
+    int a = 0, b = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, rollout_kernel, kSampThreads, 0) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, verify_prob_kernel, kSampThreads, 0) != cudaSuccess)
+        return 0;
+    return (a >= 1 && b >= 1) ? num_sms : 0;
+}
+
+cudaError_t launch_rollout(RolloutParams p, int grid, cudaStream_t st) {
+    void *args[] = {&p};
+    return cudaLaunchCooperativeKernel((void *)rollout_kernel, dim3(grid), dim3(kSampThreads), args, 0, st);
+}
+
+cudaError_t launch_verify(VerifyParams p, int grid, cudaStream_t st) {
+    if (p.verify_mode == DSPARK_GREEDY) {
+        const int rows = p.bs * (p.B + 1);
+        verify_argmax_kernel<<<dim3(8, rows), 256, 0, st>>>(p.P, rows, p.V, p.scratch, p.err);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        verify_greedy_finalize<<<(p.bs + 127) / 128, 128, 0, st>>>(p.tokens, p.bs, p.B, p.V, p.scratch, p.accept_len,
+                                                                  p.out_tokens, p.err);
+        return cudaGetLastError();
+    }
+    void *args[] = {&p};
+    return cudaLaunchCooperativeKernel((void *)verify_prob_kernel, dim3(grid), dim3(kSampThreads), args, 0, st);
+}
+
+}  // namespace ds
