@@ -1,0 +1,407 @@
+"""Benchmark of the DSpark draft-and-verify step on GB300.
+
+One step = the whole hot path on one block of the full-geometry drafter at
+bs=1, ctx 4096 (seeded synthetic inputs, bf16 weights): fc context fusion, 5
+MLA block-diffusion layers + lm_head, Markov rollout, confidence head, greedy
+verification. Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+--impl reference times the float64 CPU oracle on the host cores on a bounded
+sample of the same workload (the method has no other reference implementation).
+Multi-GPU: replicas only (every rank runs its own step; no data-path collective).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "µs per 7-token draft block at bs=1 (full geometry); achieved HBM TB/s vs peak"
+UNIT = "us"
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK), "fallback"
+
+
+def algorithmic_bytes(G, ctx: int, bs: int = 1):
+    """Bytes one step must move at least: every bf16 weight once (w2 once, the
+    block's 7 rows of w1), fp32 gains and confidence head, the latent KV once,
+    the aux states, z and ell written once and read once, the target logits."""
+    lp = G.layer_params()
+    mats = sum(v for k, v in lp.items() if k != "norms")
+    c = G.param_counts()
+    w_bf16 = 2 * (c["fc"] + G.n_layers * mats + c["lm_head"] + G.rank * G.vocab + G.block * G.rank)
+    w_f32 = 4 * (G.n_layers * lp["norms"] + 2 * G.hidden)
+    kv = bs * G.n_layers * ctx * G.kv_dim * 2
+    aux = bs * G.block * G.n_aux * G.hidden * 2
+    logits = 4 * bs * G.vocab * (2 * G.block + 2 * G.block + (G.block + 1))
+    total = w_bf16 + w_f32 + kv + aux + logits
+    return {"weights": w_bf16 + w_f32, "kv": kv, "aux": aux, "logits": logits, "total": total,
+            "fc_weight": 2 * c["fc"]}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except FileNotFoundError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle sample (baseline and reference arm)
+# ---------------------------------------------------------------------------
+def oracle_sample(w, W, I, lm_rows: int, rng_seed: int = 0):
+    """Time the float64 oracle on a bounded sample of one block: fc fusion, one
+    full layer, the lm_head on lm_rows vocabulary rows, the Markov rollout and
+    greedy verification on the full vocabulary; scale to a whole block."""
+    from oracle import network as N
+    from oracle import sampling as S
+    G = w.geom
+    ctx = I["ctx_list"][0]
+    f64 = lambda t: t.detach().to(torch.float64).cpu().numpy()
+    t_conv0 = time.perf_counter()
+    w_fc = f64(W["w_fc"])
+    aux = f64(I["aux"])[0]
+    keys = ["attn_norm", "w_qkv_a", "q_a_norm", "kv_a_norm", "w_q_b", "w_kv_b", "w_o", "mlp_norm", "w_gate", "w_up",
+            "w_down"]
+    L0 = {k: f64(W[f"l0.{k}"]) for k in keys}
+    table = I["page_table"][0].cpu().numpy()
+    cache = N.gather_cache(f64(I["kv_pools"][0]), table, ctx)
+    rows = np.random.default_rng(rng_seed).choice(G.vocab, lm_rows, replace=False)
+    w_lm = f64(W["w_lm"][torch.as_tensor(rows, device=W["w_lm"].device)])
+    w1, w2 = W["markov_w1"].cpu(), W["markov_w2"].cpu()
+    t_conv = time.perf_counter() - t_conv0
+    t0 = time.perf_counter()
+    x = N.fuse_ctx(w_fc, aux)
+    t1 = time.perf_counter()
+    pos = np.arange(G.block, dtype=np.float64) + ctx
+    x1 = N.layer(x, L0, G, cache[:, :G.kv_lora], cache[:, G.kv_lora:], pos)
+    t2 = time.perf_counter()
+    h = N.rmsnorm(x1, np.ones(G.hidden), G.eps)
+    _ = h @ w_lm.T
+    t3 = time.perf_counter()
+    z = np.asarray(np.random.default_rng(rng_seed).standard_normal((G.block, G.vocab)) * 1.7, dtype=np.float32)
+    toks, ell = S.markov_rollout(z, w1, w2, 0)
+    t4 = time.perf_counter()
+    P = np.concatenate([ell, ell[-1:]]).astype(np.float32)
+    S.verify_greedy(P, toks)
+    N.confidence(h, np.ones(G.hidden) * 0.01, 0.0)
+    t5 = time.perf_counter()
+    est = (t1 - t0) + G.n_layers * (t2 - t1) + (t3 - t2) * G.vocab / lm_rows + (t4 - t3) + (t5 - t4)
+    sampled = (t5 - t0)
+    return est, sampled, t_conv, {"fc_s": t1 - t0, "layer_s": t2 - t1, "lm_head_sample_s": t3 - t2,
+                                  "rollout_s": t4 - t3, "verify_conf_s": t5 - t4}
+
+
+def cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+# ---------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--lm-rows", type=int, default=4096)
+    args = ap.parse_args()
+    assert args.warmup >= 3 or args.impl == "reference", "at least 3 warm-up steps"
+
+    from synthetic import generate as gen
+    from synthetic.configs import FULL_STEP
+    w = FULL_STEP
+    G = w.geom
+    world, rank, local = dist_setup()
+    ctx = w.ctx[0]
+    ab = algorithmic_bytes(G, ctx)
+    config = {"workload": w.name, "model": "DSpark drafter (Kimi-K3 geometry), random init", "global_batch": w.bs * world,
+              "seq_len": ctx, "block": G.block, "draft": "greedy", "verify": "greedy", "weights": "bf16",
+              "parallelism": f"replicas{world}",
+              "l2": f"no flush: working set {ab['total'] / 1e9:.2f} GB per step > 129 MB L2"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        torch.manual_seed(0)
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        W = gen.make_weights(w, dev)
+        I = gen.make_inputs(w, dev)
+        from oracle import build as obuild
+        obuild.build()
+        for _ in range(args.warmup):
+            oracle_sample(w, W, I, args.lm_rows // 4)
+        vals = []
+        for k in range(args.steps):
+            est, sampled, _, parts = oracle_sample(w, W, I, args.lm_rows // 4, rng_seed=k)
+            vals.append(est * 1e6)
+        v = statistics.median(vals)
+        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": v / 1e3, "higher_is_better": False, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
+                "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores(), "kind": "oracle",
+                                 "sample": f"per step: fc fusion + 1 of {G.n_layers} layers + lm_head on "
+                                           f"{args.lm_rows // 4} of {G.vocab} rows + full Markov rollout + verify, "
+                                           f"scaled to one block"},
+                "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import mla_block_diffusion_gb300 as M
+    from mla_block_diffusion_gb300 import build as libbuild
+    from oracle import build as obuild
+    libbuild.build()
+    obuild.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    W = gen.make_weights(w, dev)
+    I = gen.make_inputs(w, dev)
+    bs = w.bs
+    ds = M.DSpark(G, W, max_bs=bs, max_ctx=ctx)
+    kv = ds.make_kv(I["kv_pools"], I["page_table"], I["ctx_len"], ctx)
+    x = torch.empty(bs, G.block, G.hidden, dtype=torch.float32, device=dev)
+    h_out = torch.empty_like(x)
+    z = torch.empty(bs, G.block, G.vocab, dtype=torch.float32, device=dev)
+    ell = torch.empty_like(z)
+    tokens = torch.empty(bs, G.block, dtype=torch.int32, device=dev)
+    conf = torch.empty(bs, G.block, dtype=torch.float32, device=dev)
+    acc = torch.empty(bs, dtype=torch.int32, device=dev)
+    out = torch.empty(bs, G.block + 1, dtype=torch.int32, device=dev)
+    P = torch.empty(bs, G.block + 1, G.vocab, dtype=torch.float32, device=dev)
+    smp = M.Sample(M.GREEDY, M.GREEDY, 1.0, 1.0, 1, 0)
+    aux, anchor = I["aux"], I["anchor"]
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record()
+        ds.fuse_ctx(aux, x, bs)
+        if ev is not None:
+            ev[1].record()
+        ds.draft_block(x, kv, h_out, z, bs)
+        ds.markov_rollout(z, anchor, smp, tokens, ell, bs)
+        ds.confidence(h_out, conf, bs)
+        ds.verify(P, ell, tokens, smp, acc, out, bs)
+
+    # the target's logits: the drafter's own Markov logits plus N(0, 0.5^2) noise,
+    # fixed from the first pass (the step is deterministic, so they match every step)
+    P.zero_()
+    step()
+    st = ds.check()
+    assert st == 0, f"device error {st}"
+    noise = gen.noise((bs, G.block + 1, G.vocab), w.target_noise, w.input_seed, device=dev)
+    P.copy_(torch.cat([ell, ell[:, -1:]], dim=1) + noise)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert ds.check() == 0
+
+    # ---- device-resident timing ----
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clk = ClockSampler(local)
+    clk.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    start.record()
+    for k in range(args.steps):
+        step(evs[k])
+    stop.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = clk.stop()
+    assert ds.check() == 0
+    ms = start.elapsed_time(stop) / args.steps
+    ms = max_over_ranks(ms, world)
+    fc_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+
+    # ---- end to end through the public API with host buffers ----
+    aux_h = aux.cpu().pin_memory()
+    anchor_h = anchor.cpu().pin_memory()
+    P_h = P.cpu().pin_memory()
+    acc_h = torch.empty_like(acc, device="cpu").pin_memory()
+    out_h = torch.empty_like(out, device="cpu").pin_memory()
+    conf_h = torch.empty_like(conf, device="cpu").pin_memory()
+    tok_h = torch.empty_like(tokens, device="cpu").pin_memory()
+
+    def e2e_step():
+        aux.copy_(aux_h, non_blocking=True)
+        anchor.copy_(anchor_h, non_blocking=True)
+        P.copy_(P_h, non_blocking=True)
+        step()
+        acc_h.copy_(acc, non_blocking=True)
+        out_h.copy_(out, non_blocking=True)
+        conf_h.copy_(conf, non_blocking=True)
+        tok_h.copy_(tokens, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(2):
+        e2e_step()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_step()
+    e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3 / args.steps, world)
+    h2d = aux_h.numel() * aux_h.element_size() + anchor_h.numel() * 4 + P_h.numel() * 4
+    d2h = (acc_h.numel() + out_h.numel() + tok_h.numel()) * 4 + conf_h.numel() * 4
+    accept = acc.cpu().tolist()
+
+    pk, src = peaks()
+    hbm = pk["hbm_gbs"]
+    fc_bytes = ab["fc_weight"] + bs * G.block * G.n_aux * G.hidden * 2 + bs * G.block * G.hidden * 4
+    achieved = fc_bytes / (fc_ms * 1e-3) / 1e9
+    traffic = None
+    tfile = os.path.join(ROOT, "profiles", "fc_gemm_traffic.json")
+    if os.path.exists(tfile):
+        with open(tfile) as f:
+            td = json.load(f)
+        h = hashlib.sha256(open(os.path.join(ROOT, "mla_block_diffusion_gb300", "csrc", "gemm.cuh"), "rb").read())
+        if td.get("gemm_cuh_sha256") == h.hexdigest():
+            traffic = td.get("dram_bytes_per_launch")
+    gpu_launches_per_step = 1 + G.n_layers * (11 + (1 if ds_layout_splits(ds) > 1 else 0)) + 2 + 1 + 1 + 2
+    us = ms * 1e3 / world  # whole job: one block per rank per step
+    line = {
+        "metric": METRIC, "value": us, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": config,
+        "drafted_tokens_per_s": G.block * bs * world / (ms * 1e-3),
+        "hbm": {"algorithmic_bytes_per_step": ab["total"], "achieved_TBps": ab["total"] / (ms * 1e-3) / 1e12,
+                "frac_of_peak": ab["total"] / (ms * 1e-3) / 1e9 / hbm, "peak_GBps": hbm, "peak_source": src,
+                "frac_of_8TBps": ab["total"] / (ms * 1e-3) / 8e12},
+        "roofline": {"kernel": "gemm_swapab_kernel<16> (fc fusion launch)", "bound": "hbm", "achieved": achieved,
+                     "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
+                     "algorithmic_bytes_per_launch": fc_bytes, "avg_launch_ms": fc_ms, "peak_source": src},
+        "clocks": clocks,
+        "e2e": {"value": e2e_ms * 1e3 / world, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": gpu_launches_per_step * args.steps,
+        "accept_len": accept,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        est, sampled, conv, parts = oracle_sample(w, W, I, args.lm_rows)
+        line["cpu_baseline"] = {"value": est * 1e6, "unit": UNIT, "cores": cores(), "kind": "oracle",
+                                "sample": f"fc fusion + 1 of {G.n_layers} layers (ctx {ctx}) + lm_head on "
+                                          f"{args.lm_rows} of {G.vocab} rows + full Markov rollout + greedy verify "
+                                          f"+ confidence, float64, scaled to one block; sampled {sampled:.1f} s",
+                                "parts_s": parts}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def ds_layout_splits(ds) -> int:
+    """KV split count the library uses for this workload (mirrors its split rule)."""
+    G = ds.G
+    R = G.block * G.n_heads
+    qtiles = (R + 63) // 64
+    chunks = (ds.max_ctx + G.block + 63) // 64
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    want = -(-sms // (qtiles * ds.max_bs))
+    cap = (chunks + 3) // 4
+    s = max(1, min(want, cap, 64))
+    cps = -(-chunks // s)
+    return -(-chunks // cps)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,134 @@
+"""Full-geometry parity (Kimi-K3 DSpark drafter sizes), in the launch
+configuration the benchmark times, through the C ABI.
+
+* fc fusion: sampled output channels recomputed by the oracle one by one.
+* draft block: the oracle runs all 5 layers in float64 (weights converted layer
+  by layer); h_out compared on every element, z on sampled vocabulary rows.
+* Markov rollout and verification over the full 163,840 vocabulary: bit-exact
+  on seeded stand-in logits.
+* bs = 32 with paged, ragged contexts and ctx = 95,000 with YaRN: sampled
+  sequences end to end.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import network as N
+from oracle import sampling as S
+from synthetic import generate as gen
+from synthetic.configs import BATCH_STEP, FULL_STEP, LONG_STEP
+from tests.gpu_harness import u32
+from tests.helpers import rel_l2
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-2
+LAYER_KEYS = ("attn_norm", "w_qkv_a", "q_a_norm", "kv_a_norm", "w_q_b", "w_kv_b", "w_o", "mlp_norm", "w_gate", "w_up",
+              "w_down")
+
+
+def f64(t):
+    return t.detach().to(torch.float64).cpu().numpy()
+
+
+@pytest.fixture(scope="module")
+def M():
+    import mla_block_diffusion_gb300 as M
+    from mla_block_diffusion_gb300 import build
+    build.build()
+    return M
+
+
+@pytest.fixture(scope="module")
+def weights():
+    return gen.make_weights(FULL_STEP, "cuda")
+
+
+def oracle_seq(w, W, I, b, vocab_rows):
+    """Oracle draft for sequence b: h_out [7, H] and z on the given vocabulary rows."""
+    G = w.geom
+    ctx = I["ctx_list"][b]
+    x = N.fuse_ctx(f64(W["w_fc"]), f64(I["aux"][b]))
+    table = I["page_table"][b].cpu().numpy()
+    pos = np.arange(G.block, dtype=np.float64) + ctx
+    for l in range(G.n_layers):
+        L = {k: f64(W[f"l{l}.{k}"]) for k in LAYER_KEYS}
+        pages = torch.as_tensor(table[: (ctx + G.page_size - 1) // G.page_size], device=I["kv_pools"][l].device)
+        pool = f64(I["kv_pools"][l][pages.long()])  # only this sequence's pages, renumbered
+        cache = N.gather_cache(pool, np.arange(pool.shape[0]), ctx)
+        x = N.layer(x, L, G, cache[:, :G.kv_lora], cache[:, G.kv_lora:], pos)
+    h = N.rmsnorm(x, f64(W["final_norm"]), G.eps)
+    z = h @ f64(W["w_lm"][torch.as_tensor(vocab_rows, device=W["w_lm"].device)]).T
+    return h, z
+
+
+def run_step(M, w, W, I):
+    G, bs = w.geom, w.bs
+    ds = M.DSpark(G, W, max_bs=bs, max_ctx=max(I["ctx_list"]))
+    x = torch.empty(bs, G.block, G.hidden, dtype=torch.float32, device="cuda")
+    ds.fuse_ctx(I["aux"], x, bs)
+    x0 = x.clone()
+    kv = ds.make_kv(I["kv_pools"], I["page_table"], I["ctx_len"], max(I["ctx_list"]))
+    h = torch.empty_like(x)
+    z = torch.empty(bs, G.block, G.vocab, dtype=torch.float32, device="cuda")
+    ds.draft_block(x, kv, h, z, bs)
+    assert ds.check() == 0
+    return ds, x0, h, z
+
+
+@pytest.mark.parametrize("w", [FULL_STEP, LONG_STEP, BATCH_STEP], ids=lambda w: w.name)
+def test_full_geometry_draft(M, weights, w):
+    W = weights  # every full-geometry workload draws its weights from seed 1
+    assert w.weight_seed == FULL_STEP.weight_seed
+    I = gen.make_inputs(w, "cuda")
+    ds, x0, h, z = run_step(M, w, W, I)
+    G = w.geom
+    rng = np.random.default_rng(w.input_seed)
+    # fc fusion on 512 sampled output channels of every sequence
+    ch = rng.choice(G.hidden, 512, replace=False)
+    wfc = f64(W["w_fc"][torch.as_tensor(ch, device="cuda")])
+    for b in range(w.bs):
+        ref = N.fuse_ctx(wfc, f64(I["aux"][b]))
+        assert rel_l2(x0[b].cpu().numpy()[:, ch], ref) < TOL
+    rows = np.sort(rng.choice(G.vocab, 4096, replace=False))
+    seqs = [0] if w.bs == 1 else [0, int(np.argmax(I["ctx_list"])), w.bs - 1]
+    for b in seqs:
+        oh, oz = oracle_seq(w, W, I, b, rows)
+        assert rel_l2(h[b].cpu().numpy(), oh) < TOL, b
+        assert rel_l2(z[b].cpu().numpy()[:, rows], oz) < TOL, b
+
+
+@pytest.mark.parametrize("mode,T,top_p", [(0, 1.0, 1.0), (1, 1.0, 0.95)])
+def test_full_vocab_rollout_and_verify(M, weights, mode, T, top_p):
+    G = FULL_STEP.geom
+    bs = 2
+    ds = M.DSpark(G, weights, max_bs=bs)
+    z = gen.draft_logits(bs, G.block, G.vocab, 31)
+    anchor = gen.uniform_tokens((bs,), G.vocab, 31, "anchor")
+    tokens = torch.empty(bs, G.block, dtype=torch.int32, device="cuda")
+    ell = torch.empty(bs, G.block, G.vocab, dtype=torch.float32, device="cuda")
+    smp = M.Sample(mode, mode, T, top_p, 99, 4)
+    ds.markov_rollout(z.cuda(), anchor.cuda(), smp, tokens, ell, bs)
+    assert ds.check() == 0
+    w1, w2 = weights["markov_w1"].cpu(), weights["markov_w2"].cpu()
+    Ps, toks, ells = [], [], []
+    for b in range(bs):
+        t_o, ell_o = S.markov_rollout(z[b].numpy(), w1, w2, int(anchor[b]), mode, T, top_p, seed=99, seq=b, step=4)
+        assert tokens[b].cpu().numpy().tolist() == t_o.tolist()
+        assert np.array_equal(u32(ell[b].cpu().numpy()), u32(ell_o))
+        n = gen.noise((G.block + 1, G.vocab), [0.0, 0.5][b], 31, f"tn{b}").numpy()
+        Ps.append((np.concatenate([ell_o, ell_o[-1:]]) + n).astype(np.float32))
+        toks.append(t_o)
+        ells.append(ell_o)
+    P = torch.from_numpy(np.stack(Ps)).cuda()
+    acc = torch.empty(bs, dtype=torch.int32, device="cuda")
+    out = torch.empty(bs, G.block + 1, dtype=torch.int32, device="cuda")
+    ds.verify(P, torch.from_numpy(np.stack(ells)).cuda(), torch.from_numpy(np.stack(toks)).cuda(), smp, acc, out, bs)
+    assert ds.check() == 0
+    for b in range(bs):
+        if mode == 0:
+            a, o = S.verify_greedy(Ps[b], toks[b])
+        else:
+            a, o = S.verify_prob(Ps[b], ells[b], toks[b], 0, T, top_p, seed=99, seq=b, step=4)
+        assert int(acc[b]) == a and out[b].cpu().numpy().tolist() == o.tolist(), b
+    if mode == 0:
+        assert int(acc[0]) == G.block  # zero noise: the target agrees with every draft
