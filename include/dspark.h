@@ -208,6 +208,25 @@ dspark_status dspark_verify(dspark_handle_t *h, const float *target_logits, cons
                             const dspark_sample_t *sample, int32_t *accept_len, int32_t *out_tokens, int bs,
                             void *ws, size_t ws_bytes, void *stream);
 
+/* fc context fusion without a workspace: the same product as dspark_fuse_ctx,
+ * for callers that cannot allocate device memory for a workspace (a serving
+ * process whose device memory another allocator has already reserved, a
+ * latency-critical path that may not call cudaMalloc, a plugin host that does
+ * not let libraries own device buffers). The model cards have no counterpart:
+ * this is a deployment convenience of this library.
+ * Scratch (split partials, tile counters, an error word) lives in one
+ * ~2.5 MiB array inside the library, resident on every device that loads it
+ * until the process exits. Limits: bs <= 2, hidden <= 131072; larger sizes
+ * return DSPARK_ERR_SHAPE. The first call on a device resolves the array's
+ * device address and sets the kernel's shared-memory limit; make that first
+ * call before any stream capture. Each call clears the counters it needs on
+ * its stream. All calls share the one array: calls that overlap on the GPU
+ * (different streams, or several handles at once) race and must be
+ * serialised by the caller. Device-side errors of this call are not reported
+ * through dspark_check. Allocates nothing.
+ * aux bf16 [bs, block, n_aux, hidden]; x fp32 [bs, block, hidden] (overwritten). */
+dspark_status dspark_fuse_ctx_noalloc(dspark_handle_t *h, const void *aux, float *x, int bs, void *stream);
+
 /* Synchronise the stream, return and clear the device error word
  * (DSPARK_OK if no kernel recorded an error since the last check). */
 dspark_status dspark_check(dspark_handle_t *h, void *ws, void *stream);

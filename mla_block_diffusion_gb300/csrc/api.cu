@@ -226,6 +226,15 @@ dspark_status check_ws(const dspark_handle_t *h, void *ws, size_t ws_bytes, int 
 
 }  // namespace
 
+namespace ds {
+const dspark_geom_t *handle_geom(const dspark_handle_t *h) { return &h->g; }
+int handle_num_sms(const dspark_handle_t *h) { return h->num_sms; }
+const CUtensorMap *handle_fc_map(const dspark_handle_t *h) { return &h->fc; }
+bool encode_bf16_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+    return make_map(m, base, rows, cols, box_rows);
+}
+}  // namespace ds
+
 extern "C" {
 
 const char *dspark_status_str(dspark_status s) {

@@ -84,6 +84,12 @@ struct VerifyParams {
     int *err;
 };
 
+// Read-only views of a handle and the tensor-map encoder (defined with the handle).
+const dspark_geom_t *handle_geom(const dspark_handle_t *h);
+int handle_num_sms(const dspark_handle_t *h);
+const CUtensorMap *handle_fc_map(const dspark_handle_t *h);
+bool encode_bf16_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows);
+
 size_t rollout_scratch_words(int bs, int B, int grid);
 size_t verify_scratch_words(int bs, int B, int grid);
 cudaError_t launch_rollout(RolloutParams p, int grid, cudaStream_t st);

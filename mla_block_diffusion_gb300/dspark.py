@@ -22,7 +22,8 @@ FMT_BF16, FMT_FP8, FMT_NVFP4 = 0, 1, 2
 STATUS = {0: "OK", 1: "ERR_NULL", 2: "ERR_ALIGN", 3: "ERR_SHAPE", 4: "ERR_UNSUPPORTED", 5: "ERR_CUDA",
           6: "ERR_WORKSPACE", 16: "ERR_TIMEOUT", 17: "ERR_BAD_INPUT", 18: "ERR_OOB"}
 EXPORTS = ("dspark_create", "dspark_destroy", "dspark_workspace_bytes", "dspark_fuse_ctx", "dspark_draft_block",
-           "dspark_markov_rollout", "dspark_confidence", "dspark_verify", "dspark_check", "dspark_status_str")
+           "dspark_markov_rollout", "dspark_confidence", "dspark_verify", "dspark_check", "dspark_status_str",
+           "dspark_fuse_ctx_noalloc")
 
 
 class Geom(C.Structure):
@@ -86,6 +87,7 @@ def lib():
         L.dspark_confidence.argtypes = [vp, vp, vp, i, vp]
         L.dspark_verify.argtypes = [vp, vp, vp, vp, C.POINTER(Sample), vp, vp, i, vp, sz, vp]
         L.dspark_check.argtypes = [vp, vp, vp]
+        L.dspark_fuse_ctx_noalloc.argtypes = [vp, vp, vp, i, vp]
         L.dspark_status_str.argtypes = [i]
         L.dspark_status_str.restype = C.c_char_p
         for f in EXPORTS:
@@ -178,6 +180,10 @@ class DSpark:
     def fuse_ctx(self, aux: torch.Tensor, x: torch.Tensor, bs: int):
         _chk("dspark_fuse_ctx", lib().dspark_fuse_ctx(self.h, _p(aux), _p(x), bs, _p(self.ws), self.ws_bytes,
                                                        _stream()))
+
+    def fuse_ctx_noalloc(self, aux: torch.Tensor, x: torch.Tensor, bs: int):
+        """fc fusion with the library's own fixed scratch instead of the workspace."""
+        _chk("dspark_fuse_ctx_noalloc", lib().dspark_fuse_ctx_noalloc(self.h, _p(aux), _p(x), bs, _stream()))
 
     def make_kv(self, pools: Sequence[torch.Tensor], page_table: torch.Tensor, ctx_len: torch.Tensor,
                 max_ctx: int) -> KV:
