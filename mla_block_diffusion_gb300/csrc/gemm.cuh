@@ -97,6 +97,66 @@ __device__ inline void gemm_store_swiglu(const GemmParams &p, int n, int m, floa
     p.out_bf16[(size_t)m * p.ldo + n] = __float2bfloat16(silu_f(g) * u);
 }
 
+// Sum of the split partials of one tile, contributors in increasing CTA order
+// (fixed order: the result does not depend on which CTA arrived last). Thread
+// et owns output channel et; every partial row is read as float4 vectors, four
+// contributors at a time, so the loads are independent and overlap.
+template <int BN>
+__device__ __forceinline__ void gemm_reduce_tile(const GemmParams &p, int tile, int c_lo, int c_hi, int et, int nch) {
+    const int n = tile * nch + et;
+    if (et >= nch || n >= p.n_out) return;
+    for (int c0 = 0; c0 < p.M; c0 += 16) {
+        float a1[16], a2[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) a1[j] = a2[j] = 0.f;
+        for (int cc = c_lo; cc <= c_hi; cc += 4) {
+            float4 v1[4][4], v2[4][4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (cc + u <= c_hi) {
+                    const int first_t = (int)(gemm_unit_begin(cc + u, p.units, p.grid) / p.KB);
+                    const int sl = (tile == first_t) ? 2 * (cc + u) : 2 * (cc + u) + 1;
+                    const float4 *src = (const float4 *)(p.partials + ((size_t)sl * 128 + et) * BN + c0);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) v1[u][j] = __ldcg(src + j);
+                    if (p.paired) {
+                        const float4 *src2 = src + 64 * BN / 4;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) v2[u][j] = __ldcg(src2 + j);
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (cc + u <= c_hi) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        a1[4 * j] += v1[u][j].x;
+                        a1[4 * j + 1] += v1[u][j].y;
+                        a1[4 * j + 2] += v1[u][j].z;
+                        a1[4 * j + 3] += v1[u][j].w;
+                        if (p.paired) {
+                            a2[4 * j] += v2[u][j].x;
+                            a2[4 * j + 1] += v2[u][j].y;
+                            a2[4 * j + 2] += v2[u][j].z;
+                            a2[4 * j + 3] += v2[u][j].w;
+                        }
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            if (c0 + j < p.M) {
+                if (p.paired)
+                    gemm_store_swiglu(p, n, c0 + j, a1[j], a2[j]);
+                else
+                    gemm_store(p, n, c0 + j, a1[j]);
+            }
+        }
+    }
+}
+
 template <int BN>
 __global__ void __launch_bounds__(192, 1)
     gemm_swapab_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
@@ -278,23 +338,7 @@ __global__ void __launch_bounds__(192, 1)
                 named_bar_sync(1, 128);
                 if (s_last) {
                     __threadfence();
-                    const int n = tile * nch + et;
-                    if (et < nch && n < p.n_out) {
-                        for (int m = 0; m < p.M; ++m) {
-                            float s1 = 0.f, s2 = 0.f;
-                            for (int cc = c_lo; cc <= c_hi; ++cc) {
-                                const int first_t = (int)(gemm_unit_begin(cc, p.units, p.grid) / p.KB);
-                                const int sl = (tile == first_t) ? 2 * cc : 2 * cc + 1;
-                                const float *src = p.partials + (size_t)sl * 128 * BN;
-                                s1 += __ldcg(src + (size_t)et * BN + m);
-                                if (p.paired) s2 += __ldcg(src + (size_t)(et + 64) * BN + m);
-                            }
-                            if (p.paired)
-                                gemm_store_swiglu(p, n, m, s1, s2);
-                            else
-                                gemm_store(p, n, m, s1);
-                        }
-                    }
+                    gemm_reduce_tile<BN>(p, tile, c_lo, c_hi, et, nch);
                 }
             }
             u = seg_end;

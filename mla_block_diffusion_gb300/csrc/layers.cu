@@ -12,6 +12,15 @@
 
 namespace ds {
 
+// cos/sin of pos * inv_freq: the angle is reduced modulo 2 pi in fp64 (a few
+// fp64 operations, exact enough at positions ~10^5), then evaluated in fp32.
+DS_DEVINL void rope_cs(double pos, double inv_freq, float &c, float &s) {
+    const double two_pi = 6.283185307179586476925286766559;
+    const double a = pos * inv_freq;
+    const double r = a - two_pi * rint(a / two_pi);
+    sincosf((float)r, &s, &c);
+}
+
 __device__ float block_sum(float v, float *red) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
     v = warp_sum(v);
@@ -87,9 +96,8 @@ __global__ void latent_kernel(const float *__restrict__ qkv, int ld, int q_lora,
     }
     const double pos = (double)(c + i);
     for (int p = threadIdx.x; p < d_rope / 2; p += blockDim.x) {
-        double s, co;
-        sincos(pos * rt.inv_freq[p], &s, &co);
-        const float fs = (float)s, fc = (float)co;
+        float fc, fs;
+        rope_cs(pos, rt.inv_freq[p], fc, fs);
         const float x0 = row[q_lora + kv_lora + 2 * p], x1 = row[q_lora + kv_lora + 2 * p + 1];
         blk_kv[(size_t)m * kvd + kv_lora + 2 * p] = __float2bfloat16(x0 * fc - x1 * fs);
         blk_kv[(size_t)m * kvd + kv_lora + 2 * p + 1] = __float2bfloat16(x0 * fs + x1 * fc);
@@ -98,91 +106,151 @@ __global__ void latent_kernel(const float *__restrict__ qkv, int ld, int q_lora,
 
 // ---------------------------------------------------------------------------
 // q absorption: Q_h = [W_kb,h^T q_nope,h || RoPE(q_rope,h)] per row and head,
-// bf16 [M, n_h, kv_lora + d_rope]. Grid (n_h, ceil(M / 16)); each thread owns
-// two latent columns and accumulates 16 rows over d_nope in fp32.
+// bf16 [M, n_h, kv_lora + d_rope]. Grid (n_h, kv_lora / 64): a CTA owns one
+// head and 64 latent columns; its 256 threads split d_nope into 8 groups x 32
+// column pairs, hold their slice of W_kb in registers (loaded once, all loads
+// independent) and sweep the rows in chunks of 16; the 8 partial sums are
+// added in group order through shared memory.
 // ---------------------------------------------------------------------------
 constexpr int kAbsorbRows = 16;
+constexpr int kQAbsCols = 64;
 
-__global__ void q_absorb_kernel(const float *__restrict__ q, int M, int n_h, int d_nope, int d_rope, int kv_lora,
-                                int d_v, const __nv_bfloat16 *__restrict__ w_kvb, const int32_t *__restrict__ ctx_len,
-                                int block, int max_ctx, RopeTable rt, __nv_bfloat16 *__restrict__ qt) {
-    extern __shared__ float sq[];  // [kAbsorbRows][d_nope]
-    const int h = blockIdx.x, m0 = blockIdx.y * kAbsorbRows;
+__global__ void __launch_bounds__(256) q_absorb_kernel(const float *__restrict__ q, int M, int n_h, int d_nope,
+                                                       int d_rope, int kv_lora, int d_v,
+                                                       const __nv_bfloat16 *__restrict__ w_kvb,
+                                                       const int32_t *__restrict__ ctx_len, int block, int max_ctx,
+                                                       RopeTable rt, __nv_bfloat16 *__restrict__ qt) {
+    extern __shared__ float sm[];
+    float *sq = sm;                               // [kAbsorbRows][d_nope]
+    float *red = sm + kAbsorbRows * d_nope;       // [8][kAbsorbRows][kQAbsCols]
+    const int h = blockIdx.x, c0 = blockIdx.y * kQAbsCols;
+    const int cp = threadIdx.x & 31, dg = threadIdx.x >> 5;
+    const int dper = d_nope / 8;
     const int qhd = d_nope + d_rope, kvd = kv_lora + d_rope;
-    for (int idx = threadIdx.x; idx < kAbsorbRows * d_nope; idx += blockDim.x) {
-        const int mm = idx / d_nope, d = idx % d_nope, m = m0 + mm;
-        sq[idx] = (m < M) ? q[((size_t)m * n_h + h) * qhd + d] : 0.f;
-    }
-    __syncthreads();
-    const __nv_bfloat16 *W = w_kvb + (size_t)h * (d_nope + d_v) * kv_lora;
-    for (int c = 2 * threadIdx.x; c < kv_lora; c += 2 * blockDim.x) {
+    const __nv_bfloat16 *W = w_kvb + (size_t)h * (d_nope + d_v) * kv_lora + c0 + 2 * cp;
+    float2 w[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+        w[i] = i < dper ? __bfloat1622float2(*(const __nv_bfloat162 *)(W + (size_t)(dg * dper + i) * kv_lora))
+                        : make_float2(0.f, 0.f);
+    for (int m0 = 0; m0 < M; m0 += kAbsorbRows) {
+        for (int idx = threadIdx.x; idx < kAbsorbRows * d_nope; idx += blockDim.x) {
+            const int mm = idx / d_nope, d = idx % d_nope, m = m0 + mm;
+            sq[idx] = (m < M) ? q[((size_t)m * n_h + h) * qhd + d] : 0.f;
+        }
+        __syncthreads();
         float a0[kAbsorbRows], a1[kAbsorbRows];
 #pragma unroll
         for (int mm = 0; mm < kAbsorbRows; ++mm) a0[mm] = a1[mm] = 0.f;
-        for (int d = 0; d < d_nope; ++d) {
-            const float2 w = __bfloat1622float2(*(const __nv_bfloat162 *)(W + (size_t)d * kv_lora + c));
 #pragma unroll
-            for (int mm = 0; mm < kAbsorbRows; ++mm) {
-                const float s = sq[mm * d_nope + d];
-                a0[mm] = fmaf(w.x, s, a0[mm]);
-                a1[mm] = fmaf(w.y, s, a1[mm]);
+        for (int i = 0; i < 32; ++i) {
+            if (i < dper) {
+#pragma unroll
+                for (int mm = 0; mm < kAbsorbRows; ++mm) {
+                    const float x = sq[mm * d_nope + dg * dper + i];
+                    a0[mm] = fmaf(w[i].x, x, a0[mm]);
+                    a1[mm] = fmaf(w[i].y, x, a1[mm]);
+                }
             }
         }
 #pragma unroll
-        for (int mm = 0; mm < kAbsorbRows; ++mm) {
-            const int m = m0 + mm;
-            if (m < M)
-                *(__nv_bfloat162 *)(qt + ((size_t)m * n_h + h) * kvd + c) = __floats2bfloat162_rn(a0[mm], a1[mm]);
+        for (int mm = 0; mm < kAbsorbRows; ++mm)
+            *(float2 *)(red + ((size_t)dg * kAbsorbRows + mm) * kQAbsCols + 2 * cp) = make_float2(a0[mm], a1[mm]);
+        __syncthreads();
+        for (int idx = threadIdx.x; idx < kAbsorbRows * kQAbsCols / 2; idx += blockDim.x) {
+            const int mm = idx / (kQAbsCols / 2), c2 = 2 * (idx % (kQAbsCols / 2)), m = m0 + mm;
+            float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+                const float2 v = *(const float2 *)(red + ((size_t)g * kAbsorbRows + mm) * kQAbsCols + c2);
+                s0 += v.x;
+                s1 += v.y;
+            }
+            if (m < M) *(__nv_bfloat162 *)(qt + ((size_t)m * n_h + h) * kvd + c0 + c2) = __floats2bfloat162_rn(s0, s1);
         }
+        __syncthreads();
     }
-    const int np = d_rope / 2;
-    for (int idx = threadIdx.x; idx < kAbsorbRows * np; idx += blockDim.x) {
-        const int mm = idx / np, p = idx % np, m = m0 + mm;
-        if (m >= M) continue;
-        int c = ctx_len[m / block];
-        if (c < 0 || c > max_ctx) c = 0;
-        double s, co;
-        sincos((double)(c + m % block) * rt.inv_freq[p], &s, &co);
-        const float fs = (float)s, fc = (float)co;
-        const float *src = q + ((size_t)m * n_h + h) * qhd + d_nope;
-        const float x0 = src[2 * p], x1 = src[2 * p + 1];
-        __nv_bfloat16 *dst = qt + ((size_t)m * n_h + h) * kvd + kv_lora;
-        dst[2 * p] = __float2bfloat16(x0 * fc - x1 * fs);
-        dst[2 * p + 1] = __float2bfloat16(x0 * fs + x1 * fc);
+    if (blockIdx.y == 0) {
+        const int np = d_rope / 2;
+        for (int idx = threadIdx.x; idx < M * np; idx += blockDim.x) {
+            const int m = idx / np, p = idx % np;
+            int c = ctx_len[m / block];
+            if (c < 0 || c > max_ctx) c = 0;
+            float fc, fs;
+            rope_cs((double)(c + m % block), rt.inv_freq[p], fc, fs);
+            const float *src = q + ((size_t)m * n_h + h) * qhd + d_nope;
+            const float x0 = src[2 * p], x1 = src[2 * p + 1];
+            __nv_bfloat16 *dst = qt + ((size_t)m * n_h + h) * kvd + kv_lora;
+            dst[2 * p] = __float2bfloat16(x0 * fc - x1 * fs);
+            dst[2 * p + 1] = __float2bfloat16(x0 * fs + x1 * fc);
+        }
     }
 }
 
 // ---------------------------------------------------------------------------
 // v absorption: o_h = W_vb,h o_lat,h -> bf16 [M, n_h * d_v] (operand of o_proj).
-// Grid (n_h, ceil(M / 16)); a warp per output channel e, lanes over the latent.
+// Grid (n_h, d_v / 16): a CTA owns 16 output channels of one head; 16 threads
+// per channel each hold 8-element slices of the channel's W_vb row (16-byte
+// loads, all independent, read once) and the rows sweep in chunks of 16 from
+// shared memory; the 16 partial dots are reduced with shuffles.
 // ---------------------------------------------------------------------------
-__global__ void v_absorb_kernel(const float *__restrict__ o_lat, int M, int n_h, int d_nope, int d_v, int kv_lora,
-                                const __nv_bfloat16 *__restrict__ w_kvb, __nv_bfloat16 *__restrict__ out) {
+__global__ void __launch_bounds__(256) v_absorb_kernel(const float *__restrict__ o_lat, int M, int n_h, int d_nope,
+                                                       int d_v, int kv_lora, const __nv_bfloat16 *__restrict__ w_kvb,
+                                                       __nv_bfloat16 *__restrict__ out) {
     extern __shared__ float so[];  // [kAbsorbRows][kv_lora]
-    const int h = blockIdx.x, m0 = blockIdx.y * kAbsorbRows;
-    for (int idx = threadIdx.x; idx < kAbsorbRows * kv_lora; idx += blockDim.x) {
-        const int mm = idx / kv_lora, c = idx % kv_lora, m = m0 + mm;
-        so[idx] = (m < M) ? o_lat[((size_t)m * n_h + h) * kv_lora + c] : 0.f;
-    }
-    __syncthreads();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-    for (int e = warp; e < d_v; e += nw) {
-        const __nv_bfloat16 *W = w_kvb + ((size_t)h * (d_nope + d_v) + d_nope + e) * kv_lora;
-        float acc[kAbsorbRows];
+    const int h = blockIdx.x, e = blockIdx.y * 16 + (threadIdx.x >> 4), cg = threadIdx.x & 15;
+    const __nv_bfloat16 *W = w_kvb + ((size_t)h * (d_nope + d_v) + d_nope + e) * kv_lora;
+    const int nj = (kv_lora + 127) / 128;  // <= 4
+    float wv[4][8];
 #pragma unroll
-        for (int mm = 0; mm < kAbsorbRows; ++mm) acc[mm] = 0.f;
-        for (int c = 2 * lane; c < kv_lora; c += 64) {
-            const float2 w = __bfloat1622float2(*(const __nv_bfloat162 *)(W + c));
+    for (int j = 0; j < 4; ++j) {
+        const int c = cg * 8 + 128 * j;
+        if (j < nj && c < kv_lora) {
+            const uint4 u = *(const uint4 *)(W + c);
+            const __nv_bfloat162 *b2 = (const __nv_bfloat162 *)&u;
 #pragma unroll
-            for (int mm = 0; mm < kAbsorbRows; ++mm)
-                acc[mm] = fmaf(w.x, so[mm * kv_lora + c], fmaf(w.y, so[mm * kv_lora + c + 1], acc[mm]));
+            for (int t = 0; t < 4; ++t) {
+                const float2 f = __bfloat1622float2(b2[t]);
+                wv[j][2 * t] = f.x;
+                wv[j][2 * t + 1] = f.y;
+            }
+        } else {
+#pragma unroll
+            for (int t = 0; t < 8; ++t) wv[j][t] = 0.f;
         }
+    }
+    for (int m0 = 0; m0 < M; m0 += kAbsorbRows) {
+        for (int idx = threadIdx.x; idx < kAbsorbRows * kv_lora / 4; idx += blockDim.x) {
+            const int mm = idx / (kv_lora / 4), c4 = idx % (kv_lora / 4), m = m0 + mm;
+            ((float4 *)so)[idx] = (m < M) ? ((const float4 *)(o_lat + ((size_t)m * n_h + h) * kv_lora))[c4]
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        __syncthreads();
 #pragma unroll
         for (int mm = 0; mm < kAbsorbRows; ++mm) {
-            const float v = warp_sum(acc[mm]);
+            float acc = 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int c = cg * 8 + 128 * j;
+                if (j < nj && c < kv_lora) {
+                    const float4 x0 = *(const float4 *)(so + mm * kv_lora + c);
+                    const float4 x1 = *(const float4 *)(so + mm * kv_lora + c + 4);
+                    acc = fmaf(wv[j][0], x0.x, acc);
+                    acc = fmaf(wv[j][1], x0.y, acc);
+                    acc = fmaf(wv[j][2], x0.z, acc);
+                    acc = fmaf(wv[j][3], x0.w, acc);
+                    acc = fmaf(wv[j][4], x1.x, acc);
+                    acc = fmaf(wv[j][5], x1.y, acc);
+                    acc = fmaf(wv[j][6], x1.z, acc);
+                    acc = fmaf(wv[j][7], x1.w, acc);
+                }
+            }
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
             const int m = m0 + mm;
-            if (lane == 0 && m < M) out[(size_t)m * n_h * d_v + (size_t)h * d_v + e] = __float2bfloat16(v);
+            if (cg == 0 && m < M) out[(size_t)m * n_h * d_v + (size_t)h * d_v + e] = __float2bfloat16(acc);
         }
+        __syncthreads();
     }
 }
 
@@ -410,28 +478,41 @@ __global__ void __launch_bounds__(256, 1) mla_attention_kernel(const AttnParams 
 }
 
 // Fixed-order merge of the split partials: o = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s.
+// The split weights are formed once in shared memory; each thread then reads
+// its 4 columns of every split with independent loads.
 __global__ void attn_combine_kernel(const float *__restrict__ part_o, const float *__restrict__ part_ml, int splits,
                                     int R, int DV, float *__restrict__ o_lat) {
+    __shared__ float sw[64];
+    __shared__ float sml[64][2];
+    __shared__ float sinv;
     const int r = blockIdx.x, b = blockIdx.y;
     const size_t base = (size_t)b * splits * R + r;
-    float M = -INFINITY;
-    for (int s = 0; s < splits; ++s) {
-        const float ls = part_ml[(base + (size_t)s * R) * 2 + 1];
-        if (ls > 0.f) M = fmaxf(M, part_ml[(base + (size_t)s * R) * 2]);
+    if (threadIdx.x < splits) {
+        const float2 ml = *(const float2 *)(part_ml + (base + (size_t)threadIdx.x * R) * 2);
+        sml[threadIdx.x][0] = ml.x;
+        sml[threadIdx.x][1] = ml.y;
     }
-    float den = 0.f;
-    for (int s = 0; s < splits; ++s) {
-        const float ms = part_ml[(base + (size_t)s * R) * 2], ls = part_ml[(base + (size_t)s * R) * 2 + 1];
-        if (ls > 0.f) den += exp2f(ms - M) * ls;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float M = -INFINITY;
+        for (int s = 0; s < splits; ++s)
+            if (sml[s][1] > 0.f) M = fmaxf(M, sml[s][0]);
+        float den = 0.f;
+        for (int s = 0; s < splits; ++s) {
+            const float w = sml[s][1] > 0.f ? exp2f(sml[s][0] - M) : 0.f;
+            sw[s] = w;
+            den += w * sml[s][1];
+        }
+        sinv = den > 0.f ? 1.f / den : 0.f;
     }
-    const float inv = den > 0.f ? 1.f / den : 0.f;
+    __syncthreads();
+    const float inv = sinv;
     for (int c = threadIdx.x * 4; c < DV; c += blockDim.x * 4) {
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
         for (int s = 0; s < splits; ++s) {
-            const float ms = part_ml[(base + (size_t)s * R) * 2], ls = part_ml[(base + (size_t)s * R) * 2 + 1];
-            if (!(ls > 0.f)) continue;
-            const float w = exp2f(ms - M);
-            const float4 v = *(const float4 *)(part_o + (base + (size_t)s * R) * DV + c);
+            const float w = sw[s];
+            const float4 v = __ldcg((const float4 *)(part_o + (base + (size_t)s * R) * DV + c));
             acc.x += w * v.x;
             acc.y += w * v.y;
             acc.z += w * v.z;
@@ -474,19 +555,16 @@ cudaError_t launch_latent(const float *qkv, int ld, int q_lora, int kv_lora, int
 cudaError_t launch_q_absorb(const float *q, int M, int n_h, int d_nope, int d_rope, int kv_lora, int d_v,
                             const __nv_bfloat16 *w_kvb, const int32_t *ctx_len, int block, int max_ctx,
                             const RopeTable &rt, __nv_bfloat16 *qt, cudaStream_t st) {
-    dim3 grid(n_h, (M + kAbsorbRows - 1) / kAbsorbRows);
-    int threads = kv_lora / 2;
-    if (threads > 256) threads = 256;
-    if (threads < 32) threads = 32;
-    const size_t smem = (size_t)kAbsorbRows * d_nope * sizeof(float);
-    q_absorb_kernel<<<grid, threads, smem, st>>>(q, M, n_h, d_nope, d_rope, kv_lora, d_v, w_kvb, ctx_len, block,
-                                                 max_ctx, rt, qt);
+    dim3 grid(n_h, kv_lora / kQAbsCols);
+    const size_t smem = ((size_t)kAbsorbRows * d_nope + (size_t)8 * kAbsorbRows * kQAbsCols) * sizeof(float);
+    q_absorb_kernel<<<grid, 256, smem, st>>>(q, M, n_h, d_nope, d_rope, kv_lora, d_v, w_kvb, ctx_len, block, max_ctx,
+                                             rt, qt);
     return cudaGetLastError();
 }
 
 cudaError_t launch_v_absorb(const float *o_lat, int M, int n_h, int d_nope, int d_v, int kv_lora,
                             const __nv_bfloat16 *w_kvb, __nv_bfloat16 *out, cudaStream_t st) {
-    dim3 grid(n_h, (M + kAbsorbRows - 1) / kAbsorbRows);
+    dim3 grid(n_h, d_v / 16);
     const size_t smem = (size_t)kAbsorbRows * kv_lora * sizeof(float);
     v_absorb_kernel<<<grid, 256, smem, st>>>(o_lat, M, n_h, d_nope, d_v, kv_lora, w_kvb, out);
     return cudaGetLastError();

@@ -385,6 +385,81 @@ struct RollLayout {
 
 size_t rollout_scratch_words(int bs, int B, int grid) { return RollLayout(bs, B, grid).total; }
 
+DS_DEVINL uint64_t policy_evict_last() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// 32-bit global load that asks L2 to keep the line (w2 is re-read every step).
+DS_DEVINL uint32_t ld_keep(const void *ptr, uint64_t pol) {
+    uint32_t v;
+    asm volatile("ld.global.L2::cache_hint.b32 %0, [%1], %2;" : "=r"(v) : "l"(ptr), "l"(pol));
+    return v;
+}
+
+// ell_i for NB sequences over this CTA's pairs: 16 w2 words are loaded ahead of
+// each run of 16 FMAs so the loads overlap; the chain over k stays in order.
+// Each CTA max-reduces its greedy keys (or its maxima of ell / T) into amax[b].
+template <int NB>
+__device__ void rollout_logits(const RolloutParams &p, int i, int b0, int nb, int lo, int hi,
+                               const float (*s_w1)[256], unsigned long long *amax, unsigned long long *red,
+                               uint64_t w2pol) {
+    const int V = p.V, r = p.r;
+    const uint32_t *w2 = (const uint32_t *)p.w2;  // bf16 pairs
+    unsigned long long best[NB];
+#pragma unroll
+    for (int bb = 0; bb < NB; ++bb) best[bb] = 0;
+    bool bad = false;
+    for (int pp = lo + threadIdx.x; pp < hi; pp += blockDim.x) {
+        float a0[NB], a1[NB];
+#pragma unroll
+        for (int bb = 0; bb < NB; ++bb) a0[bb] = a1[bb] = 0.f;
+        for (int k0 = 0; k0 < r; k0 += 16) {
+            uint32_t wv[16];
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk)
+                wv[kk] = (k0 + kk < r) ? ld_keep(w2 + ((size_t)(k0 + kk) * V) / 2 + pp, w2pol) : 0u;
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk) {
+                if (k0 + kk < r) {
+                    const float wx = __uint_as_float(wv[kk] << 16), wy = __uint_as_float(wv[kk] & 0xFFFF0000u);
+#pragma unroll
+                    for (int bb = 0; bb < NB; ++bb) {
+                        a0[bb] = __fmaf_rn(s_w1[bb][k0 + kk], wx, a0[bb]);
+                        a1[bb] = __fmaf_rn(s_w1[bb][k0 + kk], wy, a1[bb]);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int bb = 0; bb < NB; ++bb) {
+            if (bb < nb) {
+                const int b = b0 + bb;
+                const size_t off = ((size_t)b * p.B + i) * V + 2 * pp;
+                const float2 z = *(const float2 *)(p.z + off);
+                const float l0 = __fadd_rn(z.x, a0[bb]), l1 = __fadd_rn(z.y, a1[bb]);
+                *(float2 *)(p.ell + off) = make_float2(l0, l1);
+                if (!isfinite(l0) || !isfinite(l1)) bad = true;
+                unsigned long long k0, k1;
+                if (p.draft_mode == DSPARK_GREEDY) {
+                    k0 = argmax_key(l0, 2 * pp);
+                    k1 = argmax_key(l1, 2 * pp + 1);
+                } else {
+                    k0 = f2ord(__fdiv_rn(l0, p.T));
+                    k1 = f2ord(__fdiv_rn(l1, p.T));
+                }
+                best[bb] = max(best[bb], max(k0, k1));
+            }
+        }
+    }
+    if (bad) set_error(p.err, DSPARK_ERR_BAD_INPUT);
+    for (int bb = 0; bb < nb; ++bb) {
+        const unsigned long long m = block_max_u64(best[bb], red);
+        if (threadIdx.x == 0) atomicMax(&amax[b0 + bb], m);
+    }
+}
+
 __global__ void __launch_bounds__(kSampThreads, 1) rollout_kernel(RolloutParams p) {
     __shared__ NucleusSmem sm;
     __shared__ DrawSmem dsm;
@@ -410,7 +485,7 @@ __global__ void __launch_bounds__(kSampThreads, 1) rollout_kernel(RolloutParams 
     if (!grid_barrier(p.ctl, &s_fail, p.err)) return;
     int lo, hi;
     pair_slice(V / 2, lo, hi);
-    const __nv_bfloat162 *w2 = (const __nv_bfloat162 *)p.w2;
+    const uint64_t w2pol = policy_evict_last();
 
     for (int i = 0; i < p.B; ++i) {
         // ell_i = z_i + fp32 FMA chain of w1[t_{i-1}] against w2 (k in order)
@@ -421,48 +496,10 @@ __global__ void __launch_bounds__(kSampThreads, 1) rollout_kernel(RolloutParams 
                 s_w1[bb][k] = bb < nb ? __bfloat162float(p.w1[(size_t)s_prev[b0 + bb] * r + k]) : 0.f;
             }
             __syncthreads();
-            unsigned long long best[kRollChunk];
-#pragma unroll
-            for (int bb = 0; bb < kRollChunk; ++bb) best[bb] = 0;
-            bool bad = false;
-            for (int pp = lo + threadIdx.x; pp < hi; pp += blockDim.x) {
-                float a0[kRollChunk], a1[kRollChunk];
-#pragma unroll
-                for (int bb = 0; bb < kRollChunk; ++bb) a0[bb] = a1[bb] = 0.f;
-                for (int k = 0; k < r; ++k) {
-                    const float2 w = __bfloat1622float2(w2[((size_t)k * V) / 2 + pp]);
-#pragma unroll
-                    for (int bb = 0; bb < kRollChunk; ++bb) {
-                        a0[bb] = __fmaf_rn(s_w1[bb][k], w.x, a0[bb]);
-                        a1[bb] = __fmaf_rn(s_w1[bb][k], w.y, a1[bb]);
-                    }
-                }
-#pragma unroll
-                for (int bb = 0; bb < kRollChunk; ++bb) {
-                    if (bb < nb) {
-                        const int b = b0 + bb;
-                        const size_t off = ((size_t)b * p.B + i) * V + 2 * pp;
-                        const float2 z = *(const float2 *)(p.z + off);
-                        const float l0 = __fadd_rn(z.x, a0[bb]), l1 = __fadd_rn(z.y, a1[bb]);
-                        *(float2 *)(p.ell + off) = make_float2(l0, l1);
-                        if (!isfinite(l0) || !isfinite(l1)) bad = true;
-                        unsigned long long k0, k1;
-                        if (p.draft_mode == DSPARK_GREEDY) {
-                            k0 = argmax_key(l0, 2 * pp);
-                            k1 = argmax_key(l1, 2 * pp + 1);
-                        } else {
-                            k0 = f2ord(__fdiv_rn(l0, p.T));
-                            k1 = f2ord(__fdiv_rn(l1, p.T));
-                        }
-                        best[bb] = max(best[bb], max(k0, k1));
-                    }
-                }
-            }
-            if (bad) set_error(p.err, DSPARK_ERR_BAD_INPUT);
-            for (int bb = 0; bb < nb; ++bb) {
-                const unsigned long long m = block_max_u64(best[bb], sm.red);
-                if (threadIdx.x == 0) atomicMax(&sc[L.amax + (size_t)i * p.bs + b0 + bb], m);
-            }
+            if (nb == 1)
+                rollout_logits<1>(p, i, b0, 1, lo, hi, s_w1, sc + L.amax + (size_t)i * p.bs, sm.red, w2pol);
+            else
+                rollout_logits<kRollChunk>(p, i, b0, nb, lo, hi, s_w1, sc + L.amax + (size_t)i * p.bs, sm.red, w2pol);
             __syncthreads();
         }
         if (!grid_barrier(p.ctl, &s_fail, p.err)) return;
