@@ -203,8 +203,11 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--lm-rows", type=int, default=4096)
-    ap.add_argument("--only", choices=["fc"], default=None,
-                    help="time one kernel alone (fc: the fusion GEMM at full shape, for profiling)")
+    ap.add_argument("--only", choices=["fc", "rollout", "layer"], default=None,
+                    help="time one call alone for profiling: fc (the fusion GEMM; full shape unless --fc-hidden), "
+                         "rollout (Markov rollout, full vocabulary), layer (one full-width MLA layer, ctx 4096)")
+    ap.add_argument("--fc-hidden", type=int, default=0, help="--only fc: hidden size (output channels)")
+    ap.add_argument("--fc-aux", type=int, default=0, help="--only fc: captured states (K = aux * hidden)")
     args = ap.parse_args()
     assert args.warmup >= 3 or args.impl == "reference", "at least 3 warm-up steps"
 
@@ -222,6 +225,8 @@ def main():
 
     if args.only == "fc":
         return only_fc(args, G, world, rank, local)
+    if args.only in ("rollout", "layer"):
+        return only_call(args, G, local)
 
     if args.impl == "reference":
         if rank != 0:
@@ -438,6 +443,8 @@ def only_fc(args, G, world, rank, local):
     torch.cuda.set_device(local)
     g = replace(G, n_layers=1, n_heads=4, q_lora=64, kv_lora=64, d_nope=32, d_rope=16, d_v=16, inter=64, vocab=128,
                 rank=16)
+    if args.fc_hidden:
+        g = replace(g, hidden=args.fc_hidden, n_aux=args.fc_aux or G.n_aux)
     w = replace(FULL_STEP, geom=g)
     W = gen.make_weights(w, "cuda")
     aux = gen.make_inputs(w, "cuda")["aux"]
@@ -460,6 +467,55 @@ def only_fc(args, G, world, rank, local):
         print(json.dumps({"kernel": "gemm_swapab_kernel<16> fc fusion", "avg_launch_ms": ms,
                           "algorithmic_bytes_per_launch": nbytes, "achieved_GBps": nbytes / (ms * 1e-3) / 1e9,
                           "peak_GBps": pk["hbm_gbs"], "peak_source": src}))
+
+
+def only_call(args, G, local):
+    """One API call alone on a drafter shrunk everywhere else (for ncu captures):
+    rollout: full vocabulary and rank (w1, w2 84 MB each), greedy;
+    layer: one layer of full attention width (64 heads, latent 512 + 64) at ctx 4096."""
+    from dataclasses import replace
+    import mla_block_diffusion_gb300 as M
+    from mla_block_diffusion_gb300 import build as libbuild
+    from synthetic import generate as gen
+    from synthetic.configs import FULL_STEP
+    libbuild.build()
+    torch.cuda.set_device(local)
+    if args.only == "rollout":
+        g = replace(G, hidden=64, n_aux=1, n_layers=1, n_heads=1, q_lora=64, kv_lora=64, d_nope=8, d_rope=16, d_v=64,
+                    inter=64)
+    else:
+        g = replace(G, hidden=1024, n_aux=1, n_layers=1, q_lora=256, inter=64, vocab=128, rank=16)
+    w = replace(FULL_STEP, geom=g)
+    W = gen.make_weights(w, "cuda")
+    I = gen.make_inputs(w, "cuda")
+    ctx = I["ctx_list"][0]
+    ds = M.DSpark(g, W, max_bs=1, max_ctx=ctx)
+    x = torch.empty(1, g.block, g.hidden, dtype=torch.float32, device="cuda")
+    h = torch.empty_like(x)
+    z = gen.draft_logits(1, g.block, g.vocab, 1, device="cuda")
+    ell = torch.empty_like(z)
+    tokens = torch.empty(1, g.block, dtype=torch.int32, device="cuda")
+    kv = ds.make_kv(I["kv_pools"], I["page_table"], I["ctx_len"], ctx)
+    smp = M.Sample(M.GREEDY, M.GREEDY, 1.0, 1.0, 1, 0)
+
+    def call():
+        if args.only == "rollout":
+            ds.markov_rollout(z, I["anchor"], smp, tokens, ell, 1)
+        else:
+            ds.fuse_ctx(I["aux"], x, 1)
+            ds.draft_block(x, kv, h, z, 1)
+
+    for _ in range(args.warmup):
+        call()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for a_, b_ in evs:
+        a_.record()
+        call()
+        b_.record()
+    torch.cuda.synchronize()
+    assert ds.check() == 0
+    print(json.dumps({"only": args.only, "avg_call_ms": statistics.mean(a_.elapsed_time(b_) for a_, b_ in evs)}))
 
 
 def ds_layout_splits(ds) -> int:

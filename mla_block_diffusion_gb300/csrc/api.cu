@@ -158,8 +158,7 @@ cudaError_t gemm_t(const CUtensorMap &A, const CUtensorMap &A2, const CUtensorMa
     if (grid > num_sms) grid = num_sms;
     if (grid < 1) grid = 1;
     p.grid = (int)grid;
-    gemm_swapab_kernel<BN><<<p.grid, 192, C::kSmemBytes, st>>>(A, A2, B, p);
-    return cudaGetLastError();
+    return launch_pdl(gemm_swapab_kernel<BN>, dim3(p.grid), dim3(192), (size_t)C::kSmemBytes, st, A, A2, B, p);
 }
 
 cudaError_t gemm(const dspark_handle *h, const CUtensorMap &A, const CUtensorMap *A2, const CUtensorMap &B, int n_out,
@@ -197,8 +196,8 @@ dspark_status check_geom(const dspark_geom_t *g) {
         g->vocab <= 0 || g->rank <= 0 || g->block <= 0)
         return DSPARK_ERR_SHAPE;
     if (g->hidden % 64 || g->q_lora % 64 || g->kv_lora % 64 || g->inter % 64 || (g->n_heads * g->d_v) % 64 ||
-        g->d_rope % 2 || g->d_rope > 128 || g->vocab % 2 || g->vocab >= (1 << 18) || g->rank > 256 ||
-        g->block > 16 || g->page_size != 64 || g->d_nope > 256 || g->d_nope % 8 || g->d_v % 16 ||
+        g->d_rope % 2 || g->d_rope > 128 || g->vocab % 8 || g->vocab >= (1 << 18) || g->rank > 256 ||
+        g->block > 16 || g->page_size != 64 || g->d_nope > 256 || g->d_nope % 16 || g->d_v % 16 ||
         g->kv_lora > 512)
         return DSPARK_ERR_UNSUPPORTED;
     if (!attention_supported(g->kv_lora + g->d_rope, g->kv_lora)) return DSPARK_ERR_UNSUPPORTED;
@@ -291,7 +290,7 @@ dspark_status dspark_create(const dspark_geom_t *geom, const dspark_weights_t *w
         delete h;
         return DSPARK_ERR_CUDA;
     }
-    h->samp_grid = sampling_max_grid(h->num_sms);
+    h->samp_grid = sampling_max_grid(h->num_sms, g.vocab);
     if (h->samp_grid <= 0) {
         delete h;
         return DSPARK_ERR_CUDA;

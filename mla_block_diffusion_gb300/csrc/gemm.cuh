@@ -207,11 +207,33 @@ __global__ void __launch_bounds__(192, 1)
     // producer bookkeeping for the drain after an abort
     uint32_t armed = 0, armed_par = 0;
 
+    pdl_trigger();
     if (warp == 0) {
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
-            long long it = 0;
-            for (long long u = u0; u < u1; ++u, ++it) {
+            // Weights do not depend on the previous kernel: the first ring
+            // stages get their weight tiles before the dependency wait.
+            const long long pre = min((long long)C::kStages, u1 - u0);
+            for (long long it = 0; it < pre; ++it) {
+                const long long u = u0 + it;
+                const int s = (int)it;
+                const int tile = (int)(u / p.KB), kb = (int)(u % p.KB);
+                mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+                armed |= 1u << s;
+                uint8_t *a = sA + s * C::kABytes;
+                if (p.paired) {
+                    tma_load_2d_hint(a, &tmA, kb * 64, tile * 64, &full[s], pol);
+                    tma_load_2d_hint(a + 8192, &tmA2, kb * 64, tile * 64, &full[s], pol);
+                } else {
+                    tma_load_2d_hint(a, &tmA, kb * 64, tile * 128, &full[s], pol);
+                    tma_load_2d_hint(a + 8192, &tmA, kb * 64, tile * 128 + 64, &full[s], pol);
+                }
+            }
+            pdl_wait();
+            for (long long it = 0; it < pre; ++it)
+                tma_load_2d(sB + (int)it * C::kBBytes, &tmB, (int)((u0 + it) % p.KB) * 64, 0, &full[(int)it]);
+            long long it = pre;
+            for (long long u = u0 + pre; u < u1; ++u, ++it) {
                 const int s = (int)(it % C::kStages);
                 const uint32_t round = (uint32_t)(it / C::kStages);
                 if (!mbar_wait_bounded(&empty[s], (round & 1u) ^ 1u, &s_abort)) break;
@@ -229,8 +251,11 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 tma_load_2d(sB + s * C::kBBytes, &tmB, kb * 64, 0, &full[s]);
             }
+        } else {
+            pdl_wait();
         }
     } else if (warp == 1) {
+        pdl_wait();
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_bf16_f32(128, BN);
             long long it = 0, u = u0;
@@ -273,6 +298,7 @@ __global__ void __launch_bounds__(192, 1)
             mbar_drain(done, 0);
         }
     } else {
+        pdl_wait();
         // epilogue: warps 2..5, TMEM lane quadrant = warp % 4
         const int q = warp & 3;
         const int row = q * 32 + lane;

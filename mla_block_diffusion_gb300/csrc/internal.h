@@ -94,6 +94,6 @@ size_t rollout_scratch_words(int bs, int B, int grid);
 size_t verify_scratch_words(int bs, int B, int grid);
 cudaError_t launch_rollout(RolloutParams p, int grid, cudaStream_t st);
 cudaError_t launch_verify(VerifyParams p, int grid, cudaStream_t st);
-int sampling_max_grid(int num_sms);
+int sampling_max_grid(int num_sms, int V);
 
 }  // namespace ds

@@ -40,6 +40,8 @@ __device__ float block_sum(float v, float *red) {
 // ---------------------------------------------------------------------------
 __global__ void rmsnorm_kernel(const float *__restrict__ x, int ldx, const float *__restrict__ g, int H, float eps,
                                __nv_bfloat16 *__restrict__ y, int ldy, float *__restrict__ y32, int ldy32, int *err) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ float red[33];
     const int m = blockIdx.x;
     const float4 *xr = (const float4 *)(x + (size_t)m * ldx);
@@ -73,6 +75,8 @@ __global__ void latent_kernel(const float *__restrict__ qkv, int ld, int q_lora,
                               const float *__restrict__ g_q, const float *__restrict__ g_kv, float eps,
                               const int32_t *__restrict__ ctx_len, int block, int max_ctx, RopeTable rt,
                               __nv_bfloat16 *__restrict__ cq, __nv_bfloat16 *__restrict__ blk_kv, int *err) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ float red[33];
     const int m = blockIdx.x;
     const int b = m / block, i = m % block;
@@ -106,31 +110,34 @@ __global__ void latent_kernel(const float *__restrict__ qkv, int ld, int q_lora,
 
 // ---------------------------------------------------------------------------
 // q absorption: Q_h = [W_kb,h^T q_nope,h || RoPE(q_rope,h)] per row and head,
-// bf16 [M, n_h, kv_lora + d_rope]. Grid (n_h, kv_lora / 64): a CTA owns one
-// head and 64 latent columns; its 256 threads split d_nope into 8 groups x 32
-// column pairs, hold their slice of W_kb in registers (loaded once, all loads
-// independent) and sweep the rows in chunks of 16; the 8 partial sums are
+// bf16 [M, n_h, kv_lora + d_rope]. Grid (n_h, kv_lora / 32): a CTA owns one
+// head and 32 latent columns; its 256 threads split d_nope into 16 groups x 16
+// column pairs, hold their slice of W_kb in registers (loaded once, loads
+// independent) and sweep the rows in chunks of 16; the 16 partial sums are
 // added in group order through shared memory.
 // ---------------------------------------------------------------------------
 constexpr int kAbsorbRows = 16;
-constexpr int kQAbsCols = 64;
+constexpr int kQAbsCols = 32;
+constexpr int kQAbsGroups = 16;
 
 __global__ void __launch_bounds__(256) q_absorb_kernel(const float *__restrict__ q, int M, int n_h, int d_nope,
                                                        int d_rope, int kv_lora, int d_v,
                                                        const __nv_bfloat16 *__restrict__ w_kvb,
                                                        const int32_t *__restrict__ ctx_len, int block, int max_ctx,
                                                        RopeTable rt, __nv_bfloat16 *__restrict__ qt) {
+    pdl_trigger();
+    pdl_wait();
     extern __shared__ float sm[];
     float *sq = sm;                               // [kAbsorbRows][d_nope]
-    float *red = sm + kAbsorbRows * d_nope;       // [8][kAbsorbRows][kQAbsCols]
+    float *red = sm + kAbsorbRows * d_nope;       // [kQAbsGroups][kAbsorbRows][kQAbsCols]
     const int h = blockIdx.x, c0 = blockIdx.y * kQAbsCols;
-    const int cp = threadIdx.x & 31, dg = threadIdx.x >> 5;
-    const int dper = d_nope / 8;
+    const int cp = threadIdx.x & 15, dg = threadIdx.x >> 4;
+    const int dper = d_nope / kQAbsGroups;  // <= 16
     const int qhd = d_nope + d_rope, kvd = kv_lora + d_rope;
     const __nv_bfloat16 *W = w_kvb + (size_t)h * (d_nope + d_v) * kv_lora + c0 + 2 * cp;
-    float2 w[32];
+    float2 w[16];
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
+    for (int i = 0; i < 16; ++i)
         w[i] = i < dper ? __bfloat1622float2(*(const __nv_bfloat162 *)(W + (size_t)(dg * dper + i) * kv_lora))
                         : make_float2(0.f, 0.f);
     for (int m0 = 0; m0 < M; m0 += kAbsorbRows) {
@@ -143,7 +150,7 @@ __global__ void __launch_bounds__(256) q_absorb_kernel(const float *__restrict__
 #pragma unroll
         for (int mm = 0; mm < kAbsorbRows; ++mm) a0[mm] = a1[mm] = 0.f;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
+        for (int i = 0; i < 16; ++i) {
             if (i < dper) {
 #pragma unroll
                 for (int mm = 0; mm < kAbsorbRows; ++mm) {
@@ -161,7 +168,7 @@ __global__ void __launch_bounds__(256) q_absorb_kernel(const float *__restrict__
             const int mm = idx / (kQAbsCols / 2), c2 = 2 * (idx % (kQAbsCols / 2)), m = m0 + mm;
             float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-            for (int g = 0; g < 8; ++g) {
+            for (int g = 0; g < kQAbsGroups; ++g) {
                 const float2 v = *(const float2 *)(red + ((size_t)g * kAbsorbRows + mm) * kQAbsCols + c2);
                 s0 += v.x;
                 s1 += v.y;
@@ -190,33 +197,33 @@ __global__ void __launch_bounds__(256) q_absorb_kernel(const float *__restrict__
 // ---------------------------------------------------------------------------
 // v absorption: o_h = W_vb,h o_lat,h -> bf16 [M, n_h * d_v] (operand of o_proj).
 // Grid (n_h, d_v / 16): a CTA owns 16 output channels of one head; 16 threads
-// per channel each hold 8-element slices of the channel's W_vb row (16-byte
-// loads, all independent, read once) and the rows sweep in chunks of 16 from
-// shared memory; the 16 partial dots are reduced with shuffles.
+// per channel each hold 4-element slices of the channel's W_vb row at
+// interleaved float4 positions (so a half-warp reads 16 consecutive float4 of
+// the latent: no bank conflicts), read once; the rows sweep in chunks of 16
+// from shared memory; the 16 partial dots are reduced with shuffles.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) v_absorb_kernel(const float *__restrict__ o_lat, int M, int n_h, int d_nope,
                                                        int d_v, int kv_lora, const __nv_bfloat16 *__restrict__ w_kvb,
                                                        __nv_bfloat16 *__restrict__ out) {
+    pdl_trigger();
+    pdl_wait();
     extern __shared__ float so[];  // [kAbsorbRows][kv_lora]
     const int h = blockIdx.x, e = blockIdx.y * 16 + (threadIdx.x >> 4), cg = threadIdx.x & 15;
     const __nv_bfloat16 *W = w_kvb + ((size_t)h * (d_nope + d_v) + d_nope + e) * kv_lora;
-    const int nj = (kv_lora + 127) / 128;  // <= 4
-    float wv[4][8];
+    const int nj = kv_lora / 64;  // float4 slices per thread (<= 8)
+    float wv[8][4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int c = cg * 8 + 128 * j;
-        if (j < nj && c < kv_lora) {
-            const uint4 u = *(const uint4 *)(W + c);
-            const __nv_bfloat162 *b2 = (const __nv_bfloat162 *)&u;
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-                const float2 f = __bfloat1622float2(b2[t]);
-                wv[j][2 * t] = f.x;
-                wv[j][2 * t + 1] = f.y;
-            }
+    for (int j = 0; j < 8; ++j) {
+        if (j < nj) {
+            const uint2 u = *(const uint2 *)(W + 4 * (cg + 16 * j));
+            const float2 f0 = __bfloat1622float2(*(const __nv_bfloat162 *)&u.x);
+            const float2 f1 = __bfloat1622float2(*(const __nv_bfloat162 *)&u.y);
+            wv[j][0] = f0.x;
+            wv[j][1] = f0.y;
+            wv[j][2] = f1.x;
+            wv[j][3] = f1.y;
         } else {
-#pragma unroll
-            for (int t = 0; t < 8; ++t) wv[j][t] = 0.f;
+            wv[j][0] = wv[j][1] = wv[j][2] = wv[j][3] = 0.f;
         }
     }
     for (int m0 = 0; m0 < M; m0 += kAbsorbRows) {
@@ -226,29 +233,22 @@ __global__ void __launch_bounds__(256) v_absorb_kernel(const float *__restrict__
                                           : make_float4(0.f, 0.f, 0.f, 0.f);
         }
         __syncthreads();
-#pragma unroll
-        for (int mm = 0; mm < kAbsorbRows; ++mm) {
+        const int mmax = min(kAbsorbRows, M - m0);
+        for (int mm = 0; mm < mmax; ++mm) {
             float acc = 0.f;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int c = cg * 8 + 128 * j;
-                if (j < nj && c < kv_lora) {
-                    const float4 x0 = *(const float4 *)(so + mm * kv_lora + c);
-                    const float4 x1 = *(const float4 *)(so + mm * kv_lora + c + 4);
-                    acc = fmaf(wv[j][0], x0.x, acc);
-                    acc = fmaf(wv[j][1], x0.y, acc);
-                    acc = fmaf(wv[j][2], x0.z, acc);
-                    acc = fmaf(wv[j][3], x0.w, acc);
-                    acc = fmaf(wv[j][4], x1.x, acc);
-                    acc = fmaf(wv[j][5], x1.y, acc);
-                    acc = fmaf(wv[j][6], x1.z, acc);
-                    acc = fmaf(wv[j][7], x1.w, acc);
+            for (int j = 0; j < 8; ++j) {
+                if (j < nj) {
+                    const float4 x = *(const float4 *)(so + mm * kv_lora + 4 * (cg + 16 * j));
+                    acc = fmaf(wv[j][0], x.x, acc);
+                    acc = fmaf(wv[j][1], x.y, acc);
+                    acc = fmaf(wv[j][2], x.z, acc);
+                    acc = fmaf(wv[j][3], x.w, acc);
                 }
             }
 #pragma unroll
             for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-            const int m = m0 + mm;
-            if (cg == 0 && m < M) out[(size_t)m * n_h * d_v + (size_t)h * d_v + e] = __float2bfloat16(acc);
+            if (cg == 0) out[(size_t)(m0 + mm) * n_h * d_v + (size_t)h * d_v + e] = __float2bfloat16(acc);
         }
         __syncthreads();
     }
@@ -314,6 +314,8 @@ struct AttnCfg {
 
 template <int DQK, int DV>
 __global__ void __launch_bounds__(256, 1) mla_attention_kernel(const AttnParams p) {
+    pdl_trigger();
+    pdl_wait();
     using C = AttnCfg<DQK, DV>;
     extern __shared__ __align__(16) uint8_t smem[];
     __nv_bfloat16 *sQ = (__nv_bfloat16 *)smem;
@@ -482,6 +484,8 @@ __global__ void __launch_bounds__(256, 1) mla_attention_kernel(const AttnParams 
 // its 4 columns of every split with independent loads.
 __global__ void attn_combine_kernel(const float *__restrict__ part_o, const float *__restrict__ part_ml, int splits,
                                     int R, int DV, float *__restrict__ o_lat) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ float sw[64];
     __shared__ float sml[64][2];
     __shared__ float sinv;
@@ -526,6 +530,8 @@ __global__ void attn_combine_kernel(const float *__restrict__ part_o, const floa
 // Confidence head: c = sigmoid(w . h_out + b) per block row.
 __global__ void confidence_kernel(const float *__restrict__ h_out, int H, const float *__restrict__ w, float bias,
                                   float *__restrict__ conf) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ float red[33];
     const int m = blockIdx.x;
     float acc = 0.f;
@@ -539,35 +545,31 @@ __global__ void confidence_kernel(const float *__restrict__ h_out, int H, const 
 // ---------------------------------------------------------------------------
 cudaError_t launch_rmsnorm(const float *x, int ldx, const float *g, int H, float eps, __nv_bfloat16 *y, int ldy,
                            float *y32, int ldy32, int M, int *err, cudaStream_t st) {
-    rmsnorm_kernel<<<M, 256, 0, st>>>(x, ldx, g, H, eps, y, ldy, y32, ldy32, err);
-    return cudaGetLastError();
+    return launch_pdl(rmsnorm_kernel, dim3(M), dim3(256), 0, st, x, ldx, g, H, eps, y, ldy, y32, ldy32, err);
 }
 
 cudaError_t launch_latent(const float *qkv, int ld, int q_lora, int kv_lora, int d_rope, const float *g_q,
                           const float *g_kv, float eps, const int32_t *ctx_len, int block, int max_ctx,
                           const RopeTable &rt, __nv_bfloat16 *cq, __nv_bfloat16 *blk_kv, int M, int *err,
                           cudaStream_t st) {
-    latent_kernel<<<M, 256, 0, st>>>(qkv, ld, q_lora, kv_lora, d_rope, g_q, g_kv, eps, ctx_len, block, max_ctx, rt, cq,
-                                     blk_kv, err);
-    return cudaGetLastError();
+    return launch_pdl(latent_kernel, dim3(M), dim3(256), 0, st, qkv, ld, q_lora, kv_lora, d_rope, g_q, g_kv, eps,
+                      ctx_len, block, max_ctx, rt, cq, blk_kv, err);
 }
 
 cudaError_t launch_q_absorb(const float *q, int M, int n_h, int d_nope, int d_rope, int kv_lora, int d_v,
                             const __nv_bfloat16 *w_kvb, const int32_t *ctx_len, int block, int max_ctx,
                             const RopeTable &rt, __nv_bfloat16 *qt, cudaStream_t st) {
     dim3 grid(n_h, kv_lora / kQAbsCols);
-    const size_t smem = ((size_t)kAbsorbRows * d_nope + (size_t)8 * kAbsorbRows * kQAbsCols) * sizeof(float);
-    q_absorb_kernel<<<grid, 256, smem, st>>>(q, M, n_h, d_nope, d_rope, kv_lora, d_v, w_kvb, ctx_len, block, max_ctx,
-                                             rt, qt);
-    return cudaGetLastError();
+    const size_t smem = ((size_t)kAbsorbRows * d_nope + (size_t)kQAbsGroups * kAbsorbRows * kQAbsCols) * sizeof(float);
+    return launch_pdl(q_absorb_kernel, grid, dim3(256), smem, st, q, M, n_h, d_nope, d_rope, kv_lora, d_v, w_kvb,
+                      ctx_len, block, max_ctx, rt, qt);
 }
 
 cudaError_t launch_v_absorb(const float *o_lat, int M, int n_h, int d_nope, int d_v, int kv_lora,
                             const __nv_bfloat16 *w_kvb, __nv_bfloat16 *out, cudaStream_t st) {
     dim3 grid(n_h, d_v / 16);
     const size_t smem = (size_t)kAbsorbRows * kv_lora * sizeof(float);
-    v_absorb_kernel<<<grid, 256, smem, st>>>(o_lat, M, n_h, d_nope, d_v, kv_lora, w_kvb, out);
-    return cudaGetLastError();
+    return launch_pdl(v_absorb_kernel, grid, dim3(256), smem, st, o_lat, M, n_h, d_nope, d_v, kv_lora, w_kvb, out);
 }
 
 template <int DQK, int DV>
@@ -581,8 +583,7 @@ static cudaError_t launch_attn_t(const AttnParams &p, int bs, int qtiles, cudaSt
         attr = true;
     }
     dim3 grid(qtiles, p.splits, bs);
-    mla_attention_kernel<DQK, DV><<<grid, 256, C::kSmem, st>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(mla_attention_kernel<DQK, DV>, grid, dim3(256), (size_t)C::kSmem, st, p);
 }
 
 bool attention_supported(int dqk, int dv) {
@@ -604,14 +605,13 @@ cudaError_t launch_attention(const AttnParams &p, int bs, int dqk, int dv, cudaS
     else
         return cudaErrorInvalidValue;
     if (e != cudaSuccess || p.splits == 1) return e;
-    attn_combine_kernel<<<dim3(p.R, bs), 128, 0, st>>>(p.part_o, p.part_ml, p.splits, p.R, dv, p.o_lat);
-    return cudaGetLastError();
+    return launch_pdl(attn_combine_kernel, dim3(p.R, bs), dim3(128), 0, st, p.part_o, p.part_ml, p.splits, p.R, dv,
+                      p.o_lat);
 }
 
 cudaError_t launch_confidence(const float *h_out, int H, const float *w, float bias, float *conf, int M,
                               cudaStream_t st) {
-    confidence_kernel<<<M, 256, 0, st>>>(h_out, H, w, bias, conf);
-    return cudaGetLastError();
+    return launch_pdl(confidence_kernel, dim3(M), dim3(256), 0, st, h_out, H, w, bias, conf);
 }
 
 }  // namespace ds

@@ -391,54 +391,108 @@ DS_DEVINL uint64_t policy_evict_last() {
     return pol;
 }
 
-// 32-bit global load that asks L2 to keep the line (w2 is re-read every step).
-DS_DEVINL uint32_t ld_keep(const void *ptr, uint64_t pol) {
-    uint32_t v;
-    asm volatile("ld.global.L2::cache_hint.b32 %0, [%1], %2;" : "=r"(v) : "l"(ptr), "l"(pol));
-    return v;
+// w2 streaming ring: the CTA's slice of every w2 row (its vocabulary pairs
+// [lo, hi), whole 16-byte quads) is copied in chunks of kRollKC rows into
+// kRollStages shared-memory stages by all threads with 16-byte cp.async (L2
+// evict-last: w2 is re-read every step). w2 does not depend on the drafted
+// tokens, so the ring runs ahead of the compute across steps and barriers.
+constexpr int kRollKC = 16;
+constexpr int kRollStages = 5;
+
+struct RollRing {
+    uint8_t *stage;          // [kRollStages][kRollKC][slice_bytes]
+    uint32_t slice_bytes;    // (hi - lo) * 4
+    int nchunks;             // chunks per pass over w2
+    long long issued, consumed, total;
+};
+
+DS_DEVINL void cp_async16_keep(void *dst, const void *src, uint64_t pol) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+                 "l"(pol)
+                 : "memory");
+}
+DS_DEVINL void cp_async_commit_group() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+DS_DEVINL void cp_async_wait_group() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// ell_i for NB sequences over this CTA's pairs: 16 w2 words are loaded ahead of
-// each run of 16 FMAs so the loads overlap; the chain over k stays in order.
+// All threads: copy chunk number ring.issued into its stage (one commit group
+// per chunk per thread, empty when past the end).
+DS_DEVINL void ring_issue(RollRing &rg, const RolloutParams &p, int lo, uint64_t pol) {
+    if (rg.issued < rg.total) {
+        const long long c = rg.issued;
+        const int s = (int)(c % kRollStages);
+        const int k0 = (int)(c % rg.nchunks) * kRollKC;
+        const int rows = min(kRollKC, p.r - k0);
+        const int quads = (int)(rg.slice_bytes / 16);
+        const uint8_t *src = (const uint8_t *)p.w2 + ((size_t)k0 * p.V + 2 * (size_t)lo) * 2;
+        uint8_t *dst = rg.stage + (size_t)s * kRollKC * rg.slice_bytes;
+        for (int seg = threadIdx.x; seg < rows * quads; seg += blockDim.x) {
+            const int kk = seg / quads, q = seg - kk * quads;
+            cp_async16_keep(dst + (size_t)kk * rg.slice_bytes + 16 * q, src + (size_t)kk * p.V * 2 + 16 * q, pol);
+        }
+    }
+    cp_async_commit_group();
+    rg.issued++;
+}
+
+// ell_i for NB sequences over this CTA's pairs (thread t owns pairs lo + t and
+// lo + t + blockDim): w2 comes from the ring; the chain over k stays in order.
 // Each CTA max-reduces its greedy keys (or its maxima of ell / T) into amax[b].
 template <int NB>
-__device__ void rollout_logits(const RolloutParams &p, int i, int b0, int nb, int lo, int hi,
+__device__ bool rollout_logits(const RolloutParams &p, int i, int b0, int nb, int lo, int hi, RollRing &rg,
                                const float (*s_w1)[256], unsigned long long *amax, unsigned long long *red,
-                               uint64_t w2pol) {
+                               uint64_t pol) {
     const int V = p.V, r = p.r;
-    const uint32_t *w2 = (const uint32_t *)p.w2;  // bf16 pairs
+    float a[2][NB][2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int bb = 0; bb < NB; ++bb) a[j][bb][0] = a[j][bb][1] = 0.f;
+    const int q0 = threadIdx.x, q1 = threadIdx.x + blockDim.x;
+    const bool has0 = lo + q0 < hi, has1 = lo + q1 < hi;
+    for (int ch = 0; ch < rg.nchunks; ++ch) {
+        const long long c = rg.consumed;
+        const int s = (int)(c % kRollStages);
+        cp_async_wait_group<kRollStages - 2>();  // this thread's copies of chunk c have landed
+        __syncthreads();                          // ... and everyone's; stage of chunk c-1 is free
+        ring_issue(rg, p, lo, pol);
+        const uint32_t *w = (const uint32_t *)(rg.stage + (size_t)s * kRollKC * rg.slice_bytes);
+        const int k0 = ch * kRollKC, rows = min(kRollKC, r - k0);
+        const int wpr = rg.slice_bytes / 4;  // words (pairs) per row
+#pragma unroll 4
+        for (int kk = 0; kk < rows; ++kk) {
+            const uint32_t w0 = has0 ? w[kk * wpr + q0] : 0u, w1v = has1 ? w[kk * wpr + q1] : 0u;
+            const float x0 = __uint_as_float(w0 << 16), y0 = __uint_as_float(w0 & 0xFFFF0000u);
+            const float x1 = __uint_as_float(w1v << 16), y1 = __uint_as_float(w1v & 0xFFFF0000u);
+#pragma unroll
+            for (int bb = 0; bb < NB; ++bb) {
+                const float u = s_w1[bb][k0 + kk];
+                a[0][bb][0] = __fmaf_rn(u, x0, a[0][bb][0]);
+                a[0][bb][1] = __fmaf_rn(u, y0, a[0][bb][1]);
+                a[1][bb][0] = __fmaf_rn(u, x1, a[1][bb][0]);
+                a[1][bb][1] = __fmaf_rn(u, y1, a[1][bb][1]);
+            }
+        }
+        rg.consumed = c + 1;
+    }
+    __syncthreads();
     unsigned long long best[NB];
 #pragma unroll
     for (int bb = 0; bb < NB; ++bb) best[bb] = 0;
     bool bad = false;
-    for (int pp = lo + threadIdx.x; pp < hi; pp += blockDim.x) {
-        float a0[NB], a1[NB];
 #pragma unroll
-        for (int bb = 0; bb < NB; ++bb) a0[bb] = a1[bb] = 0.f;
-        for (int k0 = 0; k0 < r; k0 += 16) {
-            uint32_t wv[16];
-#pragma unroll
-            for (int kk = 0; kk < 16; ++kk)
-                wv[kk] = (k0 + kk < r) ? ld_keep(w2 + ((size_t)(k0 + kk) * V) / 2 + pp, w2pol) : 0u;
-#pragma unroll
-            for (int kk = 0; kk < 16; ++kk) {
-                if (k0 + kk < r) {
-                    const float wx = __uint_as_float(wv[kk] << 16), wy = __uint_as_float(wv[kk] & 0xFFFF0000u);
-#pragma unroll
-                    for (int bb = 0; bb < NB; ++bb) {
-                        a0[bb] = __fmaf_rn(s_w1[bb][k0 + kk], wx, a0[bb]);
-                        a1[bb] = __fmaf_rn(s_w1[bb][k0 + kk], wy, a1[bb]);
-                    }
-                }
-            }
-        }
+    for (int j = 0; j < 2; ++j) {
+        const int pp = lo + (j ? q1 : q0);
+        if (pp >= hi) continue;
 #pragma unroll
         for (int bb = 0; bb < NB; ++bb) {
             if (bb < nb) {
                 const int b = b0 + bb;
                 const size_t off = ((size_t)b * p.B + i) * V + 2 * pp;
                 const float2 z = *(const float2 *)(p.z + off);
-                const float l0 = __fadd_rn(z.x, a0[bb]), l1 = __fadd_rn(z.y, a1[bb]);
+                const float l0 = __fadd_rn(z.x, a[j][bb][0]), l1 = __fadd_rn(z.y, a[j][bb][1]);
                 *(float2 *)(p.ell + off) = make_float2(l0, l1);
                 if (!isfinite(l0) || !isfinite(l1)) bad = true;
                 unsigned long long k0, k1;
@@ -454,11 +508,26 @@ __device__ void rollout_logits(const RolloutParams &p, int i, int b0, int nb, in
         }
     }
     if (bad) set_error(p.err, DSPARK_ERR_BAD_INPUT);
-    for (int bb = 0; bb < nb; ++bb) {
-        const unsigned long long m = block_max_u64(best[bb], red);
-        if (threadIdx.x == 0) atomicMax(&amax[b0 + bb], m);
+#pragma unroll
+    for (int bb = 0; bb < NB; ++bb) {
+        if (bb < nb) {
+            const unsigned long long m = block_max_u64(best[bb], red);
+            if (threadIdx.x == 0) atomicMax(&amax[b0 + bb], m);
+        }
     }
+    return true;
 }
+
+// Vocabulary pairs of this CTA for the rollout: quads of 4 pairs (16 bytes of
+// a w2 row) so every bulk copy is 16-byte aligned.
+DS_DEVINL void quad_slice(int V, int &lo, int &hi) {
+    const int nq = V / 8;
+    lo = 4 * (int)((long long)blockIdx.x * nq / gridDim.x);
+    hi = 4 * (int)((long long)(blockIdx.x + 1) * nq / gridDim.x);
+}
+
+// Every copy the ring still has in flight lands before the kernel exits.
+DS_DEVINL void ring_drain() { cp_async_wait_group<0>(); }
 
 __global__ void __launch_bounds__(kSampThreads, 1) rollout_kernel(RolloutParams p) {
     __shared__ NucleusSmem sm;
@@ -467,10 +536,22 @@ __global__ void __launch_bounds__(kSampThreads, 1) rollout_kernel(RolloutParams 
     __shared__ int s_prev[kMaxSampBs];
     __shared__ volatile int s_fail;
     __shared__ const float *s_rows[kRowsPerGroup];
+    extern __shared__ __align__(128) uint8_t ring_smem[];
     const RollLayout L(p.bs, p.B, gridDim.x);
     unsigned long long *sc = p.scratch;
     const int V = p.V, r = p.r;
+    int lo, hi;
+    quad_slice(V, lo, hi);
+    RollRing rg;
+    rg.stage = ring_smem;
+    rg.slice_bytes = (uint32_t)(hi - lo) * 4u;
+    rg.nchunks = (r + kRollKC - 1) / kRollKC;
+    rg.issued = rg.consumed = 0;
+    rg.total = (long long)p.B * ((p.bs + kRollChunk - 1) / kRollChunk) * rg.nchunks;
+    const uint64_t pol = policy_evict_last();
     if (threadIdx.x == 0) s_fail = 0;
+    if (hi <= lo) rg.total = 0;
+    for (int st = 0; st < kRollStages - 1; ++st) ring_issue(rg, p, lo, pol);
     for (size_t w = (size_t)blockIdx.x * blockDim.x + threadIdx.x; w < L.total; w += (size_t)gridDim.x * blockDim.x)
         sc[w] = 0;
     for (int b = threadIdx.x; b < p.bs; b += blockDim.x) {
@@ -482,27 +563,31 @@ __global__ void __launch_bounds__(kSampThreads, 1) rollout_kernel(RolloutParams 
         s_prev[b] = a;
     }
     __threadfence();
-    if (!grid_barrier(p.ctl, &s_fail, p.err)) return;
-    int lo, hi;
-    pair_slice(V / 2, lo, hi);
-    const uint64_t w2pol = policy_evict_last();
+    bool ok = grid_barrier(p.ctl, &s_fail, p.err);
 
-    for (int i = 0; i < p.B; ++i) {
+    for (int i = 0; i < p.B && ok; ++i) {
         // ell_i = z_i + fp32 FMA chain of w1[t_{i-1}] against w2 (k in order)
-        for (int b0 = 0; b0 < p.bs; b0 += kRollChunk) {
+        for (int b0 = 0; b0 < p.bs && ok; b0 += kRollChunk) {
             const int nb = min(kRollChunk, p.bs - b0);
             for (int idx = threadIdx.x; idx < kRollChunk * r; idx += blockDim.x) {
                 const int bb = idx / r, k = idx % r;
                 s_w1[bb][k] = bb < nb ? __bfloat162float(p.w1[(size_t)s_prev[b0 + bb] * r + k]) : 0.f;
             }
             __syncthreads();
-            if (nb == 1)
-                rollout_logits<1>(p, i, b0, 1, lo, hi, s_w1, sc + L.amax + (size_t)i * p.bs, sm.red, w2pol);
-            else
-                rollout_logits<kRollChunk>(p, i, b0, nb, lo, hi, s_w1, sc + L.amax + (size_t)i * p.bs, sm.red, w2pol);
+            if (hi > lo) {
+                if (nb == 1)
+                    ok = rollout_logits<1>(p, i, b0, 1, lo, hi, rg, s_w1, sc + L.amax + (size_t)i * p.bs, sm.red,
+                                           pol);
+                else
+                    ok = rollout_logits<kRollChunk>(p, i, b0, nb, lo, hi, rg, s_w1, sc + L.amax + (size_t)i * p.bs,
+                                                    sm.red, pol);
+            }
             __syncthreads();
         }
-        if (!grid_barrier(p.ctl, &s_fail, p.err)) return;
+        if (!ok || !grid_barrier(p.ctl, &s_fail, p.err)) {
+            ok = false;
+            break;
+        }
         if (p.draft_mode == DSPARK_GREEDY) {
             for (int b = threadIdx.x; b < p.bs; b += blockDim.x) {
                 const int t = argmax_token(ldcg_u64(&sc[L.amax + (size_t)i * p.bs + b]));
@@ -513,7 +598,7 @@ __global__ void __launch_bounds__(kSampThreads, 1) rollout_kernel(RolloutParams 
             continue;
         }
         // probabilistic: nucleus of ell_i / T per sequence, then a draw
-        for (int g0 = 0; g0 < p.bs; g0 += kRowsPerGroup) {
+        for (int g0 = 0; g0 < p.bs && ok; g0 += kRowsPerGroup) {
             const int nr = min(kRowsPerGroup, p.bs - g0);
             if (threadIdx.x < nr) {
                 s_rows[threadIdx.x] = p.ell + ((size_t)(g0 + threadIdx.x) * p.B + i) * V;
@@ -521,8 +606,10 @@ __global__ void __launch_bounds__(kSampThreads, 1) rollout_kernel(RolloutParams 
             }
             __syncthreads();
             if (!group_nucleus(s_rows, nr, V, p.T, p.top_p, sm, sc + L.S + (size_t)i * p.bs + g0,
-                               sc + L.hist + ((size_t)i * p.bs + g0) * kRadixPasses * 256, p.ctl, &s_fail, p.err))
-                return;
+                               sc + L.hist + ((size_t)i * p.bs + g0) * kRadixPasses * 256, p.ctl, &s_fail, p.err)) {
+                ok = false;
+                break;
+            }
             for (int rr = 0; rr < nr; ++rr) {
                 const int b = g0 + rr;
                 const float *row = s_rows[rr];
@@ -535,11 +622,16 @@ __global__ void __launch_bounds__(kSampThreads, 1) rollout_kernel(RolloutParams 
                 const uint32_t W = philox_word(p.seed, (uint32_t)b, p.step, (uint32_t)i, 1u) >> 8;
                 int32_t *pick = (int32_t *)&sc[L.pick + (size_t)i * p.bs + b];
                 if (!grid_draw(wf, V, W, sc + L.parts + ((size_t)i * p.bs + b) * gridDim.x * 2, pick, dsm, p.ctl,
-                               &s_fail, p.err))
-                    return;
+                               &s_fail, p.err)) {
+                    ok = false;
+                    break;
+                }
             }
         }
-        if (!grid_barrier(p.ctl, &s_fail, p.err)) return;
+        if (!ok || !grid_barrier(p.ctl, &s_fail, p.err)) {
+            ok = false;
+            break;
+        }
         for (int b = threadIdx.x; b < p.bs; b += blockDim.x) {
             const int t = (int)(uint32_t)ldcg_u64(&sc[L.pick + (size_t)i * p.bs + b]);
             s_prev[b] = t;
@@ -547,6 +639,7 @@ __global__ void __launch_bounds__(kSampThreads, 1) rollout_kernel(RolloutParams 
         }
         __syncthreads();
     }
+    ring_drain();
 }
 
 // ---------------------------------------------------------------------------
@@ -555,6 +648,8 @@ __global__ void __launch_bounds__(kSampThreads, 1) rollout_kernel(RolloutParams 
 // Greedy: row argmax keys (zero between launches) then a finalize kernel that
 // also returns the keys to zero.
 __global__ void verify_argmax_kernel(const float *__restrict__ P, int rows, int V, unsigned long long *keys, int *err) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ unsigned long long red[33];
     const int row = blockIdx.y;
     const int nslices = gridDim.x;
@@ -576,6 +671,8 @@ __global__ void verify_argmax_kernel(const float *__restrict__ P, int rows, int 
 
 __global__ void verify_greedy_finalize(const int32_t *__restrict__ tokens, int bs, int B, int V,
                                        unsigned long long *keys, int32_t *accept_len, int32_t *out_tokens, int *err) {
+    pdl_trigger();
+    pdl_wait();
     const int b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b >= bs) return;
     unsigned long long *k = keys + (size_t)b * (B + 1);
@@ -743,9 +840,21 @@ __global__ void __launch_bounds__(kSampThreads, 1) verify_prob_kernel(VerifyPara
 // ---------------------------------------------------------------------------
 // Host launchers
 // ---------------------------------------------------------------------------
-int sampling_max_grid(int num_sms) {
+// Dynamic shared memory of the rollout's w2 ring for a vocabulary and grid.
+size_t rollout_ring_bytes(int V, int grid) {
+    const int nq = V / 8;
+    const int max_quads = (nq + grid - 1) / grid + 1;
+    return (size_t)kRollStages * kRollKC * max_quads * 16;
+}
+
+int sampling_max_grid(int num_sms, int V) {
     int a = 0, b = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, rollout_kernel, kSampThreads, 0) != cudaSuccess) return 0;
+    // the rollout gives each thread at most two vocabulary pairs of its CTA's slice
+    if (4 * ((V / 8 + num_sms - 1) / num_sms) > 2 * kSampThreads) return 0;
+    const size_t ring = rollout_ring_bytes(V, num_sms);
+    if (cudaFuncSetAttribute(rollout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ring) != cudaSuccess)
+        return 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, rollout_kernel, kSampThreads, ring) != cudaSuccess) return 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, verify_prob_kernel, kSampThreads, 0) != cudaSuccess)
         return 0;
     return (a >= 1 && b >= 1) ? num_sms : 0;
@@ -753,18 +862,18 @@ int sampling_max_grid(int num_sms) {
 
 cudaError_t launch_rollout(RolloutParams p, int grid, cudaStream_t st) {
     void *args[] = {&p};
-    return cudaLaunchCooperativeKernel((void *)rollout_kernel, dim3(grid), dim3(kSampThreads), args, 0, st);
+    return cudaLaunchCooperativeKernel((void *)rollout_kernel, dim3(grid), dim3(kSampThreads), args,
+                                       rollout_ring_bytes(p.V, grid), st);
 }
 
 cudaError_t launch_verify(VerifyParams p, int grid, cudaStream_t st) {
     if (p.verify_mode == DSPARK_GREEDY) {
         const int rows = p.bs * (p.B + 1);
-        verify_argmax_kernel<<<dim3(8, rows), 256, 0, st>>>(p.P, rows, p.V, p.scratch, p.err);
-        cudaError_t e = cudaGetLastError();
+        cudaError_t e = launch_pdl(verify_argmax_kernel, dim3(8, rows), dim3(256), 0, st, p.P, rows, p.V, p.scratch,
+                                   p.err);
         if (e != cudaSuccess) return e;
-        verify_greedy_finalize<<<(p.bs + 127) / 128, 128, 0, st>>>(p.tokens, p.bs, p.B, p.V, p.scratch, p.accept_len,
-                                                                  p.out_tokens, p.err);
-        return cudaGetLastError();
+        return launch_pdl(verify_greedy_finalize, dim3((p.bs + 127) / 128), dim3(128), 0, st, p.tokens, p.bs, p.B, p.V,
+                          p.scratch, p.accept_len, p.out_tokens, p.err);
     }
     void *args[] = {&p};
     return cudaLaunchCooperativeKernel((void *)verify_prob_kernel, dim3(grid), dim3(kSampThreads), args, 0, st);
