@@ -44,21 +44,28 @@ def peaks():
     return dict(FALLBACK), "fallback"
 
 
-def algorithmic_bytes(G, ctx: int, bs: int = 1):
-    """Bytes one step must move at least: every bf16 weight once (w2 once, the
+def algorithmic_bytes(G, ctx: int, bs: int = 1, fmt: str = "bf16"):
+    """Bytes one step must move at least: every weight once (w2 once, the
     block's 7 rows of w1), fp32 gains and confidence head, the latent KV once,
-    the aux states, z and ell written once and read once, the target logits."""
+    the aux states, z and ell written once and read once, the target logits.
+    FP8 / NVFP4 (fc, q_b, o, gate, up, down): 1 byte + a 4-byte scale per row, or
+    half a byte + one scale byte per 16."""
     lp = G.layer_params()
     mats = sum(v for k, v in lp.items() if k != "norms")
     c = G.param_counts()
-    w_bf16 = 2 * (c["fc"] + G.n_layers * mats + c["lm_head"] + G.rank * G.vocab + G.block * G.rank)
+    qn = c["quantised"]
+    q_rows = G.hidden + G.n_layers * (G.n_heads * G.q_head_dim + G.hidden + 2 * G.inter + G.hidden)
+    per = {"bf16": 2.0, "fp8": 1.0, "nvfp4": 0.5 + 1.0 / 16}[fmt]
+    extra = {"bf16": 0, "fp8": 4 * q_rows, "nvfp4": 0}[fmt]
+    w_bf16 = 2 * (c["fc"] + G.n_layers * mats + c["lm_head"] + G.rank * G.vocab + G.block * G.rank) \
+        - int(2 * qn) + int(per * qn) + extra
     w_f32 = 4 * (G.n_layers * lp["norms"] + 2 * G.hidden)
     kv = bs * G.n_layers * ctx * G.kv_dim * 2
     aux = bs * G.block * G.n_aux * G.hidden * 2
     logits = 4 * bs * G.vocab * (2 * G.block + 2 * G.block + (G.block + 1))
     total = w_bf16 + w_f32 + kv + aux + logits
     return {"weights": w_bf16 + w_f32, "kv": kv, "aux": aux, "logits": logits, "total": total,
-            "fc_weight": 2 * c["fc"]}
+            "fc_weight": int(per * c["fc"]) + (4 * G.hidden if fmt == "fp8" else 0)}
 
 
 class ClockSampler:
@@ -208,18 +215,21 @@ def main():
                          "rollout (Markov rollout, full vocabulary), layer (one full-width MLA layer, ctx 4096)")
     ap.add_argument("--fc-hidden", type=int, default=0, help="--only fc: hidden size (output channels)")
     ap.add_argument("--fc-aux", type=int, default=0, help="--only fc: captured states (K = aux * hidden)")
+    ap.add_argument("--format", choices=["bf16", "fp8", "nvfp4"], default="bf16",
+                    help="weight format of fc, q_b, o, gate, up, down (the weight-format sweep workloads)")
+    ap.add_argument("--no-drift", action="store_true", help="--format fp8|nvfp4: skip the drift report")
     args = ap.parse_args()
     assert args.warmup >= 3 or args.impl == "reference", "at least 3 warm-up steps"
 
     from synthetic import generate as gen
-    from synthetic.configs import FULL_STEP
-    w = FULL_STEP
+    from synthetic.configs import FP8_STEP, FULL_STEP, NVFP4_STEP
+    w = {"bf16": FULL_STEP, "fp8": FP8_STEP, "nvfp4": NVFP4_STEP}[args.format]
     G = w.geom
     world, rank, local = dist_setup()
     ctx = w.ctx[0]
-    ab = algorithmic_bytes(G, ctx)
+    ab = algorithmic_bytes(G, ctx, fmt=args.format)
     config = {"workload": w.name, "model": "DSpark drafter (Kimi-K3 geometry), random init", "global_batch": w.bs * world,
-              "seq_len": ctx, "block": G.block, "draft": "greedy", "verify": "greedy", "weights": "bf16",
+              "seq_len": ctx, "block": G.block, "draft": "greedy", "verify": "greedy", "weights": args.format,
               "parallelism": f"replicas{world}",
               "l2": f"no flush: working set {ab['total'] / 1e9:.2f} GB per step > 129 MB L2"}
 
@@ -265,7 +275,12 @@ def main():
     W = gen.make_weights(w, dev)
     I = gen.make_inputs(w, dev)
     bs = w.bs
-    ds = M.DSpark(G, W, max_bs=bs, max_ctx=ctx)
+    Wd = W
+    if args.format != "bf16":
+        from synthetic import quantize as Q
+        Wd = Q.quantise_weights(W, args.format, G.n_layers)
+        torch.cuda.empty_cache()
+    ds = M.DSpark(G, Wd, max_bs=bs, max_ctx=ctx, weight_format=w.weight_format)
     kv = ds.make_kv(I["kv_pools"], I["page_table"], I["ctx_len"], ctx)
     x = torch.empty(bs, G.block, G.hidden, dtype=torch.float32, device=dev)
     h_out = torch.empty_like(x)
@@ -417,6 +432,9 @@ def main():
         "gpu_launches": gpu_launches_per_step * args.steps,
         "accept_len": accept,
     }
+    if args.format != "bf16" and not args.no_drift and rank == 0:
+        line["drift"] = drift_report(w, W, I, h_out, z, ctx)
+        line["vs_bf16_note"] = "drift: this format's GPU outputs against the float64 oracle on the original bf16 weights"
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         est, sampled, conv, parts = oracle_sample(w, W, I, args.lm_rows)
         line["cpu_baseline"] = {"value": est * 1e6, "unit": UNIT, "cores": cores(), "kind": "oracle",
@@ -429,6 +447,34 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def drift_report(w, W, I, h_out, z, ctx):
+    """Weight-format drift: the GPU outputs with quantised weights against the
+    float64 oracle on the original bf16 weights (hidden-state relative error, logit
+    relative error, per-position greedy agreement)."""
+    from oracle import network as N
+    G = w.geom
+    f64 = lambda t: t.detach().to(torch.float64).cpu().numpy()
+    keys = ["attn_norm", "w_qkv_a", "q_a_norm", "kv_a_norm", "w_q_b", "w_kv_b", "w_o", "mlp_norm", "w_gate", "w_up",
+            "w_down"]
+    x = N.fuse_ctx(f64(W["w_fc"]), f64(I["aux"][0]))
+    table = I["page_table"][0]
+    pages = table[: (ctx + G.page_size - 1) // G.page_size].long()
+    pos = np.arange(G.block, dtype=np.float64) + ctx
+    for l in range(G.n_layers):
+        L = {k: f64(W[f"l{l}.{k}"]) for k in keys}
+        pool = f64(I["kv_pools"][l][pages])
+        cache = N.gather_cache(pool, np.arange(pool.shape[0]), ctx)
+        x = N.layer(x, L, G, cache[:, :G.kv_lora], cache[:, G.kv_lora:], pos)
+    h = N.rmsnorm(x, f64(W["final_norm"]), G.eps)
+    zo = np.empty((G.block, G.vocab))
+    for lo in range(0, G.vocab, 16384):
+        zo[:, lo:lo + 16384] = h @ f64(W["w_lm"][lo:lo + 16384]).T
+    hg, zg = h_out[0].double().cpu().numpy(), z[0].double().cpu().numpy()
+    rel = lambda a, b: float(np.linalg.norm(a - b) / np.linalg.norm(b))
+    agree = float(np.mean(np.argmax(zg, axis=1) == np.argmax(zo, axis=1)))
+    return {"h_out_rel_l2": rel(hg, h), "z_rel_l2": rel(zg, zo), "greedy_agreement": agree}
 
 
 def only_fc(args, G, world, rank, local):

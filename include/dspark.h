@@ -47,7 +47,8 @@ typedef enum {
     DSPARK_ERR_CUDA = 5,          /* a CUDA runtime or driver call failed */
     DSPARK_ERR_WORKSPACE = 6,     /* workspace pointer null or smaller than required */
     DSPARK_ERR_TIMEOUT = 16,      /* device: a bounded inter-CTA wait expired */
-    DSPARK_ERR_BAD_INPUT = 17,    /* device: a logit or intermediate was not finite */
+    DSPARK_ERR_BAD_INPUT = 17,    /* device: a logit or intermediate was not finite, or an
+                                     activation entering an FP8/NVFP4 GEMM exceeded 65504 */
     DSPARK_ERR_OOB = 18           /* device: page id, token id or ctx_len out of range */
 } dspark_status;
 
@@ -62,7 +63,11 @@ enum { DSPARK_GREEDY = 0, DSPARK_PROBABILISTIC = 1 };
  * Supported by the kernels: hidden, q_lora, kv_lora, inter, n_heads*d_v
  * multiples of 64; (kv_lora + d_rope, kv_lora) one of (576, 512), (288, 256),
  * (160, 128), (80, 64); d_nope <= 256; d_rope even and <= 128; block <= 16;
- * rank <= 256; vocab even and < 2^18; page_size 64; weight_format BF16.
+ * rank <= 256; vocab even and < 2^18; page_size 64; weight_format BF16, FP8
+ * (E4M3 per output row) or NVFP4 (E2M1, E4M3 group-16 scales, global scale;
+ * then hidden, q_lora, n_heads*d_v and inter multiples of 256). With FP8 or
+ * NVFP4, block * bs <= 64 per call and the activations entering those GEMMs
+ * stay within +-65504 (they are taken in f16; see DSPARK_ERR_BAD_INPUT).
  */
 typedef struct {
     int hidden, n_aux, n_layers, n_heads;

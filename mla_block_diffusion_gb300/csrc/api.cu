@@ -11,6 +11,7 @@
 #include <new>
 
 #include "gemm.cuh"
+#include "gemm_q.cuh"
 #include "internal.h"
 
 using namespace ds;
@@ -52,7 +53,42 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, ui
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// uint8 matrix [rows, cols_bytes] (quantised weights or their group scales).
+bool make_map_u8(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols_bytes, uint32_t box_inner,
+                 uint32_t box_rows, bool swizzle128) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || !base) return false;
+    cuuint64_t dims[2] = {cols_bytes, rows};
+    cuuint64_t strides[1] = {cols_bytes};
+    cuuint32_t box[2] = {box_inner, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+// A weight-only quantised matrix: raw-code and group-scale descriptors plus its
+// output scales.
+struct QMat {
+    CUtensorMap data, scales;
+    const float *rowscale;  // FP8 per-channel
+    float gscale;           // NVFP4 per-tensor
+};
+
+bool make_qmat(QMat *q, const dspark_mat_t &m, int fmt, uint64_t rows, uint64_t cols) {
+    if (fmt == DSPARK_FMT_FP8) {
+        q->rowscale = (const float *)m.scale;
+        q->gscale = 1.f;
+        return make_map_u8(&q->data, m.data, rows, cols, 128, 64, true) &&
+               make_map_u8(&q->scales, m.data, rows, cols, 128, 64, true);
+    }
+    q->rowscale = nullptr;
+    q->gscale = m.global_scale;
+    return make_map_u8(&q->data, m.data, rows, cols / 2, 128, 64, true) &&
+           make_map_u8(&q->scales, m.scale, rows, cols / 16, 16, 64, false);
+}
 
 int bn_for(int M) {
     if (M <= 16) return 16;
@@ -81,6 +117,9 @@ struct dspark_handle {
     CUtensorMap fc, lm_head;
     CUtensorMap qkv_a[DSPARK_MAX_LAYERS], q_b[DSPARK_MAX_LAYERS], o[DSPARK_MAX_LAYERS], gate[DSPARK_MAX_LAYERS],
         up[DSPARK_MAX_LAYERS], down[DSPARK_MAX_LAYERS];
+    // weight-only formats: the quantised matrices
+    QMat qfc, qq_b[DSPARK_MAX_LAYERS], qo[DSPARK_MAX_LAYERS], qgate[DSPARK_MAX_LAYERS], qup[DSPARK_MAX_LAYERS],
+        qdown[DSPARK_MAX_LAYERS];
     // activation descriptors, cached per (workspace, bs)
     const void *c_ws = nullptr;
     int c_bs = -1;
@@ -190,6 +229,62 @@ cudaError_t gemm(const dspark_handle *h, const CUtensorMap &A, const CUtensorMap
     }
 }
 
+template <int BN, int FMT>
+cudaError_t gemm_q_t(const QMat &A, const QMat *A2, const CUtensorMap &B, GemmParams p, int num_sms,
+                     cudaStream_t st) {
+    using C = GemmQCfg<BN, FMT>;
+    static bool attr = false;
+    if (!attr) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(gemm_q_kernel<BN, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    p.KB = (p.K + C::kKR - 1) / C::kKR;
+    p.units = (long long)p.tiles * p.KB;
+    long long grid = p.units / 2;
+    if (grid > num_sms) grid = num_sms;
+    if (grid < 1) grid = 1;
+    p.grid = (int)grid;
+    p.qscale = A.rowscale;
+    p.qscale2 = A2 ? A2->rowscale : nullptr;
+    p.gscale = A.gscale;
+    p.gscale2 = A2 ? A2->gscale : 1.f;
+    const QMat &a2 = A2 ? *A2 : A;
+    return launch_pdl(gemm_q_kernel<BN, FMT>, dim3(p.grid), dim3(C::kThreads), (size_t)C::kSmemBytes, st, A.data,
+                      a2.data, A.scales, a2.scales, B, p);
+}
+
+cudaError_t gemm_q(const dspark_handle *h, const QMat &A, const QMat *A2, const CUtensorMap &B, int n_out, int K, int M,
+                   int epi, float *out_f32, __nv_bfloat16 *out_bf16, int ldo, void *ws, cudaStream_t st) {
+    GemmParams p;
+    memset(&p, 0, sizeof(p));
+    p.n_out = n_out;
+    p.K = K;
+    p.M = M;
+    p.paired = A2 != nullptr;
+    p.epi = epi;
+    p.out_f32 = out_f32;
+    p.out_bf16 = out_bf16;
+    p.ldo = ldo;
+    p.tiles = p.paired ? (n_out + 63) / 64 : (n_out + 127) / 128;
+    if (p.tiles > kMaxCounters) return cudaErrorInvalidValue;
+    p.counters = (int *)((char *)ws + kCtlCounters);
+    p.err = (int *)((char *)ws + kCtlErr);
+    p.partials = (float *)((char *)ws + kCtlBytes);
+    const int bn = bn_for(M);
+    if (h->g.weight_format == DSPARK_FMT_FP8) {
+        if (bn == 16) return gemm_q_t<16, DSPARK_FMT_FP8>(A, A2, B, p, h->num_sms, st);
+        if (bn == 32) return gemm_q_t<32, DSPARK_FMT_FP8>(A, A2, B, p, h->num_sms, st);
+        if (bn == 64) return gemm_q_t<64, DSPARK_FMT_FP8>(A, A2, B, p, h->num_sms, st);
+    } else {
+        if (bn == 16) return gemm_q_t<16, DSPARK_FMT_NVFP4>(A, A2, B, p, h->num_sms, st);
+        if (bn == 32) return gemm_q_t<32, DSPARK_FMT_NVFP4>(A, A2, B, p, h->num_sms, st);
+        if (bn == 64) return gemm_q_t<64, DSPARK_FMT_NVFP4>(A, A2, B, p, h->num_sms, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
 dspark_status check_geom(const dspark_geom_t *g) {
     if (g->hidden <= 0 || g->n_aux <= 0 || g->n_layers <= 0 || g->n_layers > DSPARK_MAX_LAYERS || g->n_heads <= 0 ||
         g->q_lora <= 0 || g->kv_lora <= 0 || g->d_nope <= 0 || g->d_rope <= 0 || g->d_v <= 0 || g->inter <= 0 ||
@@ -201,7 +296,14 @@ dspark_status check_geom(const dspark_geom_t *g) {
         g->kv_lora > 512)
         return DSPARK_ERR_UNSUPPORTED;
     if (!attention_supported(g->kv_lora + g->d_rope, g->kv_lora)) return DSPARK_ERR_UNSUPPORTED;
-    if (g->weight_format != DSPARK_FMT_BF16) return DSPARK_ERR_UNSUPPORTED;
+    if (g->weight_format != DSPARK_FMT_BF16 && g->weight_format != DSPARK_FMT_FP8 &&
+        g->weight_format != DSPARK_FMT_NVFP4)
+        return DSPARK_ERR_UNSUPPORTED;
+    // NVFP4 group-scale rows (in / 16 bytes) must be whole 16-byte TMA strides
+    if (g->weight_format == DSPARK_FMT_NVFP4 &&
+        ((g->n_aux * g->hidden) % 256 || g->q_lora % 256 || (g->n_heads * g->d_v) % 256 || g->hidden % 256 ||
+         g->inter % 256))
+        return DSPARK_ERR_UNSUPPORTED;
     if (!(g->eps >= 0.f) || !(g->rope_theta > 0.f)) return DSPARK_ERR_SHAPE;
     if ((g->vocab + 127) / 128 > kMaxCounters) return DSPARK_ERR_UNSUPPORTED;
     return DSPARK_OK;
@@ -218,6 +320,7 @@ dspark_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DSPARK_OK :
 bool bad_sampling(float T, float top_p) { return !(T > 0.f) || !isfinite(T) || !(top_p > 0.f) || !(top_p <= 1.f); }
 
 dspark_status check_ws(const dspark_handle_t *h, void *ws, size_t ws_bytes, int bs, int max_ctx) {
+    if (h->g.weight_format != DSPARK_FMT_BF16 && h->g.block * bs > 64) return DSPARK_ERR_UNSUPPORTED;
     if (!ws) return DSPARK_ERR_WORKSPACE;
     if (!aligned16(ws)) return DSPARK_ERR_ALIGN;
     if (ws_bytes < layout_for(h, bs, max_ctx).total) return DSPARK_ERR_WORKSPACE;
@@ -279,6 +382,21 @@ dspark_status dspark_create(const dspark_geom_t *geom, const dspark_weights_t *w
         REQ(L.w_up.data);
         REQ(L.w_down.data);
     }
+    if (g.weight_format != DSPARK_FMT_BF16) {
+        auto req_mat = [&](const dspark_mat_t &m) -> dspark_status {
+            if (!m.scale) return DSPARK_ERR_NULL;
+            if (!aligned16(m.scale)) return DSPARK_ERR_ALIGN;
+            if (g.weight_format == DSPARK_FMT_NVFP4 && !(m.global_scale > 0.f)) return DSPARK_ERR_SHAPE;
+            return DSPARK_OK;
+        };
+        dspark_status q = req_mat(wts->w_fc);
+        for (int l = 0; l < g.n_layers && q == DSPARK_OK; ++l) {
+            const dspark_layer_weights_t &L = wts->layers[l];
+            for (const dspark_mat_t *m : {&L.w_q_b, &L.w_o, &L.w_gate, &L.w_up, &L.w_down})
+                if (q == DSPARK_OK) q = req_mat(*m);
+        }
+        if (q != DSPARK_OK) return q;
+    }
     if (!encode_fn()) return DSPARK_ERR_CUDA;
     dspark_handle *h = new (std::nothrow) dspark_handle();
     if (!h) return DSPARK_ERR_CUDA;
@@ -313,17 +431,31 @@ dspark_status dspark_create(const dspark_geom_t *geom, const dspark_weights_t *w
         mscale2 = m * m;
     }
     h->scale_log2 = (float)(mscale2 / sqrt((double)(g.d_nope + g.d_rope)) * 1.4426950408889634);
-    bool ok = make_map(&h->fc, wts->w_fc.data, g.hidden, (uint64_t)g.n_aux * g.hidden, 64) &&
-              make_map(&h->lm_head, wts->w_lm, g.vocab, g.hidden, 64);
+    const bool bf16w = g.weight_format == DSPARK_FMT_BF16;
+    bool ok = make_map(&h->lm_head, wts->w_lm, g.vocab, g.hidden, 64) &&
+              (!bf16w || make_map(&h->fc, wts->w_fc.data, g.hidden, (uint64_t)g.n_aux * g.hidden, 64));
     const int kvd = g.kv_lora + g.d_rope;
     for (int l = 0; l < g.n_layers && ok; ++l) {
         const dspark_layer_weights_t &L = wts->layers[l];
-        ok = make_map(&h->qkv_a[l], L.w_qkv_a, g.q_lora + kvd, g.hidden, 64) &&
-             make_map(&h->q_b[l], L.w_q_b.data, (uint64_t)g.n_heads * (g.d_nope + g.d_rope), g.q_lora, 64) &&
-             make_map(&h->o[l], L.w_o.data, g.hidden, (uint64_t)g.n_heads * g.d_v, 64) &&
-             make_map(&h->gate[l], L.w_gate.data, g.inter, g.hidden, 64) &&
-             make_map(&h->up[l], L.w_up.data, g.inter, g.hidden, 64) &&
-             make_map(&h->down[l], L.w_down.data, g.hidden, g.inter, 64);
+        ok = make_map(&h->qkv_a[l], L.w_qkv_a, g.q_lora + kvd, g.hidden, 64);
+        if (ok && bf16w)
+            ok = make_map(&h->q_b[l], L.w_q_b.data, (uint64_t)g.n_heads * (g.d_nope + g.d_rope), g.q_lora, 64) &&
+                 make_map(&h->o[l], L.w_o.data, g.hidden, (uint64_t)g.n_heads * g.d_v, 64) &&
+                 make_map(&h->gate[l], L.w_gate.data, g.inter, g.hidden, 64) &&
+                 make_map(&h->up[l], L.w_up.data, g.inter, g.hidden, 64) &&
+                 make_map(&h->down[l], L.w_down.data, g.hidden, g.inter, 64);
+    }
+    const int fmt = g.weight_format;
+    if (ok && fmt != DSPARK_FMT_BF16) {
+        ok = make_qmat(&h->qfc, wts->w_fc, fmt, g.hidden, (uint64_t)g.n_aux * g.hidden);
+        for (int l = 0; l < g.n_layers && ok; ++l) {
+            const dspark_layer_weights_t &L = wts->layers[l];
+            ok = make_qmat(&h->qq_b[l], L.w_q_b, fmt, (uint64_t)g.n_heads * (g.d_nope + g.d_rope), g.q_lora) &&
+                 make_qmat(&h->qo[l], L.w_o, fmt, g.hidden, (uint64_t)g.n_heads * g.d_v) &&
+                 make_qmat(&h->qgate[l], L.w_gate, fmt, g.inter, g.hidden) &&
+                 make_qmat(&h->qup[l], L.w_up, fmt, g.inter, g.hidden) &&
+                 make_qmat(&h->qdown[l], L.w_down, fmt, g.hidden, g.inter);
+        }
     }
     if (!ok) {
         delete h;
@@ -355,6 +487,9 @@ dspark_status dspark_fuse_ctx(dspark_handle_t *h, const void *aux, float *x, int
         h->c_aux = aux;
         h->c_aux_bs = bs;
     }
+    if (g.weight_format != DSPARK_FMT_BF16)
+        return cuda_status(gemm_q(h, h->qfc, nullptr, h->b_aux, g.hidden, g.n_aux * g.hidden, M, EPI_STORE, x, nullptr,
+                                  g.hidden, ws, (cudaStream_t)stream));
     return cuda_status(gemm(h, h->fc, nullptr, h->b_aux, g.hidden, g.n_aux * g.hidden, M, EPI_STORE, x, nullptr,
                             g.hidden, ws, (cudaStream_t)stream));
 }
@@ -416,6 +551,7 @@ dspark_status dspark_draft_block(dspark_handle_t *h, float *x, const dspark_kv_t
     do {                                               \
         if ((call) != cudaSuccess) return DSPARK_ERR_CUDA; \
     } while (0)
+    const bool quant = g.weight_format != DSPARK_FMT_BF16;
     for (int l = 0; l < g.n_layers; ++l) {
         const dspark_layer_weights_t &W = h->w.layers[l];
         RUN(launch_rmsnorm(x, g.hidden, W.attn_norm, g.hidden, g.eps, hn, g.hidden, nullptr, 0, M, err, s));
@@ -423,17 +559,26 @@ dspark_status dspark_draft_block(dspark_handle_t *h, float *x, const dspark_kv_t
                  g.q_lora + kvd, ws, s));
         RUN(launch_latent(qkv, g.q_lora + kvd, g.q_lora, g.kv_lora, g.d_rope, W.q_a_norm, W.kv_a_norm, g.eps,
                           kv->ctx_len, g.block, kv->max_ctx, h->rope, cq, blk, M, err, s));
-        RUN(gemm(h, h->q_b[l], nullptr, h->b_cq, g.n_heads * qhd, g.q_lora, M, EPI_STORE, q, nullptr,
-                 g.n_heads * qhd, ws, s));
+        RUN(quant ? gemm_q(h, h->qq_b[l], nullptr, h->b_cq, g.n_heads * qhd, g.q_lora, M, EPI_STORE, q, nullptr,
+                           g.n_heads * qhd, ws, s)
+                  : gemm(h, h->q_b[l], nullptr, h->b_cq, g.n_heads * qhd, g.q_lora, M, EPI_STORE, q, nullptr,
+                         g.n_heads * qhd, ws, s));
         RUN(launch_q_absorb(q, M, g.n_heads, g.d_nope, g.d_rope, g.kv_lora, g.d_v, (const __nv_bfloat16 *)W.w_kv_b,
                             kv->ctx_len, g.block, kv->max_ctx, h->rope, qt, s));
         ap.pool = (const __nv_bfloat16 *)kv->pools[l];
         RUN(launch_attention(ap, bs, kvd, g.kv_lora, s));
         RUN(launch_v_absorb(olat, M, g.n_heads, g.d_nope, g.d_v, g.kv_lora, (const __nv_bfloat16 *)W.w_kv_b, ov, s));
-        RUN(gemm(h, h->o[l], nullptr, h->b_ov, g.hidden, g.n_heads * g.d_v, M, EPI_ADD, x, nullptr, g.hidden, ws, s));
+        RUN(quant ? gemm_q(h, h->qo[l], nullptr, h->b_ov, g.hidden, g.n_heads * g.d_v, M, EPI_ADD, x, nullptr, g.hidden,
+                           ws, s)
+                  : gemm(h, h->o[l], nullptr, h->b_ov, g.hidden, g.n_heads * g.d_v, M, EPI_ADD, x, nullptr, g.hidden, ws,
+                         s));
         RUN(launch_rmsnorm(x, g.hidden, W.mlp_norm, g.hidden, g.eps, hn, g.hidden, nullptr, 0, M, err, s));
-        RUN(gemm(h, h->gate[l], &h->up[l], h->b_hn, g.inter, g.hidden, M, EPI_SWIGLU, nullptr, act, g.inter, ws, s));
-        RUN(gemm(h, h->down[l], nullptr, h->b_act, g.hidden, g.inter, M, EPI_ADD, x, nullptr, g.hidden, ws, s));
+        RUN(quant ? gemm_q(h, h->qgate[l], &h->qup[l], h->b_hn, g.inter, g.hidden, M, EPI_SWIGLU, nullptr, act, g.inter,
+                           ws, s)
+                  : gemm(h, h->gate[l], &h->up[l], h->b_hn, g.inter, g.hidden, M, EPI_SWIGLU, nullptr, act, g.inter, ws,
+                         s));
+        RUN(quant ? gemm_q(h, h->qdown[l], nullptr, h->b_act, g.hidden, g.inter, M, EPI_ADD, x, nullptr, g.hidden, ws, s)
+                  : gemm(h, h->down[l], nullptr, h->b_act, g.hidden, g.inter, M, EPI_ADD, x, nullptr, g.hidden, ws, s));
     }
     RUN(launch_rmsnorm(x, g.hidden, h->w.final_norm, g.hidden, g.eps, hout, g.hidden, h_out, g.hidden, M, err, s));
     RUN(gemm(h, h->lm_head, nullptr, h->b_hout, g.vocab, g.hidden, M, EPI_STORE, z, nullptr, g.vocab, ws, s));

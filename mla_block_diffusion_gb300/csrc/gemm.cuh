@@ -47,7 +47,18 @@ struct GemmParams {
     float *partials;    // [2 * grid][128][BN]
     int *counters;      // [tiles], zero between launches
     int *err;
+    // weight-only formats: the accumulator row of output channel n is multiplied by
+    // qscale[n] (FP8 per-channel scales; qscale2 for the up rows of a paired tile) or
+    // by gscale / gscale2 (NVFP4 per-tensor scales). Unused for bf16 weights.
+    const float *qscale, *qscale2;
+    float gscale, gscale2;
 };
+
+// Per-row output multiplier of a weight-only quantised matrix.
+__device__ inline float gemm_row_scale(const GemmParams &p, int n, bool second) {
+    if (p.qscale) return second ? p.qscale2[n] : p.qscale[n];
+    return second ? p.gscale2 : p.gscale;
+}
 
 constexpr int kGemmMaxSmem = 232448;
 
@@ -101,7 +112,7 @@ __device__ inline void gemm_store_swiglu(const GemmParams &p, int n, int m, floa
 // (fixed order: the result does not depend on which CTA arrived last). Thread
 // et owns output channel et; every partial row is read as float4 vectors, four
 // contributors at a time, so the loads are independent and overlap.
-template <int BN>
+template <int BN, bool SCALED = false, int U = 4>
 __device__ __forceinline__ void gemm_reduce_tile(const GemmParams &p, int tile, int c_lo, int c_hi, int et, int nch) {
     const int n = tile * nch + et;
     if (et >= nch || n >= p.n_out) return;
@@ -109,10 +120,10 @@ __device__ __forceinline__ void gemm_reduce_tile(const GemmParams &p, int tile, 
         float a1[16], a2[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) a1[j] = a2[j] = 0.f;
-        for (int cc = c_lo; cc <= c_hi; cc += 4) {
-            float4 v1[4][4], v2[4][4];
+        for (int cc = c_lo; cc <= c_hi; cc += U) {
+            float4 v1[U][4], v2[U][4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < U; ++u) {
                 if (cc + u <= c_hi) {
                     const int first_t = (int)(gemm_unit_begin(cc + u, p.units, p.grid) / p.KB);
                     const int sl = (tile == first_t) ? 2 * (cc + u) : 2 * (cc + u) + 1;
@@ -127,7 +138,7 @@ __device__ __forceinline__ void gemm_reduce_tile(const GemmParams &p, int tile, 
                 }
             }
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < U; ++u) {
                 if (cc + u <= c_hi) {
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
@@ -143,6 +154,14 @@ __device__ __forceinline__ void gemm_reduce_tile(const GemmParams &p, int tile, 
                         }
                     }
                 }
+            }
+        }
+        if (SCALED) {
+            const float f1 = gemm_row_scale(p, n, false), f2 = p.paired ? gemm_row_scale(p, n, true) : 0.f;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                a1[j] *= f1;
+                a2[j] *= f2;
             }
         }
 #pragma unroll

@@ -109,6 +109,14 @@ def _p(t: Optional[torch.Tensor]):
     return None if t is None else C.c_void_p(t.data_ptr())
 
 
+def _mat(v) -> "Mat":
+    """A matrix entry: a bf16 tensor, or (data, scale, global_scale) for FP8 / NVFP4."""
+    if isinstance(v, tuple):
+        d, sc, g = v
+        return Mat(_p(d), _p(sc), float(g))
+    return Mat(_p(v), None, 1.0)
+
+
 def _stream():
     return C.c_void_p(torch.cuda.current_stream().cuda_stream)
 
@@ -122,7 +130,9 @@ class DSpark:
     """One drafter (geometry + device-resident weights) bound to libdspark.
 
     ``W`` maps names to device tensors (bf16 matrices row-major [out, in], fp32
-    norm gains and confidence head), as produced by the seeded generators.
+    norm gains and confidence head), as produced by the seeded generators. With
+    ``weight_format`` FP8 or NVFP4 the quantised matrices (fc, q_b, o, gate, up,
+    down) are (data, scale, global_scale) triples.
     The workspace is allocated here, zero-filled, for up to ``max_bs``
     sequences and contexts of ``max_ctx`` tokens.
     """
@@ -134,7 +144,7 @@ class DSpark:
         L = lib()
         self.geom = geom_struct(G, weight_format)
         w = Weights()
-        w.w_fc = Mat(_p(W["w_fc"]), None, 1.0)
+        w.w_fc = _mat(W["w_fc"])
         for l in range(G.n_layers):
             P = f"l{l}."
             lw = w.layers[l]
@@ -142,13 +152,13 @@ class DSpark:
             lw.w_qkv_a = _p(W[P + "w_qkv_a"])
             lw.q_a_norm = _p(W[P + "q_a_norm"])
             lw.kv_a_norm = _p(W[P + "kv_a_norm"])
-            lw.w_q_b = Mat(_p(W[P + "w_q_b"]), None, 1.0)
+            lw.w_q_b = _mat(W[P + "w_q_b"])
             lw.w_kv_b = _p(W[P + "w_kv_b"])
-            lw.w_o = Mat(_p(W[P + "w_o"]), None, 1.0)
+            lw.w_o = _mat(W[P + "w_o"])
             lw.mlp_norm = _p(W[P + "mlp_norm"])
-            lw.w_gate = Mat(_p(W[P + "w_gate"]), None, 1.0)
-            lw.w_up = Mat(_p(W[P + "w_up"]), None, 1.0)
-            lw.w_down = Mat(_p(W[P + "w_down"]), None, 1.0)
+            lw.w_gate = _mat(W[P + "w_gate"])
+            lw.w_up = _mat(W[P + "w_up"])
+            lw.w_down = _mat(W[P + "w_down"])
         w.final_norm = _p(W["final_norm"])
         w.w_lm = _p(W["w_lm"])
         w.markov_w1 = _p(W["markov_w1"])

@@ -103,7 +103,11 @@ def test_host_argument_checks(L):
     bad = M.geom_struct(FULL)
     bad.vocab = 1 << 18
     assert L.dspark_create(C.byref(bad), C.byref(_fake_weights(FULL)), C.byref(h)) == 4
-    bad = M.geom_struct(TINY, weight_format=M.FMT_FP8)
+    bad = M.geom_struct(TINY, weight_format=7)  # no such format
+    assert L.dspark_create(C.byref(bad), C.byref(w), C.byref(h)) == 4
+    bad = M.geom_struct(TINY, weight_format=M.FMT_FP8)  # FP8 needs per-channel scales
+    assert L.dspark_create(C.byref(bad), C.byref(w), C.byref(h)) == 1
+    bad = M.geom_struct(TINY, weight_format=M.FMT_NVFP4)  # q_lora 128: group-scale rows not 16-byte strides
     assert L.dspark_create(C.byref(bad), C.byref(w), C.byref(h)) == 4
     w2 = _fake_weights(TINY)
     w2.layers[1].w_up = M.dspark.Mat(None, None, 1.0)

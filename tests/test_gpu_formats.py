@@ -1,0 +1,103 @@
+"""Weight-only FP8 and NVFP4 through the C ABI against the oracle on the decoded
+weights ("Kimi-K3-DSpark-NVFP4": FP8 per-channel and NVFP4 group-16 weight-only).
+Tolerance: relative L2 <= 3e-2 on hidden states and logits."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import formats as F
+from oracle import network as N
+from synthetic import generate as gen
+from synthetic import quantize as Q
+from synthetic.configs import FORMAT_FP8, FORMAT_NVFP4, TINY_STEP
+from tests.gpu_harness import MID, workload
+from tests.helpers import f64, rel_l2
+
+pytestmark = pytest.mark.gpu
+TOL = 3e-2
+FMTS = {"fp8": FORMAT_FP8, "nvfp4": FORMAT_NVFP4}
+KEYS = ("attn_norm", "w_qkv_a", "q_a_norm", "kv_a_norm", "w_q_b", "w_kv_b", "w_o", "mlp_norm", "w_gate", "w_up",
+        "w_down")
+
+
+@pytest.fixture(scope="module")
+def M():
+    import mla_block_diffusion_gb300 as M
+    from mla_block_diffusion_gb300 import build
+    build.build()
+    return M
+
+
+def decode(v, fmt):
+    """Oracle-side decoding of one matrix entry to float64."""
+    if not isinstance(v, tuple):
+        return f64(v)
+    d, sc, g = v
+    if fmt == "fp8":
+        return F.dequant_fp8(d.cpu().numpy(), sc.cpu().numpy())
+    return F.dequant_nvfp4(d.cpu().numpy(), sc.cpu().numpy(), g)
+
+
+def to_dev(Wq):
+    out = {}
+    for k, v in Wq.items():
+        out[k] = tuple(x.cuda() if torch.is_tensor(x) else x for x in v) if isinstance(v, tuple) else v.cuda()
+    return out
+
+
+@pytest.mark.parametrize("fmt,w", [("fp8", TINY_STEP), ("fp8", workload(MID, 2, (300, 90), seed=9)),
+                                   ("nvfp4", workload(MID, 2, (300, 90), seed=9))],
+                         ids=["fp8_tiny", "fp8_mid", "nvfp4_mid"])
+def test_weight_only_draft(M, fmt, w):
+    G, bs = w.geom, w.bs
+    W = gen.make_weights(w, "cpu")
+    I = gen.make_inputs(w, "cpu")
+    Wq = Q.quantise_weights(W, fmt, G.n_layers)
+    ds = M.DSpark(G, to_dev(Wq), max_bs=bs, max_ctx=max(I["ctx_list"]), weight_format=FMTS[fmt])
+    x = torch.empty(bs, G.block, G.hidden, dtype=torch.float32, device="cuda")
+    ds.fuse_ctx(I["aux"].cuda(), x, bs)
+    x0 = x.clone()
+    kv = ds.make_kv([p.cuda() for p in I["kv_pools"]], I["page_table"].cuda(), I["ctx_len"].cuda(),
+                    max(I["ctx_list"]))
+    h = torch.empty_like(x)
+    z = torch.empty(bs, G.block, G.vocab, dtype=torch.float32, device="cuda")
+    ds.draft_block(x, kv, h, z, bs)
+    assert ds.check() == 0
+    layers = [{k: decode(Wq[f"l{l}.{k}"], fmt) for k in KEYS} for l in range(G.n_layers)]
+    w_fc = decode(Wq["w_fc"], fmt)
+    pools = [f64(p) for p in I["kv_pools"]]
+    table = I["page_table"].numpy()
+    for b, ctx in enumerate(I["ctx_list"]):
+        ox = N.fuse_ctx(w_fc, f64(I["aux"][b]))
+        assert rel_l2(x0[b].cpu().numpy(), ox) < TOL
+        caches = [N.gather_cache(p, table[b], ctx) for p in pools]
+        oh, oz = N.draft_block(ox, layers, f64(W["final_norm"]), f64(W["w_lm"]), G, caches, ctx)
+        assert rel_l2(h[b].cpu().numpy(), oh) < TOL, b
+        assert rel_l2(z[b].cpu().numpy(), oz) < TOL, b
+
+
+def test_nvfp4_rejects_unaligned_geometry(M):
+    G = TINY_STEP.geom  # q_lora 128: group-scale rows of 8 bytes are not TMA strides
+    W = gen.make_weights(TINY_STEP, "cpu")
+    Wq = Q.quantise_weights(W, "nvfp4", G.n_layers)
+    with pytest.raises(M.DSparkError) as e:
+        M.DSpark(G, to_dev(Wq), max_bs=1, weight_format=FORMAT_NVFP4)
+    assert e.value.status == 4
+
+
+def test_activation_beyond_f16_range_is_reported(M):
+    """The quantised GEMMs take activations in f16: a magnitude above 65504 is
+    reported as DSPARK_ERR_BAD_INPUT (17), and a clean call afterwards is OK."""
+    w = TINY_STEP
+    G = w.geom
+    W = gen.make_weights(w, "cpu")
+    I = gen.make_inputs(w, "cpu")
+    ds = M.DSpark(G, to_dev(Q.quantise_weights(W, "fp8", G.n_layers)), max_bs=1, weight_format=FORMAT_FP8)
+    x = torch.empty(1, G.block, G.hidden, dtype=torch.float32, device="cuda")
+    aux = I["aux"].cuda()
+    bad = aux.clone()
+    bad.view(-1)[5] = 70000.0
+    ds.fuse_ctx(bad, x, 1)
+    assert ds.check() == 17
+    ds.fuse_ctx(aux, x, 1)
+    assert ds.check() == 0
