@@ -527,7 +527,7 @@ def only_call(args, G, local):
     libbuild.build()
     torch.cuda.set_device(local)
     if args.only == "rollout":
-        g = replace(G, hidden=64, n_aux=1, n_layers=1, n_heads=1, q_lora=64, kv_lora=64, d_nope=8, d_rope=16, d_v=64,
+        g = replace(G, hidden=64, n_aux=1, n_layers=1, n_heads=1, q_lora=64, kv_lora=64, d_nope=16, d_rope=16, d_v=64,
                     inter=64)
     else:
         g = replace(G, hidden=1024, n_aux=1, n_layers=1, q_lora=256, inter=64, vocab=128, rank=16)

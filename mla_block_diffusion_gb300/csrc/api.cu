@@ -54,6 +54,19 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, ui
 }
 
 // uint8 matrix [rows, cols_bytes] (quantised weights or their group scales).
+bool encode_map_u32(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_inner,
+                    uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || !base) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 4};
+    cuuint32_t box[2] = {box_inner, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_map_u8(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols_bytes, uint32_t box_inner,
                  uint32_t box_rows, bool swizzle128) {
     EncodeTiledFn fn = encode_fn();
@@ -115,6 +128,7 @@ struct dspark_handle {
     RopeTable rope;
     float scale_log2;
     CUtensorMap fc, lm_head;
+    CUtensorMap w2;             // Markov w2 as uint32 pairs [rank, vocab / 2], rollout boxes
     CUtensorMap qkv_a[DSPARK_MAX_LAYERS], q_b[DSPARK_MAX_LAYERS], o[DSPARK_MAX_LAYERS], gate[DSPARK_MAX_LAYERS],
         up[DSPARK_MAX_LAYERS], down[DSPARK_MAX_LAYERS];
     // weight-only formats: the quantised matrices
@@ -432,7 +446,10 @@ dspark_status dspark_create(const dspark_geom_t *geom, const dspark_weights_t *w
     }
     h->scale_log2 = (float)(mscale2 / sqrt((double)(g.d_nope + g.d_rope)) * 1.4426950408889634);
     const bool bf16w = g.weight_format == DSPARK_FMT_BF16;
-    bool ok = make_map(&h->lm_head, wts->w_lm, g.vocab, g.hidden, 64) &&
+    int roll_box_w = 0, roll_nbox = 0;
+    rollout_box(g.vocab, h->samp_grid, &roll_box_w, &roll_nbox);
+    bool ok = encode_map_u32(&h->w2, wts->markov_w2, g.rank, (uint64_t)g.vocab / 2, (uint32_t)roll_box_w, 16) &&
+              make_map(&h->lm_head, wts->w_lm, g.vocab, g.hidden, 64) &&
               (!bf16w || make_map(&h->fc, wts->w_fc.data, g.hidden, (uint64_t)g.n_aux * g.hidden, 64));
     const int kvd = g.kv_lora + g.d_rope;
     for (int l = 0; l < g.n_layers && ok; ++l) {
@@ -622,7 +639,7 @@ dspark_status dspark_markov_rollout(dspark_handle_t *h, const float *z, const in
     p.scratch = (unsigned long long *)((char *)ws + L.scratch);
     p.ctl = (SampleCtl *)((char *)ws + kCtlSample);
     p.err = (int *)((char *)ws + kCtlErr);
-    return cuda_status(launch_rollout(p, h->samp_grid, (cudaStream_t)stream));
+    return cuda_status(launch_rollout(h->w2, p, h->samp_grid, (cudaStream_t)stream));
 }
 
 dspark_status dspark_confidence(dspark_handle_t *h, const float *h_out, float *conf, int bs, void *stream) {

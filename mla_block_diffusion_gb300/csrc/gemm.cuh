@@ -110,30 +110,29 @@ __device__ inline void gemm_store_swiglu(const GemmParams &p, int n, int m, floa
 
 // Sum of the split partials of one tile, contributors in increasing CTA order
 // (fixed order: the result does not depend on which CTA arrived last). Thread
-// et owns output channel et; every partial row is read as float4 vectors, four
-// contributors at a time, so the loads are independent and overlap.
-template <int BN, bool SCALED = false, int U = 4>
-__device__ __forceinline__ void gemm_reduce_tile(const GemmParams &p, int tile, int c_lo, int c_hi, int et, int nch) {
-    const int n = tile * nch + et;
-    if (et >= nch || n >= p.n_out) return;
-    for (int c0 = 0; c0 < p.M; c0 += 16) {
-        float a1[16], a2[16];
+// et owns output channel et and takes the valid rows in chunks of 8: the two
+// float4 of every contributor of a batch of U are loaded before any is added,
+// so a tile split over up to U CTAs costs one L2 round trip per chunk.
+template <int BN, bool SCALED, int U, bool PAIRED>
+__device__ __forceinline__ void gemm_reduce_impl(const GemmParams &p, int tile, int c_lo, int c_hi, int et, int n) {
+    for (int c0 = 0; c0 < p.M; c0 += 8) {
+        float a1[8], a2[8];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) a1[j] = a2[j] = 0.f;
+        for (int j = 0; j < 8; ++j) a1[j] = a2[j] = 0.f;
         for (int cc = c_lo; cc <= c_hi; cc += U) {
-            float4 v1[U][4], v2[U][4];
+            float4 v1[U][2], v2[PAIRED ? U : 1][2];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 if (cc + u <= c_hi) {
                     const int first_t = (int)(gemm_unit_begin(cc + u, p.units, p.grid) / p.KB);
                     const int sl = (tile == first_t) ? 2 * (cc + u) : 2 * (cc + u) + 1;
                     const float4 *src = (const float4 *)(p.partials + ((size_t)sl * 128 + et) * BN + c0);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) v1[u][j] = __ldcg(src + j);
-                    if (p.paired) {
+                    v1[u][0] = __ldcg(src);
+                    v1[u][1] = __ldcg(src + 1);
+                    if (PAIRED) {
                         const float4 *src2 = src + 64 * BN / 4;
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) v2[u][j] = __ldcg(src2 + j);
+                        v2[u][0] = __ldcg(src2);
+                        v2[u][1] = __ldcg(src2 + 1);
                     }
                 }
             }
@@ -141,12 +140,12 @@ __device__ __forceinline__ void gemm_reduce_tile(const GemmParams &p, int tile, 
             for (int u = 0; u < U; ++u) {
                 if (cc + u <= c_hi) {
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
+                    for (int j = 0; j < 2; ++j) {
                         a1[4 * j] += v1[u][j].x;
                         a1[4 * j + 1] += v1[u][j].y;
                         a1[4 * j + 2] += v1[u][j].z;
                         a1[4 * j + 3] += v1[u][j].w;
-                        if (p.paired) {
+                        if (PAIRED) {
                             a2[4 * j] += v2[u][j].x;
                             a2[4 * j + 1] += v2[u][j].y;
                             a2[4 * j + 2] += v2[u][j].z;
@@ -157,23 +156,33 @@ __device__ __forceinline__ void gemm_reduce_tile(const GemmParams &p, int tile, 
             }
         }
         if (SCALED) {
-            const float f1 = gemm_row_scale(p, n, false), f2 = p.paired ? gemm_row_scale(p, n, true) : 0.f;
+            const float f1 = gemm_row_scale(p, n, false), f2 = PAIRED ? gemm_row_scale(p, n, true) : 0.f;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
+            for (int j = 0; j < 8; ++j) {
                 a1[j] *= f1;
                 a2[j] *= f2;
             }
         }
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
+        for (int j = 0; j < 8; ++j) {
             if (c0 + j < p.M) {
-                if (p.paired)
+                if (PAIRED)
                     gemm_store_swiglu(p, n, c0 + j, a1[j], a2[j]);
                 else
                     gemm_store(p, n, c0 + j, a1[j]);
             }
         }
     }
+}
+
+template <int BN, bool SCALED = false, int U = 8>
+__device__ __forceinline__ void gemm_reduce_tile(const GemmParams &p, int tile, int c_lo, int c_hi, int et, int nch) {
+    const int n = tile * nch + et;
+    if (et >= nch || n >= p.n_out) return;
+    if (p.paired)
+        gemm_reduce_impl<BN, SCALED, (U > 1 ? U / 2 : 1), true>(p, tile, c_lo, c_hi, et, n);
+    else
+        gemm_reduce_impl<BN, SCALED, U, false>(p, tile, c_lo, c_hi, et, n);
 }
 
 template <int BN>

@@ -406,7 +406,7 @@ __global__ void __launch_bounds__(GemmQCfg<BN, FMT>::kThreads, 1)
                 named_bar_sync(1, 128);
                 if (s_last) {
                     __threadfence();
-                    gemm_reduce_tile<BN, true, 1>(p, tile, c_lo, c_hi, et, nch);
+                    gemm_reduce_tile<BN, true, 2>(p, tile, c_lo, c_hi, et, nch);
                 }
             }
             u = seg_end;

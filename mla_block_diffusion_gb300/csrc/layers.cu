@@ -36,32 +36,56 @@ __device__ float block_sum(float v, float *red) {
 
 // ---------------------------------------------------------------------------
 // RMSNorm: y = x / sqrt(mean(x^2) + eps) * g, written as bf16 (GEMM operand)
-// and optionally fp32. One CTA per row; H a multiple of 4.
+// and optionally fp32. One CTA per row; H a multiple of 4. The gains are read
+// before the wait on the producing kernel; the first 4 * blockDim float4 of the
+// row stay in registers between the two passes.
 // ---------------------------------------------------------------------------
-__global__ void rmsnorm_kernel(const float *__restrict__ x, int ldx, const float *__restrict__ g, int H, float eps,
-                               __nv_bfloat16 *__restrict__ y, int ldy, float *__restrict__ y32, int ldy32, int *err) {
+constexpr int kNormThreads = 512;
+
+__global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const float *__restrict__ x, int ldx,
+                                                               const float *__restrict__ g, int H, float eps,
+                                                               __nv_bfloat16 *__restrict__ y, int ldy,
+                                                               float *__restrict__ y32, int ldy32, int *err) {
     pdl_trigger();
-    pdl_wait();
     __shared__ float red[33];
-    const int m = blockIdx.x;
+    const int m = blockIdx.x, n4 = H / 4;
     const float4 *xr = (const float4 *)(x + (size_t)m * ldx);
+    const float4 *g4 = (const float4 *)g;
+    float4 gr[4], v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int i = threadIdx.x + u * blockDim.x;
+        gr[u] = i < n4 ? __ldg(g4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    pdl_wait();
     float ss = 0.f;
-    for (int i = threadIdx.x; i < H / 4; i += blockDim.x) {
-        float4 v = xr[i];
-        ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int i = threadIdx.x + u * blockDim.x;
+        v[u] = i < n4 ? xr[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) ss += v[u].x * v[u].x + v[u].y * v[u].y + v[u].z * v[u].z + v[u].w * v[u].w;
+    for (int i = threadIdx.x + 4 * blockDim.x; i < n4; i += blockDim.x) {
+        const float4 t = xr[i];
+        ss += t.x * t.x + t.y * t.y + t.z * t.z + t.w * t.w;
     }
     ss = block_sum(ss, red);
     if (!isfinite(ss) && threadIdx.x == 0) set_error(err, DSPARK_ERR_BAD_INPUT);
     const float r = rsqrtf(ss / (float)H + eps);
-    const float4 *g4 = (const float4 *)g;
-    for (int i = threadIdx.x; i < H / 4; i += blockDim.x) {
-        float4 v = xr[i], gg = g4[i];
-        float4 o = make_float4(v.x * r * gg.x, v.y * r * gg.y, v.z * r * gg.z, v.w * r * gg.w);
+    auto emit = [&](int i, float4 t, float4 gg) {
+        const float4 o = make_float4(t.x * r * gg.x, t.y * r * gg.y, t.z * r * gg.z, t.w * r * gg.w);
         __nv_bfloat162 *yb = (__nv_bfloat162 *)(y + (size_t)m * ldy + 4 * i);
         yb[0] = __floats2bfloat162_rn(o.x, o.y);
         yb[1] = __floats2bfloat162_rn(o.z, o.w);
         if (y32) ((float4 *)(y32 + (size_t)m * ldy32))[i] = o;
+    };
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int i = threadIdx.x + u * blockDim.x;
+        if (i < n4) emit(i, v[u], gr[u]);
     }
+    for (int i = threadIdx.x + 4 * blockDim.x; i < n4; i += blockDim.x) emit(i, xr[i], g4[i]);
 }
 
 // ---------------------------------------------------------------------------
@@ -110,66 +134,67 @@ __global__ void latent_kernel(const float *__restrict__ qkv, int ld, int q_lora,
 
 // ---------------------------------------------------------------------------
 // q absorption: Q_h = [W_kb,h^T q_nope,h || RoPE(q_rope,h)] per row and head,
-// bf16 [M, n_h, kv_lora + d_rope]. Grid (n_h, kv_lora / 32): a CTA owns one
-// head and 32 latent columns; its 256 threads split d_nope into 16 groups x 16
-// column pairs, hold their slice of W_kb in registers (loaded once, loads
-// independent) and sweep the rows in chunks of 16; the 16 partial sums are
-// added in group order through shared memory.
+// bf16 [M, n_h, kv_lora + d_rope]. Grid (n_h, kv_lora / 64), 128 threads: a CTA
+// owns one head and 64 latent columns; warp w takes the quarter w of d_nope and
+// lane l the column pair 2l, so every d row of W_kb is one coalesced 128-byte
+// read. The thread's W_kb slice (<= 64 bf16 pairs) is loaded once into
+// registers; the rows sweep in chunks of 8 from shared memory and the four
+// quarter sums are added in quarter order.
 // ---------------------------------------------------------------------------
 constexpr int kAbsorbRows = 16;
-constexpr int kQAbsCols = 32;
-constexpr int kQAbsGroups = 16;
+constexpr int kQAbsRows = 8;
+constexpr int kQAbsCols = 64;
 
-__global__ void __launch_bounds__(256) q_absorb_kernel(const float *__restrict__ q, int M, int n_h, int d_nope,
+__global__ void __launch_bounds__(128) q_absorb_kernel(const float *__restrict__ q, int M, int n_h, int d_nope,
                                                        int d_rope, int kv_lora, int d_v,
                                                        const __nv_bfloat16 *__restrict__ w_kvb,
                                                        const int32_t *__restrict__ ctx_len, int block, int max_ctx,
                                                        RopeTable rt, __nv_bfloat16 *__restrict__ qt) {
     pdl_trigger();
-    pdl_wait();
     extern __shared__ float sm[];
-    float *sq = sm;                               // [kAbsorbRows][d_nope]
-    float *red = sm + kAbsorbRows * d_nope;       // [kQAbsGroups][kAbsorbRows][kQAbsCols]
+    float *sq = sm;                             // [kQAbsRows][d_nope]
+    float *red = sm + kQAbsRows * d_nope;       // [4][kQAbsRows][kQAbsCols]
     const int h = blockIdx.x, c0 = blockIdx.y * kQAbsCols;
-    const int cp = threadIdx.x & 15, dg = threadIdx.x >> 4;
-    const int dper = d_nope / kQAbsGroups;  // <= 16
+    const int lane = threadIdx.x & 31, qd = threadIdx.x >> 5;
+    const int dq = d_nope / 4;  // <= 64
     const int qhd = d_nope + d_rope, kvd = kv_lora + d_rope;
-    const __nv_bfloat16 *W = w_kvb + (size_t)h * (d_nope + d_v) * kv_lora + c0 + 2 * cp;
-    float2 w[16];
+    // the weights do not depend on the previous kernel: load them before the wait
+    const __nv_bfloat16 *W = w_kvb + ((size_t)h * (d_nope + d_v) + qd * dq) * kv_lora + c0 + 2 * lane;
+    uint32_t w[64];
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
-        w[i] = i < dper ? __bfloat1622float2(*(const __nv_bfloat162 *)(W + (size_t)(dg * dper + i) * kv_lora))
-                        : make_float2(0.f, 0.f);
-    for (int m0 = 0; m0 < M; m0 += kAbsorbRows) {
-        for (int idx = threadIdx.x; idx < kAbsorbRows * d_nope; idx += blockDim.x) {
+    for (int i = 0; i < 64; ++i) w[i] = i < dq ? __ldg((const unsigned int *)(W + (size_t)i * kv_lora)) : 0u;
+    pdl_wait();
+    for (int m0 = 0; m0 < M; m0 += kQAbsRows) {
+        for (int idx = threadIdx.x; idx < kQAbsRows * d_nope; idx += blockDim.x) {
             const int mm = idx / d_nope, d = idx % d_nope, m = m0 + mm;
             sq[idx] = (m < M) ? q[((size_t)m * n_h + h) * qhd + d] : 0.f;
         }
         __syncthreads();
-        float a0[kAbsorbRows], a1[kAbsorbRows];
+        float a0[kQAbsRows], a1[kQAbsRows];
 #pragma unroll
-        for (int mm = 0; mm < kAbsorbRows; ++mm) a0[mm] = a1[mm] = 0.f;
+        for (int mm = 0; mm < kQAbsRows; ++mm) a0[mm] = a1[mm] = 0.f;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            if (i < dper) {
+        for (int i = 0; i < 64; ++i) {
+            if (i < dq) {
+                const float2 wf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[i]));
 #pragma unroll
-                for (int mm = 0; mm < kAbsorbRows; ++mm) {
-                    const float x = sq[mm * d_nope + dg * dper + i];
-                    a0[mm] = fmaf(w[i].x, x, a0[mm]);
-                    a1[mm] = fmaf(w[i].y, x, a1[mm]);
+                for (int mm = 0; mm < kQAbsRows; ++mm) {
+                    const float x = sq[mm * d_nope + qd * dq + i];
+                    a0[mm] = fmaf(wf.x, x, a0[mm]);
+                    a1[mm] = fmaf(wf.y, x, a1[mm]);
                 }
             }
         }
 #pragma unroll
-        for (int mm = 0; mm < kAbsorbRows; ++mm)
-            *(float2 *)(red + ((size_t)dg * kAbsorbRows + mm) * kQAbsCols + 2 * cp) = make_float2(a0[mm], a1[mm]);
+        for (int mm = 0; mm < kQAbsRows; ++mm)
+            *(float2 *)(red + ((size_t)qd * kQAbsRows + mm) * kQAbsCols + 2 * lane) = make_float2(a0[mm], a1[mm]);
         __syncthreads();
-        for (int idx = threadIdx.x; idx < kAbsorbRows * kQAbsCols / 2; idx += blockDim.x) {
+        for (int idx = threadIdx.x; idx < kQAbsRows * kQAbsCols / 2; idx += blockDim.x) {
             const int mm = idx / (kQAbsCols / 2), c2 = 2 * (idx % (kQAbsCols / 2)), m = m0 + mm;
             float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-            for (int g = 0; g < kQAbsGroups; ++g) {
-                const float2 v = *(const float2 *)(red + ((size_t)g * kAbsorbRows + mm) * kQAbsCols + c2);
+            for (int g = 0; g < 4; ++g) {
+                const float2 v = *(const float2 *)(red + ((size_t)g * kQAbsRows + mm) * kQAbsCols + c2);
                 s0 += v.x;
                 s1 += v.y;
             }
@@ -527,15 +552,35 @@ __global__ void attn_combine_kernel(const float *__restrict__ part_o, const floa
     }
 }
 
-// Confidence head: c = sigmoid(w . h_out + b) per block row.
+// Confidence head: c = sigmoid(w . h_out + b) per block row (H a multiple of 4;
+// one CTA per row, the weight slice read before the wait, fixed-order sums).
 __global__ void confidence_kernel(const float *__restrict__ h_out, int H, const float *__restrict__ w, float bias,
                                   float *__restrict__ conf) {
     pdl_trigger();
-    pdl_wait();
     __shared__ float red[33];
-    const int m = blockIdx.x;
+    const int m = blockIdx.x, n4 = H / 4;
+    const float4 *w4 = (const float4 *)w;
+    const float4 *x4 = (const float4 *)(h_out + (size_t)m * H);
+    float4 wr[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int i = threadIdx.x + u * blockDim.x;
+        wr[u] = i < n4 ? __ldg(w4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    pdl_wait();
     float acc = 0.f;
-    for (int i = threadIdx.x; i < H; i += blockDim.x) acc = fmaf(w[i], h_out[(size_t)m * H + i], acc);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int i = threadIdx.x + u * blockDim.x;
+        if (i < n4) {
+            const float4 x = x4[i];
+            acc = fmaf(wr[u].x, x.x, fmaf(wr[u].y, x.y, fmaf(wr[u].z, x.z, fmaf(wr[u].w, x.w, acc))));
+        }
+    }
+    for (int i = threadIdx.x + 4 * blockDim.x; i < n4; i += blockDim.x) {
+        const float4 ww = w4[i], x = x4[i];
+        acc = fmaf(ww.x, x.x, fmaf(ww.y, x.y, fmaf(ww.z, x.z, fmaf(ww.w, x.w, acc))));
+    }
     acc = block_sum(acc, red);
     if (threadIdx.x == 0) conf[m] = 1.f / (1.f + expf(-(acc + bias)));
 }
@@ -545,7 +590,8 @@ __global__ void confidence_kernel(const float *__restrict__ h_out, int H, const 
 // ---------------------------------------------------------------------------
 cudaError_t launch_rmsnorm(const float *x, int ldx, const float *g, int H, float eps, __nv_bfloat16 *y, int ldy,
                            float *y32, int ldy32, int M, int *err, cudaStream_t st) {
-    return launch_pdl(rmsnorm_kernel, dim3(M), dim3(256), 0, st, x, ldx, g, H, eps, y, ldy, y32, ldy32, err);
+    return launch_pdl(rmsnorm_kernel, dim3(M), dim3(kNormThreads), 0, st, x, ldx, g, H, eps, y, ldy, y32, ldy32,
+                      err);
 }
 
 cudaError_t launch_latent(const float *qkv, int ld, int q_lora, int kv_lora, int d_rope, const float *g_q,
@@ -560,8 +606,8 @@ cudaError_t launch_q_absorb(const float *q, int M, int n_h, int d_nope, int d_ro
                             const __nv_bfloat16 *w_kvb, const int32_t *ctx_len, int block, int max_ctx,
                             const RopeTable &rt, __nv_bfloat16 *qt, cudaStream_t st) {
     dim3 grid(n_h, kv_lora / kQAbsCols);
-    const size_t smem = ((size_t)kAbsorbRows * d_nope + (size_t)kQAbsGroups * kAbsorbRows * kQAbsCols) * sizeof(float);
-    return launch_pdl(q_absorb_kernel, grid, dim3(256), smem, st, q, M, n_h, d_nope, d_rope, kv_lora, d_v, w_kvb,
+    const size_t smem = ((size_t)kQAbsRows * d_nope + (size_t)4 * kQAbsRows * kQAbsCols) * sizeof(float);
+    return launch_pdl(q_absorb_kernel, grid, dim3(128), smem, st, q, M, n_h, d_nope, d_rope, kv_lora, d_v, w_kvb,
                       ctx_len, block, max_ctx, rt, qt);
 }
 
@@ -611,7 +657,7 @@ cudaError_t launch_attention(const AttnParams &p, int bs, int dqk, int dv, cudaS
 
 cudaError_t launch_confidence(const float *h_out, int H, const float *w, float bias, float *conf, int M,
                               cudaStream_t st) {
-    return launch_pdl(confidence_kernel, dim3(M), dim3(256), 0, st, h_out, H, w, bias, conf);
+    return launch_pdl(confidence_kernel, dim3(M), dim3(512), 0, st, h_out, H, w, bias, conf);
 }
 
 }  // namespace ds

@@ -24,6 +24,8 @@
 // resident) and synchronise through a bounded grid barrier in the workspace.
 #include "internal.h"
 
+#include <algorithm>
+
 namespace ds {
 
 constexpr int kSampThreads = 512;
@@ -391,93 +393,194 @@ DS_DEVINL uint64_t policy_evict_last() {
     return pol;
 }
 
-// w2 streaming ring: the CTA's slice of every w2 row (its vocabulary pairs
-// [lo, hi), whole 16-byte quads) is copied in chunks of kRollKC rows into
-// kRollStages shared-memory stages by all threads with 16-byte cp.async (L2
-// evict-last: w2 is re-read every step). w2 does not depend on the drafted
-// tokens, so the ring runs ahead of the compute across steps and barriers.
+// w2 storage of the rollout. The CTA owns the vocabulary pairs [lo, hi) (whole
+// 16-byte quads); thread t owns pair lo + t ("primary") and, when the slice is
+// wider than the CTA, pair lo + t + blockDim ("secondary").
+//  - Rows [0, Kt) of the primary pairs live in tensor memory for the whole
+//    kernel (Kt = min(r, 128): 128 columns per thread, all 512 columns of the
+//    SM), rows [0, Kt) of the secondary pairs in shared memory; both are read
+//    from global memory once at kernel start.
+//  - Rows [Kt, r) stream every pass through a ring of kRollStages shared-memory
+//    stages of kRollKC rows, filled by 2D tensor copies issued by thread 0
+//    (L2 evict-last: w2 is re-read every step) and completing on "full"
+//    mbarriers; every warp releases a stage on its "empty" mbarrier. w2 does
+//    not depend on the drafted tokens, so the ring runs ahead of the compute
+//    across steps and grid barriers.
+// The tensor-memory part is used when the secondary pairs fit kRollSec slots.
 constexpr int kRollKC = 16;
-constexpr int kRollStages = 5;
+constexpr int kRollStages = 4;
+constexpr int kRollTmemRows = 128;
+constexpr int kRollSec = 32;
+constexpr int kRollWarps = kSampThreads / 32;
 
+// A stage holds nbox tensor boxes of kRollKC rows x box_w pairs (w2 seen as a
+// uint32 matrix [r, V / 2]); the CTA's slice starts at pair lo of every box row.
 struct RollRing {
-    uint8_t *stage;          // [kRollStages][kRollKC][slice_bytes]
-    uint32_t slice_bytes;    // (hi - lo) * 4
-    int nchunks;             // chunks per pass over w2
-    long long issued, consumed, total;
+    uint8_t *stage;           // [kRollStages][nbox][kRollKC][box_w] uint32
+    uint64_t *full, *empty;   // [kRollStages] each
+    int box_w, nbox;          // pairs per box row, boxes per stage
+    uint32_t stage_bytes;
+    int kt;                   // rows held on chip (tensor memory / secondary smem)
+    int nchunks;              // streamed chunks per pass over w2 (rows kt .. r-1)
+    long long issued;         // chunks issued (thread 0's count)
+    long long consumed;       // chunks read by this thread
+    long long total;
 };
 
-DS_DEVINL void cp_async16_keep(void *dst, const void *src, uint64_t pol) {
-    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
-                 "l"(pol)
-                 : "memory");
-}
-DS_DEVINL void cp_async_commit_group() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-DS_DEVINL void cp_async_wait_group() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+// Box width and count of the w2 tiles of a rollout over V with grid CTAs: the
+// largest slice (pairs) in as few boxes of <= 256 pairs as possible, the width
+// a multiple of 4 pairs (16 bytes).
+__host__ __device__ void rollout_box(int V, int grid, int *box_w, int *nbox) {
+    const int nq = V / 8;
+    const int max_pairs = 4 * ((nq + grid - 1) / grid);
+    const int n = (max_pairs + 255) / 256;
+    *nbox = n < 1 ? 1 : n;
+    *box_w = ((max_pairs + *nbox - 1) / *nbox + 3) / 4 * 4;
+    if (*box_w < 4) *box_w = 4;
 }
 
-// All threads: copy chunk number ring.issued into its stage (one commit group
-// per chunk per thread, empty when past the end).
-DS_DEVINL void ring_issue(RollRing &rg, const RolloutParams &p, int lo, uint64_t pol) {
-    if (rg.issued < rg.total) {
-        const long long c = rg.issued;
-        const int s = (int)(c % kRollStages);
-        const int k0 = (int)(c % rg.nchunks) * kRollKC;
-        const int rows = min(kRollKC, p.r - k0);
-        const int quads = (int)(rg.slice_bytes / 16);
-        const uint8_t *src = (const uint8_t *)p.w2 + ((size_t)k0 * p.V + 2 * (size_t)lo) * 2;
-        uint8_t *dst = rg.stage + (size_t)s * kRollKC * rg.slice_bytes;
-        for (int seg = threadIdx.x; seg < rows * quads; seg += blockDim.x) {
-            const int kk = seg / quads, q = seg - kk * quads;
-            cp_async16_keep(dst + (size_t)kk * rg.slice_bytes + 16 * q, src + (size_t)kk * p.V * 2 + 16 * q, pol);
+// Thread 0: issue the next chunk into its stage once every warp has released
+// the stage's previous chunk. False on a timeout or an abort.
+DS_DEVINL bool ring_issue(RollRing &rg, const CUtensorMap *tm, int lo, uint64_t pol, volatile int *abort) {
+    if (rg.issued >= rg.total) return true;
+    const long long c = rg.issued;
+    const int s = (int)(c % kRollStages);
+    if (c >= kRollStages &&
+        !mbar_wait_bounded(&rg.empty[s], (uint32_t)((c / kRollStages - 1) & 1), abort))
+        return false;
+    const int k0 = rg.kt + (int)(c % rg.nchunks) * kRollKC;
+    mbar_arrive_expect_tx(&rg.full[s], rg.stage_bytes);
+    uint8_t *dst = rg.stage + (size_t)s * rg.stage_bytes;
+    for (int j = 0; j < rg.nbox; ++j)
+        tma_load_2d_hint(dst + (size_t)j * kRollKC * rg.box_w * 4, tm, lo + j * rg.box_w, k0, &rg.full[s], pol);
+    rg.issued = c + 1;
+    return true;
+}
+
+// Every chunk issued lands before the kernel exits (bounded waits).
+DS_DEVINL void ring_drain(RollRing &rg) {
+    if (threadIdx.x != 0) return;
+    for (long long c = rg.consumed; c < rg.issued; ++c)
+        mbar_drain(&rg.full[c % kRollStages], (uint32_t)((c / kRollStages) & 1));
+}
+
+// Packed fp32 pairs: two independent IEEE fp32 FMAs (round to nearest) per
+// instruction, each lane bit-identical to fmaf.
+DS_DEVINL uint64_t pack_f2(uint32_t lo_bits, uint32_t hi_bits) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo_bits), "r"(hi_bits));
+    return r;
+}
+DS_DEVINL void unpack_f2(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+DS_DEVINL void fma_f2(uint64_t &acc, uint64_t a, uint64_t b) {
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
+}
+
+// One chunk of the chains: for every row the bf16 pair of w2 is widened to two
+// fp32 values and each of the NB sequences takes one packed FMA (k in order).
+template <int NB, bool TWO>
+DS_DEVINL void roll_chunk(const uint32_t *w, int wpr, int rows, int k0, int o0, int o1, bool has0, bool has1,
+                          const uint64_t (*s_u)[256], uint64_t (&a0)[NB], uint64_t (&a1)[NB]) {
+#pragma unroll 4
+    for (int kk = 0; kk < rows; ++kk) {
+        const uint32_t w0 = has0 ? w[kk * wpr + o0] : 0u;
+        const uint64_t xy0 = pack_f2(w0 << 16, w0 & 0xFFFF0000u);
+        uint64_t xy1 = 0;
+        if (TWO) {
+            const uint32_t w1v = has1 ? w[kk * wpr + o1] : 0u;
+            xy1 = pack_f2(w1v << 16, w1v & 0xFFFF0000u);
+        }
+#pragma unroll
+        for (int bb = 0; bb < NB; ++bb) {
+            const uint64_t uu = s_u[bb][k0 + kk];
+            fma_f2(a0[bb], uu, xy0);
+            if (TWO) fma_f2(a1[bb], uu, xy1);
         }
     }
-    cp_async_commit_group();
-    rg.issued++;
 }
 
 // ell_i for NB sequences over this CTA's pairs (thread t owns pairs lo + t and
 // lo + t + blockDim): w2 comes from the ring; the chain over k stays in order.
 // Each CTA max-reduces its greedy keys (or its maxima of ell / T) into amax[b].
+// A failed wait sets *s_fail; every thread still reaches the block reduction.
+// Rows [0, kt) of the chains from tensor memory (primary pairs: this thread's
+// lane and columns) and the secondary rows in shared memory. Warp-collective.
+template <int NB, bool TWO>
+DS_DEVINL void roll_tmem_rows(uint32_t taddr, int kt, const uint32_t (*s_sec)[kRollSec], int t, bool has1,
+                              const uint64_t (*s_u)[256], uint64_t (&a0)[NB], uint64_t (&a1)[NB]) {
+    for (int k16 = 0; k16 < kt; k16 += 16) {
+        uint32_t v[16];
+        tmem_ld16u(taddr + (uint32_t)k16, v);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const int k = k16 + j;
+            if (k < kt) {
+                const uint64_t xy0 = pack_f2(v[j] << 16, v[j] & 0xFFFF0000u);
+                uint64_t xy1 = 0;
+                if (TWO) {
+                    const uint32_t w1v = has1 ? s_sec[k][t] : 0u;
+                    xy1 = pack_f2(w1v << 16, w1v & 0xFFFF0000u);
+                }
+#pragma unroll
+                for (int bb = 0; bb < NB; ++bb) {
+                    const uint64_t uu = s_u[bb][k];
+                    fma_f2(a0[bb], uu, xy0);
+                    if (TWO) fma_f2(a1[bb], uu, xy1);
+                }
+            }
+        }
+    }
+}
+
 template <int NB>
-__device__ bool rollout_logits(const RolloutParams &p, int i, int b0, int nb, int lo, int hi, RollRing &rg,
-                               const float (*s_w1)[256], unsigned long long *amax, unsigned long long *red,
-                               uint64_t pol) {
+__device__ void rollout_logits(const RolloutParams &p, const CUtensorMap *tm, int i, int b0, int nb, int lo, int hi,
+                               RollRing &rg, uint32_t taddr, const uint32_t (*s_sec)[kRollSec],
+                               const uint64_t (*s_u)[256], unsigned long long *amax, unsigned long long *red,
+                               uint64_t pol, volatile int *s_fail) {
     const int V = p.V, r = p.r;
-    float a[2][NB][2];
+    uint64_t a0[NB], a1[NB];
 #pragma unroll
-    for (int j = 0; j < 2; ++j)
-#pragma unroll
-        for (int bb = 0; bb < NB; ++bb) a[j][bb][0] = a[j][bb][1] = 0.f;
+    for (int bb = 0; bb < NB; ++bb) a0[bb] = a1[bb] = 0ull;
     const int q0 = threadIdx.x, q1 = threadIdx.x + blockDim.x;
     const bool has0 = lo + q0 < hi, has1 = lo + q1 < hi;
+    const bool two = __any_sync(0xffffffffu, has1);  // warp-uniform
+    const int lane = threadIdx.x & 31;
+    // word offsets of the thread's pairs in a stage (row 0)
+    const int o0 = (q0 / rg.box_w) * kRollKC * rg.box_w + q0 % rg.box_w;
+    const int o1 = (q1 / rg.box_w) * kRollKC * rg.box_w + q1 % rg.box_w;
+    if (rg.kt > 0) {
+        if (two)
+            roll_tmem_rows<NB, true>(taddr, rg.kt, s_sec, threadIdx.x, has1, s_u, a0, a1);
+        else
+            roll_tmem_rows<NB, false>(taddr, rg.kt, s_sec, threadIdx.x, has1, s_u, a0, a1);
+    }
+    bool failed = false;
     for (int ch = 0; ch < rg.nchunks; ++ch) {
         const long long c = rg.consumed;
         const int s = (int)(c % kRollStages);
-        cp_async_wait_group<kRollStages - 2>();  // this thread's copies of chunk c have landed
-        __syncthreads();                          // ... and everyone's; stage of chunk c-1 is free
-        ring_issue(rg, p, lo, pol);
-        const uint32_t *w = (const uint32_t *)(rg.stage + (size_t)s * kRollKC * rg.slice_bytes);
-        const int k0 = ch * kRollKC, rows = min(kRollKC, r - k0);
-        const int wpr = rg.slice_bytes / 4;  // words (pairs) per row
-#pragma unroll 4
-        for (int kk = 0; kk < rows; ++kk) {
-            const uint32_t w0 = has0 ? w[kk * wpr + q0] : 0u, w1v = has1 ? w[kk * wpr + q1] : 0u;
-            const float x0 = __uint_as_float(w0 << 16), y0 = __uint_as_float(w0 & 0xFFFF0000u);
-            const float x1 = __uint_as_float(w1v << 16), y1 = __uint_as_float(w1v & 0xFFFF0000u);
-#pragma unroll
-            for (int bb = 0; bb < NB; ++bb) {
-                const float u = s_w1[bb][k0 + kk];
-                a[0][bb][0] = __fmaf_rn(u, x0, a[0][bb][0]);
-                a[0][bb][1] = __fmaf_rn(u, y0, a[0][bb][1]);
-                a[1][bb][0] = __fmaf_rn(u, x1, a[1][bb][0]);
-                a[1][bb][1] = __fmaf_rn(u, y1, a[1][bb][1]);
-            }
+        if (!failed && threadIdx.x == 0 && !ring_issue(rg, tm, lo, pol, s_fail)) {
+            set_error(p.err, DSPARK_ERR_TIMEOUT);
+            *s_fail = 1;
         }
-        rg.consumed = c + 1;
+        if (!failed && !mbar_wait_bounded(&rg.full[s], (uint32_t)((c / kRollStages) & 1), s_fail)) {
+            set_error(p.err, DSPARK_ERR_TIMEOUT);
+            failed = true;
+        }
+        if (!failed) {
+            const uint32_t *w = (const uint32_t *)(rg.stage + (size_t)s * rg.stage_bytes);
+            const int k0 = rg.kt + ch * kRollKC, rows = min(kRollKC, r - k0);
+            if (two)
+                roll_chunk<NB, true>(w, rg.box_w, rows, k0, o0, o1, has0, has1, s_u, a0, a1);
+            else
+                roll_chunk<NB, false>(w, rg.box_w, rows, k0, o0, o1, has0, has1, s_u, a0, a1);
+            rg.consumed = c + 1;
+        }
+        __syncwarp();
+        if (lane == 0 && !failed) mbar_arrive(&rg.empty[s]);
     }
-    __syncthreads();
+    if (failed) *s_fail = 1;
     unsigned long long best[NB];
 #pragma unroll
     for (int bb = 0; bb < NB; ++bb) best[bb] = 0;
@@ -490,9 +593,11 @@ __device__ bool rollout_logits(const RolloutParams &p, int i, int b0, int nb, in
         for (int bb = 0; bb < NB; ++bb) {
             if (bb < nb) {
                 const int b = b0 + bb;
+                float d0, d1;
+                unpack_f2(j ? a1[bb] : a0[bb], d0, d1);
                 const size_t off = ((size_t)b * p.B + i) * V + 2 * pp;
                 const float2 z = *(const float2 *)(p.z + off);
-                const float l0 = __fadd_rn(z.x, a[j][bb][0]), l1 = __fadd_rn(z.y, a[j][bb][1]);
+                const float l0 = __fadd_rn(z.x, d0), l1 = __fadd_rn(z.y, d1);
                 *(float2 *)(p.ell + off) = make_float2(l0, l1);
                 if (!isfinite(l0) || !isfinite(l1)) bad = true;
                 unsigned long long k0, k1;
@@ -515,7 +620,6 @@ __device__ bool rollout_logits(const RolloutParams &p, int i, int b0, int nb, in
             if (threadIdx.x == 0) atomicMax(&amax[b0 + bb], m);
         }
     }
-    return true;
 }
 
 // Vocabulary pairs of this CTA for the rollout: quads of 4 pairs (16 bytes of
@@ -526,17 +630,19 @@ DS_DEVINL void quad_slice(int V, int &lo, int &hi) {
     hi = 4 * (int)((long long)(blockIdx.x + 1) * nq / gridDim.x);
 }
 
-// Every copy the ring still has in flight lands before the kernel exits.
-DS_DEVINL void ring_drain() { cp_async_wait_group<0>(); }
-
-__global__ void __launch_bounds__(kSampThreads, 1) rollout_kernel(RolloutParams p) {
+__global__ void __launch_bounds__(kSampThreads, 1)
+    rollout_kernel(const __grid_constant__ CUtensorMap tmW2, RolloutParams p) {
     __shared__ NucleusSmem sm;
     __shared__ DrawSmem dsm;
-    __shared__ float s_w1[kRollChunk][256];
+    __shared__ __align__(16) uint64_t s_u[kRollChunk][256];  // (u, u) fp32 pairs of w1[t_{i-1}]
+    __shared__ __align__(8) uint64_t s_full[kRollStages], s_empty[kRollStages];
     __shared__ int s_prev[kMaxSampBs];
     __shared__ volatile int s_fail;
     __shared__ const float *s_rows[kRowsPerGroup];
+    __shared__ uint32_t s_tmem_base;
+    __shared__ uint32_t s_sec[kRollTmemRows][kRollSec];  // secondary pairs, rows [0, kt)
     extern __shared__ __align__(128) uint8_t ring_smem[];
+    static_assert(kSampThreads == 512, "tensor-memory layout: 4 warps per lane quadrant, 128 columns each");
     const RollLayout L(p.bs, p.B, gridDim.x);
     unsigned long long *sc = p.scratch;
     const int V = p.V, r = p.r;
@@ -544,14 +650,55 @@ __global__ void __launch_bounds__(kSampThreads, 1) rollout_kernel(RolloutParams 
     quad_slice(V, lo, hi);
     RollRing rg;
     rg.stage = ring_smem;
-    rg.slice_bytes = (uint32_t)(hi - lo) * 4u;
-    rg.nchunks = (r + kRollKC - 1) / kRollKC;
+    rg.full = s_full;
+    rg.empty = s_empty;
+    rollout_box(V, gridDim.x, &rg.box_w, &rg.nbox);
+    rg.stage_bytes = (uint32_t)(rg.nbox * kRollKC * rg.box_w * 4);
+    // on-chip rows when every CTA's secondary pairs fit the kRollSec slots
+    const int max_pairs = 4 * ((V / 8 + (int)gridDim.x - 1) / (int)gridDim.x);
+    rg.kt = (max_pairs <= kSampThreads + kRollSec) ? min(r, kRollTmemRows) : 0;
+    rg.nchunks = (r - rg.kt + kRollKC - 1) / kRollKC;
     rg.issued = rg.consumed = 0;
     rg.total = (long long)p.B * ((p.bs + kRollChunk - 1) / kRollChunk) * rg.nchunks;
     const uint64_t pol = policy_evict_last();
-    if (threadIdx.x == 0) s_fail = 0;
     if (hi <= lo) rg.total = 0;
-    for (int st = 0; st < kRollStages - 1; ++st) ring_issue(rg, p, lo, pol);
+    if (threadIdx.x == 0) {
+        s_fail = 0;
+        for (int st = 0; st < kRollStages; ++st) {
+            mbar_init(&s_full[st], 1);
+            mbar_init(&s_empty[st], kRollWarps);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        tma_prefetch_desc(&tmW2);
+        for (int st = 0; st < kRollStages - 1; ++st) ring_issue(rg, &tmW2, lo, pol, &s_fail);
+    }
+    // rows [0, kt) of w2 into tensor memory (primary pairs) and shared memory (secondary)
+    const int warp = threadIdx.x >> 5;
+    if (rg.kt > 0 && warp == 0) tmem_alloc(&s_tmem_base, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t taddr = s_tmem_base + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(128 * (warp >> 2));
+    if (rg.kt > 0) {
+        const uint32_t *w2w = (const uint32_t *)p.w2;
+        const size_t rowp = (size_t)V / 2;
+        const bool has0 = lo + (int)threadIdx.x < hi;
+        for (int k32 = 0; k32 < rg.kt; k32 += 32) {
+            uint32_t v[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                v[j] = (has0 && k32 + j < rg.kt) ? __ldg(w2w + (size_t)(k32 + j) * rowp + lo + threadIdx.x) : 0u;
+            tmem_st32(taddr + (uint32_t)k32, v);
+        }
+        tmem_st_wait();
+        if (threadIdx.x < kRollSec) {
+            const int q1 = lo + (int)threadIdx.x + (int)blockDim.x;
+            for (int k = 0; k < rg.kt; ++k) s_sec[k][threadIdx.x] = q1 < hi ? __ldg(w2w + (size_t)k * rowp + q1) : 0u;
+        }
+    }
     for (size_t w = (size_t)blockIdx.x * blockDim.x + threadIdx.x; w < L.total; w += (size_t)gridDim.x * blockDim.x)
         sc[w] = 0;
     for (int b = threadIdx.x; b < p.bs; b += blockDim.x) {
@@ -571,18 +718,20 @@ __global__ void __launch_bounds__(kSampThreads, 1) rollout_kernel(RolloutParams 
             const int nb = min(kRollChunk, p.bs - b0);
             for (int idx = threadIdx.x; idx < kRollChunk * r; idx += blockDim.x) {
                 const int bb = idx / r, k = idx % r;
-                s_w1[bb][k] = bb < nb ? __bfloat162float(p.w1[(size_t)s_prev[b0 + bb] * r + k]) : 0.f;
+                const float u = bb < nb ? __bfloat162float(p.w1[(size_t)s_prev[b0 + bb] * r + k]) : 0.f;
+                s_u[bb][k] = pack_f2(__float_as_uint(u), __float_as_uint(u));
             }
             __syncthreads();
             if (hi > lo) {
                 if (nb == 1)
-                    ok = rollout_logits<1>(p, i, b0, 1, lo, hi, rg, s_w1, sc + L.amax + (size_t)i * p.bs, sm.red,
-                                           pol);
+                    rollout_logits<1>(p, &tmW2, i, b0, 1, lo, hi, rg, taddr, s_sec, s_u,
+                                      sc + L.amax + (size_t)i * p.bs, sm.red, pol, &s_fail);
                 else
-                    ok = rollout_logits<kRollChunk>(p, i, b0, nb, lo, hi, rg, s_w1, sc + L.amax + (size_t)i * p.bs,
-                                                    sm.red, pol);
+                    rollout_logits<kRollChunk>(p, &tmW2, i, b0, nb, lo, hi, rg, taddr, s_sec, s_u,
+                                               sc + L.amax + (size_t)i * p.bs, sm.red, pol, &s_fail);
             }
             __syncthreads();
+            ok = !s_fail;
         }
         if (!ok || !grid_barrier(p.ctl, &s_fail, p.err)) {
             ok = false;
@@ -639,7 +788,13 @@ __global__ void __launch_bounds__(kSampThreads, 1) rollout_kernel(RolloutParams 
         }
         __syncthreads();
     }
-    ring_drain();
+    ring_drain(rg);
+    tc_fence_before();
+    __syncthreads();
+    if (rg.kt > 0 && warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(s_tmem_base, 512);
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -659,10 +814,22 @@ __global__ void verify_argmax_kernel(const float *__restrict__ P, int rows, int 
     unsigned long long best = 0;
     bool bad = false;
     const float *pr = P + (size_t)row * V;
-    for (int pp = lo + threadIdx.x; pp < hi; pp += blockDim.x) {
-        const float2 l = *(const float2 *)(pr + 2 * pp);
-        if (!isfinite(l.x) || !isfinite(l.y)) bad = true;
-        best = max(best, max(argmax_key(l.x, 2 * pp), argmax_key(l.y, 2 * pp + 1)));
+    // four independent pair loads in flight per thread
+    for (int pp0 = lo + threadIdx.x; pp0 < hi; pp0 += 4 * blockDim.x) {
+        float2 l[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int pp = pp0 + u * blockDim.x;
+            l[u] = pp < hi ? __ldcs((const float2 *)(pr + 2 * pp)) : make_float2(0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int pp = pp0 + u * blockDim.x;
+            if (pp < hi) {
+                if (!isfinite(l[u].x) || !isfinite(l[u].y)) bad = true;
+                best = max(best, max(argmax_key(l[u].x, 2 * pp), argmax_key(l[u].y, 2 * pp + 1)));
+            }
+        }
     }
     if (bad) set_error(err, DSPARK_ERR_BAD_INPUT);
     best = block_max_u64(best, red);
@@ -842,9 +1009,9 @@ __global__ void __launch_bounds__(kSampThreads, 1) verify_prob_kernel(VerifyPara
 // ---------------------------------------------------------------------------
 // Dynamic shared memory of the rollout's w2 ring for a vocabulary and grid.
 size_t rollout_ring_bytes(int V, int grid) {
-    const int nq = V / 8;
-    const int max_quads = (nq + grid - 1) / grid + 1;
-    return (size_t)kRollStages * kRollKC * max_quads * 16;
+    int box_w, nbox;
+    rollout_box(V, grid, &box_w, &nbox);
+    return (size_t)kRollStages * nbox * kRollKC * box_w * 4;
 }
 
 int sampling_max_grid(int num_sms, int V) {
@@ -860,8 +1027,9 @@ int sampling_max_grid(int num_sms, int V) {
     return (a >= 1 && b >= 1) ? num_sms : 0;
 }
 
-cudaError_t launch_rollout(RolloutParams p, int grid, cudaStream_t st) {
-    void *args[] = {&p};
+cudaError_t launch_rollout(const CUtensorMap &w2_map, RolloutParams p, int grid, cudaStream_t st) {
+    CUtensorMap tm = w2_map;
+    void *args[] = {&tm, &p};
     return cudaLaunchCooperativeKernel((void *)rollout_kernel, dim3(grid), dim3(kSampThreads), args,
                                        rollout_ring_bytes(p.V, grid), st);
 }
@@ -869,8 +1037,10 @@ cudaError_t launch_rollout(RolloutParams p, int grid, cudaStream_t st) {
 cudaError_t launch_verify(VerifyParams p, int grid, cudaStream_t st) {
     if (p.verify_mode == DSPARK_GREEDY) {
         const int rows = p.bs * (p.B + 1);
-        cudaError_t e = launch_pdl(verify_argmax_kernel, dim3(8, rows), dim3(256), 0, st, p.P, rows, p.V, p.scratch,
-                                   p.err);
+        // about two CTAs per SM over all rows
+        const int slices = std::max(1, std::min(64, (2 * grid + rows - 1) / rows));
+        cudaError_t e = launch_pdl(verify_argmax_kernel, dim3(slices, rows), dim3(256), 0, st, p.P, rows, p.V,
+                                   p.scratch, p.err);
         if (e != cudaSuccess) return e;
         return launch_pdl(verify_greedy_finalize, dim3((p.bs + 127) / 128), dim3(128), 0, st, p.tokens, p.bs, p.B, p.V,
                           p.scratch, p.accept_len, p.out_tokens, p.err);
