@@ -116,6 +116,7 @@ size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
 struct Layout {
     size_t partials, hn, qkv, cq, q, qt, blk, olat, part_o, part_ml, ov, act, hout, scratch, total;
     int splits, tok_per_split;
+    int tc, cps;                 // tensor-core attention and its chunks per split
 };
 
 }  // namespace
@@ -138,6 +139,10 @@ struct dspark_handle {
     const void *c_ws = nullptr;
     int c_bs = -1;
     CUtensorMap b_hn, b_cq, b_ov, b_act, b_hout;
+    CUtensorMap b_blk;                       // block latents, tensor-core attention
+    const void *c_pool[DSPARK_MAX_LAYERS] = {};
+    int c_npages[DSPARK_MAX_LAYERS] = {};
+    CUtensorMap pool_map[DSPARK_MAX_LAYERS]; // per-layer page pools, tensor-core attention
     const void *c_aux = nullptr;
     int c_aux_bs = -1;
     CUtensorMap b_aux;
@@ -168,7 +173,11 @@ Layout layout_for(const dspark_handle *h, int bs, int max_ctx) {
     const size_t M = (size_t)g.block * bs;
     const size_t kvd = g.kv_lora + g.d_rope;
     const size_t R = (size_t)g.block * g.n_heads;
-    L.splits = attn_splits(h, bs, max_ctx, &L.tok_per_split);
+    L.tc = attention_tc_supported((int)kvd, g.kv_lora) ? 1 : 0;
+    L.cps = 0;
+    L.tok_per_split = 0;
+    L.splits = L.tc ? attention_tc_splits((int)R, g.kv_lora, bs, max_ctx, h->num_sms, &L.cps)
+                    : attn_splits(h, bs, max_ctx, &L.tok_per_split);
     size_t off = kCtlBytes;
     auto take = [&](size_t bytes) {
         const size_t o = off;
@@ -540,7 +549,8 @@ dspark_status dspark_draft_block(dspark_handle_t *h, float *x, const dspark_kv_t
         const uint32_t bn = bn_for(M);
         if (!make_map(&h->b_hn, hn, M, g.hidden, bn) || !make_map(&h->b_cq, cq, M, g.q_lora, bn) ||
             !make_map(&h->b_ov, ov, M, (uint64_t)g.n_heads * g.d_v, bn) ||
-            !make_map(&h->b_act, act, M, g.inter, bn) || !make_map(&h->b_hout, hout, M, g.hidden, bn))
+            !make_map(&h->b_act, act, M, g.inter, bn) || !make_map(&h->b_hout, hout, M, g.hidden, bn) ||
+            (L.tc && !make_map(&h->b_blk, blk, M, kvd, 64)))
             return DSPARK_ERR_CUDA;
         h->c_ws = ws;
         h->c_bs = bs;
@@ -583,7 +593,17 @@ dspark_status dspark_draft_block(dspark_handle_t *h, float *x, const dspark_kv_t
         RUN(launch_q_absorb(q, M, g.n_heads, g.d_nope, g.d_rope, g.kv_lora, g.d_v, (const __nv_bfloat16 *)W.w_kv_b,
                             kv->ctx_len, g.block, kv->max_ctx, h->rope, qt, s));
         ap.pool = (const __nv_bfloat16 *)kv->pools[l];
-        RUN(launch_attention(ap, bs, kvd, g.kv_lora, s));
+        if (L.tc) {
+            if (h->c_pool[l] != kv->pools[l] || h->c_npages[l] != kv->n_pages) {
+                if (!make_map(&h->pool_map[l], kv->pools[l], (uint64_t)kv->n_pages * g.page_size, kvd, 64))
+                    return DSPARK_ERR_CUDA;
+                h->c_pool[l] = kv->pools[l];
+                h->c_npages[l] = kv->n_pages;
+            }
+            RUN(launch_attention_tc(h->pool_map[l], h->b_blk, ap, L.cps, bs, kvd, g.kv_lora, s));
+        } else {
+            RUN(launch_attention(ap, bs, kvd, g.kv_lora, s));
+        }
         RUN(launch_v_absorb(olat, M, g.n_heads, g.d_nope, g.d_v, g.kv_lora, (const __nv_bfloat16 *)W.w_kv_b, ov, s));
         RUN(quant ? gemm_q(h, h->qo[l], nullptr, h->b_ov, g.hidden, g.n_heads * g.d_v, M, EPI_ADD, x, nullptr, g.hidden,
                            ws, s)

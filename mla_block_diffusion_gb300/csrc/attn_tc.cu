@@ -1,0 +1,456 @@
+// MLA attention of the draft block on the 5th-generation tensor core.
+//
+// Every query row of a sequence (block tokens x heads) attends to the same
+// latent keys K_j = [c_kv,j || k_r,j] and values V_j = c_kv,j: the cache tokens
+// 0..ctx-1 from the paged latent pool plus the block's own latents, with no
+// mask (non-causal block) ("Kimi-K3-DSpark-NVFP4", Model Overview; the MLA
+// absorbed form, "kimi-k3-dspark-gguf", Runtime status).
+//
+// A CTA owns 128 query rows, one range of 64-token chunks of the KV sequence
+// (a split) and one 128-column part of the latent output (4 CTAs share a row
+// tile and recompute its scores: the tensor core has the headroom, tensor
+// memory does not). Tensor memory (all 512 columns):
+//   [0, DQK/2)       Q tile, bf16 pairs (A operand of S = Q K^T)
+//   64 columns       S, fp32 (128 rows x 64 keys)
+//   32 columns       P = exp2(S - m), bf16 pairs (A operand of O += P V)
+//   DVP columns      O, fp32 (128 rows x the CTA's output columns)
+// A chunk is one page of the pool (64 rows of DQK bf16), brought by TMA as
+// DQK/64 boxes of 64 x 64 in the 128-byte swizzle: K-major for S, and the same
+// bytes read MN-major give V for O. The softmax keeps a per-row reference max
+// and rescales O only when a new maximum exceeds it by more than 2^8 (the
+// result is the same: O and the row sum carry the same reference).
+//
+// Roles (6 warps): warp 0 TMA producer; warp 1 MMA issuer and tensor-memory
+// owner; warps 2-5 load Q, run the softmax (one thread per row) and write the
+// split partial. All waits are bounded; a timeout raises DSPARK_ERR_TIMEOUT.
+#include "internal.h"
+
+namespace ds {
+
+constexpr int kTcRows = 128;     // query rows per CTA (tcgen05 M)
+constexpr int kTcKeys = 64;      // keys per chunk (one page)
+constexpr int kTcStages = 3;     // KV chunk stages in shared memory
+constexpr float kTcRescaleLog2 = 8.f;
+
+template <int DQK, int DV>
+struct TcCfg {
+    static constexpr int kBoxes = (DQK + 63) / 64;         // 64-column boxes per key row
+    static constexpr int kDQKP = kBoxes * 64;              // padded score width
+    static constexpr int kDVP = DV < 128 ? DV : 128;       // output columns per CTA
+    static constexpr int kParts = DV / kDVP;
+    static constexpr int kBoxBytes = kTcKeys * 128;        // 64 rows x 128 B
+    static constexpr int kTileBytes = kBoxes * kBoxBytes;
+    static constexpr int kQCol = 0;
+    static constexpr int kSCol = kDQKP / 2;
+    static constexpr int kPCol = kSCol + 64;
+    static constexpr int kOCol = kPCol + 32;
+    static constexpr int kSmem = 1024 + kTcStages * kTileBytes + 256;
+    static_assert(kOCol + kDVP <= 512, "tensor memory");
+    static_assert(DV % kDVP == 0 && kDVP % 64 == 0, "output part: whole 64-column atoms");
+    static_assert(kSmem <= 232448, "shared memory");
+};
+
+bool attention_tc_supported(int dqk, int dv) { return dqk == 576 && dv == 512; }
+
+struct TcAttnParams {
+    const __nv_bfloat16 *qt;      // [bs, R, DQK]
+    int R;                        // rows per sequence
+    int n_pages;
+    const int32_t *page_table;    // [bs, max_pages]
+    int max_pages;
+    const int32_t *ctx_len;       // [bs]
+    int max_ctx;
+    int block;                    // the block's own latents: rows b * block .. of blk_kv
+    int splits, cps;              // splits and chunks per split (chunk index space: ctx pages, then the block)
+    float scale_log2;
+    float *o_lat;                 // [bs, R, DV] (splits == 1)
+    float *part_o;                // [bs, splits, R, DV]
+    float *part_ml;               // [bs, splits, R, 2]
+    int *err;
+};
+
+DS_DEVINL void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+        "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
+
+// 16 columns of the warp's lane quadrant without the completion wait (several
+// loads share one tcgen05.wait::ld).
+DS_DEVINL void tmem_ld16_nw(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+DS_DEVINL void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+DS_DEVINL uint32_t pack_bf16x2(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+// Warp-uniform bounded wait (every lane takes the same branch after it).
+DS_DEVINL bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
+    return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, abort));
+}
+
+template <int DQK, int DV>
+__global__ void __launch_bounds__(192, 1)
+    mla_attention_tc_kernel(const __grid_constant__ CUtensorMap tmPool, const __grid_constant__ CUtensorMap tmBlk,
+                            const TcAttnParams p) {
+    using C = TcCfg<DQK, DV>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t *sKV = smem;
+    uint64_t *bars = (uint64_t *)(smem + kTcStages * C::kTileBytes);
+    uint64_t *kv_full = bars, *kv_empty = bars + kTcStages;
+    uint64_t *s_full = bars + 2 * kTcStages, *s_free = s_full + 1, *p_ready = s_full + 2, *pv_done = s_full + 3;
+    uint64_t *q_ready = s_full + 4, *mma_done = s_full + 5;
+    __shared__ uint32_t s_tmem;
+    __shared__ volatile int s_abort;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tile = blockIdx.x / C::kParts, part = blockIdx.x % C::kParts;
+    const int split = blockIdx.y, b = blockIdx.z;
+    const int r0 = tile * kTcRows;
+
+    pdl_trigger();
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kTcStages; ++i) {
+            mbar_init(&kv_full[i], 1);
+            mbar_init(&kv_empty[i], 1);
+        }
+        mbar_init(s_full, 1);
+        mbar_init(s_free, 4);
+        mbar_init(p_ready, 4);
+        mbar_init(pv_done, 1);
+        mbar_init(q_ready, 4);
+        mbar_init(mma_done, 1);
+        s_abort = 0;
+        fence_mbar_init();
+    }
+    if (threadIdx.x == 32) {
+        tma_prefetch_desc(&tmPool);
+        tma_prefetch_desc(&tmBlk);
+    }
+    if (warp == 1) tmem_alloc(&s_tmem, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+
+    // ctx_len, the page table and the page pool are inputs of the step: read
+    // before the dependency wait (the queries and the block latents are not)
+    int ctx = p.ctx_len[b];
+    if (ctx < 0 || ctx > p.max_ctx) {
+        if (threadIdx.x == 0) set_error(p.err, DSPARK_ERR_OOB);
+        ctx = 0;
+    }
+    const int npages = (ctx + kTcKeys - 1) / kTcKeys;  // chunks [0, npages): pages; chunk npages: the block
+    const int c_begin = split * p.cps;
+    const int c_end = min(npages + 1, c_begin + p.cps);
+    const int nch = c_end > c_begin ? c_end - c_begin : 0;
+    int issued = 0;
+
+    if (warp != 0 || lane != 0) pdl_wait();
+    if (warp == 0) {
+        if (lane == 0) {
+            bool waited = false;
+            for (int i = 0; i < nch; ++i) {
+                const int st = i % kTcStages;
+                if (!waited && (i >= kTcStages || c_begin + i >= npages)) {
+                    pdl_wait();
+                    waited = true;
+                }
+                if (i >= kTcStages &&
+                    !mbar_wait_bounded(&kv_empty[st], (uint32_t)((i / kTcStages - 1) & 1), &s_abort))
+                    break;
+                const int c = c_begin + i;
+                mbar_arrive_expect_tx(&kv_full[st], (uint32_t)C::kTileBytes);
+                uint8_t *dst = sKV + st * C::kTileBytes;
+                if (c < npages) {
+                    int pg = p.page_table[(size_t)b * p.max_pages + c];
+                    if (pg < 0 || pg >= p.n_pages) {
+                        set_error(p.err, DSPARK_ERR_OOB);
+                        pg = 0;
+                    }
+#pragma unroll 1
+                    for (int j = 0; j < C::kBoxes; ++j)
+                        tma_load_2d(dst + j * C::kBoxBytes, &tmPool, j * 64, pg * kTcKeys, &kv_full[st]);
+                } else {
+#pragma unroll 1
+                    for (int j = 0; j < C::kBoxes; ++j)
+                        tma_load_2d(dst + j * C::kBoxBytes, &tmBlk, j * 64, b * p.block, &kv_full[st]);
+                }
+                issued = i + 1;
+            }
+            if (!waited) pdl_wait();
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idS = idesc_bf16_f32(kTcRows, kTcKeys);
+            constexpr uint32_t idPV = idesc_bf16_f32(kTcRows, C::kDVP) | kIdescBMajorMN;
+            // S(i) = Q K_i^T once K_i has landed and the softmax has read S(i-1)
+            auto issue_s = [&](int i) -> bool {
+                const int st = i % kTcStages;
+                if (!mbar_wait_bounded(&kv_full[st], (uint32_t)((i / kTcStages) & 1), &s_abort)) return false;
+                if (i > 0 && !mbar_wait_bounded(s_free, (uint32_t)((i - 1) & 1), &s_abort)) return false;
+                tc_fence_after();
+                const uint32_t base = smem_u32(sKV + st * C::kTileBytes);
+#pragma unroll 1
+                for (int kk = 0; kk < C::kDQKP / 16; ++kk) {
+                    const uint64_t bd = sdesc_k_sw128(base + (kk >> 2) * C::kBoxBytes) + (uint64_t)(2 * (kk & 3));
+                    mma_bf16_tmem_a(tmem + C::kSCol, tmem + C::kQCol + 8 * kk, bd, idS, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(s_full);
+                return true;
+            };
+            bool ok = nch == 0 || (mbar_wait_bounded(q_ready, 0, &s_abort) && issue_s(0));
+            for (int i = 0; i < nch && ok; ++i) {
+                const int st = i % kTcStages;
+                // the next chunk's scores overlap this chunk's softmax
+                if (i + 1 < nch && !issue_s(i + 1)) break;
+                if (!mbar_wait_bounded(p_ready, (uint32_t)(i & 1), &s_abort)) break;
+                tc_fence_after();
+                const uint32_t base = smem_u32(sKV + st * C::kTileBytes);
+                const uint32_t vbase = base + (part * C::kDVP / 64) * C::kBoxBytes;
+#pragma unroll
+                for (int kk = 0; kk < kTcKeys / 16; ++kk) {
+                    const uint64_t vd = sdesc_mn_sw128(vbase + kk * 16 * 128, C::kBoxBytes, 1024);
+                    mma_bf16_tmem_a(tmem + C::kOCol, tmem + C::kPCol + 8 * kk, vd, idPV, (i > 0 || kk > 0) ? 1u : 0u);
+                }
+                mma_commit(pv_done);
+                mma_commit(&kv_empty[st]);
+            }
+            mma_commit(mma_done);
+            mbar_drain(mma_done, 0);
+        }
+        __syncwarp();
+    } else {
+        // warps 2..5: one query row per thread (TMEM lane quadrant = warp % 4)
+        const int q4 = warp & 3;
+        const int row = 32 * q4 + lane, r = r0 + row;
+        const bool rv = r < p.R;
+        const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
+        // Q row into tensor memory (bf16 pairs; the padding past DQK is zero)
+        const __nv_bfloat16 *qrow = p.qt + ((size_t)b * p.R + (rv ? r : 0)) * DQK;
+        auto qload = [&](int c32, uint4 (&u)[8]) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int e = 2 * c32 + 8 * j;
+                u[j] = (rv && e < DQK) ? __ldg((const uint4 *)(qrow + e)) : make_uint4(0u, 0u, 0u, 0u);
+            }
+        };
+        uint4 qa[8], qb[8];
+        qload(0, qa);
+#pragma unroll 1
+        for (int c32 = 0; c32 < C::kDQKP / 2; c32 += 64) {
+            if (c32 + 32 < C::kDQKP / 2) qload(c32 + 32, qb);  // next batch in flight while this one is stored
+            uint32_t v[32];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                v[4 * j] = qa[j].x;
+                v[4 * j + 1] = qa[j].y;
+                v[4 * j + 2] = qa[j].z;
+                v[4 * j + 3] = qa[j].w;
+            }
+            tmem_st32(tl + C::kQCol + c32, v);
+            if (c32 + 32 < C::kDQKP / 2) {
+                if (c32 + 64 < C::kDQKP / 2) qload(c32 + 64, qa);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    v[4 * j] = qb[j].x;
+                    v[4 * j + 1] = qb[j].y;
+                    v[4 * j + 2] = qb[j].z;
+                    v[4 * j + 3] = qb[j].w;
+                }
+                tmem_st32(tl + C::kQCol + c32 + 32, v);
+            }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(q_ready);
+
+        float m_ref = -INFINITY, lsum = 0.f;
+        bool ok = true;
+        int done = 0;
+        for (int i = 0; i < nch; ++i) {
+            const int c = c_begin + i;
+            const int nvalid = c < npages ? min(kTcKeys, ctx - c * kTcKeys) : p.block;
+            if (!warp_wait(s_full, (uint32_t)(i & 1), &s_abort)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t sr[4][16];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) tmem_ld16_nw(tl + C::kSCol + 16 * t, sr[t]);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(s_free);
+            float s[64];
+            float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int j = 0; j < 64; ++j) {
+                s[j] = j < nvalid ? __uint_as_float(sr[j >> 4][j & 15]) * p.scale_log2 : -INFINITY;
+                mx4[j & 3] = fmaxf(mx4[j & 3], s[j]);
+            }
+            const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+            const float m_new = fmaxf(m_ref, mx);
+            const bool rescale = (m_ref == -INFINITY) ? (m_new != -INFINITY) : (m_new > m_ref + kTcRescaleLog2);
+            float corr = 1.f;
+            if (rescale) {
+                corr = (m_ref == -INFINITY) ? 0.f : exp2f(m_ref - m_new);
+                m_ref = m_new;
+            }
+            uint32_t pk[32];
+            float ls4[4] = {0.f, 0.f, 0.f, 0.f};
+            const bool live = m_ref != -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const float p0 = live ? exp2f(s[2 * j] - m_ref) : 0.f;
+                const float p1 = live ? exp2f(s[2 * j + 1] - m_ref) : 0.f;
+                ls4[j & 3] += p0 + p1;
+                pk[j] = pack_bf16x2(p0, p1);
+            }
+            lsum = lsum * corr + ((ls4[0] + ls4[1]) + (ls4[2] + ls4[3]));
+            // P and O are free once the previous chunk's P V has completed
+            if (i > 0 && !warp_wait(pv_done, (uint32_t)((i - 1) & 1), &s_abort)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (i > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
+#pragma unroll 1
+                for (int t = 0; t < C::kDVP / 16; ++t) {
+                    float v[16];
+                    uint32_t u[16];
+                    tmem_ld16(tl + C::kOCol + 16 * t, v);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) u[j] = __float_as_uint(v[j] * corr);
+                    tmem_st16(tl + C::kOCol + 16 * t, u);
+                }
+            }
+            if (nvalid < kTcKeys) {
+                // keys past the valid range: zero their value rows (this CTA's columns) so that
+                // P = 0 meets finite values in P V
+                uint8_t *tileb = sKV + (i % kTcStages) * C::kTileBytes + (part * C::kDVP / 64) * C::kBoxBytes;
+                const int nrow = kTcKeys - nvalid, per_box = nrow * 8;  // 16-byte pieces per box
+                for (int idx = threadIdx.x - 64; idx < per_box * (C::kDVP / 64); idx += 128) {
+                    const int bx = idx / per_box, rem = idx % per_box;
+                    *(uint4 *)(tileb + bx * C::kBoxBytes + (nvalid + rem / 8) * 128 + (rem % 8) * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            }
+            tmem_st32(tl + C::kPCol, pk);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_ready);
+            done = i + 1;
+        }
+        if (ok && done > 0 && !warp_wait(pv_done, (uint32_t)((done - 1) & 1), &s_abort)) ok = false;
+        tc_fence_after();
+        if (ok) {
+            const size_t pr = ((size_t)b * p.splits + split) * p.R + (rv ? r : 0);
+            const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+            float *dst = p.splits == 1 ? p.o_lat + ((size_t)b * p.R + (rv ? r : 0)) * DV + part * C::kDVP
+                                       : p.part_o + pr * DV + part * C::kDVP;
+#pragma unroll 1
+            for (int t = 0; t < C::kDVP / 16; ++t) {
+                float v[16];
+                if (done > 0) {
+                    tmem_ld16(tl + C::kOCol + 16 * t, v);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) v[j] = 0.f;
+                }
+                if (rv) {
+#pragma unroll
+                    for (int j = 0; j < 16; j += 4) {
+                        float4 o = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+                        if (p.splits == 1) o = make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+                        *(float4 *)(dst + 16 * t + j) = o;
+                    }
+                }
+            }
+            if (rv && p.splits > 1 && part == 0) *(float2 *)(p.part_ml + pr * 2) = make_float2(m_ref, lsum);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (s_abort) {
+        if (threadIdx.x == 0) set_error(p.err, DSPARK_ERR_TIMEOUT);
+        if (warp == 0 && lane == 0) {
+            // the last chunk issued to each stage lands before shared memory is released
+            for (int i = issued - 1; i >= 0 && i >= issued - kTcStages; --i)
+                mbar_drain(&kv_full[i % kTcStages], (uint32_t)((i / kTcStages) & 1));
+        }
+        __syncthreads();
+    }
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// Split plan of the tensor-core attention: about one wave of CTAs
+// (row tiles x output parts x splits x sequences), whole chunks per split.
+int attention_tc_splits(int R, int dv, int bs, int max_ctx, int num_sms, int *cps) {
+    const int tiles = (R + kTcRows - 1) / kTcRows;
+    const int parts = dv / (dv < 128 ? dv : 128);
+    const int chunks = (max_ctx + kTcKeys - 1) / kTcKeys + 1;
+    int s = num_sms / (tiles * parts * bs);
+    if (s < 1) s = 1;
+    if (s > chunks) s = chunks;
+    if (s > 64) s = 64;
+    *cps = (chunks + s - 1) / s;
+    return (chunks + *cps - 1) / *cps;
+}
+
+cudaError_t launch_attention_tc(const CUtensorMap &pool_map, const CUtensorMap &blk_map, const AttnParams &a,
+                                int cps, int bs, int dqk, int dv, cudaStream_t st) {
+    if (!attention_tc_supported(dqk, dv)) return cudaErrorInvalidValue;
+    using C = TcCfg<576, 512>;
+    static bool attr = false;
+    if (!attr) {
+        const cudaError_t e = cudaFuncSetAttribute(mla_attention_tc_kernel<576, 512>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    TcAttnParams p;
+    memset(&p, 0, sizeof(p));
+    p.qt = a.qt;
+    p.R = a.R;
+    p.n_pages = a.n_pages;
+    p.page_table = a.page_table;
+    p.max_pages = a.max_pages;
+    p.ctx_len = a.ctx_len;
+    p.max_ctx = a.max_ctx;
+    p.block = a.block;
+    p.splits = a.splits;
+    p.cps = cps;
+    p.scale_log2 = a.scale_log2;
+    p.o_lat = a.o_lat;
+    p.part_o = a.part_o;
+    p.part_ml = a.part_ml;
+    p.err = a.err;
+    const int tiles = (a.R + kTcRows - 1) / kTcRows;
+    dim3 grid(tiles * C::kParts, a.splits, bs);
+    cudaError_t e = launch_pdl(mla_attention_tc_kernel<576, 512>, grid, dim3(192), (size_t)C::kSmem, st, pool_map,
+                               blk_map, p);
+    if (e != cudaSuccess || a.splits == 1) return e;
+    return launch_attn_combine(a, bs, dv, st);
+}
+
+}  // namespace ds

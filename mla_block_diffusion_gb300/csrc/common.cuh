@@ -146,6 +146,22 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// Shared-memory matrix descriptor for an MN-major operand in the 128-byte
+// swizzled layout: rows of 128 bytes hold 64 consecutive MN elements of one k,
+// 8 consecutive k rows form a 1024-byte atom; atoms repeat along k every
+// sbo_bytes and along MN every lbo_bytes.
+DS_DEVINL uint64_t sdesc_mn_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+// Instruction-descriptor bit that reads the B operand MN-major.
+constexpr uint32_t kIdescBMajorMN = 1u << 16;
+
 // Instruction descriptor, kind::f16: f16 A and B, fp32 accumulator, both K-major.
 __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
     return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);

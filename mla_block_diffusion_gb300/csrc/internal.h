@@ -42,6 +42,14 @@ cudaError_t launch_v_absorb(const float *o_lat, int M, int n_h, int d_nope, int 
                             const __nv_bfloat16 *w_kvb, __nv_bfloat16 *out, cudaStream_t st);
 bool attention_supported(int dqk, int dv);
 cudaError_t launch_attention(const AttnParams &p, int bs, int dqk, int dv, cudaStream_t st);
+cudaError_t launch_attn_combine(const AttnParams &p, int bs, int dv, cudaStream_t st);
+// Tensor-core attention (latent 512 + rope 64): pool_map views one layer's page
+// pool as bf16 [n_pages * 64, dqk], blk_map the block latents [bs * block, dqk],
+// both with 64 x 64 boxes in the 128-byte swizzle.
+bool attention_tc_supported(int dqk, int dv);
+int attention_tc_splits(int R, int dv, int bs, int max_ctx, int num_sms, int *cps);
+cudaError_t launch_attention_tc(const CUtensorMap &pool_map, const CUtensorMap &blk_map, const AttnParams &a,
+                                int cps, int bs, int dqk, int dv, cudaStream_t st);
 cudaError_t launch_confidence(const float *h_out, int H, const float *w, float bias, float *conf, int M,
                               cudaStream_t st);
 

@@ -16,8 +16,9 @@ namespace ds {
 // fp64 operations, exact enough at positions ~10^5), then evaluated in fp32.
 DS_DEVINL void rope_cs(double pos, double inv_freq, float &c, float &s) {
     const double two_pi = 6.283185307179586476925286766559;
+    const double inv_two_pi = 0.15915494309189533576888376337251;
     const double a = pos * inv_freq;
-    const double r = a - two_pi * rint(a / two_pi);
+    const double r = fma(-two_pi, rint(a * inv_two_pi), a);  // a reduced to about [-pi, pi]
     sincosf((float)r, &s, &c);
 }
 
@@ -165,9 +166,18 @@ __global__ void __launch_bounds__(128) q_absorb_kernel(const float *__restrict__
     for (int i = 0; i < 64; ++i) w[i] = i < dq ? __ldg((const unsigned int *)(W + (size_t)i * kv_lora)) : 0u;
     pdl_wait();
     for (int m0 = 0; m0 < M; m0 += kQAbsRows) {
-        for (int idx = threadIdx.x; idx < kQAbsRows * d_nope; idx += blockDim.x) {
-            const int mm = idx / d_nope, d = idx % d_nope, m = m0 + mm;
-            sq[idx] = (m < M) ? q[((size_t)m * n_h + h) * qhd + d] : 0.f;
+        // one round of independent loads: thread t takes d = t, t + 128 of every row
+#pragma unroll
+        for (int dd = 0; dd < 2; ++dd) {
+            const int d = threadIdx.x + dd * 128;
+            float v[kQAbsRows];
+#pragma unroll
+            for (int mm = 0; mm < kQAbsRows; ++mm)
+                v[mm] = (d < d_nope && m0 + mm < M) ? q[((size_t)(m0 + mm) * n_h + h) * qhd + d] : 0.f;
+            if (d < d_nope) {
+#pragma unroll
+                for (int mm = 0; mm < kQAbsRows; ++mm) sq[mm * d_nope + d] = v[mm];
+            }
         }
         __syncthreads();
         float a0[kQAbsRows], a1[kQAbsRows];
@@ -202,9 +212,10 @@ __global__ void __launch_bounds__(128) q_absorb_kernel(const float *__restrict__
         }
         __syncthreads();
     }
-    if (blockIdx.y == 0) {
+    {
+        // RoPE of q_rope, the rows spread over the head's column blocks
         const int np = d_rope / 2;
-        for (int idx = threadIdx.x; idx < M * np; idx += blockDim.x) {
+        for (int idx = blockIdx.y * blockDim.x + threadIdx.x; idx < M * np; idx += gridDim.y * blockDim.x) {
             const int m = idx / np, p = idx % np;
             int c = ctx_len[m / block];
             if (c < 0 || c > max_ctx) c = 0;
@@ -651,6 +662,10 @@ cudaError_t launch_attention(const AttnParams &p, int bs, int dqk, int dv, cudaS
     else
         return cudaErrorInvalidValue;
     if (e != cudaSuccess || p.splits == 1) return e;
+    return launch_attn_combine(p, bs, dv, st);
+}
+
+cudaError_t launch_attn_combine(const AttnParams &p, int bs, int dv, cudaStream_t st) {
     return launch_pdl(attn_combine_kernel, dim3(p.R, bs), dim3(128), 0, st, p.part_o, p.part_ml, p.splits, p.R, dv,
                       p.o_lat);
 }

@@ -18,6 +18,10 @@ from tests.helpers import f64, oracle_layers
 # split KV loop for attention (latent widths covered by the attention kernel).
 MID = Geometry(hidden=1024, n_aux=5, n_layers=2, n_heads=16, q_lora=256, kv_lora=256, d_nope=64, d_rope=32,
                d_v=64, inter=2048, vocab=8192, rank=32)
+# The full latent width (512 + 64): the tensor-core attention path, with 40
+# heads so a sequence's 280 query rows span three 128-row tiles (the last ragged).
+MIDLAT = Geometry(hidden=1024, n_aux=2, n_layers=1, n_heads=40, q_lora=256, kv_lora=512, d_nope=32, d_rope=64,
+                  d_v=32, inter=1024, vocab=4096, rank=32)
 MID128 = Geometry(hidden=768, n_aux=3, n_layers=1, n_heads=12, q_lora=192, kv_lora=128, d_nope=48, d_rope=32,
                   d_v=48, inter=1536, vocab=6144, rank=24, block=5)
 

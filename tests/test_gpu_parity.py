@@ -12,7 +12,7 @@ from oracle import network as N
 from oracle import sampling as S
 from synthetic import generate as gen
 from synthetic.configs import TINY, TINY_STEP
-from tests.gpu_harness import MID, MID128, draw, gpu_draft, oracle_draft, to_cuda, u32, workload
+from tests.gpu_harness import MID, MID128, MIDLAT, draw, gpu_draft, oracle_draft, to_cuda, u32, workload
 from tests.helpers import f64, rel_l2
 
 pytestmark = pytest.mark.gpu
@@ -52,6 +52,9 @@ def test_tiny_step_draft(M):
     (MID, 3, (1000, 77, 300)),     # split KV loop, ragged pages, three sequences
     (MID, 1, (0,)),                # empty context: only the block's own latents
     (MID128, 2, (130, 4000)),      # block 5, 3 aux states, long/short mix
+    (MIDLAT, 3, (1000, 77, 4097)),  # tensor-core attention: partial pages, a one-token last page, splits
+    (MIDLAT, 1, (0,)),             # tensor-core attention: only the block's own latents
+    (MIDLAT, 2, (64, 640)),        # tensor-core attention: contexts ending on page boundaries
 ])
 def test_mid_draft(M, G, bs, ctx):
     w = workload(G, bs, ctx, seed=7)
