@@ -62,7 +62,8 @@ enum { DSPARK_GREEDY = 0, DSPARK_PROBABILISTIC = 1 };
  * works"; [P2] "Architecture metadata"; [P3] "Model Overview").
  * Supported by the kernels: hidden, q_lora, kv_lora, inter, n_heads*d_v
  * multiples of 64; (kv_lora + d_rope, kv_lora) one of (576, 512), (288, 256),
- * (160, 128), (80, 64); d_nope <= 256; d_rope even and <= 128; block <= 16;
+ * (160, 128), (80, 64); q_lora + kv_lora <= 8192; d_nope <= 256; d_rope a
+ * multiple of 4 and <= 128; block <= 16;
  * rank <= 256; vocab even and < 2^18; page_size 64; weight_format BF16, FP8
  * (E4M3 per output row) or NVFP4 (E2M1, E4M3 group-16 scales, global scale;
  * then hidden, q_lora, n_heads*d_v and inter multiples of 256). With FP8 or

@@ -314,9 +314,9 @@ dspark_status check_geom(const dspark_geom_t *g) {
         g->vocab <= 0 || g->rank <= 0 || g->block <= 0)
         return DSPARK_ERR_SHAPE;
     if (g->hidden % 64 || g->q_lora % 64 || g->kv_lora % 64 || g->inter % 64 || (g->n_heads * g->d_v) % 64 ||
-        g->d_rope % 2 || g->d_rope > 128 || g->vocab % 8 || g->vocab >= (1 << 18) || g->rank > 256 ||
+        g->d_rope % 4 || g->d_rope > 128 || g->vocab % 8 || g->vocab >= (1 << 18) || g->rank > 256 ||
         g->block > 16 || g->page_size != 64 || g->d_nope > 256 || g->d_nope % 16 || g->d_v % 16 ||
-        g->kv_lora > 512)
+        g->kv_lora > 512 || g->q_lora + g->kv_lora > 8192)
         return DSPARK_ERR_UNSUPPORTED;
     if (!attention_supported(g->kv_lora + g->d_rope, g->kv_lora)) return DSPARK_ERR_UNSUPPORTED;
     if (g->weight_format != DSPARK_FMT_BF16 && g->weight_format != DSPARK_FMT_FP8 &&

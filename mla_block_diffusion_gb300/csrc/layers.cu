@@ -96,38 +96,87 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const float *__re
 //   -> the block's own latent KV entries [c_kv || k_r] bf16.
 // Angles are formed in fp64 (positions reach ~10^5).
 // ---------------------------------------------------------------------------
-__global__ void latent_kernel(const float *__restrict__ qkv, int ld, int q_lora, int kv_lora, int d_rope,
-                              const float *__restrict__ g_q, const float *__restrict__ g_kv, float eps,
-                              const int32_t *__restrict__ ctx_len, int block, int max_ctx, RopeTable rt,
-                              __nv_bfloat16 *__restrict__ cq, __nv_bfloat16 *__restrict__ blk_kv, int *err) {
+__device__ float2 block_sum2(float2 v, float2 *red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+    v.x = warp_sum(v.x);
+    v.y = warp_sum(v.y);
+    __syncthreads();
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    float2 r = (threadIdx.x < nw) ? red[threadIdx.x] : make_float2(0.f, 0.f);
+    if (warp == 0) {
+        r.x = warp_sum(r.x);
+        r.y = warp_sum(r.y);
+    }
+    if (threadIdx.x == 0) red[32] = r;
+    __syncthreads();
+    return red[32];
+}
+
+constexpr int kLatentThreads = 512;
+
+// One CTA per row; q_lora and kv_lora multiples of 4. Each thread keeps its
+// float4 pieces of the row (at most 4: the row holds up to 2048 + 512 values).
+__global__ void __launch_bounds__(kLatentThreads) latent_kernel(
+    const float *__restrict__ qkv, int ld, int q_lora, int kv_lora, int d_rope, const float *__restrict__ g_q,
+    const float *__restrict__ g_kv, float eps, const int32_t *__restrict__ ctx_len, int block, int max_ctx,
+    RopeTable rt, __nv_bfloat16 *__restrict__ cq, __nv_bfloat16 *__restrict__ blk_kv, int *err) {
     pdl_trigger();
-    pdl_wait();
-    __shared__ float red[33];
+    __shared__ float2 red[33];
     const int m = blockIdx.x;
     const int b = m / block, i = m % block;
-    const float *row = qkv + (size_t)m * ld;
-    float sq = 0.f, sk = 0.f;
-    for (int j = threadIdx.x; j < q_lora; j += blockDim.x) sq += row[j] * row[j];
-    for (int j = threadIdx.x; j < kv_lora; j += blockDim.x) sk += row[q_lora + j] * row[q_lora + j];
-    sq = block_sum(sq, red);
-    sk = block_sum(sk, red);
-    if ((!isfinite(sq) || !isfinite(sk)) && threadIdx.x == 0) set_error(err, DSPARK_ERR_BAD_INPUT);
-    const float rq = rsqrtf(sq / (float)q_lora + eps), rk = rsqrtf(sk / (float)kv_lora + eps);
-    for (int j = threadIdx.x; j < q_lora; j += blockDim.x)
-        cq[(size_t)m * q_lora + j] = __float2bfloat16(row[j] * rq * g_q[j]);
-    const int kvd = kv_lora + d_rope;
-    for (int j = threadIdx.x; j < kv_lora; j += blockDim.x)
-        blk_kv[(size_t)m * kvd + j] = __float2bfloat16(row[q_lora + j] * rk * g_kv[j]);
+    const int nq4 = q_lora / 4, nk4 = kv_lora / 4, n4 = nq4 + nk4;
+    const float4 *row = (const float4 *)(qkv + (size_t)m * ld);
+    // gains first (inputs of the step), then the row
+    float4 gr[4], v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int t = threadIdx.x + u * blockDim.x;
+        gr[u] = t < nq4 ? __ldg((const float4 *)g_q + t)
+                        : (t < n4 ? __ldg((const float4 *)g_kv + (t - nq4)) : make_float4(0.f, 0.f, 0.f, 0.f));
+    }
     int c = ctx_len[b];
+    pdl_wait();
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int t = threadIdx.x + u * blockDim.x;
+        v[u] = t < n4 ? row[t] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float2 ss = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int t = threadIdx.x + u * blockDim.x;
+        const float sq = v[u].x * v[u].x + v[u].y * v[u].y + v[u].z * v[u].z + v[u].w * v[u].w;
+        if (t < nq4)
+            ss.x += sq;
+        else
+            ss.y += sq;
+    }
+    ss = block_sum2(ss, red);
+    if ((!isfinite(ss.x) || !isfinite(ss.y)) && threadIdx.x == 0) set_error(err, DSPARK_ERR_BAD_INPUT);
+    const float rq = rsqrtf(ss.x / (float)q_lora + eps), rk = rsqrtf(ss.y / (float)kv_lora + eps);
+    const int kvd = kv_lora + d_rope;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int t = threadIdx.x + u * blockDim.x;
+        if (t < n4) {
+            const float r = t < nq4 ? rq : rk;
+            __nv_bfloat16 *dst = t < nq4 ? cq + (size_t)m * q_lora + 4 * t : blk_kv + (size_t)m * kvd + 4 * (t - nq4);
+            __nv_bfloat162 *d2 = (__nv_bfloat162 *)dst;
+            d2[0] = __floats2bfloat162_rn(v[u].x * r * gr[u].x, v[u].y * r * gr[u].y);
+            d2[1] = __floats2bfloat162_rn(v[u].z * r * gr[u].z, v[u].w * r * gr[u].w);
+        }
+    }
     if (c < 0 || c > max_ctx) {
         if (threadIdx.x == 0) set_error(err, DSPARK_ERR_OOB);
         c = 0;
     }
     const double pos = (double)(c + i);
+    const float *rp = qkv + (size_t)m * ld + q_lora + kv_lora;
     for (int p = threadIdx.x; p < d_rope / 2; p += blockDim.x) {
         float fc, fs;
         rope_cs(pos, rt.inv_freq[p], fc, fs);
-        const float x0 = row[q_lora + kv_lora + 2 * p], x1 = row[q_lora + kv_lora + 2 * p + 1];
+        const float x0 = rp[2 * p], x1 = rp[2 * p + 1];
         blk_kv[(size_t)m * kvd + kv_lora + 2 * p] = __float2bfloat16(x0 * fc - x1 * fs);
         blk_kv[(size_t)m * kvd + kv_lora + 2 * p + 1] = __float2bfloat16(x0 * fs + x1 * fc);
     }
@@ -146,6 +195,7 @@ constexpr int kAbsorbRows = 16;
 constexpr int kQAbsRows = 8;
 constexpr int kQAbsCols = 64;
 
+template <int MAXDQ>
 __global__ void __launch_bounds__(128) q_absorb_kernel(const float *__restrict__ q, int M, int n_h, int d_nope,
                                                        int d_rope, int kv_lora, int d_v,
                                                        const __nv_bfloat16 *__restrict__ w_kvb,
@@ -161,9 +211,9 @@ __global__ void __launch_bounds__(128) q_absorb_kernel(const float *__restrict__
     const int qhd = d_nope + d_rope, kvd = kv_lora + d_rope;
     // the weights do not depend on the previous kernel: load them before the wait
     const __nv_bfloat16 *W = w_kvb + ((size_t)h * (d_nope + d_v) + qd * dq) * kv_lora + c0 + 2 * lane;
-    uint32_t w[64];
+    uint32_t w[MAXDQ];
 #pragma unroll
-    for (int i = 0; i < 64; ++i) w[i] = i < dq ? __ldg((const unsigned int *)(W + (size_t)i * kv_lora)) : 0u;
+    for (int i = 0; i < MAXDQ; ++i) w[i] = i < dq ? __ldg((const unsigned int *)(W + (size_t)i * kv_lora)) : 0u;
     pdl_wait();
     for (int m0 = 0; m0 < M; m0 += kQAbsRows) {
         // one round of independent loads: thread t takes d = t, t + 128 of every row
@@ -184,7 +234,7 @@ __global__ void __launch_bounds__(128) q_absorb_kernel(const float *__restrict__
 #pragma unroll
         for (int mm = 0; mm < kQAbsRows; ++mm) a0[mm] = a1[mm] = 0.f;
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
+        for (int i = 0; i < MAXDQ; ++i) {
             if (i < dq) {
                 const float2 wf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[i]));
 #pragma unroll
@@ -238,20 +288,22 @@ __global__ void __launch_bounds__(128) q_absorb_kernel(const float *__restrict__
 // the latent: no bank conflicts), read once; the rows sweep in chunks of 16
 // from shared memory; the 16 partial dots are reduced with shuffles.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) v_absorb_kernel(const float *__restrict__ o_lat, int M, int n_h, int d_nope,
+constexpr int kVAbsRows = 8;
+
+__global__ void __launch_bounds__(256, 4) v_absorb_kernel(const float *__restrict__ o_lat, int M, int n_h, int d_nope,
                                                        int d_v, int kv_lora, const __nv_bfloat16 *__restrict__ w_kvb,
                                                        __nv_bfloat16 *__restrict__ out) {
     pdl_trigger();
-    pdl_wait();
-    extern __shared__ float so[];  // [kAbsorbRows][kv_lora]
+    extern __shared__ float so[];  // [kVAbsRows][kv_lora]
     const int h = blockIdx.x, e = blockIdx.y * 16 + (threadIdx.x >> 4), cg = threadIdx.x & 15;
     const __nv_bfloat16 *W = w_kvb + ((size_t)h * (d_nope + d_v) + d_nope + e) * kv_lora;
     const int nj = kv_lora / 64;  // float4 slices per thread (<= 8)
+    // the weights do not depend on the previous kernel: read them before the wait
     float wv[8][4];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         if (j < nj) {
-            const uint2 u = *(const uint2 *)(W + 4 * (cg + 16 * j));
+            const uint2 u = __ldg((const uint2 *)(W + 4 * (cg + 16 * j)));
             const float2 f0 = __bfloat1622float2(*(const __nv_bfloat162 *)&u.x);
             const float2 f1 = __bfloat1622float2(*(const __nv_bfloat162 *)&u.y);
             wv[j][0] = f0.x;
@@ -262,14 +314,28 @@ __global__ void __launch_bounds__(256) v_absorb_kernel(const float *__restrict__
             wv[j][0] = wv[j][1] = wv[j][2] = wv[j][3] = 0.f;
         }
     }
-    for (int m0 = 0; m0 < M; m0 += kAbsorbRows) {
-        for (int idx = threadIdx.x; idx < kAbsorbRows * kv_lora / 4; idx += blockDim.x) {
-            const int mm = idx / (kv_lora / 4), c4 = idx % (kv_lora / 4), m = m0 + mm;
-            ((float4 *)so)[idx] = (m < M) ? ((const float4 *)(o_lat + ((size_t)m * n_h + h) * kv_lora))[c4]
-                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+    pdl_wait();
+    const int c4n = kv_lora / 4;  // float4 per row (<= 128)
+    for (int m0 = 0; m0 < M; m0 += kVAbsRows) {
+        // one round of loads: thread t takes float4 column t % c4n of rows t / c4n + k * (256 / c4n)
+        // kv_lora = 512: two rows per pass, four passes, all loads issued first
+        float4 v[4];
+        const int rstep = blockDim.x / c4n, c4 = threadIdx.x % c4n, rr0 = threadIdx.x / c4n;
+        for (int k0 = 0; k0 * rstep < kVAbsRows; k0 += 4) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int mm = rr0 + (k0 + k) * rstep, m = m0 + mm;
+                v[k] = (mm < kVAbsRows && m < M) ? ((const float4 *)(o_lat + ((size_t)m * n_h + h) * kv_lora))[c4]
+                                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int mm = rr0 + (k0 + k) * rstep;
+                if (mm < kVAbsRows) ((float4 *)so)[mm * c4n + c4] = v[k];
+            }
         }
         __syncthreads();
-        const int mmax = min(kAbsorbRows, M - m0);
+        const int mmax = min(kVAbsRows, M - m0);
         for (int mm = 0; mm < mmax; ++mm) {
             float acc = 0.f;
 #pragma unroll
@@ -522,9 +588,7 @@ __global__ void attn_combine_kernel(const float *__restrict__ part_o, const floa
                                     int R, int DV, float *__restrict__ o_lat) {
     pdl_trigger();
     pdl_wait();
-    __shared__ float sw[64];
     __shared__ float sml[64][2];
-    __shared__ float sinv;
     const int r = blockIdx.x, b = blockIdx.y;
     const size_t base = (size_t)b * splits * R + r;
     if (threadIdx.x < splits) {
@@ -533,25 +597,19 @@ __global__ void attn_combine_kernel(const float *__restrict__ part_o, const floa
         sml[threadIdx.x][1] = ml.y;
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        float M = -INFINITY;
-        for (int s = 0; s < splits; ++s)
-            if (sml[s][1] > 0.f) M = fmaxf(M, sml[s][0]);
-        float den = 0.f;
-        for (int s = 0; s < splits; ++s) {
-            const float w = sml[s][1] > 0.f ? exp2f(sml[s][0] - M) : 0.f;
-            sw[s] = w;
-            den += w * sml[s][1];
-        }
-        sinv = den > 0.f ? 1.f / den : 0.f;
-    }
-    __syncthreads();
-    const float inv = sinv;
+    // every thread forms the same weights from shared memory (fixed split order)
+    float M = -INFINITY;
+    for (int s = 0; s < splits; ++s)
+        if (sml[s][1] > 0.f) M = fmaxf(M, sml[s][0]);
+    float den = 0.f;
+    for (int s = 0; s < splits; ++s)
+        if (sml[s][1] > 0.f) den += exp2f(sml[s][0] - M) * sml[s][1];
+    const float inv = den > 0.f ? 1.f / den : 0.f;
     for (int c = threadIdx.x * 4; c < DV; c += blockDim.x * 4) {
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 8
         for (int s = 0; s < splits; ++s) {
-            const float w = sw[s];
+            const float w = sml[s][1] > 0.f ? exp2f(sml[s][0] - M) : 0.f;
             const float4 v = __ldcg((const float4 *)(part_o + (base + (size_t)s * R) * DV + c));
             acc.x += w * v.x;
             acc.y += w * v.y;
@@ -609,7 +667,7 @@ cudaError_t launch_latent(const float *qkv, int ld, int q_lora, int kv_lora, int
                           const float *g_kv, float eps, const int32_t *ctx_len, int block, int max_ctx,
                           const RopeTable &rt, __nv_bfloat16 *cq, __nv_bfloat16 *blk_kv, int M, int *err,
                           cudaStream_t st) {
-    return launch_pdl(latent_kernel, dim3(M), dim3(256), 0, st, qkv, ld, q_lora, kv_lora, d_rope, g_q, g_kv, eps,
+    return launch_pdl(latent_kernel, dim3(M), dim3(kLatentThreads), 0, st, qkv, ld, q_lora, kv_lora, d_rope, g_q, g_kv, eps,
                       ctx_len, block, max_ctx, rt, cq, blk_kv, err);
 }
 
@@ -618,14 +676,15 @@ cudaError_t launch_q_absorb(const float *q, int M, int n_h, int d_nope, int d_ro
                             const RopeTable &rt, __nv_bfloat16 *qt, cudaStream_t st) {
     dim3 grid(n_h, kv_lora / kQAbsCols);
     const size_t smem = ((size_t)kQAbsRows * d_nope + (size_t)4 * kQAbsRows * kQAbsCols) * sizeof(float);
-    return launch_pdl(q_absorb_kernel, grid, dim3(128), smem, st, q, M, n_h, d_nope, d_rope, kv_lora, d_v, w_kvb,
+    // the thread's k_b slice (d_nope / 4 rows) in registers: 32 covers d_nope <= 128
+    return launch_pdl(d_nope <= 128 ? q_absorb_kernel<32> : q_absorb_kernel<64>, grid, dim3(128), smem, st, q, M, n_h, d_nope, d_rope, kv_lora, d_v, w_kvb,
                       ctx_len, block, max_ctx, rt, qt);
 }
 
 cudaError_t launch_v_absorb(const float *o_lat, int M, int n_h, int d_nope, int d_v, int kv_lora,
                             const __nv_bfloat16 *w_kvb, __nv_bfloat16 *out, cudaStream_t st) {
     dim3 grid(n_h, d_v / 16);
-    const size_t smem = (size_t)kAbsorbRows * kv_lora * sizeof(float);
+    const size_t smem = (size_t)kVAbsRows * kv_lora * sizeof(float);
     return launch_pdl(v_absorb_kernel, grid, dim3(256), smem, st, o_lat, M, n_h, d_nope, d_v, kv_lora, w_kvb, out);
 }
 
