@@ -186,3 +186,39 @@ def gather_cache(pool: np.ndarray, page_table_row: np.ndarray, ctx_len: int) -> 
     P = pool.shape[1]
     j = np.arange(ctx_len)
     return pool[np.asarray(page_table_row)[j // P], j % P]
+
+
+def kv_entries(x: np.ndarray, L: Dict[str, np.ndarray], geom, positions: np.ndarray) -> np.ndarray:
+    """Latent cache entries [c_kv || k_r] (kv_lora + d_rope each) of tokens with
+    context features x [n, H] at the given positions, for one layer: the layer's
+    attention pre-norm, the kv_a rows of the fused q_a || kv_a projection, the
+    latent norm and RoPE on the rope part -- the same entry the layer forms for
+    its block rows ("Kimi-K3-DSpark-NVFP4", Model Overview: draft and target
+    share one 576-element latent layout, so the draft's pages unify with the
+    target's cache)."""
+    G = geom
+    inv_freq = rope_inv_freq(G.d_rope, G.rope_theta, G.yarn_factor, G.yarn_orig_ctx, G.yarn_alpha, G.yarn_beta)
+    h = rmsnorm(x, L["attn_norm"], G.eps)
+    kv = h @ L["w_qkv_a"][G.q_lora:].T
+    c_kv = rmsnorm(kv[:, :G.kv_lora], L["kv_a_norm"], G.eps)
+    k_r = apply_rope(kv[:, G.kv_lora:], positions, inv_freq)
+    return np.concatenate([c_kv, k_r], axis=1)
+
+
+def kv_append(x_new: np.ndarray, layers: Sequence[Dict[str, np.ndarray]], geom, pools: Sequence[np.ndarray],
+              page_table: np.ndarray, ctx_len: np.ndarray, n_new: np.ndarray):
+    """Append the latent entries of newly verified tokens to every layer's paged
+    cache. Sequence b's token j < n_new[b] (context features x_new[b, j]) goes
+    to position ctx_len[b] + j, i.e. pool[page_table[b, pos // P], pos % P].
+    Returns new pools (copies) and the new context lengths ctx_len + n_new."""
+    out = [p.copy() for p in pools]
+    P = out[0].shape[1]
+    for b in range(x_new.shape[0]):
+        n = int(n_new[b])
+        if n == 0:
+            continue
+        pos = int(ctx_len[b]) + np.arange(n)
+        for l, L in enumerate(layers):
+            e = kv_entries(x_new[b, :n], L, geom, pos)
+            out[l][np.asarray(page_table[b])[pos // P], pos % P] = e
+    return out, np.asarray(ctx_len) + np.asarray(n_new)
