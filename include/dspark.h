@@ -214,6 +214,23 @@ dspark_status dspark_verify(dspark_handle_t *h, const float *target_logits, cons
                             const dspark_sample_t *sample, int32_t *accept_len, int32_t *out_tokens, int bs,
                             void *ws, size_t ws_bytes, void *stream);
 
+/* (6) Latent-cache append of newly verified tokens ("Kimi-K3-DSpark-NVFP4",
+ * Model Overview: draft and target share one 576-element latent layout, so the
+ * draft's pages unify with the target's cache). For every layer l and every
+ * sequence b, token j < n_new[b] with context features x_new[b, j, :] gets the
+ * entry [RMSNorm(c_kv) * kv_a_norm || RoPE(k_r, pos)] (kv = the kv_a rows of
+ * w_qkv_a applied to RMSNorm(x_new) * attn_norm) written to
+ * kv->pools[l][page_table[b, pos / 64], pos % 64] with pos = ctx_len[b] + j;
+ * afterwards ctx_len[b] += n_new[b] (device, in place).
+ * x_new fp32 [bs, n_max, hidden], every row finite (rows j >= n_new[b] are read
+ * and ignored); n_new int32 [bs] on the device; 1 <= n_max <= block + 1 and
+ * n_max * bs <= 224. The workspace is the one of dspark_draft_block for the same
+ * bs and kv->max_ctx. Device errors (DSPARK_ERR_OOB): n_new outside [0, n_max],
+ * a position at or beyond max_pages * 64, a page id outside [0, n_pages); such
+ * entries are not written and that sequence's ctx_len is not advanced. */
+dspark_status dspark_kv_append(dspark_handle_t *h, const float *x_new, int n_max, const int32_t *n_new,
+                               const dspark_kv_t *kv, int bs, void *ws, size_t ws_bytes, void *stream);
+
 /* fc context fusion without a workspace: the same product as dspark_fuse_ctx,
  * for callers that cannot allocate device memory for a workspace (a serving
  * process whose device memory another allocator has already reserved, a

@@ -114,7 +114,7 @@ int bn_for(int M) {
 size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct Layout {
-    size_t partials, hn, qkv, cq, q, qt, blk, olat, part_o, part_ml, ov, act, hout, scratch, total;
+    size_t partials, hn, qkv, cq, q, qt, blk, olat, part_o, part_ml, ov, act, hout, scratch, app_hn, app_kv, total;
     int splits, tok_per_split;
     int tc, cps;                 // tensor-core attention and its chunks per split
 };
@@ -140,6 +140,10 @@ struct dspark_handle {
     int c_bs = -1;
     CUtensorMap b_hn, b_cq, b_ov, b_act, b_hout;
     CUtensorMap b_blk;                       // block latents, tensor-core attention
+    CUtensorMap kva[DSPARK_MAX_LAYERS];      // kv_a rows of the fused q_a || kv_a weights
+    const void *c_app_ws = nullptr;
+    int c_app_rows = -1;
+    CUtensorMap b_app;                       // normed context features of appended tokens
     const void *c_pool[DSPARK_MAX_LAYERS] = {};
     int c_npages[DSPARK_MAX_LAYERS] = {};
     CUtensorMap pool_map[DSPARK_MAX_LAYERS]; // per-layer page pools, tensor-core attention
@@ -201,6 +205,10 @@ Layout layout_for(const dspark_handle *h, int bs, int max_ctx) {
     const size_t sw1 = rollout_scratch_words(bs, g.block, h->num_sms);
     const size_t sw2 = verify_scratch_words(bs, g.block, h->num_sms);
     L.scratch = take((sw1 > sw2 ? sw1 : sw2) * 8);
+    // latent-cache append: up to block + 1 new tokens per sequence
+    const size_t A = (size_t)(g.block + 1) * bs;
+    L.app_hn = take(A * g.hidden * 2);
+    L.app_kv = take(A * kvd * 4);
     L.total = off;
     return L;
 }
@@ -463,7 +471,8 @@ dspark_status dspark_create(const dspark_geom_t *geom, const dspark_weights_t *w
     const int kvd = g.kv_lora + g.d_rope;
     for (int l = 0; l < g.n_layers && ok; ++l) {
         const dspark_layer_weights_t &L = wts->layers[l];
-        ok = make_map(&h->qkv_a[l], L.w_qkv_a, g.q_lora + kvd, g.hidden, 64);
+        ok = make_map(&h->qkv_a[l], L.w_qkv_a, g.q_lora + kvd, g.hidden, 64) &&
+             make_map(&h->kva[l], (const char *)L.w_qkv_a + (size_t)g.q_lora * g.hidden * 2, kvd, g.hidden, 64);
         if (ok && bf16w)
             ok = make_map(&h->q_b[l], L.w_q_b.data, (uint64_t)g.n_heads * (g.d_nope + g.d_rope), g.q_lora, 64) &&
                  make_map(&h->o[l], L.w_o.data, g.hidden, (uint64_t)g.n_heads * g.d_v, 64) &&
@@ -619,7 +628,6 @@ dspark_status dspark_draft_block(dspark_handle_t *h, float *x, const dspark_kv_t
     }
     RUN(launch_rmsnorm(x, g.hidden, h->w.final_norm, g.hidden, g.eps, hout, g.hidden, h_out, g.hidden, M, err, s));
     RUN(gemm(h, h->lm_head, nullptr, h->b_hout, g.vocab, g.hidden, M, EPI_STORE, z, nullptr, g.vocab, ws, s));
-#undef RUN
     return DSPARK_OK;
 }
 
@@ -660,6 +668,49 @@ dspark_status dspark_markov_rollout(dspark_handle_t *h, const float *z, const in
     p.ctl = (SampleCtl *)((char *)ws + kCtlSample);
     p.err = (int *)((char *)ws + kCtlErr);
     return cuda_status(launch_rollout(h->w2, p, h->samp_grid, (cudaStream_t)stream));
+}
+
+dspark_status dspark_kv_append(dspark_handle_t *h, const float *x_new, int n_max, const int32_t *n_new,
+                               const dspark_kv_t *kv, int bs, void *ws, size_t ws_bytes, void *stream) {
+    if (!h || !kv) return DSPARK_ERR_NULL;
+    const dspark_geom_t &g = h->g;
+    if (bs <= 0 || bs > kMaxBs || n_max <= 0 || n_max > g.block + 1 || kv->max_ctx < 0 || kv->n_pages <= 0 ||
+        kv->max_pages <= 0)
+        return DSPARK_ERR_SHAPE;
+    if (n_max * bs > 224) return DSPARK_ERR_UNSUPPORTED;
+    REQ(x_new);
+    REQ(n_new);
+    REQ(kv->page_table);
+    REQ(kv->ctx_len);
+    for (int l = 0; l < g.n_layers; ++l) REQ(kv->pools[l]);
+    if (!ws) return DSPARK_ERR_WORKSPACE;
+    if (!aligned16(ws)) return DSPARK_ERR_ALIGN;
+    const Layout L = layout_for(h, bs, kv->max_ctx);
+    if (ws_bytes < L.total) return DSPARK_ERR_WORKSPACE;
+    cudaStream_t s = (cudaStream_t)stream;
+    char *w = (char *)ws;
+    int *err = (int *)(w + kCtlErr);
+    const int A = n_max * bs;
+    const int kvd = g.kv_lora + g.d_rope;
+    __nv_bfloat16 *hn = (__nv_bfloat16 *)(w + L.app_hn);
+    float *kvo = (float *)(w + L.app_kv);
+    if (h->c_app_ws != ws || h->c_app_rows != A) {
+        if (!make_map(&h->b_app, hn, A, g.hidden, bn_for(A))) return DSPARK_ERR_CUDA;
+        h->c_app_ws = ws;
+        h->c_app_rows = A;
+    }
+    const int cap = kv->max_pages * g.page_size;
+    for (int l = 0; l < g.n_layers; ++l) {
+        const dspark_layer_weights_t &W = h->w.layers[l];
+        RUN(launch_rmsnorm(x_new, g.hidden, W.attn_norm, g.hidden, g.eps, hn, g.hidden, nullptr, 0, A, err, s));
+        RUN(gemm(h, h->kva[l], nullptr, h->b_app, kvd, g.hidden, A, EPI_STORE, kvo, nullptr, kvd, ws, s));
+        RUN(launch_kv_scatter(kvo, g.kv_lora, g.d_rope, W.kv_a_norm, g.eps, h->rope, n_new, n_max, kv->ctx_len,
+                              kv->page_table, kv->max_pages, g.page_size, kv->n_pages, cap,
+                              (__nv_bfloat16 *)kv->pools[l], bs, err, s));
+    }
+    // the append is the one call that advances ctx_len (documented in the header)
+    RUN(launch_ctx_advance(const_cast<int32_t *>(kv->ctx_len), n_new, n_max, cap, bs, err, s));
+    return DSPARK_OK;
 }
 
 dspark_status dspark_confidence(dspark_handle_t *h, const float *h_out, float *conf, int bs, void *stream) {

@@ -43,6 +43,16 @@ cudaError_t launch_v_absorb(const float *o_lat, int M, int n_h, int d_nope, int 
 bool attention_supported(int dqk, int dv);
 cudaError_t launch_attention(const AttnParams &p, int bs, int dqk, int dv, cudaStream_t st);
 cudaError_t launch_attn_combine(const AttnParams &p, int bs, int dv, cudaStream_t st);
+// Latent-cache append: rows b * n_max + j (j < n_new[b]) of kv [*, kv_lora + d_rope]
+// become [RMSNorm(c_kv) * g || RoPE(k_r, ctx_len[b] + j)] bf16 in the page pool;
+// then ctx_len[b] += n_new[b]. Positions at or beyond cap, invalid pages and
+// n_new outside [0, n_max] are reported (DSPARK_ERR_OOB) and not written.
+cudaError_t launch_kv_scatter(const float *kv, int kv_lora, int d_rope, const float *g_kv, float eps,
+                              const RopeTable &rt, const int32_t *n_new, int n_max, const int32_t *ctx_len,
+                              const int32_t *page_table, int max_pages, int page, int n_pages, int cap,
+                              __nv_bfloat16 *pool, int bs, int *err, cudaStream_t st);
+cudaError_t launch_ctx_advance(int32_t *ctx_len, const int32_t *n_new, int n_max, int cap, int bs, int *err,
+                               cudaStream_t st);
 // Tensor-core attention (latent 512 + rope 64): pool_map views one layer's page
 // pool as bf16 [n_pages * 64, dqk], blk_map the block latents [bs * block, dqk],
 // both with 64 x 64 boxes in the 128-byte swizzle.

@@ -655,6 +655,73 @@ __global__ void confidence_kernel(const float *__restrict__ h_out, int H, const 
 }
 
 // ---------------------------------------------------------------------------
+// Latent-cache append of newly verified tokens: per layer the kv_a projection of
+// their context features (a GEMM before this kernel) becomes the cache entry
+// [RMSNorm(c_kv) * g || RoPE(k_r, pos)] -- the layout the layer forms for its own
+// block rows -- written at pos = ctx_len + j through the page table. One CTA per
+// (token slot, sequence); slots j >= n_new[b] write nothing.
+// ---------------------------------------------------------------------------
+__global__ void kv_scatter_kernel(const float *__restrict__ kv, int kv_lora, int d_rope,
+                                  const float *__restrict__ g_kv, float eps, RopeTable rt,
+                                  const int32_t *__restrict__ n_new, int n_max, const int32_t *__restrict__ ctx_len,
+                                  const int32_t *__restrict__ page_table, int max_pages, int page, int n_pages, int cap,
+                                  __nv_bfloat16 *__restrict__ pool, int *err) {
+    pdl_trigger();
+    pdl_wait();
+    __shared__ float red[33];
+    const int j = blockIdx.x, b = blockIdx.y;
+    const int kvd = kv_lora + d_rope;
+    const int n = n_new[b];
+    if (n < 0 || n > n_max) {
+        if (threadIdx.x == 0 && j == 0) set_error(err, DSPARK_ERR_OOB);
+        return;
+    }
+    if (j >= n) return;
+    const int c = ctx_len[b];
+    const int pos = c + j;
+    if (c < 0 || pos >= cap) {
+        if (threadIdx.x == 0) set_error(err, DSPARK_ERR_OOB);
+        return;
+    }
+    const int pg = page_table[(size_t)b * max_pages + pos / page];
+    if (pg < 0 || pg >= n_pages) {
+        if (threadIdx.x == 0) set_error(err, DSPARK_ERR_OOB);
+        return;
+    }
+    const float *row = kv + ((size_t)b * n_max + j) * kvd;
+    float ss = 0.f;
+    for (int i = threadIdx.x; i < kv_lora; i += blockDim.x) ss += row[i] * row[i];
+    ss = block_sum(ss, red);
+    if (!isfinite(ss) && threadIdx.x == 0) set_error(err, DSPARK_ERR_BAD_INPUT);
+    const float r = rsqrtf(ss / (float)kv_lora + eps);
+    __nv_bfloat16 *dst = pool + ((size_t)pg * page + pos % page) * kvd;
+    for (int i = threadIdx.x; i < kv_lora; i += blockDim.x) dst[i] = __float2bfloat16(row[i] * r * g_kv[i]);
+    for (int q = threadIdx.x; q < d_rope / 2; q += blockDim.x) {
+        float fc, fs;
+        rope_cs((double)pos, rt.inv_freq[q], fc, fs);
+        const float x0 = row[kv_lora + 2 * q], x1 = row[kv_lora + 2 * q + 1];
+        dst[kv_lora + 2 * q] = __float2bfloat16(x0 * fc - x1 * fs);
+        dst[kv_lora + 2 * q + 1] = __float2bfloat16(x0 * fs + x1 * fc);
+    }
+}
+
+// ctx_len[b] += n_new[b] once every layer's entries are written (a sequence whose
+// new length would pass the capacity keeps its length; the error is reported).
+__global__ void ctx_advance_kernel(int32_t *__restrict__ ctx_len, const int32_t *__restrict__ n_new, int n_max,
+                                   int cap, int bs, int *err) {
+    pdl_trigger();
+    pdl_wait();
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= bs) return;
+    const int n = n_new[b], c = ctx_len[b];
+    if (n < 0 || n > n_max || c < 0 || c + n > cap) {
+        set_error(err, DSPARK_ERR_OOB);
+        return;
+    }
+    ctx_len[b] = c + n;
+}
+
+// ---------------------------------------------------------------------------
 // Host-side launch wrappers
 // ---------------------------------------------------------------------------
 cudaError_t launch_rmsnorm(const float *x, int ldx, const float *g, int H, float eps, __nv_bfloat16 *y, int ldy,
@@ -727,6 +794,19 @@ cudaError_t launch_attention(const AttnParams &p, int bs, int dqk, int dv, cudaS
 cudaError_t launch_attn_combine(const AttnParams &p, int bs, int dv, cudaStream_t st) {
     return launch_pdl(attn_combine_kernel, dim3(p.R, bs), dim3(128), 0, st, p.part_o, p.part_ml, p.splits, p.R, dv,
                       p.o_lat);
+}
+
+cudaError_t launch_kv_scatter(const float *kv, int kv_lora, int d_rope, const float *g_kv, float eps,
+                              const RopeTable &rt, const int32_t *n_new, int n_max, const int32_t *ctx_len,
+                              const int32_t *page_table, int max_pages, int page, int n_pages, int cap,
+                              __nv_bfloat16 *pool, int bs, int *err, cudaStream_t st) {
+    return launch_pdl(kv_scatter_kernel, dim3(n_max, bs), dim3(128), 0, st, kv, kv_lora, d_rope, g_kv, eps, rt, n_new,
+                      n_max, ctx_len, page_table, max_pages, page, n_pages, cap, pool, err);
+}
+
+cudaError_t launch_ctx_advance(int32_t *ctx_len, const int32_t *n_new, int n_max, int cap, int bs, int *err,
+                               cudaStream_t st) {
+    return launch_pdl(ctx_advance_kernel, dim3((bs + 31) / 32), dim3(32), 0, st, ctx_len, n_new, n_max, cap, bs, err);
 }
 
 cudaError_t launch_confidence(const float *h_out, int H, const float *w, float bias, float *conf, int M,

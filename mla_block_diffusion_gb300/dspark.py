@@ -23,7 +23,7 @@ STATUS = {0: "OK", 1: "ERR_NULL", 2: "ERR_ALIGN", 3: "ERR_SHAPE", 4: "ERR_UNSUPP
           6: "ERR_WORKSPACE", 16: "ERR_TIMEOUT", 17: "ERR_BAD_INPUT", 18: "ERR_OOB"}
 EXPORTS = ("dspark_create", "dspark_destroy", "dspark_workspace_bytes", "dspark_fuse_ctx", "dspark_draft_block",
            "dspark_markov_rollout", "dspark_confidence", "dspark_verify", "dspark_check", "dspark_status_str",
-           "dspark_fuse_ctx_noalloc")
+           "dspark_fuse_ctx_noalloc", "dspark_kv_append")
 
 
 class Geom(C.Structure):
@@ -88,6 +88,7 @@ def lib():
         L.dspark_verify.argtypes = [vp, vp, vp, vp, C.POINTER(Sample), vp, vp, i, vp, sz, vp]
         L.dspark_check.argtypes = [vp, vp, vp]
         L.dspark_fuse_ctx_noalloc.argtypes = [vp, vp, vp, i, vp]
+        L.dspark_kv_append.argtypes = [vp, vp, i, vp, C.POINTER(KV), i, vp, sz, vp]
         L.dspark_status_str.argtypes = [i]
         L.dspark_status_str.restype = C.c_char_p
         for f in EXPORTS:
@@ -198,6 +199,8 @@ class DSpark:
     def make_kv(self, pools: Sequence[torch.Tensor], page_table: torch.Tensor, ctx_len: torch.Tensor,
                 max_ctx: int) -> KV:
         kv = KV()
+        # the struct holds raw device pointers: keep the tensors alive as long as it lives
+        kv._keep = (list(pools), page_table, ctx_len)
         for l, t in enumerate(pools):
             kv.pools[l] = t.data_ptr()
         kv.n_pages = int(pools[0].shape[0])
@@ -223,6 +226,13 @@ class DSpark:
         _chk("dspark_verify", lib().dspark_verify(self.h, _p(target_logits), _p(ell), _p(tokens), C.byref(sample),
                                                    _p(accept_len), _p(out_tokens), bs, _p(self.ws), self.ws_bytes,
                                                    _stream()))
+
+    def kv_append(self, x_new: torch.Tensor, n_new: torch.Tensor, kv: KV, bs: int):
+        """Write the latent entries of newly verified tokens (x_new [bs, n_max, H]) into every
+        layer's page pool at ctx_len + j, then advance ctx_len by n_new (device, in place)."""
+        n_max = int(x_new.shape[1])
+        _chk("dspark_kv_append", lib().dspark_kv_append(self.h, _p(x_new), n_max, _p(n_new), C.byref(kv), bs,
+                                                         _p(self.ws), self.ws_bytes, _stream()))
 
     def check(self) -> int:
         """Synchronise and return (and clear) the device error word."""
