@@ -55,8 +55,8 @@ def algorithmic_bytes(G, ctx: int, bs: int = 1, fmt: str = "bf16"):
     c = G.param_counts()
     qn = c["quantised"]
     q_rows = G.hidden + G.n_layers * (G.n_heads * G.q_head_dim + G.hidden + 2 * G.inter + G.hidden)
-    per = {"bf16": 2.0, "fp8": 1.0, "nvfp4": 0.5 + 1.0 / 16}[fmt]
-    extra = {"bf16": 0, "fp8": 4 * q_rows, "nvfp4": 0}[fmt]
+    per = {"bf16": 2.0, "fp8": 1.0, "nvfp4": 0.5 + 1.0 / 16, "mxfp4": 0.5 + 1.0 / 32}[fmt]
+    extra = {"bf16": 0, "fp8": 4 * q_rows, "nvfp4": 0, "mxfp4": 0}[fmt]
     w_bf16 = 2 * (c["fc"] + G.n_layers * mats + c["lm_head"] + G.rank * G.vocab + G.block * G.rank) \
         - int(2 * qn) + int(per * qn) + extra
     w_f32 = 4 * (G.n_layers * lp["norms"] + 2 * G.hidden)
@@ -210,20 +210,21 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--lm-rows", type=int, default=4096)
-    ap.add_argument("--only", choices=["fc", "rollout", "layer"], default=None,
+    ap.add_argument("--only", choices=["fc", "rollout", "layer", "append"], default=None,
                     help="time one call alone for profiling: fc (the fusion GEMM; full shape unless --fc-hidden), "
-                         "rollout (Markov rollout, full vocabulary), layer (one full-width MLA layer, ctx 4096)")
+                         "rollout (Markov rollout, full vocabulary), layer (one full-width MLA layer, ctx 4096), "
+                         "append (latent-cache append of 8 verified tokens, all 5 layers, full hidden/latent)")
     ap.add_argument("--fc-hidden", type=int, default=0, help="--only fc: hidden size (output channels)")
     ap.add_argument("--fc-aux", type=int, default=0, help="--only fc: captured states (K = aux * hidden)")
-    ap.add_argument("--format", choices=["bf16", "fp8", "nvfp4"], default="bf16",
+    ap.add_argument("--format", choices=["bf16", "fp8", "nvfp4", "mxfp4"], default="bf16",
                     help="weight format of fc, q_b, o, gate, up, down (the weight-format sweep workloads)")
-    ap.add_argument("--no-drift", action="store_true", help="--format fp8|nvfp4: skip the drift report")
+    ap.add_argument("--no-drift", action="store_true", help="--format fp8|nvfp4|mxfp4: skip the drift report")
     args = ap.parse_args()
     assert args.warmup >= 3 or args.impl == "reference", "at least 3 warm-up steps"
 
     from synthetic import generate as gen
-    from synthetic.configs import FP8_STEP, FULL_STEP, NVFP4_STEP
-    w = {"bf16": FULL_STEP, "fp8": FP8_STEP, "nvfp4": NVFP4_STEP}[args.format]
+    from synthetic.configs import FP8_STEP, FULL_STEP, MXFP4_STEP, NVFP4_STEP
+    w = {"bf16": FULL_STEP, "fp8": FP8_STEP, "nvfp4": NVFP4_STEP, "mxfp4": MXFP4_STEP}[args.format]
     G = w.geom
     world, rank, local = dist_setup()
     ctx = w.ctx[0]
@@ -235,6 +236,8 @@ def main():
 
     if args.only == "fc":
         return only_fc(args, G, world, rank, local)
+    if args.only == "append":
+        return only_append(args, G, local)
     if args.only in ("rollout", "layer"):
         return only_call(args, G, local)
 
@@ -562,6 +565,52 @@ def only_call(args, G, local):
     torch.cuda.synchronize()
     assert ds.check() == 0
     print(json.dumps({"only": args.only, "avg_call_ms": statistics.mean(a_.elapsed_time(b_) for a_, b_ in evs)}))
+
+
+def only_append(args, G, local):
+    """dspark_kv_append alone: 8 newly verified tokens of one sequence into all layers' page pools,
+    full hidden size and latent width (the other dimensions shrunk; the device holds < 1 GB).
+    Algorithmic bytes: the kv_a rows of every layer's fused q_a || kv_a weights, the context
+    features and the written entries."""
+    from dataclasses import replace
+    import mla_block_diffusion_gb300 as M
+    from mla_block_diffusion_gb300 import build as libbuild
+    from synthetic import generate as gen
+    from synthetic.configs import FULL_STEP
+    libbuild.build()
+    torch.cuda.set_device(local)
+    g = replace(G, inter=64, vocab=128, rank=16)
+    w = replace(FULL_STEP, geom=g)
+    W = gen.make_weights(w, "cuda")
+    I = gen.make_inputs(w, "cuda")
+    ctx0 = I["ctx_list"][0]
+    n = g.block + 1
+    P = g.page_size
+    # one spare page after the sequence's pages
+    table = torch.cat([I["page_table"], torch.full((1, 1), I["n_pages"], dtype=torch.int32, device="cuda")], dim=1)
+    pools = [torch.cat([p, torch.zeros((1, P, g.kv_dim), dtype=p.dtype, device="cuda")]) for p in I["kv_pools"]]
+    ctx = torch.tensor([ctx0], dtype=torch.int32, device="cuda")
+    ds = M.DSpark(g, W, max_bs=1, max_ctx=ctx0 + n)
+    kv = ds.make_kv(pools, table, ctx, ctx0 + n)
+    x_new = gen.normal((1, n, g.hidden), 1.0, 7, "x_new", "cuda").float()
+    n_new = torch.tensor([n], dtype=torch.int32, device="cuda")
+    times = []
+    for k in range(args.warmup + args.steps):
+        ctx.fill_(ctx0)
+        a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a_.record()
+        ds.kv_append(x_new, n_new, kv, 1)
+        b_.record()
+        torch.cuda.synchronize()
+        if k >= args.warmup:
+            times.append(a_.elapsed_time(b_))
+    assert ds.check() == 0 and int(ctx.item()) == ctx0 + n
+    ms = statistics.median(times)
+    nbytes = g.n_layers * (g.kv_dim * g.hidden * 2 + n * g.kv_dim * 2) + n * g.hidden * 4
+    pk, src = peaks()
+    print(json.dumps({"only": "append", "tokens": n, "layers": g.n_layers, "median_call_ms": ms,
+                      "algorithmic_bytes": nbytes, "achieved_GBps": nbytes / (ms * 1e-3) / 1e9,
+                      "peak_GBps": pk["hbm_gbs"], "peak_source": src}))
 
 
 def ds_layout_splits(ds) -> int:

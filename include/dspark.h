@@ -47,12 +47,13 @@ typedef enum {
     DSPARK_ERR_CUDA = 5,          /* a CUDA runtime or driver call failed */
     DSPARK_ERR_WORKSPACE = 6,     /* workspace pointer null or smaller than required */
     DSPARK_ERR_TIMEOUT = 16,      /* device: a bounded inter-CTA wait expired */
-    DSPARK_ERR_BAD_INPUT = 17,    /* device: a logit or intermediate was not finite, or an
-                                     activation entering an FP8/NVFP4 GEMM exceeded 65504 */
+    DSPARK_ERR_BAD_INPUT = 17,    /* device: a logit or intermediate was not finite, an
+                                     activation entering an FP8/NVFP4/MXFP4 GEMM exceeded
+                                     65504, or an MXFP4 scale lies outside 2^-22 .. 2^13 */
     DSPARK_ERR_OOB = 18           /* device: page id, token id or ctx_len out of range */
 } dspark_status;
 
-enum { DSPARK_FMT_BF16 = 0, DSPARK_FMT_FP8 = 1, DSPARK_FMT_NVFP4 = 2 };
+enum { DSPARK_FMT_BF16 = 0, DSPARK_FMT_FP8 = 1, DSPARK_FMT_NVFP4 = 2, DSPARK_FMT_MXFP4 = 3 };
 enum { DSPARK_GREEDY = 0, DSPARK_PROBABILISTIC = 1 };
 
 /*
@@ -65,9 +66,10 @@ enum { DSPARK_GREEDY = 0, DSPARK_PROBABILISTIC = 1 };
  * (160, 128), (80, 64); q_lora + kv_lora <= 8192; d_nope <= 256; d_rope a
  * multiple of 4 and <= 128; block <= 16;
  * rank <= 256; vocab even and < 2^18; page_size 64; weight_format BF16, FP8
- * (E4M3 per output row) or NVFP4 (E2M1, E4M3 group-16 scales, global scale;
- * then hidden, q_lora, n_heads*d_v and inter multiples of 256). With FP8 or
- * NVFP4, block * bs <= 64 per call and the activations entering those GEMMs
+ * (E4M3 per output row), NVFP4 (E2M1, E4M3 group-16 scales, global scale;
+ * then hidden, q_lora, n_heads*d_v and inter multiples of 256) or MXFP4 (E2M1,
+ * E8M0 power-of-two scales per 32 inputs; then those sizes multiples of 512).
+ * With FP8, NVFP4 or MXFP4, block * bs <= 64 per call and the activations entering those GEMMs
  * stay within +-65504 (they are taken in f16; see DSPARK_ERR_BAD_INPUT).
  */
 typedef struct {
@@ -86,7 +88,9 @@ typedef struct {
 /* One quantisable matrix: bf16 data, or FP8 E4M3 data [out,in] + fp32 scale
  * [out], or NVFP4 packed E2M1 data [out,in/2] + E4M3 scales [out,in/16] + a
  * global fp32 scale ([P3] "What is quantized to what": MLP, o_proj, q_b_proj,
- * context_proj; group 16 with E4M3 scales). */
+ * context_proj; group 16 with E4M3 scales), or MXFP4 packed E2M1 data
+ * [out,in/2] + E8M0 scale bytes [out,in/32] (2^(byte - 127); the global scale
+ * is ignored). Packed codes: the even input in the low nibble. */
 typedef struct {
     const void *data;
     const void *scale;

@@ -98,6 +98,11 @@ bool make_qmat(QMat *q, const dspark_mat_t &m, int fmt, uint64_t rows, uint64_t 
                make_map_u8(&q->scales, m.data, rows, cols, 128, 64, true);
     }
     q->rowscale = nullptr;
+    if (fmt == DSPARK_FMT_MXFP4) {
+        q->gscale = 1.f;
+        return make_map_u8(&q->data, m.data, rows, cols / 2, 128, 64, true) &&
+               make_map_u8(&q->scales, m.scale, rows, cols / 32, 16, 64, false);
+    }
     q->gscale = m.global_scale;
     return make_map_u8(&q->data, m.data, rows, cols / 2, 128, 64, true) &&
            make_map_u8(&q->scales, m.scale, rows, cols / 16, 16, 64, false);
@@ -308,10 +313,14 @@ cudaError_t gemm_q(const dspark_handle *h, const QMat &A, const QMat *A2, const 
         if (bn == 16) return gemm_q_t<16, DSPARK_FMT_FP8>(A, A2, B, p, h->num_sms, st);
         if (bn == 32) return gemm_q_t<32, DSPARK_FMT_FP8>(A, A2, B, p, h->num_sms, st);
         if (bn == 64) return gemm_q_t<64, DSPARK_FMT_FP8>(A, A2, B, p, h->num_sms, st);
-    } else {
+    } else if (h->g.weight_format == DSPARK_FMT_NVFP4) {
         if (bn == 16) return gemm_q_t<16, DSPARK_FMT_NVFP4>(A, A2, B, p, h->num_sms, st);
         if (bn == 32) return gemm_q_t<32, DSPARK_FMT_NVFP4>(A, A2, B, p, h->num_sms, st);
         if (bn == 64) return gemm_q_t<64, DSPARK_FMT_NVFP4>(A, A2, B, p, h->num_sms, st);
+    } else {
+        if (bn == 16) return gemm_q_t<16, DSPARK_FMT_MXFP4>(A, A2, B, p, h->num_sms, st);
+        if (bn == 32) return gemm_q_t<32, DSPARK_FMT_MXFP4>(A, A2, B, p, h->num_sms, st);
+        if (bn == 64) return gemm_q_t<64, DSPARK_FMT_MXFP4>(A, A2, B, p, h->num_sms, st);
     }
     return cudaErrorInvalidValue;
 }
@@ -328,7 +337,12 @@ dspark_status check_geom(const dspark_geom_t *g) {
         return DSPARK_ERR_UNSUPPORTED;
     if (!attention_supported(g->kv_lora + g->d_rope, g->kv_lora)) return DSPARK_ERR_UNSUPPORTED;
     if (g->weight_format != DSPARK_FMT_BF16 && g->weight_format != DSPARK_FMT_FP8 &&
-        g->weight_format != DSPARK_FMT_NVFP4)
+        g->weight_format != DSPARK_FMT_NVFP4 && g->weight_format != DSPARK_FMT_MXFP4)
+        return DSPARK_ERR_UNSUPPORTED;
+    // MXFP4 stages cover 512 inputs (16 scale bytes per row: whole 16-byte TMA boxes)
+    if (g->weight_format == DSPARK_FMT_MXFP4 &&
+        ((g->n_aux * g->hidden) % 512 || g->q_lora % 512 || (g->n_heads * g->d_v) % 512 || g->hidden % 512 ||
+         g->inter % 512))
         return DSPARK_ERR_UNSUPPORTED;
     // NVFP4 group-scale rows (in / 16 bytes) must be whole 16-byte TMA strides
     if (g->weight_format == DSPARK_FMT_NVFP4 &&

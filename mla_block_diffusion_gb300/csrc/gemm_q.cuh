@@ -36,12 +36,20 @@ struct QFmt;
 template <>
 struct QFmt<DSPARK_FMT_FP8> {
     static constexpr int kKR = 128;          // k per raw stage (128 bytes per row)
+    static constexpr int kDataBytes = 128 * 128;
     static constexpr int kScaleBytes = 0;
 };
 template <>
 struct QFmt<DSPARK_FMT_NVFP4> {
     static constexpr int kKR = 256;          // k per raw stage (128 bytes of packed codes per row)
+    static constexpr int kDataBytes = 128 * 128;
     static constexpr int kScaleBytes = 128 * 16;  // 16 group scales per row
+};
+template <>
+struct QFmt<DSPARK_FMT_MXFP4> {
+    static constexpr int kKR = 512;          // k per raw stage (256 bytes of packed codes per row, two halves)
+    static constexpr int kDataBytes = 2 * 128 * 128;
+    static constexpr int kScaleBytes = 128 * 16;  // 16 power-of-two scales (groups of 32) per row
 };
 
 constexpr int kQConvThreads = 256;
@@ -50,7 +58,7 @@ template <int BN, int FMT>
 struct GemmQCfg {
     static constexpr int kKR = QFmt<FMT>::kKR;
     static constexpr int kNSub = kKR / 64;
-    static constexpr int kDataBytes = 128 * 128;
+    static constexpr int kDataBytes = QFmt<FMT>::kDataBytes;
     static constexpr int kScaleBytes = QFmt<FMT>::kScaleBytes;
     static constexpr int kBBytes = BN * 128;
     static constexpr int kRawBytes = kDataBytes + kScaleBytes + kNSub * kBBytes;
@@ -64,7 +72,7 @@ struct GemmQCfg {
     static constexpr int kRawStages = kRawFit > 12 ? 12 : kRawFit;
     static constexpr int kSmemBytes = kFixed + kRawStages * kRawBytes;
     static constexpr int kThreads = 192 + kQConvThreads;
-    static_assert(kRawStages >= 3 && kAStages >= 4, "rings too shallow");
+    static_assert(kRawStages >= 2 && kRawStages * kKR >= 384 && kAStages >= 4, "rings too shallow");
     static_assert(kRawBytes % 1024 == 0, "1024-byte stage alignment");
 };
 
@@ -88,8 +96,22 @@ DS_DEVINL uint32_t mul_f16x2(uint32_t a, uint32_t b) {
 DS_DEVINL uint32_t sw128_off(int r, int c) { return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4)); }
 
 // Row r of sub-block sb (64 k) of a raw stage, decoded to 32 f16 pairs (even k low).
+// 2^(e - 127) of an E8M0 scale as an f16 pair, for e - 127 in [-22, 13], where
+// every E2M1 value times the scale is exact in f16; other scales set *bad.
+DS_DEVINL uint32_t e8m0_to_f16x2(uint32_t e, bool &bad) {
+    const int k = (int)e - 127;
+    uint32_t h;
+    if (k < -22 || k > 13) {
+        bad = true;
+        h = 0u;
+    } else {
+        h = k >= -14 ? (uint32_t)(k + 15) << 10 : 1u << (k + 24);
+    }
+    return h * 0x10001u;
+}
+
 template <int FMT>
-DS_DEVINL void convert_row(const uint8_t *raw, int sb, int r, uint32_t (&o)[32]) {
+DS_DEVINL void convert_row(const uint8_t *raw, int sb, int r, uint32_t (&o)[32], bool &bad) {
     if (FMT == DSPARK_FMT_FP8) {
         // 128 E4M3 codes per row in 8 swizzled 16-byte chunks; sub-block sb = chunks 4sb..4sb+3
 #pragma unroll
@@ -100,6 +122,24 @@ DS_DEVINL void convert_row(const uint8_t *raw, int sb, int r, uint32_t (&o)[32])
             for (int t = 0; t < 4; ++t) {
                 o[8 * c + 2 * t] = e4m3x2_to_f16x2(w[t] & 0xFFFFu);
                 o[8 * c + 2 * t + 1] = e4m3x2_to_f16x2(w[t] >> 16);
+            }
+        }
+    } else if (FMT == DSPARK_FMT_MXFP4) {
+        // 512 E2M1 codes per row: two halves of 256 (128 bytes, 8 swizzled chunks of 32
+        // codes each); sub-block sb = half sb / 4, chunks 2 (sb % 4), +1; 16 E8M0 scales per
+        // row (one per 32 codes) follow the data
+        const uint8_t *half = raw + (sb >> 2) * (128 * 128);
+        const uint8_t *scales = raw + 2 * 128 * 128 + r * 16 + 2 * sb;
+        const uint32_t sg[2] = {e8m0_to_f16x2(scales[0], bad), e8m0_to_f16x2(scales[1], bad)};
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            const uint4 v = *(const uint4 *)(half + sw128_off(r, 2 * (sb & 3) + c));
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+#pragma unroll
+                for (int bt = 0; bt < 4; ++bt)
+                    o[16 * c + 4 * t + bt] = mul_f16x2(e2m1x2_to_f16x2((w[t] >> (8 * bt)) & 0xFFu), sg[c]);
             }
         }
     } else {
@@ -199,7 +239,7 @@ __global__ void __launch_bounds__(GemmQCfg<BN, FMT>::kThreads, 1)
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmA2);
         tma_prefetch_desc(&tmB);
-        if (FMT == DSPARK_FMT_NVFP4) {
+        if (FMT != DSPARK_FMT_FP8) {
             tma_prefetch_desc(&tmS);
             tma_prefetch_desc(&tmS2);
         }
@@ -217,9 +257,13 @@ __global__ void __launch_bounds__(GemmQCfg<BN, FMT>::kThreads, 1)
         const int row0 = p.paired ? tile * 64 : tile * 128;
         const int row1 = p.paired ? tile * 64 : tile * 128 + 64;
         const CUtensorMap *m1 = p.paired ? &tmA2 : &tmA;
-        tma_load_2d_hint(raw, &tmA, kr * 128, row0, &raw_full[s], pol);
-        tma_load_2d_hint(raw + 8192, m1, kr * 128, row1, &raw_full[s], pol);
-        if (FMT == DSPARK_FMT_NVFP4) {
+        tma_load_2d_hint(raw, &tmA, kr * (C::kDataBytes / 128), row0, &raw_full[s], pol);
+        tma_load_2d_hint(raw + 8192, m1, kr * (C::kDataBytes / 128), row1, &raw_full[s], pol);
+        if (FMT == DSPARK_FMT_MXFP4) {  // second half of the 256 packed bytes per row
+            tma_load_2d_hint(raw + 16384, &tmA, kr * 256 + 128, row0, &raw_full[s], pol);
+            tma_load_2d_hint(raw + 16384 + 8192, m1, kr * 256 + 128, row1, &raw_full[s], pol);
+        }
+        if (FMT != DSPARK_FMT_FP8) {
             const CUtensorMap *n1 = p.paired ? &tmS2 : &tmS;
             tma_load_2d_hint(raw + C::kDataBytes, &tmS, kr * 16, row0, &raw_full[s], pol);
             tma_load_2d_hint(raw + C::kDataBytes + 1024, n1, kr * 16, row1, &raw_full[s], pol);
@@ -324,7 +368,9 @@ __global__ void __launch_bounds__(GemmQCfg<BN, FMT>::kThreads, 1)
             if (!named_bar_and(3 + g, kQConvThreads / 2, got && !s_abort)) break;
             uint32_t v[32];
             uint8_t *rawp = sRaw + s * C::kRawBytes;
-            convert_row<FMT>(rawp, sb, r, v);
+            bool bad_scale = false;
+            convert_row<FMT>(rawp, sb, r, v, bad_scale);
+            if (bad_scale) set_error(p.err, DSPARK_ERR_BAD_INPUT);
             bf16_tile_to_f16<BN>(rawp + C::kDataBytes + C::kScaleBytes + sb * C::kBBytes, gthr, p.err);
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             tc_fence_after();

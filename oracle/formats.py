@@ -11,6 +11,10 @@ decoded (dequantised) weights.
 * NVFP4 weight-only ("Kimi-K3-DSpark-NVFP4", header: group-16, E4M3 group scales,
   weight-only): w = E2M1(q) * E4M3(s_group) * global; two codes per byte, the even
   element in the low nibble.
+* MXFP4 weight-only (the cards' third format, "Kimi-K3-DSpark-NVFP4", Measurement:
+  the MXFP4 column; its encoding is the OCP Microscaling v1.0 MXFP4 element type):
+  w = E2M1(q) * 2^(s_group - 127) with an E8M0 scale byte per group of 32 inputs
+  (255 is NaN); two codes per byte, the even element in the low nibble.
 """
 from __future__ import annotations
 
@@ -57,3 +61,26 @@ def dequant_nvfp4(packed: np.ndarray, scales: np.ndarray, global_scale: float) -
     codes[:, 1::2] = packed >> 4
     s = E4M3_TABLE[np.asarray(scales, dtype=np.uint8)]           # [out, in/16]
     return E2M1_TABLE[codes] * np.repeat(s, 16, axis=1) * float(global_scale)
+
+
+def e8m0_value(code: int) -> float:
+    """E8M0 scale: 2^(code - 127); code 255 is NaN."""
+    code = int(code) & 0xFF
+    if code == 0xFF:
+        return float("nan")
+    return 2.0 ** (code - 127)
+
+
+E8M0_TABLE = np.array([e8m0_value(c) for c in range(256)], dtype=np.float64)
+
+
+def dequant_mxfp4(packed: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """packed uint8 [out, in/2] (even element low nibble), scales uint8 [out, in/32]."""
+    packed = np.asarray(packed, dtype=np.uint8)
+    out_f, half = packed.shape
+    codes = np.empty((out_f, 2 * half), dtype=np.uint8)
+    codes[:, 0::2] = packed & 0xF
+    codes[:, 1::2] = packed >> 4
+    vals = E2M1_TABLE[codes]
+    s = E8M0_TABLE[np.asarray(scales, dtype=np.uint8)]
+    return vals * np.repeat(s, 32, axis=1)

@@ -28,6 +28,7 @@ PURPOSE_BONUS = 4
 FORMAT_BF16 = 0
 FORMAT_FP8 = 1
 FORMAT_NVFP4 = 2
+FORMAT_MXFP4 = 3
 
 
 @dataclass(frozen=True)
@@ -151,5 +152,7 @@ FP8_STEP = Workload("full_bs1_ctx4096_fp8", FULL, bs=1, ctx=(4096,), weight_seed
                     weight_format=FORMAT_FP8)
 NVFP4_STEP = Workload("full_bs1_ctx4096_nvfp4", FULL, bs=1, ctx=(4096,), weight_seed=1,
                       input_seed=5, weight_format=FORMAT_NVFP4)
+MXFP4_STEP = Workload("full_bs1_ctx4096_mxfp4", FULL, bs=1, ctx=(4096,), weight_seed=1,
+                      input_seed=5, weight_format=FORMAT_MXFP4)
 
-WORKLOADS = {w.name: w for w in (TINY_STEP, FULL_STEP, LONG_STEP, BATCH_STEP, FP8_STEP, NVFP4_STEP)}
+WORKLOADS = {w.name: w for w in (TINY_STEP, FULL_STEP, LONG_STEP, BATCH_STEP, FP8_STEP, NVFP4_STEP, MXFP4_STEP)}

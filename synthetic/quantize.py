@@ -1,4 +1,4 @@
-"""Weight-only FP8 / NVFP4 versions of the seeded bf16 weights (input preparation).
+"""Weight-only FP8 / NVFP4 / MXFP4 versions of the seeded bf16 weights (input preparation).
 
 The model cards ship FP8 and NVFP4 artefacts of the drafter ("Kimi-K3-DSpark-NVFP4":
 "compressed-tensors nvfp4-pack-quantized, group-16, E4M3 group scales, weight-only";
@@ -67,6 +67,23 @@ def quant_nvfp4(w: torch.Tensor) -> Tuple[torch.Tensor, torch.Tensor, float]:
     return packed.contiguous(), s.view(torch.uint8).contiguous(), float(g)
 
 
+def quant_mxfp4(w: torch.Tensor) -> Tuple[torch.Tensor, torch.Tensor, float]:
+    """bf16 [out, in] -> (packed E2M1 uint8 [out, in/2], E8M0 scale bytes uint8 [out, in/32], 1.0).
+    OCP MX: shared exponent floor(log2(amax_group)) - 2 (the largest E2M1 exponent), elements
+    rounded to the nearest E2M1 value of w / 2^shared (ties to the even code), saturating at 6."""
+    out_f, in_f = w.shape
+    assert in_f % 32 == 0
+    wf = w.to(torch.float64)
+    grp = wf.view(out_f, in_f // 32, 32)
+    amax = grp.abs().amax(dim=2)
+    ex = torch.where(amax > 0, torch.floor(torch.log2(torch.where(amax > 0, amax, torch.ones_like(amax)))) - 2,
+                     torch.full_like(amax, -127.0)).clamp(-127, 127)
+    x = grp / torch.pow(2.0, ex)[..., None]
+    codes = _e2m1_codes(x).view(out_f, in_f)
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).to(torch.uint8)
+    return packed.contiguous(), (ex + 127).to(torch.uint8).contiguous(), 1.0
+
+
 def quantise_weights(W: Dict[str, torch.Tensor], fmt: str, n_layers: int) -> Dict[str, object]:
     """Return a copy of the weight dict where the quantised matrices are replaced by
     (data, scale, global_scale) triples; everything else is shared."""
@@ -78,6 +95,8 @@ def quantise_weights(W: Dict[str, torch.Tensor], fmt: str, n_layers: int) -> Dic
             out[n] = (d, sc, 1.0)
         elif fmt == "nvfp4":
             out[n] = quant_nvfp4(W[n])
+        elif fmt == "mxfp4":
+            out[n] = quant_mxfp4(W[n])
         else:
             raise ValueError(fmt)
     return out

@@ -1,6 +1,9 @@
-"""Weight-only FP8 and NVFP4 through the C ABI against the oracle on the decoded
-weights ("Kimi-K3-DSpark-NVFP4": FP8 per-channel and NVFP4 group-16 weight-only).
-Tolerance: relative L2 <= 3e-2 on hidden states and logits."""
+"""Weight-only FP8, NVFP4 and MXFP4 through the C ABI against the oracle on the
+decoded weights ("Kimi-K3-DSpark-NVFP4": FP8 per-channel and NVFP4 group-16
+weight-only; MXFP4 the cards' third format). Tolerance: relative L2 <= 3e-2 on
+hidden states and logits."""
+from dataclasses import replace
+
 import numpy as np
 import pytest
 import torch
@@ -9,13 +12,14 @@ from oracle import formats as F
 from oracle import network as N
 from synthetic import generate as gen
 from synthetic import quantize as Q
-from synthetic.configs import FORMAT_FP8, FORMAT_NVFP4, TINY_STEP
+from synthetic.configs import FORMAT_FP8, FORMAT_MXFP4, FORMAT_NVFP4, TINY_STEP
 from tests.gpu_harness import MID, workload
 from tests.helpers import f64, rel_l2
 
 pytestmark = pytest.mark.gpu
 TOL = 3e-2
-FMTS = {"fp8": FORMAT_FP8, "nvfp4": FORMAT_NVFP4}
+FMTS = {"fp8": FORMAT_FP8, "nvfp4": FORMAT_NVFP4, "mxfp4": FORMAT_MXFP4}
+MIDMX = replace(MID, q_lora=512)  # every quantised input dimension a multiple of 512
 KEYS = ("attn_norm", "w_qkv_a", "q_a_norm", "kv_a_norm", "w_q_b", "w_kv_b", "w_o", "mlp_norm", "w_gate", "w_up",
         "w_down")
 
@@ -35,6 +39,8 @@ def decode(v, fmt):
     d, sc, g = v
     if fmt == "fp8":
         return F.dequant_fp8(d.cpu().numpy(), sc.cpu().numpy())
+    if fmt == "mxfp4":
+        return F.dequant_mxfp4(d.cpu().numpy(), sc.cpu().numpy())
     return F.dequant_nvfp4(d.cpu().numpy(), sc.cpu().numpy(), g)
 
 
@@ -46,8 +52,9 @@ def to_dev(Wq):
 
 
 @pytest.mark.parametrize("fmt,w", [("fp8", TINY_STEP), ("fp8", workload(MID, 2, (300, 90), seed=9)),
-                                   ("nvfp4", workload(MID, 2, (300, 90), seed=9))],
-                         ids=["fp8_tiny", "fp8_mid", "nvfp4_mid"])
+                                   ("nvfp4", workload(MID, 2, (300, 90), seed=9)),
+                                   ("mxfp4", workload(MIDMX, 2, (300, 90), seed=9))],
+                         ids=["fp8_tiny", "fp8_mid", "nvfp4_mid", "mxfp4_mid"])
 def test_weight_only_draft(M, fmt, w):
     G, bs = w.geom, w.bs
     W = gen.make_weights(w, "cpu")
@@ -101,3 +108,25 @@ def test_activation_beyond_f16_range_is_reported(M):
     assert ds.check() == 17
     ds.fuse_ctx(aux, x, 1)
     assert ds.check() == 0
+
+
+def test_mxfp4_scale_out_of_f16_range_is_reported(M):
+    """An MXFP4 scale below 2^-22 (E8M0 byte 104) cannot be decoded exactly in f16:
+    DSPARK_ERR_BAD_INPUT (17); a clean call afterwards is OK."""
+    w = workload(MIDMX, 1, (64,), seed=9)
+    G = w.geom
+    W = gen.make_weights(w, "cpu")
+    I = gen.make_inputs(w, "cpu")
+    Wq = Q.quantise_weights(W, "mxfp4", G.n_layers)
+    d, sc, g = Wq["w_fc"]
+    bad = sc.clone()
+    bad[0, 0] = 104
+    Wb = dict(Wq)
+    Wb["w_fc"] = (d, bad, g)
+    x = torch.empty(1, G.block, G.hidden, dtype=torch.float32, device="cuda")
+    ds = M.DSpark(G, to_dev(Wb), max_bs=1, weight_format=FORMAT_MXFP4)
+    ds.fuse_ctx(I["aux"].cuda(), x, 1)
+    assert ds.check() == 17
+    ds2 = M.DSpark(G, to_dev(Wq), max_bs=1, weight_format=FORMAT_MXFP4)
+    ds2.fuse_ctx(I["aux"].cuda(), x, 1)
+    assert ds2.check() == 0

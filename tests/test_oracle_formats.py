@@ -57,3 +57,40 @@ def test_quantisation_error_of_gaussian_weights():
     snr = lambda e: 10 * np.log10((ref ** 2).sum() / (e ** 2).sum())
     assert 26 < snr(e8) < 36
     assert 15 < snr(e4) < 25
+
+
+def test_e8m0_scales():
+    assert F.e8m0_value(127) == 1.0
+    assert F.e8m0_value(0) == 2.0 ** -127
+    assert F.e8m0_value(254) == 2.0 ** 127
+    assert F.e8m0_value(130) == 8.0
+    assert np.isnan(F.e8m0_value(255))
+
+
+def test_mxfp4_hand_decoded_row():
+    # 64 inputs: group 0 scale 2^-3, group 1 scale 2^2; codes 1 (0.5) and 0xF (-6) alternate
+    packed = np.full((1, 32), 0xF1, dtype=np.uint8)   # low nibble 1 (even inputs), high nibble 0xF (odd)
+    scales = np.array([[124, 129]], dtype=np.uint8)
+    w = F.dequant_mxfp4(packed, scales)
+    assert w.shape == (1, 64)
+    assert np.all(w[0, 0:32:2] == 0.5 * 2.0 ** -3) and np.all(w[0, 1:32:2] == -6 * 2.0 ** -3)
+    assert np.all(w[0, 32::2] == 0.5 * 4) and np.all(w[0, 33::2] == -6 * 4)
+
+
+def test_mxfp4_round_trip_and_saturation():
+    rng = np.random.default_rng(4)
+    grid = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6])
+    # groups whose largest magnitude is 6 * 2^k: the shared exponent is k and every value survives
+    k = rng.integers(-8, 3, size=(3, 4))
+    vals = rng.choice(grid, size=(3, 4, 32)) * rng.choice([-1, 1], size=(3, 4, 32))
+    vals[..., 0] = 6.0
+    w = (vals * 2.0 ** k[..., None]).reshape(3, 128)
+    d, s, _ = Q.quant_mxfp4(torch.tensor(w, dtype=torch.float64))
+    assert np.array_equal(F.dequant_mxfp4(d.numpy(), s.numpy()), w)
+    # amax 7 * 2^k: shared exponent floor(log2 7) - 2 = 0, so 7 saturates to 6 (the OCP rule)
+    w2 = np.zeros((1, 32))
+    w2[0, 0] = 7.0
+    w2[0, 1] = 0.25
+    d, s, _ = Q.quant_mxfp4(torch.tensor(w2, dtype=torch.float64))
+    out = F.dequant_mxfp4(d.numpy(), s.numpy())
+    assert out[0, 0] == 6.0 and int(s[0, 0]) == 127 and out[0, 1] in (0.0, 0.5)
