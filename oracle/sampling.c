@@ -397,3 +397,228 @@ int oracle_verify_prob(const float *P, const float *ell, const int32_t *tokens, 
     return oracle_verify_prob_core(P, ell, tokens, B, V, draft_greedy, T, top_p, U, Wres, Wb,
                                    accept_len, out_tokens);
 }
+
+/* ---------------------------------------------------------------------------
+ * Block verification ("Kimi-K3-DSpark-NVFP4", Quick Start / Sampling options:
+ * rejection_sample_method "block" verifies the drafted block as a unit; the
+ * method of Sun, Mendlovic, Leviathan, Aharoni, Beirami, Ro, Suresh, "Block
+ * Verification Accelerates Speculative Decoding", 2024). With p(.) the target
+ * rows and q(.) the draft rows of the sampling spec, X_1..X_B the drafted tokens:
+ *   pi_0 = 1, pi_i = min(pi_{i-1} p_{i-1}(X_i) / q_{i-1}(X_i), 1)
+ *   S_i  = sum_x max(pi_i p_i(x) - q_i(x), 0)                (i < B)
+ *   h_i  = S_i / (S_i + 1 - pi_i) (i < B),  h_B = pi_B
+ *   eta_i ~ Bernoulli(h_i) independently, tau = max {i : eta_i = 1} (0 if none)
+ *   emit X_1..X_tau, then a token from max(pi_tau p_tau - q_tau, 0) (tau < B)
+ *   or from p_B (tau = B).
+ * Numerics (the paper gives none): p_i(x) and q_i(x) are the spec's exact
+ * rationals E / S rounded once to double; every mass term is formed in double
+ * (multiply, then subtract, no contraction), truncated to a multiple of 2^-80
+ * and summed exactly in 128 bits, so the sums do not depend on the order of
+ * summation. eta_i = (U_i < h_i * 2^32) with the 32-bit uniform U_i (purpose
+ * 2, position i-1); the final token is drawn like the spec's other draws with
+ * the 24-bit uniform of purpose 3 at position tau (the bonus: purpose 4).
+ * ------------------------------------------------------------------------- */
+static u128 fx80(double x)
+{
+    if (!(x > 0.0)) return 0;
+    uint64_t b;
+    memcpy(&b, &x, 8);
+    const int e = (int)((b >> 52) & 0x7FF);
+    if (e == 0) return 0; /* below 2^-1022 */
+    const uint64_t m = (b & ((1ull << 52) - 1)) | (1ull << 52);
+    const int sh = e - 995; /* x * 2^80 = m * 2^(e - 1075 + 80) */
+    if (sh >= 0) return (u128)m << sh;
+    if (sh <= -53) return 0;
+    return (u128)(m >> (-sh));
+}
+
+/* The value of a 2^-80 fixed-point sum as a double: its top 53 bits, exactly. */
+static double fx80_to_double(u128 s)
+{
+    if (s == 0) return 0.0;
+    const uint64_t hi = (uint64_t)(s >> 64), lo = (uint64_t)s;
+    const int n = hi ? 128 - __builtin_clzll(hi) : 64 - __builtin_clzll(lo);
+    if (n <= 53) return ldexp((double)lo, -80);
+    return ldexp((double)(uint64_t)(s >> (n - 53)), n - 53 - 80);
+}
+
+typedef struct {
+    int B, V, dg;
+    uint64_t *Ep, *Eq;   /* rows 0..B of p, 0..B-1 of q: in-nucleus weights (0 outside) */
+    uint64_t Sp[65], Sq[65];
+    const int32_t *tokens;
+} brows_t;
+
+static double bp(const brows_t *r, int i, int v) { return (double)r->Ep[(size_t)i * r->V + v] / (double)r->Sp[i]; }
+static double bq(const brows_t *r, int i, int v)
+{
+    if (r->dg) return v == r->tokens[i] ? 1.0 : 0.0;
+    return (double)r->Eq[(size_t)i * r->V + v] / (double)r->Sq[i];
+}
+static u128 bmass_term(const brows_t *r, int i, double pi, int v)
+{
+    double d = pi * bp(r, i, v);
+    d = d - bq(r, i, v);
+    return fx80(d);
+}
+static u128 bmass(const brows_t *r, int i, double pi)
+{
+    u128 s = 0;
+    for (int v = 0; v < r->V; ++v) s += bmass_term(r, i, pi, v);
+    return s;
+}
+
+static int brows_load(brows_t *r, const float *P, const float *ell, const int32_t *tokens, int B, int V, int dg,
+                      float T, float top_p)
+{
+    r->B = B;
+    r->V = V;
+    r->dg = dg;
+    r->tokens = tokens;
+    r->Ep = (uint64_t *)malloc(sizeof(uint64_t) * (size_t)(B + 1) * V);
+    r->Eq = (uint64_t *)malloc(sizeof(uint64_t) * (size_t)(B > 0 ? B : 1) * V);
+    if (!r->Ep || !r->Eq) return ERR_ALLOC;
+    for (int i = 0; i < B; ++i)
+        if (tokens[i] < 0 || tokens[i] >= V) return ERR_OOB;
+    for (int i = 0; i <= B; ++i) {
+        uint64_t *E = r->Ep + (size_t)i * V;
+        oracle_nucleus_t nu;
+        int st = oracle_row_weights(P + (size_t)i * V, V, T, E);
+        if (!st) st = oracle_nucleus(E, V, top_p, &nu);
+        if (st) return st;
+        for (int v = 0; v < V; ++v) E[v] = in_nucleus(E, v, nu.kstar);
+        r->Sp[i] = nu.Sn;
+    }
+    for (int i = 0; i < B && !dg; ++i) {
+        uint64_t *E = r->Eq + (size_t)i * V;
+        oracle_nucleus_t nu;
+        int st = oracle_row_weights(ell + (size_t)i * V, V, T, E);
+        if (!st) st = oracle_nucleus(E, V, top_p, &nu);
+        if (st) return st;
+        for (int v = 0; v < V; ++v) E[v] = in_nucleus(E, v, nu.kstar);
+        r->Sq[i] = nu.Sn;
+    }
+    return OK;
+}
+
+static void brows_free(brows_t *r)
+{
+    free(r->Ep);
+    free(r->Eq);
+}
+
+/* pi_0..pi_B and h_1..h_B (h[0] = 0) of one sequence. */
+static void bstats(const brows_t *r, double *pi, double *h)
+{
+    const int B = r->B;
+    pi[0] = 1.0;
+    h[0] = 0.0;
+    for (int i = 1; i <= B; ++i) {
+        const int t = r->tokens[i - 1];
+        const double a = bp(r, i - 1, t), c = bq(r, i - 1, t);
+        if (c == 0.0) {
+            pi[i] = (a > 0.0 && pi[i - 1] > 0.0) ? 1.0 : 0.0;
+        } else {
+            const double x = pi[i - 1] * (a / c);
+            pi[i] = x < 1.0 ? x : 1.0;
+        }
+    }
+    for (int i = 1; i < B; ++i) {
+        const double S = fx80_to_double(bmass(r, i, pi[i]));
+        const double den = S + (1.0 - pi[i]);
+        h[i] = den > 0.0 ? S / den : 0.0;
+    }
+    if (B > 0) h[B] = pi[B];
+}
+
+int oracle_verify_block_stats(const float *P, const float *ell, const int32_t *tokens, int B, int V,
+                              int draft_greedy, float T, float top_p, double *pi, double *h)
+{
+    if (B > 64) return ERR_OOB;
+    brows_t r;
+    int st = brows_load(&r, P, ell, tokens, B, V, draft_greedy, T, top_p);
+    if (!st) bstats(&r, pi, h);
+    brows_free(&r);
+    return st;
+}
+
+/* Residual weights at position i for the given pi (2^-80 fixed point, as lo/hi words). */
+int oracle_block_residual_weights(const float *P, const float *ell, const int32_t *tokens, int B, int V,
+                                  int draft_greedy, float T, float top_p, int i, double pi, uint64_t *w)
+{
+    if (B > 64 || i < 0 || i >= B) return ERR_OOB;
+    brows_t r;
+    int st = brows_load(&r, P, ell, tokens, B, V, draft_greedy, T, top_p);
+    if (!st)
+        for (int v = 0; v < V; ++v) {
+            const u128 x = bmass_term(&r, i, pi, v);
+            w[2 * v] = (uint64_t)x;
+            w[2 * v + 1] = (uint64_t)(x >> 64);
+        }
+    brows_free(&r);
+    return st;
+}
+
+int oracle_verify_block_core(const float *P, const float *ell, const int32_t *tokens, int B, int V,
+                             int draft_greedy, float T, float top_p, const uint32_t *U, const uint32_t *Wres,
+                             uint32_t Wbonus, int32_t *accept_len, int32_t *out_tokens)
+{
+    if (B > 64) return ERR_OOB;
+    for (int i = 0; i <= B; ++i) out_tokens[i] = -1;
+    brows_t r;
+    int st = brows_load(&r, P, ell, tokens, B, V, draft_greedy, T, top_p);
+    if (st) {
+        brows_free(&r);
+        return st;
+    }
+    double pi[65], h[65];
+    bstats(&r, pi, h);
+    int tau = 0;
+    for (int i = 1; i <= B; ++i)
+        if ((double)U[i - 1] < h[i] * 4294967296.0) tau = i;
+    for (int i = 0; i < tau; ++i) out_tokens[i] = tokens[i];
+    *accept_len = tau;
+    if (tau == B) {
+        int32_t bonus;
+        st = draw_from_logits(P + (size_t)B * V, V, T, top_p, Wbonus, r.Ep, &bonus);
+        if (!st) out_tokens[B] = bonus;
+    } else {
+        const u128 R = bmass(&r, tau, pi[tau]);
+        const uint32_t W = Wres[tau] & 0xFFFFFFu;
+        if (R == 0) {
+            /* no residual mass left at 2^-80 resolution: draw from the target row */
+            int32_t pick;
+            st = draw_from_logits(P + (size_t)tau * V, V, T, top_p, W, r.Ep, &pick);
+            if (!st) out_tokens[tau] = pick;
+        } else {
+            const u128 target = (R * (u128)W) >> 24;
+            u128 cum = 0;
+            int32_t pick = -1;
+            for (int v = 0; v < V; ++v) {
+                cum += bmass_term(&r, tau, pi[tau], v);
+                if (cum > target) {
+                    pick = v;
+                    break;
+                }
+            }
+            out_tokens[tau] = pick;
+        }
+    }
+    brows_free(&r);
+    return st;
+}
+
+int oracle_verify_block(const float *P, const float *ell, const int32_t *tokens, int B, int V, int draft_greedy,
+                        float T, float top_p, uint64_t seed, uint32_t seq, uint32_t step, int32_t *accept_len,
+                        int32_t *out_tokens)
+{
+    uint32_t U[64], Wres[64];
+    if (B > 64) return ERR_OOB;
+    for (int i = 0; i < B; ++i) {
+        U[i] = oracle_uniform_u32(seed, seq, step, (uint32_t)i, 2u);
+        Wres[i] = oracle_uniform_u32(seed, seq, step, (uint32_t)i, 3u) >> 8;
+    }
+    uint32_t Wb = oracle_uniform_u32(seed, seq, step, (uint32_t)B, 4u) >> 8;
+    return oracle_verify_block_core(P, ell, tokens, B, V, draft_greedy, T, top_p, U, Wres, Wb, accept_len,
+                                    out_tokens);
+}

@@ -43,6 +43,14 @@ def lib():
         L.oracle_verify_prob.argtypes = [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int,
                                          C.c_float, C.c_float, C.c_uint64, C.c_uint32, C.c_uint32,
                                          C.c_void_p, C.c_void_p]
+        vp = C.c_void_p
+        L.oracle_verify_block_stats.argtypes = [vp, vp, vp, C.c_int, C.c_int, C.c_int, C.c_float, C.c_float, vp, vp]
+        L.oracle_block_residual_weights.argtypes = [vp, vp, vp, C.c_int, C.c_int, C.c_int, C.c_float, C.c_float,
+                                                    C.c_int, C.c_double, vp]
+        L.oracle_verify_block_core.argtypes = [vp, vp, vp, C.c_int, C.c_int, C.c_int, C.c_float, C.c_float, vp, vp,
+                                               C.c_uint32, vp, vp]
+        L.oracle_verify_block.argtypes = [vp, vp, vp, C.c_int, C.c_int, C.c_int, C.c_float, C.c_float, C.c_uint64,
+                                          C.c_uint32, C.c_uint32, vp, vp]
     return _lib
 
 
@@ -168,4 +176,51 @@ def verify_prob(P, ell, tokens, draft_greedy: int, T: float, top_p: float, seed:
     out = np.zeros(B + 1, dtype=np.int32)
     _chk(lib().oracle_verify_prob(_ptr(P), _ptr(ell), _ptr(tokens), B, P.shape[1], draft_greedy, T, top_p,
                                   seed, seq, step, C.byref(a), _ptr(out)))
+    return a.value, out
+
+
+def _vargs(P, ell, tokens):
+    P = np.ascontiguousarray(P, dtype=np.float32)
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+    B = tokens.shape[0]
+    ell = np.ascontiguousarray(ell if ell is not None else np.zeros((max(B, 1), P.shape[1])), dtype=np.float32)
+    return P, ell, tokens, B
+
+
+def block_stats(P, ell, tokens, draft_greedy: int, T: float, top_p: float):
+    """Block verification's pi_0..pi_B and h_0..h_B (h_0 = 0) for one drafted block."""
+    P, ell, tokens, B = _vargs(P, ell, tokens)
+    pi = np.zeros(B + 1)
+    h = np.zeros(B + 1)
+    _chk(lib().oracle_verify_block_stats(_ptr(P), _ptr(ell), _ptr(tokens), B, P.shape[1], draft_greedy, T, top_p,
+                                         _ptr(pi), _ptr(h)))
+    return pi, h
+
+
+def block_residual_weights(P, ell, tokens, draft_greedy: int, T: float, top_p: float, i: int, pi: float):
+    """Fixed-point (2^-80) residual weights max(pi p_i - q_i, 0) of position i, as Python ints."""
+    P, ell, tokens, B = _vargs(P, ell, tokens)
+    w = np.zeros(2 * P.shape[1], dtype=np.uint64)
+    _chk(lib().oracle_block_residual_weights(_ptr(P), _ptr(ell), _ptr(tokens), B, P.shape[1], draft_greedy, T,
+                                             top_p, i, pi, _ptr(w)))
+    return [int(w[2 * v]) | (int(w[2 * v + 1]) << 64) for v in range(P.shape[1])]
+
+
+def verify_block_core(P, ell, tokens, draft_greedy: int, T: float, top_p: float, U, Wres, Wbonus: int):
+    P, ell, tokens, B = _vargs(P, ell, tokens)
+    U = np.ascontiguousarray(U, dtype=np.uint32)
+    Wres = np.ascontiguousarray(Wres, dtype=np.uint32)
+    a = C.c_int32()
+    out = np.zeros(B + 1, dtype=np.int32)
+    _chk(lib().oracle_verify_block_core(_ptr(P), _ptr(ell), _ptr(tokens), B, P.shape[1], draft_greedy, T, top_p,
+                                        _ptr(U), _ptr(Wres), Wbonus, C.byref(a), _ptr(out)))
+    return a.value, out
+
+
+def verify_block(P, ell, tokens, draft_greedy: int, T: float, top_p: float, seed: int, seq: int, step: int):
+    P, ell, tokens, B = _vargs(P, ell, tokens)
+    a = C.c_int32()
+    out = np.zeros(B + 1, dtype=np.int32)
+    _chk(lib().oracle_verify_block(_ptr(P), _ptr(ell), _ptr(tokens), B, P.shape[1], draft_greedy, T, top_p, seed,
+                                   seq, step, C.byref(a), _ptr(out)))
     return a.value, out
