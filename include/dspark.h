@@ -54,7 +54,7 @@ typedef enum {
 } dspark_status;
 
 enum { DSPARK_FMT_BF16 = 0, DSPARK_FMT_FP8 = 1, DSPARK_FMT_NVFP4 = 2, DSPARK_FMT_MXFP4 = 3 };
-enum { DSPARK_GREEDY = 0, DSPARK_PROBABILISTIC = 1 };
+enum { DSPARK_GREEDY = 0, DSPARK_PROBABILISTIC = 1, DSPARK_BLOCK = 2 /* verify_mode only */ };
 
 /*
  * Drafter geometry. Full Kimi-K3 DSpark: hidden 7168, 5 captured states, 5
@@ -145,7 +145,7 @@ typedef struct {
  * purpose); purposes 1 draft, 2 accept, 3 residual, 4 bonus. */
 typedef struct {
     int draft_mode;     /* DSPARK_GREEDY or DSPARK_PROBABILISTIC */
-    int verify_mode;    /* DSPARK_GREEDY or DSPARK_PROBABILISTIC */
+    int verify_mode;    /* DSPARK_GREEDY, DSPARK_PROBABILISTIC or DSPARK_BLOCK */
     float temperature;  /* > 0 for probabilistic modes */
     float top_p;        /* (0, 1] */
     uint64_t seed;
@@ -212,6 +212,14 @@ dspark_status dspark_confidence(dspark_handle_t *h, const float *h_out, float *c
  * min(1, p_i(t_i)/q_i(t_i)); on the first reject draw from norm(max(0, p - q));
  * if all are accepted draw a bonus from p_{block+1}. Exact integer arithmetic
  * on 2^32-scaled weights; with a greedy draft q_i is one-hot on t_i.
+ * Block (DSPARK_BLOCK, [P3] "Sampling options": rejection_sample_method block
+ * verifies the drafted block as a unit; the published block verification
+ * method): pi_0 = 1, pi_i = min(pi_{i-1} p_{i-1}(t_i)/q_{i-1}(t_i), 1),
+ * h_i = S_i / (S_i + 1 - pi_i) with S_i = sum_x max(pi_i p_i(x) - q_i(x), 0),
+ * h_block = pi_block; independent decisions U_i < h_i * 2^32; the last accepted
+ * position tau; then a draw from max(pi_tau p_tau - q_tau, 0) (tau < block) or
+ * the bonus. Probabilities are the spec's rationals rounded once to double;
+ * residual terms are doubles truncated to 2^-80 and summed exactly in 128 bits.
  * accept_len int32 [bs] in 0..block; out_tokens int32 [bs, block+1] (accepted
  * drafts, then the correction or bonus token, then -1). */
 dspark_status dspark_verify(dspark_handle_t *h, const float *target_logits, const float *ell, const int32_t *tokens,

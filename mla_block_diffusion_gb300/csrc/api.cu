@@ -745,9 +745,11 @@ dspark_status dspark_verify(dspark_handle_t *h, const float *target_logits, cons
     REQ(tokens);
     REQ(accept_len);
     REQ(out_tokens);
-    if (sample->verify_mode != DSPARK_GREEDY && sample->verify_mode != DSPARK_PROBABILISTIC) return DSPARK_ERR_SHAPE;
+    if (sample->verify_mode != DSPARK_GREEDY && sample->verify_mode != DSPARK_PROBABILISTIC &&
+        sample->verify_mode != DSPARK_BLOCK)
+        return DSPARK_ERR_SHAPE;
     if (sample->draft_mode != DSPARK_GREEDY && sample->draft_mode != DSPARK_PROBABILISTIC) return DSPARK_ERR_SHAPE;
-    const bool prob = sample->verify_mode == DSPARK_PROBABILISTIC;
+    const bool prob = sample->verify_mode != DSPARK_GREEDY;  // token-by-token or block
     if (prob && bad_sampling(sample->temperature, sample->top_p)) return DSPARK_ERR_SHAPE;
     if (prob && sample->draft_mode != DSPARK_GREEDY) REQ(ell);
     const dspark_status st = check_ws(h, ws, ws_bytes, bs, 0);

@@ -863,7 +863,7 @@ __global__ void verify_greedy_finalize(const int32_t *__restrict__ tokens, int b
 // p rows 0..B, then (unless the draft was greedy) q rows 0..B-1:
 //   gM [bs*R] | gS [bs*R] | gH [groups][passes][kRowsPerGroup][256] | stats [bs*R][2] | parts [bs][grid][2]
 struct VerLayout {
-    size_t gM, gS, gH, stats, parts, total;
+    size_t gM, gS, gH, stats, parts, mass, total;
     int R, nrows, groups;
     __host__ __device__ VerLayout(int bs, int B, int grid, int draft_greedy) {
         R = draft_greedy ? B + 1 : 2 * B + 1;
@@ -874,7 +874,8 @@ struct VerLayout {
         gH = gS + nrows;
         stats = gH + (size_t)groups * kRadixPasses * kRowsPerGroup * 256;
         parts = stats + (size_t)nrows * 2;
-        total = parts + (size_t)bs * grid * 2;
+        mass = parts + (size_t)bs * grid * 2;           // block verification: [bs][B][grid][2]
+        total = mass + (size_t)bs * B * grid * 2;
     }
 };
 
@@ -1005,6 +1006,231 @@ __global__ void __launch_bounds__(kSampThreads, 1) verify_prob_kernel(VerifyPara
 }
 
 // ---------------------------------------------------------------------------
+// Block verification (the oracle's description: rejection_sample_method
+// "block", the published block verification method). Probabilities are the
+// spec's in-nucleus rationals rounded once to double; every residual-mass term
+// is a double (multiply, then subtract) truncated to a multiple of 2^-80, and
+// the masses are exact 128-bit sums, so the decisions match the oracle bit for
+// bit whatever the order of summation.
+// ---------------------------------------------------------------------------
+constexpr int kMaxBlockRows = 17;  // block <= 16, plus the bonus row
+
+DS_DEVINL unsigned __int128 fx80(double x) {
+    if (!(x > 0.0)) return 0;
+    const unsigned long long b = (unsigned long long)__double_as_longlong(x);
+    const int e = (int)((b >> 52) & 0x7FF);
+    if (e == 0) return 0;
+    const unsigned long long m = (b & ((1ull << 52) - 1)) | (1ull << 52);
+    const int sh = e - 995;  // x * 2^80 = m * 2^(e - 1075 + 80)
+    if (sh >= 0) return (unsigned __int128)m << sh;
+    if (sh <= -53) return 0;
+    return (unsigned __int128)(m >> (-sh));
+}
+
+DS_DEVINL double fx80_to_double(unsigned __int128 s) {
+    if (s == 0) return 0.0;
+    const unsigned long long hi = (unsigned long long)(s >> 64), lo = (unsigned long long)s;
+    const int n = hi ? 128 - __clzll((long long)hi) : 64 - __clzll((long long)lo);
+    if (n <= 53) return ldexp((double)lo, -80);
+    return ldexp((double)(unsigned long long)(s >> (n - 53)), n - 53 - 80);
+}
+
+// One row of the spec as in-nucleus probabilities (one-hot for a greedy draft).
+struct BlockRow {
+    const float *row;
+    float m;
+    unsigned long long kstar, S;
+    int onehot;  // -1: a spec row; else the one token of a greedy draft
+    DS_DEVINL double prob(int v, float T) const {
+        if (onehot >= 0) return v == onehot ? 1.0 : 0.0;
+        const unsigned long long E = weight_of(row[v], T, m);
+        const unsigned long long e = key_of(E, v) >= kstar ? E : 0ull;
+        return __ddiv_rn((double)e, (double)S);
+    }
+};
+
+DS_DEVINL unsigned __int128 block_term(const BlockRow &rp, const BlockRow &rq, double pi, float T, int v) {
+    return fx80(__dsub_rn(__dmul_rn(pi, rp.prob(v, T)), rq.prob(v, T)));
+}
+
+// Sum of 128-bit values over the CTA (thread 0 gets the total).
+DS_DEVINL unsigned __int128 block_sum_u128(unsigned __int128 v, DrawSmem &ds_) {
+    unsigned long long lo = (unsigned long long)v, hi = (unsigned long long)(v >> 64);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long lo2 = __shfl_xor_sync(0xffffffffu, lo, o), hi2 = __shfl_xor_sync(0xffffffffu, hi, o);
+        const unsigned long long s = lo + lo2;
+        hi = hi + hi2 + (s < lo ? 1ull : 0ull);
+        lo = s;
+    }
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) {
+        ds_.lo[threadIdx.x >> 5] = lo;
+        ds_.hi[threadIdx.x >> 5] = hi;
+    }
+    __syncthreads();
+    unsigned __int128 t = 0;
+    if (threadIdx.x == 0)
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += ((unsigned __int128)ds_.hi[w] << 64) | ds_.lo[w];
+    return t;
+}
+
+__global__ void __launch_bounds__(kSampThreads, 1) verify_block_kernel(VerifyParams p) {
+    __shared__ NucleusSmem sm;
+    __shared__ DrawSmem dsm;
+    __shared__ volatile int s_fail;
+    __shared__ const float *s_rows[kRowsPerGroup];
+    __shared__ double s_pi[kMaxSampBs][kMaxBlockRows];
+    __shared__ int s_tau[kMaxSampBs];
+    const VerLayout L(p.bs, p.B, gridDim.x, p.draft_greedy);
+    unsigned long long *sc = p.scratch;
+    const int V = p.V, B = p.B, R = L.R;
+    const float T = p.T;
+    if (threadIdx.x == 0) s_fail = 0;
+    for (size_t w = (size_t)blockIdx.x * blockDim.x + threadIdx.x; w < L.total; w += (size_t)gridDim.x * blockDim.x)
+        sc[w] = 0;
+    __threadfence();
+    if (!grid_barrier(p.ctl, &s_fail, p.err)) return;
+    // nucleus statistics of every target and draft row
+    for (int g = 0; g < L.groups; ++g) {
+        const int r0 = g * kRowsPerGroup, nr = min(kRowsPerGroup, L.nrows - r0);
+        if (threadIdx.x < nr) s_rows[threadIdx.x] = ver_row(p, r0 + threadIdx.x);
+        __syncthreads();
+        if (!group_max(s_rows, nr, V, T, sm, sc + L.gM + r0, p.ctl, &s_fail, p.err)) return;
+        if (!group_nucleus(s_rows, nr, V, T, p.top_p, sm, sc + L.gS + r0,
+                           sc + L.gH + (size_t)g * kRadixPasses * kRowsPerGroup * 256, p.ctl, &s_fail, p.err))
+            return;
+        if (blockIdx.x == 0 && threadIdx.x < nr) {
+            sc[L.stats + (size_t)(r0 + threadIdx.x) * 2] = sm.kstar[threadIdx.x];
+            sc[L.stats + (size_t)(r0 + threadIdx.x) * 2 + 1] = sm.Sn[threadIdx.x];
+        }
+        __syncthreads();
+    }
+    if (!grid_barrier(p.ctl, &s_fail, p.err)) return;
+    auto token = [&](int b, int i) -> int {
+        const int t = p.tokens[b * B + i];
+        return (t < 0 || t >= V) ? 0 : t;
+    };
+    auto rowp = [&](int b, int i) -> BlockRow {
+        const int rr = b * R + i;
+        BlockRow r;
+        r.row = p.P + ((size_t)b * (B + 1) + i) * V;
+        r.m = ord2f((uint32_t)ldcg_u64(&sc[L.gM + rr]));
+        r.kstar = ldcg_u64(&sc[L.stats + 2 * rr]);
+        r.S = ldcg_u64(&sc[L.stats + 2 * rr + 1]);
+        r.onehot = -1;
+        return r;
+    };
+    auto rowq = [&](int b, int i) -> BlockRow {
+        BlockRow r;
+        if (p.draft_greedy) {
+            r.row = nullptr;
+            r.m = 0.f;
+            r.kstar = r.S = 0;
+            r.onehot = token(b, i);
+            return r;
+        }
+        const int rr = b * R + B + 1 + i;
+        r.row = p.ell + ((size_t)b * B + i) * V;
+        r.m = ord2f((uint32_t)ldcg_u64(&sc[L.gM + rr]));
+        r.kstar = ldcg_u64(&sc[L.stats + 2 * rr]);
+        r.S = ldcg_u64(&sc[L.stats + 2 * rr + 1]);
+        r.onehot = -1;
+        return r;
+    };
+    // the ratio chain pi_0..pi_B of every sequence (identical in every CTA)
+    for (int b = threadIdx.x; b < p.bs; b += blockDim.x) {
+        double pi = 1.0;
+        s_pi[b][0] = pi;
+        for (int i = 1; i <= B; ++i) {
+            const int t0 = p.tokens[b * B + i - 1];
+            if ((t0 < 0 || t0 >= V) && blockIdx.x == 0) set_error(p.err, DSPARK_ERR_OOB);
+            const int t = token(b, i - 1);
+            const double a = rowp(b, i - 1).prob(t, T), c = rowq(b, i - 1).prob(t, T);
+            if (c == 0.0) {
+                pi = (a > 0.0 && pi > 0.0) ? 1.0 : 0.0;
+            } else {
+                const double x = __dmul_rn(pi, __ddiv_rn(a, c));
+                pi = x < 1.0 ? x : 1.0;
+            }
+            s_pi[b][i] = pi;
+        }
+    }
+    __syncthreads();
+    // residual masses S_{b,i} (i < B) over this CTA's vocabulary pairs, exact
+    {
+        int lo, hi;
+        pair_slice(V / 2, lo, hi);
+        for (int b = 0; b < p.bs; ++b) {
+            for (int i = 0; i < B; ++i) {
+                const BlockRow rp = rowp(b, i), rq = rowq(b, i);
+                const double pi = s_pi[b][i];
+                unsigned __int128 acc = 0;
+                for (int pp = lo + threadIdx.x; pp < hi; pp += blockDim.x)
+                    acc += block_term(rp, rq, pi, T, 2 * pp) + block_term(rp, rq, pi, T, 2 * pp + 1);
+                const unsigned __int128 tot = block_sum_u128(acc, dsm);
+                if (threadIdx.x == 0) {
+                    unsigned long long *dst = sc + L.mass + (((size_t)b * B + i) * gridDim.x + blockIdx.x) * 2;
+                    dst[0] = (unsigned long long)tot;
+                    dst[1] = (unsigned long long)(tot >> 64);
+                }
+            }
+        }
+    }
+    if (!grid_barrier(p.ctl, &s_fail, p.err)) return;
+    auto mass = [&](int b, int i) -> unsigned __int128 {
+        unsigned __int128 S = 0;
+        const unsigned long long *src = sc + L.mass + ((size_t)b * B + i) * gridDim.x * 2;
+        for (int c = 0; c < (int)gridDim.x; ++c)
+            S += ((unsigned __int128)ldcg_u64(&src[2 * c + 1]) << 64) | ldcg_u64(&src[2 * c]);
+        return S;
+    };
+    // decisions: eta_i = (U_i < h_i 2^32), tau = the last accepted position
+    for (int b = threadIdx.x; b < p.bs; b += blockDim.x) {
+        int tau = 0;
+        for (int i = 1; i <= B; ++i) {
+            double h;
+            if (i < B) {
+                const double S = fx80_to_double(mass(b, i));
+                const double den = __dadd_rn(S, __dsub_rn(1.0, s_pi[b][i]));
+                h = den > 0.0 ? __ddiv_rn(S, den) : 0.0;
+            } else {
+                h = s_pi[b][B];
+            }
+            const uint32_t U = philox_word(p.seed, (uint32_t)b, p.step, (uint32_t)(i - 1), 2u);
+            if ((double)U < __dmul_rn(h, 4294967296.0)) tau = i;
+        }
+        s_tau[b] = tau;
+        if (blockIdx.x == 0) {
+            p.accept_len[b] = tau;
+            for (int j = 0; j <= B; ++j) p.out_tokens[b * (B + 1) + j] = j < tau ? token(b, j) : -1;
+        }
+    }
+    __syncthreads();
+    // one draw per sequence: the residual at tau, or the bonus
+    for (int b = 0; b < p.bs; ++b) {
+        const int tau = s_tau[b];
+        int32_t *dst = p.out_tokens + b * (B + 1) + tau;
+        unsigned long long *parts = sc + L.parts + (size_t)b * gridDim.x * 2;
+        const BlockRow rp = rowp(b, tau);
+        const bool plain = tau == B || mass(b, tau) == 0;  // a spec draw from target row tau
+        const uint32_t W = philox_word(p.seed, (uint32_t)b, p.step, (uint32_t)tau, tau == B ? 4u : 3u) >> 8;
+        if (plain) {
+            auto wf = [&](int v) -> unsigned __int128 {
+                const unsigned long long E = weight_of(rp.row[v], T, rp.m);
+                return key_of(E, v) >= rp.kstar ? (unsigned __int128)E : (unsigned __int128)0;
+            };
+            if (!grid_draw(wf, V, W, parts, dst, dsm, p.ctl, &s_fail, p.err)) return;
+        } else {
+            const BlockRow rq = rowq(b, tau);
+            const double pi = s_pi[b][tau];
+            auto wf = [&](int v) -> unsigned __int128 { return block_term(rp, rq, pi, T, v); };
+            if (!grid_draw(wf, V, W, parts, dst, dsm, p.ctl, &s_fail, p.err)) return;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Host launchers
 // ---------------------------------------------------------------------------
 // Dynamic shared memory of the rollout's w2 ring for a vocabulary and grid.
@@ -1024,7 +1250,10 @@ int sampling_max_grid(int num_sms, int V) {
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, rollout_kernel, kSampThreads, ring) != cudaSuccess) return 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, verify_prob_kernel, kSampThreads, 0) != cudaSuccess)
         return 0;
-    return (a >= 1 && b >= 1) ? num_sms : 0;
+    int c = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c, verify_block_kernel, kSampThreads, 0) != cudaSuccess)
+        return 0;
+    return (a >= 1 && b >= 1 && c >= 1) ? num_sms : 0;
 }
 
 cudaError_t launch_rollout(const CUtensorMap &w2_map, RolloutParams p, int grid, cudaStream_t st) {
@@ -1046,6 +1275,8 @@ cudaError_t launch_verify(VerifyParams p, int grid, cudaStream_t st) {
                           p.scratch, p.accept_len, p.out_tokens, p.err);
     }
     void *args[] = {&p};
+    if (p.verify_mode == DSPARK_BLOCK)
+        return cudaLaunchCooperativeKernel((void *)verify_block_kernel, dim3(grid), dim3(kSampThreads), args, 0, st);
     return cudaLaunchCooperativeKernel((void *)verify_prob_kernel, dim3(grid), dim3(kSampThreads), args, 0, st);
 }
 

@@ -16,7 +16,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libdspark.so")
 
 MAX_LAYERS = 16
-GREEDY, PROBABILISTIC = 0, 1
+GREEDY, PROBABILISTIC, BLOCK = 0, 1, 2
 FMT_BF16, FMT_FP8, FMT_NVFP4, FMT_MXFP4 = 0, 1, 2, 3
 
 STATUS = {0: "OK", 1: "ERR_NULL", 2: "ERR_ALIGN", 3: "ERR_SHAPE", 4: "ERR_UNSUPPORTED", 5: "ERR_CUDA",

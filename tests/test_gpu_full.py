@@ -132,3 +132,12 @@ def test_full_vocab_rollout_and_verify(M, weights, mode, T, top_p):
         assert int(acc[b]) == a and out[b].cpu().numpy().tolist() == o.tolist(), b
     if mode == 0:
         assert int(acc[0]) == G.block  # zero noise: the target agrees with every draft
+    else:
+        # block verification of the same draft, full vocabulary
+        sb = M.Sample(mode, M.BLOCK, T, top_p, 99, 4)
+        ds.verify(P, torch.from_numpy(np.stack(ells)).cuda(), torch.from_numpy(np.stack(toks)).cuda(), sb, acc, out,
+                  bs)
+        assert ds.check() == 0
+        for b in range(bs):
+            a, o = S.verify_block(Ps[b], ells[b], toks[b], 0, T, top_p, seed=99, seq=b, step=4)
+            assert int(acc[b]) == a and out[b].cpu().numpy().tolist() == o.tolist(), b

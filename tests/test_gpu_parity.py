@@ -105,7 +105,8 @@ def _verify_inputs(G, bs, seed, draft_mode, T, top_p, noise):
 
 
 @pytest.mark.parametrize("vmode,dmode,T,top_p", [(0, 0, 1.0, 1.0), (1, 0, 1.0, 0.95), (1, 1, 1.0, 0.95),
-                                                  (1, 1, 0.8, 1.0)])
+                                                  (1, 1, 0.8, 1.0), (2, 1, 1.0, 0.95), (2, 0, 1.0, 1.0),
+                                                  (2, 1, 0.7, 0.9)])
 @pytest.mark.parametrize("G,bs", [(TINY, 4), (MID, 3)])
 def test_verify_bit_exact(M, G, bs, vmode, dmode, T, top_p):
     W, toks, ells, Ps = _verify_inputs(G, bs, 21, dmode, T, top_p, noise=(0.0, 0.02, 0.5, 2.0))
@@ -121,8 +122,10 @@ def test_verify_bit_exact(M, G, bs, vmode, dmode, T, top_p):
         for b in range(bs):
             if vmode == 0:
                 a, o = S.verify_greedy(Ps[b], toks[b])
-            else:
+            elif vmode == 1:
                 a, o = S.verify_prob(Ps[b], ells[b], toks[b], int(dmode == 0), T, top_p, seed=777, seq=b, step=step)
+            else:  # block verification
+                a, o = S.verify_block(Ps[b], ells[b], toks[b], int(dmode == 0), T, top_p, seed=777, seq=b, step=step)
             assert int(acc[b]) == a, (b, step)
             assert out[b].cpu().numpy().tolist() == o.tolist(), (b, step)
             seen.add(a)
