@@ -210,7 +210,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--lm-rows", type=int, default=4096)
-    ap.add_argument("--only", choices=["fc", "rollout", "layer", "append"], default=None,
+    ap.add_argument("--only", choices=["fc", "rollout", "layer", "append", "verify"], default=None,
                     help="time one call alone for profiling: fc (the fusion GEMM; full shape unless --fc-hidden), "
                          "rollout (Markov rollout, full vocabulary), layer (one full-width MLA layer, ctx 4096), "
                          "append (latent-cache append of 8 verified tokens, all 5 layers, full hidden/latent)")
@@ -219,7 +219,16 @@ def main():
     ap.add_argument("--format", choices=["bf16", "fp8", "nvfp4", "mxfp4"], default="bf16",
                     help="weight format of fc, q_b, o, gate, up, down (the weight-format sweep workloads)")
     ap.add_argument("--no-drift", action="store_true", help="--format fp8|nvfp4|mxfp4: skip the drift report")
+    ap.add_argument("--drift", action="store_true",
+                    help="run the weight-format drift / acceptance-ceiling harness instead of the step benchmark")
+    ap.add_argument("--blocks", type=int, default=1024, help="--drift: blocks per aux regime")
+    ap.add_argument("--regime", choices=["boot", "heavy", "gauss", "all"], default="all", help="--drift: aux regime")
+    ap.add_argument("--drift-formats", default="fp8,nvfp4,mxfp4", help="--drift: formats against the bf16 path")
+    ap.add_argument("--drift-geom", choices=["full", "mid"], default="full",
+                    help="--drift: full drafter geometry, or a small one for a quick check")
     args = ap.parse_args()
+    if args.drift:
+        return drift_harness(args)
     assert args.warmup >= 3 or args.impl == "reference", "at least 3 warm-up steps"
 
     from synthetic import generate as gen
@@ -238,6 +247,8 @@ def main():
         return only_fc(args, G, world, rank, local)
     if args.only == "append":
         return only_append(args, G, local)
+    if args.only == "verify":
+        return only_verify(args, G, local)
     if args.only in ("rollout", "layer"):
         return only_call(args, G, local)
 
@@ -611,6 +622,238 @@ def only_append(args, G, local):
     print(json.dumps({"only": "append", "tokens": n, "layers": g.n_layers, "median_call_ms": ms,
                       "algorithmic_bytes": nbytes, "achieved_GBps": nbytes / (ms * 1e-3) / 1e9,
                       "peak_GBps": pk["hbm_gbs"], "peak_source": src}))
+
+
+# ---------------------------------------------------------------------------
+# Drift / acceptance-ceiling harness ("Kimi-K3-DSpark-NVFP4", Measurement and
+# Detail): a weight format against the bf16 path on the same synthetic blocks.
+# ---------------------------------------------------------------------------
+def weight_snr_db(w_ref: torch.Tensor, w_dec: torch.Tensor) -> float:
+    """10 log10(sum w^2 / sum (w - w_decoded)^2)."""
+    w = w_ref.to(torch.float64)
+    e = w - w_dec.to(torch.float64)
+    return float(10.0 * torch.log10((w * w).sum() / (e * e).sum()))
+
+
+def kl_and_overlap(l_ref: torch.Tensor, l_var: torch.Tensor):
+    """Per row: KL(softmax(l_ref) || softmax(l_var)) and the coupling 1 - TV = sum min(p, q)."""
+    lp = torch.log_softmax(l_ref.to(torch.float64), dim=-1)
+    lq = torch.log_softmax(l_var.to(torch.float64), dim=-1)
+    p = lp.exp()
+    kl = (p * (lp - lq)).sum(-1)
+    overlap = torch.minimum(p, lq.exp()).sum(-1)
+    return kl, overlap
+
+
+def prefix_runs(agree: np.ndarray) -> np.ndarray:
+    """Length of the leading run of agreeing positions of every block ([N, B] bool)."""
+    agree = np.asarray(agree, dtype=bool)
+    run = np.cumprod(agree, axis=1)
+    return run.sum(axis=1)
+
+
+def conditional_agreement(agree: np.ndarray) -> np.ndarray:
+    """s_i = P(position i agrees | positions < i agree), the per-position sequential agreement."""
+    agree = np.asarray(agree, dtype=bool)
+    s = []
+    alive = np.ones(agree.shape[0], dtype=bool)
+    for i in range(agree.shape[1]):
+        n = alive.sum()
+        s.append(float((alive & agree[:, i]).sum() / n) if n else 0.0)
+        alive &= agree[:, i]
+    return np.array(s)
+
+
+def ceiling_from_agreement(s: np.ndarray) -> float:
+    """Drift-limited acceptance ceiling sum_k prod_{i<=k} s_i (the expected leading run)."""
+    return float(np.cumprod(np.asarray(s, dtype=np.float64)).sum())
+
+
+def pearson(a, b) -> float:
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    a = a - a.mean()
+    b = b - b.mean()
+    return float((a * b).sum() / np.sqrt((a * a).sum() * (b * b).sum()))
+
+
+_E2M1 = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0, -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0]
+
+
+def decode_weight(v, fmt: str) -> torch.Tensor:
+    """Decoded float64 matrix of a quantised weight triple (for the weight SNR)."""
+    d, sc, g = v
+    if fmt == "fp8":
+        return d.view(torch.float8_e4m3fn).to(torch.float64) * sc.to(torch.float64)[:, None]
+    codes = torch.stack([d & 0xF, d >> 4], dim=-1).reshape(d.shape[0], -1).long()
+    vals = torch.tensor(_E2M1, dtype=torch.float64, device=d.device)[codes]
+    if fmt == "nvfp4":
+        return vals * sc.view(torch.float8_e4m3fn).to(torch.float64).repeat_interleave(16, 1) * g
+    return vals * torch.pow(2.0, sc.to(torch.float64) - 127.0).repeat_interleave(32, 1)
+
+
+def drift_harness(args):
+    """Weight-format drift on the same kernels: every format against the bf16 path on the
+    same blocks ("Kimi-K3-DSpark-NVFP4", Measurement / Detail). Aux regimes: gauss (N(0,1)),
+    heavy (Student-t df 3 at unit RMS), boot (the drafter's own residual stream after each of
+    its 5 layers, from a gauss block, stands in for the 5 captured target states). Greedy
+    agreement, 1-TV and KL are teacher-forced (every format's logits corrected with the bf16
+    path's previous tokens); the sequential agreement and the ceiling use every format's own
+    greedy rollout. One JSON line per regime."""
+    from dataclasses import replace
+    import mla_block_diffusion_gb300 as M
+    from mla_block_diffusion_gb300 import build as libbuild
+    from synthetic import generate as gen
+    from synthetic import quantize as Q
+    from synthetic.configs import FULL_STEP, FORMAT_FP8, FORMAT_MXFP4, FORMAT_NVFP4
+    libbuild.build()
+    w = FULL_STEP
+    G = w.geom
+    if args.drift_geom == "mid":
+        G = replace(G, hidden=1024, n_aux=5, n_heads=16, q_lora=512, kv_lora=512, d_nope=64, d_rope=64, d_v=64,
+                    inter=2048, vocab=8192, rank=32)
+        w = replace(w, geom=G, ctx=(512,))
+    W = gen.make_weights(w, "cuda")
+    I = gen.make_inputs(w, "cuda")
+    ctx = I["ctx_list"][0]
+    fmts = [f for f in args.drift_formats.split(",") if f]
+    code = {"fp8": FORMAT_FP8, "nvfp4": FORMAT_NVFP4, "mxfp4": FORMAT_MXFP4}
+    qnames = ["w_fc"] + [f"l{l}.{k}" for l in range(G.n_layers) for k in ("w_q_b", "w_o", "w_gate", "w_up", "w_down")]
+    Wq, snr = {}, {}
+    for f in fmts:
+        Wq[f] = Q.quantise_weights(W, f, G.n_layers)
+        num = den = 0.0
+        for n in qnames:
+            ref = W[n].to(torch.float64)
+            dec = decode_weight(Wq[f][n], f)
+            num += float((ref * ref).sum())
+            den += float(((ref - dec) ** 2).sum())
+            del ref, dec
+        snr[f] = 10.0 * math.log10(num / den)
+    handles = {"bf16": M.DSpark(G, W, max_bs=1, max_ctx=ctx)}
+    for f in fmts:
+        handles[f] = M.DSpark(G, Wq[f], max_bs=1, max_ctx=ctx, weight_format=code[f])
+    depth = {}
+    for k in range(1, G.n_layers + 1):  # the boot regime's residual streams
+        Gk = replace(G, n_layers=k)
+        depth[k] = M.DSpark(Gk, {n: t for n, t in W.items() if not n.startswith("l") or int(n[1:n.index(".")]) < k},
+                            max_bs=1, max_ctx=ctx)
+    kvs = {n: h.make_kv(I["kv_pools"], I["page_table"], I["ctx_len"], ctx) for n, h in handles.items()}
+    kvd = {k: h.make_kv(I["kv_pools"], I["page_table"], I["ctx_len"], ctx) for k, h in depth.items()}
+    w1 = W["markov_w1"].float()
+    w2 = W["markov_w2"].float()
+    smp = M.Sample(M.GREEDY, M.GREEDY, 1.0, 1.0, 1, 0)
+    B, H, V = G.block, G.hidden, G.vocab
+    x = torch.empty(1, B, H, dtype=torch.float32, device="cuda")
+    h_out = torch.empty_like(x)
+    z = torch.empty(1, B, V, dtype=torch.float32, device="cuda")
+    ell = torch.empty_like(z)
+    tok = torch.empty(1, B, dtype=torch.int32, device="cuda")
+    conf = torch.empty(1, B, dtype=torch.float32, device="cuda")
+    regimes = ["boot", "heavy", "gauss"] if args.regime == "all" else [args.regime]
+    for regime in regimes:
+        acc = {f: {"greedy": [], "seq": [], "kl": [], "ov": [], "hrel": [], "conf": []} for f in fmts}
+        conf_ref = []
+        t0 = time.time()
+        for blk in range(args.blocks):
+            seed = 7000 + blk
+            if regime == "heavy":
+                aux = gen.student_t3_unit_rms((1, B, G.n_aux, H), seed, "drift_aux", "cuda")
+            else:
+                aux = gen.normal((1, B, G.n_aux, H), 1.0, seed, "drift_aux", "cuda")
+            if regime == "boot":
+                layers_out = []
+                for k in range(1, G.n_layers + 1):
+                    depth[k].fuse_ctx(aux, x, 1)
+                    depth[k].draft_block(x, kvd[k], h_out, z, 1)
+                    layers_out.append(x.clone())
+                aux = torch.stack(layers_out[:G.n_aux], dim=2).to(torch.bfloat16)
+            anchor = gen.uniform_tokens((1,), V, seed, "drift_anchor").cuda()
+            out = {}
+            for n, hd in handles.items():
+                hd.fuse_ctx(aux, x, 1)
+                hd.draft_block(x, kvs[n], h_out, z, 1)
+                hd.markov_rollout(z, anchor, smp, tok, ell, 1)
+                hd.confidence(h_out, conf, 1)
+                out[n] = (h_out[0].clone(), z[0].clone(), tok[0].clone(), conf[0].clone())
+            h_r, z_r, t_r, c_r = out["bf16"]
+            prev = torch.cat([anchor.long(), t_r[:-1].long()])
+            delta = w1[prev] @ w2                      # the Markov correction after the bf16 path's tokens
+            l_r = z_r + delta
+            conf_ref.append(c_r.cpu().numpy())
+            for f in fmts:
+                h_v, z_v, t_v, c_v = out[f]
+                l_v = z_v + delta
+                a = acc[f]
+                a["greedy"].append((l_v.argmax(-1) == l_r.argmax(-1)).cpu().numpy())
+                a["seq"].append((t_v == t_r).cpu().numpy())
+                kl, ov = kl_and_overlap(l_r, l_v)
+                a["kl"].append(kl.cpu().numpy())
+                a["ov"].append(ov.cpu().numpy())
+                a["hrel"].append(float(torch.linalg.norm(h_v - h_r) / torch.linalg.norm(h_r)))
+                a["conf"].append(c_v.cpu().numpy())
+        assert all(h.check() == 0 for h in list(handles.values()) + list(depth.values()))
+        cr = np.concatenate(conf_ref)
+        res = {}
+        for f in fmts:
+            a = acc[f]
+            seq = np.stack(a["seq"])
+            s_i = conditional_agreement(seq)
+            kl = np.concatenate(a["kl"])
+            cv = np.concatenate(a["conf"])
+            res[f] = {"weight_snr_db": round(snr[f], 2),
+                      "greedy_agreement": float(np.concatenate(a["greedy"]).mean()),
+                      "sequential_rollout": float(seq.mean()),
+                      "per_position_sequential": [round(float(v), 4) for v in s_i],
+                      "ceiling": ceiling_from_agreement(s_i),
+                      "mean_leading_run": float(prefix_runs(seq).mean()),
+                      "one_minus_tv": float(np.concatenate(a["ov"]).mean()),
+                      "kl_mean": float(kl.mean()), "kl_p99": float(np.percentile(kl, 99)),
+                      "hidden_rel_err": float(np.mean(a["hrel"])),
+                      "confidence_r": pearson(cr, cv),
+                      "flip_rate": float(np.mean((cr > 0.5) != (cv > 0.5)))}
+        print(json.dumps({"drift": regime, "blocks": args.blocks, "geometry": args.drift_geom, "ctx": ctx,
+                          "reference": "bf16 weights on the same kernels", "seconds": round(time.time() - t0, 1),
+                          "formats": res}))
+
+
+def only_verify(args, G, local):
+    """dspark_verify alone at the full vocabulary, bs=1: greedy, token-by-token probabilistic
+    and block verification of one 7-token block (sampled draft, T 1, top_p 0.95). Target
+    logits: the draft logits plus N(0, 0.5^2)."""
+    from dataclasses import replace
+    import mla_block_diffusion_gb300 as M
+    from mla_block_diffusion_gb300 import build as libbuild
+    from synthetic import generate as gen
+    from synthetic.configs import FULL_STEP
+    libbuild.build()
+    torch.cuda.set_device(local)
+    g = replace(G, hidden=64, n_aux=1, n_layers=1, n_heads=1, q_lora=64, kv_lora=64, d_nope=16, d_rope=16, d_v=64,
+                inter=64)
+    w = replace(FULL_STEP, geom=g)
+    W = gen.make_weights(w, "cuda")
+    ds = M.DSpark(g, W, max_bs=1)
+    ell = gen.draft_logits(1, g.block, g.vocab, 5, device="cuda")
+    P = torch.cat([ell, ell[:, -1:]], dim=1) + gen.noise((1, g.block + 1, g.vocab), 0.5, 5, "tn", device="cuda")
+    tokens = torch.stack([torch.argmax(ell[0, i]) for i in range(g.block)]).to(torch.int32)[None].contiguous()
+    acc = torch.empty(1, dtype=torch.int32, device="cuda")
+    out = torch.empty(1, g.block + 1, dtype=torch.int32, device="cuda")
+    res = {}
+    for name, mode, dmode in (("greedy", M.GREEDY, M.GREEDY), ("token", M.PROBABILISTIC, M.PROBABILISTIC),
+                              ("block", M.BLOCK, M.PROBABILISTIC)):
+        times = []
+        for k in range(args.warmup + args.steps):
+            smp = M.Sample(dmode, mode, 1.0, 0.95, 11, k)
+            a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a_.record()
+            ds.verify(P, ell, tokens, smp, acc, out, 1)
+            b_.record()
+            torch.cuda.synchronize()
+            if k >= args.warmup:
+                times.append(a_.elapsed_time(b_))
+        assert ds.check() == 0
+        res[name] = {"median_call_ms": statistics.median(times), "accept_len_last": int(acc.item())}
+    print(json.dumps({"only": "verify", "vocab": g.vocab, "block": g.block, "modes": res}))
 
 
 def ds_layout_splits(ds) -> int:
