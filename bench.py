@@ -508,7 +508,17 @@ def only_fc(args, G, world, rank, local):
     w = replace(FULL_STEP, geom=g)
     W = gen.make_weights(w, "cuda")
     aux = gen.make_inputs(w, "cuda")["aux"]
-    ds = M.DSpark(g, W, max_bs=1)
+    fmt = args.format
+    if fmt != "bf16":  # the weight-only formats need every quantised dimension aligned
+        from synthetic import quantize as Q
+        from synthetic.configs import FORMAT_FP8, FORMAT_MXFP4, FORMAT_NVFP4
+        g = replace(g, q_lora=512, d_v=128, inter=512)
+        w = replace(FULL_STEP, geom=g)
+        W = Q.quantise_weights(gen.make_weights(w, "cuda"), fmt, g.n_layers)
+        ds = M.DSpark(g, W, max_bs=1,
+                      weight_format={"fp8": FORMAT_FP8, "nvfp4": FORMAT_NVFP4, "mxfp4": FORMAT_MXFP4}[fmt])
+    else:
+        ds = M.DSpark(g, W, max_bs=1)
     x = torch.empty(1, g.block, g.hidden, dtype=torch.float32, device="cuda")
     for _ in range(args.warmup):
         ds.fuse_ctx(aux, x, 1)
@@ -521,10 +531,12 @@ def only_fc(args, G, world, rank, local):
     torch.cuda.synchronize()
     assert ds.check() == 0
     ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in evs)
-    nbytes = 2 * g.hidden * g.n_aux * g.hidden + g.block * g.n_aux * g.hidden * 2 + g.block * g.hidden * 4
+    per = {"bf16": 2.0, "fp8": 1.0, "nvfp4": 0.5 + 1.0 / 16, "mxfp4": 0.5 + 1.0 / 32}[fmt]
+    nbytes = int(per * g.hidden * g.n_aux * g.hidden) + g.block * g.n_aux * g.hidden * 2 + g.block * g.hidden * 4
     pk, src = peaks()
     if rank == 0:
-        print(json.dumps({"kernel": "gemm_swapab_kernel<16> fc fusion", "avg_launch_ms": ms,
+        kern = "gemm_swapab_kernel<16>" if fmt == "bf16" else f"gemm_q_kernel<16, {fmt}>"
+        print(json.dumps({"kernel": f"{kern} fc fusion", "format": fmt, "avg_launch_ms": ms,
                           "algorithmic_bytes_per_launch": nbytes, "achieved_GBps": nbytes / (ms * 1e-3) / 1e9,
                           "peak_GBps": pk["hbm_gbs"], "peak_source": src}))
 

@@ -357,15 +357,16 @@ __global__ void __launch_bounds__(GemmQCfg<BN, FMT>::kThreads, 1)
         const int g = (warp - 6) >> 2, qd = warp & 3, r = 32 * qd + lane;
         const int gthr = threadIdx.x - 192 - 128 * g;
         const long long total_sub = (u1 - u0) * NS;
+        // software pipeline: the tensor-memory store of one sub-block completes (and is
+        // announced on cvt_full) while the next one is decoded
+        int pend = -1;
         for (long long cit = g; cit < total_sub; cit += 2) {
             const long long it = cit / NS;
             const int sb = (int)(cit % NS), s = (int)(it % RS), t = (int)(cit % CS);
-            bool got = true;
-            if (gthr == 0) {
-                got = mbar_wait_bounded(&raw_full[s], (uint32_t)(it / RS) & 1u, &s_abort) &&
-                      mbar_wait_bounded(&cvt_empty[t], ((uint32_t)(cit / CS) & 1u) ^ 1u, &s_abort);
-            }
-            if (!named_bar_and(3 + g, kQConvThreads / 2, got && !s_abort)) break;
+            // every thread waits itself; the result is made warp-uniform (tcgen05.st is warp-wide)
+            const bool got = mbar_wait_bounded(&raw_full[s], (uint32_t)(it / RS) & 1u, &s_abort) &&
+                             mbar_wait_bounded(&cvt_empty[t], ((uint32_t)(cit / CS) & 1u) ^ 1u, &s_abort);
+            if (!__all_sync(0xffffffffu, got)) break;
             uint32_t v[32];
             uint8_t *rawp = sRaw + s * C::kRawBytes;
             bool bad_scale = false;
@@ -373,11 +374,19 @@ __global__ void __launch_bounds__(GemmQCfg<BN, FMT>::kThreads, 1)
             if (bad_scale) set_error(p.err, DSPARK_ERR_BAD_INPUT);
             bf16_tile_to_f16<BN>(rawp + C::kDataBytes + C::kScaleBytes + sb * C::kBBytes, gthr, p.err);
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            if (pend >= 0) {
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(&cvt_full[pend]);
+            }
             tc_fence_after();
             tmem_st32(tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)(C::kACol0 + 32 * t), v);
+            pend = t;
+        }
+        if (pend >= 0) {
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(&cvt_full[t]);
+            mbar_arrive(&cvt_full[pend]);
         }
     } else {
         pdl_wait();
