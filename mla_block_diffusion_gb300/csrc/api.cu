@@ -131,6 +131,7 @@ struct dspark_handle {
     dspark_weights_t w;
     int num_sms;
     int samp_grid;
+    bool roll_resident;         // greedy one-sequence rollout with w2 on chip
     RopeTable rope;
     float scale_log2;
     CUtensorMap fc, lm_head;
@@ -458,6 +459,7 @@ dspark_status dspark_create(const dspark_geom_t *geom, const dspark_weights_t *w
         delete h;
         return DSPARK_ERR_CUDA;
     }
+    h->roll_resident = rollout_resident_setup(g.vocab, g.rank, h->samp_grid);
     // RoPE frequencies; YaRN "NTK-by-parts" ramp when yarn_factor > 1
     memset(&h->rope, 0, sizeof(h->rope));
     for (int j = 0; j < g.d_rope / 2; ++j) {
@@ -681,7 +683,7 @@ dspark_status dspark_markov_rollout(dspark_handle_t *h, const float *z, const in
     p.scratch = (unsigned long long *)((char *)ws + L.scratch);
     p.ctl = (SampleCtl *)((char *)ws + kCtlSample);
     p.err = (int *)((char *)ws + kCtlErr);
-    return cuda_status(launch_rollout(h->w2, p, h->samp_grid, (cudaStream_t)stream));
+    return cuda_status(launch_rollout(h->w2, p, h->samp_grid, h->roll_resident, (cudaStream_t)stream));
 }
 
 dspark_status dspark_kv_append(dspark_handle_t *h, const float *x_new, int n_max, const int32_t *n_new,

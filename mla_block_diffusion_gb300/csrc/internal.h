@@ -110,7 +110,10 @@ bool encode_bf16_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t c
 
 size_t rollout_scratch_words(int bs, int B, int grid);
 size_t verify_scratch_words(int bs, int B, int grid);
-cudaError_t launch_rollout(const CUtensorMap &w2_map, RolloutParams p, int grid, cudaStream_t st);
+cudaError_t launch_rollout(const CUtensorMap &w2_map, RolloutParams p, int grid, bool resident, cudaStream_t st);
+// Whether the greedy one-sequence rollout can hold w2 on chip for this
+// vocabulary, rank and grid (sets the kernel's shared-memory limit).
+bool rollout_resident_setup(int V, int r, int grid);
 // w2 tile geometry of the rollout (pairs per box row, boxes per stage); its
 // tensor map views w2 as uint32 pairs [r, V / 2] with boxes {box_w, 16}.
 __host__ __device__ void rollout_box(int V, int grid, int *box_w, int *nbox);

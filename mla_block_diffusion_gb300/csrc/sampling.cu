@@ -798,6 +798,372 @@ __global__ void __launch_bounds__(kSampThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
+// Greedy rollout of one sequence with the CTA's w2 slice held on chip.
+//
+// The slice (pairs [lo, hi), all r rows) is read from HBM once per launch:
+//  - rows [0, 128) of the primary pairs (thread t: pair lo + t) live in
+//    tensor memory, laid out as in the streaming kernel;
+//  - rows [128, 160) of the primary pairs live in 32 registers of their thread;
+//  - rows [0, 160) of the secondary pairs (lo + 512 + t, lanes of warp 0) live
+//    in shared memory;
+//  - rows [160, r) of every pair stay in shared memory: 16-row blocks in six
+//    slots, the same slots that first stage the load (block j in slot j % 6).
+// Between steps the CTAs do not meet at a barrier: each one publishes its best
+// greedy key for step i in a word of its own and reads every CTA's word. The
+// winner's w1 row is prefetched into L2 by the CTA that found it.
+// ---------------------------------------------------------------------------
+constexpr int kResSlots = 6;
+constexpr int kResTmemRows = 128;
+constexpr int kResRegRows = 32;
+constexpr int kResOnRows = kResTmemRows + kResRegRows;
+constexpr int kResSec = 32;
+constexpr int kResMaxRank = kResOnRows + kRollKC * kResSlots;
+constexpr int kResGatherPerLane = 8;  // key words read by each lane of the gathering warp
+
+struct ResLayout {  // dynamic shared memory, bytes
+    uint32_t stage_bytes, slots, sec, u, red, bars, total;
+    __host__ __device__ ResLayout(int V, int grid) {
+        int box_w, nbox;
+        rollout_box(V, grid, &box_w, &nbox);
+        stage_bytes = (uint32_t)(nbox * kRollKC * box_w * 4);
+        slots = 0;
+        sec = slots + kResSlots * stage_bytes;
+        u = sec + kResOnRows * kResSec * 4;
+        red = u + kResMaxRank * 2;
+        bars = red + 32 * 8;
+        total = bars + kResSlots * 8;
+    }
+};
+
+// Two fp32 chains of bf16 products: lo += u * w.lo, hi += u * w.hi, where u is
+// the low (HI = false) or high half of u2. The bf16 operands widen exactly, so
+// each step is one IEEE fp32 FMA with a single rounding (identical to fmaf on
+// the widened values).
+template <bool HI>
+DS_DEVINL void fma_bf16x2(float &lo, float &hi, uint32_t u2, uint32_t w) {
+    if (HI)
+        asm("{\n\t.reg .b16 wl, wh, ul, uh;\n\tmov.b32 {wl, wh}, %2;\n\tmov.b32 {ul, uh}, %3;\n\t"
+            "fma.rn.f32.bf16 %0, uh, wl, %0;\n\tfma.rn.f32.bf16 %1, uh, wh, %1;\n\t}"
+            : "+f"(lo), "+f"(hi)
+            : "r"(w), "r"(u2));
+    else
+        asm("{\n\t.reg .b16 wl, wh, ul, uh;\n\tmov.b32 {wl, wh}, %2;\n\tmov.b32 {ul, uh}, %3;\n\t"
+            "fma.rn.f32.bf16 %0, ul, wl, %0;\n\tfma.rn.f32.bf16 %1, ul, wh, %1;\n\t}"
+            : "+f"(lo), "+f"(hi)
+            : "r"(w), "r"(u2));
+}
+
+// Chains of this thread's pairs (four fp32 accumulators: primary lo/hi, secondary lo/hi).
+struct ResAcc {
+    float p0, p1, s0, s1;
+};
+
+// Eight rows k0 .. k0 + 7 (k0 a multiple of 8): u from s_u (bf16), the primary
+// pair's words in v, the secondary pair's (TWO) in column t of s_sec.
+template <bool TWO>
+DS_DEVINL void res_rows8(const uint32_t (&v)[8], int k0, const uint32_t (*s_sec)[kResSec], int t,
+                         const uint16_t *s_u, ResAcc &a) {
+    const uint4 uq = *(const uint4 *)(s_u + k0);
+    const uint32_t u2[4] = {uq.x, uq.y, uq.z, uq.w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        if (j & 1)
+            fma_bf16x2<true>(a.p0, a.p1, u2[j >> 1], v[j]);
+        else
+            fma_bf16x2<false>(a.p0, a.p1, u2[j >> 1], v[j]);
+        if (TWO) {
+            const uint32_t w = s_sec[k0 + j][t];
+            if (j & 1)
+                fma_bf16x2<true>(a.s0, a.s1, u2[j >> 1], w);
+            else
+                fma_bf16x2<false>(a.s0, a.s1, u2[j >> 1], w);
+        }
+    }
+}
+
+// One step's chains of this thread's pairs, k in order.
+template <bool TWO>
+DS_DEVINL void res_chain(uint32_t taddr, int r, const uint32_t (&wr)[kResRegRows], const uint8_t *slots,
+                         uint32_t stage_bytes, int box_w, int o0, int o1, const uint32_t (*s_sec)[kResSec], int t,
+                         const uint16_t *s_u, ResAcc &a) {
+    // rows [0, min(r, 128)) from tensor memory, 8 columns per load, two loads in flight
+    const int nck = min(r, kResTmemRows) / 8;
+    uint32_t va[8], vb[8];
+    tmem_ld8_issue(taddr, va);
+    for (int c = 0; c < nck; c += 2) {
+        tmem_ld_wait_tied(va);
+        if (c + 1 < nck) tmem_ld8_issue(taddr + 8u * (uint32_t)(c + 1), vb);
+        res_rows8<TWO>(va, 8 * c, s_sec, t, s_u, a);
+        if (c + 1 < nck) {
+            tmem_ld_wait_tied(vb);
+            if (c + 2 < nck) tmem_ld8_issue(taddr + 8u * (uint32_t)(c + 2), va);
+            res_rows8<TWO>(vb, 8 * (c + 1), s_sec, t, s_u, a);
+        }
+    }
+    // rows [128, min(r, 160)) from registers
+    if (r > kResTmemRows) {
+#pragma unroll
+        for (int j8 = 0; j8 < kResRegRows; j8 += 8) {
+            if (kResTmemRows + j8 < r) {
+                const uint32_t v[8] = {wr[j8], wr[j8 + 1], wr[j8 + 2], wr[j8 + 3],
+                                       wr[j8 + 4], wr[j8 + 5], wr[j8 + 6], wr[j8 + 7]};
+                res_rows8<TWO>(v, kResTmemRows + j8, s_sec, t, s_u, a);
+            }
+        }
+    }
+    // rows [160, r) from the shared-memory blocks
+    for (int j = kResOnRows / kRollKC; j < r / kRollKC; ++j) {
+        const uint32_t *w = (const uint32_t *)(slots + (size_t)(j % kResSlots) * stage_bytes);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint4 uq = *(const uint4 *)(s_u + kRollKC * j + 8 * h);
+            const uint32_t u2[4] = {uq.x, uq.y, uq.z, uq.w};
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const int row = 8 * h + kk;
+                if (kk & 1)
+                    fma_bf16x2<true>(a.p0, a.p1, u2[kk >> 1], w[row * box_w + o0]);
+                else
+                    fma_bf16x2<false>(a.p0, a.p1, u2[kk >> 1], w[row * box_w + o0]);
+                if (TWO) {
+                    if (kk & 1)
+                        fma_bf16x2<true>(a.s0, a.s1, u2[kk >> 1], w[row * box_w + o1]);
+                    else
+                        fma_bf16x2<false>(a.s0, a.s1, u2[kk >> 1], w[row * box_w + o1]);
+                }
+            }
+        }
+    }
+}
+
+// ell and the greedy key of one pair.
+DS_DEVINL unsigned long long res_pair_out(float d0, float d1, float2 z, int pp, float *ell, bool &bad) {
+    const float l0 = __fadd_rn(z.x, d0), l1 = __fadd_rn(z.y, d1);
+    *(float2 *)(ell + 2 * pp) = make_float2(l0, l1);
+    if (!isfinite(l0) || !isfinite(l1)) bad = true;
+    return max(argmax_key(l0, 2 * pp), argmax_key(l1, 2 * pp + 1));
+}
+
+// Split grid barrier (one thread): arrive once this CTA's earlier writes are
+// done, wait later. The generation read before arriving is the one to wait past.
+DS_DEVINL unsigned int grid_arrive(SampleCtl *ctl) {
+    volatile unsigned int *genp = &ctl->bar_gen;
+    const unsigned int gen = *genp;
+    __threadfence();
+    if (atomicAdd(&ctl->bar_count, 1u) + 1u == gridDim.x) {
+        atomicExch(&ctl->bar_count, 0u);
+        __threadfence();
+        atomicAdd(&ctl->bar_gen, 1u);
+    }
+    return gen;
+}
+DS_DEVINL bool grid_wait(SampleCtl *ctl, unsigned int gen, int *err) {
+    volatile unsigned int *genp = &ctl->bar_gen;
+    const unsigned long long t0 = globaltimer();
+    while (*genp == gen) {
+        if (globaltimer() - t0 > kWaitLimitNs) {
+            set_error(err, DSPARK_ERR_TIMEOUT);
+            return false;
+        }
+        __nanosleep(32);
+    }
+    __threadfence();
+    return true;
+}
+
+__global__ void __launch_bounds__(kSampThreads, 1)
+    rollout_greedy_resident_kernel(const __grid_constant__ CUtensorMap tmW2, RolloutParams p) {
+    extern __shared__ __align__(128) uint8_t rsm[];
+    __shared__ volatile int s_fail;
+    __shared__ uint32_t s_tmem_base;
+    __shared__ unsigned int s_gen;
+    __shared__ int s_tok;
+    const ResLayout RL(p.V, gridDim.x);
+    uint8_t *slots = rsm + RL.slots;
+    uint32_t(*s_sec)[kResSec] = (uint32_t(*)[kResSec])(rsm + RL.sec);
+    uint16_t *s_u = (uint16_t *)(rsm + RL.u);  // bf16 bits of w1[t_{i-1}]
+    unsigned long long *red = (unsigned long long *)(rsm + RL.red);
+    uint64_t *full = (uint64_t *)(rsm + RL.bars);
+
+    const int V = p.V, r = p.r, B = p.B;
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const int grid = gridDim.x;
+    unsigned long long *keys = p.scratch;  // [B][grid]: best greedy key of every CTA per step
+    const uint16_t *w1 = (const uint16_t *)p.w1;
+    int lo, hi;
+    quad_slice(V, lo, hi);
+    const bool any = hi > lo;
+    int box_w, nbox;
+    rollout_box(V, grid, &box_w, &nbox);
+    const int nblk = r / kRollKC;
+    const int nstage = min(nblk, kResOnRows / kRollKC);
+    const uint64_t pol = policy_evict_first();  // w2 is read once per launch
+    int issued = 0, waited = 0;                 // thread 0's counts of w2 blocks
+
+    if (t == 0) {
+        s_fail = 0;
+        for (int s = 0; s < kResSlots; ++s) mbar_init(&full[s], 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(&s_tmem_base, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    auto issue = [&](int j) {
+        const int s = j % kResSlots;
+        mbar_arrive_expect_tx(&full[s], RL.stage_bytes);
+        uint8_t *dst = slots + (size_t)s * RL.stage_bytes;
+        for (int b = 0; b < nbox; ++b)
+            tma_load_2d_hint(dst + (size_t)b * kRollKC * box_w * 4, &tmW2, lo + b * box_w, kRollKC * j, &full[s], pol);
+    };
+    if (t == 0 && any) {
+        tma_prefetch_desc(&tmW2);
+        for (int j = 0; j < min(nblk, kResSlots); ++j) issue(j);
+        issued = min(nblk, kResSlots);
+    }
+    // The key words start at zero (a published key never is); every CTA's
+    // zeroing is done before any CTA publishes (split grid barrier below).
+    for (int w = blockIdx.x * blockDim.x + t; w < B * grid; w += grid * blockDim.x) keys[w] = 0ull;
+    int a = p.anchor[0];
+    if (a < 0 || a >= V) {
+        set_error(p.err, DSPARK_ERR_OOB);
+        a = 0;
+    }
+    for (int k = t; k < r; k += blockDim.x) s_u[k] = w1[(size_t)a * r + k];
+    __syncthreads();
+    if (t == 32) s_gen = grid_arrive(p.ctl);
+
+    // load: blocks 0 .. nstage-1 go to tensor memory / registers / s_sec
+    const uint32_t taddr = s_tmem_base + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(128 * (warp >> 2));
+    const int q0 = t, q1 = t + kSampThreads;
+    const bool has0 = lo + q0 < hi, has1 = lo + q1 < hi;
+    // word offsets of the pairs in a slot (row 0); lanes without a pair read word 0
+    const int o0 = has0 ? (q0 / box_w) * kRollKC * box_w + q0 % box_w : 0;
+    const int o1 = has1 ? (q1 / box_w) * kRollKC * box_w + q1 % box_w : 0;
+    uint32_t wr[kResRegRows];
+#pragma unroll
+    for (int j = 0; j < kResRegRows; ++j) wr[j] = 0u;
+    bool ok = true;
+    for (int j = 0; j < nstage; ++j) {
+        const int s = j % kResSlots;
+        bool got = ok && any && mbar_wait_bounded(&full[s], (uint32_t)((j / kResSlots) & 1), &s_fail);
+        got = __all_sync(0xffffffffu, got);
+        if (got) {
+            const uint32_t *w = (const uint32_t *)(slots + (size_t)s * RL.stage_bytes);
+            if (j < kResTmemRows / kRollKC) {
+                uint32_t v[16];
+#pragma unroll
+                for (int kk = 0; kk < 16; ++kk) v[kk] = has0 ? w[kk * box_w + o0] : 0u;
+                tmem_st16(taddr + 16u * (uint32_t)j, v);
+            } else if (j == kResTmemRows / kRollKC) {
+#pragma unroll
+                for (int kk = 0; kk < 16; ++kk) wr[kk] = has0 ? w[kk * box_w + o0] : 0u;
+            } else {
+#pragma unroll
+                for (int kk = 0; kk < 16; ++kk) wr[16 + kk] = has0 ? w[kk * box_w + o0] : 0u;
+            }
+            if (t < kResSec)
+                for (int kk = 0; kk < 16; ++kk) s_sec[kRollKC * j + kk][t] = has1 ? w[kk * box_w + o1] : 0u;
+            if (t == 0) waited = j + 1;
+        }
+        __syncthreads();
+        ok = !s_fail;
+        if (t == 0 && ok && any && j + kResSlots < nblk) {
+            issue(j + kResSlots);
+            issued = j + kResSlots + 1;
+        }
+    }
+    tmem_st_wait();
+    for (int j = nstage; j < nblk && ok && any; ++j) {
+        if (!mbar_wait_bounded(&full[j % kResSlots], (uint32_t)((j / kResSlots) & 1), &s_fail)) break;
+        if (t == 0) waited = j + 1;
+    }
+    if (t == 32 && !grid_wait(p.ctl, s_gen, p.err)) s_fail = 1;
+    __syncthreads();
+    ok = !s_fail;
+    tc_fence_after();
+
+    const bool two = __any_sync(0xffffffffu, has1);
+    for (int i = 0; i < B && ok; ++i) {
+        const float *zi = p.z + (size_t)i * V;
+        float *elli = p.ell + (size_t)i * V;
+        const float2 z0 = has0 ? *(const float2 *)(zi + 2 * (lo + q0)) : make_float2(0.f, 0.f);
+        const float2 z1 = has1 ? *(const float2 *)(zi + 2 * (lo + q1)) : make_float2(0.f, 0.f);
+        ResAcc acc = {0.f, 0.f, 0.f, 0.f};
+        if (two)
+            res_chain<true>(taddr, r, wr, slots, RL.stage_bytes, box_w, o0, o1, s_sec, t, s_u, acc);
+        else
+            res_chain<false>(taddr, r, wr, slots, RL.stage_bytes, box_w, o0, o1, s_sec, t, s_u, acc);
+        unsigned long long best = 0ull;
+        bool bad = false;
+        if (has0) best = res_pair_out(acc.p0, acc.p1, z0, lo + q0, elli, bad);
+        if (has1) best = max(best, res_pair_out(acc.s0, acc.s1, z1, lo + q1, elli, bad));
+        if (bad) set_error(p.err, DSPARK_ERR_BAD_INPUT);
+        best = warp_max_u64(best);
+        if (lane == 0) red[warp] = best;
+        __syncthreads();  // every warp's best is in red; s_u is no longer read this step
+        if (warp == 0) {
+            unsigned long long m = lane < kSampThreads / 32 ? red[lane] : 0ull;
+            m = warp_max_u64(m);
+            if (lane == 0) {
+                st_relaxed_u64(&keys[(size_t)i * grid + blockIdx.x], m ? m : 1ull);
+                if (m && i + 1 < B) prefetch_l2_bulk(w1 + (size_t)argmax_token(m) * r, (uint32_t)r * 2u);
+            }
+            // every CTA's key of step i: lane l reads CTAs l, l + 32, ... (keys are
+            // never zero once published); short sleeps between rounds
+            const unsigned long long *kp = keys + (size_t)i * grid;
+            unsigned long long g = 0ull;
+            uint32_t pending = 0u;
+            for (int c = 0; lane + 32 * c < grid; ++c) pending |= 1u << c;
+            const unsigned long long t0 = globaltimer();
+            while (__any_sync(0xffffffffu, pending != 0u)) {
+                unsigned long long kv[kResGatherPerLane];
+#pragma unroll
+                for (int c = 0; c < kResGatherPerLane; ++c)
+                    kv[c] = (pending >> c) & 1u ? ld_relaxed_u64(kp + lane + 32 * c) : 0ull;
+#pragma unroll
+                for (int c = 0; c < kResGatherPerLane; ++c)
+                    if (kv[c]) {
+                        g = max(g, kv[c]);
+                        pending &= ~(1u << c);
+                    }
+                if (pending) {
+                    if (s_fail || globaltimer() - t0 > kWaitLimitNs) {
+                        set_error(p.err, DSPARK_ERR_TIMEOUT);
+                        s_fail = 1;
+                        pending = 0u;
+                    } else {
+                        __nanosleep(20);
+                    }
+                }
+            }
+            g = warp_max_u64(g);
+            if (lane == 0) {
+                const int tok = argmax_token(g);
+                s_tok = tok;
+                if (blockIdx.x == 0) p.tokens[i] = tok;
+            }
+        }
+        __syncthreads();  // the token of step i is in s_tok
+        ok = !s_fail;
+        if (ok && i + 1 < B) {
+            const int tok = s_tok;
+            for (int k4 = t; 4 * k4 < r; k4 += blockDim.x)
+                *(uint2 *)(s_u + 4 * k4) = *(const uint2 *)(w1 + (size_t)tok * r + 4 * k4);
+        }
+        __syncthreads();  // s_u holds w1[t_i]
+    }
+    if (t == 0)
+        for (int j = waited; j < issued; ++j) mbar_drain(&full[j % kResSlots], (uint32_t)((j / kResSlots) & 1));
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(s_tmem_base, 512);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Verification
 // ---------------------------------------------------------------------------
 // Greedy: row argmax keys (zero between launches) then a finalize kernel that
@@ -1256,9 +1622,30 @@ int sampling_max_grid(int num_sms, int V) {
     return (a >= 1 && b >= 1 && c >= 1) ? num_sms : 0;
 }
 
-cudaError_t launch_rollout(const CUtensorMap &w2_map, RolloutParams p, int grid, cudaStream_t st) {
+// The resident greedy rollout needs r a multiple of 16 up to 256, at most
+// kResSec secondary pairs per CTA, a key word per CTA read by one thread each,
+// and its shared memory.
+bool rollout_resident_setup(int V, int r, int grid) {
+    if (r <= 0 || r % kRollKC != 0 || r > kResMaxRank || grid <= 0 || grid > 32 * kResGatherPerLane) return false;
+    if (4 * ((V / 8 + grid - 1) / grid) > kSampThreads + kResSec) return false;
+    const ResLayout RL(V, grid);
+    int a = 0;
+    if (cudaFuncSetAttribute(rollout_greedy_resident_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)RL.total) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, rollout_greedy_resident_kernel, kSampThreads, RL.total) !=
+            cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    return a >= 1;
+}
+
+cudaError_t launch_rollout(const CUtensorMap &w2_map, RolloutParams p, int grid, bool resident, cudaStream_t st) {
     CUtensorMap tm = w2_map;
     void *args[] = {&tm, &p};
+    if (resident && p.bs == 1 && p.draft_mode == DSPARK_GREEDY && ((uintptr_t)p.w1 & 15u) == 0)
+        return cudaLaunchCooperativeKernel((void *)rollout_greedy_resident_kernel, dim3(grid), dim3(kSampThreads),
+                                           args, ResLayout(p.V, grid).total, st);
     return cudaLaunchCooperativeKernel((void *)rollout_kernel, dim3(grid), dim3(kSampThreads), args,
                                        rollout_ring_bytes(p.V, grid), st);
 }
