@@ -238,9 +238,11 @@ cudaError_t gemm_t(const CUtensorMap &A, const CUtensorMap &A2, const CUtensorMa
 }
 
 cudaError_t gemm(const dspark_handle *h, const CUtensorMap &A, const CUtensorMap *A2, const CUtensorMap &B, int n_out,
-                 int K, int M, int epi, float *out_f32, __nv_bfloat16 *out_bf16, int ldo, void *ws, cudaStream_t st) {
+                 int K, int M, int epi, float *out_f32, __nv_bfloat16 *out_bf16, int ldo, void *ws, cudaStream_t st,
+                 const L2Prefetch *pf = nullptr) {
     GemmParams p;
     memset(&p, 0, sizeof(p));
+    if (pf) p.pf = *pf;
     p.n_out = n_out;
     p.K = K;
     p.M = M;
@@ -324,6 +326,33 @@ cudaError_t gemm_q(const dspark_handle *h, const QMat &A, const QMat *A2, const 
         if (bn == 64) return gemm_q_t<64, DSPARK_FMT_MXFP4>(A, A2, B, p, h->num_sms, st);
     }
     return cudaErrorInvalidValue;
+}
+
+// The bytes of a (possibly quantised) weight matrix of rows x cols, as L2
+// prefetch ranges: data, then the scales of the weight-only formats.
+L2Prefetch mat_prefetch(const dspark_mat_t &m, int fmt, uint64_t rows, uint64_t cols) {
+    L2Prefetch pf;
+    memset(&pf, 0, sizeof(pf));
+    uint64_t db = rows * cols * 2, sb = 0;
+    if (fmt == DSPARK_FMT_FP8) {
+        db = rows * cols;
+        sb = rows * 4;
+    } else if (fmt == DSPARK_FMT_NVFP4) {
+        db = rows * cols / 2;
+        sb = rows * cols / 16;
+    } else if (fmt == DSPARK_FMT_MXFP4) {
+        db = rows * cols / 2;
+        sb = rows * cols / 32;
+    }
+    if (m.data && aligned16(m.data)) {
+        pf.ptr[0] = (const uint8_t *)m.data;
+        pf.bytes[0] = db & ~15ull;
+    }
+    if (sb && m.scale && aligned16(m.scale)) {
+        pf.ptr[1] = (const uint8_t *)m.scale;
+        pf.bytes[1] = sb & ~15ull;
+    }
+    return pf;
 }
 
 dspark_status check_geom(const dspark_geom_t *g) {
@@ -607,8 +636,10 @@ dspark_status dspark_draft_block(dspark_handle_t *h, float *x, const dspark_kv_t
     for (int l = 0; l < g.n_layers; ++l) {
         const dspark_layer_weights_t &W = h->w.layers[l];
         RUN(launch_rmsnorm(x, g.hidden, W.attn_norm, g.hidden, g.eps, hn, g.hidden, nullptr, 0, M, err, s));
+        // q_b's weights stream into L2 while the latency-bound q_a || kv_a GEMM runs
+        const L2Prefetch pf_qb = mat_prefetch(W.w_q_b, g.weight_format, (uint64_t)g.n_heads * qhd, g.q_lora);
         RUN(gemm(h, h->qkv_a[l], nullptr, h->b_hn, g.q_lora + kvd, g.hidden, M, EPI_STORE, qkv, nullptr,
-                 g.q_lora + kvd, ws, s));
+                 g.q_lora + kvd, ws, s, &pf_qb));
         RUN(launch_latent(qkv, g.q_lora + kvd, g.q_lora, g.kv_lora, g.d_rope, W.q_a_norm, W.kv_a_norm, g.eps,
                           kv->ctx_len, g.block, kv->max_ctx, h->rope, cq, blk, M, err, s));
         RUN(quant ? gemm_q(h, h->qq_b[l], nullptr, h->b_cq, g.n_heads * qhd, g.q_lora, M, EPI_STORE, q, nullptr,

@@ -67,6 +67,7 @@ struct TcAttnParams {
     float *part_o;                // [bs, splits, R, DV]
     float *part_ml;               // [bs, splits, R, 2]
     int *err;
+    L2Prefetch pf;                // pulled into L2 by the MMA thread before its dependency wait
 };
 
 // 16 columns of the warp's lane quadrant without the completion wait (several
@@ -81,6 +82,13 @@ DS_DEVINL void tmem_ld16_nw(uint32_t taddr, uint32_t (&r)[16]) {
 }
 DS_DEVINL void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// 2^x by the MUFU instruction (relative error about 2^-22, flushes denormals).
+DS_DEVINL float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 DS_DEVINL uint32_t pack_bf16x2(float lo, float hi) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<const uint32_t *>(&v);
@@ -91,8 +99,10 @@ DS_DEVINL bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
     return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, abort));
 }
 
+// Shared memory keeps one CTA per SM; the launch bound of two only caps the
+// registers, so the next kernel's CTAs can become resident beside this one.
 template <int DQK, int DV>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(192, 2)
     mla_attention_tc_kernel(const __grid_constant__ CUtensorMap tmPool, const __grid_constant__ CUtensorMap tmBlk,
                             const TcAttnParams p) {
     using C = TcCfg<DQK, DV>;
@@ -149,6 +159,9 @@ __global__ void __launch_bounds__(192, 1)
     const int nch = c_end > c_begin ? c_end - c_begin : 0;
     int issued = 0;
 
+    if (threadIdx.x == 32)
+        l2_prefetch_share(p.pf, blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z),
+                          gridDim.x * gridDim.y * gridDim.z);
     if (warp != 0 || lane != 0) pdl_wait();
     if (warp == 0) {
         if (lane == 0) {
@@ -193,12 +206,16 @@ __global__ void __launch_bounds__(192, 1)
                 if (!mbar_wait_bounded(&kv_full[st], (uint32_t)((i / kTcStages) & 1), &s_abort)) return false;
                 if (i > 0 && !mbar_wait_bounded(s_free, (uint32_t)((i - 1) & 1), &s_abort)) return false;
                 tc_fence_after();
-                const uint32_t base = smem_u32(sKV + st * C::kTileBytes);
-#pragma unroll 1
-                for (int kk = 0; kk < C::kDQKP / 16; ++kk) {
-                    const uint64_t bd = sdesc_k_sw128(base + (kk >> 2) * C::kBoxBytes) + (uint64_t)(2 * (kk & 3));
-                    mma_bf16_tmem_a(tmem + C::kSCol, tmem + C::kQCol + 8 * kk, bd, idS, kk > 0 ? 1u : 0u);
-                }
+                // Descriptors as one base plus immediates: the 14-bit start-address field
+                // of box j, slice k is (base + 8 KB j + 32 B k) >> 4, never past 256 KB.
+                // A short issue sequence keeps this thread ahead of the tensor pipe even
+                // when a softmax warp shares its scheduler.
+                const uint64_t bd0 = sdesc_k_sw128(smem_u32(sKV + st * C::kTileBytes));
+#pragma unroll
+                for (int kk = 0; kk < C::kDQKP / 16; ++kk)
+                    mma_bf16_tmem_a(tmem + C::kSCol, tmem + C::kQCol + 8 * kk,
+                                    bd0 + (uint64_t)((kk >> 2) * (C::kBoxBytes >> 4) + 2 * (kk & 3)), idS,
+                                    kk > 0 ? 1u : 0u);
                 mma_commit(s_full);
                 return true;
             };
@@ -238,31 +255,23 @@ __global__ void __launch_bounds__(192, 1)
                 u[j] = (rv && e < DQK) ? __ldg((const uint4 *)(qrow + e)) : make_uint4(0u, 0u, 0u, 0u);
             }
         };
-        uint4 qa[8], qb[8];
-        qload(0, qa);
-#pragma unroll 1
-        for (int c32 = 0; c32 < C::kDQKP / 2; c32 += 64) {
-            if (c32 + 32 < C::kDQKP / 2) qload(c32 + 32, qb);  // next batch in flight while this one is stored
+        // nine batches of 32 columns, three in flight
+        constexpr int kQBatches = C::kDQKP / 64;
+        uint4 qv[3][8];
+#pragma unroll
+        for (int bq = 0; bq < 3 && bq < kQBatches; ++bq) qload(32 * bq, qv[bq]);
+#pragma unroll
+        for (int bq = 0; bq < kQBatches; ++bq) {
             uint32_t v[32];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                v[4 * j] = qa[j].x;
-                v[4 * j + 1] = qa[j].y;
-                v[4 * j + 2] = qa[j].z;
-                v[4 * j + 3] = qa[j].w;
+                v[4 * j] = qv[bq % 3][j].x;
+                v[4 * j + 1] = qv[bq % 3][j].y;
+                v[4 * j + 2] = qv[bq % 3][j].z;
+                v[4 * j + 3] = qv[bq % 3][j].w;
             }
-            tmem_st32(tl + C::kQCol + c32, v);
-            if (c32 + 32 < C::kDQKP / 2) {
-                if (c32 + 64 < C::kDQKP / 2) qload(c32 + 64, qa);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    v[4 * j] = qb[j].x;
-                    v[4 * j + 1] = qb[j].y;
-                    v[4 * j + 2] = qb[j].z;
-                    v[4 * j + 3] = qb[j].w;
-                }
-                tmem_st32(tl + C::kQCol + c32 + 32, v);
-            }
+            tmem_st32(tl + C::kQCol + 32 * bq, v);
+            if (bq + 3 < kQBatches) qload(32 * (bq + 3), qv[bq % 3]);
         }
         tmem_st_wait();
         tc_fence_before();
@@ -287,14 +296,14 @@ __global__ void __launch_bounds__(192, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(s_free);
-            float s[64];
+            // the maximum of the raw scores, then scaled (the scale is positive and
+            // rounding monotone, so this is the maximum of the scaled scores)
+            const bool full = nvalid >= kTcKeys;
             float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int j = 0; j < 64; ++j) {
-                s[j] = j < nvalid ? __uint_as_float(sr[j >> 4][j & 15]) * p.scale_log2 : -INFINITY;
-                mx4[j & 3] = fmaxf(mx4[j & 3], s[j]);
-            }
-            const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+            for (int j = 0; j < 64; ++j)
+                if (full || j < nvalid) mx4[j & 3] = fmaxf(mx4[j & 3], __uint_as_float(sr[j >> 4][j & 15]));
+            const float mx = __fmul_rn(fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])), p.scale_log2);
             const float m_new = fmaxf(m_ref, mx);
             const bool rescale = (m_ref == -INFINITY) ? (m_new != -INFINITY) : (m_new > m_ref + kTcRescaleLog2);
             float corr = 1.f;
@@ -305,10 +314,14 @@ __global__ void __launch_bounds__(192, 1)
             uint32_t pk[32];
             float ls4[4] = {0.f, 0.f, 0.f, 0.f};
             const bool live = m_ref != -INFINITY;
+            const float nm = live ? -m_ref : 0.f;
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
-                const float p0 = live ? exp2f(s[2 * j] - m_ref) : 0.f;
-                const float p1 = live ? exp2f(s[2 * j + 1] - m_ref) : 0.f;
+                // p = 2^(s * scale_log2 - m): one FMA and one MUFU ex2 per score
+                float p0 = ex2_approx(__fmaf_rn(__uint_as_float(sr[(2 * j) >> 4][(2 * j) & 15]), p.scale_log2, nm));
+                float p1 = ex2_approx(__fmaf_rn(__uint_as_float(sr[(2 * j + 1) >> 4][(2 * j + 1) & 15]), p.scale_log2, nm));
+                if (!live || (!full && 2 * j >= nvalid)) p0 = 0.f;
+                if (!live || (!full && 2 * j + 1 >= nvalid)) p1 = 0.f;
                 ls4[j & 3] += p0 + p1;
                 pk[j] = pack_bf16x2(p0, p1);
             }
@@ -436,6 +449,7 @@ cudaError_t launch_attention_tc(const CUtensorMap &pool_map, const CUtensorMap &
     p.part_o = a.part_o;
     p.part_ml = a.part_ml;
     p.err = a.err;
+    p.pf = a.pf;
     const int tiles = (a.R + kTcRows - 1) / kTcRows;
     dim3 grid(tiles * C::kParts, a.splits, bs);
     cudaError_t e = launch_pdl(mla_attention_tc_kernel<576, 512>, grid, dim3(192), (size_t)C::kSmem, st, pool_map,

@@ -281,6 +281,26 @@ DS_DEVINL void prefetch_l2_bulk(const void *p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
+// Up to two byte ranges (16-byte aligned starts, sizes multiples of 16) that a
+// kernel pulls into L2 for the kernel that consumes them next: weights that do
+// not depend on anything, streamed while this kernel leaves HBM idle.
+struct L2Prefetch {
+    const uint8_t *ptr[2];
+    unsigned long long bytes[2];
+};
+
+// One thread per CTA: the CTA's share of the ranges, in 64 KB prefetches.
+DS_DEVINL void l2_prefetch_range(const uint8_t *ptr, unsigned long long bytes, unsigned int cta, unsigned int ctas) {
+    constexpr unsigned long long kChunk = 65536;
+#pragma unroll 1
+    for (unsigned long long off = (unsigned long long)cta * kChunk; off < bytes; off += (unsigned long long)ctas * kChunk)
+        prefetch_l2_bulk(ptr + off, (uint32_t)(bytes - off < kChunk ? bytes - off : kChunk));
+}
+DS_DEVINL void l2_prefetch_share(const L2Prefetch &pf, unsigned int cta, unsigned int ctas) {
+    l2_prefetch_range(pf.ptr[0], pf.bytes[0], cta, ctas);
+    l2_prefetch_range(pf.ptr[1], pf.bytes[1], cta, ctas);
+}
+
 DS_DEVINL void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }

@@ -52,6 +52,7 @@ struct GemmParams {
     // by gscale / gscale2 (NVFP4 per-tensor scales). Unused for bf16 weights.
     const float *qscale, *qscale2;
     float gscale, gscale2;
+    L2Prefetch pf;      // weights of a later kernel, pulled into L2 by the producer
 };
 
 // Per-row output multiplier of a weight-only quantised matrix.
@@ -257,6 +258,7 @@ __global__ void __launch_bounds__(192, 1)
                     tma_load_2d_hint(a + 8192, &tmA, kb * 64, tile * 128 + 64, &full[s], pol);
                 }
             }
+            l2_prefetch_share(p.pf, (unsigned int)cta, (unsigned int)p.grid);
             pdl_wait();
             for (long long it = 0; it < pre; ++it)
                 tma_load_2d(sB + (int)it * C::kBBytes, &tmB, (int)((u0 + it) % p.KB) * 64, 0, &full[(int)it]);
