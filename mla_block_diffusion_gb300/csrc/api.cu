@@ -219,9 +219,33 @@ Layout layout_for(const dspark_handle *h, int bs, int max_ctx) {
     return L;
 }
 
+// Grid of a weight GEMM: about `per` units per CTA, at most one CTA per SM. A
+// pending output (the consumer sums the split partials) needs every CTA's range
+// within one tile (grid >= tiles) and few CTAs per tile; otherwise, or when no
+// pending output is asked for, the GEMM reduces in place (pend->part = nullptr).
+void gemm_grid(GemmParams &p, int per, int num_sms, int BN, GemmPending *pend) {
+    long long grid = p.units / per;
+    if (grid > num_sms) grid = num_sms;
+    if (grid < 1) grid = 1;
+    if (pend) {
+        memset(pend, 0, sizeof(*pend));
+        const long long g2 = grid < p.tiles ? p.tiles : grid;
+        if (!p.paired && p.tiles <= num_sms && g2 <= p.units && p.units * g2 < (1ll << 31)) {
+            grid = g2;
+            p.epi = EPI_PENDING;
+            pend->part = p.partials;
+            pend->units = (int)p.units;
+            pend->grid = (int)grid;
+            pend->KB = p.KB;
+            pend->BN = BN;
+        }
+    }
+    p.grid = (int)grid;
+}
+
 template <int BN>
 cudaError_t gemm_t(const CUtensorMap &A, const CUtensorMap &A2, const CUtensorMap &B, GemmParams p, int num_sms,
-                   cudaStream_t st) {
+                   cudaStream_t st, GemmPending *pend) {
     using C = GemmCfg<BN>;
     static bool attr = false;
     if (!attr) {
@@ -230,16 +254,13 @@ cudaError_t gemm_t(const CUtensorMap &A, const CUtensorMap &A2, const CUtensorMa
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    long long grid = p.units / 4;
-    if (grid > num_sms) grid = num_sms;
-    if (grid < 1) grid = 1;
-    p.grid = (int)grid;
+    gemm_grid(p, 4, num_sms, BN, pend);
     return launch_pdl(gemm_swapab_kernel<BN>, dim3(p.grid), dim3(192), (size_t)C::kSmemBytes, st, A, A2, B, p);
 }
 
 cudaError_t gemm(const dspark_handle *h, const CUtensorMap &A, const CUtensorMap *A2, const CUtensorMap &B, int n_out,
                  int K, int M, int epi, float *out_f32, __nv_bfloat16 *out_bf16, int ldo, void *ws, cudaStream_t st,
-                 const L2Prefetch *pf = nullptr) {
+                 const L2Prefetch *pf = nullptr, GemmPending *pend = nullptr) {
     GemmParams p;
     memset(&p, 0, sizeof(p));
     if (pf) p.pf = *pf;
@@ -260,17 +281,17 @@ cudaError_t gemm(const dspark_handle *h, const CUtensorMap &A, const CUtensorMap
     p.partials = (float *)((char *)ws + kCtlBytes);  // first region after the control block
     const CUtensorMap &a2 = A2 ? *A2 : A;
     switch (bn_for(M)) {
-        case 16: return gemm_t<16>(A, a2, B, p, h->num_sms, st);
-        case 32: return gemm_t<32>(A, a2, B, p, h->num_sms, st);
-        case 64: return gemm_t<64>(A, a2, B, p, h->num_sms, st);
-        case 128: return gemm_t<128>(A, a2, B, p, h->num_sms, st);
-        default: return gemm_t<224>(A, a2, B, p, h->num_sms, st);
+        case 16: return gemm_t<16>(A, a2, B, p, h->num_sms, st, pend);
+        case 32: return gemm_t<32>(A, a2, B, p, h->num_sms, st, pend);
+        case 64: return gemm_t<64>(A, a2, B, p, h->num_sms, st, pend);
+        case 128: return gemm_t<128>(A, a2, B, p, h->num_sms, st, pend);
+        default: return gemm_t<224>(A, a2, B, p, h->num_sms, st, pend);
     }
 }
 
 template <int BN, int FMT>
 cudaError_t gemm_q_t(const QMat &A, const QMat *A2, const CUtensorMap &B, GemmParams p, int num_sms,
-                     cudaStream_t st) {
+                     cudaStream_t st, GemmPending *pend) {
     using C = GemmQCfg<BN, FMT>;
     static bool attr = false;
     if (!attr) {
@@ -281,10 +302,7 @@ cudaError_t gemm_q_t(const QMat &A, const QMat *A2, const CUtensorMap &B, GemmPa
     }
     p.KB = (p.K + C::kKR - 1) / C::kKR;
     p.units = (long long)p.tiles * p.KB;
-    long long grid = p.units / 2;
-    if (grid > num_sms) grid = num_sms;
-    if (grid < 1) grid = 1;
-    p.grid = (int)grid;
+    gemm_grid(p, 2, num_sms, BN, pend);
     p.qscale = A.rowscale;
     p.qscale2 = A2 ? A2->rowscale : nullptr;
     p.gscale = A.gscale;
@@ -295,7 +313,8 @@ cudaError_t gemm_q_t(const QMat &A, const QMat *A2, const CUtensorMap &B, GemmPa
 }
 
 cudaError_t gemm_q(const dspark_handle *h, const QMat &A, const QMat *A2, const CUtensorMap &B, int n_out, int K, int M,
-                   int epi, float *out_f32, __nv_bfloat16 *out_bf16, int ldo, void *ws, cudaStream_t st) {
+                   int epi, float *out_f32, __nv_bfloat16 *out_bf16, int ldo, void *ws, cudaStream_t st,
+                   GemmPending *pend = nullptr) {
     GemmParams p;
     memset(&p, 0, sizeof(p));
     p.n_out = n_out;
@@ -313,17 +332,17 @@ cudaError_t gemm_q(const dspark_handle *h, const QMat &A, const QMat *A2, const 
     p.partials = (float *)((char *)ws + kCtlBytes);
     const int bn = bn_for(M);
     if (h->g.weight_format == DSPARK_FMT_FP8) {
-        if (bn == 16) return gemm_q_t<16, DSPARK_FMT_FP8>(A, A2, B, p, h->num_sms, st);
-        if (bn == 32) return gemm_q_t<32, DSPARK_FMT_FP8>(A, A2, B, p, h->num_sms, st);
-        if (bn == 64) return gemm_q_t<64, DSPARK_FMT_FP8>(A, A2, B, p, h->num_sms, st);
+        if (bn == 16) return gemm_q_t<16, DSPARK_FMT_FP8>(A, A2, B, p, h->num_sms, st, pend);
+        if (bn == 32) return gemm_q_t<32, DSPARK_FMT_FP8>(A, A2, B, p, h->num_sms, st, pend);
+        if (bn == 64) return gemm_q_t<64, DSPARK_FMT_FP8>(A, A2, B, p, h->num_sms, st, pend);
     } else if (h->g.weight_format == DSPARK_FMT_NVFP4) {
-        if (bn == 16) return gemm_q_t<16, DSPARK_FMT_NVFP4>(A, A2, B, p, h->num_sms, st);
-        if (bn == 32) return gemm_q_t<32, DSPARK_FMT_NVFP4>(A, A2, B, p, h->num_sms, st);
-        if (bn == 64) return gemm_q_t<64, DSPARK_FMT_NVFP4>(A, A2, B, p, h->num_sms, st);
+        if (bn == 16) return gemm_q_t<16, DSPARK_FMT_NVFP4>(A, A2, B, p, h->num_sms, st, pend);
+        if (bn == 32) return gemm_q_t<32, DSPARK_FMT_NVFP4>(A, A2, B, p, h->num_sms, st, pend);
+        if (bn == 64) return gemm_q_t<64, DSPARK_FMT_NVFP4>(A, A2, B, p, h->num_sms, st, pend);
     } else {
-        if (bn == 16) return gemm_q_t<16, DSPARK_FMT_MXFP4>(A, A2, B, p, h->num_sms, st);
-        if (bn == 32) return gemm_q_t<32, DSPARK_FMT_MXFP4>(A, A2, B, p, h->num_sms, st);
-        if (bn == 64) return gemm_q_t<64, DSPARK_FMT_MXFP4>(A, A2, B, p, h->num_sms, st);
+        if (bn == 16) return gemm_q_t<16, DSPARK_FMT_MXFP4>(A, A2, B, p, h->num_sms, st, pend);
+        if (bn == 32) return gemm_q_t<32, DSPARK_FMT_MXFP4>(A, A2, B, p, h->num_sms, st, pend);
+        if (bn == 64) return gemm_q_t<64, DSPARK_FMT_MXFP4>(A, A2, B, p, h->num_sms, st, pend);
     }
     return cudaErrorInvalidValue;
 }
@@ -633,21 +652,39 @@ dspark_status dspark_draft_block(dspark_handle_t *h, float *x, const dspark_kv_t
         if ((call) != cudaSuccess) return DSPARK_ERR_CUDA; \
     } while (0)
     const bool quant = g.weight_format != DSPARK_FMT_BF16;
+    // The q_a || kv_a, q_b, o_proj and down GEMMs leave their split partials
+    // pending; the next kernel (latent norms, q absorption, RMSNorm with the
+    // residual add) sums them while reading its input. Off when the row kernels
+    // on clusters do not fit the geometry.
+    const bool defer = row_cluster_fits(g.hidden) && row_cluster_fits(g.q_lora + kvd);
+    GemmPending pend_x, pend_qkv, pend_q, pend_o;  // part == nullptr: the output was reduced in place
+    memset(&pend_x, 0, sizeof(pend_x));
+    GemmPending *const want_qkv = defer ? &pend_qkv : nullptr, *const want_q = defer ? &pend_q : nullptr;
+    GemmPending *const want_o = defer ? &pend_o : nullptr, *const want_x = defer ? &pend_x : nullptr;
     for (int l = 0; l < g.n_layers; ++l) {
         const dspark_layer_weights_t &W = h->w.layers[l];
-        RUN(launch_rmsnorm(x, g.hidden, W.attn_norm, g.hidden, g.eps, hn, g.hidden, nullptr, 0, M, err, s));
+        if (defer)
+            RUN(launch_rmsnorm_cluster(x, g.hidden, &pend_x, true, W.attn_norm, g.hidden, g.eps, hn, g.hidden, nullptr,
+                                       0, M, err, s));
+        else
+            RUN(launch_rmsnorm(x, g.hidden, W.attn_norm, g.hidden, g.eps, hn, g.hidden, nullptr, 0, M, err, s));
         // q_b's weights stream into L2 while the latency-bound q_a || kv_a GEMM runs
         const L2Prefetch pf_qb = mat_prefetch(W.w_q_b, g.weight_format, (uint64_t)g.n_heads * qhd, g.q_lora);
         RUN(gemm(h, h->qkv_a[l], nullptr, h->b_hn, g.q_lora + kvd, g.hidden, M, EPI_STORE, qkv, nullptr,
-                 g.q_lora + kvd, ws, s, &pf_qb));
-        RUN(launch_latent(qkv, g.q_lora + kvd, g.q_lora, g.kv_lora, g.d_rope, W.q_a_norm, W.kv_a_norm, g.eps,
-                          kv->ctx_len, g.block, kv->max_ctx, h->rope, cq, blk, M, err, s));
+                 g.q_lora + kvd, ws, s, &pf_qb, want_qkv));
+        if (defer)
+            RUN(launch_latent_cluster(qkv, g.q_lora + kvd, &pend_qkv, g.q_lora, g.kv_lora, g.d_rope, W.q_a_norm,
+                                      W.kv_a_norm, g.eps, kv->ctx_len, g.block, kv->max_ctx, h->rope, cq, blk, M, err,
+                                      s));
+        else
+            RUN(launch_latent(qkv, g.q_lora + kvd, g.q_lora, g.kv_lora, g.d_rope, W.q_a_norm, W.kv_a_norm, g.eps,
+                              kv->ctx_len, g.block, kv->max_ctx, h->rope, cq, blk, M, err, s));
         RUN(quant ? gemm_q(h, h->qq_b[l], nullptr, h->b_cq, g.n_heads * qhd, g.q_lora, M, EPI_STORE, q, nullptr,
-                           g.n_heads * qhd, ws, s)
+                           g.n_heads * qhd, ws, s, want_q)
                   : gemm(h, h->q_b[l], nullptr, h->b_cq, g.n_heads * qhd, g.q_lora, M, EPI_STORE, q, nullptr,
-                         g.n_heads * qhd, ws, s));
+                         g.n_heads * qhd, ws, s, nullptr, want_q));
         RUN(launch_q_absorb(q, M, g.n_heads, g.d_nope, g.d_rope, g.kv_lora, g.d_v, (const __nv_bfloat16 *)W.w_kv_b,
-                            kv->ctx_len, g.block, kv->max_ctx, h->rope, qt, s));
+                            kv->ctx_len, g.block, kv->max_ctx, h->rope, qt, s, want_q));
         ap.pool = (const __nv_bfloat16 *)kv->pools[l];
         if (L.tc) {
             if (h->c_pool[l] != kv->pools[l] || h->c_npages[l] != kv->n_pages) {
@@ -662,18 +699,28 @@ dspark_status dspark_draft_block(dspark_handle_t *h, float *x, const dspark_kv_t
         }
         RUN(launch_v_absorb(olat, M, g.n_heads, g.d_nope, g.d_v, g.kv_lora, (const __nv_bfloat16 *)W.w_kv_b, ov, s));
         RUN(quant ? gemm_q(h, h->qo[l], nullptr, h->b_ov, g.hidden, g.n_heads * g.d_v, M, EPI_ADD, x, nullptr, g.hidden,
-                           ws, s)
+                           ws, s, want_o)
                   : gemm(h, h->o[l], nullptr, h->b_ov, g.hidden, g.n_heads * g.d_v, M, EPI_ADD, x, nullptr, g.hidden, ws,
-                         s));
-        RUN(launch_rmsnorm(x, g.hidden, W.mlp_norm, g.hidden, g.eps, hn, g.hidden, nullptr, 0, M, err, s));
+                         s, nullptr, want_o));
+        if (defer)
+            RUN(launch_rmsnorm_cluster(x, g.hidden, &pend_o, true, W.mlp_norm, g.hidden, g.eps, hn, g.hidden, nullptr, 0,
+                                       M, err, s));
+        else
+            RUN(launch_rmsnorm(x, g.hidden, W.mlp_norm, g.hidden, g.eps, hn, g.hidden, nullptr, 0, M, err, s));
         RUN(quant ? gemm_q(h, h->qgate[l], &h->qup[l], h->b_hn, g.inter, g.hidden, M, EPI_SWIGLU, nullptr, act, g.inter,
                            ws, s)
                   : gemm(h, h->gate[l], &h->up[l], h->b_hn, g.inter, g.hidden, M, EPI_SWIGLU, nullptr, act, g.inter, ws,
                          s));
-        RUN(quant ? gemm_q(h, h->qdown[l], nullptr, h->b_act, g.hidden, g.inter, M, EPI_ADD, x, nullptr, g.hidden, ws, s)
-                  : gemm(h, h->down[l], nullptr, h->b_act, g.hidden, g.inter, M, EPI_ADD, x, nullptr, g.hidden, ws, s));
+        RUN(quant ? gemm_q(h, h->qdown[l], nullptr, h->b_act, g.hidden, g.inter, M, EPI_ADD, x, nullptr, g.hidden, ws, s,
+                           want_x)
+                  : gemm(h, h->down[l], nullptr, h->b_act, g.hidden, g.inter, M, EPI_ADD, x, nullptr, g.hidden, ws, s,
+                         nullptr, want_x));
     }
-    RUN(launch_rmsnorm(x, g.hidden, h->w.final_norm, g.hidden, g.eps, hout, g.hidden, h_out, g.hidden, M, err, s));
+    if (defer)
+        RUN(launch_rmsnorm_cluster(x, g.hidden, &pend_x, true, h->w.final_norm, g.hidden, g.eps, hout, g.hidden, h_out,
+                                   g.hidden, M, err, s));
+    else
+        RUN(launch_rmsnorm(x, g.hidden, h->w.final_norm, g.hidden, g.eps, hout, g.hidden, h_out, g.hidden, M, err, s));
     RUN(gemm(h, h->lm_head, nullptr, h->b_hout, g.vocab, g.hidden, M, EPI_STORE, z, nullptr, g.vocab, ws, s));
     return DSPARK_OK;
 }

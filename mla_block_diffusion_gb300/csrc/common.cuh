@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "../../include/dspark.h"
 
 #define DS_DEVINL __device__ __forceinline__
@@ -332,9 +334,28 @@ DS_DEVINL void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // Launch with programmatic stream serialization (overlaps this kernel's
 // prologue with the tail of the previous kernel on the stream).
+// Every kernel runs with the largest shared-memory carveout. An SM holds CTAs
+// of several kernels at once only under one L1 / shared-memory split, and the
+// weight GEMMs and the attention need the largest; a small kernel that let the
+// driver pick a smaller split could not become resident beside them (and so
+// could not start early under programmatic dependent launch). Set once per kernel.
+inline void carveout_max(const void *kern) {
+    static std::mutex mu;
+    static const void *seen[128];
+    static int n = 0;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < n; ++i)
+        if (seen[i] == kern) return;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared) !=
+        cudaSuccess)
+        (void)cudaGetLastError();  // a hint: the launch proceeds without it
+    if (n < 128) seen[n++] = kern;
+}
+
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
                               Args &&...args) {
+    carveout_max((const void *)kern);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
@@ -349,5 +370,141 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
 }
 
 DS_DEVINL unsigned long long ldcg_u64(const unsigned long long *p) { return __ldcg(p); }
+
+// Same, with thread-block clusters of cx CTAs along x.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl_cluster(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                      int cx, Args &&...args) {
+    carveout_max((const void *)kern);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)cx;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
+// ---------------------------------------------------------------------------
+// Thread-block clusters: rank, barrier (every CTA of a cluster is resident at
+// once, so the barrier always completes), and loads from a peer's shared memory.
+// ---------------------------------------------------------------------------
+DS_DEVINL uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+DS_DEVINL void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Store into the same shared-memory location of CTA `rank` of the cluster
+// (visible to it after the next cluster barrier).
+DS_DEVINL void st_peer_f2(float2 *local, uint32_t rank, float2 v) {
+    uint32_t a;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(local)), "r"(rank));
+    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(a), "f"(v.x), "f"(v.y) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Split-K bookkeeping of the weight GEMMs: CTA c owns units [begin(c), begin(c+1))
+// of the (tile, k-block) order; a tile is split over the CTAs whose ranges meet it.
+// ---------------------------------------------------------------------------
+__host__ __device__ inline long long gemm_unit_begin(int c, long long units, int grid) {
+    return (long long)c * units / grid;
+}
+
+// CTA whose unit range contains unit u (ranges are non-empty: grid <= units).
+__host__ __device__ inline int gemm_cta_of_unit(long long u, long long units, int grid) {
+    int c = (int)((u * grid) / units);
+    if (c >= grid) c = grid - 1;
+    while (c + 1 < grid && gemm_unit_begin(c + 1, units, grid) <= u) ++c;
+    while (c > 0 && gemm_unit_begin(c, units, grid) > u) --c;
+    return c;
+}
+
+// A GEMM output left unreduced (pending): CTA c wrote the rows of its first tile
+// in slot 2c and of its second tile in slot 2c + 1 (a pending GEMM gives every
+// CTA at most one tile of units), row m of channel tile * 128 + r at
+// part[(slot * BN + m) * 128 + r]. The output is the sum over the tile's CTAs in
+// increasing order, so it does not depend on timing. part == nullptr: none.
+// units * grid < 2^31 (32-bit bookkeeping).
+struct GemmPending {
+    const float *part;
+    int units, grid, KB, BN;
+};
+
+// The CTAs of one tile: c_lo .. c_hi; c_lo wrote slot lo_slot, the others 2c.
+struct PendTile {
+    int c_lo, c_hi, lo_slot;
+};
+
+DS_DEVINL int pend_begin(const GemmPending &g, int c) {
+    return (int)((unsigned)c * (unsigned)g.units / (unsigned)g.grid);
+}
+DS_DEVINL int pend_cta_of(const GemmPending &g, int u) {
+    int c = (int)((unsigned)u * (unsigned)g.grid / (unsigned)g.units);
+    if (c >= g.grid) c = g.grid - 1;
+    while (c + 1 < g.grid && pend_begin(g, c + 1) <= u) ++c;
+    while (c > 0 && pend_begin(g, c) > u) --c;
+    return c;
+}
+DS_DEVINL PendTile pend_tile(const GemmPending &g, int t) {
+    PendTile r;
+    r.c_lo = pend_cta_of(g, t * g.KB);
+    r.c_hi = pend_cta_of(g, (t + 1) * g.KB - 1);
+    r.lo_slot = 2 * r.c_lo + (pend_begin(g, r.c_lo) < t * g.KB ? 1 : 0);
+    return r;
+}
+
+// Channels r .. r + 3 (r a multiple of 4) of row m of a tile: contributors in
+// batches of four loads issued before any is added (the sum stays in CTA order).
+DS_DEVINL float4 pending_sum4(const GemmPending &g, const PendTile &pt, int m, int r) {
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c0 = pt.c_lo; c0 <= pt.c_hi; c0 += 4) {
+        float4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int c = c0 + u;
+            const int sl = c == pt.c_lo ? pt.lo_slot : 2 * c;
+            v[u] = c <= pt.c_hi ? __ldcg((const float4 *)(g.part + ((size_t)sl * g.BN + m) * 128 + r))
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (c0 + u <= pt.c_hi) {
+                s.x += v[u].x;
+                s.y += v[u].y;
+                s.z += v[u].z;
+                s.w += v[u].w;
+            }
+        }
+    }
+    return s;
+}
+// Channel r of row m of a tile (same order).
+DS_DEVINL float pending_sum1(const GemmPending &g, const PendTile &pt, int m, int r) {
+    float s = 0.f;
+    for (int c0 = pt.c_lo; c0 <= pt.c_hi; c0 += 4) {
+        float v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int c = c0 + u;
+            const int sl = c == pt.c_lo ? pt.lo_slot : 2 * c;
+            v[u] = c <= pt.c_hi ? __ldcg(g.part + ((size_t)sl * g.BN + m) * 128 + r) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (c0 + u <= pt.c_hi) s += v[u];
+    }
+    return s;
+}
 
 }  // namespace ds

@@ -29,7 +29,9 @@
 
 namespace ds {
 
-enum GemmEpi { EPI_STORE = 0, EPI_ADD = 1, EPI_SWIGLU = 2 };
+// EPI_PENDING: no reduction in the GEMM; every CTA leaves its rows in the
+// partials (GemmPending layout) and the consuming kernel sums them.
+enum GemmEpi { EPI_STORE = 0, EPI_ADD = 1, EPI_SWIGLU = 2, EPI_PENDING = 3 };
 
 struct GemmParams {
     int n_out;          // output channels
@@ -71,7 +73,9 @@ struct GemmCfg {
     static constexpr int kXchgFloats = 64 * 17;
     static constexpr int kFixed = 1024 + kXchgFloats * 4 + 512;
     static constexpr int kStagesFit = (kGemmMaxSmem - kFixed) / kStageBytes;
-    static constexpr int kStages = kStagesFit > 12 ? 12 : kStagesFit;
+    // 11 stages leave about 23 KB of the SM's shared memory for the next
+    // kernel's CTAs to become resident early beside this one
+    static constexpr int kStages = kStagesFit > 11 ? 11 : kStagesFit;
     static constexpr int kSmemBytes = kFixed + kStages * kStageBytes;
     static constexpr int kTmemCols = (2 * BN <= 32)    ? 32
                                      : (2 * BN <= 64)  ? 64
@@ -81,19 +85,6 @@ struct GemmCfg {
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "tcgen05 M=128 needs N in 16..256, step 16");
     static_assert(kStages >= 3, "pipeline too shallow");
 };
-
-__host__ __device__ inline long long gemm_unit_begin(int c, long long units, int grid) {
-    return (long long)c * units / grid;
-}
-
-// CTA whose unit range contains unit u (ranges are non-empty: grid <= units).
-__device__ inline int gemm_cta_of_unit(long long u, long long units, int grid) {
-    int c = (int)((u * grid) / units);
-    if (c >= grid) c = grid - 1;
-    while (c + 1 < grid && gemm_unit_begin(c + 1, units, grid) <= u) ++c;
-    while (c > 0 && gemm_unit_begin(c, units, grid) > u) --c;
-    return c;
-}
 
 __device__ inline float silu_f(float g) { return g / (1.0f + __expf(-g)); }
 
@@ -107,6 +98,17 @@ __device__ inline void gemm_store(const GemmParams &p, int n, int m, float v) {
 
 __device__ inline void gemm_store_swiglu(const GemmParams &p, int n, int m, float g, float u) {
     p.out_bf16[(size_t)m * p.ldo + n] = __float2bfloat16(silu_f(g) * u);
+}
+
+// EPI_PENDING: 16 accumulator columns (activation rows c0 ..) of tile row `row`
+// into the slot (only the valid rows; a warp writes 128 consecutive bytes per row).
+template <int BN>
+__device__ __forceinline__ void gemm_pending_store(const GemmParams &p, int slot, int row, int c0,
+                                                   const float (&v)[16]) {
+    float *dst = p.partials + ((size_t)slot * BN + c0) * 128 + row;
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+        if (c0 + j < p.M) dst[(size_t)j * 128] = v[j];
 }
 
 // Sum of the split partials of one tile, contributors in increasing CTA order
@@ -186,8 +188,11 @@ __device__ __forceinline__ void gemm_reduce_tile(const GemmParams &p, int tile, 
         gemm_reduce_impl<BN, SCALED, U, false>(p, tile, c_lo, c_hi, et, n);
 }
 
+// Shared memory keeps one CTA per SM; the launch bound of two caps the
+// registers at 170 so that the next (small) kernel's warps fit in the register
+// files of the SM sub-partitions beside this CTA's and start early.
 template <int BN>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(192, 2)
     gemm_swapab_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                        const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
     using C = GemmCfg<BN>;
@@ -350,7 +355,9 @@ __global__ void __launch_bounds__(192, 1)
             for (int c0 = 0; c0 < BN; c0 += 16) {
                 float v[16];
                 tmem_ld16(taddr + (uint32_t)c0, v);
-                if (whole) {
+                if (p.epi == EPI_PENDING) {
+                    gemm_pending_store<BN>(p, slot, row, c0, v);
+                } else if (whole) {
                     if (p.paired) {
                         if (q >= 2) {
 #pragma unroll
@@ -381,7 +388,7 @@ __global__ void __launch_bounds__(192, 1)
             }
             tc_fence_before();
             mbar_arrive(&tempty[a]);
-            if (!whole) {
+            if (!whole && p.epi != EPI_PENDING) {
                 __threadfence();
                 named_bar_sync(1, 128);
                 const int c_lo = gemm_cta_of_unit(tbeg, p.units, p.grid);
@@ -394,7 +401,7 @@ __global__ void __launch_bounds__(192, 1)
                 named_bar_sync(1, 128);
                 if (s_last) {
                     __threadfence();
-                    gemm_reduce_tile<BN>(p, tile, c_lo, c_hi, et, nch);
+                    gemm_reduce_tile<BN, false, 4>(p, tile, c_lo, c_hi, et, nch);
                 }
             }
             u = seg_end;

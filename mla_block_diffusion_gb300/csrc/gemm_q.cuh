@@ -411,11 +411,16 @@ __global__ void __launch_bounds__(GemmQCfg<BN, FMT>::kThreads, 1)
             // output channel of this accumulator row and its scale
             const bool second = p.paired && row >= 64;
             const int n_row = p.paired ? tile * 64 + (row & 63) : tile * 128 + row;
-            const float rs = (whole && n_row < p.n_out) ? gemm_row_scale(p, n_row, second) : 1.f;
+            const bool scaled_here = whole || p.epi == EPI_PENDING;
+            const float rs = (scaled_here && n_row < p.n_out) ? gemm_row_scale(p, n_row, second) : 1.f;
             for (int c0 = 0; c0 < BN; c0 += 16) {
                 float v[16];
                 tmem_ld16(taddr + (uint32_t)c0, v);
-                if (whole) {
+                if (p.epi == EPI_PENDING) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) v[j] *= rs;
+                    gemm_pending_store<BN>(p, slot, row, c0, v);
+                } else if (whole) {
 #pragma unroll
                     for (int j = 0; j < 16; ++j) v[j] *= rs;
                     if (p.paired) {
@@ -448,7 +453,7 @@ __global__ void __launch_bounds__(GemmQCfg<BN, FMT>::kThreads, 1)
             }
             tc_fence_before();
             mbar_arrive(&tempty[a]);
-            if (!whole) {
+            if (!whole && p.epi != EPI_PENDING) {
                 __threadfence();
                 named_bar_sync(1, 128);
                 const int c_lo = gemm_cta_of_unit(tbeg, p.units, p.grid);

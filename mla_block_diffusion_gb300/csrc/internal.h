@@ -36,9 +36,22 @@ cudaError_t launch_latent(const float *qkv, int ld, int q_lora, int kv_lora, int
                           const float *g_kv, float eps, const int32_t *ctx_len, int block, int max_ctx,
                           const RopeTable &rt, __nv_bfloat16 *cq, __nv_bfloat16 *blk_kv, int M, int *err,
                           cudaStream_t st);
+// q read from q, or (pend->part set) formed from the q_b GEMM's pending partials.
 cudaError_t launch_q_absorb(const float *q, int M, int n_h, int d_nope, int d_rope, int kv_lora, int d_v,
                             const __nv_bfloat16 *w_kvb, const int32_t *ctx_len, int block, int max_ctx,
-                            const RopeTable &rt, __nv_bfloat16 *qt, cudaStream_t st);
+                            const RopeTable &rt, __nv_bfloat16 *qt, cudaStream_t st,
+                            const GemmPending *pend = nullptr);
+// Row kernels on clusters of CTAs (one cluster per row). With a pending input
+// the row is the sum of a GEMM's split partials: the RMSNorm adds it to x
+// (add) or stores it in x, then normalises; the latent kernel normalises it.
+bool row_cluster_fits(int H);
+cudaError_t launch_rmsnorm_cluster(float *x, int ldx, const GemmPending *pend, bool add, const float *g, int H,
+                                   float eps, __nv_bfloat16 *y, int ldy, float *y32, int ldy32, int M, int *err,
+                                   cudaStream_t st);
+cudaError_t launch_latent_cluster(const float *qkv, int ld, const GemmPending *pend, int q_lora, int kv_lora,
+                                  int d_rope, const float *g_q, const float *g_kv, float eps, const int32_t *ctx_len,
+                                  int block, int max_ctx, const RopeTable &rt, __nv_bfloat16 *cq,
+                                  __nv_bfloat16 *blk_kv, int M, int *err, cudaStream_t st);
 cudaError_t launch_v_absorb(const float *o_lat, int M, int n_h, int d_nope, int d_v, int kv_lora,
                             const __nv_bfloat16 *w_kvb, __nv_bfloat16 *out, cudaStream_t st);
 bool attention_supported(int dqk, int dv);

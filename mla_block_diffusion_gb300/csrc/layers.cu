@@ -8,6 +8,8 @@
 // q_a, kv_a_mqa, k_b, v_b and split RoPE dims ("kimi-k3-dspark-gguf", Runtime
 // status); kv_b absorbed, norms high precision ("Kimi-K3-DSpark-NVFP4", What is
 // quantized to what).
+#include <cstring>
+
 #include "internal.h"
 
 namespace ds {
@@ -183,6 +185,196 @@ __global__ void __launch_bounds__(kLatentThreads) latent_kernel(
 }
 
 // ---------------------------------------------------------------------------
+// Row kernels of a cluster of kRowCl CTAs per row. Each CTA owns a slice of
+// whole float4 of the row (at most kRowVals per thread, kept in registers);
+// the slices' sums of squares meet in distributed shared memory and are added
+// in rank order, so every CTA forms the same scale. The row is either read
+// (pend.part == nullptr) or formed from the split partials a GEMM left pending
+// (plus the row itself when `add`). Little shared memory, so the CTAs become
+// resident beside a running weight GEMM and wait there.
+// ---------------------------------------------------------------------------
+constexpr int kRowCl = 8;
+constexpr int kRowClThreads = 256;
+constexpr int kRowVals = 4;      // float4 per thread
+constexpr int kRowClTiles = 16;  // channel tiles a CTA's slice may touch
+
+// The tiles [t0, t0 + nt) of a pending output into shared memory.
+DS_DEVINL void row_tiles(const GemmPending &pend, int t0, int nt, PendTile *tiles) {
+    if (pend.part && (int)threadIdx.x < nt) tiles[threadIdx.x] = pend_tile(pend, t0 + threadIdx.x);
+}
+
+// This CTA's slice [i0, i1) (float4 units) of a row of n4 float4.
+DS_DEVINL void row_slice(int n4, int &i0, int &i1) {
+    const uint32_t k = cluster_rank();
+    i0 = (int)((long long)k * n4 / kRowCl);
+    i1 = (int)((long long)(k + 1) * n4 / kRowCl);
+}
+
+// The cluster's total of (a, b) over its CTAs, in rank order. Every thread of
+// every CTA calls it: thread k stores this CTA's sum into slot `rank` of CTA k,
+// one cluster barrier makes the stores visible, and every CTA adds its own
+// kRowCl slots (no remote access after the barrier, so a CTA may then exit).
+DS_DEVINL float2 cluster_sum2(float2 v, float2 *red, float2 *parts) {
+    v = block_sum2(v, red);
+    if (threadIdx.x < (unsigned)kRowCl) st_peer_f2(parts + cluster_rank(), threadIdx.x, v);
+    cluster_sync();
+    float2 t = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < kRowCl; ++k) {
+        t.x += parts[k].x;
+        t.y += parts[k].y;
+    }
+    return t;
+}
+
+// Row value at float4 index i (pending or read).
+DS_DEVINL float4 row_value(const float4 *row, const GemmPending &pend, const PendTile *tiles, int t0, int m, int i) {
+    if (!pend.part) return row[i];
+    const int n = 4 * i;
+    return pending_sum4(pend, tiles[(n >> 7) - t0], m, n & 127);
+}
+
+// RMSNorm: x <- (add ? x : 0) + pending (written back: x is the residual
+// stream), y = x / sqrt(mean(x^2) + eps) * g as bf16, y32 as fp32 when given.
+// Grid (kRowCl, M); H a multiple of 4.
+__global__ void __launch_bounds__(kRowClThreads) rmsnorm_cluster_kernel(
+    float *__restrict__ x, int ldx, GemmPending pend, int add, const float *__restrict__ g, int H, float eps,
+    __nv_bfloat16 *__restrict__ y, int ldy, float *__restrict__ y32, int ldy32, int *err) {
+    pdl_trigger();
+    __shared__ float2 red[33];
+    __shared__ float2 s_parts[kRowCl];
+    __shared__ PendTile s_tiles[kRowClTiles];
+    const int m = blockIdx.y;
+    int i0, i1;
+    row_slice(H / 4, i0, i1);
+    const int t0 = (4 * i0) >> 7, nt = i1 > i0 ? ((4 * (i1 - 1)) >> 7) - t0 + 1 : 0;
+    row_tiles(pend, t0, nt, s_tiles);  // depends only on the GEMM's shape
+    const float4 *g4 = (const float4 *)g;
+    float4 gv[kRowVals];
+#pragma unroll
+    for (int k = 0; k < kRowVals; ++k) {
+        const int i = i0 + threadIdx.x + k * kRowClThreads;
+        gv[k] = i < i1 ? __ldg(g4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    __syncthreads();
+    pdl_wait();
+    float4 *xr = (float4 *)(x + (size_t)m * ldx);
+    float4 v[kRowVals];
+    float ss = 0.f;
+    // the row itself first (the residual, or the plain input), then the partials
+#pragma unroll
+    for (int k = 0; k < kRowVals; ++k) {
+        const int i = i0 + threadIdx.x + k * kRowClThreads;
+        v[k] = (i < i1 && (!pend.part || add)) ? xr[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int k = 0; k < kRowVals; ++k) {
+        const int i = i0 + threadIdx.x + k * kRowClThreads;
+        if (i < i1 && pend.part) {
+            const int n = 4 * i;
+            const float4 p = pending_sum4(pend, s_tiles[(n >> 7) - t0], m, n & 127);
+            v[k] = make_float4(v[k].x + p.x, v[k].y + p.y, v[k].z + p.z, v[k].w + p.w);
+            xr[i] = v[k];
+        }
+        ss += v[k].x * v[k].x + v[k].y * v[k].y + v[k].z * v[k].z + v[k].w * v[k].w;
+    }
+    const float tot = cluster_sum2(make_float2(ss, 0.f), red, s_parts).x;
+    if (!isfinite(tot) && threadIdx.x == 0 && cluster_rank() == 0) set_error(err, DSPARK_ERR_BAD_INPUT);
+    const float r = rsqrtf(tot / (float)H + eps);
+#pragma unroll
+    for (int k = 0; k < kRowVals; ++k) {
+        const int i = i0 + threadIdx.x + k * kRowClThreads;
+        if (i < i1) {
+            const float4 t = v[k], gg = gv[k];
+            const float4 o = make_float4(t.x * r * gg.x, t.y * r * gg.y, t.z * r * gg.z, t.w * r * gg.w);
+            __nv_bfloat162 *yb = (__nv_bfloat162 *)(y + (size_t)m * ldy + 4 * i);
+            yb[0] = __floats2bfloat162_rn(o.x, o.y);
+            yb[1] = __floats2bfloat162_rn(o.z, o.w);
+            if (y32) ((float4 *)(y32 + (size_t)m * ldy32))[i] = o;
+        }
+    }
+}
+
+// Latent norms and RoPE of the q_a || kv_a output (see latent_kernel), the row
+// read or formed from pending partials. Grid (kRowCl, M).
+__global__ void __launch_bounds__(kRowClThreads) latent_cluster_kernel(
+    const float *__restrict__ qkv, int ld, GemmPending pend, int q_lora, int kv_lora, int d_rope,
+    const float *__restrict__ g_q, const float *__restrict__ g_kv, float eps, const int32_t *__restrict__ ctx_len,
+    int block, int max_ctx, RopeTable rt, __nv_bfloat16 *__restrict__ cq, __nv_bfloat16 *__restrict__ blk_kv,
+    int *err) {
+    pdl_trigger();
+    __shared__ float2 red[33];
+    __shared__ float2 s_parts[kRowCl];
+    __shared__ PendTile s_tiles[kRowClTiles];
+    const int m = blockIdx.y, b = m / block, pos_i = m % block;
+    const int nq4 = q_lora / 4, nk4 = kv_lora / 4, n4 = nq4 + nk4 + d_rope / 4;
+    int i0, i1;
+    row_slice(n4, i0, i1);
+    const int t0 = (4 * i0) >> 7, nt = i1 > i0 ? ((4 * (i1 - 1)) >> 7) - t0 + 1 : 0;
+    row_tiles(pend, t0, nt, s_tiles);
+    float4 gv[kRowVals];
+#pragma unroll
+    for (int k = 0; k < kRowVals; ++k) {
+        const int i = i0 + threadIdx.x + k * kRowClThreads;
+        gv[k] = i < nq4 ? __ldg((const float4 *)g_q + i)
+                        : (i < nq4 + nk4 && i < i1 ? __ldg((const float4 *)g_kv + (i - nq4))
+                                                   : make_float4(0.f, 0.f, 0.f, 0.f));
+    }
+    int c = ctx_len[b];
+    __syncthreads();
+    pdl_wait();
+    const float4 *row = (const float4 *)(qkv + (size_t)m * ld);
+    float4 v[kRowVals];
+    float2 ss = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < kRowVals; ++k) {
+        const int i = i0 + threadIdx.x + k * kRowClThreads;
+        v[k] = i < i1 ? row_value(row, pend, s_tiles, t0, m, i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float sq = v[k].x * v[k].x + v[k].y * v[k].y + v[k].z * v[k].z + v[k].w * v[k].w;
+        if (i < nq4)
+            ss.x += sq;
+        else if (i < nq4 + nk4)
+            ss.y += sq;
+    }
+    ss = cluster_sum2(ss, red, s_parts);
+    if ((!isfinite(ss.x) || !isfinite(ss.y)) && threadIdx.x == 0 && cluster_rank() == 0)
+        set_error(err, DSPARK_ERR_BAD_INPUT);
+    const float rq = rsqrtf(ss.x / (float)q_lora + eps), rk = rsqrtf(ss.y / (float)kv_lora + eps);
+    if (c < 0 || c > max_ctx) {
+        if (threadIdx.x == 0 && cluster_rank() == 0) set_error(err, DSPARK_ERR_OOB);
+        c = 0;
+    }
+    const int kvd = kv_lora + d_rope;
+#pragma unroll
+    for (int k = 0; k < kRowVals; ++k) {
+        const int i = i0 + threadIdx.x + k * kRowClThreads;
+        if (i >= i1) continue;
+        const float4 t = v[k];
+        if (i < nq4 + nk4) {
+            const bool isq = i < nq4;
+            const float r = isq ? rq : rk;
+            const float4 gg = gv[k];
+            __nv_bfloat162 *d2 = (__nv_bfloat162 *)(isq ? cq + (size_t)m * q_lora + 4 * i
+                                                        : blk_kv + (size_t)m * kvd + 4 * (i - nq4));
+            d2[0] = __floats2bfloat162_rn(t.x * r * gg.x, t.y * r * gg.y);
+            d2[1] = __floats2bfloat162_rn(t.z * r * gg.z, t.w * r * gg.w);
+        } else {
+            // two RoPE pairs (2p, 2p + 1), p = 2 (i - nq4 - nk4) and the next
+            const int p = 2 * (i - nq4 - nk4);
+            const double pos = (double)(c + pos_i);
+            float c0, s0, c1, s1;
+            rope_cs(pos, rt.inv_freq[p], c0, s0);
+            rope_cs(pos, rt.inv_freq[p + 1], c1, s1);
+            __nv_bfloat16 *dst = blk_kv + (size_t)m * kvd + kv_lora + 2 * p;
+            dst[0] = __float2bfloat16(t.x * c0 - t.y * s0);
+            dst[1] = __float2bfloat16(t.x * s0 + t.y * c0);
+            dst[2] = __float2bfloat16(t.z * c1 - t.w * s1);
+            dst[3] = __float2bfloat16(t.z * s1 + t.w * c1);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // q absorption: Q_h = [W_kb,h^T q_nope,h || RoPE(q_rope,h)] per row and head,
 // bf16 [M, n_h, kv_lora + d_rope]. Grid (n_h, kv_lora / 64), 128 threads: a CTA
 // owns one head and 64 latent columns; warp w takes the quarter w of d_nope and
@@ -193,6 +385,7 @@ __global__ void __launch_bounds__(kLatentThreads) latent_kernel(
 // ---------------------------------------------------------------------------
 constexpr int kAbsorbRows = 16;
 constexpr int kQAbsRows = 8;
+constexpr int kQAbsTiles = 4;  // channel tiles of one head's q (d_nope + d_rope <= 384)
 constexpr int kQAbsCols = 64;
 
 template <int MAXDQ>
@@ -200,15 +393,26 @@ __global__ void __launch_bounds__(128) q_absorb_kernel(const float *__restrict__
                                                        int d_rope, int kv_lora, int d_v,
                                                        const __nv_bfloat16 *__restrict__ w_kvb,
                                                        const int32_t *__restrict__ ctx_len, int block, int max_ctx,
-                                                       RopeTable rt, __nv_bfloat16 *__restrict__ qt) {
+                                                       RopeTable rt, __nv_bfloat16 *__restrict__ qt,
+                                                       GemmPending pend) {
     pdl_trigger();
     extern __shared__ float sm[];
+    __shared__ PendTile s_tiles[kQAbsTiles];
     float *sq = sm;                             // [kQAbsRows][d_nope]
     float *red = sm + kQAbsRows * d_nope;       // [4][kQAbsRows][kQAbsCols]
     const int h = blockIdx.x, c0 = blockIdx.y * kQAbsCols;
     const int lane = threadIdx.x & 31, qd = threadIdx.x >> 5;
     const int dq = d_nope / 4;  // <= 64
     const int qhd = d_nope + d_rope, kvd = kv_lora + d_rope;
+    // q may be pending (the q_b GEMM's split partials): the slots of the head's channel tiles
+    const int qt0 = (h * qhd) >> 7, qnt = ((h * qhd + qhd - 1) >> 7) - qt0 + 1;
+    if (pend.part && (int)threadIdx.x < qnt) s_tiles[threadIdx.x] = pend_tile(pend, qt0 + threadIdx.x);
+    __syncthreads();
+    auto qval = [&](int m, int d) -> float {
+        if (!pend.part) return q[((size_t)m * n_h + h) * qhd + d];
+        const int n = h * qhd + d;
+        return pending_sum1(pend, s_tiles[(n >> 7) - qt0], m, n & 127);
+    };
     // the weights do not depend on the previous kernel: load them before the wait
     const __nv_bfloat16 *W = w_kvb + ((size_t)h * (d_nope + d_v) + qd * dq) * kv_lora + c0 + 2 * lane;
     uint32_t w[MAXDQ];
@@ -223,7 +427,7 @@ __global__ void __launch_bounds__(128) q_absorb_kernel(const float *__restrict__
             float v[kQAbsRows];
 #pragma unroll
             for (int mm = 0; mm < kQAbsRows; ++mm)
-                v[mm] = (d < d_nope && m0 + mm < M) ? q[((size_t)(m0 + mm) * n_h + h) * qhd + d] : 0.f;
+                v[mm] = (d < d_nope && m0 + mm < M) ? qval(m0 + mm, d) : 0.f;
             if (d < d_nope) {
 #pragma unroll
                 for (int mm = 0; mm < kQAbsRows; ++mm) sq[mm * d_nope + d] = v[mm];
@@ -271,8 +475,7 @@ __global__ void __launch_bounds__(128) q_absorb_kernel(const float *__restrict__
             if (c < 0 || c > max_ctx) c = 0;
             float fc, fs;
             rope_cs((double)(c + m % block), rt.inv_freq[p], fc, fs);
-            const float *src = q + ((size_t)m * n_h + h) * qhd + d_nope;
-            const float x0 = src[2 * p], x1 = src[2 * p + 1];
+            const float x0 = qval(m, d_nope + 2 * p), x1 = qval(m, d_nope + 2 * p + 1);
             __nv_bfloat16 *dst = qt + ((size_t)m * n_h + h) * kvd + kv_lora;
             dst[2 * p] = __float2bfloat16(x0 * fc - x1 * fs);
             dst[2 * p + 1] = __float2bfloat16(x0 * fs + x1 * fc);
@@ -740,12 +943,46 @@ cudaError_t launch_latent(const float *qkv, int ld, int q_lora, int kv_lora, int
 
 cudaError_t launch_q_absorb(const float *q, int M, int n_h, int d_nope, int d_rope, int kv_lora, int d_v,
                             const __nv_bfloat16 *w_kvb, const int32_t *ctx_len, int block, int max_ctx,
-                            const RopeTable &rt, __nv_bfloat16 *qt, cudaStream_t st) {
+                            const RopeTable &rt, __nv_bfloat16 *qt, cudaStream_t st, const GemmPending *pend) {
+    GemmPending pd;
+    memset(&pd, 0, sizeof(pd));
+    if (pend) pd = *pend;
     dim3 grid(n_h, kv_lora / kQAbsCols);
     const size_t smem = ((size_t)kQAbsRows * d_nope + (size_t)4 * kQAbsRows * kQAbsCols) * sizeof(float);
     // the thread's k_b slice (d_nope / 4 rows) in registers: 32 covers d_nope <= 128
     return launch_pdl(d_nope <= 128 ? q_absorb_kernel<32> : q_absorb_kernel<64>, grid, dim3(128), smem, st, q, M, n_h, d_nope, d_rope, kv_lora, d_v, w_kvb,
-                      ctx_len, block, max_ctx, rt, qt);
+                      ctx_len, block, max_ctx, rt, qt, pd);
+}
+
+// Whether a row of H channels fits the cluster row kernels' tile bookkeeping.
+bool row_cluster_fits(int H) {
+    const int slice4 = (H / 4 + kRowCl - 1) / kRowCl;
+    return H % 4 == 0 && slice4 <= kRowVals * kRowClThreads && slice4 * 4 / 128 + 2 <= kRowClTiles;
+}
+
+cudaError_t launch_rmsnorm_cluster(float *x, int ldx, const GemmPending *pend, bool add, const float *g, int H,
+                                   float eps, __nv_bfloat16 *y, int ldy, float *y32, int ldy32, int M, int *err,
+                                   cudaStream_t st) {
+    if (!row_cluster_fits(H)) return cudaErrorInvalidValue;
+    GemmPending pd;
+    memset(&pd, 0, sizeof(pd));
+    if (pend) pd = *pend;
+    return launch_pdl_cluster(rmsnorm_cluster_kernel, dim3(kRowCl, M), dim3(kRowClThreads), 0, st, kRowCl, x, ldx,
+                              pd, add ? 1 : 0, g, H, eps, y, ldy, y32, ldy32, err);
+}
+
+cudaError_t launch_latent_cluster(const float *qkv, int ld, const GemmPending *pend, int q_lora, int kv_lora,
+                                  int d_rope, const float *g_q, const float *g_kv, float eps, const int32_t *ctx_len,
+                                  int block, int max_ctx, const RopeTable &rt, __nv_bfloat16 *cq,
+                                  __nv_bfloat16 *blk_kv, int M, int *err, cudaStream_t st) {
+    const int H = q_lora + kv_lora + d_rope;
+    if (!row_cluster_fits(H) || q_lora % 4 || kv_lora % 4 || d_rope % 4) return cudaErrorInvalidValue;
+    GemmPending pd;
+    memset(&pd, 0, sizeof(pd));
+    if (pend) pd = *pend;
+    return launch_pdl_cluster(latent_cluster_kernel, dim3(kRowCl, M), dim3(kRowClThreads), 0, st, kRowCl, qkv, ld,
+                              pd, q_lora, kv_lora, d_rope, g_q, g_kv, eps, ctx_len, block, max_ctx, rt, cq, blk_kv,
+                              err);
 }
 
 cudaError_t launch_v_absorb(const float *o_lat, int M, int n_h, int d_nope, int d_v, int kv_lora,

@@ -1641,6 +1641,8 @@ bool rollout_resident_setup(int V, int r, int grid) {
 }
 
 cudaError_t launch_rollout(const CUtensorMap &w2_map, RolloutParams p, int grid, bool resident, cudaStream_t st) {
+    carveout_max((const void *)rollout_greedy_resident_kernel);
+    carveout_max((const void *)rollout_kernel);
     CUtensorMap tm = w2_map;
     void *args[] = {&tm, &p};
     if (resident && p.bs == 1 && p.draft_mode == DSPARK_GREEDY && ((uintptr_t)p.w1 & 15u) == 0)
@@ -1662,6 +1664,8 @@ cudaError_t launch_verify(VerifyParams p, int grid, cudaStream_t st) {
                           p.scratch, p.accept_len, p.out_tokens, p.err);
     }
     void *args[] = {&p};
+    carveout_max((const void *)verify_block_kernel);
+    carveout_max((const void *)verify_prob_kernel);
     if (p.verify_mode == DSPARK_BLOCK)
         return cudaLaunchCooperativeKernel((void *)verify_block_kernel, dim3(grid), dim3(kSampThreads), args, 0, st);
     return cudaLaunchCooperativeKernel((void *)verify_prob_kernel, dim3(grid), dim3(kSampThreads), args, 0, st);
