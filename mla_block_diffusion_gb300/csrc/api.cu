@@ -314,9 +314,10 @@ cudaError_t gemm_q_t(const QMat &A, const QMat *A2, const CUtensorMap &B, GemmPa
 
 cudaError_t gemm_q(const dspark_handle *h, const QMat &A, const QMat *A2, const CUtensorMap &B, int n_out, int K, int M,
                    int epi, float *out_f32, __nv_bfloat16 *out_bf16, int ldo, void *ws, cudaStream_t st,
-                   GemmPending *pend = nullptr) {
+                   GemmPending *pend = nullptr, const L2Prefetch *pf = nullptr) {
     GemmParams p;
     memset(&p, 0, sizeof(p));
+    if (pf) p.pf = *pf;
     p.n_out = n_out;
     p.K = K;
     p.M = M;
@@ -679,10 +680,18 @@ dspark_status dspark_draft_block(dspark_handle_t *h, float *x, const dspark_kv_t
         else
             RUN(launch_latent(qkv, g.q_lora + kvd, g.q_lora, g.kv_lora, g.d_rope, W.q_a_norm, W.kv_a_norm, g.eps,
                               kv->ctx_len, g.block, kv->max_ctx, h->rope, cq, blk, M, err, s));
+        // kv_b (k_b for the q absorption next, v_b for the v absorption) streams
+        // into L2 while the q_b GEMM runs
+        L2Prefetch pf_kvb;
+        memset(&pf_kvb, 0, sizeof(pf_kvb));
+        if (aligned16(W.w_kv_b)) {
+            pf_kvb.ptr[0] = (const uint8_t *)W.w_kv_b;
+            pf_kvb.bytes[0] = ((uint64_t)g.n_heads * (g.d_nope + g.d_v) * g.kv_lora * 2) & ~15ull;
+        }
         RUN(quant ? gemm_q(h, h->qq_b[l], nullptr, h->b_cq, g.n_heads * qhd, g.q_lora, M, EPI_STORE, q, nullptr,
-                           g.n_heads * qhd, ws, s, want_q)
+                           g.n_heads * qhd, ws, s, want_q, &pf_kvb)
                   : gemm(h, h->q_b[l], nullptr, h->b_cq, g.n_heads * qhd, g.q_lora, M, EPI_STORE, q, nullptr,
-                         g.n_heads * qhd, ws, s, nullptr, want_q));
+                         g.n_heads * qhd, ws, s, &pf_kvb, want_q));
         RUN(launch_q_absorb(q, M, g.n_heads, g.d_nope, g.d_rope, g.kv_lora, g.d_v, (const __nv_bfloat16 *)W.w_kv_b,
                             kv->ctx_len, g.block, kv->max_ctx, h->rope, qt, s, want_q));
         ap.pool = (const __nv_bfloat16 *)kv->pools[l];

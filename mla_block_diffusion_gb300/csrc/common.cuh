@@ -465,20 +465,21 @@ DS_DEVINL PendTile pend_tile(const GemmPending &g, int t) {
 }
 
 // Channels r .. r + 3 (r a multiple of 4) of row m of a tile: contributors in
-// batches of four loads issued before any is added (the sum stays in CTA order).
+// batches of eight loads issued before any is added (the sum stays in CTA order).
+constexpr int kPendBatch = 8;
 DS_DEVINL float4 pending_sum4(const GemmPending &g, const PendTile &pt, int m, int r) {
     float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int c0 = pt.c_lo; c0 <= pt.c_hi; c0 += 4) {
-        float4 v[4];
+    for (int c0 = pt.c_lo; c0 <= pt.c_hi; c0 += kPendBatch) {
+        float4 v[kPendBatch];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < kPendBatch; ++u) {
             const int c = c0 + u;
             const int sl = c == pt.c_lo ? pt.lo_slot : 2 * c;
             v[u] = c <= pt.c_hi ? __ldcg((const float4 *)(g.part + ((size_t)sl * g.BN + m) * 128 + r))
                                 : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < kPendBatch; ++u) {
             if (c0 + u <= pt.c_hi) {
                 s.x += v[u].x;
                 s.y += v[u].y;
@@ -492,16 +493,16 @@ DS_DEVINL float4 pending_sum4(const GemmPending &g, const PendTile &pt, int m, i
 // Channel r of row m of a tile (same order).
 DS_DEVINL float pending_sum1(const GemmPending &g, const PendTile &pt, int m, int r) {
     float s = 0.f;
-    for (int c0 = pt.c_lo; c0 <= pt.c_hi; c0 += 4) {
-        float v[4];
+    for (int c0 = pt.c_lo; c0 <= pt.c_hi; c0 += kPendBatch) {
+        float v[kPendBatch];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < kPendBatch; ++u) {
             const int c = c0 + u;
             const int sl = c == pt.c_lo ? pt.lo_slot : 2 * c;
             v[u] = c <= pt.c_hi ? __ldcg(g.part + ((size_t)sl * g.BN + m) * 128 + r) : 0.f;
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
+        for (int u = 0; u < kPendBatch; ++u)
             if (c0 + u <= pt.c_hi) s += v[u];
     }
     return s;

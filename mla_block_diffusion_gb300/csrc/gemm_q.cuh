@@ -285,6 +285,7 @@ __global__ void __launch_bounds__(GemmQCfg<BN, FMT>::kThreads, 1)
                 armed |= 1u << (int)it;
                 load_weights(u0 + it, (int)it, pol);
             }
+            l2_prefetch_share(p.pf, (unsigned int)cta, (unsigned int)p.grid);
             pdl_wait();
             for (long long it = 0; it < pre; ++it) load_acts(u0 + it, (int)it);
             long long it = pre;

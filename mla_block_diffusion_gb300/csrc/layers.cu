@@ -484,6 +484,138 @@ __global__ void __launch_bounds__(128) q_absorb_kernel(const float *__restrict__
 }
 
 // ---------------------------------------------------------------------------
+// q absorption on 256-column chunks (the form the draft step uses): grid
+// (n_h, ceil(kv_lora / 256)), 256 threads, one CTA per head and chunk, so the
+// whole grid is one wave (its k_b slices come from L2: the q_b GEMM pulls
+// kv_b there while it runs). Warp w takes
+// columns [64 (w % 4), +64) of the chunk (lane l the pair 2l) and the half
+// w / 4 of d_nope; the thread's slice (d_nope / 2 rows of one column pair)
+// stays in registers. Rows sweep in chunks of 4 from shared memory; the two
+// halves' sums are added in half order.
+// ---------------------------------------------------------------------------
+constexpr int kQAbs2Cols = 256;
+constexpr int kQAbs2Threads = 256;
+constexpr int kQAbs2Rows = 4;
+constexpr int kQAbs2MaxRope = 128;
+
+template <int MAXDH>
+__global__ void __launch_bounds__(kQAbs2Threads, 1) q_absorb2_kernel(
+    const float *__restrict__ q, int M, int n_h, int d_nope, int d_rope, int kv_lora, int d_v,
+    const __nv_bfloat16 *__restrict__ w_kvb, const int32_t *__restrict__ ctx_len, int block, int max_ctx,
+    RopeTable rt, __nv_bfloat16 *__restrict__ qt, GemmPending pend) {
+    pdl_trigger();
+    // the head's q rows of a chunk of 8: nope and rope parts, staged in one batch of loads
+    constexpr int LD = 2 * MAXDH + kQAbs2MaxRope;
+    constexpr int kPer = kQAbsRows * LD / kQAbs2Threads;  // staged positions per thread
+    __shared__ __align__(16) float sq[kQAbsRows][LD];
+    __shared__ float2 red[kQAbs2Rows][kQAbs2Cols / 2];  // the second half's sums
+    __shared__ PendTile s_tiles[kQAbsTiles];
+    const int h = blockIdx.x, c0 = blockIdx.y * kQAbs2Cols;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int cg = warp & 3, half = warp >> 2;
+    const int dh = d_nope / 2;
+    const int cp = 32 * cg + lane;  // column pair within the chunk
+    const int col = c0 + 2 * cp;
+    const bool colv = col < kv_lora;
+    const int qhd = d_nope + d_rope, kvd = kv_lora + d_rope;
+    const int qt0 = (h * qhd) >> 7, qnt = ((h * qhd + qhd - 1) >> 7) - qt0 + 1;
+    if (pend.part && (int)threadIdx.x < qnt) s_tiles[threadIdx.x] = pend_tile(pend, qt0 + threadIdx.x);
+    // the k_b slice does not depend on the previous kernel: load it before the wait
+    const __nv_bfloat16 *W = w_kvb + ((size_t)h * (d_nope + d_v) + half * dh) * kv_lora + col;
+    uint32_t w[MAXDH];
+#pragma unroll
+    for (int i = 0; i < MAXDH; ++i)
+        w[i] = (i < dh && colv) ? __ldg((const unsigned int *)(W + (size_t)i * kv_lora)) : 0u;
+    const int np = d_rope / 2;
+    __syncthreads();
+    for (int m0 = 0; m0 < M; m0 += kQAbsRows) {
+        // this thread's RoPE pair of the chunk (CTA column chunk 0 rotates): the angle
+        // depends only on the inputs, so it is formed before the dependency wait
+        const int rp = threadIdx.x, rmm = rp / (np > 0 ? np : 1), rpp = rp % (np > 0 ? np : 1);
+        const bool rope_here = blockIdx.y == 0 && np > 0 && rp < kQAbsRows * np && m0 + rmm < M;
+        float fc = 1.f, fs = 0.f;
+        if (rope_here) {
+            const int m = m0 + rmm;
+            int c = ctx_len[m / block];
+            if (c < 0 || c > max_ctx) c = 0;
+            rope_cs((double)(c + m % block), rt.inv_freq[rpp], fc, fs);
+        }
+        if (m0 == 0) pdl_wait();
+        // every position of the staged rows is written: the sweep multiplies the
+        // ones past d_nope by zero weights, and stale bits there could be Inf or NaN
+        float v[kPer];
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int idx = threadIdx.x + k * kQAbs2Threads, mm = idx / LD, pos = idx % LD, m = m0 + mm;
+            const int d = pos < d_nope ? pos : (pos >= 2 * MAXDH && pos < 2 * MAXDH + d_rope ? d_nope + pos - 2 * MAXDH : -1);
+            v[k] = 0.f;
+            if (m < M && d >= 0) {
+                if (!pend.part) {
+                    v[k] = q[((size_t)m * n_h + h) * qhd + d];
+                } else {
+                    const int n = h * qhd + d;
+                    v[k] = pending_sum1(pend, s_tiles[(n >> 7) - qt0], m, n & 127);
+                }
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int idx = threadIdx.x + k * kQAbs2Threads;
+            sq[idx / LD][idx % LD] = v[k];
+        }
+        __syncthreads();
+        if (rope_here) {
+            const int m = m0 + rmm;
+            const float x0 = sq[rmm][2 * MAXDH + 2 * rpp], x1 = sq[rmm][2 * MAXDH + 2 * rpp + 1];
+            __nv_bfloat16 *dst = qt + ((size_t)m * n_h + h) * kvd + kv_lora;
+            dst[2 * rpp] = __float2bfloat16(x0 * fc - x1 * fs);
+            dst[2 * rpp + 1] = __float2bfloat16(x0 * fs + x1 * fc);
+        }
+        for (int r0 = 0; r0 < kQAbsRows; r0 += kQAbs2Rows) {
+            float a0[kQAbs2Rows], a1[kQAbs2Rows];
+#pragma unroll
+            for (int mm = 0; mm < kQAbs2Rows; ++mm) a0[mm] = a1[mm] = 0.f;
+            const float *sqh = &sq[r0][0] + half * dh;
+#pragma unroll
+            for (int i = 0; i < MAXDH; i += 4) {
+                float2 wf[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) wf[j] = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[i + j]));
+#pragma unroll
+                for (int mm = 0; mm < kQAbs2Rows; ++mm) {
+                    const float4 x = *(const float4 *)(sqh + mm * LD + i);
+                    a0[mm] = fmaf(wf[0].x, x.x, a0[mm]);
+                    a1[mm] = fmaf(wf[0].y, x.x, a1[mm]);
+                    a0[mm] = fmaf(wf[1].x, x.y, a0[mm]);
+                    a1[mm] = fmaf(wf[1].y, x.y, a1[mm]);
+                    a0[mm] = fmaf(wf[2].x, x.z, a0[mm]);
+                    a1[mm] = fmaf(wf[2].y, x.z, a1[mm]);
+                    a0[mm] = fmaf(wf[3].x, x.w, a0[mm]);
+                    a1[mm] = fmaf(wf[3].y, x.w, a1[mm]);
+                }
+            }
+            if (half == 1) {
+#pragma unroll
+                for (int mm = 0; mm < kQAbs2Rows; ++mm) red[mm][cp] = make_float2(a0[mm], a1[mm]);
+            }
+            __syncthreads();
+            if (half == 0 && colv) {
+#pragma unroll
+                for (int mm = 0; mm < kQAbs2Rows; ++mm) {
+                    const int m = m0 + r0 + mm;
+                    if (m < M) {
+                        const float2 o = red[mm][cp];
+                        *(__nv_bfloat162 *)(qt + ((size_t)m * n_h + h) * kvd + col) =
+                            __floats2bfloat162_rn(a0[mm] + o.x, a1[mm] + o.y);
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // v absorption: o_h = W_vb,h o_lat,h -> bf16 [M, n_h * d_v] (operand of o_proj).
 // Grid (n_h, d_v / 16): a CTA owns 16 output channels of one head; 16 threads
 // per channel each hold 4-element slices of the channel's W_vb row at
@@ -947,6 +1079,10 @@ cudaError_t launch_q_absorb(const float *q, int M, int n_h, int d_nope, int d_ro
     GemmPending pd;
     memset(&pd, 0, sizeof(pd));
     if (pend) pd = *pend;
+    if (d_nope <= 128 && d_nope % 8 == 0 && d_rope <= kQAbs2MaxRope && d_rope / 2 * kQAbsRows <= kQAbs2Threads)
+        return launch_pdl(q_absorb2_kernel<64>, dim3(n_h, (kv_lora + kQAbs2Cols - 1) / kQAbs2Cols),
+                          dim3(kQAbs2Threads), 0, st, q, M, n_h, d_nope, d_rope, kv_lora, d_v, w_kvb, ctx_len, block,
+                          max_ctx, rt, qt, pd);
     dim3 grid(n_h, kv_lora / kQAbsCols);
     const size_t smem = ((size_t)kQAbsRows * d_nope + (size_t)4 * kQAbsRows * kQAbsCols) * sizeof(float);
     // the thread's k_b slice (d_nope / 4 rows) in registers: 32 covers d_nope <= 128
