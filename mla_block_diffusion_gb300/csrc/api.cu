@@ -241,6 +241,8 @@ void gemm_grid(GemmParams &p, int per, int num_sms, int BN, GemmPending *pend) {
         }
     }
     p.grid = (int)grid;
+    // pairwise reduction: every CTA's range covers at least one tile
+    p.pair_red = (p.epi != EPI_PENDING && BN <= 32 && p.units / p.grid >= p.KB) ? 1 : 0;
 }
 
 template <int BN>

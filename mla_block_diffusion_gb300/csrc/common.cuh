@@ -370,6 +370,8 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
 }
 
 DS_DEVINL unsigned long long ldcg_u64(const unsigned long long *p) { return __ldcg(p); }
+DS_DEVINL int ld_volatile_i32(const int *p) { return *(const volatile int *)p; }
+DS_DEVINL void st_volatile_i32(int *p, int v) { *(volatile int *)p = v; }
 
 // Same, with thread-block clusters of cx CTAs along x.
 template <typename... KArgs, typename... Args>
@@ -467,19 +469,20 @@ DS_DEVINL PendTile pend_tile(const GemmPending &g, int t) {
 // Channels r .. r + 3 (r a multiple of 4) of row m of a tile: contributors in
 // batches of eight loads issued before any is added (the sum stays in CTA order).
 constexpr int kPendBatch = 8;
+template <int BATCH = kPendBatch>
 DS_DEVINL float4 pending_sum4(const GemmPending &g, const PendTile &pt, int m, int r) {
     float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int c0 = pt.c_lo; c0 <= pt.c_hi; c0 += kPendBatch) {
-        float4 v[kPendBatch];
+    for (int c0 = pt.c_lo; c0 <= pt.c_hi; c0 += BATCH) {
+        float4 v[BATCH];
 #pragma unroll
-        for (int u = 0; u < kPendBatch; ++u) {
+        for (int u = 0; u < BATCH; ++u) {
             const int c = c0 + u;
             const int sl = c == pt.c_lo ? pt.lo_slot : 2 * c;
             v[u] = c <= pt.c_hi ? __ldcg((const float4 *)(g.part + ((size_t)sl * g.BN + m) * 128 + r))
                                 : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
-        for (int u = 0; u < kPendBatch; ++u) {
+        for (int u = 0; u < BATCH; ++u) {
             if (c0 + u <= pt.c_hi) {
                 s.x += v[u].x;
                 s.y += v[u].y;

@@ -55,6 +55,13 @@ struct GemmParams {
     const float *qscale, *qscale2;
     float gscale, gscale2;
     L2Prefetch pf;      // weights of a later kernel, pulled into L2 by the producer
+    // Pairwise reduction (every CTA's range covers at least one tile, so a split
+    // tile has two contributors): CTA c + 1 takes the tile's last k-blocks first
+    // thing, writes them to its slot 2(c + 1) and raises counters[tile]; CTA c,
+    // which reaches the tile's first k-blocks last, reads that partial ahead of
+    // its own last MMA, adds it (fixed order: c's sum, then c + 1's) and runs the
+    // epilogue, then lowers the flag. No atomic and no second pass.
+    int pair_red;
 };
 
 // Per-row output multiplier of a weight-only quantised matrix.
@@ -341,23 +348,58 @@ __global__ void __launch_bounds__(192, 2)
         const int nch = p.paired ? 64 : 128;
         int seg = 0;
         long long u = u0;
+        constexpr int kPairMax = BN <= 32 ? BN : 1;  // pairwise reduction for BN <= 32
         while (u < u1) {
             const int tile = (int)(u / p.KB);
             const long long tbeg = (long long)tile * p.KB, tend = tbeg + p.KB;
             const long long seg_end = min(u1, tend);
             const bool whole = (u == tbeg) && (seg_end == tend);
+            const bool pair_head = p.pair_red && !whole && seg_end == u1 && u1 < tend;  // this CTA reduces
+            const bool pair_tail = p.pair_red && !whole && u == u0 && u0 > tbeg;        // CTA c - 1 reduces
             const int a = seg & 1;
-            const bool got = mbar_wait_bounded(&tfull[a], ((uint32_t)seg >> 1) & 1u, &s_abort);
+            float pv[kPairMax];
+            bool got = true;
+            if (pair_head && BN <= 32) {
+                // CTA c + 1's partial of this tile, read before this CTA's own last MMA completes
+                if (et == 0) {
+                    const unsigned long long t0 = globaltimer();
+                    while (ld_volatile_i32(&p.counters[tile]) == 0) {
+                        if (s_abort || globaltimer() - t0 > kWaitLimitNs) {
+                            s_abort = 1;
+                            break;
+                        }
+                    }
+                    __threadfence();
+                }
+                named_bar_sync(1, 128);
+                const float4 *src = (const float4 *)(p.partials + ((size_t)(2 * (cta + 1)) * 128 + row) * BN);
+#pragma unroll
+                for (int j = 0; j < kPairMax / 4; ++j) {
+                    const float4 t = __ldcg(src + j);
+                    pv[4 * j] = t.x;
+                    pv[4 * j + 1] = t.y;
+                    pv[4 * j + 2] = t.z;
+                    pv[4 * j + 3] = t.w;
+                }
+                got = !s_abort;
+            }
+            got = got && mbar_wait_bounded(&tfull[a], ((uint32_t)seg >> 1) & 1u, &s_abort);
             if (!named_bar_and(2, 128, got)) break;  // uniform exit keeps the named barriers matched
             tc_fence_after();
             const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * BN);
             const int slot = (tile == (int)(u0 / p.KB)) ? 2 * cta : 2 * cta + 1;
+            const bool final = whole || (pair_head && BN <= 32);
+#pragma unroll
             for (int c0 = 0; c0 < BN; c0 += 16) {
                 float v[16];
                 tmem_ld16(taddr + (uint32_t)c0, v);
+                if (pair_head && BN <= 32) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) v[j] += pv[(c0 + j) % kPairMax];
+                }
                 if (p.epi == EPI_PENDING) {
                     gemm_pending_store<BN>(p, slot, row, c0, v);
-                } else if (whole) {
+                } else if (final) {
                     if (p.paired) {
                         if (q >= 2) {
 #pragma unroll
@@ -388,7 +430,14 @@ __global__ void __launch_bounds__(192, 2)
             }
             tc_fence_before();
             mbar_arrive(&tempty[a]);
-            if (!whole && p.epi != EPI_PENDING) {
+            if (pair_head && BN <= 32) {
+                named_bar_sync(1, 128);
+                if (et == 0) p.counters[tile] = 0;  // the flag is consumed
+            } else if (pair_tail && BN <= 32) {
+                __threadfence();
+                named_bar_sync(1, 128);
+                if (et == 0) st_volatile_i32(&p.counters[tile], 1);
+            } else if (!whole && p.epi != EPI_PENDING) {
                 __threadfence();
                 named_bar_sync(1, 128);
                 const int c_lo = gemm_cta_of_unit(tbeg, p.units, p.grid);
