@@ -195,7 +195,7 @@ __global__ void __launch_bounds__(kLatentThreads) latent_kernel(
 // ---------------------------------------------------------------------------
 constexpr int kRowCl = 8;
 constexpr int kRowClThreads = 256;
-constexpr int kRowVals = 4;      // float4 per thread
+constexpr int kRowVals = 2;      // float4 per thread
 constexpr int kRowClTiles = 16;  // channel tiles a CTA's slice may touch
 
 // The tiles [t0, t0 + nt) of a pending output into shared memory.
