@@ -704,11 +704,19 @@ dspark_status dspark_draft_block(dspark_handle_t *h, float *x, const dspark_kv_t
                 h->c_pool[l] = kv->pools[l];
                 h->c_npages[l] = kv->n_pages;
             }
-            RUN(launch_attention_tc(h->pool_map[l], h->b_blk, ap, L.cps, bs, kvd, g.kv_lora, s));
+            // the split combine is fused with the v absorption when it fits
+            const bool fused = attn_combine_vabsorb_fits(g.d_v, g.kv_lora, L.splits);
+            RUN(launch_attention_tc(h->pool_map[l], h->b_blk, ap, L.cps, bs, kvd, g.kv_lora, s, !fused));
+            if (fused)
+                RUN(launch_attn_combine_vabsorb(ap, M, g.n_heads, g.d_nope, g.d_v, g.kv_lora,
+                                                (const __nv_bfloat16 *)W.w_kv_b, ov, s));
+            else
+                RUN(launch_v_absorb(olat, M, g.n_heads, g.d_nope, g.d_v, g.kv_lora, (const __nv_bfloat16 *)W.w_kv_b,
+                                    ov, s));
         } else {
             RUN(launch_attention(ap, bs, kvd, g.kv_lora, s));
+            RUN(launch_v_absorb(olat, M, g.n_heads, g.d_nope, g.d_v, g.kv_lora, (const __nv_bfloat16 *)W.w_kv_b, ov, s));
         }
-        RUN(launch_v_absorb(olat, M, g.n_heads, g.d_nope, g.d_v, g.kv_lora, (const __nv_bfloat16 *)W.w_kv_b, ov, s));
         RUN(quant ? gemm_q(h, h->qo[l], nullptr, h->b_ov, g.hidden, g.n_heads * g.d_v, M, EPI_ADD, x, nullptr, g.hidden,
                            ws, s, want_o)
                   : gemm(h, h->o[l], nullptr, h->b_ov, g.hidden, g.n_heads * g.d_v, M, EPI_ADD, x, nullptr, g.hidden, ws,

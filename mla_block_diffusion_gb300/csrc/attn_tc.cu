@@ -422,7 +422,7 @@ int attention_tc_splits(int R, int dv, int bs, int max_ctx, int num_sms, int *cp
 }
 
 cudaError_t launch_attention_tc(const CUtensorMap &pool_map, const CUtensorMap &blk_map, const AttnParams &a,
-                                int cps, int bs, int dqk, int dv, cudaStream_t st) {
+                                int cps, int bs, int dqk, int dv, cudaStream_t st, bool combine) {
     if (!attention_tc_supported(dqk, dv)) return cudaErrorInvalidValue;
     using C = TcCfg<576, 512>;
     static bool attr = false;
@@ -454,7 +454,7 @@ cudaError_t launch_attention_tc(const CUtensorMap &pool_map, const CUtensorMap &
     dim3 grid(tiles * C::kParts, a.splits, bs);
     cudaError_t e = launch_pdl(mla_attention_tc_kernel<576, 512>, grid, dim3(192), (size_t)C::kSmem, st, pool_map,
                                blk_map, p);
-    if (e != cudaSuccess || a.splits == 1) return e;
+    if (e != cudaSuccess || a.splits == 1 || !combine) return e;
     return launch_attn_combine(a, bs, dv, st);
 }
 

@@ -52,6 +52,11 @@ cudaError_t launch_latent_cluster(const float *qkv, int ld, const GemmPending *p
                                   int d_rope, const float *g_q, const float *g_kv, float eps, const int32_t *ctx_len,
                                   int block, int max_ctx, const RopeTable &rt, __nv_bfloat16 *cq,
                                   __nv_bfloat16 *blk_kv, int M, int *err, cudaStream_t st);
+// The attention's split combine fused with the v absorption (the split
+// partials, or o_lat when there is one split, -> bf16 [M, n_h * d_v]).
+bool attn_combine_vabsorb_fits(int d_v, int kv_lora, int splits);
+cudaError_t launch_attn_combine_vabsorb(const AttnParams &p, int M, int n_h, int d_nope, int d_v, int kv_lora,
+                                        const __nv_bfloat16 *w_kvb, __nv_bfloat16 *out, cudaStream_t st);
 cudaError_t launch_v_absorb(const float *o_lat, int M, int n_h, int d_nope, int d_v, int kv_lora,
                             const __nv_bfloat16 *w_kvb, __nv_bfloat16 *out, cudaStream_t st);
 bool attention_supported(int dqk, int dv);
@@ -72,8 +77,9 @@ cudaError_t launch_ctx_advance(int32_t *ctx_len, const int32_t *n_new, int n_max
 // both with 64 x 64 boxes in the 128-byte swizzle.
 bool attention_tc_supported(int dqk, int dv);
 int attention_tc_splits(int R, int dv, int bs, int max_ctx, int num_sms, int *cps);
+// combine = false: the caller combines the splits (launch_attn_combine_vabsorb).
 cudaError_t launch_attention_tc(const CUtensorMap &pool_map, const CUtensorMap &blk_map, const AttnParams &a,
-                                int cps, int bs, int dqk, int dv, cudaStream_t st);
+                                int cps, int bs, int dqk, int dv, cudaStream_t st, bool combine = true);
 cudaError_t launch_confidence(const float *h_out, int H, const float *w, float bias, float *conf, int M,
                               cudaStream_t st);
 

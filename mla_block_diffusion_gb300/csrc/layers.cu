@@ -616,6 +616,152 @@ __global__ void __launch_bounds__(kQAbs2Threads, 1) q_absorb2_kernel(
 }
 
 // ---------------------------------------------------------------------------
+// Split combine fused with the v absorption (after the tensor-core attention):
+// grid (n_h, ceil(M / 4)), 512 threads, one CTA per head and 4 rows. The CTA
+// copies the head's v_b rows (d_v x kv_lora bf16; in L2: the q_b GEMM pulls
+// kv_b in) into shared memory with asynchronous copies issued before the
+// dependency wait, rows padded by 16 bytes (the rows a warp reads at once fall
+// in different banks); forms its rows of o_lat from the attention's split
+// partials (weights 2^(m_s - M) / sum_s 2^(m_s - M) l_s over the non-empty
+// splits, in split order; o_lat is read as is when there is one split), every
+// split's load in flight at once; then thread t forms the dot products of
+// channel t % 128 over the quarter t / 128 of the latent for the 4 rows, and
+// the quarters are added in order through shared memory.
+// ---------------------------------------------------------------------------
+constexpr int kCVRows = 4;
+constexpr int kCVThreads = 512;
+constexpr int kCVMaxSplit = 16;
+constexpr int kCVChan = kCVThreads / 4;  // channels per pass
+
+DS_DEVINL void cp_async16(void *smem_dst, const void *gmem_src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
+}
+
+__global__ void __launch_bounds__(kCVThreads) attn_combine_vabsorb_kernel(
+    const float *__restrict__ part_o, const float *__restrict__ part_ml, int splits, int R,
+    const float *__restrict__ o_lat, int M, int n_h, int block, int d_nope, int d_v, int kv_lora,
+    const __nv_bfloat16 *__restrict__ w_kvb, __nv_bfloat16 *__restrict__ out) {
+    pdl_trigger();
+    extern __shared__ __align__(16) uint8_t smc[];
+    const int wstride = kv_lora * 2 + 16;                              // bytes per staged v_b row
+    uint8_t *sw = smc;                                                 // [d_v][wstride]
+    float *so = (float *)(smc + (size_t)d_v * wstride);                // [kCVRows][kv_lora]
+    float *swt = so + kCVRows * kv_lora;                               // [kCVRows][kCVMaxSplit]
+    float *sred = swt + kCVRows * kCVMaxSplit;                         // [4 quarters][kCVRows][kCVChan]
+    const int h = blockIdx.x, m0 = blockIdx.y * kCVRows;
+    const int mr = min(kCVRows, M - m0);
+    const int c8n = kv_lora / 8, c4n = kv_lora / 4;
+    // the head's v_b rows: weights of the step, copied before the dependency wait
+    const uint4 *W4 = (const uint4 *)(w_kvb + ((size_t)h * (d_nope + d_v) + d_nope) * kv_lora);
+    for (int i = threadIdx.x; i < d_v * c8n; i += blockDim.x)
+        cp_async16(sw + (size_t)(i / c8n) * wstride + (i % c8n) * 16, W4 + i);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    pdl_wait();
+    if (splits > 1) {
+        if ((int)threadIdx.x < mr) {
+            const int m = m0 + threadIdx.x, b = m / block, r = (m % block) * n_h + h;
+            const float *ml = part_ml + ((size_t)b * splits * R + r) * 2;
+            float2 v[kCVMaxSplit];
+#pragma unroll
+            for (int s = 0; s < kCVMaxSplit; ++s)
+                v[s] = s < splits ? __ldcg((const float2 *)(ml + (size_t)s * R * 2)) : make_float2(0.f, 0.f);
+            float mx = -INFINITY;
+#pragma unroll
+            for (int s = 0; s < kCVMaxSplit; ++s)
+                if (s < splits && v[s].y > 0.f) mx = fmaxf(mx, v[s].x);
+            float den = 0.f;
+#pragma unroll
+            for (int s = 0; s < kCVMaxSplit; ++s)
+                if (s < splits && v[s].y > 0.f) den += exp2f(v[s].x - mx) * v[s].y;
+            const float inv = den > 0.f ? 1.f / den : 0.f;
+#pragma unroll
+            for (int s = 0; s < kCVMaxSplit; ++s)
+                swt[threadIdx.x * kCVMaxSplit + s] = (s < splits && v[s].y > 0.f) ? exp2f(v[s].x - mx) * inv : 0.f;
+        }
+        __syncthreads();
+        for (int i = threadIdx.x; i < kCVRows * c4n; i += blockDim.x) {
+            const int mm = i / c4n, c4 = i % c4n;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (mm < mr) {
+                const int m = m0 + mm, b = m / block, r = (m % block) * n_h + h;
+                const float4 *src = (const float4 *)(part_o + ((size_t)b * splits * R + r) * kv_lora) + c4;
+                const size_t sstep = (size_t)R * kv_lora / 4;
+                float4 v[kCVMaxSplit];
+#pragma unroll
+                for (int s = 0; s < kCVMaxSplit; ++s)
+                    v[s] = s < splits ? __ldcg(src + s * sstep) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int s = 0; s < kCVMaxSplit; ++s) {
+                    if (s < splits) {
+                        const float w = swt[mm * kCVMaxSplit + s];
+                        acc.x += w * v[s].x;
+                        acc.y += w * v[s].y;
+                        acc.z += w * v[s].z;
+                        acc.w += w * v[s].w;
+                    }
+                }
+            }
+            ((float4 *)so)[mm * c4n + c4] = acc;
+        }
+    } else {
+        for (int i = threadIdx.x; i < kCVRows * c4n; i += blockDim.x) {
+            const int mm = i / c4n, c4 = i % c4n;
+            ((float4 *)so)[i] = mm < mr ? __ldcg((const float4 *)(o_lat + ((size_t)(m0 + mm) * n_h + h) * kv_lora) + c4)
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncthreads();
+    // v absorption: channel e = e0 + t % 128, latent quarter q = t / 128
+    const int q = threadIdx.x / kCVChan, cq = kv_lora / 4;
+    for (int e0 = 0; e0 < d_v; e0 += kCVChan) {
+        const int e = e0 + (int)(threadIdx.x % kCVChan);
+        float a[kCVRows] = {0.f, 0.f, 0.f, 0.f};
+        if (e < d_v) {
+            const uint8_t *wr = sw + (size_t)e * wstride + q * cq * 2;
+            const float *orow = so + q * cq;
+            for (int c = 0; c < cq; c += 8) {
+                const uint4 wq = *(const uint4 *)(wr + c * 2);
+                const uint32_t wu[4] = {wq.x, wq.y, wq.z, wq.w};
+                float wf[8];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&wu[j]));
+                    wf[2 * j] = f.x;
+                    wf[2 * j + 1] = f.y;
+                }
+#pragma unroll
+                for (int mm = 0; mm < kCVRows; ++mm) {
+                    const float4 x0 = *(const float4 *)(orow + mm * kv_lora + c);
+                    const float4 x1 = *(const float4 *)(orow + mm * kv_lora + c + 4);
+                    a[mm] = fmaf(wf[0], x0.x, a[mm]);
+                    a[mm] = fmaf(wf[1], x0.y, a[mm]);
+                    a[mm] = fmaf(wf[2], x0.z, a[mm]);
+                    a[mm] = fmaf(wf[3], x0.w, a[mm]);
+                    a[mm] = fmaf(wf[4], x1.x, a[mm]);
+                    a[mm] = fmaf(wf[5], x1.y, a[mm]);
+                    a[mm] = fmaf(wf[6], x1.z, a[mm]);
+                    a[mm] = fmaf(wf[7], x1.w, a[mm]);
+                }
+            }
+        }
+#pragma unroll
+        for (int mm = 0; mm < kCVRows; ++mm) sred[(q * kCVRows + mm) * kCVChan + threadIdx.x % kCVChan] = a[mm];
+        __syncthreads();
+        if ((int)threadIdx.x < kCVRows * kCVChan) {
+            const int mm = threadIdx.x / kCVChan, ee = threadIdx.x % kCVChan, e2 = e0 + ee;
+            if (mm < mr && e2 < d_v) {
+                float t = 0.f;
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq) t += sred[(qq * kCVRows + mm) * kCVChan + ee];
+                out[(size_t)(m0 + mm) * n_h * d_v + (size_t)h * d_v + e2] = __float2bfloat16(t);
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------------------
 // v absorption: o_h = W_vb,h o_lat,h -> bf16 [M, n_h * d_v] (operand of o_proj).
 // Grid (n_h, d_v / 16): a CTA owns 16 output channels of one head; 16 threads
 // per channel each hold 4-element slices of the channel's W_vb row at
@@ -1162,6 +1308,35 @@ cudaError_t launch_attention(const AttnParams &p, int bs, int dqk, int dv, cudaS
         return cudaErrorInvalidValue;
     if (e != cudaSuccess || p.splits == 1) return e;
     return launch_attn_combine(p, bs, dv, st);
+}
+
+// Shared memory of the fused combine + v absorption.
+static size_t cvabs_smem(int d_v, int kv_lora) {
+    return (size_t)d_v * (kv_lora * 2 + 16) + (size_t)kCVRows * kv_lora * 4 + (size_t)kCVRows * kCVMaxSplit * 4 +
+           (size_t)4 * kCVRows * kCVChan * 4;
+}
+
+bool attn_combine_vabsorb_fits(int d_v, int kv_lora, int splits) {
+    return kv_lora % 16 == 0 && splits <= kCVMaxSplit && cvabs_smem(d_v, kv_lora) <= 227u * 1024u;
+}
+
+cudaError_t launch_attn_combine_vabsorb(const AttnParams &p, int M, int n_h, int d_nope, int d_v, int kv_lora,
+                                        const __nv_bfloat16 *w_kvb, __nv_bfloat16 *out, cudaStream_t st) {
+    const size_t smem = cvabs_smem(d_v, kv_lora);
+    static std::mutex mu;
+    static size_t set_bytes = 0;  // the largest limit set so far (handles of several geometries)
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (smem > set_bytes) {
+            const cudaError_t e = cudaFuncSetAttribute(attn_combine_vabsorb_kernel,
+                                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+            set_bytes = smem;
+        }
+    }
+    return launch_pdl(attn_combine_vabsorb_kernel, dim3(n_h, (M + kCVRows - 1) / kCVRows), dim3(kCVThreads), smem,
+                      st, p.part_o, p.part_ml, p.splits, p.R, p.o_lat, M, n_h, p.block, d_nope, d_v, kv_lora, w_kvb,
+                      out);
 }
 
 cudaError_t launch_attn_combine(const AttnParams &p, int bs, int dv, cudaStream_t st) {
