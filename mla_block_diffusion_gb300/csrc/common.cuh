@@ -407,6 +407,22 @@ DS_DEVINL uint32_t cluster_rank() {
 DS_DEVINL void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// Split cluster barrier without memory ordering (ordering comes from elsewhere):
+// arrive early, wait before the CTA may stop being a target of its peers.
+DS_DEVINL void cluster_arrive_relaxed() { asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory"); }
+DS_DEVINL void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+
+// Asynchronous store of two floats into the same shared-memory location of CTA
+// `rank`, counted as 8 transaction bytes on that CTA's mbarrier at local_bar.
+DS_DEVINL void st_async_peer_f2(float2 *local_dst, uint64_t *local_bar, uint32_t rank, float2 v) {
+    uint32_t a, b;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(local_dst)), "r"(rank));
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(b) : "r"(smem_u32(local_bar)), "r"(rank));
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(a),
+                 "f"(v.x), "f"(v.y), "r"(b)
+                 : "memory");
+}
+
 // Store into the same shared-memory location of CTA `rank` of the cluster
 // (visible to it after the next cluster barrier).
 DS_DEVINL void st_peer_f2(float2 *local, uint32_t rank, float2 v) {

@@ -210,14 +210,27 @@ DS_DEVINL void row_slice(int n4, int &i0, int &i1) {
     i1 = (int)((long long)(k + 1) * n4 / kRowCl);
 }
 
-// The cluster's total of (a, b) over its CTAs, in rank order. Every thread of
-// every CTA calls it: thread k stores this CTA's sum into slot `rank` of CTA k,
-// one cluster barrier makes the stores visible, and every CTA adds its own
-// kRowCl slots (no remote access after the barrier, so a CTA may then exit).
-DS_DEVINL float2 cluster_sum2(float2 v, float2 *red, float2 *parts) {
-    v = block_sum2(v, red);
-    if (threadIdx.x < (unsigned)kRowCl) st_peer_f2(parts + cluster_rank(), threadIdx.x, v);
+// The cluster's exchange of (a, b) sums. Before the dependency wait each CTA
+// sets up a local mbarrier that expects one 8-byte value from every CTA of the
+// cluster (cluster_sum_setup, then a cluster barrier so that no value arrives
+// before its barrier exists). cluster_sum2: thread k sends this CTA's sum to
+// slot `rank` of CTA k (st.async, counted on CTA k's mbarrier), every thread
+// arrives on a relaxed cluster barrier (waited at exit: a CTA stays a valid
+// target until every peer has sent), the CTA waits for its own eight values and
+// adds them in rank order. Every thread of every CTA calls both.
+DS_DEVINL void cluster_sum_setup(uint64_t *bar) {
+    if (threadIdx.x == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(bar, (uint32_t)(kRowCl * sizeof(float2)));
+    }
     cluster_sync();
+}
+DS_DEVINL float2 cluster_sum2(float2 v, float2 *red, float2 *parts, uint64_t *bar, volatile int *fail) {
+    v = block_sum2(v, red);
+    if (threadIdx.x < (unsigned)kRowCl) st_async_peer_f2(parts + cluster_rank(), bar, threadIdx.x, v);
+    cluster_arrive_relaxed();
+    if (!mbar_wait_bounded(bar, 0, fail)) *fail = 1;
     float2 t = make_float2(0.f, 0.f);
 #pragma unroll
     for (int k = 0; k < kRowCl; ++k) {
@@ -243,6 +256,8 @@ __global__ void __launch_bounds__(kRowClThreads) rmsnorm_cluster_kernel(
     pdl_trigger();
     __shared__ float2 red[33];
     __shared__ float2 s_parts[kRowCl];
+    __shared__ __align__(8) uint64_t s_bar;
+    __shared__ volatile int s_fail;
     __shared__ PendTile s_tiles[kRowClTiles];
     const int m = blockIdx.y;
     int i0, i1;
@@ -256,7 +271,8 @@ __global__ void __launch_bounds__(kRowClThreads) rmsnorm_cluster_kernel(
         const int i = i0 + threadIdx.x + k * kRowClThreads;
         gv[k] = i < i1 ? __ldg(g4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    __syncthreads();
+    if (threadIdx.x == 0) s_fail = 0;
+    cluster_sum_setup(&s_bar);
     pdl_wait();
     float4 *xr = (float4 *)(x + (size_t)m * ldx);
     float4 v[kRowVals];
@@ -278,7 +294,8 @@ __global__ void __launch_bounds__(kRowClThreads) rmsnorm_cluster_kernel(
         }
         ss += v[k].x * v[k].x + v[k].y * v[k].y + v[k].z * v[k].z + v[k].w * v[k].w;
     }
-    const float tot = cluster_sum2(make_float2(ss, 0.f), red, s_parts).x;
+    const float tot = cluster_sum2(make_float2(ss, 0.f), red, s_parts, &s_bar, &s_fail).x;
+    if (threadIdx.x == 0 && s_fail) set_error(err, DSPARK_ERR_TIMEOUT);
     if (!isfinite(tot) && threadIdx.x == 0 && cluster_rank() == 0) set_error(err, DSPARK_ERR_BAD_INPUT);
     const float r = rsqrtf(tot / (float)H + eps);
 #pragma unroll
@@ -293,6 +310,7 @@ __global__ void __launch_bounds__(kRowClThreads) rmsnorm_cluster_kernel(
             if (y32) ((float4 *)(y32 + (size_t)m * ldy32))[i] = o;
         }
     }
+    cluster_wait();
 }
 
 // Latent norms and RoPE of the q_a || kv_a output (see latent_kernel), the row
@@ -305,6 +323,8 @@ __global__ void __launch_bounds__(kRowClThreads) latent_cluster_kernel(
     pdl_trigger();
     __shared__ float2 red[33];
     __shared__ float2 s_parts[kRowCl];
+    __shared__ __align__(8) uint64_t s_bar;
+    __shared__ volatile int s_fail;
     __shared__ PendTile s_tiles[kRowClTiles];
     const int m = blockIdx.y, b = m / block, pos_i = m % block;
     const int nq4 = q_lora / 4, nk4 = kv_lora / 4, n4 = nq4 + nk4 + d_rope / 4;
@@ -321,7 +341,8 @@ __global__ void __launch_bounds__(kRowClThreads) latent_cluster_kernel(
                                                    : make_float4(0.f, 0.f, 0.f, 0.f));
     }
     int c = ctx_len[b];
-    __syncthreads();
+    if (threadIdx.x == 0) s_fail = 0;
+    cluster_sum_setup(&s_bar);
     pdl_wait();
     const float4 *row = (const float4 *)(qkv + (size_t)m * ld);
     float4 v[kRowVals];
@@ -336,7 +357,8 @@ __global__ void __launch_bounds__(kRowClThreads) latent_cluster_kernel(
         else if (i < nq4 + nk4)
             ss.y += sq;
     }
-    ss = cluster_sum2(ss, red, s_parts);
+    ss = cluster_sum2(ss, red, s_parts, &s_bar, &s_fail);
+    if (threadIdx.x == 0 && s_fail) set_error(err, DSPARK_ERR_TIMEOUT);
     if ((!isfinite(ss.x) || !isfinite(ss.y)) && threadIdx.x == 0 && cluster_rank() == 0)
         set_error(err, DSPARK_ERR_BAD_INPUT);
     const float rq = rsqrtf(ss.x / (float)q_lora + eps), rk = rsqrtf(ss.y / (float)kv_lora + eps);
@@ -372,6 +394,7 @@ __global__ void __launch_bounds__(kRowClThreads) latent_cluster_kernel(
             dst[3] = __float2bfloat16(t.z * s1 + t.w * c1);
         }
     }
+    cluster_wait();
 }
 
 // ---------------------------------------------------------------------------
