@@ -53,6 +53,20 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, ui
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// bf16 tensor [outer, rows, cols] read in boxes of 64 columns x box_rows rows of
+// one outer index, 128-byte swizzle; rows past `rows` read as zero.
+bool make_map_3d(CUtensorMap *m, const void *base, uint64_t outer, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || !base) return false;
+    cuuint64_t dims[3] = {cols, rows, outer};
+    cuuint64_t strides[2] = {cols * 2, rows * cols * 2};
+    cuuint32_t box[3] = {64, box_rows, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // uint8 matrix [rows, cols_bytes] (quantised weights or their group scales).
 bool encode_map_u32(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_inner,
                     uint32_t box_rows) {
@@ -146,6 +160,7 @@ struct dspark_handle {
     int c_bs = -1;
     CUtensorMap b_hn, b_cq, b_ov, b_act, b_hout;
     CUtensorMap b_blk;                       // block latents, tensor-core attention
+    CUtensorMap b_qt;                        // absorbed queries [bs, block * heads, kvd], tensor-core attention
     CUtensorMap kva[DSPARK_MAX_LAYERS];      // kv_a rows of the fused q_a || kv_a weights
     const void *c_app_ws = nullptr;
     int c_app_rows = -1;
@@ -626,7 +641,8 @@ dspark_status dspark_draft_block(dspark_handle_t *h, float *x, const dspark_kv_t
         if (!make_map(&h->b_hn, hn, M, g.hidden, bn) || !make_map(&h->b_cq, cq, M, g.q_lora, bn) ||
             !make_map(&h->b_ov, ov, M, (uint64_t)g.n_heads * g.d_v, bn) ||
             !make_map(&h->b_act, act, M, g.inter, bn) || !make_map(&h->b_hout, hout, M, g.hidden, bn) ||
-            (L.tc && !make_map(&h->b_blk, blk, M, kvd, 64)))
+            (L.tc && (!make_map(&h->b_blk, blk, M, kvd, 64) ||
+                      !make_map_3d(&h->b_qt, qt, bs, (uint64_t)g.block * g.n_heads, kvd, 128))))
             return DSPARK_ERR_CUDA;
         h->c_ws = ws;
         h->c_bs = bs;
@@ -706,7 +722,7 @@ dspark_status dspark_draft_block(dspark_handle_t *h, float *x, const dspark_kv_t
             }
             // the split combine is fused with the v absorption when it fits
             const bool fused = attn_combine_vabsorb_fits(g.d_v, g.kv_lora, L.splits);
-            RUN(launch_attention_tc(h->pool_map[l], h->b_blk, ap, L.cps, bs, kvd, g.kv_lora, s, !fused));
+            RUN(launch_attention_tc(h->pool_map[l], h->b_blk, h->b_qt, ap, L.cps, bs, kvd, g.kv_lora, s, !fused));
             if (fused)
                 RUN(launch_attn_combine_vabsorb(ap, M, g.n_heads, g.d_nope, g.d_v, g.kv_lora,
                                                 (const __nv_bfloat16 *)W.w_kv_b, ov, s));

@@ -20,8 +20,13 @@
 // and rescales O only when a new maximum exceeds it by more than 2^8 (the
 // result is the same: O and the row sum carry the same reference).
 //
+// The Q tile (128 rows x DQK) arrives by TMA in the space of KV stages 1 and 2
+// (the first chunk is prefetched into stage 0 before the dependency wait, the
+// next two pages into L2); the softmax warps move it from shared to tensor
+// memory, after which the two stages take KV chunks again.
+//
 // Roles (6 warps): warp 0 TMA producer; warp 1 MMA issuer and tensor-memory
-// owner; warps 2-5 load Q, run the softmax (one thread per row) and write the
+// owner; warps 2-5 move Q, run the softmax (one thread per row) and write the
 // split partial. All waits are bounded; a timeout raises DSPARK_ERR_TIMEOUT.
 #include "internal.h"
 
@@ -44,7 +49,10 @@ struct TcCfg {
     static constexpr int kSCol = kDQKP / 2;
     static constexpr int kPCol = kSCol + 64;
     static constexpr int kOCol = kPCol + 32;
+    static constexpr int kQBoxBytes = kTcRows * 128;       // 128 rows x 64 bf16
+    static constexpr int kQBytes = kBoxes * kQBoxBytes;
     static constexpr int kSmem = 1024 + kTcStages * kTileBytes + 256;
+    static_assert(kQBytes <= (kTcStages - 1) * kTileBytes, "the Q tile fits KV stages 1..");
     static_assert(kOCol + kDVP <= 512, "tensor memory");
     static_assert(DV % kDVP == 0 && kDVP % 64 == 0, "output part: whole 64-column atoms");
     static_assert(kSmem <= 232448, "shared memory");
@@ -54,6 +62,7 @@ bool attention_tc_supported(int dqk, int dv) { return dqk == 576 && dv == 512; }
 
 struct TcAttnParams {
     const __nv_bfloat16 *qt;      // [bs, R, DQK]
+    const __nv_bfloat16 *pool;    // [n_pages, 64, DQK] (L2 prefetch of the first pages)
     int R;                        // rows per sequence
     int n_pages;
     const int32_t *page_table;    // [bs, max_pages]
@@ -104,7 +113,7 @@ DS_DEVINL bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
 template <int DQK, int DV>
 __global__ void __launch_bounds__(192, 2)
     mla_attention_tc_kernel(const __grid_constant__ CUtensorMap tmPool, const __grid_constant__ CUtensorMap tmBlk,
-                            const TcAttnParams p) {
+                            const __grid_constant__ CUtensorMap tmQ, const TcAttnParams p) {
     using C = TcCfg<DQK, DV>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -112,7 +121,8 @@ __global__ void __launch_bounds__(192, 2)
     uint64_t *bars = (uint64_t *)(smem + kTcStages * C::kTileBytes);
     uint64_t *kv_full = bars, *kv_empty = bars + kTcStages;
     uint64_t *s_full = bars + 2 * kTcStages, *s_free = s_full + 1, *p_ready = s_full + 2, *pv_done = s_full + 3;
-    uint64_t *q_ready = s_full + 4, *mma_done = s_full + 5;
+    uint64_t *q_ready = s_full + 4, *mma_done = s_full + 5, *q_full = s_full + 6;
+    uint8_t *sQ = smem + C::kTileBytes;  // KV stages 1.. until the Q tile is in tensor memory
     __shared__ uint32_t s_tmem;
     __shared__ volatile int s_abort;
 
@@ -133,12 +143,14 @@ __global__ void __launch_bounds__(192, 2)
         mbar_init(pv_done, 1);
         mbar_init(q_ready, 4);
         mbar_init(mma_done, 1);
+        mbar_init(q_full, 1);
         s_abort = 0;
         fence_mbar_init();
     }
     if (threadIdx.x == 32) {
         tma_prefetch_desc(&tmPool);
         tma_prefetch_desc(&tmBlk);
+        tma_prefetch_desc(&tmQ);
     }
     if (warp == 1) tmem_alloc(&s_tmem, 512);
     tc_fence_before();
@@ -158,6 +170,7 @@ __global__ void __launch_bounds__(192, 2)
     const int c_end = min(npages + 1, c_begin + p.cps);
     const int nch = c_end > c_begin ? c_end - c_begin : 0;
     int issued = 0;
+    bool q_issued = false;
 
     if (threadIdx.x == 32)
         l2_prefetch_share(p.pf, blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z),
@@ -165,16 +178,9 @@ __global__ void __launch_bounds__(192, 2)
     if (warp != 0 || lane != 0) pdl_wait();
     if (warp == 0) {
         if (lane == 0) {
-            bool waited = false;
-            for (int i = 0; i < nch; ++i) {
+            // KV chunk c of this split into stage st
+            auto load_chunk = [&](int i) {
                 const int st = i % kTcStages;
-                if (!waited && (i >= kTcStages || c_begin + i >= npages)) {
-                    pdl_wait();
-                    waited = true;
-                }
-                if (i >= kTcStages &&
-                    !mbar_wait_bounded(&kv_empty[st], (uint32_t)((i / kTcStages - 1) & 1), &s_abort))
-                    break;
                 const int c = c_begin + i;
                 mbar_arrive_expect_tx(&kv_full[st], (uint32_t)C::kTileBytes);
                 uint8_t *dst = sKV + st * C::kTileBytes;
@@ -192,9 +198,38 @@ __global__ void __launch_bounds__(192, 2)
                     for (int j = 0; j < C::kBoxes; ++j)
                         tma_load_2d(dst + j * C::kBoxBytes, &tmBlk, j * 64, b * p.block, &kv_full[st]);
                 }
-                issued = i + 1;
+            };
+            // before the dependency wait: the first chunk when it is a page of the pool
+            // (an input of the step), and the next two pages into L2
+            if (nch > 0 && c_begin < npages) {
+                load_chunk(0);
+                issued = 1;
             }
-            if (!waited) pdl_wait();
+            for (int i = 1; i < kTcStages && i < nch && c_begin + i < npages; ++i) {
+                const int pg = p.page_table[(size_t)b * p.max_pages + c_begin + i];
+                if (pg >= 0 && pg < p.n_pages)
+                    prefetch_l2_bulk(p.pool + (size_t)pg * kTcKeys * DQK, (uint32_t)C::kTileBytes);
+            }
+            pdl_wait();
+            mbar_arrive_expect_tx(q_full, (uint32_t)C::kQBytes);
+#pragma unroll 1
+            for (int j = 0; j < C::kBoxes; ++j) tma_load_3d(sQ + j * C::kQBoxBytes, &tmQ, j * 64, r0, b, q_full);
+            q_issued = true;
+            if (issued == 0 && nch > 0) {
+                load_chunk(0);
+                issued = 1;
+            }
+            // stages 1.. hold the Q tile until the softmax warps have moved it
+            if (nch > 1 && mbar_wait_bounded(q_ready, 0, &s_abort)) {
+                for (int i = 1; i < nch; ++i) {
+                    const int st = i % kTcStages;
+                    if (i >= kTcStages &&
+                        !mbar_wait_bounded(&kv_empty[st], (uint32_t)((i / kTcStages - 1) & 1), &s_abort))
+                        break;
+                    load_chunk(i);
+                    issued = i + 1;
+                }
+            }
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -246,42 +281,33 @@ __global__ void __launch_bounds__(192, 2)
         const int row = 32 * q4 + lane, r = r0 + row;
         const bool rv = r < p.R;
         const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
-        // Q row into tensor memory (bf16 pairs; the padding past DQK is zero)
-        const __nv_bfloat16 *qrow = p.qt + ((size_t)b * p.R + (rv ? r : 0)) * DQK;
-        auto qload = [&](int c32, uint4 (&u)[8]) {
+        // Q row from the TMA tile (128-byte swizzle: 16-byte piece j of row r sits at
+        // piece j ^ (r & 7)) into tensor memory as bf16 pairs; rows past R are zero
+        bool ok = warp_wait(q_full, 0, &s_abort);
+        if (ok) {
+            const uint8_t *qrow = sQ + row * 128;
+#pragma unroll 1
+            for (int bq = 0; bq < C::kBoxes; ++bq) {
+                uint32_t v[32];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int e = 2 * c32 + 8 * j;
-                u[j] = (rv && e < DQK) ? __ldg((const uint4 *)(qrow + e)) : make_uint4(0u, 0u, 0u, 0u);
+                for (int j = 0; j < 8; ++j) {
+                    const uint4 u = *(const uint4 *)(qrow + bq * C::kQBoxBytes + ((j ^ (row & 7)) << 4));
+                    v[4 * j] = u.x;
+                    v[4 * j + 1] = u.y;
+                    v[4 * j + 2] = u.z;
+                    v[4 * j + 3] = u.w;
+                }
+                tmem_st32(tl + C::kQCol + 32 * bq, v);
             }
-        };
-        // nine batches of 32 columns, three in flight
-        constexpr int kQBatches = C::kDQKP / 64;
-        uint4 qv[3][8];
-#pragma unroll
-        for (int bq = 0; bq < 3 && bq < kQBatches; ++bq) qload(32 * bq, qv[bq]);
-#pragma unroll
-        for (int bq = 0; bq < kQBatches; ++bq) {
-            uint32_t v[32];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                v[4 * j] = qv[bq % 3][j].x;
-                v[4 * j + 1] = qv[bq % 3][j].y;
-                v[4 * j + 2] = qv[bq % 3][j].z;
-                v[4 * j + 3] = qv[bq % 3][j].w;
-            }
-            tmem_st32(tl + C::kQCol + 32 * bq, v);
-            if (bq + 3 < kQBatches) qload(32 * (bq + 3), qv[bq % 3]);
         }
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(q_ready);
+        if (lane == 0 && ok) mbar_arrive(q_ready);
 
         float m_ref = -INFINITY, lsum = 0.f;
-        bool ok = true;
         int done = 0;
-        for (int i = 0; i < nch; ++i) {
+        for (int i = 0; i < nch && ok; ++i) {
             const int c = c_begin + i;
             const int nvalid = c < npages ? min(kTcKeys, ctx - c * kTcKeys) : p.block;
             if (!warp_wait(s_full, (uint32_t)(i & 1), &s_abort)) {
@@ -398,6 +424,7 @@ __global__ void __launch_bounds__(192, 2)
             // the last chunk issued to each stage lands before shared memory is released
             for (int i = issued - 1; i >= 0 && i >= issued - kTcStages; --i)
                 mbar_drain(&kv_full[i % kTcStages], (uint32_t)((i / kTcStages) & 1));
+            if (q_issued) mbar_drain(q_full, 0);
         }
         __syncthreads();
     }
@@ -421,7 +448,8 @@ int attention_tc_splits(int R, int dv, int bs, int max_ctx, int num_sms, int *cp
     return (chunks + *cps - 1) / *cps;
 }
 
-cudaError_t launch_attention_tc(const CUtensorMap &pool_map, const CUtensorMap &blk_map, const AttnParams &a,
+cudaError_t launch_attention_tc(const CUtensorMap &pool_map, const CUtensorMap &blk_map, const CUtensorMap &q_map,
+                                const AttnParams &a,
                                 int cps, int bs, int dqk, int dv, cudaStream_t st, bool combine) {
     if (!attention_tc_supported(dqk, dv)) return cudaErrorInvalidValue;
     using C = TcCfg<576, 512>;
@@ -435,6 +463,7 @@ cudaError_t launch_attention_tc(const CUtensorMap &pool_map, const CUtensorMap &
     TcAttnParams p;
     memset(&p, 0, sizeof(p));
     p.qt = a.qt;
+    p.pool = a.pool;
     p.R = a.R;
     p.n_pages = a.n_pages;
     p.page_table = a.page_table;
@@ -453,7 +482,7 @@ cudaError_t launch_attention_tc(const CUtensorMap &pool_map, const CUtensorMap &
     const int tiles = (a.R + kTcRows - 1) / kTcRows;
     dim3 grid(tiles * C::kParts, a.splits, bs);
     cudaError_t e = launch_pdl(mla_attention_tc_kernel<576, 512>, grid, dim3(192), (size_t)C::kSmem, st, pool_map,
-                               blk_map, p);
+                               blk_map, q_map, p);
     if (e != cudaSuccess || a.splits == 1 || !combine) return e;
     return launch_attn_combine(a, bs, dv, st);
 }

@@ -100,6 +100,15 @@ DS_DEVINL void tma_load_2d(void *smem_dst, const CUtensorMap *m, int x, int y, u
         : "memory");
 }
 
+// 3D form: x innermost (elements), y the row, z the outer index.
+DS_DEVINL void tma_load_3d(void *smem_dst, const CUtensorMap *m, int x, int y, int z, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
+            smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // Same, with an L2 cache-policy hint (used to mark streamed weights evict-first).
 DS_DEVINL void tma_load_2d_hint(void *smem_dst, const CUtensorMap *m, int x, int y, uint64_t *bar,
                                 uint64_t policy) {
@@ -509,6 +518,48 @@ DS_DEVINL float4 pending_sum4(const GemmPending &g, const PendTile &pt, int m, i
     }
     return s;
 }
+// NP positions at once (channels r[j] .. r[j] + 3 of row m[j] of tile pt[j]): the
+// first CMAX contributors of every position are loaded before any is added, so
+// the positions share one round trip; contributors past CMAX follow in order.
+// Each sum runs over its tile's CTAs in increasing order (as pending_sum4).
+template <int NP, int CMAX>
+DS_DEVINL void pending_sum4_multi(const GemmPending &g, const PendTile (&pt)[NP], const int (&m)[NP],
+                                  const int (&r)[NP], const bool (&live)[NP], float4 (&out)[NP]) {
+    float4 v[NP][CMAX];
+#pragma unroll
+    for (int j = 0; j < NP; ++j) {
+#pragma unroll
+        for (int u = 0; u < CMAX; ++u) {
+            const int c = pt[j].c_lo + u;
+            const int sl = u == 0 ? pt[j].lo_slot : 2 * c;
+            v[j][u] = (live[j] && c <= pt[j].c_hi)
+                          ? __ldcg((const float4 *)(g.part + ((size_t)sl * g.BN + m[j]) * 128 + r[j]))
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < NP; ++j) {
+        float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int u = 0; u < CMAX; ++u) {
+            if (live[j] && pt[j].c_lo + u <= pt[j].c_hi) {
+                s.x += v[j][u].x;
+                s.y += v[j][u].y;
+                s.z += v[j][u].z;
+                s.w += v[j][u].w;
+            }
+        }
+        for (int c = pt[j].c_lo + CMAX; live[j] && c <= pt[j].c_hi; ++c) {
+            const float4 w = __ldcg((const float4 *)(g.part + ((size_t)(2 * c) * g.BN + m[j]) * 128 + r[j]));
+            s.x += w.x;
+            s.y += w.y;
+            s.z += w.z;
+            s.w += w.w;
+        }
+        out[j] = s;
+    }
+}
+
 // Channel r of row m of a tile (same order).
 DS_DEVINL float pending_sum1(const GemmPending &g, const PendTile &pt, int m, int r) {
     float s = 0.f;

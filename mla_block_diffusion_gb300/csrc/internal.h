@@ -78,8 +78,8 @@ cudaError_t launch_ctx_advance(int32_t *ctx_len, const int32_t *n_new, int n_max
 bool attention_tc_supported(int dqk, int dv);
 int attention_tc_splits(int R, int dv, int bs, int max_ctx, int num_sms, int *cps);
 // combine = false: the caller combines the splits (launch_attn_combine_vabsorb).
-cudaError_t launch_attention_tc(const CUtensorMap &pool_map, const CUtensorMap &blk_map, const AttnParams &a,
-                                int cps, int bs, int dqk, int dv, cudaStream_t st, bool combine = true);
+cudaError_t launch_attention_tc(const CUtensorMap &pool_map, const CUtensorMap &blk_map, const CUtensorMap &q_map,
+                                const AttnParams &a, int cps, int bs, int dqk, int dv, cudaStream_t st, bool combine = true);
 cudaError_t launch_confidence(const float *h_out, int H, const float *w, float bias, float *conf, int M,
                               cudaStream_t st);
 

@@ -513,12 +513,12 @@ __global__ void __launch_bounds__(128) q_absorb_kernel(const float *__restrict__
 // kv_b there while it runs). Warp w takes
 // columns [64 (w % 4), +64) of the chunk (lane l the pair 2l) and the half
 // w / 4 of d_nope; the thread's slice (d_nope / 2 rows of one column pair)
-// stays in registers. Rows sweep in chunks of 4 from shared memory; the two
+// stays in registers. The 8 staged rows are swept at once from shared memory; the two
 // halves' sums are added in half order.
 // ---------------------------------------------------------------------------
 constexpr int kQAbs2Cols = 256;
 constexpr int kQAbs2Threads = 256;
-constexpr int kQAbs2Rows = 4;
+constexpr int kQAbs2Rows = 8;
 constexpr int kQAbs2MaxRope = 128;
 
 template <int MAXDH>
@@ -529,7 +529,8 @@ __global__ void __launch_bounds__(kQAbs2Threads, 1) q_absorb2_kernel(
     pdl_trigger();
     // the head's q rows of a chunk of 8: nope and rope parts, staged in one batch of loads
     constexpr int LD = 2 * MAXDH + kQAbs2MaxRope;
-    constexpr int kPer = kQAbsRows * LD / kQAbs2Threads;  // staged positions per thread
+    constexpr int kPer4 = kQAbsRows * LD / 4 / kQAbs2Threads;  // staged float4 per thread
+    static_assert(kQAbsRows * LD % (4 * kQAbs2Threads) == 0, "whole float4 per thread");
     __shared__ __align__(16) float sq[kQAbsRows][LD];
     __shared__ float2 red[kQAbs2Rows][kQAbs2Cols / 2];  // the second half's sums
     __shared__ PendTile s_tiles[kQAbsTiles];
@@ -565,26 +566,37 @@ __global__ void __launch_bounds__(kQAbs2Threads, 1) q_absorb2_kernel(
         }
         if (m0 == 0) pdl_wait();
         // every position of the staged rows is written: the sweep multiplies the
-        // ones past d_nope by zero weights, and stale bits there could be Inf or NaN
-        float v[kPer];
+        // ones past d_nope by zero weights, and stale bits there could be Inf or NaN.
+        // Four positions per load; a pending q_b output is summed for all of the
+        // thread's positions in one round trip.
+        float4 v[kPer4];
+        {
+            PendTile tl[kPer4];
+            int mr[kPer4], rr[kPer4];
+            bool live[kPer4];
 #pragma unroll
-        for (int k = 0; k < kPer; ++k) {
-            const int idx = threadIdx.x + k * kQAbs2Threads, mm = idx / LD, pos = idx % LD, m = m0 + mm;
-            const int d = pos < d_nope ? pos : (pos >= 2 * MAXDH && pos < 2 * MAXDH + d_rope ? d_nope + pos - 2 * MAXDH : -1);
-            v[k] = 0.f;
-            if (m < M && d >= 0) {
+            for (int k = 0; k < kPer4; ++k) {
+                const int idx = threadIdx.x + k * kQAbs2Threads, mm = idx / (LD / 4), pos = 4 * (idx % (LD / 4));
+                const int m = m0 + mm;
+                const int d = pos < d_nope ? pos
+                                           : (pos >= 2 * MAXDH && pos < 2 * MAXDH + d_rope ? d_nope + pos - 2 * MAXDH : -1);
+                live[k] = m < M && d >= 0;
+                const int n = h * qhd + (live[k] ? d : 0);
+                mr[k] = live[k] ? m : 0;
+                rr[k] = n & 127;
+                v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (!pend.part) {
-                    v[k] = q[((size_t)m * n_h + h) * qhd + d];
+                    if (live[k]) v[k] = __ldg((const float4 *)(q + ((size_t)m * n_h + h) * qhd + d));
                 } else {
-                    const int n = h * qhd + d;
-                    v[k] = pending_sum1(pend, s_tiles[(n >> 7) - qt0], m, n & 127);
+                    tl[k] = s_tiles[(n >> 7) - qt0];
                 }
             }
+            if (pend.part) pending_sum4_multi<kPer4, 4>(pend, tl, mr, rr, live, v);
         }
 #pragma unroll
-        for (int k = 0; k < kPer; ++k) {
+        for (int k = 0; k < kPer4; ++k) {
             const int idx = threadIdx.x + k * kQAbs2Threads;
-            sq[idx / LD][idx % LD] = v[k];
+            *(float4 *)&sq[idx / (LD / 4)][4 * (idx % (LD / 4))] = v[k];
         }
         __syncthreads();
         if (rope_here) {
@@ -1248,7 +1260,8 @@ cudaError_t launch_q_absorb(const float *q, int M, int n_h, int d_nope, int d_ro
     GemmPending pd;
     memset(&pd, 0, sizeof(pd));
     if (pend) pd = *pend;
-    if (d_nope <= 128 && d_nope % 8 == 0 && d_rope <= kQAbs2MaxRope && d_rope / 2 * kQAbsRows <= kQAbs2Threads)
+    if (d_nope <= 128 && d_nope % 8 == 0 && d_rope % 4 == 0 && d_rope <= kQAbs2MaxRope &&
+        d_rope / 2 * kQAbsRows <= kQAbs2Threads)
         return launch_pdl(q_absorb2_kernel<64>, dim3(n_h, (kv_lora + kQAbs2Cols - 1) / kQAbs2Cols),
                           dim3(kQAbs2Threads), 0, st, q, M, n_h, d_nope, d_rope, kv_lora, d_v, w_kvb, ctx_len, block,
                           max_ctx, rt, qt, pd);
