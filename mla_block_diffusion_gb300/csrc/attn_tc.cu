@@ -21,9 +21,10 @@
 // result is the same: O and the row sum carry the same reference).
 //
 // The Q tile (128 rows x DQK) arrives by TMA in the space of KV stages 1 and 2
-// (the first chunk is prefetched into stage 0 before the dependency wait, the
-// next two pages into L2); the softmax warps move it from shared to tensor
-// memory, after which the two stages take KV chunks again.
+// (the first chunk goes to stage 0); the softmax warps move it from shared to
+// tensor memory, after which the two stages take KV chunks again. A stage's
+// boxes outside the CTA's value columns are refilled as soon as the scores
+// that read them are done, the value boxes once P V has read them.
 //
 // Roles (6 warps): warp 0 TMA producer; warp 1 MMA issuer and tensor-memory
 // owner; warps 2-5 move Q, run the softmax (one thread per row) and write the
@@ -35,6 +36,7 @@ namespace ds {
 constexpr int kTcRows = 128;     // query rows per CTA (tcgen05 M)
 constexpr int kTcKeys = 64;      // keys per chunk (one page)
 constexpr int kTcStages = 3;     // KV chunk stages in shared memory
+constexpr int kTcPgAhead = 8;    // page numbers the producer reads ahead of their chunks
 constexpr float kTcRescaleLog2 = 8.f;
 
 template <int DQK, int DV>
@@ -62,7 +64,6 @@ bool attention_tc_supported(int dqk, int dv) { return dqk == 576 && dv == 512; }
 
 struct TcAttnParams {
     const __nv_bfloat16 *qt;      // [bs, R, DQK]
-    const __nv_bfloat16 *pool;    // [n_pages, 64, DQK] (L2 prefetch of the first pages)
     int R;                        // rows per sequence
     int n_pages;
     const int32_t *page_table;    // [bs, max_pages]
@@ -122,9 +123,11 @@ __global__ void __launch_bounds__(192, 2)
     uint64_t *kv_full = bars, *kv_empty = bars + kTcStages;
     uint64_t *s_full = bars + 2 * kTcStages, *s_free = s_full + 1, *p_ready = s_full + 2, *pv_done = s_full + 3;
     uint64_t *q_ready = s_full + 4, *mma_done = s_full + 5, *q_full = s_full + 6;
+    uint64_t *kv_kfree = s_full + 7;  // [kTcStages]: a stage's score-only boxes are free
     uint8_t *sQ = smem + C::kTileBytes;  // KV stages 1.. until the Q tile is in tensor memory
     __shared__ uint32_t s_tmem;
     __shared__ volatile int s_abort;
+    __shared__ int s_pg[kTcPgAhead];  // page ring of the producer
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tile = blockIdx.x / C::kParts, part = blockIdx.x % C::kParts;
@@ -136,6 +139,7 @@ __global__ void __launch_bounds__(192, 2)
         for (int i = 0; i < kTcStages; ++i) {
             mbar_init(&kv_full[i], 1);
             mbar_init(&kv_empty[i], 1);
+            mbar_init(&kv_kfree[i], 1);
         }
         mbar_init(s_full, 1);
         mbar_init(s_free, 4);
@@ -178,56 +182,80 @@ __global__ void __launch_bounds__(192, 2)
     if (warp != 0 || lane != 0) pdl_wait();
     if (warp == 0) {
         if (lane == 0) {
-            // KV chunk c of this split into stage st
-            auto load_chunk = [&](int i) {
+            // Boxes of KV chunk i into stage i % kTcStages: the value boxes of this
+            // CTA's output part (vals) or all the others. Every chunk's expected
+            // bytes are set with its first boxes.
+            constexpr int kVb = C::kDVP / 64;  // value boxes of the part
+            const int vb0 = part * kVb;
+            auto load_boxes = [&](int i, int pg, bool vals) {
                 const int st = i % kTcStages;
-                const int c = c_begin + i;
-                mbar_arrive_expect_tx(&kv_full[st], (uint32_t)C::kTileBytes);
+                if (!vals) mbar_arrive_expect_tx(&kv_full[st], (uint32_t)C::kTileBytes);
                 uint8_t *dst = sKV + st * C::kTileBytes;
-                if (c < npages) {
-                    int pg = p.page_table[(size_t)b * p.max_pages + c];
-                    if (pg < 0 || pg >= p.n_pages) {
-                        set_error(p.err, DSPARK_ERR_OOB);
-                        pg = 0;
-                    }
 #pragma unroll 1
-                    for (int j = 0; j < C::kBoxes; ++j)
+                for (int j = 0; j < C::kBoxes; ++j) {
+                    if ((j >= vb0 && j < vb0 + kVb) != vals) continue;
+                    if (pg >= 0)
                         tma_load_2d(dst + j * C::kBoxBytes, &tmPool, j * 64, pg * kTcKeys, &kv_full[st]);
-                } else {
-#pragma unroll 1
-                    for (int j = 0; j < C::kBoxes; ++j)
+                    else
                         tma_load_2d(dst + j * C::kBoxBytes, &tmBlk, j * 64, b * p.block, &kv_full[st]);
                 }
             };
-            // before the dependency wait: the first chunk when it is a page of the pool
-            // (an input of the step), and the next two pages into L2
-            if (nch > 0 && c_begin < npages) {
-                load_chunk(0);
-                issued = 1;
-            }
-            for (int i = 1; i < kTcStages && i < nch && c_begin + i < npages; ++i) {
-                const int pg = p.page_table[(size_t)b * p.max_pages + c_begin + i];
-                if (pg >= 0 && pg < p.n_pages)
-                    prefetch_l2_bulk(p.pool + (size_t)pg * kTcKeys * DQK, (uint32_t)C::kTileBytes);
-            }
+            // The first kTcPgAhead page numbers (inputs of the step) are requested in one
+            // round of loads before the dependency wait; the Q tile goes first after it,
+            // then chunk 0. A ring of page numbers keeps the loop free of waits on
+            // page-table loads. (No bulk L2 prefetch of pages: it occupies the same copy
+            // engine as the chunk loads and delays them.)
+            int raw[kTcPgAhead];
+#pragma unroll
+            for (int i = 0; i < kTcPgAhead; ++i)
+                raw[i] = (i < nch && c_begin + i < npages) ? __ldg(p.page_table + (size_t)b * p.max_pages + c_begin + i) : 0;
             pdl_wait();
             mbar_arrive_expect_tx(q_full, (uint32_t)C::kQBytes);
 #pragma unroll 1
             for (int j = 0; j < C::kBoxes; ++j) tma_load_3d(sQ + j * C::kQBoxBytes, &tmQ, j * 64, r0, b, q_full);
             q_issued = true;
-            if (issued == 0 && nch > 0) {
-                load_chunk(0);
+#pragma unroll
+            for (int i = 0; i < kTcPgAhead; ++i) {
+                const bool is_page = i < nch && c_begin + i < npages;
+                int pg = raw[i];
+                if (is_page && (pg < 0 || pg >= p.n_pages)) {
+                    set_error(p.err, DSPARK_ERR_OOB);
+                    pg = 0;
+                }
+                s_pg[i] = is_page ? pg : -1;
+            }
+            if (nch > 0) {
+                load_boxes(0, s_pg[0], false);
+                load_boxes(0, s_pg[0], true);
                 issued = 1;
             }
-            // stages 1.. hold the Q tile until the softmax warps have moved it
+            // Stages 1.. hold the Q tile until the softmax warps have moved it. A stage's
+            // boxes other than this part's values are free once the scores of the chunk
+            // before have been computed, the value boxes once its P V has been; a chunk
+            // whose first boxes are out always gets the rest, so it lands even after an abort.
             if (nch > 1 && mbar_wait_bounded(q_ready, 0, &s_abort)) {
                 for (int i = 1; i < nch; ++i) {
                     const int st = i % kTcStages;
-                    if (i >= kTcStages &&
-                        !mbar_wait_bounded(&kv_empty[st], (uint32_t)((i / kTcStages - 1) & 1), &s_abort))
-                        break;
-                    load_chunk(i);
+                    const uint32_t par = (uint32_t)((i / kTcStages - 1) & 1);
+                    if (i >= kTcStages && !mbar_wait_bounded(&kv_kfree[st], par, &s_abort)) break;
+                    const int pg = s_pg[i % kTcPgAhead];
+                    load_boxes(i, pg, false);
+                    if (i >= kTcStages) mbar_wait_bounded(&kv_empty[st], par, &s_abort);
+                    load_boxes(i, pg, true);
                     issued = i + 1;
+                    if (s_abort) break;
+                    if (i + kTcPgAhead < nch) {
+                        const int c = c_begin + i + kTcPgAhead;
+                        int pn = -1;
+                        if (c < npages) {
+                            pn = p.page_table[(size_t)b * p.max_pages + c];
+                            if (pn < 0 || pn >= p.n_pages) {
+                                set_error(p.err, DSPARK_ERR_OOB);
+                                pn = 0;
+                            }
+                        }
+                        s_pg[i % kTcPgAhead] = pn;
+                    }
                 }
             }
         }
@@ -252,6 +280,7 @@ __global__ void __launch_bounds__(192, 2)
                                     bd0 + (uint64_t)((kk >> 2) * (C::kBoxBytes >> 4) + 2 * (kk & 3)), idS,
                                     kk > 0 ? 1u : 0u);
                 mma_commit(s_full);
+                mma_commit(&kv_kfree[st]);
                 return true;
             };
             bool ok = nch == 0 || (mbar_wait_bounded(q_ready, 0, &s_abort) && issue_s(0));
@@ -395,21 +424,28 @@ __global__ void __launch_bounds__(192, 2)
             const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
             float *dst = p.splits == 1 ? p.o_lat + ((size_t)b * p.R + (rv ? r : 0)) * DV + part * C::kDVP
                                        : p.part_o + pr * DV + part * C::kDVP;
-#pragma unroll 1
-            for (int t = 0; t < C::kDVP / 16; ++t) {
-                float v[16];
+            // 64 columns per tensor-memory round trip
+#pragma unroll
+            for (int t = 0; t < C::kDVP / 64; ++t) {
+                uint32_t u[4][16];
                 if (done > 0) {
-                    tmem_ld16(tl + C::kOCol + 16 * t, v);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) tmem_ld16_nw(tl + C::kOCol + 64 * t + 16 * k, u[k]);
+                    tmem_ld_wait();
                 } else {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) v[j] = 0.f;
+                    for (int k = 0; k < 4; ++k)
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) u[k][j] = 0u;
                 }
                 if (rv) {
 #pragma unroll
-                    for (int j = 0; j < 16; j += 4) {
-                        float4 o = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+                    for (int j = 0; j < 64; j += 4) {
+                        float4 o = make_float4(__uint_as_float(u[j >> 4][j & 15]), __uint_as_float(u[j >> 4][(j & 15) + 1]),
+                                               __uint_as_float(u[j >> 4][(j & 15) + 2]),
+                                               __uint_as_float(u[j >> 4][(j & 15) + 3]));
                         if (p.splits == 1) o = make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
-                        *(float4 *)(dst + 16 * t + j) = o;
+                        *(float4 *)(dst + 64 * t + j) = o;
                     }
                 }
             }
@@ -463,7 +499,6 @@ cudaError_t launch_attention_tc(const CUtensorMap &pool_map, const CUtensorMap &
     TcAttnParams p;
     memset(&p, 0, sizeof(p));
     p.qt = a.qt;
-    p.pool = a.pool;
     p.R = a.R;
     p.n_pages = a.n_pages;
     p.page_table = a.page_table;
