@@ -406,7 +406,6 @@ __global__ void __launch_bounds__(kRowClThreads) latent_cluster_kernel(
 // registers; the rows sweep in chunks of 8 from shared memory and the four
 // quarter sums are added in quarter order.
 // ---------------------------------------------------------------------------
-constexpr int kAbsorbRows = 16;
 constexpr int kQAbsRows = 8;
 constexpr int kQAbsTiles = 4;  // channel tiles of one head's q (d_nope + d_rope <= 384)
 constexpr int kQAbsCols = 64;
@@ -657,20 +656,22 @@ __global__ void __launch_bounds__(kQAbs2Threads, 1) q_absorb2_kernel(
 // kv_b in) into shared memory with asynchronous copies issued before the
 // dependency wait, rows padded by 16 bytes (the rows a warp reads at once fall
 // in different banks); forms its rows of o_lat from the attention's split
-// partials (weights 2^(m_s - M) / sum_s 2^(m_s - M) l_s over the non-empty
-// splits, in split order; o_lat is read as is when there is one split), every
-// split's load in flight at once; then thread t forms the dot products of
-// channel t % 128 over the quarter t / 128 of the latent for the 4 rows, and
-// the quarters are added in order through shared memory.
+// partials (sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s over the non-empty
+// splits, in split order; o_lat is read as is when there is one split), each
+// thread loading its row's (m_s, l_s) with its partials in one round trip;
+// then thread t forms the dot products of the channel pair (t % 64, 64 + t % 64)
+// over the eighth t / 64 of the latent for the 4 rows, and the eighths are
+// added in order through shared memory.
 // ---------------------------------------------------------------------------
 constexpr int kCVRows = 4;
 constexpr int kCVThreads = 512;
 constexpr int kCVMaxSplit = 16;
-constexpr int kCVChan = kCVThreads / 4;  // channels per pass
-
 DS_DEVINL void cp_async16(void *smem_dst, const void *gmem_src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
 }
+
+constexpr int kCVPairs = 64;                     // channel pairs per pass
+constexpr int kCVParts = kCVThreads / kCVPairs;  // latent parts (8)
 
 __global__ void __launch_bounds__(kCVThreads) attn_combine_vabsorb_kernel(
     const float *__restrict__ part_o, const float *__restrict__ part_ml, int splits, int R,
@@ -681,60 +682,53 @@ __global__ void __launch_bounds__(kCVThreads) attn_combine_vabsorb_kernel(
     const int wstride = kv_lora * 2 + 16;                              // bytes per staged v_b row
     uint8_t *sw = smc;                                                 // [d_v][wstride]
     float *so = (float *)(smc + (size_t)d_v * wstride);                // [kCVRows][kv_lora]
-    float *swt = so + kCVRows * kv_lora;                               // [kCVRows][kCVMaxSplit]
-    float *sred = swt + kCVRows * kCVMaxSplit;                         // [4 quarters][kCVRows][kCVChan]
+    float *sred = so + kCVRows * kv_lora;                              // [kCVParts][kCVRows][2 kCVPairs]
     const int h = blockIdx.x, m0 = blockIdx.y * kCVRows;
     const int mr = min(kCVRows, M - m0);
-    const int c8n = kv_lora / 8, c4n = kv_lora / 4;
+    const int c4n = kv_lora / 4;
     // the head's v_b rows: weights of the step, copied before the dependency wait
+    const int c8n = kv_lora / 8;
     const uint4 *W4 = (const uint4 *)(w_kvb + ((size_t)h * (d_nope + d_v) + d_nope) * kv_lora);
     for (int i = threadIdx.x; i < d_v * c8n; i += blockDim.x)
         cp_async16(sw + (size_t)(i / c8n) * wstride + (i % c8n) * 16, W4 + i);
     asm volatile("cp.async.commit_group;" ::: "memory");
     pdl_wait();
     if (splits > 1) {
-        if ((int)threadIdx.x < mr) {
-            const int m = m0 + threadIdx.x, b = m / block, r = (m % block) * n_h + h;
-            const float *ml = part_ml + ((size_t)b * splits * R + r) * 2;
-            float2 v[kCVMaxSplit];
-#pragma unroll
-            for (int s = 0; s < kCVMaxSplit; ++s)
-                v[s] = s < splits ? __ldcg((const float2 *)(ml + (size_t)s * R * 2)) : make_float2(0.f, 0.f);
-            float mx = -INFINITY;
-#pragma unroll
-            for (int s = 0; s < kCVMaxSplit; ++s)
-                if (s < splits && v[s].y > 0.f) mx = fmaxf(mx, v[s].x);
-            float den = 0.f;
-#pragma unroll
-            for (int s = 0; s < kCVMaxSplit; ++s)
-                if (s < splits && v[s].y > 0.f) den += exp2f(v[s].x - mx) * v[s].y;
-            const float inv = den > 0.f ? 1.f / den : 0.f;
-#pragma unroll
-            for (int s = 0; s < kCVMaxSplit; ++s)
-                swt[threadIdx.x * kCVMaxSplit + s] = (s < splits && v[s].y > 0.f) ? exp2f(v[s].x - mx) * inv : 0.f;
-        }
-        __syncthreads();
+        // each thread loads its row's (max, sum) pairs with its partials (one round
+        // trip) and forms the weights itself
         for (int i = threadIdx.x; i < kCVRows * c4n; i += blockDim.x) {
             const int mm = i / c4n, c4 = i % c4n;
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
             if (mm < mr) {
                 const int m = m0 + mm, b = m / block, r = (m % block) * n_h + h;
+                const float *ml = part_ml + ((size_t)b * splits * R + r) * 2;
                 const float4 *src = (const float4 *)(part_o + ((size_t)b * splits * R + r) * kv_lora) + c4;
                 const size_t sstep = (size_t)R * kv_lora / 4;
+                float2 w[kCVMaxSplit];
                 float4 v[kCVMaxSplit];
 #pragma unroll
-                for (int s = 0; s < kCVMaxSplit; ++s)
+                for (int s = 0; s < kCVMaxSplit; ++s) {
+                    w[s] = s < splits ? __ldcg((const float2 *)(ml + (size_t)s * R * 2)) : make_float2(0.f, 0.f);
                     v[s] = s < splits ? __ldcg(src + s * sstep) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+                float mx = -INFINITY;
+#pragma unroll
+                for (int s = 0; s < kCVMaxSplit; ++s)
+                    if (s < splits && w[s].y > 0.f) mx = fmaxf(mx, w[s].x);
+                float den = 0.f;
 #pragma unroll
                 for (int s = 0; s < kCVMaxSplit; ++s) {
-                    if (s < splits) {
-                        const float w = swt[mm * kCVMaxSplit + s];
-                        acc.x += w * v[s].x;
-                        acc.y += w * v[s].y;
-                        acc.z += w * v[s].z;
-                        acc.w += w * v[s].w;
+                    if (s < splits && w[s].y > 0.f) {
+                        const float e = exp2f(w[s].x - mx);
+                        den += e * w[s].y;
+                        acc.x += e * v[s].x;
+                        acc.y += e * v[s].y;
+                        acc.z += e * v[s].z;
+                        acc.w += e * v[s].w;
                     }
                 }
+                const float inv = den > 0.f ? 1.f / den : 0.f;
+                acc = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
             }
             ((float4 *)so)[mm * c4n + c4] = acc;
         }
@@ -747,48 +741,57 @@ __global__ void __launch_bounds__(kCVThreads) attn_combine_vabsorb_kernel(
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
-    // v absorption: channel e = e0 + t % 128, latent quarter q = t / 128
-    const int q = threadIdx.x / kCVChan, cq = kv_lora / 4;
-    for (int e0 = 0; e0 < d_v; e0 += kCVChan) {
-        const int e = e0 + (int)(threadIdx.x % kCVChan);
-        float a[kCVRows] = {0.f, 0.f, 0.f, 0.f};
-        if (e < d_v) {
-            const uint8_t *wr = sw + (size_t)e * wstride + q * cq * 2;
-            const float *orow = so + q * cq;
-            for (int c = 0; c < cq; c += 8) {
-                const uint4 wq = *(const uint4 *)(wr + c * 2);
-                const uint32_t wu[4] = {wq.x, wq.y, wq.z, wq.w};
-                float wf[8];
+    // v absorption: thread t takes the channel pair (e0 + t % 64, e0 + 64 + t % 64)
+    // over the latent eighth t / 64 for the 4 rows (one read of a row of o serves
+    // both channels); the eighths are added in order through shared memory
+    const int part = threadIdx.x / kCVPairs, pr = threadIdx.x % kCVPairs, cp = kv_lora / kCVParts;
+    for (int e0 = 0; e0 < d_v; e0 += 2 * kCVPairs) {
+        const int ea = e0 + pr, eb = e0 + kCVPairs + pr;
+        float a[2][kCVRows];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&wu[j]));
-                    wf[2 * j] = f.x;
-                    wf[2 * j + 1] = f.y;
+        for (int mm = 0; mm < kCVRows; ++mm) a[0][mm] = a[1][mm] = 0.f;
+        if (ea < d_v) {
+            const bool hb = eb < d_v;
+            const uint8_t *wa = sw + (size_t)ea * wstride + part * cp * 2;
+            const uint8_t *wb = sw + (size_t)(hb ? eb : ea) * wstride + part * cp * 2;
+            const float *orow = so + part * cp;
+            for (int c = 0; c < cp; c += 8) {
+                float wf[2][8];
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const uint4 wq = *(const uint4 *)((k ? wb : wa) + c * 2);
+                    const uint32_t wu[4] = {wq.x, wq.y, wq.z, wq.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&wu[j]));
+                        wf[k][2 * j] = f.x;
+                        wf[k][2 * j + 1] = f.y;
+                    }
                 }
 #pragma unroll
                 for (int mm = 0; mm < kCVRows; ++mm) {
                     const float4 x0 = *(const float4 *)(orow + mm * kv_lora + c);
                     const float4 x1 = *(const float4 *)(orow + mm * kv_lora + c + 4);
-                    a[mm] = fmaf(wf[0], x0.x, a[mm]);
-                    a[mm] = fmaf(wf[1], x0.y, a[mm]);
-                    a[mm] = fmaf(wf[2], x0.z, a[mm]);
-                    a[mm] = fmaf(wf[3], x0.w, a[mm]);
-                    a[mm] = fmaf(wf[4], x1.x, a[mm]);
-                    a[mm] = fmaf(wf[5], x1.y, a[mm]);
-                    a[mm] = fmaf(wf[6], x1.z, a[mm]);
-                    a[mm] = fmaf(wf[7], x1.w, a[mm]);
+                    const float x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+                    for (int k = 0; k < 2; ++k)
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) a[k][mm] = fmaf(wf[k][j], x[j], a[k][mm]);
                 }
             }
         }
 #pragma unroll
-        for (int mm = 0; mm < kCVRows; ++mm) sred[(q * kCVRows + mm) * kCVChan + threadIdx.x % kCVChan] = a[mm];
+        for (int mm = 0; mm < kCVRows; ++mm) {
+            sred[(part * kCVRows + mm) * (2 * kCVPairs) + pr] = a[0][mm];
+            sred[(part * kCVRows + mm) * (2 * kCVPairs) + kCVPairs + pr] = a[1][mm];
+        }
         __syncthreads();
-        if ((int)threadIdx.x < kCVRows * kCVChan) {
-            const int mm = threadIdx.x / kCVChan, ee = threadIdx.x % kCVChan, e2 = e0 + ee;
+        if ((int)threadIdx.x < kCVRows * 2 * kCVPairs) {
+            const int mm = threadIdx.x / (2 * kCVPairs), ee = threadIdx.x % (2 * kCVPairs), e2 = e0 + ee;
             if (mm < mr && e2 < d_v) {
                 float t = 0.f;
 #pragma unroll
-                for (int qq = 0; qq < 4; ++qq) t += sred[(qq * kCVRows + mm) * kCVChan + ee];
+                for (int pp = 0; pp < kCVParts; ++pp) t += sred[(pp * kCVRows + mm) * (2 * kCVPairs) + ee];
                 out[(size_t)(m0 + mm) * n_h * d_v + (size_t)h * d_v + e2] = __float2bfloat16(t);
             }
         }
@@ -1348,12 +1351,11 @@ cudaError_t launch_attention(const AttnParams &p, int bs, int dqk, int dv, cudaS
 
 // Shared memory of the fused combine + v absorption.
 static size_t cvabs_smem(int d_v, int kv_lora) {
-    return (size_t)d_v * (kv_lora * 2 + 16) + (size_t)kCVRows * kv_lora * 4 + (size_t)kCVRows * kCVMaxSplit * 4 +
-           (size_t)4 * kCVRows * kCVChan * 4;
+    return (size_t)d_v * (kv_lora * 2 + 16) + (size_t)kCVRows * kv_lora * 4 + (size_t)kCVParts * kCVRows * 2 * kCVPairs * 4;
 }
 
 bool attn_combine_vabsorb_fits(int d_v, int kv_lora, int splits) {
-    return kv_lora % 16 == 0 && splits <= kCVMaxSplit && cvabs_smem(d_v, kv_lora) <= 227u * 1024u;
+    return kv_lora % (8 * kCVParts) == 0 && splits <= kCVMaxSplit && cvabs_smem(d_v, kv_lora) <= 227u * 1024u;
 }
 
 cudaError_t launch_attn_combine_vabsorb(const AttnParams &p, int M, int n_h, int d_nope, int d_v, int kv_lora,
