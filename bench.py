@@ -428,7 +428,7 @@ def main():
         h = hashlib.sha256(open(os.path.join(ROOT, "mla_block_diffusion_gb300", "csrc", "gemm.cuh"), "rb").read())
         if td.get("gemm_cuh_sha256") == h.hexdigest():
             traffic = td.get("dram_bytes_per_launch")
-    gpu_launches_per_step = 1 + G.n_layers * (11 + (1 if ds_layout_splits(ds) > 1 else 0)) + 2 + 1 + 1 + 2
+    gpu_launches_per_step = ds_launches_per_step(ds)
     us = ms * 1e3 / world  # whole job: one block per rank per step
     line = {
         "metric": METRIC, "value": us, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -866,6 +866,31 @@ def only_verify(args, G, local):
         assert ds.check() == 0
         res[name] = {"median_call_ms": statistics.median(times), "accept_len_last": int(acc.item())}
     print(json.dumps({"only": "verify", "vocab": g.vocab, "block": g.block, "modes": res}))
+
+
+def ds_launches_per_step(ds) -> int:
+    """Kernels one greedy draft-and-verify step launches (mirrors the library's choices).
+
+    fc; per layer RMSNorm, q_a||kv_a, latent norms, q_b, q absorption, attention,
+    split combine + v absorption (one fused kernel on the tensor-core path; two
+    kernels otherwise when the KV sequence is split), o_proj, RMSNorm, gate/up,
+    down; then the final RMSNorm, lm_head, rollout, confidence and the two verify
+    kernels.
+    """
+    G = ds.G
+    R = G.block * G.n_heads
+    if G.kv_lora + G.d_rope == 576 and G.kv_lora == 512:  # tensor-core attention
+        sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+        tiles, parts = -(-R // 128), G.kv_lora // 128
+        chunks = -(-ds.max_ctx // 64) + 1
+        s = max(1, min(sms // (tiles * parts * ds.max_bs), chunks, 64))
+        cps = -(-chunks // s)
+        splits = -(-chunks // cps)
+        fused = G.kv_lora % 64 == 0 and splits <= 16
+        per_layer = 11 + (1 if splits > 1 and not fused else 0)
+    else:
+        per_layer = 11 + (1 if ds_layout_splits(ds) > 1 else 0)
+    return 1 + G.n_layers * per_layer + 2 + 1 + 1 + 2
 
 
 def ds_layout_splits(ds) -> int:
