@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(GemmQCfg<BN, FMT>::kThreads, 1)
             mbar_init(&raw_empty[s], 1);
         }
         for (int s = 0; s < CS; ++s) {
-            mbar_init(&cvt_full[s], kQConvThreads / 2);
+            mbar_init(&cvt_full[s], kQConvThreads / 2 / 32);  // one arrival per converter warp
             mbar_init(&cvt_empty[s], 1);
         }
         for (int a = 0; a < 2; ++a) {
@@ -359,7 +359,8 @@ __global__ void __launch_bounds__(GemmQCfg<BN, FMT>::kThreads, 1)
         const int gthr = threadIdx.x - 192 - 128 * g;
         const long long total_sub = (u1 - u0) * NS;
         // software pipeline: the tensor-memory store of one sub-block completes (and is
-        // announced on cvt_full) while the next one is decoded
+        // announced on cvt_full, once per warp: 128 arrivals on one barrier serialise)
+        // while the next one is decoded
         int pend = -1;
         for (long long cit = g; cit < total_sub; cit += 2) {
             const long long it = cit / NS;
@@ -378,7 +379,8 @@ __global__ void __launch_bounds__(GemmQCfg<BN, FMT>::kThreads, 1)
             if (pend >= 0) {
                 tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(&cvt_full[pend]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&cvt_full[pend]);
             }
             tc_fence_after();
             tmem_st32(tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)(C::kACol0 + 32 * t), v);
@@ -387,7 +389,8 @@ __global__ void __launch_bounds__(GemmQCfg<BN, FMT>::kThreads, 1)
         if (pend >= 0) {
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(&cvt_full[pend]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&cvt_full[pend]);
         }
     } else {
         pdl_wait();
