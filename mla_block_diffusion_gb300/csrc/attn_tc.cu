@@ -77,7 +77,6 @@ struct TcAttnParams {
     float *part_o;                // [bs, splits, R, DV]
     float *part_ml;               // [bs, splits, R, 2]
     int *err;
-    L2Prefetch pf;                // pulled into L2 by the MMA thread before its dependency wait
 };
 
 // 16 columns of the warp's lane quadrant without the completion wait (several
@@ -176,9 +175,6 @@ __global__ void __launch_bounds__(192, 2)
     int issued = 0;
     bool q_issued = false;
 
-    if (threadIdx.x == 32)
-        l2_prefetch_share(p.pf, blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z),
-                          gridDim.x * gridDim.y * gridDim.z);
     if (warp != 0 || lane != 0) pdl_wait();
     if (warp == 0) {
         if (lane == 0) {
@@ -513,7 +509,6 @@ cudaError_t launch_attention_tc(const CUtensorMap &pool_map, const CUtensorMap &
     p.part_o = a.part_o;
     p.part_ml = a.part_ml;
     p.err = a.err;
-    p.pf = a.pf;
     const int tiles = (a.R + kTcRows - 1) / kTcRows;
     dim3 grid(tiles * C::kParts, a.splits, bs);
     cudaError_t e = launch_pdl(mla_attention_tc_kernel<576, 512>, grid, dim3(192), (size_t)C::kSmem, st, pool_map,

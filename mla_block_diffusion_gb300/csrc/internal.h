@@ -27,7 +27,6 @@ struct AttnParams {
     float *part_o;                  // [bs, splits, R, DV]
     float *part_ml;                 // [bs, splits, R, 2]
     int *err;
-    L2Prefetch pf;                  // weights of the next GEMM, pulled into L2 meanwhile
 };
 
 cudaError_t launch_rmsnorm(const float *x, int ldx, const float *g, int H, float eps, __nv_bfloat16 *y, int ldy,
