@@ -184,3 +184,142 @@ def test_gather_cache_follows_page_table():
     assert out.tolist() == [pool[2, 0].tolist(), pool[2, 1].tolist(), pool[2, 2].tolist(),
                             pool[0, 0].tolist(), pool[0, 1].tolist(), pool[0, 2].tolist(), pool[3, 0].tolist()]
     assert N.gather_cache(pool, np.array([1]), 0).shape == (0, 2)
+
+
+def _uniform_err():
+    """Relative error of the oracle layer against its closed form when every query is zero."""
+    G = TINY
+    rng = np.random.default_rng(11)
+    L = dict(_rand_layer(rng, G, std=0.1))
+    L["w_q_b"] = np.zeros_like(L["w_q_b"])
+    x = rng.standard_normal((7, G.hidden))
+    ctx = 23
+    cache = rng.standard_normal((ctx, G.kv_dim))
+    got = N.layer(x, L, G, cache[:, :G.kv_lora], cache[:, G.kv_lora:], np.arange(7) + float(ctx))
+    h = x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + G.eps)
+    kv = (h @ L["w_qkv_a"].T)[:, G.q_lora:G.q_lora + G.kv_lora]
+    c_blk = kv / np.sqrt(np.mean(kv * kv, axis=-1, keepdims=True) + G.eps)
+    mean_c = (cache[:, :G.kv_lora].sum(axis=0) + c_blk.sum(axis=0)) / (ctx + 7)
+    per = G.d_nope + G.d_v
+    o = np.concatenate([L["w_kv_b"][hh * per + G.d_nope:(hh + 1) * per] @ mean_c for hh in range(G.n_heads)])
+    x1 = x + (L["w_o"] @ o)[None, :]
+    h2 = x1 / np.sqrt(np.mean(x1 * x1, axis=-1, keepdims=True) + G.eps)
+    g = h2 @ L["w_gate"].T
+    want = x1 + ((g / (1 + np.exp(-g))) * (h2 @ L["w_up"].T)) @ L["w_down"].T
+    return np.max(np.abs(got - want)) / np.max(np.abs(want))
+
+
+def test_layer_with_zero_queries_attends_uniformly_to_cache_and_block():
+    """q = 0 makes every score 0, so each query row's attention is the plain mean of the
+    latents of all ctx cache rows and all 7 block rows (non-causal: every row sees the
+    whole block), absorbed by each head's v_b (rows d_nope.. of the head's kv_b block),
+    concatenated head by head into o_proj. The planted mistakes below (a causal mask, a
+    dropped block, swapped k_b / v_b halves, a reversed head order) each break it."""
+    assert _uniform_err() < 1e-12
+
+
+def test_layer_is_invariant_to_a_consistent_head_permutation():
+    """Renumbering the heads in q_b (row blocks), kv_b (row blocks) and o_proj (column
+    blocks) together leaves the layer unchanged; renumbering only q_b does not (each
+    head's queries must meet its own k_b / v_b and o_proj columns)."""
+    G = TINY
+    rng = np.random.default_rng(12)
+    L = _rand_layer(rng, G, std=0.1)
+    x = rng.standard_normal((7, G.hidden))
+    cache = rng.standard_normal((19, G.kv_dim))
+    pos = np.arange(7) + 19.0
+    base = N.layer(x, L, G, cache[:, :G.kv_lora], cache[:, G.kv_lora:], pos)
+    perm = rng.permutation(G.n_heads)
+    assert not np.array_equal(perm, np.arange(G.n_heads))
+
+    def rows(w, per):
+        return np.concatenate([w[p * per:(p + 1) * per] for p in perm])
+
+    qhd, kvh = G.d_nope + G.d_rope, G.d_nope + G.d_v
+    w_o = np.concatenate([L["w_o"][:, p * G.d_v:(p + 1) * G.d_v] for p in perm], axis=1)
+    P = dict(L, w_q_b=rows(L["w_q_b"], qhd), w_kv_b=rows(L["w_kv_b"], kvh), w_o=w_o)
+    out = N.layer(x, P, G, cache[:, :G.kv_lora], cache[:, G.kv_lora:], pos)
+    assert np.max(np.abs(out - base)) < 1e-12 * np.max(np.abs(base))
+    Q = dict(L, w_q_b=rows(L["w_q_b"], qhd))
+    assert np.max(np.abs(N.layer(x, Q, G, cache[:, :G.kv_lora], cache[:, G.kv_lora:], pos) - base)) > 1e-6
+
+
+def test_planted_mistakes_fail_the_composition_pin(monkeypatch):
+    """Mistakes planted in the oracle (on the CPU) each break the zero-query pin."""
+    assert _uniform_err() < 1e-12
+    real_attn, real_split = N.mla_attention, N.split_kv_b
+
+    def drop_block(q_nope, q_rope, c_kv, k_r, w_kb, w_vb, scale, absorbed=True):
+        T = q_nope.shape[0]  # attends to the cache only
+        return real_attn(q_nope, q_rope, c_kv[:-T], k_r[:-T], w_kb, w_vb, scale, absorbed)
+
+    def causal(q_nope, q_rope, c_kv, k_r, w_kb, w_vb, scale, absorbed=True):
+        T, J = q_nope.shape[0], c_kv.shape[0]  # block row t sees the cache and block rows <= t
+        return np.stack([real_attn(q_nope[t:t + 1], q_rope[t:t + 1], c_kv[:J - T + t + 1], k_r[:J - T + t + 1],
+                                   w_kb, w_vb, scale, absorbed)[0] for t in range(T)])
+
+    def heads_reversed(*a, **k):
+        return real_attn(*a, **k)[:, ::-1, :]
+
+    def kb_vb_swapped(w, n_heads, d_nope, d_v, kv_lora):
+        kb, vb = real_split(w, n_heads, d_nope, d_v, kv_lora)
+        return vb, kb
+
+    for name, fn in (("mla_attention", drop_block), ("mla_attention", causal),
+                     ("mla_attention", heads_reversed), ("split_kv_b", kb_vb_swapped)):
+        with monkeypatch.context() as m:
+            m.setattr(N, name, fn)
+            assert _uniform_err() > 1e-6, fn.__name__
+
+
+def _shift_err(cache_of=None):
+    """Largest difference between the draft block and the same step with every position
+    shifted by 1000 (cache keys roped at j + 1000, block row i at ctx + i + 1000)."""
+    G = TINY
+    rng = np.random.default_rng(13)
+    layers = [_rand_layer(rng, G, std=0.1) for _ in range(G.n_layers)]
+    x = rng.standard_normal((7, G.hidden))
+    ctx, shift = 17, 1000.0
+    inv = N.rope_inv_freq(G.d_rope, G.rope_theta)
+    lat = [rng.standard_normal((ctx, G.kv_lora)) for _ in range(G.n_layers)]
+    raw = [rng.standard_normal((ctx, G.d_rope)) for _ in range(G.n_layers)]
+    caches = [np.concatenate([lat[l], N.apply_rope(raw[l], np.arange(ctx, dtype=np.float64), inv)], axis=1)
+              for l in range(G.n_layers)]
+    if cache_of is not None:
+        caches = [caches[cache_of(l)] for l in range(G.n_layers)]
+    w_lm = rng.standard_normal((G.vocab, G.hidden)) * 0.02
+    h1, _ = N.draft_block(x, layers, np.ones(G.hidden), w_lm, G, caches, ctx)
+    x2 = x
+    for l, L in enumerate(layers):
+        kr = N.apply_rope(raw[l], np.arange(ctx, dtype=np.float64) + shift, inv)
+        x2 = N.layer(x2, L, G, lat[l], kr, np.arange(7.0) + ctx + shift)
+    h2 = N.rmsnorm(x2, np.ones(G.hidden), G.eps)
+    return np.max(np.abs(h1 - h2))
+
+
+def test_positions_are_relative_and_the_block_follows_its_cache():
+    """RoPE makes scores depend on relative positions only. With no cache, shifting the
+    block's positions leaves a layer unchanged; with a cache whose keys were roped at
+    positions 0..ctx-1, the draft block (block row i at ctx + i, layer l reading cache l)
+    equals the same step with every position shifted by 1000. Placing the block at i
+    instead of ctx + i, or giving every layer the same cache, breaks it (planted below)."""
+    G = TINY
+    rng = np.random.default_rng(14)
+    L = _rand_layer(rng, G, std=0.1)
+    x = rng.standard_normal((7, G.hidden))
+    empty = np.zeros((0, G.kv_lora)), np.zeros((0, G.d_rope))
+    a = N.layer(x, L, G, *empty, np.arange(7.0))
+    b = N.layer(x, L, G, *empty, np.arange(7.0) + 1000.0)
+    assert np.max(np.abs(a - b)) < 1e-9 * np.max(np.abs(a))
+    assert _shift_err() < 1e-9
+    assert _shift_err(cache_of=lambda l: 0) > 1e-6  # every layer reading layer 0's cache
+
+
+def test_planted_position_mistake_fails_the_pin(monkeypatch):
+    real_layer = N.layer
+
+    def block_at_zero(x, L, geom, ckv, kr, positions, absorbed=True):
+        return real_layer(x, L, geom, ckv, kr, positions - positions[0], absorbed)
+
+    monkeypatch.setattr(N, "layer", block_at_zero)
+    assert _shift_err() > 1e-6
