@@ -198,3 +198,26 @@ def test_probabilistic_verify_uses_spec_uniforms():
         a2, out2 = S.verify_prob_core(P, ell, tokens, 0, 1.0, 0.95, U, Wr, Wb)
         assert a == a2 and np.array_equal(out, out2)
         assert 0 <= a <= B and np.all(out[a + 1:] == -1) and 0 <= out[a] < V
+
+
+def test_planted_role_swap_fails_the_enumeration(monkeypatch):
+    """A verify that swaps the target's and the draft's roles (accepting with q/p and
+    resampling from max(0, q - p)), planted on the CPU, no longer reproduces the
+    target's law under exact enumeration."""
+    real = S.verify_prob_core
+
+    def swapped(P, ell, tokens, draft_greedy, T, top_p, U, Wres, Wbonus):
+        B = ell.shape[0]
+        P2 = np.concatenate([ell, P[B:]], axis=0).astype(np.float32)
+        return real(P2, np.ascontiguousarray(P[:B]), tokens, draft_greedy, T, top_p, U, Wres, Wbonus)
+
+    monkeypatch.setattr(S, "verify_prob_core", swapped)
+    V, T, top_p = 3, 1.0, 1.0
+    rng = np.random.default_rng(21)
+    p1 = (rng.standard_normal(V) * 1.5).astype(np.float32)
+    p2 = (rng.standard_normal(V) * 1.5).astype(np.float32)
+    q1 = (rng.standard_normal(V) * 1.5).astype(np.float32)
+    first, _, _, _ = _enumerate(lambda t: np.stack([p1, p2]), lambda t: np.stack([q1]), [_dist(q1, T, top_p), {}],
+                                V, 1, T, top_p, 0)
+    target1 = _dist(p1, T, top_p)
+    assert max(abs(first[v] - target1[v]) for v in range(V)) > Fraction(1, 100)
