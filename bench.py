@@ -27,6 +27,14 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+# --oracle-threads N: the oracle's BLAS threads must be fixed before numpy loads
+for _i, _a in enumerate(sys.argv):
+    if _a.startswith("--oracle-threads"):
+        _n = _a.split("=", 1)[1] if "=" in _a else (sys.argv[_i + 1] if _i + 1 < len(sys.argv) else "0")
+        if _n.isdigit() and int(_n) > 0:
+            for _k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+                os.environ[_k] = _n
+
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
@@ -44,7 +52,7 @@ def peaks():
     return dict(FALLBACK), "fallback"
 
 
-def algorithmic_bytes(G, ctx: int, bs: int = 1, fmt: str = "bf16"):
+def algorithmic_bytes(G, ctx, bs: int = 1, fmt: str = "bf16"):
     """Bytes one step must move at least: every weight once (w2 once, the
     block's 7 rows of w1), fp32 gains and confidence head, the latent KV once,
     the aux states, z and ell written once and read once, the target logits.
@@ -57,10 +65,11 @@ def algorithmic_bytes(G, ctx: int, bs: int = 1, fmt: str = "bf16"):
     q_rows = G.hidden + G.n_layers * (G.n_heads * G.q_head_dim + G.hidden + 2 * G.inter + G.hidden)
     per = {"bf16": 2.0, "fp8": 1.0, "nvfp4": 0.5 + 1.0 / 16, "mxfp4": 0.5 + 1.0 / 32}[fmt]
     extra = {"bf16": 0, "fp8": 4 * q_rows, "nvfp4": 0, "mxfp4": 0}[fmt]
-    w_bf16 = 2 * (c["fc"] + G.n_layers * mats + c["lm_head"] + G.rank * G.vocab + G.block * G.rank) \
+    w_bf16 = 2 * (c["fc"] + G.n_layers * mats + c["lm_head"] + G.rank * G.vocab + bs * G.block * G.rank) \
         - int(2 * qn) + int(per * qn) + extra
     w_f32 = 4 * (G.n_layers * lp["norms"] + 2 * G.hidden)
-    kv = bs * G.n_layers * ctx * G.kv_dim * 2
+    ctx_total = sum(ctx) if isinstance(ctx, (list, tuple)) else bs * ctx
+    kv = G.n_layers * ctx_total * G.kv_dim * 2
     aux = bs * G.block * G.n_aux * G.hidden * 2
     logits = 4 * bs * G.vocab * (2 * G.block + 2 * G.block + (G.block + 1))
     total = w_bf16 + w_f32 + kv + aux + logits
@@ -149,49 +158,108 @@ def max_over_ranks(x: float, world: int) -> float:
 
 
 # ---------------------------------------------------------------------------
-# CPU oracle sample (baseline and reference arm)
+# CPU oracle (baseline and reference arm): one whole block, float64
 # ---------------------------------------------------------------------------
-def oracle_sample(w, W, I, lm_rows: int, rng_seed: int = 0):
-    """Time the float64 oracle on a bounded sample of one block: fc fusion, one
-    full layer, the lm_head on lm_rows vocabulary rows, the Markov rollout and
-    greedy verification on the full vocabulary; scale to a whole block."""
+LAYER_KEYS = ("attn_norm", "w_qkv_a", "q_a_norm", "kv_a_norm", "w_q_b", "w_kv_b", "w_o", "mlp_norm", "w_gate", "w_up",
+              "w_down")
+
+
+def _mem_available_bytes() -> int:
+    """Host memory this process may still use: MemAvailable, capped by a cgroup limit."""
+    avail = 0
+    try:
+        with open("/proc/meminfo") as f:
+            for ln in f:
+                if ln.startswith("MemAvailable:"):
+                    avail = int(ln.split()[1]) * 1024
+    except OSError:
+        pass
+    for cg in ("/sys/fs/cgroup/memory.max", "/sys/fs/cgroup/memory/memory.limit_in_bytes"):
+        try:
+            with open(cg) as f:
+                v = f.read().strip()
+            if v.isdigit():
+                avail = min(avail, int(v)) if avail else int(v)
+        except OSError:
+            pass
+    return avail
+
+
+class OracleWeights:
+    """float64 copies of the drafter's weights for the oracle (input preparation: the
+    bf16 -> float64 conversion is exact). Kept across blocks when the host has room
+    for them (about 8 bytes per parameter), else converted again at every use. The
+    conversion time is reported apart from the oracle's compute time."""
+
+    LM_CHUNK = 8192
+
+    def __init__(self, W, G):
+        self.W, self.G = W, G
+        need = 8 * sum(int(t.numel()) for t in W.values() if torch.is_tensor(t))
+        self.keep = _mem_available_bytes() > 3 * need
+        self.cache = {}
+        self.conv_s = 0.0
+
+    def get(self, name, lo=None, hi=None):
+        key = (name, lo, hi)
+        if key in self.cache:
+            return self.cache[key]
+        t0 = time.perf_counter()
+        t = self.W[name] if lo is None else self.W[name][lo:hi]
+        a = t.detach().to(torch.float64).cpu().numpy()
+        self.conv_s += time.perf_counter() - t0
+        if self.keep:
+            self.cache[key] = a
+        return a
+
+    def lm_chunks(self):
+        V = self.G.vocab
+        for lo in range(0, V, self.LM_CHUNK):
+            yield lo, self.get("w_lm", lo, min(V, lo + self.LM_CHUNK))
+
+
+def oracle_block(OW, G, I, b, draft_mode, verify_mode, T, top_p, P=None):
+    """One whole block of the float64 oracle for sequence b: fc fusion, every layer,
+    the final norm, the full lm_head, the Markov rollout, the confidence head and the
+    verification the workload uses (greedy, token-wise probabilistic or block).
+    Returns the seconds of oracle compute; weight conversions are not counted
+    (OW.conv_s holds them)."""
     from oracle import network as N
     from oracle import sampling as S
-    G = w.geom
-    ctx = I["ctx_list"][0]
+    ctx = I["ctx_list"][b]
+    conv0 = OW.conv_s
     f64 = lambda t: t.detach().to(torch.float64).cpu().numpy()
-    t_conv0 = time.perf_counter()
-    w_fc = f64(W["w_fc"])
-    aux = f64(I["aux"])[0]
-    keys = ["attn_norm", "w_qkv_a", "q_a_norm", "kv_a_norm", "w_q_b", "w_kv_b", "w_o", "mlp_norm", "w_gate", "w_up",
-            "w_down"]
-    L0 = {k: f64(W[f"l0.{k}"]) for k in keys}
-    table = I["page_table"][0].cpu().numpy()
-    cache = N.gather_cache(f64(I["kv_pools"][0]), table, ctx)
-    rows = np.random.default_rng(rng_seed).choice(G.vocab, lm_rows, replace=False)
-    w_lm = f64(W["w_lm"][torch.as_tensor(rows, device=W["w_lm"].device)])
-    w1, w2 = W["markov_w1"].cpu(), W["markov_w2"].cpu()
-    t_conv = time.perf_counter() - t_conv0
+    aux = f64(I["aux"][b])
+    table = I["page_table"][b]
+    pages = table[: (ctx + G.page_size - 1) // G.page_size].long()
+    caches = []
+    for l in range(G.n_layers):
+        pool = f64(I["kv_pools"][l][pages])
+        caches.append(N.gather_cache(pool, np.arange(pool.shape[0]), ctx))
+    w1, w2 = OW.W["markov_w1"].cpu(), OW.W["markov_w2"].cpu()
     t0 = time.perf_counter()
-    x = N.fuse_ctx(w_fc, aux)
-    t1 = time.perf_counter()
+    x = N.fuse_ctx(OW.get("w_fc"), aux)
     pos = np.arange(G.block, dtype=np.float64) + ctx
-    x1 = N.layer(x, L0, G, cache[:, :G.kv_lora], cache[:, G.kv_lora:], pos)
-    t2 = time.perf_counter()
-    h = N.rmsnorm(x1, np.ones(G.hidden), G.eps)
-    _ = h @ w_lm.T
-    t3 = time.perf_counter()
-    z = np.asarray(np.random.default_rng(rng_seed).standard_normal((G.block, G.vocab)) * 1.7, dtype=np.float32)
-    toks, ell = S.markov_rollout(z, w1, w2, 0)
-    t4 = time.perf_counter()
-    P = np.concatenate([ell, ell[-1:]]).astype(np.float32)
-    S.verify_greedy(P, toks)
-    N.confidence(h, np.ones(G.hidden) * 0.01, 0.0)
-    t5 = time.perf_counter()
-    est = (t1 - t0) + G.n_layers * (t2 - t1) + (t3 - t2) * G.vocab / lm_rows + (t4 - t3) + (t5 - t4)
-    sampled = (t5 - t0)
-    return est, sampled, t_conv, {"fc_s": t1 - t0, "layer_s": t2 - t1, "lm_head_sample_s": t3 - t2,
-                                  "rollout_s": t4 - t3, "verify_conf_s": t5 - t4}
+    for l in range(G.n_layers):
+        L = {k: OW.get(f"l{l}.{k}") for k in LAYER_KEYS}
+        x = N.layer(x, L, G, caches[l][:, :G.kv_lora], caches[l][:, G.kv_lora:], pos)
+    h = N.rmsnorm(x, OW.get("final_norm"), G.eps)
+    z = np.empty((G.block, G.vocab), dtype=np.float64)
+    for lo, wl in OW.lm_chunks():
+        z[:, lo:lo + wl.shape[0]] = h @ wl.T
+    zf = z.astype(np.float32)
+    anchor = int(I["anchor"][b])
+    toks, ell = S.markov_rollout(zf, w1, w2, anchor, draft_mode, T, top_p, seed=1, seq=b, step=0)
+    N.confidence(h, OW.get("w_conf"), float(OW.W["b_conf"].item()))
+    Pb = np.concatenate([ell, ell[-1:]]).astype(np.float32) if P is None else P
+    if verify_mode == 0:
+        S.verify_greedy(Pb, toks)
+    elif verify_mode == 1:
+        S.verify_prob(Pb, ell, toks, draft_mode, T, top_p, seed=1, seq=b, step=0)
+    else:
+        S.verify_block(Pb, ell, toks, draft_mode, T, top_p, seed=1, seq=b, step=0)
+    t1 = time.perf_counter()
+    return (t1 - t0) - (OW.conv_s - conv0)
 
 
 def cores():
@@ -201,6 +269,54 @@ def cores():
         return os.cpu_count()
 
 
+def oracle_threads() -> int:
+    """Threads the oracle's BLAS may use (the --oracle-threads setting, else every core)."""
+    for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        v = os.environ.get(k)
+        if v and v.isdigit():
+            return int(v)
+    return cores()
+
+
+# ---------------------------------------------------------------------------
+# Workloads
+# ---------------------------------------------------------------------------
+def select_workload(args):
+    """The workload of one bench line and its sampling modes: (workload, draft, verify, T, top_p)."""
+    from synthetic.configs import BATCH_STEP, FP8_STEP, FULL_STEP, LONG_STEP, MXFP4_STEP, NVFP4_STEP
+    if args.workload == "full_bs1_ctx4096":
+        w = {"bf16": FULL_STEP, "fp8": FP8_STEP, "nvfp4": NVFP4_STEP, "mxfp4": MXFP4_STEP}[args.format]
+    else:
+        if args.format != "bf16":
+            raise SystemExit("--format applies to the full_bs1_ctx4096 workload")
+        w = {"full_bs1_ctx95000_yarn": LONG_STEP, "full_bs32_paged": BATCH_STEP}[args.workload]
+    draft, verify, T, top_p = w.draft_mode, w.verify_mode, w.temperature, w.top_p
+    if args.sampling == "probabilistic":  # the cards' production sampling: T 1.0, top_p 0.95
+        draft, verify, T, top_p = 1, 1, 1.0, 0.95
+    elif args.sampling == "greedy":
+        draft, verify = 0, 0
+    if args.verify == "block":
+        verify = 2
+        if draft == 0 and args.sampling is None:
+            T, top_p = 1.0, 0.95
+    elif args.verify == "probabilistic":
+        verify = 1
+        if draft == 0 and args.sampling is None:
+            T, top_p = 1.0, 0.95
+    return w, draft, verify, T, top_p
+
+
+MODE_NAMES = {0: "greedy", 1: "probabilistic", 2: "block"}
+
+
+def attention_flops(G, ctx_list, with_block: bool = True) -> float:
+    """Tensor-core attention FLOPs of one step: every query row of every head against
+    every key (scores over the 576-wide key, P V over the 512-wide latent)."""
+    R = G.block * G.n_heads
+    keys = sum(c + (G.block if with_block else 0) for c in ctx_list)
+    return 2.0 * R * keys * (G.kv_lora + G.d_rope + G.kv_lora) * G.n_layers
+
+
 # ---------------------------------------------------------------------------
 def main():
     ap = argparse.ArgumentParser()
@@ -208,14 +324,26 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="full_bs1_ctx4096",
+                    choices=["full_bs1_ctx4096", "full_bs1_ctx95000_yarn", "full_bs32_paged"],
+                    help="full_bs1_ctx4096: the headline (bs 1, ctx 4096); full_bs1_ctx95000_yarn: 95,000-token "
+                         "latent cache, YaRN-16, probabilistic draft and verify at T 1.0, top_p 0.95; "
+                         "full_bs32_paged: 32 sequences, paged ragged contexts in [1k, 16k], greedy")
+    ap.add_argument("--sampling", choices=["greedy", "probabilistic"], default=None,
+                    help="draft and verify sampling (default: the workload's); probabilistic = T 1.0, top_p 0.95")
+    ap.add_argument("--verify", choices=["greedy", "probabilistic", "block"], default=None,
+                    help="verification rule (default: the workload's)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--lm-rows", type=int, default=4096)
+    ap.add_argument("--oracle-threads", type=int, default=0,
+                    help="threads of the oracle's BLAS (set before numpy loads; 0: every core)")
     ap.add_argument("--only", choices=["fc", "rollout", "layer", "append", "verify"], default=None,
                     help="time one call alone for profiling: fc (the fusion GEMM; full shape unless --fc-hidden), "
                          "rollout (Markov rollout, full vocabulary), layer (one full-width MLA layer, ctx 4096), "
                          "append (latent-cache append of 8 verified tokens, all 5 layers, full hidden/latent)")
     ap.add_argument("--fc-hidden", type=int, default=0, help="--only fc: hidden size (output channels)")
     ap.add_argument("--fc-aux", type=int, default=0, help="--only fc: captured states (K = aux * hidden)")
+    ap.add_argument("--roll-mode", choices=["greedy", "probabilistic"], default="greedy",
+                    help="--only rollout: draft sampling (probabilistic: T 1.0, top_p 0.95)")
     ap.add_argument("--format", choices=["bf16", "fp8", "nvfp4", "mxfp4"], default="bf16",
                     help="weight format of fc, q_b, o, gate, up, down (the weight-format sweep workloads)")
     ap.add_argument("--no-drift", action="store_true", help="--format fp8|nvfp4|mxfp4: skip the drift report")
@@ -226,20 +354,29 @@ def main():
     ap.add_argument("--drift-formats", default="fp8,nvfp4,mxfp4", help="--drift: formats against the bf16 path")
     ap.add_argument("--drift-geom", choices=["full", "mid"], default="full",
                     help="--drift: full drafter geometry, or a small one for a quick check")
+    ap.add_argument("--drift-oracle-blocks", type=int, default=0,
+                    help="--drift: also compare bf16 and every format with the float64 oracle on this many blocks "
+                         "per regime (the FP32-reference rows)")
     args = ap.parse_args()
     if args.drift:
         return drift_harness(args)
     assert args.warmup >= 3 or args.impl == "reference", "at least 3 warm-up steps"
 
     from synthetic import generate as gen
-    from synthetic.configs import FP8_STEP, FULL_STEP, MXFP4_STEP, NVFP4_STEP
-    w = {"bf16": FULL_STEP, "fp8": FP8_STEP, "nvfp4": NVFP4_STEP, "mxfp4": MXFP4_STEP}[args.format]
+    w, draft_mode, verify_mode, T, top_p = select_workload(args)
     G = w.geom
     world, rank, local = dist_setup()
-    ctx = w.ctx[0]
-    ab = algorithmic_bytes(G, ctx, fmt=args.format)
-    config = {"workload": w.name, "model": "DSpark drafter (Kimi-K3 geometry), random init", "global_batch": w.bs * world,
-              "seq_len": ctx, "block": G.block, "draft": "greedy", "verify": "greedy", "weights": args.format,
+    ctx_list = gen.context_lengths(w)
+    max_ctx = max(ctx_list)
+    bs = w.bs
+    ab = algorithmic_bytes(G, ctx_list, bs=bs, fmt=args.format)
+    config = {"workload": w.name, "model": "DSpark drafter (Kimi-K3 geometry), random init",
+              "global_batch": bs * world, "blocks_per_step": bs * world,
+              "seq_len": max_ctx if bs == 1 else f"{min(ctx_list)}..{max_ctx} (mean {statistics.mean(ctx_list):.0f})",
+              "block": G.block, "draft": MODE_NAMES[draft_mode], "verify": MODE_NAMES[verify_mode],
+              "temperature": T if (draft_mode or verify_mode) else None,
+              "top_p": top_p if (draft_mode or verify_mode) else None, "weights": args.format,
+              "rope": "yarn-16 from 65536" if G.yarn_factor > 1 else "plain",
               "parallelism": f"replicas{world}",
               "l2": f"no flush: working set {ab['total'] / 1e9:.2f} GB per step > 129 MB L2"}
 
@@ -255,26 +392,27 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        torch.manual_seed(0)
         dev = "cuda" if torch.cuda.is_available() else "cpu"
         W = gen.make_weights(w, dev)
         I = gen.make_inputs(w, dev)
         from oracle import build as obuild
         obuild.build()
+        OW = OracleWeights(W, G)
         for _ in range(args.warmup):
-            oracle_sample(w, W, I, args.lm_rows // 4)
+            oracle_block(OW, G, I, 0, draft_mode, verify_mode, T, top_p)
         vals = []
         for k in range(args.steps):
-            est, sampled, _, parts = oracle_sample(w, W, I, args.lm_rows // 4, rng_seed=k)
-            vals.append(est * 1e6)
+            vals.append(oracle_block(OW, G, I, 0, draft_mode, verify_mode, T, top_p) * bs * 1e6)
         v = statistics.median(vals)
+        sample = (f"per step: one whole block of sequence 0 ({G.n_layers} layers, ctx {ctx_list[0]}, the full "
+                  f"lm_head, rollout, confidence, {MODE_NAMES[verify_mode]} verify), float64"
+                  + (f", times {bs} sequences" if bs > 1 else ""))
         line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": v / 1e3, "higher_is_better": False, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
-                "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores(), "kind": "oracle",
-                                 "sample": f"per step: fc fusion + 1 of {G.n_layers} layers + lm_head on "
-                                           f"{args.lm_rows // 4} of {G.vocab} rows + full Markov rollout + verify, "
-                                           f"scaled to one block"},
+                "cpu_baseline": {"value": v, "unit": UNIT, "cores": oracle_threads(), "kind": "oracle",
+                                 "sample": sample, "weight_conversion_s": round(OW.conv_s, 1),
+                                 "weights_kept": OW.keep},
                 "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
         return
@@ -288,14 +426,13 @@ def main():
     dev = torch.device("cuda", local)
     W = gen.make_weights(w, dev)
     I = gen.make_inputs(w, dev)
-    bs = w.bs
     Wd = W
     if args.format != "bf16":
         from synthetic import quantize as Q
         Wd = Q.quantise_weights(W, args.format, G.n_layers)
         torch.cuda.empty_cache()
-    ds = M.DSpark(G, Wd, max_bs=bs, max_ctx=ctx, weight_format=w.weight_format)
-    kv = ds.make_kv(I["kv_pools"], I["page_table"], I["ctx_len"], ctx)
+    ds = M.DSpark(G, Wd, max_bs=bs, max_ctx=max_ctx, weight_format=w.weight_format)
+    kv = ds.make_kv(I["kv_pools"], I["page_table"], I["ctx_len"], max_ctx)
     x = torch.empty(bs, G.block, G.hidden, dtype=torch.float32, device=dev)
     h_out = torch.empty_like(x)
     z = torch.empty(bs, G.block, G.vocab, dtype=torch.float32, device=dev)
@@ -305,21 +442,17 @@ def main():
     acc = torch.empty(bs, dtype=torch.int32, device=dev)
     out = torch.empty(bs, G.block + 1, dtype=torch.int32, device=dev)
     P = torch.empty(bs, G.block + 1, G.vocab, dtype=torch.float32, device=dev)
-    smp = M.Sample(M.GREEDY, M.GREEDY, 1.0, 1.0, 1, 0)
+    smp = M.Sample(draft_mode, verify_mode, T, top_p, 1, 0)
     aux, anchor = I["aux"], I["anchor"]
 
-    def step(ev=None):
-        if ev is not None:
-            ev[0].record()
+    def step():
         ds.fuse_ctx(aux, x, bs)
-        if ev is not None:
-            ev[1].record()
         ds.draft_block(x, kv, h_out, z, bs)
         ds.markov_rollout(z, anchor, smp, tokens, ell, bs)
         ds.confidence(h_out, conf, bs)
         ds.verify(P, ell, tokens, smp, acc, out, bs)
 
-    # the target's logits: the drafter's own Markov logits plus N(0, 0.5^2) noise,
+    # the target's logits: the drafter's own Markov logits plus N(0, sigma^2) noise,
     # fixed from the first pass (the step is deterministic, so they match every step)
     P.zero_()
     step()
@@ -327,6 +460,7 @@ def main():
     assert st == 0, f"device error {st}"
     noise = gen.noise((bs, G.block + 1, G.vocab), w.target_noise, w.input_seed, device=dev)
     P.copy_(torch.cat([ell, ell[:, -1:]], dim=1) + noise)
+    del noise
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -374,15 +508,63 @@ def main():
     ms = start.elapsed_time(stop) / args.steps
     ms = max_over_ranks(ms, world)
 
-    # ---- the dominant kernel alone: fc fusion GEMM launches (514 MB of weights each, > L2) ----
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    torch.cuda.synchronize()
-    for a_, b_ in evs:
-        a_.record()
-        ds.fuse_ctx(aux, x, bs)
-        b_.record()
-    torch.cuda.synchronize()
-    fc_ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in evs)
+    def timed(call, n):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        torch.cuda.synchronize()
+        for a_, b_ in evs:
+            a_.record()
+            call()
+            b_.record()
+        torch.cuda.synchronize()
+        return statistics.mean(a_.elapsed_time(b_) for a_, b_ in evs)
+
+    pk, src = peaks()
+    hbm = pk["hbm_gbs"]
+    roofline = None
+    if G.yarn_factor > 1 or max_ctx > 32768:
+        # long context: the attention is the dominant kernel and tensor-bound. Its
+        # KV-dependent time is the difference between the layers at the workload's
+        # context and the same launches with every context length set to 0 (same
+        # grid: the splits beyond the context exit at once).
+        zero_ctx = torch.zeros_like(I["ctx_len"])
+        kv0 = ds.make_kv(I["kv_pools"], I["page_table"], zero_ctx, max_ctx)
+        n = max(3, args.steps // 2)
+        ms_ctx = timed(lambda: (ds.fuse_ctx(aux, x, bs), ds.draft_block(x, kv, h_out, z, bs)), n)
+        ms_0 = timed(lambda: (ds.fuse_ctx(aux, x, bs), ds.draft_block(x, kv0, h_out, z, bs)), n)
+        fl = attention_flops(G, ctx_list, with_block=False)
+        tf_peak = pk.get("bf16_tflops_sustained", pk.get("bf16_tflops", FALLBACK["bf16_tflops"]))
+        d = max(ms_ctx - ms_0, 1e-6)
+        achieved = fl / (d * 1e-3) / 1e12
+        roofline = {"kernel": "mla_attention_tc_kernel<576,512> (KV part, all layers: draft layers at the context "
+                              "minus the same launches at context 0)",
+                    "bound": "tensor", "achieved": achieved, "peak": tf_peak, "unit": "TFLOP/s",
+                    "frac": achieved / tf_peak, "traffic": None, "algorithmic_flops_per_step": fl,
+                    "kv_part_ms": d, "draft_ms_at_ctx": ms_ctx, "draft_ms_at_ctx0": ms_0,
+                    "peak_source": src + " (sustained bf16)"}
+    # ---- the GEMM (dominant kernel class at short context): the fc fusion launch, which
+    # the API isolates (the same gemm_swapab_kernel as the step's other 26 weight GEMMs;
+    # 514 MB of weights > L2) ----
+    fc_ms = timed(lambda: ds.fuse_ctx(aux, x, bs), args.steps)
+    fc_bytes = ab["fc_weight"] + bs * G.block * G.n_aux * G.hidden * 2 + bs * G.block * G.hidden * 4
+    fc_achieved = fc_bytes / (fc_ms * 1e-3) / 1e9
+    traffic = None
+    tfile = os.path.join(ROOT, "profiles", "fc_gemm_traffic.json")
+    if os.path.exists(tfile) and args.format == "bf16" and bs == 1:
+        with open(tfile) as f:
+            td = json.load(f)
+        h = hashlib.sha256(open(os.path.join(ROOT, "mla_block_diffusion_gb300", "csrc", "gemm.cuh"), "rb").read())
+        if td.get("gemm_cuh_sha256") == h.hexdigest():
+            traffic = td.get("dram_bytes_per_launch")
+    gemm_line = {"kernel": ("gemm_swapab_kernel" if args.format == "bf16" else "gemm_q_kernel")
+                 + f"<{min(224, max(16, 1 << (bs * G.block - 1).bit_length()))}> (fc fusion launch; the step's "
+                   "weight-GEMM class)",
+                 "bound": "hbm", "achieved": fc_achieved, "peak": hbm, "unit": "GB/s", "frac": fc_achieved / hbm,
+                 "traffic": traffic, "algorithmic_bytes_per_launch": fc_bytes, "avg_launch_ms": fc_ms,
+                 "peak_source": src}
+    if roofline is None:
+        roofline = gemm_line
+    else:
+        roofline["gemm"] = gemm_line
 
     # ---- end to end through the public API with host buffers ----
     aux_h = aux.cpu().pin_memory()
@@ -416,20 +598,8 @@ def main():
     d2h = (acc_h.numel() + out_h.numel() + tok_h.numel()) * 4 + conf_h.numel() * 4
     accept = acc.cpu().tolist()
 
-    pk, src = peaks()
-    hbm = pk["hbm_gbs"]
-    fc_bytes = ab["fc_weight"] + bs * G.block * G.n_aux * G.hidden * 2 + bs * G.block * G.hidden * 4
-    achieved = fc_bytes / (fc_ms * 1e-3) / 1e9
-    traffic = None
-    tfile = os.path.join(ROOT, "profiles", "fc_gemm_traffic.json")
-    if os.path.exists(tfile):
-        with open(tfile) as f:
-            td = json.load(f)
-        h = hashlib.sha256(open(os.path.join(ROOT, "mla_block_diffusion_gb300", "csrc", "gemm.cuh"), "rb").read())
-        if td.get("gemm_cuh_sha256") == h.hexdigest():
-            traffic = td.get("dram_bytes_per_launch")
-    gpu_launches_per_step = ds_launches_per_step(ds)
-    us = ms * 1e3 / world  # whole job: one block per rank per step
+    gpu_launches_per_step = ds_launches_per_step(ds, bs=bs, draft_mode=draft_mode, verify_mode=verify_mode)
+    us = ms * 1e3 / world  # whole job: every rank runs its own step
     line = {
         "metric": METRIC, "value": us, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
@@ -438,24 +608,27 @@ def main():
         "hbm": {"algorithmic_bytes_per_step": ab["total"], "achieved_TBps": ab["total"] / (ms * 1e-3) / 1e12,
                 "frac_of_peak": ab["total"] / (ms * 1e-3) / 1e9 / hbm, "peak_GBps": hbm, "peak_source": src,
                 "frac_of_8TBps": ab["total"] / (ms * 1e-3) / 8e12},
-        "roofline": {"kernel": "gemm_swapab_kernel<16> (fc fusion launch)", "bound": "hbm", "achieved": achieved,
-                     "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
-                     "algorithmic_bytes_per_launch": fc_bytes, "avg_launch_ms": fc_ms, "peak_source": src},
+        "roofline": roofline,
         "clocks": clocks,
         "e2e": {"value": e2e_ms * 1e3 / world, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": gpu_launches_per_step * args.steps,
-        "accept_len": accept,
+        "accept_len": accept if bs <= 8 else {"histogram_0_to_7": np.bincount(np.asarray(accept), minlength=G.block + 1)
+                                                                     .tolist()},
     }
+    if G.yarn_factor > 1 or max_ctx > 32768:
+        line["attention_flops_per_step"] = attention_flops(G, ctx_list)
     if args.format != "bf16" and not args.no_drift and rank == 0:
-        line["drift"] = drift_report(w, W, I, h_out, z, ctx)
+        line["drift"] = drift_report(w, W, I, h_out, z, max_ctx)
         line["vs_bf16_note"] = "drift: this format's GPU outputs against the float64 oracle on the original bf16 weights"
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        est, sampled, conv, parts = oracle_sample(w, W, I, args.lm_rows)
-        line["cpu_baseline"] = {"value": est * 1e6, "unit": UNIT, "cores": cores(), "kind": "oracle",
-                                "sample": f"fc fusion + 1 of {G.n_layers} layers (ctx {ctx}) + lm_head on "
-                                          f"{args.lm_rows} of {G.vocab} rows + full Markov rollout + greedy verify "
-                                          f"+ confidence, float64, scaled to one block; sampled {sampled:.1f} s",
-                                "parts_s": parts}
+        OW = OracleWeights(W, G)
+        secs = oracle_block(OW, G, I, 0, draft_mode, verify_mode, T, top_p,
+                            P=P[0].cpu().numpy() if bs == 1 else None)
+        line["cpu_baseline"] = {"value": secs * bs * 1e6, "unit": UNIT, "cores": oracle_threads(), "kind": "oracle",
+                                "sample": f"one whole block of sequence 0 ({G.n_layers} layers, ctx {ctx_list[0]}, the "
+                                          f"full lm_head, rollout, confidence, {MODE_NAMES[verify_mode]} verify), "
+                                          f"float64" + (f", times {bs} sequences" if bs > 1 else "")
+                                          + f"; weight conversion {OW.conv_s:.1f} s not counted"}
     if rank == 0:
         print(json.dumps(line))
     if world > 1:
@@ -568,7 +741,9 @@ def only_call(args, G, local):
     ell = torch.empty_like(z)
     tokens = torch.empty(1, g.block, dtype=torch.int32, device="cuda")
     kv = ds.make_kv(I["kv_pools"], I["page_table"], I["ctx_len"], ctx)
-    smp = M.Sample(M.GREEDY, M.GREEDY, 1.0, 1.0, 1, 0)
+    prob = args.only == "rollout" and args.roll_mode == "probabilistic"
+    smp = M.Sample(M.PROBABILISTIC, M.PROBABILISTIC, 1.0, 0.95, 1, 0) if prob else M.Sample(M.GREEDY, M.GREEDY, 1.0,
+                                                                                             1.0, 1, 0)
 
     def call():
         if args.only == "rollout":
@@ -868,14 +1043,20 @@ def only_verify(args, G, local):
     print(json.dumps({"only": "verify", "vocab": g.vocab, "block": g.block, "modes": res}))
 
 
-def ds_launches_per_step(ds) -> int:
-    """Kernels one greedy draft-and-verify step launches (mirrors the library's choices).
+def verify_launches(verify_mode: int) -> int:
+    """Kernels of one dspark_verify call: greedy takes the row argmax and a finalize
+    kernel; probabilistic and block verification one cooperative kernel."""
+    return 2 if verify_mode == 0 else 1
+
+
+def ds_launches_per_step(ds, bs: int = 1, draft_mode: int = 0, verify_mode: int = 0) -> int:
+    """Kernels one draft-and-verify step launches (mirrors the library's choices).
 
     fc; per layer RMSNorm, q_a||kv_a, latent norms, q_b, q absorption, attention,
     split combine + v absorption (one fused kernel on the tensor-core path; two
     kernels otherwise when the KV sequence is split), o_proj, RMSNorm, gate/up,
-    down; then the final RMSNorm, lm_head, rollout, confidence and the two verify
-    kernels.
+    down; then the final RMSNorm, lm_head, rollout (one kernel), confidence and
+    the verify kernels.
     """
     G = ds.G
     R = G.block * G.n_heads
@@ -890,7 +1071,7 @@ def ds_launches_per_step(ds) -> int:
         per_layer = 11 + (1 if splits > 1 and not fused else 0)
     else:
         per_layer = 11 + (1 if ds_layout_splits(ds) > 1 else 0)
-    return 1 + G.n_layers * per_layer + 2 + 1 + 1 + 2
+    return 1 + G.n_layers * per_layer + 2 + 1 + 1 + verify_launches(verify_mode)
 
 
 def ds_layout_splits(ds) -> int:

@@ -25,7 +25,9 @@
  *  - The workspace is caller-allocated (dspark_workspace_bytes) and must be
  *    zero-filled once before its first use; the kernels keep its counters at
  *    zero afterwards. After dspark_check() reports DSPARK_ERR_TIMEOUT the
- *    workspace must be zero-filled again.
+ *    workspace must be zero-filled again. Bytes 72..79 of the workspace hold
+ *    an optional limit, in nanoseconds (uint64), on the waits of the rollout's
+ *    and verification's CTAs for one another; 0 (the zero fill) means 2 s.
  *  - Batch size bs is 1..32 for every call.
  */
 #ifndef DSPARK_H
@@ -252,18 +254,23 @@ dspark_status dspark_kv_append(dspark_handle_t *h, const float *x_new, int n_max
  * Scratch (split partials, tile counters, an error word) lives in one
  * ~2.5 MiB array inside the library, resident on every device that loads it
  * until the process exits. Limits: bs <= 2, hidden <= 131072; larger sizes
- * return DSPARK_ERR_SHAPE. The first call on a device resolves the array's
- * device address and sets the kernel's shared-memory limit; make that first
- * call before any stream capture. Each call clears the counters it needs on
- * its stream. All calls share the one array: calls that overlap on the GPU
- * (different streams, or several handles at once) race and must be
- * serialised by the caller. Device-side errors of this call are not reported
- * through dspark_check. Allocates nothing.
+ * return DSPARK_ERR_SHAPE. Only bf16 fc weights: a handle with another
+ * weight_format gets DSPARK_ERR_UNSUPPORTED before anything is launched. The
+ * first call on a device resolves the array's device address and sets the
+ * kernel's shared-memory limit (host threads making that first call at once
+ * are serialised); make that first call before any stream capture. Each call
+ * clears the tile counters it needs on its stream. All calls share the one
+ * array: calls that overlap on the GPU (different streams, or several handles
+ * at once) race and must be serialised by the caller. Device-side errors of
+ * this call (an expired bounded wait) stay in the array's own error word until
+ * dspark_check(h, NULL, stream) reads and clears it. Allocates nothing.
  * aux bf16 [bs, block, n_aux, hidden]; x fp32 [bs, block, hidden] (overwritten). */
 dspark_status dspark_fuse_ctx_noalloc(dspark_handle_t *h, const void *aux, float *x, int bs, void *stream);
 
 /* Synchronise the stream, return and clear the device error word
- * (DSPARK_OK if no kernel recorded an error since the last check). */
+ * (DSPARK_OK if no kernel recorded an error since the last check). With
+ * ws == NULL the word read is the one of dspark_fuse_ctx_noalloc's fixed
+ * scratch on the current device. */
 dspark_status dspark_check(dspark_handle_t *h, void *ws, void *stream);
 
 const char *dspark_status_str(dspark_status s);

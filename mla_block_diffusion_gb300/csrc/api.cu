@@ -895,7 +895,8 @@ dspark_status dspark_verify(dspark_handle_t *h, const float *target_logits, cons
 }
 
 dspark_status dspark_check(dspark_handle_t *h, void *ws, void *stream) {
-    if (!h || !ws) return DSPARK_ERR_NULL;
+    if (!h) return DSPARK_ERR_NULL;
+    if (!ws) return noalloc_check(stream);  // the allocation-free fusion's own error word
     if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return DSPARK_ERR_CUDA;
     int err = 0;
     if (cudaMemcpy(&err, (char *)ws + kCtlErr, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)

@@ -82,10 +82,13 @@ cudaError_t launch_attention_tc(const CUtensorMap &pool_map, const CUtensorMap &
 cudaError_t launch_confidence(const float *h_out, int H, const float *w, float bias, float *conf, int M,
                               cudaStream_t st);
 
-// Grid-barrier words inside the workspace (zero before the first launch).
+// Grid-barrier words inside the workspace (zero before the first launch), and
+// the limit of the sampling kernels' inter-CTA waits in nanoseconds (0: the
+// default kWaitLimitNs; a caller may set a shorter one).
 struct SampleCtl {
     unsigned int bar_count;
     unsigned int bar_gen;
+    unsigned long long wait_ns;
 };
 
 struct RolloutParams {
@@ -126,6 +129,10 @@ const dspark_geom_t *handle_geom(const dspark_handle_t *h);
 int handle_num_sms(const dspark_handle_t *h);
 const CUtensorMap *handle_fc_map(const dspark_handle_t *h);
 bool encode_bf16_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows);
+
+// Error word of the allocation-free fusion's fixed scratch on the current
+// device (synchronises the stream; reads and clears the word).
+dspark_status noalloc_check(void *stream);
 
 size_t rollout_scratch_words(int bs, int B, int grid);
 size_t verify_scratch_words(int bs, int B, int grid);

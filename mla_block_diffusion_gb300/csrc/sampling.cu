@@ -147,6 +147,12 @@ __device__ unsigned long long block_sum_u64(unsigned long long v, unsigned long 
     return red[32];
 }
 
+// Limit of the inter-CTA waits: the workspace's wait_ns when set, else kWaitLimitNs.
+DS_DEVINL unsigned long long grid_wait_limit(const SampleCtl *ctl) {
+    const unsigned long long w = *(const volatile unsigned long long *)&ctl->wait_ns;
+    return w ? w : kWaitLimitNs;
+}
+
 // ---------------------------------------------------------------------------
 // Bounded grid barrier (all CTAs resident: cooperative launch). On expiry the
 // error word gets DSPARK_ERR_TIMEOUT and every later barrier returns false.
@@ -163,9 +169,9 @@ __device__ bool grid_barrier(SampleCtl *ctl, volatile int *s_fail, int *err) {
             __threadfence();
             atomicAdd(&ctl->bar_gen, 1u);
         } else {
-            const unsigned long long t0 = globaltimer();
+            const unsigned long long t0 = globaltimer(), limit = grid_wait_limit(ctl);
             while (*genp == gen) {
-                if (globaltimer() - t0 > kWaitLimitNs) {
+                if (globaltimer() - t0 > limit) {
                     set_error(err, DSPARK_ERR_TIMEOUT);
                     *s_fail = 1;
                     break;
@@ -959,9 +965,9 @@ DS_DEVINL unsigned int grid_arrive(SampleCtl *ctl) {
 }
 DS_DEVINL bool grid_wait(SampleCtl *ctl, unsigned int gen, int *err) {
     volatile unsigned int *genp = &ctl->bar_gen;
-    const unsigned long long t0 = globaltimer();
+    const unsigned long long t0 = globaltimer(), limit = grid_wait_limit(ctl);
     while (*genp == gen) {
-        if (globaltimer() - t0 > kWaitLimitNs) {
+        if (globaltimer() - t0 > limit) {
             set_error(err, DSPARK_ERR_TIMEOUT);
             return false;
         }
@@ -1115,7 +1121,7 @@ __global__ void __launch_bounds__(kSampThreads, 1)
             unsigned long long g = 0ull;
             uint32_t pending = 0u;
             for (int c = 0; lane + 32 * c < grid; ++c) pending |= 1u << c;
-            const unsigned long long t0 = globaltimer();
+            const unsigned long long t0 = globaltimer(), limit = grid_wait_limit(p.ctl);
             while (__any_sync(0xffffffffu, pending != 0u)) {
                 unsigned long long kv[kResGatherPerLane];
 #pragma unroll
@@ -1128,7 +1134,7 @@ __global__ void __launch_bounds__(kSampThreads, 1)
                         pending &= ~(1u << c);
                     }
                 if (pending) {
-                    if (s_fail || globaltimer() - t0 > kWaitLimitNs) {
+                    if (s_fail || globaltimer() - t0 > limit) {
                         set_error(p.err, DSPARK_ERR_TIMEOUT);
                         s_fail = 1;
                         pending = 0u;

@@ -237,3 +237,7 @@ class DSpark:
     def check(self) -> int:
         """Synchronise and return (and clear) the device error word."""
         return lib().dspark_check(self.h, _p(self.ws), _stream())
+
+    def check_noalloc(self) -> int:
+        """Synchronise and return (and clear) the error word of the allocation-free fusion's fixed scratch."""
+        return lib().dspark_check(self.h, None, _stream())

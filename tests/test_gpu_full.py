@@ -91,10 +91,21 @@ def test_full_geometry_draft(M, weights, w):
         assert rel_l2(x0[b].cpu().numpy()[:, ch], ref) < TOL
     rows = np.sort(rng.choice(G.vocab, 4096, replace=False))
     seqs = [0] if w.bs == 1 else [0, int(np.argmax(I["ctx_list"])), w.bs - 1]
+    conf = torch.empty(w.bs, G.block, dtype=torch.float32, device="cuda")
+    ds.confidence(h, conf, w.bs)
+    assert ds.check() == 0
+    w_conf, b_conf = f64(W["w_conf"]), float(W["b_conf"].item())
     for b in seqs:
         oh, oz = oracle_seq(w, W, I, b, rows)
         assert rel_l2(h[b].cpu().numpy(), oh) < TOL, b
         assert rel_l2(z[b].cpu().numpy()[:, rows], oz) < TOL, b
+        # confidence head at the full hidden size: on the GPU's own h_out (same input: the
+        # head alone, fp32 accumulation over 7168 terms) and on the oracle's h_out (end to
+        # end: the hidden states' 1e-2 relative error passes through w_c with the
+        # sigmoid's slope <= 1/4, a few 1e-3 for these weights)
+        c = conf[b].cpu().numpy().astype(np.float64)
+        assert np.max(np.abs(c - N.confidence(h[b].cpu().double().numpy(), w_conf, b_conf))) < 1e-5, b
+        assert np.max(np.abs(c - N.confidence(oh, w_conf, b_conf))) < 2e-2, b
 
 
 @pytest.mark.parametrize("mode,T,top_p", [(0, 1.0, 1.0), (1, 1.0, 0.95)])
@@ -141,3 +152,54 @@ def test_full_vocab_rollout_and_verify(M, weights, mode, T, top_p):
         for b in range(bs):
             a, o = S.verify_block(Ps[b], ells[b], toks[b], 0, T, top_p, seed=99, seq=b, step=4)
             assert int(acc[b]) == a and out[b].cpu().numpy().tolist() == o.tolist(), b
+
+
+def test_full_rollout_greedy_bs1(M, weights):
+    """bs = 1 greedy over V = 163,840 with rank 256 and the full weights: the
+    on-chip (resident) rollout the benchmark step runs. Tokens and every logit
+    bit-exact against the oracle, for several anchors, two calls each."""
+    G = FULL_STEP.geom
+    ds = M.DSpark(G, weights, max_bs=1)
+    w1, w2 = weights["markov_w1"].cpu(), weights["markov_w2"].cpu()
+    for k, anchor in enumerate((0, 81234, G.vocab - 1)):
+        z = gen.draft_logits(1, G.block, G.vocab, 40 + k)
+        t_o, ell_o = S.markov_rollout(z[0].numpy(), w1, w2, anchor)
+        a = torch.tensor([anchor], dtype=torch.int32, device="cuda")
+        for call in range(2):
+            tokens = torch.full((1, G.block), -1, dtype=torch.int32, device="cuda")
+            ell = torch.full((1, G.block, G.vocab), float("nan"), dtype=torch.float32, device="cuda")
+            ds.markov_rollout(z.cuda(), a, M.Sample(0, 0, 1.0, 1.0, 5, call), tokens, ell, 1)
+            assert ds.check() == 0
+            assert tokens[0].cpu().numpy().tolist() == t_o.tolist(), (anchor, call)
+            assert np.array_equal(u32(ell[0].cpu().numpy()), u32(ell_o)), (anchor, call)
+
+
+@pytest.mark.parametrize("V,r", [(163840, 256), (165376, 256), (156000, 208), (163840, 144)])
+def test_resident_rollout_rank_and_slice_edges(M, V, r):
+    """The resident rollout's storage classes at sizes where all of them are in
+    use: rank rows 0-127 in tensor memory, 128-159 in registers, 160-255 in
+    shared-memory slots; with about 152 CTAs a vocabulary above 155,648 gives
+    every CTA more than 512 pairs, so the secondary pairs are used (165,376:
+    every CTA holds 544 pairs, the most the kernel takes). Markov weights with
+    std 0.25 so the correction moves the argmax. Bit-exact against the oracle."""
+    from dataclasses import replace
+    from synthetic.configs import FULL
+    G = replace(FULL, hidden=64, n_aux=1, n_layers=1, n_heads=1, q_lora=64, kv_lora=64, d_nope=16, d_rope=16, d_v=64,
+                inter=64, vocab=V, rank=r)
+    w = replace(FULL_STEP, geom=G)
+    W = gen.make_weights(w, "cuda")
+    W["markov_w1"] = gen.normal((V, r), 0.25, 17, "m1", "cuda")
+    W["markov_w2"] = gen.normal((r, V), 0.25, 17, "m2", "cuda")
+    ds = M.DSpark(G, W, max_bs=1)
+    w1, w2 = W["markov_w1"].cpu(), W["markov_w2"].cpu()
+    z = gen.draft_logits(1, G.block, V, 50 + r)
+    anchor = gen.uniform_tokens((1,), V, r, "anchor")
+    t_o, ell_o = S.markov_rollout(z[0].numpy(), w1, w2, int(anchor[0]))
+    tokens = torch.full((1, G.block), -1, dtype=torch.int32, device="cuda")
+    ell = torch.empty(1, G.block, V, dtype=torch.float32, device="cuda")
+    ds.markov_rollout(z.cuda(), anchor.cuda(), M.Sample(0, 0, 1.0, 1.0, 5, 0), tokens, ell, 1)
+    assert ds.check() == 0
+    assert tokens[0].cpu().numpy().tolist() == t_o.tolist()
+    assert np.array_equal(u32(ell[0].cpu().numpy()), u32(ell_o))
+    # the correction decides at least one position (the test exercises the chain, not z alone)
+    assert any(int(np.argmax(z[0, i].numpy())) != int(t_o[i]) for i in range(G.block))
