@@ -938,8 +938,15 @@ def drift_harness(args):
     tok = torch.empty(1, B, dtype=torch.int32, device="cuda")
     conf = torch.empty(1, B, dtype=torch.float32, device="cuda")
     regimes = ["boot", "heavy", "gauss"] if args.regime == "all" else [args.regime]
+    n_or = args.drift_oracle_blocks
+    OW = None
+    if n_or > 0:
+        from oracle import build as obuild
+        obuild.build()
+        OW = OracleWeights(W, G)
     for regime in regimes:
         acc = {f: {"greedy": [], "seq": [], "kl": [], "ov": [], "hrel": [], "conf": []} for f in fmts}
+        acc_or = {f: {"greedy": [], "seq": [], "hrel": []} for f in ["bf16"] + fmts}
         conf_ref = []
         t0 = time.time()
         for blk in range(args.blocks):
@@ -963,6 +970,19 @@ def drift_harness(args):
                 hd.markov_rollout(z, anchor, smp, tok, ell, 1)
                 hd.confidence(h_out, conf, 1)
                 out[n] = (h_out[0].clone(), z[0].clone(), tok[0].clone(), conf[0].clone())
+            if blk < n_or:
+                # the float64 oracle on the same block: the FP32-class reference of the cards'
+                # table, against which bf16 itself is the noise floor
+                h_o, z_o, t_o = oracle_drift_block(OW, G, aux, I, ctx, int(anchor.item()))
+                prev_o = torch.as_tensor(np.concatenate([[int(anchor.item())], t_o[:-1]]), device="cuda").long()
+                delta_o = (w1[prev_o] @ w2).double().cpu().numpy()
+                g_o = np.argmax(z_o + delta_o, axis=1)
+                for n in ["bf16"] + fmts:
+                    h_n, z_n, t_n, _ = out[n]
+                    acc_or[n]["greedy"].append(np.argmax(z_n.double().cpu().numpy() + delta_o, axis=1) == g_o)
+                    acc_or[n]["seq"].append(t_n.cpu().numpy() == t_o)
+                    hn = h_n.double().cpu().numpy()
+                    acc_or[n]["hrel"].append(float(np.linalg.norm(hn - h_o) / np.linalg.norm(h_o)))
             h_r, z_r, t_r, c_r = out["bf16"]
             prev = torch.cat([anchor.long(), t_r[:-1].long()])
             delta = w1[prev] @ w2                      # the Markov correction after the bf16 path's tokens
@@ -999,9 +1019,44 @@ def drift_harness(args):
                       "hidden_rel_err": float(np.mean(a["hrel"])),
                       "confidence_r": pearson(cr, cv),
                       "flip_rate": float(np.mean((cr > 0.5) != (cv > 0.5)))}
+        vs_oracle = None
+        if n_or > 0:
+            vs_oracle = {}
+            for n in ["bf16"] + fmts:
+                seq = np.stack(acc_or[n]["seq"])
+                s_i = conditional_agreement(seq)
+                vs_oracle[n] = {"greedy_agreement": float(np.concatenate(acc_or[n]["greedy"]).mean()),
+                                "sequential_rollout": float(seq.mean()),
+                                "per_position_sequential": [round(float(v), 4) for v in s_i],
+                                "ceiling": ceiling_from_agreement(s_i),
+                                "hidden_rel_err": float(np.mean(acc_or[n]["hrel"]))}
         print(json.dumps({"drift": regime, "blocks": args.blocks, "geometry": args.drift_geom, "ctx": ctx,
+                          "vs_float64_oracle": vs_oracle, "oracle_blocks": n_or,
                           "reference": "bf16 weights on the same kernels", "seconds": round(time.time() - t0, 1),
                           "formats": res}))
+
+
+def oracle_drift_block(OW, G, aux, I, ctx, anchor):
+    """The float64 oracle on one drift block (sequence 0's cache): h_out [B, H], z [B, V]
+    and its own greedy Markov rollout from the anchor."""
+    from oracle import network as N
+    from oracle import sampling as S
+    f64 = lambda t: t.detach().to(torch.float64).cpu().numpy()
+    table = I["page_table"][0]
+    pages = table[: (ctx + G.page_size - 1) // G.page_size].long()
+    x = N.fuse_ctx(OW.get("w_fc"), f64(aux[0]))
+    pos = np.arange(G.block, dtype=np.float64) + ctx
+    for l in range(G.n_layers):
+        L = {k: OW.get(f"l{l}.{k}") for k in LAYER_KEYS}
+        pool = f64(I["kv_pools"][l][pages])
+        cache = N.gather_cache(pool, np.arange(pool.shape[0]), ctx)
+        x = N.layer(x, L, G, cache[:, :G.kv_lora], cache[:, G.kv_lora:], pos)
+    h = N.rmsnorm(x, OW.get("final_norm"), G.eps)
+    z = np.empty((G.block, G.vocab), dtype=np.float64)
+    for lo, wl in OW.lm_chunks():
+        z[:, lo:lo + wl.shape[0]] = h @ wl.T
+    toks, _ = S.markov_rollout(z.astype(np.float32), OW.W["markov_w1"].cpu(), OW.W["markov_w2"].cpu(), anchor)
+    return h, z, toks
 
 
 def only_verify(args, G, local):

@@ -9,8 +9,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libdspark.so")
-SOURCES = ["api.cu", "layers.cu", "attn_tc.cu", "sampling.cu", "noalloc.cu"]
-HEADERS = ["common.cuh", "gemm.cuh", "gemm_q.cuh", "internal.h", os.path.join("..", "..", "include", "dspark.h")]
+SOURCES = ["api.cu", "layers.cu", "attn_tc.cu", "sampling.cu", "verify.cu", "noalloc.cu"]
+HEADERS = ["common.cuh", "gemm.cuh", "gemm_q.cuh", "internal.h", "sampling_spec.cuh", os.path.join("..", "..", "include", "dspark.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
 

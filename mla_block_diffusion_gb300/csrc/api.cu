@@ -20,7 +20,7 @@ namespace {
 
 constexpr int kMaxBs = 32;
 constexpr size_t kCtlBytes = 64 * 1024;
-constexpr size_t kCtlErr = 0, kCtlSample = 64, kCtlKeys = 128, kCtlCounters = 16896;
+constexpr size_t kCtlErr = 0, kCtlSample = 64, kCtlKeys = 128, kCtlDraw = 8192, kCtlCounters = 16896;
 constexpr int kMaxCounters = (int)((kCtlBytes - kCtlCounters) / sizeof(int));
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -526,6 +526,10 @@ dspark_status dspark_create(const dspark_geom_t *geom, const dspark_weights_t *w
         return DSPARK_ERR_CUDA;
     }
     h->roll_resident = rollout_resident_setup(g.vocab, g.rank, h->samp_grid);
+    if (!verify_setup(g.vocab)) {
+        delete h;
+        return DSPARK_ERR_CUDA;
+    }
     // RoPE frequencies; YaRN "NTK-by-parts" ramp when yarn_factor > 1
     memset(&h->rope, 0, sizeof(h->rope));
     for (int j = 0; j < g.d_rope / 2; ++j) {
@@ -891,6 +895,7 @@ dspark_status dspark_verify(dspark_handle_t *h, const float *target_logits, cons
         prob ? (unsigned long long *)((char *)ws + L.scratch) : (unsigned long long *)((char *)ws + kCtlKeys);
     p.ctl = (SampleCtl *)((char *)ws + kCtlSample);
     p.err = (int *)((char *)ws + kCtlErr);
+    p.draw_count = (unsigned int *)((char *)ws + kCtlDraw);
     return cuda_status(launch_verify(p, h->samp_grid, (cudaStream_t)stream));
 }
 

@@ -116,10 +116,12 @@ struct VerifyParams {
     int32_t *out_tokens;            // [bs, B + 1]
     int bs, B, V;
     int verify_mode, draft_greedy;
+    int stage;                      // the draws stage their rows in shared memory (set by the launcher)
+    unsigned int *draw_count;       // [bs] CTAs done per sequence (zero between launches)
     float T, top_p;
     unsigned long long seed;
     unsigned int step;
-    unsigned long long *scratch;    // greedy: zero between launches; probabilistic: zeroed at start
+    unsigned long long *scratch;    // greedy: argmax keys, zero between launches; else row statistics and masses
     SampleCtl *ctl;
     int *err;
 };
@@ -144,6 +146,8 @@ bool rollout_resident_setup(int V, int r, int grid);
 // tensor map views w2 as uint32 pairs [r, V / 2] with boxes {box_w, 16}.
 __host__ __device__ void rollout_box(int V, int grid, int *box_w, int *nbox);
 cudaError_t launch_verify(VerifyParams p, int grid, cudaStream_t st);
+// Shared-memory limit of the verification's nucleus kernel for this vocabulary.
+bool verify_setup(int V);
 int sampling_max_grid(int num_sms, int V);
 
 }  // namespace ds

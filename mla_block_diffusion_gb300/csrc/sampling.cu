@@ -22,130 +22,14 @@
 //
 // The rollout and the probabilistic verify run cooperatively (all CTAs
 // resident) and synchronise through a bounded grid barrier in the workspace.
-#include "internal.h"
+#include "sampling_spec.cuh"
 
 #include <algorithm>
 
 namespace ds {
 
-constexpr int kSampThreads = 512;
 constexpr int kRowsPerGroup = 8;    // rows whose histograms share one pass
 constexpr int kRadixPasses = 7;     // keys < 2^51, digits at bits 48, 40, ..., 0
-constexpr int kMaxSampBs = 32;
-
-// ---------------------------------------------------------------------------
-// Counter-based uniforms: Philox4x32-10, first output word.
-// ---------------------------------------------------------------------------
-DS_DEVINL uint32_t philox_word(unsigned long long seed, uint32_t seq, uint32_t step, uint32_t pos, uint32_t purpose) {
-    uint32_t c0 = step, c1 = seq, c2 = pos, c3 = purpose;
-    uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
-#pragma unroll
-    for (int round = 0; round < 10; ++round) {
-        if (round) {
-            k0 += 0x9E3779B9u;
-            k1 += 0xBB67AE85u;
-        }
-        const uint32_t lo0 = 0xD2511F53u * c0, hi0 = __umulhi(0xD2511F53u, c0);
-        const uint32_t lo1 = 0xCD9E8D57u * c2, hi1 = __umulhi(0xCD9E8D57u, c2);
-        const uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
-        c0 = n0;
-        c1 = lo1;
-        c2 = n2;
-        c3 = lo0;
-    }
-    return c0;
-}
-
-// ---------------------------------------------------------------------------
-// Own fp32 exp for x <= 0 (every step one IEEE operation).
-// ---------------------------------------------------------------------------
-DS_DEVINL float exp_hat(float x) {
-    if (!(x >= -23.0f)) return 0.0f;
-    const float n = rintf(__fmul_rn(x, 1.44269502162933349609375f));
-    float r = __fmaf_rn(-n, 0.693145751953125f, x);
-    r = __fmaf_rn(-n, 1.428606765330187045037746429443359375e-06f, r);
-    float p = 1.98412701138295233249664306640625e-04f;
-    p = __fmaf_rn(p, r, 1.388888922519981861114501953125e-03f);
-    p = __fmaf_rn(p, r, 8.333333767950534820556640625e-03f);
-    p = __fmaf_rn(p, r, 4.16666679084300994873046875e-02f);
-    p = __fmaf_rn(p, r, 1.66666671633720397949218750e-01f);
-    p = __fmaf_rn(p, r, 0.5f);
-    p = __fmaf_rn(p, r, 1.0f);
-    p = __fmaf_rn(p, r, 1.0f);
-    return __fmul_rn(p, __int_as_float(((int)n + 127) << 23));
-}
-
-DS_DEVINL unsigned long long weight_of(float l, float T, float m) {
-    const float y = __fdiv_rn(l, T);
-    const float e = exp_hat(__fsub_rn(y, m));
-    return (unsigned long long)__fmul_rn(e, 4294967296.0f);
-}
-
-DS_DEVINL unsigned long long key_of(unsigned long long E, int v) {
-    return (E << 18) | (unsigned long long)((1u << 18) - 1u - (uint32_t)v);
-}
-
-// Order-preserving map of fp32 to uint32 (NaN excluded by the callers).
-DS_DEVINL uint32_t f2ord(float f) {
-    const uint32_t u = __float_as_uint(f);
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-DS_DEVINL float ord2f(uint32_t o) { return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o); }
-
-// Greedy key: larger value first, lower id on ties (-0 counts as +0).
-DS_DEVINL unsigned long long argmax_key(float l, int v) {
-    if (l == 0.0f) l = 0.0f;
-    return ((unsigned long long)f2ord(l) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)v);
-}
-DS_DEVINL int argmax_token(unsigned long long key) { return (int)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull)); }
-
-DS_DEVINL unsigned long long top_p_q32(float top_p) {
-    if (!(top_p > 0.0f)) return 0ull;
-    if (top_p >= 1.0f) return 1ull << 32;
-    return (unsigned long long)((double)top_p * 4294967296.0);
-}
-
-// ---------------------------------------------------------------------------
-// Block reductions
-// ---------------------------------------------------------------------------
-DS_DEVINL unsigned long long warp_max_u64(unsigned long long v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const unsigned long long w = __shfl_xor_sync(0xffffffffu, v, o);
-        v = w > v ? w : v;
-    }
-    return v;
-}
-DS_DEVINL unsigned long long warp_sum_u64(unsigned long long v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
-
-__device__ unsigned long long block_max_u64(unsigned long long v, unsigned long long *red) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    v = warp_max_u64(v);
-    __syncthreads();
-    if (lane == 0) red[warp] = v;
-    __syncthreads();
-    unsigned long long r = (threadIdx.x < (blockDim.x >> 5)) ? red[threadIdx.x] : 0ull;
-    if (warp == 0) r = warp_max_u64(r);
-    if (threadIdx.x == 0) red[32] = r;
-    __syncthreads();
-    return red[32];
-}
-__device__ unsigned long long block_sum_u64(unsigned long long v, unsigned long long *red) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    v = warp_sum_u64(v);
-    __syncthreads();
-    if (lane == 0) red[warp] = v;
-    __syncthreads();
-    unsigned long long r = (threadIdx.x < (blockDim.x >> 5)) ? red[threadIdx.x] : 0ull;
-    if (warp == 0) r = warp_sum_u64(r);
-    if (threadIdx.x == 0) red[32] = r;
-    __syncthreads();
-    return red[32];
-}
 
 // Limit of the inter-CTA waits: the workspace's wait_ns when set, else kWaitLimitNs.
 DS_DEVINL unsigned long long grid_wait_limit(const SampleCtl *ctl) {
@@ -1170,439 +1054,6 @@ __global__ void __launch_bounds__(kSampThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
-// Verification
-// ---------------------------------------------------------------------------
-// Greedy: row argmax keys (zero between launches) then a finalize kernel that
-// also returns the keys to zero.
-__global__ void verify_argmax_kernel(const float *__restrict__ P, int rows, int V, unsigned long long *keys, int *err) {
-    pdl_trigger();
-    pdl_wait();
-    __shared__ unsigned long long red[33];
-    const int row = blockIdx.y;
-    const int nslices = gridDim.x;
-    const int npairs = V / 2;
-    const int lo = (int)((long long)blockIdx.x * npairs / nslices);
-    const int hi = (int)((long long)(blockIdx.x + 1) * npairs / nslices);
-    unsigned long long best = 0;
-    bool bad = false;
-    const float *pr = P + (size_t)row * V;
-    // four independent pair loads in flight per thread
-    for (int pp0 = lo + threadIdx.x; pp0 < hi; pp0 += 4 * blockDim.x) {
-        float2 l[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int pp = pp0 + u * blockDim.x;
-            l[u] = pp < hi ? __ldcs((const float2 *)(pr + 2 * pp)) : make_float2(0.f, 0.f);
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int pp = pp0 + u * blockDim.x;
-            if (pp < hi) {
-                if (!isfinite(l[u].x) || !isfinite(l[u].y)) bad = true;
-                best = max(best, max(argmax_key(l[u].x, 2 * pp), argmax_key(l[u].y, 2 * pp + 1)));
-            }
-        }
-    }
-    if (bad) set_error(err, DSPARK_ERR_BAD_INPUT);
-    best = block_max_u64(best, red);
-    if (threadIdx.x == 0) atomicMax(&keys[row], best);
-}
-
-__global__ void verify_greedy_finalize(const int32_t *__restrict__ tokens, int bs, int B, int V,
-                                       unsigned long long *keys, int32_t *accept_len, int32_t *out_tokens, int *err) {
-    pdl_trigger();
-    pdl_wait();
-    const int b = blockIdx.x * blockDim.x + threadIdx.x;
-    if (b >= bs) return;
-    unsigned long long *k = keys + (size_t)b * (B + 1);
-    int a = 0;
-    for (; a < B; ++a) {
-        const int t = tokens[b * B + a];
-        if (t < 0 || t >= V) {
-            set_error(err, DSPARK_ERR_OOB);
-            break;
-        }
-        if (argmax_token(k[a]) != t) break;
-        out_tokens[b * (B + 1) + a] = t;
-    }
-    out_tokens[b * (B + 1) + a] = argmax_token(k[a]);
-    for (int j = a + 1; j <= B; ++j) out_tokens[b * (B + 1) + j] = -1;
-    accept_len[b] = a;
-    for (int j = 0; j <= B; ++j) k[j] = 0;
-}
-
-// Probabilistic (cooperative). scratch layout (words), R rows per sequence:
-// p rows 0..B, then (unless the draft was greedy) q rows 0..B-1:
-//   gM [bs*R] | gS [bs*R] | gH [groups][passes][kRowsPerGroup][256] | stats [bs*R][2] | parts [bs][grid][2]
-struct VerLayout {
-    size_t gM, gS, gH, stats, parts, mass, total;
-    int R, nrows, groups;
-    __host__ __device__ VerLayout(int bs, int B, int grid, int draft_greedy) {
-        R = draft_greedy ? B + 1 : 2 * B + 1;
-        nrows = bs * R;
-        groups = (nrows + kRowsPerGroup - 1) / kRowsPerGroup;
-        gM = 0;
-        gS = gM + nrows;
-        gH = gS + nrows;
-        stats = gH + (size_t)groups * kRadixPasses * kRowsPerGroup * 256;
-        parts = stats + (size_t)nrows * 2;
-        mass = parts + (size_t)bs * grid * 2;           // block verification: [bs][B][grid][2]
-        total = mass + (size_t)bs * B * grid * 2;
-    }
-};
-
-size_t verify_scratch_words(int bs, int B, int grid) { return VerLayout(bs, B, grid, 0).total; }
-
-DS_DEVINL const float *ver_row(const VerifyParams &p, int gr) {
-    const int R = p.draft_greedy ? p.B + 1 : 2 * p.B + 1, b = gr / R, j = gr % R;
-    if (j <= p.B) return p.P + ((size_t)b * (p.B + 1) + j) * p.V;
-    return p.ell + ((size_t)b * p.B + (j - p.B - 1)) * p.V;
-}
-
-__global__ void __launch_bounds__(kSampThreads, 1) verify_prob_kernel(VerifyParams p) {
-    __shared__ NucleusSmem sm;
-    __shared__ DrawSmem dsm;
-    __shared__ volatile int s_fail;
-    __shared__ const float *s_rows[kRowsPerGroup];
-    __shared__ int s_acc[kMaxSampBs];
-    __shared__ int s_kind[kMaxSampBs];  // 0: residual draw at position s_acc, 1: bonus draw
-    const VerLayout L(p.bs, p.B, gridDim.x, p.draft_greedy);
-    unsigned long long *sc = p.scratch;
-    const int V = p.V;
-    if (threadIdx.x == 0) s_fail = 0;
-    for (size_t w = (size_t)blockIdx.x * blockDim.x + threadIdx.x; w < L.total; w += (size_t)gridDim.x * blockDim.x)
-        sc[w] = 0;
-    __threadfence();
-    if (!grid_barrier(p.ctl, &s_fail, p.err)) return;
-    for (int g = 0; g < L.groups; ++g) {
-        const int r0 = g * kRowsPerGroup, nr = min(kRowsPerGroup, L.nrows - r0);
-        if (threadIdx.x < nr) s_rows[threadIdx.x] = ver_row(p, r0 + threadIdx.x);
-        __syncthreads();
-        if (!group_max(s_rows, nr, V, p.T, sm, sc + L.gM + r0, p.ctl, &s_fail, p.err)) return;
-        if (!group_nucleus(s_rows, nr, V, p.T, p.top_p, sm, sc + L.gS + r0,
-                           sc + L.gH + (size_t)g * kRadixPasses * kRowsPerGroup * 256, p.ctl, &s_fail, p.err))
-            return;
-        if (blockIdx.x == 0 && threadIdx.x < nr) {
-            sc[L.stats + (size_t)(r0 + threadIdx.x) * 2] = sm.kstar[threadIdx.x];
-            sc[L.stats + (size_t)(r0 + threadIdx.x) * 2 + 1] = sm.Sn[threadIdx.x];
-        }
-        __syncthreads();
-    }
-    if (!grid_barrier(p.ctl, &s_fail, p.err)) return;
-    // accept chain per sequence (computed identically by every CTA)
-    for (int b = threadIdx.x; b < p.bs; b += blockDim.x) {
-        const int R = L.R;
-        int a = 0, kind = 1;
-        for (; a < p.B; ++a) {
-            int t = p.tokens[b * p.B + a];
-            if (t < 0 || t >= V) {
-                set_error(p.err, DSPARK_ERR_OOB);
-                t = 0;
-            }
-            const int rp = b * R + a, rq = b * R + p.B + 1 + a;
-            const float mp = ord2f((uint32_t)ldcg_u64(&sc[L.gM + rp]));
-            const unsigned long long ksp = ldcg_u64(&sc[L.stats + 2 * rp]), Sp = ldcg_u64(&sc[L.stats + 2 * rp + 1]);
-            const unsigned long long Ept = weight_of(p.P[((size_t)b * (p.B + 1) + a) * V + t], p.T, mp);
-            const unsigned long long ep = key_of(Ept, t) >= ksp ? Ept : 0ull;
-            unsigned long long eq, Sq;
-            if (p.draft_greedy) {
-                eq = 1;
-                Sq = 1;
-            } else {
-                const float mq = ord2f((uint32_t)ldcg_u64(&sc[L.gM + rq]));
-                const unsigned long long ksq = ldcg_u64(&sc[L.stats + 2 * rq]);
-                Sq = ldcg_u64(&sc[L.stats + 2 * rq + 1]);
-                const unsigned long long Eqt = weight_of(p.ell[((size_t)b * p.B + a) * V + t], p.T, mq);
-                eq = key_of(Eqt, t) >= ksq ? Eqt : 0ull;
-            }
-            const uint32_t U = philox_word(p.seed, (uint32_t)b, p.step, (uint32_t)a, 2u);
-            const unsigned __int128 lhs = (unsigned __int128)U * eq * Sp;
-            const unsigned __int128 rhs = ((unsigned __int128)ep << 32) * Sq;
-            if (!(lhs < rhs)) {
-                kind = 0;
-                break;
-            }
-            if (blockIdx.x == 0) p.out_tokens[b * (p.B + 1) + a] = t;
-        }
-        s_acc[b] = a;
-        s_kind[b] = kind;
-        if (blockIdx.x == 0) {
-            p.accept_len[b] = a;
-            for (int j = a + 1; j <= p.B; ++j) p.out_tokens[b * (p.B + 1) + j] = -1;
-        }
-    }
-    __syncthreads();
-    // one draw per sequence: the residual at the first reject, or the bonus
-    for (int b = 0; b < p.bs; ++b) {
-        const int a = s_acc[b], kind = s_kind[b], R = L.R;
-        const int prow_i = kind ? p.B : a;
-        const int rp = b * R + prow_i;
-        const float *prow = p.P + ((size_t)b * (p.B + 1) + prow_i) * V;
-        const float mp = ord2f((uint32_t)ldcg_u64(&sc[L.gM + rp]));
-        const unsigned long long ksp = ldcg_u64(&sc[L.stats + 2 * rp]), Sp = ldcg_u64(&sc[L.stats + 2 * rp + 1]);
-        const float T = p.T;
-        int32_t *dst = p.out_tokens + b * (p.B + 1) + a;
-        unsigned long long *parts = sc + L.parts + (size_t)b * gridDim.x * 2;
-        if (kind) {
-            const uint32_t W = philox_word(p.seed, (uint32_t)b, p.step, (uint32_t)p.B, 4u) >> 8;
-            auto wf = [&](int v) -> unsigned __int128 {
-                const unsigned long long E = weight_of(prow[v], T, mp);
-                return key_of(E, v) >= ksp ? (unsigned __int128)E : (unsigned __int128)0;
-            };
-            if (!grid_draw(wf, V, W, parts, dst, dsm, p.ctl, &s_fail, p.err)) return;
-        } else {
-            const uint32_t W = philox_word(p.seed, (uint32_t)b, p.step, (uint32_t)a, 3u) >> 8;
-            const int t = min(max(p.tokens[b * p.B + a], 0), V - 1);
-            const int rq = b * R + p.B + 1 + a;
-            const float *qrow = p.ell + ((size_t)b * p.B + a) * V;
-            const bool dg = p.draft_greedy != 0;
-            const float mq = dg ? 0.f : ord2f((uint32_t)ldcg_u64(&sc[L.gM + rq]));
-            const unsigned long long ksq = dg ? 0ull : ldcg_u64(&sc[L.stats + 2 * rq]);
-            const unsigned long long Sq = dg ? 1ull : ldcg_u64(&sc[L.stats + 2 * rq + 1]);
-            auto wf = [&](int v) -> unsigned __int128 {
-                const unsigned long long Ep = weight_of(prow[v], T, mp);
-                const unsigned long long ep = key_of(Ep, v) >= ksp ? Ep : 0ull;
-                unsigned long long eq;
-                if (dg) {
-                    eq = (v == t) ? 1ull : 0ull;
-                } else {
-                    const unsigned long long Eq = weight_of(qrow[v], T, mq);
-                    eq = key_of(Eq, v) >= ksq ? Eq : 0ull;
-                }
-                const unsigned __int128 x = (unsigned __int128)ep * Sq, y = (unsigned __int128)eq * Sp;
-                return x > y ? x - y : (unsigned __int128)0;
-            };
-            if (!grid_draw(wf, V, W, parts, dst, dsm, p.ctl, &s_fail, p.err)) return;
-        }
-    }
-}
-
-// ---------------------------------------------------------------------------
-// Block verification (the oracle's description: rejection_sample_method
-// "block", the published block verification method). Probabilities are the
-// spec's in-nucleus rationals rounded once to double; every residual-mass term
-// is a double (multiply, then subtract) truncated to a multiple of 2^-80, and
-// the masses are exact 128-bit sums, so the decisions match the oracle bit for
-// bit whatever the order of summation.
-// ---------------------------------------------------------------------------
-constexpr int kMaxBlockRows = 17;  // block <= 16, plus the bonus row
-
-DS_DEVINL unsigned __int128 fx80(double x) {
-    if (!(x > 0.0)) return 0;
-    const unsigned long long b = (unsigned long long)__double_as_longlong(x);
-    const int e = (int)((b >> 52) & 0x7FF);
-    if (e == 0) return 0;
-    const unsigned long long m = (b & ((1ull << 52) - 1)) | (1ull << 52);
-    const int sh = e - 995;  // x * 2^80 = m * 2^(e - 1075 + 80)
-    if (sh >= 0) return (unsigned __int128)m << sh;
-    if (sh <= -53) return 0;
-    return (unsigned __int128)(m >> (-sh));
-}
-
-DS_DEVINL double fx80_to_double(unsigned __int128 s) {
-    if (s == 0) return 0.0;
-    const unsigned long long hi = (unsigned long long)(s >> 64), lo = (unsigned long long)s;
-    const int n = hi ? 128 - __clzll((long long)hi) : 64 - __clzll((long long)lo);
-    if (n <= 53) return ldexp((double)lo, -80);
-    return ldexp((double)(unsigned long long)(s >> (n - 53)), n - 53 - 80);
-}
-
-// One row of the spec as in-nucleus probabilities (one-hot for a greedy draft).
-struct BlockRow {
-    const float *row;
-    float m;
-    unsigned long long kstar, S;
-    int onehot;  // -1: a spec row; else the one token of a greedy draft
-    DS_DEVINL double prob(int v, float T) const {
-        if (onehot >= 0) return v == onehot ? 1.0 : 0.0;
-        const unsigned long long E = weight_of(row[v], T, m);
-        const unsigned long long e = key_of(E, v) >= kstar ? E : 0ull;
-        return __ddiv_rn((double)e, (double)S);
-    }
-};
-
-DS_DEVINL unsigned __int128 block_term(const BlockRow &rp, const BlockRow &rq, double pi, float T, int v) {
-    return fx80(__dsub_rn(__dmul_rn(pi, rp.prob(v, T)), rq.prob(v, T)));
-}
-
-// Sum of 128-bit values over the CTA (thread 0 gets the total).
-DS_DEVINL unsigned __int128 block_sum_u128(unsigned __int128 v, DrawSmem &ds_) {
-    unsigned long long lo = (unsigned long long)v, hi = (unsigned long long)(v >> 64);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const unsigned long long lo2 = __shfl_xor_sync(0xffffffffu, lo, o), hi2 = __shfl_xor_sync(0xffffffffu, hi, o);
-        const unsigned long long s = lo + lo2;
-        hi = hi + hi2 + (s < lo ? 1ull : 0ull);
-        lo = s;
-    }
-    __syncthreads();
-    if ((threadIdx.x & 31) == 0) {
-        ds_.lo[threadIdx.x >> 5] = lo;
-        ds_.hi[threadIdx.x >> 5] = hi;
-    }
-    __syncthreads();
-    unsigned __int128 t = 0;
-    if (threadIdx.x == 0)
-        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += ((unsigned __int128)ds_.hi[w] << 64) | ds_.lo[w];
-    return t;
-}
-
-__global__ void __launch_bounds__(kSampThreads, 1) verify_block_kernel(VerifyParams p) {
-    __shared__ NucleusSmem sm;
-    __shared__ DrawSmem dsm;
-    __shared__ volatile int s_fail;
-    __shared__ const float *s_rows[kRowsPerGroup];
-    __shared__ double s_pi[kMaxSampBs][kMaxBlockRows];
-    __shared__ int s_tau[kMaxSampBs];
-    const VerLayout L(p.bs, p.B, gridDim.x, p.draft_greedy);
-    unsigned long long *sc = p.scratch;
-    const int V = p.V, B = p.B, R = L.R;
-    const float T = p.T;
-    if (threadIdx.x == 0) s_fail = 0;
-    for (size_t w = (size_t)blockIdx.x * blockDim.x + threadIdx.x; w < L.total; w += (size_t)gridDim.x * blockDim.x)
-        sc[w] = 0;
-    __threadfence();
-    if (!grid_barrier(p.ctl, &s_fail, p.err)) return;
-    // nucleus statistics of every target and draft row
-    for (int g = 0; g < L.groups; ++g) {
-        const int r0 = g * kRowsPerGroup, nr = min(kRowsPerGroup, L.nrows - r0);
-        if (threadIdx.x < nr) s_rows[threadIdx.x] = ver_row(p, r0 + threadIdx.x);
-        __syncthreads();
-        if (!group_max(s_rows, nr, V, T, sm, sc + L.gM + r0, p.ctl, &s_fail, p.err)) return;
-        if (!group_nucleus(s_rows, nr, V, T, p.top_p, sm, sc + L.gS + r0,
-                           sc + L.gH + (size_t)g * kRadixPasses * kRowsPerGroup * 256, p.ctl, &s_fail, p.err))
-            return;
-        if (blockIdx.x == 0 && threadIdx.x < nr) {
-            sc[L.stats + (size_t)(r0 + threadIdx.x) * 2] = sm.kstar[threadIdx.x];
-            sc[L.stats + (size_t)(r0 + threadIdx.x) * 2 + 1] = sm.Sn[threadIdx.x];
-        }
-        __syncthreads();
-    }
-    if (!grid_barrier(p.ctl, &s_fail, p.err)) return;
-    auto token = [&](int b, int i) -> int {
-        const int t = p.tokens[b * B + i];
-        return (t < 0 || t >= V) ? 0 : t;
-    };
-    auto rowp = [&](int b, int i) -> BlockRow {
-        const int rr = b * R + i;
-        BlockRow r;
-        r.row = p.P + ((size_t)b * (B + 1) + i) * V;
-        r.m = ord2f((uint32_t)ldcg_u64(&sc[L.gM + rr]));
-        r.kstar = ldcg_u64(&sc[L.stats + 2 * rr]);
-        r.S = ldcg_u64(&sc[L.stats + 2 * rr + 1]);
-        r.onehot = -1;
-        return r;
-    };
-    auto rowq = [&](int b, int i) -> BlockRow {
-        BlockRow r;
-        if (p.draft_greedy) {
-            r.row = nullptr;
-            r.m = 0.f;
-            r.kstar = r.S = 0;
-            r.onehot = token(b, i);
-            return r;
-        }
-        const int rr = b * R + B + 1 + i;
-        r.row = p.ell + ((size_t)b * B + i) * V;
-        r.m = ord2f((uint32_t)ldcg_u64(&sc[L.gM + rr]));
-        r.kstar = ldcg_u64(&sc[L.stats + 2 * rr]);
-        r.S = ldcg_u64(&sc[L.stats + 2 * rr + 1]);
-        r.onehot = -1;
-        return r;
-    };
-    // the ratio chain pi_0..pi_B of every sequence (identical in every CTA)
-    for (int b = threadIdx.x; b < p.bs; b += blockDim.x) {
-        double pi = 1.0;
-        s_pi[b][0] = pi;
-        for (int i = 1; i <= B; ++i) {
-            const int t0 = p.tokens[b * B + i - 1];
-            if ((t0 < 0 || t0 >= V) && blockIdx.x == 0) set_error(p.err, DSPARK_ERR_OOB);
-            const int t = token(b, i - 1);
-            const double a = rowp(b, i - 1).prob(t, T), c = rowq(b, i - 1).prob(t, T);
-            if (c == 0.0) {
-                pi = (a > 0.0 && pi > 0.0) ? 1.0 : 0.0;
-            } else {
-                const double x = __dmul_rn(pi, __ddiv_rn(a, c));
-                pi = x < 1.0 ? x : 1.0;
-            }
-            s_pi[b][i] = pi;
-        }
-    }
-    __syncthreads();
-    // residual masses S_{b,i} (i < B) over this CTA's vocabulary pairs, exact
-    {
-        int lo, hi;
-        pair_slice(V / 2, lo, hi);
-        for (int b = 0; b < p.bs; ++b) {
-            for (int i = 0; i < B; ++i) {
-                const BlockRow rp = rowp(b, i), rq = rowq(b, i);
-                const double pi = s_pi[b][i];
-                unsigned __int128 acc = 0;
-                for (int pp = lo + threadIdx.x; pp < hi; pp += blockDim.x)
-                    acc += block_term(rp, rq, pi, T, 2 * pp) + block_term(rp, rq, pi, T, 2 * pp + 1);
-                const unsigned __int128 tot = block_sum_u128(acc, dsm);
-                if (threadIdx.x == 0) {
-                    unsigned long long *dst = sc + L.mass + (((size_t)b * B + i) * gridDim.x + blockIdx.x) * 2;
-                    dst[0] = (unsigned long long)tot;
-                    dst[1] = (unsigned long long)(tot >> 64);
-                }
-            }
-        }
-    }
-    if (!grid_barrier(p.ctl, &s_fail, p.err)) return;
-    auto mass = [&](int b, int i) -> unsigned __int128 {
-        unsigned __int128 S = 0;
-        const unsigned long long *src = sc + L.mass + ((size_t)b * B + i) * gridDim.x * 2;
-        for (int c = 0; c < (int)gridDim.x; ++c)
-            S += ((unsigned __int128)ldcg_u64(&src[2 * c + 1]) << 64) | ldcg_u64(&src[2 * c]);
-        return S;
-    };
-    // decisions: eta_i = (U_i < h_i 2^32), tau = the last accepted position
-    for (int b = threadIdx.x; b < p.bs; b += blockDim.x) {
-        int tau = 0;
-        for (int i = 1; i <= B; ++i) {
-            double h;
-            if (i < B) {
-                const double S = fx80_to_double(mass(b, i));
-                const double den = __dadd_rn(S, __dsub_rn(1.0, s_pi[b][i]));
-                h = den > 0.0 ? __ddiv_rn(S, den) : 0.0;
-            } else {
-                h = s_pi[b][B];
-            }
-            const uint32_t U = philox_word(p.seed, (uint32_t)b, p.step, (uint32_t)(i - 1), 2u);
-            if ((double)U < __dmul_rn(h, 4294967296.0)) tau = i;
-        }
-        s_tau[b] = tau;
-        if (blockIdx.x == 0) {
-            p.accept_len[b] = tau;
-            for (int j = 0; j <= B; ++j) p.out_tokens[b * (B + 1) + j] = j < tau ? token(b, j) : -1;
-        }
-    }
-    __syncthreads();
-    // one draw per sequence: the residual at tau, or the bonus
-    for (int b = 0; b < p.bs; ++b) {
-        const int tau = s_tau[b];
-        int32_t *dst = p.out_tokens + b * (B + 1) + tau;
-        unsigned long long *parts = sc + L.parts + (size_t)b * gridDim.x * 2;
-        const BlockRow rp = rowp(b, tau);
-        const bool plain = tau == B || mass(b, tau) == 0;  // a spec draw from target row tau
-        const uint32_t W = philox_word(p.seed, (uint32_t)b, p.step, (uint32_t)tau, tau == B ? 4u : 3u) >> 8;
-        if (plain) {
-            auto wf = [&](int v) -> unsigned __int128 {
-                const unsigned long long E = weight_of(rp.row[v], T, rp.m);
-                return key_of(E, v) >= rp.kstar ? (unsigned __int128)E : (unsigned __int128)0;
-            };
-            if (!grid_draw(wf, V, W, parts, dst, dsm, p.ctl, &s_fail, p.err)) return;
-        } else {
-            const BlockRow rq = rowq(b, tau);
-            const double pi = s_pi[b][tau];
-            auto wf = [&](int v) -> unsigned __int128 { return block_term(rp, rq, pi, T, v); };
-            if (!grid_draw(wf, V, W, parts, dst, dsm, p.ctl, &s_fail, p.err)) return;
-        }
-    }
-}
-
-// ---------------------------------------------------------------------------
 // Host launchers
 // ---------------------------------------------------------------------------
 // Dynamic shared memory of the rollout's w2 ring for a vocabulary and grid.
@@ -1613,19 +1064,14 @@ size_t rollout_ring_bytes(int V, int grid) {
 }
 
 int sampling_max_grid(int num_sms, int V) {
-    int a = 0, b = 0;
+    int a = 0;
     // the rollout gives each thread at most two vocabulary pairs of its CTA's slice
     if (4 * ((V / 8 + num_sms - 1) / num_sms) > 2 * kSampThreads) return 0;
     const size_t ring = rollout_ring_bytes(V, num_sms);
     if (cudaFuncSetAttribute(rollout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ring) != cudaSuccess)
         return 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, rollout_kernel, kSampThreads, ring) != cudaSuccess) return 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, verify_prob_kernel, kSampThreads, 0) != cudaSuccess)
-        return 0;
-    int c = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c, verify_block_kernel, kSampThreads, 0) != cudaSuccess)
-        return 0;
-    return (a >= 1 && b >= 1 && c >= 1) ? num_sms : 0;
+    return a >= 1 ? num_sms : 0;
 }
 
 // The resident greedy rollout needs r a multiple of 16 up to 256, at most
@@ -1656,25 +1102,6 @@ cudaError_t launch_rollout(const CUtensorMap &w2_map, RolloutParams p, int grid,
                                            args, ResLayout(p.V, grid).total, st);
     return cudaLaunchCooperativeKernel((void *)rollout_kernel, dim3(grid), dim3(kSampThreads), args,
                                        rollout_ring_bytes(p.V, grid), st);
-}
-
-cudaError_t launch_verify(VerifyParams p, int grid, cudaStream_t st) {
-    if (p.verify_mode == DSPARK_GREEDY) {
-        const int rows = p.bs * (p.B + 1);
-        // about two CTAs per SM over all rows
-        const int slices = std::max(1, std::min(64, (2 * grid + rows - 1) / rows));
-        cudaError_t e = launch_pdl(verify_argmax_kernel, dim3(slices, rows), dim3(256), 0, st, p.P, rows, p.V,
-                                   p.scratch, p.err);
-        if (e != cudaSuccess) return e;
-        return launch_pdl(verify_greedy_finalize, dim3((p.bs + 127) / 128), dim3(128), 0, st, p.tokens, p.bs, p.B, p.V,
-                          p.scratch, p.accept_len, p.out_tokens, p.err);
-    }
-    void *args[] = {&p};
-    carveout_max((const void *)verify_block_kernel);
-    carveout_max((const void *)verify_prob_kernel);
-    if (p.verify_mode == DSPARK_BLOCK)
-        return cudaLaunchCooperativeKernel((void *)verify_block_kernel, dim3(grid), dim3(kSampThreads), args, 0, st);
-    return cudaLaunchCooperativeKernel((void *)verify_prob_kernel, dim3(grid), dim3(kSampThreads), args, 0, st);
 }
 
 }  // namespace ds

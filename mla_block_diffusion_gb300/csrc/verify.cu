@@ -1,0 +1,1276 @@
+// Lossless verification of a drafted block against the target's logits.
+//
+// Model cards: the target verifies the 7 drafted tokens in one pass and the
+// output distribution equals the target's ("kimi-k3-dspark-gguf", intro);
+// greedy verification is an argmax match, probabilistic verification samples
+// at temperature T with top-p, and "rejection_sample_method": "block" verifies
+// the drafted block as a unit ("Kimi-K3-DSpark-NVFP4", Quick Start / Sampling
+// options). Block verification follows the published block verification
+// method (Sun et al. 2024).
+//
+// Greedy: the argmax of every target row (lowest id on ties), then the first
+// mismatch.
+//
+// Probabilistic (token by token) and block: every row's exact top-p nucleus
+// first. For a row l at temperature T the spec's weights are
+// E_v = floor(2^32 exp^(l_v / T - m)) with keys K_v = (E_v << 18) | (2^18-1-v);
+// the nucleus is every key >= K*, where K* is the key at which the running
+// weight of the keys in descending order first reaches
+// tau = max(1, floor(S * P32 / 2^32)), S = sum E. One cluster of 8 CTAs holds
+// one row in shared memory and finds K* exactly:
+//   1. a histogram of E over 33 x 64 bins (E's binary exponent and the next 6
+//      bits: every bin holds a contiguous range of E, so whole bins lie above
+//      or below the crossing), merged over the cluster and copied to every
+//      CTA through distributed shared memory; its total is S;
+//   2. the crossing bin (the suffix weight from the top reaches tau);
+//   3. the keys of that bin (a few hundred for flat rows) gathered into one
+//      CTA, which ranks them exactly.
+// When the crossing bin holds more keys than that CTA takes (ties, flat rows
+// of huge vocabularies), refinement levels over 10-bit digits of the key
+// narrow it down instead. No grid-wide barrier and no global atomics. Then one
+// cluster per sequence makes the accept decisions (one lane per position) and
+// the one draw of the step (a weighted pick in id order).
+#include "sampling_spec.cuh"
+
+#include <algorithm>
+
+namespace ds {
+
+// ---------------------------------------------------------------------------
+// Distributed shared memory: loads, stores and an atomic add on the same
+// shared-memory location of another CTA of the cluster. Stores become visible
+// to that CTA after the next cluster barrier both pass.
+// ---------------------------------------------------------------------------
+DS_DEVINL uint32_t peer_addr(const void *local, uint32_t rank) {
+    uint32_t a;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(local)), "r"(rank));
+    return a;
+}
+DS_DEVINL unsigned long long ld_peer_u64(const void *local, uint32_t rank) {
+    unsigned long long v;
+    asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(peer_addr(local, rank)) : "memory");
+    return v;
+}
+DS_DEVINL uint32_t ld_peer_u32(const void *local, uint32_t rank) {
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(peer_addr(local, rank)) : "memory");
+    return v;
+}
+DS_DEVINL void st_peer_u64(void *local, uint32_t rank, unsigned long long v) {
+    asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(peer_addr(local, rank)), "l"(v) : "memory");
+}
+DS_DEVINL void st_peer_u32(void *local, uint32_t rank, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(peer_addr(local, rank)), "r"(v) : "memory");
+}
+DS_DEVINL uint32_t atom_add_peer_u32(void *local, uint32_t rank, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(peer_addr(local, rank)), "r"(v)
+                 : "memory");
+    return old;
+}
+
+// 1D bulk copy global -> shared, completing on an mbarrier (16-byte aligned
+// addresses, size a multiple of 16).
+DS_DEVINL void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+constexpr int kVCl = 8;          // CTAs per cluster
+constexpr int kVThreads = 1024;
+constexpr int kVWarps = kVThreads / 32;
+constexpr int kSub = 32;         // bins per group
+constexpr int kMant0 = 6;        // level 0: binary exponent of E (0..32) x 6 mantissa bits
+constexpr int kBins0 = 33 << kMant0;
+constexpr int kGroups0 = kBins0 / kSub;
+constexpr int kDigitBits = 10;   // refinement levels: 10-bit digits of the key
+constexpr int kBinsK = 1 << kDigitBits;
+constexpr int kGroupsK = kBinsK / kSub;
+constexpr int kHistBins = kBinsK > kBins0 ? kBinsK : kBins0;
+constexpr int kMaxGroups = kHistBins / kSub;
+constexpr int kCandCap = kVThreads;  // keys of the crossing bin ranked in one CTA
+constexpr int kMaxLevels = 8;        // level 0 + at most 5 refinements of the 44-bit residual key
+constexpr int kMassSlices = 16;      // CTAs per block-verification row for the residual masses
+constexpr size_t kStageMax = 200 * 1024;  // largest staging of the draw rows in shared memory
+constexpr int kStatWords = 4;
+
+// Part [lo, hi) of cluster rank c over ids [r0, r1): whole quads from r0, the
+// last CTA to r1.
+DS_DEVINL void cl_part(int r0, int r1, int c, int &lo, int &hi) {
+    const int nq = (r1 - r0) / 4;
+    lo = r0 + 4 * (int)((long long)c * nq / kVCl);
+    hi = c == kVCl - 1 ? r1 : r0 + 4 * (int)((long long)(c + 1) * nq / kVCl);
+}
+__host__ __device__ inline int max_part(int V) { return 4 * ((V / 4 + kVCl - 1) / kVCl) + 4; }
+
+// Level-0 bin of a weight E >= 1: 64 * msb(E) + the 6 bits below the msb.
+DS_DEVINL int coarse_bin(unsigned long long E) {
+    const int msb = 63 - __clzll((long long)E);
+    const unsigned frac = msb >= kMant0 ? (unsigned)(E >> (msb - kMant0)) & 63u : (unsigned)(E << (kMant0 - msb)) & 63u;
+    return (msb << kMant0) + (int)frac;
+}
+// The same from the bits of e (E = weight_bits(e) >= 1): msb(E) = exponent(e) - 95,
+// and for msb >= 6 the 6 bits below it are e's top mantissa bits.
+DS_DEVINL int coarse_bin_bits(float e) {
+    const uint32_t u = __float_as_uint(e);
+    const int ex = (int)(u >> 23);
+    if (ex >= 95 + kMant0) return ((ex - 95) << kMant0) + (int)((u >> (23 - kMant0)) & 63u);
+    return coarse_bin(weight_bits(e));
+}
+// The smallest E of level-0 bin b and the number of low bits of E that vary inside it.
+DS_DEVINL void coarse_range(int b, unsigned long long &lo, int &wbits) {
+    const int msb = b >> kMant0, frac = b & 63;
+    if (msb >= kMant0) {
+        lo = (unsigned long long)(64 + frac) << (msb - kMant0);
+        wbits = msb - kMant0;
+    } else {
+        lo = (unsigned long long)(64 + frac) >> (kMant0 - msb);
+        wbits = 0;
+    }
+}
+
+// First group merged by cluster rank r (groups [gstart(r), gstart(r + 1))).
+DS_DEVINL int gstart(int ngroups, int r) { return r * ngroups / kVCl; }
+
+// Shared memory of the nucleus kernel (dynamic): the row part, this CTA's
+// histogram of the current level (a bin's weight as two 32-bit sums, of E's
+// low 16 bits and of E >> 16: 32-bit shared-memory atomics; a CTA's bin holds
+// fewer than 2^15 elements of E <= 2^32), the merged histogram (every CTA holds
+// all of it), and the gathered keys of the crossing bin (rank 0).
+struct NucLayout {
+    size_t row, h2, hc, mw, mc, gtot, cand, total;
+    __host__ __device__ explicit NucLayout(int V) {
+        size_t o = 0;
+        row = o;
+        o += (size_t)max_part(V) * 4;
+        o = (o + 15) & ~(size_t)15;
+        h2 = o;  // per bin {sum of E & 0xFFFF, sum of E >> 16}
+        o += (size_t)kHistBins * 8;
+        hc = o;
+        o += (size_t)kHistBins * 4;
+        o = (o + 15) & ~(size_t)15;
+        mw = o;
+        o += (size_t)kHistBins * 8;
+        mc = o;
+        o += (size_t)kHistBins * 4;
+        o = (o + 15) & ~(size_t)15;
+        gtot = o;
+        o += (size_t)kMaxGroups * 8;
+        cand = o;
+        o += (size_t)kCandCap * 8;
+        total = o;
+    }
+};
+
+// Per-row refinement state, identical in every CTA of the row's cluster.
+struct NucState {
+    float m;                        // max of l / T
+    int b0, sh, done, d;
+    unsigned long long S, tau, above, lo, pre, Sn, kstar;
+    float elo, ehi;                 // the level-0 crossing bin as a range of e = E / 2^32
+    // crossing of the last level
+    int fbin;
+    unsigned fcount;
+    unsigned long long fw, fabove;
+};
+
+// Inclusive suffix sums over the lanes of a warp (lane l: sum of lanes >= l).
+DS_DEVINL unsigned long long warp_suffix_u64(unsigned long long v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long w = __shfl_down_sync(0xffffffffu, v, o);
+        if (lane + o < 32) v += w;
+    }
+    return v;
+}
+
+// Warp 0: the crossing of the merged histogram (local copies): the largest bin
+// whose suffix weight (itself and every bin above it) reaches `need`. Fills
+// st.fbin / fw / fcount / fabove (weight of the bins above it). At level 0
+// (need == 0) the row's total S and tau = max(1, floor(S * P32 / 2^32)) come
+// from the same group totals first. Lane l holds groups 4l .. 4l + 3. Returns
+// false when the whole histogram weighs less than need.
+DS_DEVINL bool find_crossing(int ngroups, unsigned long long need, unsigned long long P32,
+                             const unsigned long long *gtot, const unsigned long long *mw, const uint32_t *mc,
+                             NucState &st) {
+    const int lane = threadIdx.x & 31;
+    unsigned long long gv[4], tot = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int g = 4 * lane + q;
+        gv[q] = g < ngroups ? gtot[g] : 0ull;
+        tot += gv[q];
+    }
+    const unsigned long long suf = warp_suffix_u64(tot);
+    if (need == 0) {  // level 0: the row's total weight sets tau
+        const unsigned long long S = __shfl_sync(0xffffffffu, suf, 0);
+        const unsigned long long tau = (unsigned long long)(((unsigned __int128)S * P32) >> 32);
+        need = tau < 1 ? 1 : tau;
+        if (lane == 0) {
+            st.S = S;
+            st.tau = need;
+        }
+    }
+    const unsigned mask = __ballot_sync(0xffffffffu, suf >= need);
+    if (!mask) return false;
+    const int L = 31 - __clz((int)mask);
+    // inside lane L: the highest of its groups whose suffix reaches need
+    int g = 0;
+    unsigned long long above_g = 0;
+    if (lane == L) {
+        unsigned long long acc = suf - tot;
+        for (int q = 3; q >= 0; --q) {
+            if (acc + gv[q] >= need) {
+                g = 4 * lane + q;
+                break;
+            }
+            acc += gv[q];
+        }
+        above_g = acc;
+    }
+    g = __shfl_sync(0xffffffffu, g, L);
+    above_g = __shfl_sync(0xffffffffu, above_g, L);
+    const unsigned long long w = mw[g * kSub + lane];
+    const uint32_t c = mc[g * kSub + lane];
+    const unsigned long long suf2 = warp_suffix_u64(w);
+    const unsigned long long need2 = need - above_g;
+    const unsigned mask2 = __ballot_sync(0xffffffffu, suf2 >= need2);
+    if (!mask2) return false;
+    const int j = 31 - __clz((int)mask2);
+    const unsigned long long ex = __shfl_sync(0xffffffffu, suf2 - w, j);
+    const unsigned long long wj = __shfl_sync(0xffffffffu, w, j);
+    const uint32_t cj = __shfl_sync(0xffffffffu, c, j);
+    if (lane == 0) {
+        st.fbin = g * kSub + j;
+        st.fw = wj;
+        st.fcount = cj;
+        st.fabove = above_g + ex;
+    }
+    return true;
+}
+
+// Row gr of the verification: target rows 0..B of every sequence, then (with a
+// sampled draft) its draft rows 0..B-1.
+__host__ __device__ inline int ver_rows_per_seq(const VerifyParams &p) { return p.draft_greedy ? p.B + 1 : 2 * p.B + 1; }
+DS_DEVINL const float *ver_row(const VerifyParams &p, int gr) {
+    const int R = ver_rows_per_seq(p), b = gr / R, j = gr % R;
+    if (j <= p.B) return p.P + ((size_t)b * (p.B + 1) + j) * p.V;
+    return p.ell + ((size_t)b * p.B + (j - p.B - 1)) * p.V;
+}
+// The drafted token scored by row gr (-1 for the bonus row).
+DS_DEVINL int ver_row_token(const VerifyParams &p, int gr) {
+    const int R = ver_rows_per_seq(p), b = gr / R, j = gr % R;
+    const int pos = j < p.B ? j : (j == p.B ? -1 : j - p.B - 1);
+    return pos < 0 ? -1 : p.tokens[b * p.B + pos];
+}
+
+// Per-row statistics, 4 words per row: the ordered max of l / T, K*, S_n (weight
+// of the nucleus), and e_t (the nucleus weight of the row's drafted token: E_t if
+// its key is in the nucleus, else 0; 0 for the bonus row).
+struct RowStats {
+    float m;
+    unsigned long long kstar, Sn, et;
+};
+DS_DEVINL RowStats row_stats(const VerifyParams &p, int gr) {
+    const unsigned long long *s = p.scratch + kStatWords * (size_t)gr;
+    RowStats r;
+    r.m = ord2f((uint32_t)s[0]);
+    r.kstar = s[1];
+    r.Sn = s[2];
+    r.et = s[3];
+    return r;
+}
+
+// Whether element (e, key) lies in the current refinement range: the level-0
+// crossing bin (e in [elo, ehi)) and the known top bits of its residual key.
+DS_DEVINL bool in_range(float e, unsigned long long key, const NucState &st) {
+    if (!(e >= st.elo && e < st.ehi)) return false;
+    return ((key - (st.lo << 18)) >> st.sh) == st.pre;
+}
+
+// Rank 0: the row's statistics (the drafted token's nucleus weight from its logit).
+DS_DEVINL void write_stats(const VerifyParams &p, int gr, int tok, float lt, float T, const NucState &st,
+                           unsigned long long kstar) {
+    unsigned long long et = 0;
+    if (tok >= 0) {
+        const unsigned long long E = weight_of(lt, T, st.m);
+        et = key_of(E, tok) >= kstar ? E : 0ull;
+    }
+    unsigned long long *o = p.scratch + kStatWords * (size_t)gr;
+    o[0] = f2ord(st.m);
+    o[1] = kstar;
+    o[2] = st.Sn;
+    o[3] = et;
+}
+
+// ---------------------------------------------------------------------------
+// Exact top-p nucleus of every row: grid (8, rows), clusters of 8 along x.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kVThreads, 1) nucleus_rows_kernel(VerifyParams p) {
+    extern __shared__ __align__(16) uint8_t vsm[];
+    __shared__ NucState st;
+    __shared__ unsigned long long red[33];
+    __shared__ unsigned long long s_cmax, s_key;
+    __shared__ uint32_t s_cnt, s_n;
+    __shared__ float s_lt;
+    pdl_trigger();
+    const NucLayout NL(p.V);
+    float *yv = (float *)(vsm + NL.row);
+    uint32_t *h2 = (uint32_t *)(vsm + NL.h2), *hc = (uint32_t *)(vsm + NL.hc);
+    unsigned long long *mw = (unsigned long long *)(vsm + NL.mw);
+    uint32_t *mc = (uint32_t *)(vsm + NL.mc);
+    unsigned long long *gtot = (unsigned long long *)(vsm + NL.gtot);
+    unsigned long long *cand = (unsigned long long *)(vsm + NL.cand);
+    const uint32_t rank = cluster_rank();
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const int gr = blockIdx.y;
+    int lo, hi;
+    cl_part(0, p.V, (int)rank, lo, hi);
+    const int n = hi - lo;
+    const float T = p.T;
+    for (int i = t; i < kHistBins; i += kVThreads) {
+        *(uint2 *)(h2 + 2 * i) = make_uint2(0u, 0u);
+        hc[i] = 0;
+    }
+    if (t == 0) s_cnt = 0;
+    pdl_wait();
+    const float *row = ver_row(p, gr);
+    int tok = -1;
+    if (rank == 0 && t == 0) {  // the drafted token's logit, read early
+        tok = ver_row_token(p, gr);
+        if (tok >= p.V || tok < -1) {
+            set_error(p.err, DSPARK_ERR_OOB);
+            tok = 0;
+        }
+        s_lt = tok >= 0 ? row[tok] : 0.f;
+    }
+    // 1. y = l / T into shared memory, this CTA's max
+    const float *rp = row + lo;
+    unsigned long long mx = 0;
+    bool bad = false;
+    for (int j = 4 * t; j < n; j += 4 * kVThreads) {
+        const float4 l = __ldg((const float4 *)(rp + j));
+        const float y0 = div_T(l.x, T), y1 = div_T(l.y, T), y2 = div_T(l.z, T), y3 = div_T(l.w, T);
+        if (!isfinite(y0) || !isfinite(y1) || !isfinite(y2) || !isfinite(y3)) bad = true;
+        *(float4 *)(yv + j) = make_float4(y0, y1, y2, y3);
+        mx = max(mx, (unsigned long long)max(max(f2ord(y0), f2ord(y1)), max(f2ord(y2), f2ord(y3))));
+    }
+    if (bad) set_error(p.err, DSPARK_ERR_BAD_INPUT);
+    mx = block_max_u64(mx, red);
+    if (t == 0) s_cmax = mx;
+    cluster_sync();
+    if (t == 0) {
+        unsigned long long m = 0;
+        for (int r = 0; r < kVCl; ++r) m = max(m, ld_peer_u64(&s_cmax, (uint32_t)r));
+        st.m = ord2f((uint32_t)m);
+        st.above = 0;
+        st.done = 0;
+        st.Sn = 0;
+        st.kstar = ~0ull;
+        st.b0 = 0;
+        st.sh = 0;
+        st.lo = 0;
+        st.pre = 0;
+        st.d = 0;
+        st.elo = 0.f;
+        st.ehi = 0.f;
+    }
+    __syncthreads();
+    // 2. e = exp^(y - m) in place and the level-0 histogram (its total is S)
+    const float m = st.m;
+    for (int j = t; j < n; j += kVThreads) {
+        const float e = exp_hat(__fsub_rn(yv[j], m));
+        yv[j] = e;
+        const unsigned long long E = weight_bits(e);
+        if (E) {
+            const int bin = coarse_bin_bits(e);
+            atomicAdd(&h2[2 * bin], (uint32_t)(E & 0xFFFFu));
+            atomicAdd(&h2[2 * bin + 1], (uint32_t)(E >> 16));
+        }
+    }
+    const unsigned long long P32 = top_p_q32(p.top_p);
+    // 3. merge and copy to every CTA, find the crossing; rank the crossing
+    // bin's keys, or refine further when there are too many of them
+    for (int level = 0; level < kMaxLevels; ++level) {
+        const int ngroups = level ? kGroupsK : kGroups0;
+        if (level > 0) {
+            const int sh = st.sh, d = st.d;
+            for (int j = t; j < n; j += kVThreads) {
+                const float e = yv[j];
+                if (!(e >= st.elo && e < st.ehi)) continue;
+                const unsigned long long E = weight_bits(e);
+                const unsigned long long R = key_of(E, lo + j) - (st.lo << 18);
+                if ((R >> sh) != st.pre) continue;
+                const int bin = (int)((R >> (sh - d)) & ((1ull << d) - 1));
+                atomicAdd(&h2[2 * bin], (uint32_t)(E & 0xFFFFu));
+                atomicAdd(&h2[2 * bin + 1], (uint32_t)(E >> 16));
+                atomicAdd(&hc[bin], 1u);
+            }
+        }
+        cluster_sync();  // A: every CTA's histogram of this level is complete
+        {
+            const int g0 = gstart(ngroups, (int)rank), g1 = gstart(ngroups, (int)rank + 1);
+            if (warp < g1 - g0) {
+                const int bin = (g0 + warp) * kSub + lane;
+                unsigned long long w = 0;
+                uint32_t c = 0;
+#pragma unroll
+                for (int r = 0; r < kVCl; ++r) {
+                    const unsigned long long v = ld_peer_u64(h2 + 2 * bin, (uint32_t)r);
+                    w += (v & 0xFFFFFFFFull) + ((v >> 32) << 16);
+                    if (level > 0) c += ld_peer_u32(hc + bin, (uint32_t)r);
+                }
+                const unsigned long long gsum = warp_sum_u64(w);
+#pragma unroll
+                for (int r = 0; r < kVCl; ++r) {
+                    st_peer_u64(mw + bin, (uint32_t)r, w);
+                    st_peer_u32(mc + bin, (uint32_t)r, c);
+                    if (lane == 0) st_peer_u64(gtot + g0 + warp, (uint32_t)r, gsum);
+                }
+            }
+        }
+        cluster_sync();  // B: every CTA holds the merged histogram; peers are done with this one
+        for (int i = t; i < kHistBins; i += kVThreads) {
+            *(uint2 *)(h2 + 2 * i) = make_uint2(0u, 0u);
+            hc[i] = 0;
+        }
+        if (warp == 0) {
+            const bool found = find_crossing(ngroups, level ? st.tau - st.above : 0ull, P32, gtot, mw, mc, st);
+            if (lane == 0) {
+                if (!found) {  // the weights never reach tau (non-finite input): an empty nucleus
+                    set_error(p.err, DSPARK_ERR_BAD_INPUT);
+                    st.done = 2;
+                } else {
+                    st.above += st.fabove;
+                    if (level == 0) {
+                        st.b0 = st.fbin;
+                        int wb;
+                        coarse_range(st.b0, st.lo, wb);
+                        st.sh = wb + 18;
+                        st.pre = 0;
+                        // E in [lo, lo + 2^wb) <=> e in [lo, lo + 2^wb) / 2^32 (exact in fp32)
+                        st.elo = __uint_as_float(0x2F800000u) * (float)st.lo;  // 2^-32 * lo
+                        st.ehi = __uint_as_float(0x2F800000u) * (float)(st.lo + (1ull << wb));
+                    } else {
+                        st.pre = (st.pre << st.d) | (unsigned long long)st.fbin;
+                        st.sh -= st.d;
+                    }
+                    st.d = st.sh < kDigitBits ? st.sh : kDigitBits;
+                    if (level > 0 && (st.fcount == 1 || st.sh == 0)) {
+                        st.Sn = st.above + st.fw;
+                        st.done = 1;
+                    }
+                }
+            }
+        }
+        __syncthreads();
+        if (st.done) break;
+        if (level == 0) {
+            // gather the crossing bin's keys into rank 0
+            for (int j = t; j < n; j += kVThreads) {
+                const float e = yv[j];
+                if (!(e >= st.elo && e < st.ehi)) continue;
+                const uint32_t slot = atom_add_peer_u32(&s_cnt, 0u, 1u);
+                if (slot < (uint32_t)kCandCap) st_peer_u64(cand + slot, 0u, key_of(weight_bits(e), lo + j));
+            }
+            cluster_sync();  // G: every key is in rank 0
+            if (t == 0) s_n = ld_peer_u32(&s_cnt, 0u);
+            cluster_sync();  // every CTA has read the count (rank 0 may leave afterwards)
+            const uint32_t N = s_n;
+            if (N <= (uint32_t)kCandCap) {
+                if (rank == 0) {
+                    // the keys in descending order (bitonic sort; the unused slots hold 0,
+                    // below every key), then K* is the key whose running weight reaches need
+                    if (t >= (int)N) cand[t] = 0ull;
+                    __syncthreads();
+                    for (int k = 2; k <= kCandCap; k <<= 1) {
+                        for (int j = k >> 1; j > 0; j >>= 1) {
+                            const int q = t ^ j;
+                            if (q > t) {
+                                const unsigned long long x = cand[t], y = cand[q];
+                                const bool desc = (t & k) == 0;
+                                if (desc ? x < y : x > y) {
+                                    cand[t] = y;
+                                    cand[q] = x;
+                                }
+                            }
+                            __syncthreads();
+                        }
+                    }
+                    const unsigned long long k = cand[t], E = k >> 18;
+                    // inclusive prefix of E over the sorted keys
+                    unsigned long long inc = E;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const unsigned long long w = __shfl_up_sync(0xffffffffu, inc, o);
+                        if (lane >= o) inc += w;
+                    }
+                    if (lane == 31) red[warp] = inc;
+                    __syncthreads();
+                    if (warp == 0) {
+                        unsigned long long x = red[lane], xi = x;
+#pragma unroll
+                        for (int o = 1; o < 32; o <<= 1) {
+                            const unsigned long long w = __shfl_up_sync(0xffffffffu, xi, o);
+                            if (lane >= o) xi += w;
+                        }
+                        red[lane] = xi - x;  // exclusive prefix of the warp totals
+                    }
+                    __syncthreads();
+                    inc += red[warp];
+                    const unsigned long long need = st.tau - st.above;
+                    if (E && inc >= need && inc - E < need) {
+                        st.kstar = k;
+                        st.Sn = st.above + inc;
+                    }
+                    __syncthreads();
+                    if (t == 0) write_stats(p, gr, tok, s_lt, T, st, st.kstar);
+                }
+                return;
+            }
+        }
+    }
+    if (!st.done && t == 0) set_error(p.err, DSPARK_ERR_BAD_INPUT);
+    // the one key of the final bin: its CTA stores it in rank 0's shared memory
+    if (st.done == 1) {
+        for (int j = t; j < n; j += kVThreads) {
+            const float e = yv[j];
+            if (!(e >= st.elo && e < st.ehi)) continue;
+            const unsigned long long key = key_of(weight_bits(e), lo + j);
+            if (in_range(e, key, st)) st_peer_u64(&s_key, 0u, key);
+        }
+    }
+    cluster_sync();  // the key is in rank 0; no CTA leaves while a peer may still read its shared memory
+    if (rank == 0 && t == 0) write_stats(p, gr, tok, s_lt, T, st, st.done == 1 ? s_key : ~0ull);
+}
+
+// ---------------------------------------------------------------------------
+// One weighted pick by the CTAs of a cluster over ids [r0, r1): the smallest v
+// whose running weight base + sum_{r0 <= u <= v} weight(u) exceeds the target.
+// With W24 >= 0 the range is the whole draw (base 0) and the target is
+// floor(total * W24 / 2^24) of the range's total; otherwise `target` is given.
+// Every warp sums a contiguous segment of the CTA's part (lanes strided, so
+// the reads are coalesced), the cluster learns each CTA's total through
+// distributed shared memory, and the one warp whose segment holds the target
+// walks it lane-contiguously. Writes v to *out (nothing when no weight
+// reaches the target).
+// ---------------------------------------------------------------------------
+struct DrawScan {
+    unsigned long long wlo[kVWarps], whi[kVWarps];  // warp totals, then their exclusive prefixes
+    unsigned long long tlo, thi;   // this CTA's total
+    unsigned long long blo, bhi;   // weight before this CTA (plus base)
+    unsigned long long glo, ghi;   // the target
+};
+
+DS_DEVINL void u128_split(unsigned __int128 v, unsigned long long &lo, unsigned long long &hi) {
+    lo = (unsigned long long)v;
+    hi = (unsigned long long)(v >> 64);
+}
+DS_DEVINL unsigned __int128 u128_join(unsigned long long lo, unsigned long long hi) {
+    return ((unsigned __int128)hi << 64) | lo;
+}
+DS_DEVINL unsigned __int128 shfl_u128(unsigned __int128 v, int src) {
+    unsigned long long lo, hi;
+    u128_split(v, lo, hi);
+    return u128_join(__shfl_sync(0xffffffffu, lo, src), __shfl_sync(0xffffffffu, hi, src));
+}
+DS_DEVINL unsigned __int128 warp_sum_u128(unsigned __int128 v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        unsigned long long lo, hi;
+        u128_split(v, lo, hi);
+        v += u128_join(__shfl_xor_sync(0xffffffffu, lo, o), __shfl_xor_sync(0xffffffffu, hi, o));
+    }
+    return v;
+}
+// Inclusive prefix over the lanes (lane order).
+DS_DEVINL unsigned __int128 warp_incl_u128(unsigned __int128 v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        unsigned long long lo, hi;
+        u128_split(v, lo, hi);
+        const unsigned __int128 w = u128_join(__shfl_up_sync(0xffffffffu, lo, o), __shfl_up_sync(0xffffffffu, hi, o));
+        if (lane >= o) v += w;
+    }
+    return v;
+}
+
+template <class WF>
+DS_DEVINL void cluster_pick(WF weight, int r0, int r1, long long W24, unsigned __int128 base, unsigned __int128 target,
+                            int32_t *out, DrawScan &ds_) {
+    const uint32_t rank = cluster_rank();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int lo, hi;
+    cl_part(r0, r1, (int)rank, lo, hi);
+    const int n = hi - lo;
+    const int segw = 32 * ((n + 32 * kVWarps - 1) / (32 * kVWarps));
+    const int s0 = lo + warp * segw, s1 = min(hi, s0 + segw);
+    unsigned __int128 mine = 0;
+    for (int v = s0 + lane; v < s1; v += 32) mine += weight(v);
+    mine = warp_sum_u128(mine);
+    if (lane == 0) u128_split(mine, ds_.wlo[warp], ds_.whi[warp]);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned __int128 acc = 0;
+        for (int w = 0; w < kVWarps; ++w) {
+            const unsigned __int128 x = u128_join(ds_.wlo[w], ds_.whi[w]);
+            u128_split(acc, ds_.wlo[w], ds_.whi[w]);
+            acc += x;
+        }
+        u128_split(acc, ds_.tlo, ds_.thi);
+    }
+    cluster_sync();  // every CTA's total is in its shared memory
+    if (threadIdx.x == 0) {
+        unsigned __int128 before = 0, total = 0;
+        for (int r = 0; r < kVCl; ++r) {
+            const unsigned __int128 x = u128_join(ld_peer_u64(&ds_.tlo, (uint32_t)r), ld_peer_u64(&ds_.thi, (uint32_t)r));
+            if (r < (int)rank) before += x;
+            total += x;
+        }
+        const unsigned __int128 tg = W24 >= 0 ? (total * (unsigned __int128)(W24 & 0xFFFFFF)) >> 24 : target;
+        u128_split(base + before, ds_.blo, ds_.bhi);
+        u128_split(tg, ds_.glo, ds_.ghi);
+    }
+    cluster_sync();  // peers have read this CTA's total
+    const unsigned __int128 tg = u128_join(ds_.glo, ds_.ghi);
+    const unsigned __int128 start = u128_join(ds_.blo, ds_.bhi) + u128_join(ds_.wlo[warp], ds_.whi[warp]);
+    if (s0 < s1 && start <= tg && tg < start + mine) {
+        // this warp's segment holds the target: lanes take contiguous runs
+        const int per = (s1 - s0 + 31) / 32;
+        const int v0 = s0 + lane * per, v1 = min(s1, v0 + per);
+        unsigned __int128 run = 0;
+        for (int v = v0; v < v1; ++v) run += weight(v);
+        const unsigned __int128 incl = warp_incl_u128(run);
+        const unsigned __int128 st0 = start + incl - run;
+        if (v0 < v1 && st0 <= tg && tg < st0 + run) {
+            unsigned __int128 cum = st0;
+            for (int v = v0; v < v1; ++v) {
+                cum += weight(v);
+                if (cum > tg) {
+                    *out = v;
+                    break;
+                }
+            }
+        }
+    }
+}
+
+// A draw over a whole vocabulary of V ids.
+template <class WF>
+DS_DEVINL void cluster_draw(WF weight, int V, uint32_t W24, int32_t *out, DrawScan &ds_) {
+    cluster_pick(weight, 0, V, (long long)(W24 & 0xFFFFFFu), 0, 0, out, ds_);
+}
+
+// Stage this CTA's part of up to two rows (cl_part of [0, V)) into shared
+// memory with bulk copies; returns false if the copies did not land in time.
+DS_DEVINL bool stage_rows(float *dst0, const float *row0, float *dst1, const float *row1, int V, uint64_t *bar,
+                          volatile int *s_fail) {
+    int lo, hi;
+    cl_part(0, V, (int)cluster_rank(), lo, hi);
+    const uint32_t bytes = (uint32_t)(hi - lo) * 4u;
+    if (threadIdx.x == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(bar, bytes * (row1 ? 2u : 1u));
+        constexpr uint32_t kPiece = 32768;
+        for (uint32_t o = 0; o < bytes; o += kPiece) {
+            const uint32_t b = bytes - o < kPiece ? bytes - o : kPiece;
+            bulk_g2s((uint8_t *)dst0 + o, (const uint8_t *)(row0 + lo) + o, b, bar);
+            if (row1) bulk_g2s((uint8_t *)dst1 + o, (const uint8_t *)(row1 + lo) + o, b, bar);
+        }
+    }
+    __syncthreads();
+    bool ok = mbar_wait_bounded(bar, 0, s_fail);
+    __syncthreads();
+    ok = ok && !*s_fail;
+    if (!ok && threadIdx.x == 0) mbar_drain(bar, 0);  // copies in flight land before the buffer is abandoned
+    __syncthreads();
+    return ok;
+}
+
+// A weighted pick by one CTA over ids [r0, r1): the smallest v whose running
+// weight base + sum_{r0 <= u <= v} weight(u) exceeds `target` (warp segments
+// summed with coalesced reads; the warp holding the target walks it
+// lane-contiguously). Writes v to *out (nothing when no weight reaches it).
+template <class WF>
+DS_DEVINL void cta_pick(WF weight, int r0, int r1, unsigned __int128 base, unsigned __int128 target, int32_t *out,
+                        DrawScan &ds_) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = (int)(blockDim.x >> 5);
+    const int n = r1 - r0;
+    const int segw = 32 * ((n + 32 * nw - 1) / (32 * nw));
+    const int s0 = r0 + warp * segw, s1 = min(r1, s0 + segw);
+    unsigned __int128 mine = 0;
+    for (int v = s0 + lane; v < s1; v += 32) mine += weight(v);
+    mine = warp_sum_u128(mine);
+    if (lane == 0) u128_split(mine, ds_.wlo[warp], ds_.whi[warp]);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned __int128 acc = base;
+        for (int w = 0; w < nw; ++w) {
+            const unsigned __int128 x = u128_join(ds_.wlo[w], ds_.whi[w]);
+            u128_split(acc, ds_.wlo[w], ds_.whi[w]);
+            acc += x;
+        }
+    }
+    __syncthreads();
+    const unsigned __int128 start = u128_join(ds_.wlo[warp], ds_.whi[warp]);
+    if (s0 < s1 && start <= target && target < start + mine) {
+        const int per = (s1 - s0 + 31) / 32;
+        const int v0 = s0 + lane * per, v1 = min(s1, v0 + per);
+        unsigned __int128 run = 0;
+        for (int v = v0; v < v1; ++v) run += weight(v);
+        const unsigned __int128 incl = warp_incl_u128(run);
+        const unsigned __int128 st0 = start + incl - run;
+        if (v0 < v1 && st0 <= target && target < st0 + run) {
+            unsigned __int128 cum = st0;
+            for (int v = v0; v < v1; ++v) {
+                cum += weight(v);
+                if (cum > target) {
+                    *out = v;
+                    break;
+                }
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Token-by-token probabilistic verification. Accept t_i iff
+// U * Eq_t * Sp < 2^32 * Ep_t * Sq (U 32-bit, purpose 2); on the first reject
+// draw from max(0, Ep_v Sq - Eq_v Sp) (purpose 3), after 7 accepts draw the
+// bonus from the last target row (purpose 4). With a greedy draft q is one-hot
+// on the drafted token (Eq = Sq = 1). The accept test of every position uses
+// only its rows' statistics, so the B tests run at once (one lane each) and
+// the first failing one ends the run. The draw: kDrawSlices CTAs per sequence
+// sum the weights of their vocabulary slices (every SM takes part), then one
+// CTA per sequence picks inside the slice that holds the target.
+// ---------------------------------------------------------------------------
+constexpr int kDrawSlices = 128;
+
+// Warp 0: the number of accepted drafts of sequence b (B if all), and this
+// lane's drafted token (position = lane).
+DS_DEVINL int token_accepts(const VerifyParams &p, int b, int &t) {
+    const int a = threadIdx.x & 31, B = p.B, V = p.V, R = ver_rows_per_seq(p);
+    bool acc = false;
+    t = 0;
+    if (a < B) {
+        t = p.tokens[b * B + a];
+        if (t < 0 || t >= V) {
+            set_error(p.err, DSPARK_ERR_OOB);
+            t = 0;
+        }
+        const RowStats sp = row_stats(p, b * R + a);
+        unsigned long long eq = 1, Sq = 1;
+        if (!p.draft_greedy) {
+            const RowStats sq = row_stats(p, b * R + B + 1 + a);
+            eq = sq.et;
+            Sq = sq.Sn;
+        }
+        const uint32_t U = philox_word(p.seed, (uint32_t)b, p.step, (uint32_t)a, 2u);
+        const unsigned __int128 lhs = (unsigned __int128)U * eq * sp.Sn;
+        const unsigned __int128 rhs = ((unsigned __int128)sp.et << 32) * Sq;
+        acc = lhs < rhs;
+    }
+    const unsigned rej = __ballot_sync(0xffffffffu, a < B && !acc);
+    return rej ? __ffs((int)rej) - 1 : B;
+}
+
+// The draw's weight of id v after `a` accepts: the bonus row's nucleus weight
+// (a == B) or the residual max(0, Ep_v Sq - Eq_v Sp) at position a.
+struct TokenDraw {
+    const float *prow, *qrow;
+    float T, mp, mq;
+    unsigned long long ksp, Sp, ksq, Sq;
+    int bonus, dg, t;
+    DS_DEVINL unsigned __int128 operator()(int v) const {
+        const unsigned long long Ep = weight_of(prow[v], T, mp);
+        const unsigned long long ep = key_of(Ep, v) >= ksp ? Ep : 0ull;
+        if (bonus) return ep;
+        unsigned long long eq;
+        if (dg) {
+            eq = (v == t) ? 1ull : 0ull;
+        } else {
+            const unsigned long long Eq = weight_of(qrow[v], T, mq);
+            eq = key_of(Eq, v) >= ksq ? Eq : 0ull;
+        }
+        const unsigned __int128 x = (unsigned __int128)ep * Sq, y = (unsigned __int128)eq * Sp;
+        return x > y ? x - y : (unsigned __int128)0;
+    }
+};
+DS_DEVINL TokenDraw token_draw(const VerifyParams &p, int b, int a) {
+    const int B = p.B, V = p.V, R = ver_rows_per_seq(p);
+    TokenDraw d;
+    d.bonus = a == B;
+    d.dg = p.draft_greedy;
+    d.T = p.T;
+    const int pi = d.bonus ? B : a;
+    d.prow = p.P + ((size_t)b * (B + 1) + pi) * V;
+    const RowStats sp = row_stats(p, b * R + pi);
+    d.mp = sp.m;
+    d.ksp = sp.kstar;
+    d.Sp = sp.Sn;
+    d.qrow = p.ell + ((size_t)b * B + (d.bonus ? 0 : a)) * V;
+    d.t = d.bonus ? 0 : min(max(p.tokens[b * B + a], 0), V - 1);
+    d.mq = 0.f;
+    d.ksq = 0;
+    d.Sq = 1;
+    if (!d.bonus && !d.dg) {
+        const RowStats sq = row_stats(p, b * R + B + 1 + a);
+        d.mq = sq.m;
+        d.ksq = sq.kstar;
+        d.Sq = sq.Sn;
+    }
+    return d;
+}
+// Slice x of kDrawSlices over [0, V).
+DS_DEVINL void draw_slice(int V, int x, int &lo, int &hi) {
+    lo = (int)((long long)V * x / kDrawSlices);
+    hi = (int)((long long)V * (x + 1) / kDrawSlices);
+}
+// Partial sums of the draws: [b][slice] * 2 words, after the row statistics and the block masses.
+DS_DEVINL unsigned long long *draw_parts(const VerifyParams &p) {
+    return p.scratch + kStatWords * (size_t)p.bs * (2 * p.B + 1) + (size_t)p.bs * p.B * kMassSlices * 2;
+}
+
+// grid (kDrawSlices, bs): every CTA sums the draw weights of its slice; the
+// last CTA of a sequence to finish (a counter in the workspace, returned to
+// zero by that CTA) makes the decisions, writes the outputs, finds the slice
+// that holds the draw's target floor(total * W24 / 2^24) and picks inside it.
+// No CTA waits for another.
+__global__ void __launch_bounds__(256) verify_token_draw_kernel(VerifyParams p) {
+    __shared__ DrawScan dsm;
+    __shared__ int s_a, s_last, s_slice;
+    __shared__ unsigned long long s_blo, s_bhi, s_tlo, s_thi;
+    pdl_trigger();
+    pdl_wait();
+    const int b = blockIdx.y, B = p.B;
+    int t = 0;
+    if (threadIdx.x < 32) {
+        const int a = token_accepts(p, b, t);
+        if (threadIdx.x == 0) s_a = a;
+    }
+    __syncthreads();
+    const int a = s_a;
+    const TokenDraw d = token_draw(p, b, a);
+    int lo, hi;
+    draw_slice(p.V, blockIdx.x, lo, hi);
+    unsigned __int128 acc = 0;
+    for (int v = lo + threadIdx.x; v < hi; v += blockDim.x) acc += d(v);
+    acc = warp_sum_u128(acc);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) u128_split(acc, dsm.wlo[warp], dsm.whi[warp]);
+    __syncthreads();
+    unsigned long long *parts = draw_parts(p) + (size_t)b * kDrawSlices * 2;
+    if (threadIdx.x == 0) {
+        unsigned __int128 tot = 0;
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += u128_join(dsm.wlo[w], dsm.whi[w]);
+        parts[2 * blockIdx.x] = (unsigned long long)tot;
+        parts[2 * blockIdx.x + 1] = (unsigned long long)(tot >> 64);
+        __threadfence();
+        const unsigned old = atomicAdd(p.draw_count + b, 1u);
+        s_last = old == (unsigned)(kDrawSlices - 1);
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    if (threadIdx.x == 0) p.draw_count[b] = 0u;
+    // the outputs
+    if (threadIdx.x < 32) {
+        if (lane < a) p.out_tokens[b * (B + 1) + lane] = t;
+        if (lane > a && lane <= B) p.out_tokens[b * (B + 1) + lane] = -1;
+        if (lane == 0) p.accept_len[b] = a;
+    }
+    // the slice totals' exclusive prefix (thread c: slice c), the target and its slice
+    const int c = threadIdx.x;
+    unsigned __int128 x = 0;
+    if (c < kDrawSlices) x = u128_join(ldcg_u64(parts + 2 * c), ldcg_u64(parts + 2 * c + 1));
+    const unsigned __int128 inc = warp_incl_u128(x);
+    if (lane == 31) u128_split(inc, dsm.wlo[warp], dsm.whi[warp]);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned __int128 s0 = 0;
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
+            const unsigned __int128 y = u128_join(dsm.wlo[w], dsm.whi[w]);
+            u128_split(s0, dsm.wlo[w], dsm.whi[w]);
+            s0 += y;
+        }
+        const uint32_t W = philox_word(p.seed, (uint32_t)b, p.step, (uint32_t)a, a == B ? 4u : 3u) >> 8;
+        u128_split((s0 * (unsigned __int128)(W & 0xFFFFFFu)) >> 24, s_tlo, s_thi);
+        s_slice = kDrawSlices - 1;
+    }
+    __syncthreads();
+    const unsigned __int128 tg = u128_join(s_tlo, s_thi);
+    const unsigned __int128 ex = u128_join(dsm.wlo[warp], dsm.whi[warp]) + inc - x;
+    if (c < kDrawSlices && x > 0 && ex <= tg && tg < ex + x) {
+        s_slice = c;
+        u128_split(ex, s_blo, s_bhi);
+    }
+    __syncthreads();
+    draw_slice(p.V, s_slice, lo, hi);
+    cta_pick(d, lo, hi, u128_join(s_blo, s_bhi), tg, p.out_tokens + b * (B + 1) + a, dsm);
+}
+
+// ---------------------------------------------------------------------------
+// Block verification (rejection_sample_method "block"; the published block
+// verification method). Probabilities are the spec's in-nucleus rationals
+// rounded once to double; every residual-mass term is a double (multiply,
+// then subtract) truncated to a multiple of 2^-80, and the masses are exact
+// 128-bit sums, so the decisions do not depend on the order of summation.
+// ---------------------------------------------------------------------------
+DS_DEVINL unsigned __int128 fx80(double x) {
+    if (!(x > 0.0)) return 0;
+    const unsigned long long bits = (unsigned long long)__double_as_longlong(x);
+    const int e = (int)((bits >> 52) & 0x7FF);
+    if (e == 0) return 0;
+    const unsigned long long mnt = (bits & ((1ull << 52) - 1)) | (1ull << 52);
+    const int sh = e - 995;  // x * 2^80 = mnt * 2^(e - 1075 + 80)
+    if (sh >= 0) return (unsigned __int128)mnt << sh;
+    if (sh <= -53) return 0;
+    return (unsigned __int128)(mnt >> (-sh));
+}
+
+DS_DEVINL double fx80_to_double(unsigned __int128 s) {
+    if (s == 0) return 0.0;
+    const unsigned long long hi = (unsigned long long)(s >> 64), lo = (unsigned long long)s;
+    const int n = hi ? 128 - __clzll((long long)hi) : 64 - __clzll((long long)lo);
+    if (n <= 53) return ldexp((double)lo, -80);
+    return ldexp((double)(unsigned long long)(s >> (n - 53)), n - 53 - 80);
+}
+
+// One row of the spec as in-nucleus probabilities (one-hot for a greedy draft).
+struct BlockRow {
+    const float *row;
+    float m;
+    unsigned long long kstar, S;
+    int onehot;  // -1: a spec row; else the one token of a greedy draft
+    DS_DEVINL double prob(int v, float T) const {
+        if (onehot >= 0) return v == onehot ? 1.0 : 0.0;
+        const unsigned long long E = weight_of(row[v], T, m);
+        const unsigned long long e = key_of(E, v) >= kstar ? E : 0ull;
+        return e ? __ddiv_rn((double)e, (double)S) : 0.0;
+    }
+};
+
+DS_DEVINL unsigned __int128 block_term(const BlockRow &rp, const BlockRow &rq, double pi, float T, int v) {
+    return fx80(__dsub_rn(__dmul_rn(pi, rp.prob(v, T)), rq.prob(v, T)));
+}
+
+DS_DEVINL int block_token(const VerifyParams &p, int b, int i) {
+    const int t = p.tokens[b * p.B + i];
+    return (t < 0 || t >= p.V) ? 0 : t;
+}
+DS_DEVINL BlockRow block_rowp(const VerifyParams &p, int b, int i) {
+    BlockRow r;
+    r.row = p.P + ((size_t)b * (p.B + 1) + i) * p.V;
+    const RowStats s = row_stats(p, b * ver_rows_per_seq(p) + i);
+    r.m = s.m;
+    r.kstar = s.kstar;
+    r.S = s.Sn;
+    r.onehot = -1;
+    return r;
+}
+DS_DEVINL BlockRow block_rowq(const VerifyParams &p, int b, int i) {
+    BlockRow r;
+    if (p.draft_greedy) {
+        r.row = nullptr;
+        r.m = 0.f;
+        r.kstar = r.S = 0;
+        r.onehot = block_token(p, b, i);
+        return r;
+    }
+    r.row = p.ell + ((size_t)b * p.B + i) * p.V;
+    const RowStats s = row_stats(p, b * ver_rows_per_seq(p) + p.B + 1 + i);
+    r.m = s.m;
+    r.kstar = s.kstar;
+    r.S = s.Sn;
+    r.onehot = -1;
+    return r;
+}
+constexpr int kMaxBlockRows = 17;  // block <= 16, plus the bonus row
+
+// Warp 0: pi_0..pi_B of sequence b into pis[] (pi_0 = 1,
+// pi_k = min(pi_{k-1} p_{k-1}(t_k) / q_{k-1}(t_k), 1)); the per-position ratios
+// come from the rows' statistics (one lane each), the chain from lane 0.
+DS_DEVINL void block_pis(const VerifyParams &p, int b, double *pis) {
+    const int lane = threadIdx.x & 31, B = p.B, R = ver_rows_per_seq(p);
+    double a = 0.0, c = 1.0;
+    if (lane < B) {
+        const RowStats sp = row_stats(p, b * R + lane);
+        a = sp.et ? __ddiv_rn((double)sp.et, (double)sp.Sn) : 0.0;
+        if (!p.draft_greedy) {
+            const RowStats sq = row_stats(p, b * R + B + 1 + lane);
+            c = sq.et ? __ddiv_rn((double)sq.et, (double)sq.Sn) : 0.0;
+        }
+    }
+    double pi = 1.0;
+    if (lane == 0) pis[0] = 1.0;
+    for (int k = 1; k <= B; ++k) {
+        const double ak = __shfl_sync(0xffffffffu, a, k - 1), ck = __shfl_sync(0xffffffffu, c, k - 1);
+        if (ck == 0.0) {
+            pi = (ak > 0.0 && pi > 0.0) ? 1.0 : 0.0;
+        } else {
+            const double x = __dmul_rn(pi, __ddiv_rn(ak, ck));
+            pi = x < 1.0 ? x : 1.0;
+        }
+        if (lane == 0) pis[k] = pi;
+    }
+}
+// Partial residual masses: [(b * B + i) * kMassSlices + slice] * 2 words, after the row statistics.
+DS_DEVINL unsigned long long *block_masses(const VerifyParams &p) {
+    return p.scratch + kStatWords * (size_t)p.bs * ver_rows_per_seq(p);
+}
+
+// Residual masses S_i = sum_x max(pi_i p_i(x) - q_i(x), 0) for i < B: grid
+// (kMassSlices, bs * B), one vocabulary slice per CTA.
+__global__ void __launch_bounds__(256) verify_block_mass_kernel(VerifyParams p) {
+    __shared__ double s_pis[kMaxBlockRows];
+    __shared__ unsigned long long rlo[8], rhi[8];
+    pdl_trigger();
+    pdl_wait();
+    const int b = blockIdx.y / p.B, i = blockIdx.y % p.B;
+    if (threadIdx.x < 32) {
+        if (blockIdx.x == 0 && i == 0 && threadIdx.x < p.B) {
+            const int t0 = p.tokens[b * p.B + threadIdx.x];
+            if (t0 < 0 || t0 >= p.V) set_error(p.err, DSPARK_ERR_OOB);
+        }
+        block_pis(p, b, s_pis);
+    }
+    __syncthreads();
+    const double pi = s_pis[i];
+    const BlockRow rp = block_rowp(p, b, i), rq = block_rowq(p, b, i);
+    const int np = p.V / 2;
+    const int lo = (int)((long long)blockIdx.x * np / gridDim.x), hi = (int)((long long)(blockIdx.x + 1) * np / gridDim.x);
+    unsigned __int128 acc = 0;
+    for (int pp = lo + threadIdx.x; pp < hi; pp += blockDim.x)
+        acc += block_term(rp, rq, pi, p.T, 2 * pp) + block_term(rp, rq, pi, p.T, 2 * pp + 1);
+    acc = warp_sum_u128(acc);
+    if ((threadIdx.x & 31) == 0) u128_split(acc, rlo[threadIdx.x >> 5], rhi[threadIdx.x >> 5]);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned __int128 tot = 0;
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += u128_join(rlo[w], rhi[w]);
+        unsigned long long *dst = block_masses(p) + ((size_t)blockIdx.y * gridDim.x + blockIdx.x) * 2;
+        dst[0] = (unsigned long long)tot;
+        dst[1] = (unsigned long long)(tot >> 64);
+    }
+}
+
+// Decisions and the one draw of block verification: grid (8, bs), clusters of 8.
+// eta_i = (U_i < h_i 2^32) with h_i = S_i / (S_i + 1 - pi_i) (i < B), h_B = pi_B;
+// tau = the last accepted position; then a draw from max(pi_tau p_tau - q_tau, 0)
+// (purpose 3), from target row tau when that residual is empty, or the bonus
+// (purpose 4) when tau = B. The residual draw's total and its slice totals are
+// the masses of position tau, so only the slice that holds the target is walked.
+__global__ void __launch_bounds__(kVThreads, 1) verify_block_final_kernel(VerifyParams p) {
+    extern __shared__ __align__(16) float tsm[];  // the staged target row (when p.stage)
+    __shared__ DrawScan dsm;
+    __shared__ double s_pis[kMaxBlockRows];
+    __shared__ int s_tau, s_plain, s_slice;
+    __shared__ unsigned long long s_rlo, s_rhi, s_tlo, s_thi;
+    __shared__ __align__(8) uint64_t s_bar;
+    __shared__ volatile int s_fail;
+    pdl_trigger();
+    if (threadIdx.x == 0) s_fail = 0;
+    pdl_wait();
+    const int b = blockIdx.y, B = p.B, V = p.V;
+    const uint32_t rank = cluster_rank();
+    const unsigned long long *ms = block_masses(p);
+    if (threadIdx.x < 32) {
+        block_pis(p, b, s_pis);
+        // masses of positions 0..B-1 (lane i) and the decisions (one lane each)
+        const int i = threadIdx.x;
+        unsigned __int128 Si = 0;
+        if (i < B) {
+            const unsigned long long *src = ms + ((size_t)(b * B + i) * kMassSlices) * 2;
+            for (int c = 0; c < kMassSlices; ++c) Si += u128_join(src[2 * c], src[2 * c + 1]);
+        }
+        __syncwarp();
+        bool eta = false;
+        if (i >= 1 && i <= B) {
+            const double pi_i = s_pis[i];
+            double h;
+            if (i < B) {
+                const double S = fx80_to_double(Si);
+                const double den = __dadd_rn(S, __dsub_rn(1.0, pi_i));
+                h = den > 0.0 ? __ddiv_rn(S, den) : 0.0;
+            } else {
+                h = pi_i;
+            }
+            const uint32_t U = philox_word(p.seed, (uint32_t)b, p.step, (uint32_t)(i - 1), 2u);
+            eta = (double)U < __dmul_rn(h, 4294967296.0);
+        }
+        const unsigned acc = __ballot_sync(0xffffffffu, eta);
+        const int tau = acc ? 31 - __clz((int)acc) : 0;  // the last accepted position
+        const unsigned __int128 St = shfl_u128(Si, tau);
+        if (i == 0) {
+            s_tau = tau;
+            s_plain = (tau == B || St == 0) ? 1 : 0;
+            if (!s_plain) {
+                // the residual draw's target and the mass slice that holds it
+                const uint32_t W = philox_word(p.seed, (uint32_t)b, p.step, (uint32_t)tau, 3u) >> 8;
+                const unsigned __int128 tg = (St * (unsigned __int128)(W & 0xFFFFFFu)) >> 24;
+                const unsigned long long *src = ms + ((size_t)(b * B + tau) * kMassSlices) * 2;
+                unsigned __int128 before = 0;
+                int c = 0;
+                for (; c < kMassSlices - 1; ++c) {
+                    const unsigned __int128 x = u128_join(src[2 * c], src[2 * c + 1]);
+                    if (before + x > tg) break;
+                    before += x;
+                }
+                s_slice = c;
+                u128_split(before, s_rlo, s_rhi);
+                u128_split(tg, s_tlo, s_thi);
+            }
+        }
+        if (rank == 0) {
+            if (i == 0) p.accept_len[b] = tau;
+            if (i <= B) p.out_tokens[b * (B + 1) + i] = i < tau ? block_token(p, b, i) : -1;
+        }
+    }
+    __syncthreads();
+    const int tau = s_tau;
+    int32_t *dst = p.out_tokens + b * (B + 1) + tau;
+    const BlockRow rp = block_rowp(p, b, tau);
+    const float T = p.T;
+    if (s_plain) {
+        const uint32_t W = philox_word(p.seed, (uint32_t)b, p.step, (uint32_t)tau, tau == B ? 4u : 3u) >> 8;
+        const float *pb = rp.row;
+        int off = 0;
+        if (p.stage) {
+            if (stage_rows(tsm, rp.row, nullptr, nullptr, V, &s_bar, &s_fail)) {
+                int hi;
+                cl_part(0, V, (int)rank, off, hi);
+                pb = tsm;
+            } else {
+                set_error(p.err, DSPARK_ERR_TIMEOUT);
+            }
+        }
+        auto wf = [&](int v) -> unsigned __int128 {
+            const unsigned long long E = weight_of(pb[v - off], T, rp.m);
+            return key_of(E, v) >= rp.kstar ? (unsigned __int128)E : (unsigned __int128)0;
+        };
+        cluster_draw(wf, V, W, dst, dsm);
+    } else {
+        const BlockRow rq = block_rowq(p, b, tau);
+        const double pi = s_pis[tau];
+        auto wf = [&](int v) -> unsigned __int128 { return block_term(rp, rq, pi, T, v); };
+        const int np = V / 2, c = s_slice;
+        const int r0 = 2 * (int)((long long)c * np / kMassSlices), r1 = 2 * (int)((long long)(c + 1) * np / kMassSlices);
+        cluster_pick(wf, r0, r1, -1, u128_join(s_rlo, s_rhi), u128_join(s_tlo, s_thi), dst, dsm);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Greedy: row argmax keys (zero between launches) then a finalize kernel that
+// also returns the keys to zero.
+// ---------------------------------------------------------------------------
+__global__ void verify_argmax_kernel(const float *__restrict__ P, int rows, int V, unsigned long long *keys, int *err) {
+    pdl_trigger();
+    pdl_wait();
+    __shared__ unsigned long long red[33];
+    const int row = blockIdx.y;
+    const int nslices = gridDim.x;
+    const int npairs = V / 2;
+    const int lo = (int)((long long)blockIdx.x * npairs / nslices);
+    const int hi = (int)((long long)(blockIdx.x + 1) * npairs / nslices);
+    unsigned long long best = 0;
+    bool bad = false;
+    const float *pr = P + (size_t)row * V;
+    // four independent pair loads in flight per thread
+    for (int pp0 = lo + threadIdx.x; pp0 < hi; pp0 += 4 * blockDim.x) {
+        float2 l[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int pp = pp0 + u * blockDim.x;
+            l[u] = pp < hi ? __ldcs((const float2 *)(pr + 2 * pp)) : make_float2(0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int pp = pp0 + u * blockDim.x;
+            if (pp < hi) {
+                if (!isfinite(l[u].x) || !isfinite(l[u].y)) bad = true;
+                best = max(best, max(argmax_key(l[u].x, 2 * pp), argmax_key(l[u].y, 2 * pp + 1)));
+            }
+        }
+    }
+    if (bad) set_error(err, DSPARK_ERR_BAD_INPUT);
+    best = block_max_u64(best, red);
+    if (threadIdx.x == 0) atomicMax(&keys[row], best);
+}
+
+__global__ void verify_greedy_finalize(const int32_t *__restrict__ tokens, int bs, int B, int V,
+                                       unsigned long long *keys, int32_t *accept_len, int32_t *out_tokens, int *err) {
+    pdl_trigger();
+    pdl_wait();
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= bs) return;
+    unsigned long long *k = keys + (size_t)b * (B + 1);
+    int a = 0;
+    for (; a < B; ++a) {
+        const int t = tokens[b * B + a];
+        if (t < 0 || t >= V) {
+            set_error(err, DSPARK_ERR_OOB);
+            break;
+        }
+        if (argmax_token(k[a]) != t) break;
+        out_tokens[b * (B + 1) + a] = t;
+    }
+    out_tokens[b * (B + 1) + a] = argmax_token(k[a]);
+    for (int j = a + 1; j <= B; ++j) out_tokens[b * (B + 1) + j] = -1;
+    accept_len[b] = a;
+    for (int j = 0; j <= B; ++j) k[j] = 0;
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+size_t verify_scratch_words(int bs, int B, int grid) {
+    (void)grid;
+    return kStatWords * (size_t)bs * (2 * B + 1) + (size_t)bs * B * kMassSlices * 2 + (size_t)bs * kDrawSlices * 2;
+}
+
+bool verify_setup(int V) {
+    const size_t smem = NucLayout(V).total;
+    const size_t stage2 = (size_t)2 * max_part(V) * 4;
+    if (cudaFuncSetAttribute(nucleus_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess ||
+        (stage2 <= kStageMax && cudaFuncSetAttribute(verify_block_final_kernel,
+                                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                     (int)(stage2 / 2)) != cudaSuccess)) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    return true;
+}
+
+cudaError_t launch_verify(VerifyParams p, int grid, cudaStream_t st) {
+    if (p.verify_mode == DSPARK_GREEDY) {
+        const int rows = p.bs * (p.B + 1);
+        // about two CTAs per SM over all rows
+        const int slices = std::max(1, std::min(64, (2 * grid + rows - 1) / rows));
+        cudaError_t e = launch_pdl(verify_argmax_kernel, dim3(slices, rows), dim3(256), 0, st, p.P, rows, p.V,
+                                   p.scratch, p.err);
+        if (e != cudaSuccess) return e;
+        return launch_pdl(verify_greedy_finalize, dim3((p.bs + 127) / 128), dim3(128), 0, st, p.tokens, p.bs, p.B, p.V,
+                          p.scratch, p.accept_len, p.out_tokens, p.err);
+    }
+    const int nrows = p.bs * ver_rows_per_seq(p);
+    cudaError_t e = launch_pdl_cluster(nucleus_rows_kernel, dim3(kVCl, nrows), dim3(kVThreads), NucLayout(p.V).total,
+                                       st, kVCl, p);
+    if (e != cudaSuccess) return e;
+    const size_t stage2 = (size_t)2 * max_part(p.V) * 4;
+    p.stage = stage2 <= kStageMax ? 1 : 0;
+    if (p.verify_mode == DSPARK_BLOCK) {
+        e = launch_pdl(verify_block_mass_kernel, dim3(kMassSlices, p.bs * p.B), dim3(256), 0, st, p);
+        if (e != cudaSuccess) return e;
+        return launch_pdl_cluster(verify_block_final_kernel, dim3(kVCl, p.bs), dim3(kVThreads),
+                                  p.stage ? stage2 / 2 : 0, st, kVCl, p);
+    }
+    return launch_pdl(verify_token_draw_kernel, dim3(kDrawSlices, p.bs), dim3(256), 0, st, p);
+}
+
+}  // namespace ds
