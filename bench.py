@@ -1093,8 +1093,19 @@ def only_verify(args, G, local):
             torch.cuda.synchronize()
             if k >= args.warmup:
                 times.append(a_.elapsed_time(b_))
+        # back to back (launches queued ahead, as in the step's graph): per-call device time
+        n = max(args.steps, 10)
+        smp = M.Sample(dmode, mode, 1.0, 0.95, 11, 0)
+        a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a_.record()
+        for _ in range(n):
+            ds.verify(P, ell, tokens, smp, acc, out, 1)
+        b_.record()
+        torch.cuda.synchronize()
         assert ds.check() == 0
-        res[name] = {"median_call_ms": statistics.median(times), "accept_len_last": int(acc.item())}
+        res[name] = {"median_call_ms": statistics.median(times), "back_to_back_call_ms": a_.elapsed_time(b_) / n,
+                     "accept_len_last": int(acc.item())}
     print(json.dumps({"only": "verify", "vocab": g.vocab, "block": g.block, "modes": res}))
 
 

@@ -306,6 +306,73 @@ DS_DEVINL void write_stats(const VerifyParams &p, int gr, int tok, float lt, flo
     o[3] = et;
 }
 
+// Rank 0 (the whole CTA): K* among the N <= kCandCap gathered keys of the
+// level-0 crossing bin, by histogram refinement over 10-bit digits of their
+// residual keys (key - (lo << 18), st.sh bits): the crossing digit of each round
+// narrows the active keys until one is left. hw / hc are 1024-bin scratch.
+DS_DEVINL void cta_select(const unsigned long long *cand, uint32_t N, NucState &st, unsigned long long *hw,
+                          uint32_t *hc, unsigned long long *gt) {
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const unsigned long long key = t < (int)N ? cand[t] : 0ull, E = key >> 18;
+    const unsigned long long R = key - (st.lo << 18);
+    bool active = t < (int)N;
+    for (int round = 0; round < 6; ++round) {
+        const int sh = st.sh, d = sh < kDigitBits ? sh : kDigitBits;
+        hw[t] = 0;
+        hc[t] = 0;
+        __syncthreads();
+        const int digit = (int)((R >> (sh - d)) & ((1ull << d) - 1));
+        if (active) {
+            atomicAdd(&hw[digit], E);
+            atomicAdd(&hc[digit], 1u);
+        }
+        __syncthreads();
+        {
+            const unsigned long long gs = warp_sum_u64(hw[t]);
+            if (lane == 0) gt[warp] = gs;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            const unsigned long long need = st.tau - st.above;
+            const unsigned long long tot = gt[lane], suf = warp_suffix_u64(tot);
+            const unsigned mask = __ballot_sync(0xffffffffu, suf >= need);
+            const int g = mask ? 31 - __clz((int)mask) : 0;
+            const unsigned long long above_g = __shfl_sync(0xffffffffu, suf - tot, g);
+            const unsigned long long w = hw[g * kSub + lane];
+            const uint32_t c = hc[g * kSub + lane];
+            const unsigned long long suf2 = warp_suffix_u64(w);
+            const unsigned mask2 = __ballot_sync(0xffffffffu, suf2 >= need - above_g);
+            const int j = mask2 ? 31 - __clz((int)mask2) : 0;
+            const unsigned long long ex = __shfl_sync(0xffffffffu, suf2 - w, j);
+            const unsigned long long wj = __shfl_sync(0xffffffffu, w, j);
+            const uint32_t cj = __shfl_sync(0xffffffffu, c, j);
+            if (lane == 0) {
+                if (!mask || !mask2) {
+                    st.done = 2;  // unreachable with exact weights
+                } else {
+                    st.fbin = g * kSub + j;
+                    st.fw = wj;
+                    st.fcount = cj;
+                    st.above += above_g + ex;
+                    st.pre = (st.pre << d) | (unsigned long long)st.fbin;
+                    st.sh = sh - d;
+                    if (cj == 1 || st.sh == 0) {
+                        st.Sn = st.above + wj;
+                        st.done = 1;
+                    }
+                }
+            }
+        }
+        __syncthreads();
+        active = active && digit == st.fbin;
+        if (st.done) {
+            if (st.done == 1 && active) st.kstar = key;
+            __syncthreads();
+            return;
+        }
+    }
+}
+
 // ---------------------------------------------------------------------------
 // Exact top-p nucleus of every row: grid (8, rows), clusters of 8 along x.
 // ---------------------------------------------------------------------------
@@ -314,7 +381,7 @@ __global__ void __launch_bounds__(kVThreads, 1) nucleus_rows_kernel(VerifyParams
     __shared__ NucState st;
     __shared__ unsigned long long red[33];
     __shared__ unsigned long long s_cmax, s_key;
-    __shared__ uint32_t s_cnt, s_n;
+    __shared__ uint32_t s_cnt, s_lcnt, s_base, s_counts[kVCl];
     __shared__ float s_lt;
     pdl_trigger();
     const NucLayout NL(p.V);
@@ -469,65 +536,37 @@ __global__ void __launch_bounds__(kVThreads, 1) nucleus_rows_kernel(VerifyParams
         __syncthreads();
         if (st.done) break;
         if (level == 0) {
-            // gather the crossing bin's keys into rank 0
+            // gather the crossing bin's keys into rank 0: count them here, reserve
+            // a range of rank 0's slots with one atomic, tell every CTA the count
+            if (t == 0) s_lcnt = 0;
+            __syncthreads();
+            for (int j = t; j < n; j += kVThreads) {
+                const float e = yv[j];
+                if (e >= st.elo && e < st.ehi) atomicAdd(&s_lcnt, 1u);
+            }
+            __syncthreads();
+            if (t == 0) {
+                s_base = atom_add_peer_u32(&s_cnt, 0u, s_lcnt);
+                for (int r = 0; r < kVCl; ++r) st_peer_u32(&s_counts[rank], (uint32_t)r, s_lcnt);
+                s_lcnt = 0;
+            }
+            __syncthreads();
             for (int j = t; j < n; j += kVThreads) {
                 const float e = yv[j];
                 if (!(e >= st.elo && e < st.ehi)) continue;
-                const uint32_t slot = atom_add_peer_u32(&s_cnt, 0u, 1u);
+                const uint32_t slot = s_base + atomicAdd(&s_lcnt, 1u);
                 if (slot < (uint32_t)kCandCap) st_peer_u64(cand + slot, 0u, key_of(weight_bits(e), lo + j));
             }
-            cluster_sync();  // G: every key is in rank 0
-            if (t == 0) s_n = ld_peer_u32(&s_cnt, 0u);
-            cluster_sync();  // every CTA has read the count (rank 0 may leave afterwards)
-            const uint32_t N = s_n;
+            cluster_sync();  // G: every key is in rank 0, every count in every CTA
+            uint32_t N = 0;
+            for (int r = 0; r < kVCl; ++r) N += s_counts[r];
             if (N <= (uint32_t)kCandCap) {
                 if (rank == 0) {
-                    // the keys in descending order (bitonic sort; the unused slots hold 0,
-                    // below every key), then K* is the key whose running weight reaches need
-                    if (t >= (int)N) cand[t] = 0ull;
-                    __syncthreads();
-                    for (int k = 2; k <= kCandCap; k <<= 1) {
-                        for (int j = k >> 1; j > 0; j >>= 1) {
-                            const int q = t ^ j;
-                            if (q > t) {
-                                const unsigned long long x = cand[t], y = cand[q];
-                                const bool desc = (t & k) == 0;
-                                if (desc ? x < y : x > y) {
-                                    cand[t] = y;
-                                    cand[q] = x;
-                                }
-                            }
-                            __syncthreads();
-                        }
+                    cta_select(cand, N, st, mw, mc, red);
+                    if (t == 0) {
+                        if (st.done != 1) set_error(p.err, DSPARK_ERR_BAD_INPUT);
+                        write_stats(p, gr, tok, s_lt, T, st, st.done == 1 ? st.kstar : ~0ull);
                     }
-                    const unsigned long long k = cand[t], E = k >> 18;
-                    // inclusive prefix of E over the sorted keys
-                    unsigned long long inc = E;
-#pragma unroll
-                    for (int o = 1; o < 32; o <<= 1) {
-                        const unsigned long long w = __shfl_up_sync(0xffffffffu, inc, o);
-                        if (lane >= o) inc += w;
-                    }
-                    if (lane == 31) red[warp] = inc;
-                    __syncthreads();
-                    if (warp == 0) {
-                        unsigned long long x = red[lane], xi = x;
-#pragma unroll
-                        for (int o = 1; o < 32; o <<= 1) {
-                            const unsigned long long w = __shfl_up_sync(0xffffffffu, xi, o);
-                            if (lane >= o) xi += w;
-                        }
-                        red[lane] = xi - x;  // exclusive prefix of the warp totals
-                    }
-                    __syncthreads();
-                    inc += red[warp];
-                    const unsigned long long need = st.tau - st.above;
-                    if (E && inc >= need && inc - E < need) {
-                        st.kstar = k;
-                        st.Sn = st.above + inc;
-                    }
-                    __syncthreads();
-                    if (t == 0) write_stats(p, gr, tok, s_lt, T, st, st.kstar);
                 }
                 return;
             }
