@@ -28,8 +28,7 @@
 
 namespace ds {
 
-constexpr int kRowsPerGroup = 8;    // rows whose histograms share one pass
-constexpr int kRadixPasses = 7;     // keys < 2^51, digits at bits 48, 40, ..., 0
+constexpr int kRowsPerGroup = 8;    // rows whose histograms share one grid barrier per level
 
 // Limit of the inter-CTA waits: the workspace's wait_ns when set, else kWaitLimitNs.
 DS_DEVINL unsigned long long grid_wait_limit(const SampleCtl *ctl) {
@@ -76,182 +75,252 @@ DS_DEVINL void pair_slice(int npairs, int &lo, int &hi) {
 }
 
 // ---------------------------------------------------------------------------
-// Exact nucleus of up to kRowsPerGroup rows by radix select over the grid.
-// Row r has logits rowp[r] (V entries) and its max ymax[r] of l / T known.
-// Produces kstar[r], Sn[r] in the shared memory of every CTA (identical).
+// Exact nucleus of up to kRowsPerGroup rows over the grid (each CTA owns a
+// slice of every row), for the probabilistic draft. Level 0 histograms the
+// binary exponent (octave) of E; the crossing octave (the suffix weight from
+// the top reaches tau) holds K*. Every later level histograms the next 10 bits
+// of the residual key R = K - (2^octave << 18) inside the crossing range, until
+// the crossing bin holds one key (its largest key is K*). A CTA adds only its
+// non-empty bins to the row's global level buffer (one atomic each), so each
+// level costs one grid barrier and few global atomics.
 // ---------------------------------------------------------------------------
+constexpr int kGBins = 1024;   // bins of a refinement level (10-bit digits); the octave level uses 33
+constexpr int kGDigit = 10;
+constexpr int kGLevels = 6;    // the octave + at most 5 digits of the <= 50-bit residual key
+
+// Global histogram of one row and level: weights, counts, largest keys and the
+// totals of groups of 32 bins (zero on entry).
+struct GLevel {
+    unsigned long long w[kGBins];
+    unsigned int c[kGBins];
+    unsigned long long k[kGBins];
+    unsigned long long g[kGBins / 32];
+};
+
 struct NucleusSmem {
-    unsigned long long hist[kRowsPerGroup][256];
-    unsigned long long prefix[kRowsPerGroup];
-    unsigned long long above[kRowsPerGroup];
-    unsigned long long tau[kRowsPerGroup];
-    unsigned long long kstar[kRowsPerGroup];
-    unsigned long long Sn[kRowsPerGroup];
-    unsigned long long last_bin[kRowsPerGroup];
+    unsigned long long hw[kGBins];  // this CTA's histogram of one row and level
+    unsigned int hc[kGBins];
+    unsigned long long hk[kGBins];
+    // per-row state (identical in every CTA)
+    unsigned long long tau[kRowsPerGroup], above[kRowsPerGroup], pre[kRowsPerGroup];
+    unsigned long long kstar[kRowsPerGroup], Sn[kRowsPerGroup];
+    int oct[kRowsPerGroup], sh[kRowsPerGroup], done[kRowsPerGroup];
     float ymax[kRowsPerGroup];
     unsigned long long red[33];
 };
 
+DS_DEVINL int octave_of(unsigned long long E) { return 63 - __clzll((long long)E); }
+
+__device__ bool grid_nucleus(const float *const *rowp, int nrows, int V, float T, float top_p, NucleusSmem &sm,
+                             GLevel *gl, SampleCtl *ctl, volatile int *s_fail, int *err) {
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    int lo, hi;
+    pair_slice(V / 2, lo, hi);
+    const unsigned long long P32 = top_p_q32(top_p);
+    if (t < nrows) {
+        sm.done[t] = 0;
+        sm.above[t] = 0;
+        sm.pre[t] = 0;
+        sm.oct[t] = 0;
+        sm.sh[t] = 0;
+        sm.kstar[t] = ~0ull;
+        sm.Sn[t] = 0;
+    }
+    __syncthreads();
+    for (int level = 0; level < kGLevels; ++level) {
+        const int nb = level ? kGBins : 33;
+        for (int r = 0; r < nrows; ++r) {
+            if (sm.done[r]) continue;
+            for (int i = t; i < nb; i += blockDim.x) {
+                sm.hw[i] = 0;
+                sm.hc[i] = 0;
+                sm.hk[i] = 0;
+            }
+            __syncthreads();
+            const float ym = sm.ymax[r];
+            const int oct = sm.oct[r], sh = sm.sh[r], d = sh < kGDigit ? sh : kGDigit;
+            const unsigned long long pre = sm.pre[r], base = (1ull << oct) << 18;
+            const float *row = rowp[r];
+            for (int pp = lo + t; pp < hi; pp += blockDim.x) {
+                const float2 l = *(const float2 *)(row + 2 * pp);
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int v = 2 * pp + e;
+                    const unsigned long long E = weight_of(e ? l.y : l.x, T, ym);
+                    if (!E) continue;
+                    const unsigned long long K = key_of(E, v);
+                    int bin;
+                    if (level == 0) {
+                        bin = octave_of(E);
+                    } else {
+                        if (octave_of(E) != oct) continue;
+                        const unsigned long long R = K - base;
+                        if ((R >> sh) != pre) continue;
+                        bin = (int)((R >> (sh - d)) & ((1ull << d) - 1));
+                    }
+                    atomicAdd(&sm.hw[bin], E);
+                    atomicAdd(&sm.hc[bin], 1u);
+                    atomicMax(&sm.hk[bin], K);
+                }
+            }
+            __syncthreads();
+            GLevel &G = gl[level * nrows + r];
+            for (int i = t; i < nb; i += blockDim.x) {
+                if (sm.hc[i]) {
+                    atomicAdd(&G.w[i], sm.hw[i]);
+                    atomicAdd(&G.c[i], sm.hc[i]);
+                    atomicMax(&G.k[i], sm.hk[i]);
+                }
+            }
+            for (int g = warp; 32 * g < nb; g += blockDim.x >> 5) {
+                const unsigned long long gs = warp_sum_u64(32 * g + lane < nb ? sm.hw[32 * g + lane] : 0ull);
+                if (lane == 0 && gs) atomicAdd(&G.g[g], gs);
+            }
+            __syncthreads();
+        }
+        if (!grid_barrier(ctl, s_fail, err)) return false;
+        // every CTA finds every row's crossing the same way (warp r: row r)
+        if (warp < nrows && !sm.done[warp]) {
+            const int r = warp;
+            const GLevel &G = gl[level * nrows + r];
+            const int ngroups = (nb + 31) / 32;
+            const unsigned long long tot = lane < ngroups ? ldcg_u64(&G.g[lane]) : 0ull;
+            const unsigned long long suf = warp_suffix_u64(tot);
+            unsigned long long need;
+            if (level == 0) {
+                const unsigned long long S = __shfl_sync(0xffffffffu, suf, 0);
+                const unsigned long long tau = (unsigned long long)(((unsigned __int128)S * P32) >> 32);
+                need = tau < 1 ? 1 : tau;
+                if (lane == 0) sm.tau[r] = need;
+            } else {
+                need = sm.tau[r] - sm.above[r];
+            }
+            const unsigned mask = __ballot_sync(0xffffffffu, suf >= need);
+            const int g = mask ? 31 - __clz((int)mask) : 0;
+            const unsigned long long above_g = __shfl_sync(0xffffffffu, suf - tot, g);
+            const int bi = 32 * g + lane;
+            const unsigned long long w = bi < nb ? ldcg_u64(&G.w[bi]) : 0ull;
+            const unsigned c = bi < nb ? __ldcg(&G.c[bi]) : 0u;
+            const unsigned long long k = bi < nb ? ldcg_u64(&G.k[bi]) : 0ull;
+            const unsigned long long suf2 = warp_suffix_u64(w);
+            const unsigned mask2 = __ballot_sync(0xffffffffu, suf2 >= need - above_g);
+            const int j = mask2 ? 31 - __clz((int)mask2) : 0;
+            const unsigned long long ex = __shfl_sync(0xffffffffu, suf2 - w, j);
+            const unsigned long long wj = __shfl_sync(0xffffffffu, w, j);
+            const unsigned cj = __shfl_sync(0xffffffffu, c, j);
+            const unsigned long long kj = __shfl_sync(0xffffffffu, k, j);
+            if (lane == 0) {
+                if (!mask || !mask2) {  // the weights never reach tau (non-finite input)
+                    set_error(err, DSPARK_ERR_BAD_INPUT);
+                    sm.done[r] = 2;
+                } else {
+                    const int bin = 32 * g + j;
+                    sm.above[r] += above_g + ex;
+                    if (level == 0) {
+                        sm.oct[r] = bin;
+                        sm.sh[r] = bin + 18;
+                        sm.pre[r] = 0;
+                    } else {
+                        const int sh = sm.sh[r], d = sh < kGDigit ? sh : kGDigit;
+                        sm.pre[r] = (sm.pre[r] << d) | (unsigned long long)(bin);
+                        sm.sh[r] = sh - d;
+                    }
+                    if (cj == 1 || (level > 0 && sm.sh[r] == 0)) {
+                        sm.kstar[r] = kj;
+                        sm.Sn[r] = sm.above[r] + wj;
+                        sm.done[r] = 1;
+                    }
+                }
+            }
+        }
+        __syncthreads();
+        bool all = true;
+        for (int r = 0; r < nrows; ++r) all = all && sm.done[r] != 0;
+        if (all) return true;
+    }
+    if (t == 0) set_error(err, DSPARK_ERR_BAD_INPUT);
+    return true;
+}
+
+// Weighted draws of nrows rows at once over vocabulary ids in ascending order:
+// for row r the smallest v whose running weight exceeds floor(total_r * W24_r / 2^24),
+// with weight = E_v inside the row's nucleus (key >= kstar[r]), else 0; total_r = Sn[r].
+// gParts: [nrows][gridDim.x][2] words (overwritten). One grid barrier. The CTA
+// holding row r's target writes the id to outs[r].
 struct DrawSmem {
     unsigned long long lo[kSampThreads], hi[kSampThreads];
     unsigned long long tot[4];
 };
 
-// gS: [nrows] global sums; gH: [kRadixPasses][nrows][256] global histograms (zero on entry).
-__device__ bool group_nucleus(const float *const *rowp, int nrows, int V, float T, float top_p, NucleusSmem &sm,
-                              unsigned long long *gS, unsigned long long *gH, SampleCtl *ctl, volatile int *s_fail,
-                              int *err) {
+__device__ bool grid_draw_rows(const float *const *rowp, int nrows, int V, float T, NucleusSmem &sm,
+                               const uint32_t *W24, unsigned long long *gParts, int32_t *const *outs, DrawSmem &ds_,
+                               SampleCtl *ctl, volatile int *s_fail, int *err) {
     int lo, hi;
     pair_slice(V / 2, lo, hi);
+    const int t = threadIdx.x;
     for (int r = 0; r < nrows; ++r) {
+        const float *row = rowp[r];
+        const float ym = sm.ymax[r];
+        const unsigned long long ks = sm.kstar[r];
         unsigned long long s = 0;
-        for (int pp = lo + threadIdx.x; pp < hi; pp += blockDim.x) {
-            const float2 l = *(const float2 *)(rowp[r] + 2 * pp);
-            s += weight_of(l.x, T, sm.ymax[r]) + weight_of(l.y, T, sm.ymax[r]);
+        for (int pp = lo + t; pp < hi; pp += blockDim.x) {
+            const float2 l = *(const float2 *)(row + 2 * pp);
+            const unsigned long long E0 = weight_of(l.x, T, ym), E1 = weight_of(l.y, T, ym);
+            s += (key_of(E0, 2 * pp) >= ks ? E0 : 0ull) + (key_of(E1, 2 * pp + 1) >= ks ? E1 : 0ull);
         }
-        s = block_sum_u64(s, sm.red);
-        if (threadIdx.x == 0 && s) atomicAdd(&gS[r], s);
+        s = block_sum_u64(s, sm.red);  // a CTA's slice weighs < 2^50
+        if (t == 0) gParts[((size_t)r * gridDim.x + blockIdx.x) * 2] = s;
     }
     if (!grid_barrier(ctl, s_fail, err)) return false;
-    const unsigned long long P32 = top_p_q32(top_p);
-    if (threadIdx.x < nrows) {
-        const unsigned long long S = ldcg_u64(&gS[threadIdx.x]);
-        const unsigned long long tau = (unsigned long long)(((unsigned __int128)S * P32) >> 32);
-        sm.tau[threadIdx.x] = tau < 1 ? 1 : tau;
-        sm.prefix[threadIdx.x] = 0;
-        sm.above[threadIdx.x] = 0;
-    }
-    __syncthreads();
-    for (int pass = 0; pass < kRadixPasses; ++pass) {
-        const int shift = 48 - 8 * pass;
-        for (int i = threadIdx.x; i < nrows * 256; i += blockDim.x) (&sm.hist[0][0])[i] = 0;
+    for (int r = 0; r < nrows; ++r) {
+        // the slice totals' prefix up to this CTA (threads c: CTA c)
+        unsigned long long before = 0, total = 0;
+        for (int c = t; c < (int)gridDim.x; c += blockDim.x) {
+            const unsigned long long x = ldcg_u64(&gParts[((size_t)r * gridDim.x + c) * 2]);
+            total += x;
+            if (c < (int)blockIdx.x) before += x;
+        }
+        before = block_sum_u64(before, sm.red);
+        total = block_sum_u64(total, sm.red);
+        const unsigned long long mine = ldcg_u64(&gParts[((size_t)r * gridDim.x + blockIdx.x) * 2]);
+        const unsigned long long target = (unsigned long long)(((unsigned __int128)total * (W24[r] & 0xFFFFFFu)) >> 24);
+        if (!(mine > 0 && before <= target && target < before + mine)) continue;  // uniform over the CTA
+        // this CTA holds the target: contiguous pairs per thread, then a scan
+        const float *row = rowp[r];
+        const float ym = sm.ymax[r];
+        const unsigned long long ks = sm.kstar[r];
+        auto wf = [&](int v) -> unsigned long long {
+            const unsigned long long E = weight_of(row[v], T, ym);
+            return key_of(E, v) >= ks ? E : 0ull;
+        };
+        const int n = hi - lo;
+        const int per = (n + blockDim.x - 1) / blockDim.x;
+        const int t0 = lo + t * per, t1 = min(hi, t0 + per);
+        unsigned long long my = 0;
+        for (int pp = t0; pp < t1; ++pp) my += wf(2 * pp) + wf(2 * pp + 1);
+        ds_.lo[t] = my;
         __syncthreads();
-        for (int r = 0; r < nrows; ++r) {
-            const unsigned long long want = sm.prefix[r] >> (shift + 8);
-            for (int pp = lo + threadIdx.x; pp < hi; pp += blockDim.x) {
-                const float2 l = *(const float2 *)(rowp[r] + 2 * pp);
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int v = 2 * pp + e;
-                    const unsigned long long E = weight_of(e ? l.y : l.x, T, sm.ymax[r]);
-                    const unsigned long long key = key_of(E, v);
-                    if (E && (key >> (shift + 8)) == want) atomicAdd(&sm.hist[r][(key >> shift) & 255], E);
+        if (t == 0) {
+            unsigned long long acc = before;
+            for (int u = 0; u < (int)blockDim.x; ++u) {
+                const unsigned long long x = ds_.lo[u];
+                ds_.lo[u] = acc;
+                acc += x;
+            }
+        }
+        __syncthreads();
+        const unsigned long long ex = ds_.lo[t];
+        if (t0 < t1 && ex <= target && target < ex + my) {
+            unsigned long long cum = ex;
+            for (int v = 2 * t0; v < 2 * t1; ++v) {
+                cum += wf(v);
+                if (cum > target) {
+                    *outs[r] = v;
+                    break;
                 }
             }
         }
         __syncthreads();
-        unsigned long long *gp = gH + (size_t)pass * nrows * 256;
-        for (int i = threadIdx.x; i < nrows * 256; i += blockDim.x) {
-            const unsigned long long h = (&sm.hist[0][0])[i];
-            if (h) atomicAdd(&gp[i], h);
-        }
-        if (!grid_barrier(ctl, s_fail, err)) return false;
-        // every CTA resolves the digit the same way: the largest bin whose
-        // suffix weight (including itself) reaches tau
-        if (threadIdx.x < nrows) {
-            const int r = threadIdx.x;
-            const unsigned long long *hr = gp + (size_t)r * 256;
-            unsigned long long cum = sm.above[r];
-            int d = 255;
-            for (; d > 0; --d) {
-                const unsigned long long h = ldcg_u64(&hr[d]);
-                if (cum + h >= sm.tau[r]) break;
-                cum += h;
-            }
-            sm.prefix[r] |= (unsigned long long)d << shift;
-            sm.last_bin[r] = ldcg_u64(&hr[d]);
-            sm.above[r] = cum;
-        }
-        __syncthreads();
-    }
-    if (threadIdx.x < nrows) {
-        sm.kstar[threadIdx.x] = sm.prefix[threadIdx.x];
-        sm.Sn[threadIdx.x] = sm.above[threadIdx.x] + sm.last_bin[threadIdx.x];
-    }
-    __syncthreads();
-    return true;
-}
-
-// Row maxima of y = l / T for a group of rows -> sm.ymax (one grid barrier).
-__device__ bool group_max(const float *const *rowp, int nrows, int V, float T, NucleusSmem &sm, unsigned long long *gM,
-                          SampleCtl *ctl, volatile int *s_fail, int *err) {
-    int lo, hi;
-    pair_slice(V / 2, lo, hi);
-    for (int r = 0; r < nrows; ++r) {
-        unsigned long long mx = 0;
-        bool bad = false;
-        for (int pp = lo + threadIdx.x; pp < hi; pp += blockDim.x) {
-            const float2 l = *(const float2 *)(rowp[r] + 2 * pp);
-            const float y0 = __fdiv_rn(l.x, T), y1 = __fdiv_rn(l.y, T);
-            if (!isfinite(y0) || !isfinite(y1)) bad = true;
-            const unsigned long long a = f2ord(y0), b = f2ord(y1);
-            mx = max(mx, max(a, b));
-        }
-        if (bad) set_error(err, DSPARK_ERR_BAD_INPUT);
-        mx = block_max_u64(mx, sm.red);
-        if (threadIdx.x == 0) atomicMax(&gM[r], mx);
-    }
-    if (!grid_barrier(ctl, s_fail, err)) return false;
-    if (threadIdx.x < nrows) sm.ymax[threadIdx.x] = ord2f((uint32_t)ldcg_u64(&gM[threadIdx.x]));
-    __syncthreads();
-    return true;
-}
-
-// Weighted draw over vocabulary ids in ascending order: the smallest v whose
-// running weight exceeds floor(total * W / 2^24), total = sum of weight(v).
-// gParts holds [gridDim.x][2] words (overwritten). The CTA holding the target
-// writes the token to *out.
-template <class WF>
-__device__ bool grid_draw(WF weight, int V, uint32_t W24, unsigned long long *gParts, int32_t *out, DrawSmem &ds_,
-                          SampleCtl *ctl, volatile int *s_fail, int *err) {
-    int lo, hi;
-    pair_slice(V / 2, lo, hi);
-    const int n = hi - lo;
-    const int per = (n + blockDim.x - 1) / blockDim.x;  // contiguous pairs per thread
-    const int t0 = lo + threadIdx.x * per, t1 = min(hi, t0 + per);
-    unsigned __int128 mine = 0;
-    for (int pp = t0; pp < t1; ++pp) mine += weight(2 * pp) + weight(2 * pp + 1);
-    ds_.lo[threadIdx.x] = (unsigned long long)mine;
-    ds_.hi[threadIdx.x] = (unsigned long long)(mine >> 64);
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        unsigned __int128 acc = 0;
-        for (int t = 0; t < (int)blockDim.x; ++t) {
-            acc += ((unsigned __int128)ds_.hi[t] << 64) | ds_.lo[t];
-            ds_.lo[t] = (unsigned long long)acc;
-            ds_.hi[t] = (unsigned long long)(acc >> 64);
-        }
-        gParts[2 * blockIdx.x] = ds_.lo[blockDim.x - 1];
-        gParts[2 * blockIdx.x + 1] = ds_.hi[blockDim.x - 1];
-    }
-    if (!grid_barrier(ctl, s_fail, err)) return false;
-    if (threadIdx.x == 0) {
-        unsigned __int128 before = 0, total = 0;
-        for (int c = 0; c < (int)gridDim.x; ++c) {
-            const unsigned __int128 pc = ((unsigned __int128)ldcg_u64(&gParts[2 * c + 1]) << 64) | ldcg_u64(&gParts[2 * c]);
-            if (c < (int)blockIdx.x) before += pc;
-            total += pc;
-        }
-        ds_.tot[0] = (unsigned long long)before;
-        ds_.tot[1] = (unsigned long long)(before >> 64);
-        ds_.tot[2] = (unsigned long long)total;
-        ds_.tot[3] = (unsigned long long)(total >> 64);
-    }
-    __syncthreads();
-    const unsigned __int128 before = ((unsigned __int128)ds_.tot[1] << 64) | ds_.tot[0];
-    const unsigned __int128 total = ((unsigned __int128)ds_.tot[3] << 64) | ds_.tot[2];
-    const unsigned __int128 target = (total * (unsigned __int128)(W24 & 0xFFFFFFu)) >> 24;
-    const unsigned __int128 incl = before + (((unsigned __int128)ds_.hi[threadIdx.x] << 64) | ds_.lo[threadIdx.x]);
-    const unsigned __int128 excl = incl - mine;
-    if (t0 < t1 && excl <= target && target < incl) {
-        unsigned __int128 cum = excl;
-        for (int v = 2 * t0; v < 2 * t1; ++v) {
-            cum += weight(v);
-            if (cum > target) {
-                *out = v;
-                break;
-            }
-        }
     }
     return true;
 }
@@ -262,16 +331,16 @@ __device__ bool grid_draw(WF weight, int V, uint32_t W24, unsigned long long *gP
 constexpr int kRollChunk = 8;  // sequences per pass over w2
 
 // scratch layout (words):
-//   amax [B][bs] | S [B][bs] | hist [B][bs][passes][256] | parts [B][bs][grid][2] | pick [B][bs]
+//   amax [B][bs] | pick [B][bs] | parts [B][bs][grid][2] | levels [B][bs][kGLevels] GLevel
+// (the level buffers of step i, group g: [kGLevels][rows of g], rows from g * kRowsPerGroup)
 struct RollLayout {
-    size_t amax, S, hist, parts, pick, total;
+    size_t amax, pick, parts, levels, total;
     __host__ __device__ RollLayout(int bs, int B, int grid) {
         amax = 0;
-        S = amax + (size_t)B * bs;
-        hist = S + (size_t)B * bs;
-        parts = hist + (size_t)B * bs * kRadixPasses * 256;
-        pick = parts + (size_t)B * bs * grid * 2;
-        total = pick + (size_t)B * bs;
+        pick = amax + (size_t)B * bs;
+        parts = pick + (size_t)B * bs;
+        levels = parts + (size_t)B * bs * grid * 2;
+        total = levels + (size_t)B * bs * kGLevels * (sizeof(GLevel) / 8);
     }
 };
 
@@ -529,6 +598,8 @@ __global__ void __launch_bounds__(kSampThreads, 1)
     __shared__ int s_prev[kMaxSampBs];
     __shared__ volatile int s_fail;
     __shared__ const float *s_rows[kRowsPerGroup];
+    __shared__ uint32_t s_w24[kRowsPerGroup];
+    __shared__ int32_t *s_outs[kRowsPerGroup];
     __shared__ uint32_t s_tmem_base;
     __shared__ uint32_t s_sec[kRollTmemRows][kRollSec];  // secondary pairs, rows [0, kt)
     extern __shared__ __align__(128) uint8_t ring_smem[];
@@ -589,7 +660,9 @@ __global__ void __launch_bounds__(kSampThreads, 1)
             for (int k = 0; k < rg.kt; ++k) s_sec[k][threadIdx.x] = q1 < hi ? __ldg(w2w + (size_t)k * rowp + q1) : 0u;
         }
     }
-    for (size_t w = (size_t)blockIdx.x * blockDim.x + threadIdx.x; w < L.total; w += (size_t)gridDim.x * blockDim.x)
+    // the level buffers of the nucleus are needed (and zeroed) only for a probabilistic draft
+    const size_t zero_words = p.draft_mode == DSPARK_GREEDY ? L.levels : L.total;
+    for (size_t w = (size_t)blockIdx.x * blockDim.x + threadIdx.x; w < zero_words; w += (size_t)gridDim.x * blockDim.x)
         sc[w] = 0;
     for (int b = threadIdx.x; b < p.bs; b += blockDim.x) {
         int a = p.anchor[b];
@@ -644,27 +717,21 @@ __global__ void __launch_bounds__(kSampThreads, 1)
                 sm.ymax[threadIdx.x] = ord2f((uint32_t)ldcg_u64(&sc[L.amax + (size_t)i * p.bs + g0 + threadIdx.x]));
             }
             __syncthreads();
-            if (!group_nucleus(s_rows, nr, V, p.T, p.top_p, sm, sc + L.S + (size_t)i * p.bs + g0,
-                               sc + L.hist + ((size_t)i * p.bs + g0) * kRadixPasses * 256, p.ctl, &s_fail, p.err)) {
+            GLevel *gl = (GLevel *)(sc + L.levels) + ((size_t)i * p.bs + g0) * kGLevels;
+            if (!grid_nucleus(s_rows, nr, V, p.T, p.top_p, sm, gl, p.ctl, &s_fail, p.err)) {
                 ok = false;
                 break;
             }
-            for (int rr = 0; rr < nr; ++rr) {
-                const int b = g0 + rr;
-                const float *row = s_rows[rr];
-                const unsigned long long kstar = sm.kstar[rr];
-                const float ym = sm.ymax[rr], T = p.T;
-                auto wf = [&](int v) -> unsigned __int128 {
-                    const unsigned long long E = weight_of(row[v], T, ym);
-                    return key_of(E, v) >= kstar ? (unsigned __int128)E : (unsigned __int128)0;
-                };
-                const uint32_t W = philox_word(p.seed, (uint32_t)b, p.step, (uint32_t)i, 1u) >> 8;
-                int32_t *pick = (int32_t *)&sc[L.pick + (size_t)i * p.bs + b];
-                if (!grid_draw(wf, V, W, sc + L.parts + ((size_t)i * p.bs + b) * gridDim.x * 2, pick, dsm, p.ctl,
-                               &s_fail, p.err)) {
-                    ok = false;
-                    break;
-                }
+            if (threadIdx.x < nr) {
+                const int b = g0 + threadIdx.x;
+                s_w24[threadIdx.x] = philox_word(p.seed, (uint32_t)b, p.step, (uint32_t)i, 1u) >> 8;
+                s_outs[threadIdx.x] = (int32_t *)&sc[L.pick + (size_t)i * p.bs + b];
+            }
+            __syncthreads();
+            if (!grid_draw_rows(s_rows, nr, V, p.T, sm, s_w24, sc + L.parts + ((size_t)i * p.bs + g0) * gridDim.x * 2,
+                                s_outs, dsm, p.ctl, &s_fail, p.err)) {
+                ok = false;
+                break;
             }
         }
         if (!ok || !grid_barrier(p.ctl, &s_fail, p.err)) {

@@ -113,6 +113,16 @@ DS_DEVINL unsigned long long warp_max_u64(unsigned long long v) {
     }
     return v;
 }
+// Inclusive suffix sums over the lanes of a warp (lane l: sum of lanes >= l).
+DS_DEVINL unsigned long long warp_suffix_u64(unsigned long long v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long w = __shfl_down_sync(0xffffffffu, v, o);
+        if (lane + o < 32) v += w;
+    }
+    return v;
+}
 DS_DEVINL unsigned long long warp_sum_u64(unsigned long long v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);

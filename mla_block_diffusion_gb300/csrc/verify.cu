@@ -176,17 +176,6 @@ struct NucState {
     unsigned long long fw, fabove;
 };
 
-// Inclusive suffix sums over the lanes of a warp (lane l: sum of lanes >= l).
-DS_DEVINL unsigned long long warp_suffix_u64(unsigned long long v) {
-    const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const unsigned long long w = __shfl_down_sync(0xffffffffu, v, o);
-        if (lane + o < 32) v += w;
-    }
-    return v;
-}
-
 // Warp 0: the crossing of the merged histogram (local copies): the largest bin
 // whose suffix weight (itself and every bin above it) reaches `need`. Fills
 // st.fbin / fw / fcount / fabove (weight of the bins above it). At level 0
