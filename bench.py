@@ -1128,12 +1128,12 @@ def ds_launches_per_step(ds, bs: int = 1, draft_mode: int = 0, verify_mode: int 
     R = G.block * G.n_heads
     if G.kv_lora + G.d_rope == 576 and G.kv_lora == 512:  # tensor-core attention
         sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
-        tiles, parts = -(-R // 128), G.kv_lora // 128
+        tiles, parts = -(-R // 128), G.kv_lora // 256
         chunks = -(-ds.max_ctx // 64) + 1
-        s = max(1, min(sms // (tiles * parts * ds.max_bs), chunks, 64))
+        s = max(1, min(sms // (tiles * parts * ds.max_bs), chunks, 20))
         cps = -(-chunks // s)
         splits = -(-chunks // cps)
-        fused = G.kv_lora % 64 == 0 and splits <= 16
+        fused = G.kv_lora % 64 == 0 and splits <= 20
         per_layer = 11 + (1 if splits > 1 and not fused else 0)
     else:
         per_layer = 11 + (1 if ds_layout_splits(ds) > 1 else 0)

@@ -7,10 +7,12 @@
 // absorbed form, "kimi-k3-dspark-gguf", Runtime status).
 //
 // A CTA owns 128 query rows, one range of 64-token chunks of the KV sequence
-// (a split) and one 128-column part of the latent output (4 CTAs share a row
-// tile and recompute its scores: the tensor core has the headroom, tensor
-// memory does not). Tensor memory (all 512 columns):
-//   [0, DQK/2)       Q tile, bf16 pairs (A operand of S = Q K^T)
+// (a split) and one 256-column half of the latent output (2 CTAs share a row
+// tile and both compute its scores: tensor memory holds 256 output columns
+// beside S and P, not 512). The Q tile is the A operand of S = Q K^T in two
+// pieces: its first 320 dimensions stay in shared memory (five 128 x 64 boxes
+// in the 128-byte swizzle), the last 256 in tensor memory. Tensor memory:
+//   [0, 128)         Q dimensions 320..575, bf16 pairs
 //   64 columns       S, fp32 (128 rows x 64 keys)
 //   32 columns       P = exp2(S - m), bf16 pairs (A operand of O += P V)
 //   DVP columns      O, fp32 (128 rows x the CTA's output columns)
@@ -20,9 +22,10 @@
 // and rescales O only when a new maximum exceeds it by more than 2^8 (the
 // result is the same: O and the row sum carry the same reference).
 //
-// The Q tile (128 rows x DQK) arrives by TMA in the space of KV stages 1 and 2
-// (the first chunk goes to stage 0); the softmax warps move it from shared to
-// tensor memory, after which the two stages take KV chunks again. A stage's
+// The Q tile (128 rows x DQK) arrives by TMA: its shared-memory piece in its
+// own region, its tensor-memory piece in the space of KV stage 1 (the first
+// chunk goes to stage 0); the softmax warps move that piece to tensor memory,
+// after which stage 1 takes KV chunks again. A stage's
 // boxes outside the CTA's value columns are refilled as soon as the scores
 // that read them are done, the value boxes once P V has read them.
 //
@@ -35,7 +38,7 @@ namespace ds {
 
 constexpr int kTcRows = 128;     // query rows per CTA (tcgen05 M)
 constexpr int kTcKeys = 64;      // keys per chunk (one page)
-constexpr int kTcStages = 3;     // KV chunk stages in shared memory
+constexpr int kTcStages = 2;     // KV chunk stages in shared memory
 constexpr int kTcPgAhead = 8;    // page numbers the producer reads ahead of their chunks
 constexpr float kTcRescaleLog2 = 8.f;
 
@@ -43,18 +46,21 @@ template <int DQK, int DV>
 struct TcCfg {
     static constexpr int kBoxes = (DQK + 63) / 64;         // 64-column boxes per key row
     static constexpr int kDQKP = kBoxes * 64;              // padded score width
-    static constexpr int kDVP = DV < 128 ? DV : 128;       // output columns per CTA
+    static constexpr int kDVP = DV < 256 ? DV : 256;       // output columns per CTA
     static constexpr int kParts = DV / kDVP;
     static constexpr int kBoxBytes = kTcKeys * 128;        // 64 rows x 128 B
     static constexpr int kTileBytes = kBoxes * kBoxBytes;
+    static constexpr int kQBoxBytes = kTcRows * 128;       // 128 rows x 64 bf16
+    static constexpr int kQsBoxes = 5;                     // Q boxes kept in shared memory (A from a descriptor)
+    static constexpr int kQtBoxes = kBoxes - kQsBoxes;     // Q boxes in tensor memory
+    static constexpr int kQsBytes = kQsBoxes * kQBoxBytes;
+    static constexpr int kQtBytes = kQtBoxes * kQBoxBytes;
     static constexpr int kQCol = 0;
-    static constexpr int kSCol = kDQKP / 2;
+    static constexpr int kSCol = kQtBoxes * 32;
     static constexpr int kPCol = kSCol + 64;
     static constexpr int kOCol = kPCol + 32;
-    static constexpr int kQBoxBytes = kTcRows * 128;       // 128 rows x 64 bf16
-    static constexpr int kQBytes = kBoxes * kQBoxBytes;
-    static constexpr int kSmem = 1024 + kTcStages * kTileBytes + 256;
-    static_assert(kQBytes <= (kTcStages - 1) * kTileBytes, "the Q tile fits KV stages 1..");
+    static constexpr int kSmem = 1024 + kQsBytes + kTcStages * kTileBytes + 256;
+    static_assert(kQtBytes <= (kTcStages - 1) * kTileBytes, "the tensor-memory piece of Q fits KV stage 1");
     static_assert(kOCol + kDVP <= 512, "tensor memory");
     static_assert(DV % kDVP == 0 && kDVP % 64 == 0, "output part: whole 64-column atoms");
     static_assert(kSmem <= 232448, "shared memory");
@@ -117,13 +123,14 @@ __global__ void __launch_bounds__(192, 2)
     using C = TcCfg<DQK, DV>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    uint8_t *sKV = smem;
-    uint64_t *bars = (uint64_t *)(smem + kTcStages * C::kTileBytes);
+    uint8_t *sQs = smem;                   // Q dimensions 0 .. 64 * kQsBoxes - 1 (A operand from shared memory)
+    uint8_t *sKV = smem + C::kQsBytes;
+    uint64_t *bars = (uint64_t *)(sKV + kTcStages * C::kTileBytes);
     uint64_t *kv_full = bars, *kv_empty = bars + kTcStages;
     uint64_t *s_full = bars + 2 * kTcStages, *s_free = s_full + 1, *p_ready = s_full + 2, *pv_done = s_full + 3;
     uint64_t *q_ready = s_full + 4, *mma_done = s_full + 5, *q_full = s_full + 6;
     uint64_t *kv_kfree = s_full + 7;  // [kTcStages]: a stage's score-only boxes are free
-    uint8_t *sQ = smem + C::kTileBytes;  // KV stages 1.. until the Q tile is in tensor memory
+    uint8_t *sQ = sKV + C::kTileBytes;  // Q's tensor-memory piece, in KV stage 1 until it is moved
     __shared__ uint32_t s_tmem;
     __shared__ volatile int s_abort;
     __shared__ int s_pg[kTcPgAhead];  // page ring of the producer
@@ -206,9 +213,12 @@ __global__ void __launch_bounds__(192, 2)
             for (int i = 0; i < kTcPgAhead; ++i)
                 raw[i] = (i < nch && c_begin + i < npages) ? __ldg(p.page_table + (size_t)b * p.max_pages + c_begin + i) : 0;
             pdl_wait();
-            mbar_arrive_expect_tx(q_full, (uint32_t)C::kQBytes);
+            mbar_arrive_expect_tx(q_full, (uint32_t)(C::kQsBytes + C::kQtBytes));
 #pragma unroll 1
-            for (int j = 0; j < C::kBoxes; ++j) tma_load_3d(sQ + j * C::kQBoxBytes, &tmQ, j * 64, r0, b, q_full);
+            for (int j = 0; j < C::kBoxes; ++j) {
+                uint8_t *dst = j < C::kQsBoxes ? sQs + j * C::kQBoxBytes : sQ + (j - C::kQsBoxes) * C::kQBoxBytes;
+                tma_load_3d(dst, &tmQ, j * 64, r0, b, q_full);
+            }
             q_issued = true;
 #pragma unroll
             for (int i = 0; i < kTcPgAhead; ++i) {
@@ -270,11 +280,15 @@ __global__ void __launch_bounds__(192, 2)
                 // A short issue sequence keeps this thread ahead of the tensor pipe even
                 // when a softmax warp shares its scheduler.
                 const uint64_t bd0 = sdesc_k_sw128(smem_u32(sKV + st * C::kTileBytes));
+                const uint64_t ad0 = sdesc_k_sw128(smem_u32(sQs));
 #pragma unroll
-                for (int kk = 0; kk < C::kDQKP / 16; ++kk)
-                    mma_bf16_tmem_a(tmem + C::kSCol, tmem + C::kQCol + 8 * kk,
-                                    bd0 + (uint64_t)((kk >> 2) * (C::kBoxBytes >> 4) + 2 * (kk & 3)), idS,
-                                    kk > 0 ? 1u : 0u);
+                for (int kk = 0; kk < 4 * C::kQsBoxes; ++kk)
+                    mma_bf16(tmem + C::kSCol, ad0 + (uint64_t)((kk >> 2) * (C::kQBoxBytes >> 4) + 2 * (kk & 3)),
+                             bd0 + (uint64_t)((kk >> 2) * (C::kBoxBytes >> 4) + 2 * (kk & 3)), idS, kk > 0 ? 1u : 0u);
+#pragma unroll
+                for (int kk = 4 * C::kQsBoxes; kk < C::kDQKP / 16; ++kk)
+                    mma_bf16_tmem_a(tmem + C::kSCol, tmem + C::kQCol + 8 * (kk - 4 * C::kQsBoxes),
+                                    bd0 + (uint64_t)((kk >> 2) * (C::kBoxBytes >> 4) + 2 * (kk & 3)), idS, 1u);
                 mma_commit(s_full);
                 mma_commit(&kv_kfree[st]);
                 return true;
@@ -306,13 +320,14 @@ __global__ void __launch_bounds__(192, 2)
         const int row = 32 * q4 + lane, r = r0 + row;
         const bool rv = r < p.R;
         const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
-        // Q row from the TMA tile (128-byte swizzle: 16-byte piece j of row r sits at
-        // piece j ^ (r & 7)) into tensor memory as bf16 pairs; rows past R are zero
+        // Q row's tensor-memory piece from the TMA tile (128-byte swizzle: 16-byte
+        // piece j of row r sits at piece j ^ (r & 7)) into tensor memory as bf16
+        // pairs; rows past R are zero
         bool ok = warp_wait(q_full, 0, &s_abort);
         if (ok) {
             const uint8_t *qrow = sQ + row * 128;
 #pragma unroll 1
-            for (int bq = 0; bq < C::kBoxes; ++bq) {
+            for (int bq = 0; bq < C::kQtBoxes; ++bq) {
                 uint32_t v[32];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
@@ -470,12 +485,12 @@ __global__ void __launch_bounds__(192, 2)
 // (row tiles x output parts x splits x sequences), whole chunks per split.
 int attention_tc_splits(int R, int dv, int bs, int max_ctx, int num_sms, int *cps) {
     const int tiles = (R + kTcRows - 1) / kTcRows;
-    const int parts = dv / (dv < 128 ? dv : 128);
+    const int parts = dv / (dv < 256 ? dv : 256);
     const int chunks = (max_ctx + kTcKeys - 1) / kTcKeys + 1;
     int s = num_sms / (tiles * parts * bs);
     if (s < 1) s = 1;
     if (s > chunks) s = chunks;
-    if (s > 64) s = 64;
+    if (s > 20) s = 20;  // the fused split combine takes up to 20 splits
     *cps = (chunks + s - 1) / s;
     return (chunks + *cps - 1) / *cps;
 }

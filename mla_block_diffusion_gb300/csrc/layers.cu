@@ -665,7 +665,7 @@ __global__ void __launch_bounds__(kQAbs2Threads, 1) q_absorb2_kernel(
 // ---------------------------------------------------------------------------
 constexpr int kCVRows = 4;
 constexpr int kCVThreads = 512;
-constexpr int kCVMaxSplit = 16;
+constexpr int kCVMaxSplit = 20;
 DS_DEVINL void cp_async16(void *smem_dst, const void *gmem_src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
 }
