@@ -30,6 +30,7 @@
 // narrow it down instead. No grid-wide barrier and no global atomics. Then one
 // cluster per sequence makes the accept decisions (one lane per position) and
 // the one draw of the step (a weighted pick in id order).
+#include "exact_div.cuh"
 #include "sampling_spec.cuh"
 
 #include <algorithm>
@@ -969,22 +970,31 @@ DS_DEVINL double fx80_to_double(unsigned __int128 s) {
     return ldexp((double)(unsigned long long)(s >> (n - 53)), n - 53 - 80);
 }
 
-// One row of the spec as in-nucleus probabilities (one-hot for a greedy draft).
+// One row of the spec as in-nucleus probabilities (one-hot for a greedy draft):
+// the rational e / S rounded once to double (exact_div: the IEEE quotient in
+// integer arithmetic).
 struct BlockRow {
     const float *row;
     float m;
     unsigned long long kstar, S;
+    ExactDivisor div;
     int onehot;  // -1: a spec row; else the one token of a greedy draft
     DS_DEVINL double prob(int v, float T) const {
         if (onehot >= 0) return v == onehot ? 1.0 : 0.0;
         const unsigned long long E = weight_of(row[v], T, m);
         const unsigned long long e = key_of(E, v) >= kstar ? E : 0ull;
-        return e ? __ddiv_rn((double)e, (double)S) : 0.0;
+        return e ? exact_div(e, div) : 0.0;
     }
 };
 
+// fx80(RN(RN(pi p(v)) - q(v))); the double operations that cannot change the
+// value are skipped (p = 0 gives no term, pi = 1 and q = 0 are exact).
 DS_DEVINL unsigned __int128 block_term(const BlockRow &rp, const BlockRow &rq, double pi, float T, int v) {
-    return fx80(__dsub_rn(__dmul_rn(pi, rp.prob(v, T)), rq.prob(v, T)));
+    const double a = rp.prob(v, T);
+    if (a == 0.0) return 0;
+    const double x = pi == 1.0 ? a : __dmul_rn(pi, a);
+    const double c = rq.prob(v, T);
+    return fx80(c == 0.0 ? x : __dsub_rn(x, c));
 }
 
 DS_DEVINL int block_token(const VerifyParams &p, int b, int i) {
@@ -998,6 +1008,7 @@ DS_DEVINL BlockRow block_rowp(const VerifyParams &p, int b, int i) {
     r.m = s.m;
     r.kstar = s.kstar;
     r.S = s.Sn;
+    r.div = exact_divisor(s.Sn ? s.Sn : 1ull);
     r.onehot = -1;
     return r;
 }
@@ -1007,6 +1018,7 @@ DS_DEVINL BlockRow block_rowq(const VerifyParams &p, int b, int i) {
         r.row = nullptr;
         r.m = 0.f;
         r.kstar = r.S = 0;
+        r.div = exact_divisor(1ull);
         r.onehot = block_token(p, b, i);
         return r;
     }
@@ -1015,6 +1027,7 @@ DS_DEVINL BlockRow block_rowq(const VerifyParams &p, int b, int i) {
     r.m = s.m;
     r.kstar = s.kstar;
     r.S = s.Sn;
+    r.div = exact_divisor(s.Sn ? s.Sn : 1ull);
     r.onehot = -1;
     return r;
 }
