@@ -52,6 +52,16 @@ def peaks():
     return dict(FALLBACK), "fallback"
 
 
+def gemm_kernel_name(fmt: str, M: int) -> str:
+    """The weight-GEMM kernel the library launches for this format at M activation rows."""
+    bn = min(224, max(16, 1 << (M - 1).bit_length()))
+    if fmt == "bf16":
+        return f"gemm_swapab_kernel<{bn}>"
+    if fmt == "fp8" and bn <= 32:
+        return f"gemm_f8_kernel<{8 if M <= 8 else bn}>"
+    return f"gemm_q_kernel<{bn}, {fmt}>"
+
+
 def algorithmic_bytes(G, ctx, bs: int = 1, fmt: str = "bf16"):
     """Bytes one step must move at least: every weight once (w2 once, the
     block's 7 rows of w1), fp32 gains and confidence head, the latent KV once,
@@ -555,9 +565,8 @@ def main():
         h = hashlib.sha256(open(os.path.join(ROOT, "mla_block_diffusion_gb300", "csrc", "gemm.cuh"), "rb").read())
         if td.get("gemm_cuh_sha256") == h.hexdigest():
             traffic = td.get("dram_bytes_per_launch")
-    gemm_line = {"kernel": ("gemm_swapab_kernel" if args.format == "bf16" else "gemm_q_kernel")
-                 + f"<{min(224, max(16, 1 << (bs * G.block - 1).bit_length()))}> (fc fusion launch; the step's "
-                   "weight-GEMM class)",
+    gemm_line = {"kernel": gemm_kernel_name(args.format, bs * G.block) + " (fc fusion launch; the step's "
+                                                                         "weight-GEMM class)",
                  "bound": "hbm", "achieved": fc_achieved, "peak": hbm, "unit": "GB/s", "frac": fc_achieved / hbm,
                  "traffic": traffic, "algorithmic_bytes_per_launch": fc_bytes, "avg_launch_ms": fc_ms,
                  "peak_source": src}
@@ -708,7 +717,7 @@ def only_fc(args, G, world, rank, local):
     nbytes = int(per * g.hidden * g.n_aux * g.hidden) + g.block * g.n_aux * g.hidden * 2 + g.block * g.hidden * 4
     pk, src = peaks()
     if rank == 0:
-        kern = "gemm_swapab_kernel<16>" if fmt == "bf16" else f"gemm_q_kernel<16, {fmt}>"
+        kern = gemm_kernel_name(fmt, g.block)
         print(json.dumps({"kernel": f"{kern} fc fusion", "format": fmt, "avg_launch_ms": ms,
                           "algorithmic_bytes_per_launch": nbytes, "achieved_GBps": nbytes / (ms * 1e-3) / 1e9,
                           "peak_GBps": pk["hbm_gbs"], "peak_source": src}))

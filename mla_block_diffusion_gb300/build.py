@@ -10,7 +10,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libdspark.so")
 SOURCES = ["api.cu", "layers.cu", "attn_tc.cu", "sampling.cu", "verify.cu", "noalloc.cu"]
-HEADERS = ["common.cuh", "gemm.cuh", "gemm_q.cuh", "internal.h", "sampling_spec.cuh", "exact_div.cuh", os.path.join("..", "..", "include", "dspark.h")]
+HEADERS = ["common.cuh", "gemm.cuh", "gemm_q.cuh", "gemm_f8.cuh", "internal.h", "sampling_spec.cuh", "exact_div.cuh", os.path.join("..", "..", "include", "dspark.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
 

@@ -12,6 +12,7 @@
 
 #include "gemm.cuh"
 #include "gemm_q.cuh"
+#include "gemm_f8.cuh"
 #include "internal.h"
 
 using namespace ds;
@@ -94,12 +95,29 @@ bool make_map_u8(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols_
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The same bytes seen as 16-bit elements (cols_bytes / 2 of them per row): a
+// 128-byte box row is 64 elements instead of 128, and the tensor-memory-access
+// unit moves the tile in half the element steps. The shared-memory image of a
+// tile is identical to the byte view's (the swizzle acts on 16-byte chunks).
+bool make_map_u16view(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols_bytes, uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || !base || (cols_bytes & 1u)) return false;
+    cuuint64_t dims[2] = {cols_bytes / 2, rows};
+    cuuint64_t strides[1] = {cols_bytes};
+    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
 // A weight-only quantised matrix: raw-code and group-scale descriptors plus its
 // output scales.
 struct QMat {
-    CUtensorMap data, scales;
+    CUtensorMap data;    // raw codes as 16-bit elements, boxes of 128 bytes x 64 rows
+    CUtensorMap scales;
     const float *rowscale;  // FP8 per-channel
     float gscale;           // NVFP4 per-tensor
 };
@@ -108,17 +126,17 @@ bool make_qmat(QMat *q, const dspark_mat_t &m, int fmt, uint64_t rows, uint64_t 
     if (fmt == DSPARK_FMT_FP8) {
         q->rowscale = (const float *)m.scale;
         q->gscale = 1.f;
-        return make_map_u8(&q->data, m.data, rows, cols, 128, 64, true) &&
+        return make_map_u16view(&q->data, m.data, rows, cols, 64) &&
                make_map_u8(&q->scales, m.data, rows, cols, 128, 64, true);
     }
     q->rowscale = nullptr;
     if (fmt == DSPARK_FMT_MXFP4) {
         q->gscale = 1.f;
-        return make_map_u8(&q->data, m.data, rows, cols / 2, 128, 64, true) &&
+        return make_map_u16view(&q->data, m.data, rows, cols / 2, 64) &&
                make_map_u8(&q->scales, m.scale, rows, cols / 32, 16, 64, false);
     }
     q->gscale = m.global_scale;
-    return make_map_u8(&q->data, m.data, rows, cols / 2, 128, 64, true) &&
+    return make_map_u16view(&q->data, m.data, rows, cols / 2, 64) &&
            make_map_u8(&q->scales, m.scale, rows, cols / 16, 16, 64, false);
 }
 
@@ -329,7 +347,29 @@ cudaError_t gemm_q_t(const QMat &A, const QMat *A2, const CUtensorMap &B, GemmPa
                       a2.data, A.scales, a2.scales, B, p);
 }
 
-cudaError_t gemm_q(const dspark_handle *h, const QMat &A, const QMat *A2, const CUtensorMap &B, int n_out, int K, int M,
+template <int MR>
+cudaError_t gemm_f8_t(const QMat &A, const QMat *A2, GemmParams p, int num_sms, cudaStream_t st, GemmPending *pend) {
+    using C = GemmF8Cfg<MR>;
+    static bool attr = false;
+    if (!attr) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(gemm_f8_kernel<MR>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    p.KB = (p.K + 127) / 128;
+    p.units = (long long)p.tiles * p.KB;
+    gemm_grid(p, 2, num_sms, MR, pend);
+    p.pair_red = 0;
+    p.qscale = A.rowscale;
+    p.qscale2 = A2 ? A2->rowscale : nullptr;
+    const QMat &a2 = A2 ? *A2 : A;
+    return launch_pdl(gemm_f8_kernel<MR>, dim3(p.grid), dim3(C::kThreads), (size_t)C::kSmemBytes, st, A.data, a2.data,
+                      p);
+}
+
+cudaError_t gemm_q(const dspark_handle *h, const QMat &A, const QMat *A2, const CUtensorMap &B, const void *xact,
+                   int n_out, int K, int M,
                    int epi, float *out_f32, __nv_bfloat16 *out_bf16, int ldo, void *ws, cudaStream_t st,
                    GemmPending *pend = nullptr, const L2Prefetch *pf = nullptr) {
     GemmParams p;
@@ -348,10 +388,13 @@ cudaError_t gemm_q(const dspark_handle *h, const QMat &A, const QMat *A2, const 
     p.counters = (int *)((char *)ws + kCtlCounters);
     p.err = (int *)((char *)ws + kCtlErr);
     p.partials = (float *)((char *)ws + kCtlBytes);
+    p.act = (const __nv_bfloat16 *)xact;
     const int bn = bn_for(M);
     if (h->g.weight_format == DSPARK_FMT_FP8) {
-        if (bn == 16) return gemm_q_t<16, DSPARK_FMT_FP8>(A, A2, B, p, h->num_sms, st, pend);
-        if (bn == 32) return gemm_q_t<32, DSPARK_FMT_FP8>(A, A2, B, p, h->num_sms, st, pend);
+        // up to 32 activation rows: E4M3 weights straight into the tensor core
+        if (M <= 8) return gemm_f8_t<8>(A, A2, p, h->num_sms, st, pend);
+        if (bn == 16) return gemm_f8_t<16>(A, A2, p, h->num_sms, st, pend);
+        if (bn == 32) return gemm_f8_t<32>(A, A2, p, h->num_sms, st, pend);
         if (bn == 64) return gemm_q_t<64, DSPARK_FMT_FP8>(A, A2, B, p, h->num_sms, st, pend);
     } else if (h->g.weight_format == DSPARK_FMT_NVFP4) {
         if (bn == 16) return gemm_q_t<16, DSPARK_FMT_NVFP4>(A, A2, B, p, h->num_sms, st, pend);
@@ -609,7 +652,7 @@ dspark_status dspark_fuse_ctx(dspark_handle_t *h, const void *aux, float *x, int
         h->c_aux_bs = bs;
     }
     if (g.weight_format != DSPARK_FMT_BF16)
-        return cuda_status(gemm_q(h, h->qfc, nullptr, h->b_aux, g.hidden, g.n_aux * g.hidden, M, EPI_STORE, x, nullptr,
+        return cuda_status(gemm_q(h, h->qfc, nullptr, h->b_aux, aux, g.hidden, g.n_aux * g.hidden, M, EPI_STORE, x, nullptr,
                                   g.hidden, ws, (cudaStream_t)stream));
     return cuda_status(gemm(h, h->fc, nullptr, h->b_aux, g.hidden, g.n_aux * g.hidden, M, EPI_STORE, x, nullptr,
                             g.hidden, ws, (cudaStream_t)stream));
@@ -710,7 +753,7 @@ dspark_status dspark_draft_block(dspark_handle_t *h, float *x, const dspark_kv_t
             pf_kvb.ptr[0] = (const uint8_t *)W.w_kv_b;
             pf_kvb.bytes[0] = ((uint64_t)g.n_heads * (g.d_nope + g.d_v) * g.kv_lora * 2) & ~15ull;
         }
-        RUN(quant ? gemm_q(h, h->qq_b[l], nullptr, h->b_cq, g.n_heads * qhd, g.q_lora, M, EPI_STORE, q, nullptr,
+        RUN(quant ? gemm_q(h, h->qq_b[l], nullptr, h->b_cq, cq, g.n_heads * qhd, g.q_lora, M, EPI_STORE, q, nullptr,
                            g.n_heads * qhd, ws, s, want_q, &pf_kvb)
                   : gemm(h, h->q_b[l], nullptr, h->b_cq, g.n_heads * qhd, g.q_lora, M, EPI_STORE, q, nullptr,
                          g.n_heads * qhd, ws, s, &pf_kvb, want_q));
@@ -737,7 +780,7 @@ dspark_status dspark_draft_block(dspark_handle_t *h, float *x, const dspark_kv_t
             RUN(launch_attention(ap, bs, kvd, g.kv_lora, s));
             RUN(launch_v_absorb(olat, M, g.n_heads, g.d_nope, g.d_v, g.kv_lora, (const __nv_bfloat16 *)W.w_kv_b, ov, s));
         }
-        RUN(quant ? gemm_q(h, h->qo[l], nullptr, h->b_ov, g.hidden, g.n_heads * g.d_v, M, EPI_ADD, x, nullptr, g.hidden,
+        RUN(quant ? gemm_q(h, h->qo[l], nullptr, h->b_ov, ov, g.hidden, g.n_heads * g.d_v, M, EPI_ADD, x, nullptr, g.hidden,
                            ws, s, want_o)
                   : gemm(h, h->o[l], nullptr, h->b_ov, g.hidden, g.n_heads * g.d_v, M, EPI_ADD, x, nullptr, g.hidden, ws,
                          s, nullptr, want_o));
@@ -746,11 +789,11 @@ dspark_status dspark_draft_block(dspark_handle_t *h, float *x, const dspark_kv_t
                                        M, err, s));
         else
             RUN(launch_rmsnorm(x, g.hidden, W.mlp_norm, g.hidden, g.eps, hn, g.hidden, nullptr, 0, M, err, s));
-        RUN(quant ? gemm_q(h, h->qgate[l], &h->qup[l], h->b_hn, g.inter, g.hidden, M, EPI_SWIGLU, nullptr, act, g.inter,
+        RUN(quant ? gemm_q(h, h->qgate[l], &h->qup[l], h->b_hn, hn, g.inter, g.hidden, M, EPI_SWIGLU, nullptr, act, g.inter,
                            ws, s)
                   : gemm(h, h->gate[l], &h->up[l], h->b_hn, g.inter, g.hidden, M, EPI_SWIGLU, nullptr, act, g.inter, ws,
                          s));
-        RUN(quant ? gemm_q(h, h->qdown[l], nullptr, h->b_act, g.hidden, g.inter, M, EPI_ADD, x, nullptr, g.hidden, ws, s,
+        RUN(quant ? gemm_q(h, h->qdown[l], nullptr, h->b_act, act, g.hidden, g.inter, M, EPI_ADD, x, nullptr, g.hidden, ws, s,
                            want_x)
                   : gemm(h, h->down[l], nullptr, h->b_act, g.hidden, g.inter, M, EPI_ADD, x, nullptr, g.hidden, ws, s,
                          nullptr, want_x));

@@ -55,6 +55,7 @@ struct GemmParams {
     const float *qscale, *qscale2;
     float gscale, gscale2;
     L2Prefetch pf;      // weights of a later kernel, pulled into L2 by the producer
+    const __nv_bfloat16 *act;  // the activations [M, K] (read directly by the FP8 kernel)
     // Pairwise reduction (every CTA's range covers at least one tile, so a split
     // tile has two contributors): CTA c + 1 takes the tile's last k-blocks first
     // thing, writes them to its slot 2(c + 1) and raises counters[tile]; CTA c,

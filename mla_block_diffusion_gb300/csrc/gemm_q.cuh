@@ -257,11 +257,12 @@ __global__ void __launch_bounds__(GemmQCfg<BN, FMT>::kThreads, 1)
         const int row0 = p.paired ? tile * 64 : tile * 128;
         const int row1 = p.paired ? tile * 64 : tile * 128 + 64;
         const CUtensorMap *m1 = p.paired ? &tmA2 : &tmA;
-        tma_load_2d_hint(raw, &tmA, kr * (C::kDataBytes / 128), row0, &raw_full[s], pol);
-        tma_load_2d_hint(raw + 8192, m1, kr * (C::kDataBytes / 128), row1, &raw_full[s], pol);
+        // the codes' map has 16-bit elements: x counts byte pairs
+        tma_load_2d_hint(raw, &tmA, kr * (C::kDataBytes / 256), row0, &raw_full[s], pol);
+        tma_load_2d_hint(raw + 8192, m1, kr * (C::kDataBytes / 256), row1, &raw_full[s], pol);
         if (FMT == DSPARK_FMT_MXFP4) {  // second half of the 256 packed bytes per row
-            tma_load_2d_hint(raw + 16384, &tmA, kr * 256 + 128, row0, &raw_full[s], pol);
-            tma_load_2d_hint(raw + 16384 + 8192, m1, kr * 256 + 128, row1, &raw_full[s], pol);
+            tma_load_2d_hint(raw + 16384, &tmA, kr * 128 + 64, row0, &raw_full[s], pol);
+            tma_load_2d_hint(raw + 16384 + 8192, m1, kr * 128 + 64, row1, &raw_full[s], pol);
         }
         if (FMT != DSPARK_FMT_FP8) {
             const CUtensorMap *n1 = p.paired ? &tmS2 : &tmS;

@@ -93,13 +93,13 @@ def test_nvfp4_rejects_unaligned_geometry(M):
 
 
 def test_activation_beyond_f16_range_is_reported(M):
-    """The quantised GEMMs take activations in f16: a magnitude above 65504 is
+    """The NVFP4 / MXFP4 GEMMs take activations in f16: a magnitude above 65504 is
     reported as DSPARK_ERR_BAD_INPUT (17), and a clean call afterwards is OK."""
-    w = TINY_STEP
+    w = workload(MID, 1, (64,), seed=9)
     G = w.geom
     W = gen.make_weights(w, "cpu")
     I = gen.make_inputs(w, "cpu")
-    ds = M.DSpark(G, to_dev(Q.quantise_weights(W, "fp8", G.n_layers)), max_bs=1, weight_format=FORMAT_FP8)
+    ds = M.DSpark(G, to_dev(Q.quantise_weights(W, "nvfp4", G.n_layers)), max_bs=1, weight_format=FORMAT_NVFP4)
     x = torch.empty(1, G.block, G.hidden, dtype=torch.float32, device="cuda")
     aux = I["aux"].cuda()
     bad = aux.clone()
@@ -130,3 +130,51 @@ def test_mxfp4_scale_out_of_f16_range_is_reported(M):
     ds2 = M.DSpark(G, to_dev(Wq), max_bs=1, weight_format=FORMAT_MXFP4)
     ds2.fuse_ctx(I["aux"].cuda(), x, 1)
     assert ds2.check() == 0
+
+
+@pytest.mark.parametrize("bs", [1, 2, 3], ids=["rows7", "rows14", "rows21"])
+def test_fp8_fc_split_is_exact(M, bs):
+    """FP8 weights go to the tensor core as stored and every bf16 activation as the
+    sum of two E4M3 terms with a power-of-two scale per row and 128-k chunk, which
+    is exact within 2^13 of the chunk maximum. So the fc fusion equals the
+    float64 product of the decoded weights and the bf16 activations up to fp32
+    summation (relative L2 below 1e-5, where the 3e-2 format tolerance allows for
+    the quantisation itself), also for activations spread over 32 binades and
+    beyond the f16 range. Rows 7, 14 and 21 take the 8-, 16- and 32-row activation tiles."""
+    w = workload(MID, bs, (64,) * bs, seed=21)
+    G = w.geom
+    W = gen.make_weights(w, "cpu")
+    I = gen.make_inputs(w, "cpu")
+    Wq = Q.quantise_weights(W, "fp8", G.n_layers)
+    w_fc = decode(Wq["w_fc"], "fp8")
+    aux = I["aux"]
+    g = torch.Generator().manual_seed(5)
+    e = torch.randint(-24, 9, aux.shape, generator=g).to(torch.float32)
+    wide = (aux.to(torch.float32) * torch.pow(2.0, e)).to(torch.bfloat16)
+    big = aux.clone()
+    big.view(-1)[3] = 70000.0
+    ds = M.DSpark(G, to_dev(Wq), max_bs=bs, max_ctx=64, weight_format=FORMAT_FP8)
+    for a in (aux, wide, big):
+        x = torch.empty(bs, G.block, G.hidden, dtype=torch.float32, device="cuda")
+        ds.fuse_ctx(a.cuda(), x, bs)
+        assert ds.check() == 0
+        for b in range(bs):
+            assert rel_l2(x[b].cpu().numpy(), N.fuse_ctx(w_fc, f64(a[b]))) < 1e-5, b
+
+
+def test_fp8_nonfinite_activation_is_reported(M):
+    """An infinite activation reaching the FP8 GEMM is DSPARK_ERR_BAD_INPUT (17);
+    a clean call afterwards is OK."""
+    w = TINY_STEP
+    G = w.geom
+    W = gen.make_weights(w, "cpu")
+    I = gen.make_inputs(w, "cpu")
+    ds = M.DSpark(G, to_dev(Q.quantise_weights(W, "fp8", G.n_layers)), max_bs=1, weight_format=FORMAT_FP8)
+    x = torch.empty(1, G.block, G.hidden, dtype=torch.float32, device="cuda")
+    aux = I["aux"].cuda()
+    bad = aux.clone()
+    bad.view(-1)[11] = float("inf")
+    ds.fuse_ctx(bad, x, 1)
+    assert ds.check() == 17
+    ds.fuse_ctx(aux, x, 1)
+    assert ds.check() == 0
