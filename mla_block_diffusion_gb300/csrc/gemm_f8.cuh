@@ -50,7 +50,10 @@ struct GemmF8Cfg {
     static constexpr int kXchgFloats = 64 * 17;
     static constexpr int kFixed = 1024 + kXchgFloats * 4 + kSlots * kN * 4 + kSlots * kBBytes + 1024;
     static constexpr int kStagesFit = (kGemmMaxSmem - kFixed) / kABytes;
-    static constexpr int kStages = kStagesFit > 14 ? 14 : kStagesFit;
+    // 11 stages leave shared memory, and the register cap registers, for the
+    // next kernel's CTAs to become resident beside this one before it ends
+    static constexpr int kStages = kStagesFit > 11 ? 11 : kStagesFit;
+    static constexpr int kMaxRegs = MR <= 8 ? 144 : 168;
     static constexpr int kSmemBytes = kFixed + kStages * kABytes;
     // split warps 6, 7, 10 and 11: only on the SM sub-partitions (warp % 4) of
     // neither the producer (warp 0) nor the MMA issuer (warp 1), whose single
@@ -171,7 +174,7 @@ DS_DEVINL void split_chunk(const uint4 (&xv)[MR / 2], uint8_t *b8, float *sc, in
 }
 
 template <int MR>
-__global__ void __launch_bounds__(GemmF8Cfg<MR>::kThreads, 1)
+__global__ void __launch_bounds__(GemmF8Cfg<MR>::kThreads, 1) __maxnreg__(GemmF8Cfg<MR>::kMaxRegs)
     gemm_f8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                    const GemmParams p) {
     using C = GemmF8Cfg<MR>;
