@@ -558,12 +558,14 @@ def main():
     fc_bytes = ab["fc_weight"] + bs * G.block * G.n_aux * G.hidden * 2 + bs * G.block * G.hidden * 4
     fc_achieved = fc_bytes / (fc_ms * 1e-3) / 1e9
     traffic = None
-    tfile = os.path.join(ROOT, "profiles", "fc_gemm_traffic.json")
-    if os.path.exists(tfile) and args.format == "bf16" and bs == 1:
-        with open(tfile) as f:
+    # ncu DRAM bytes of this launch, valid while the kernel's source is the profiled one
+    tsrc = {"bf16": ("fc_gemm_traffic.json", "gemm.cuh", "gemm_cuh_sha256"),
+            "fp8": ("fc_gemm_f8_traffic.json", "gemm_f8.cuh", "gemm_f8_cuh_sha256")}.get(args.format)
+    if tsrc and bs == 1 and os.path.exists(os.path.join(ROOT, "profiles", tsrc[0])):
+        with open(os.path.join(ROOT, "profiles", tsrc[0])) as f:
             td = json.load(f)
-        h = hashlib.sha256(open(os.path.join(ROOT, "mla_block_diffusion_gb300", "csrc", "gemm.cuh"), "rb").read())
-        if td.get("gemm_cuh_sha256") == h.hexdigest():
+        h = hashlib.sha256(open(os.path.join(ROOT, "mla_block_diffusion_gb300", "csrc", tsrc[1]), "rb").read())
+        if td.get(tsrc[2]) == h.hexdigest():
             traffic = td.get("dram_bytes_per_launch")
     gemm_line = {"kernel": gemm_kernel_name(args.format, bs * G.block) + " (fc fusion launch; the step's "
                                                                          "weight-GEMM class)",
