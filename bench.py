@@ -1122,8 +1122,9 @@ def only_verify(args, G, local):
 
 def verify_launches(verify_mode: int) -> int:
     """Kernels of one dspark_verify call: greedy takes the row argmax and a finalize
-    kernel; probabilistic and block verification one cooperative kernel."""
-    return 2 if verify_mode == 0 else 1
+    kernel; probabilistic the nucleus kernel and the accept-and-draw kernel; block
+    verification the nucleus, residual-mass and decision kernels."""
+    return {0: 2, 1: 2, 2: 3}[verify_mode]
 
 
 def ds_launches_per_step(ds, bs: int = 1, draft_mode: int = 0, verify_mode: int = 0) -> int:

@@ -93,7 +93,7 @@ constexpr int kHistBins = kBinsK > kBins0 ? kBinsK : kBins0;
 constexpr int kMaxGroups = kHistBins / kSub;
 constexpr int kCandCap = kVThreads;  // keys of the crossing bin ranked in one CTA
 constexpr int kMaxLevels = 8;        // level 0 + at most 5 refinements of the 44-bit residual key
-constexpr int kMassSlices = 16;      // CTAs per block-verification row for the residual masses
+constexpr int kMassSlices = 64;      // CTAs per block-verification row for the residual masses (2 per lane of a warp)
 constexpr size_t kStageMax = 200 * 1024;  // largest staging of the draw rows in shared memory
 constexpr int kStatWords = 4;
 
@@ -1147,23 +1147,51 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_block_final_kernel(Verify
         const unsigned acc = __ballot_sync(0xffffffffu, eta);
         const int tau = acc ? 31 - __clz((int)acc) : 0;  // the last accepted position
         const unsigned __int128 St = shfl_u128(Si, tau);
+        const bool plain = (tau == B || St == 0);
         if (i == 0) {
             s_tau = tau;
-            s_plain = (tau == B || St == 0) ? 1 : 0;
-            if (!s_plain) {
-                // the residual draw's target and the mass slice that holds it
-                const uint32_t W = philox_word(p.seed, (uint32_t)b, p.step, (uint32_t)tau, 3u) >> 8;
-                const unsigned __int128 tg = (St * (unsigned __int128)(W & 0xFFFFFFu)) >> 24;
-                const unsigned long long *src = ms + ((size_t)(b * B + tau) * kMassSlices) * 2;
-                unsigned __int128 before = 0;
-                int c = 0;
-                for (; c < kMassSlices - 1; ++c) {
-                    const unsigned __int128 x = u128_join(src[2 * c], src[2 * c + 1]);
-                    if (before + x > tg) break;
-                    before += x;
-                }
+            s_plain = plain ? 1 : 0;
+        }
+        if (!plain) {  // warp-uniform
+            // the residual draw's target and the mass slice that holds it: lane l
+            // holds slices 2l and 2l + 1; an inclusive scan of the lane totals
+            // finds the first slice whose running mass exceeds the target
+            static_assert(kMassSlices == 64, "two slices per lane");
+            const uint32_t W = philox_word(p.seed, (uint32_t)b, p.step, (uint32_t)tau, 3u) >> 8;
+            const unsigned __int128 tg = (St * (unsigned __int128)(W & 0xFFFFFFu)) >> 24;
+            const unsigned long long *src = ms + ((size_t)(b * B + tau) * kMassSlices) * 2;
+            const unsigned __int128 x0 = u128_join(src[4 * i], src[4 * i + 1]);
+            const unsigned __int128 x1 = u128_join(src[4 * i + 2], src[4 * i + 3]);
+            unsigned __int128 incl = x0 + x1;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                unsigned long long lo, hi;
+                u128_split(incl, lo, hi);
+                const unsigned __int128 up = u128_join(__shfl_up_sync(0xffffffffu, lo, o), __shfl_up_sync(0xffffffffu, hi, o));
+                if (i >= o) incl += up;
+            }
+            const unsigned __int128 ex = incl - x0 - x1;
+            int cand = -1;
+            unsigned __int128 before = 0;
+            if (ex + x0 > tg) {
+                cand = 2 * i;
+                before = ex;
+            } else if (ex + x0 + x1 > tg) {
+                cand = 2 * i + 1;
+                before = ex + x0;
+            }
+            const unsigned hit = __ballot_sync(0xffffffffu, cand >= 0);
+            // the target lies below the total, so a slice holds it; the last slice otherwise
+            const int src_lane = hit ? __ffs((int)hit) - 1 : 31;
+            if (!hit && i == 31) {
+                cand = kMassSlices - 1;
+                before = ex + x0;
+            }
+            const int c = __shfl_sync(0xffffffffu, cand, src_lane);
+            const unsigned __int128 bf = shfl_u128(before, src_lane);
+            if (i == 0) {
                 s_slice = c;
-                u128_split(before, s_rlo, s_rhi);
+                u128_split(bf, s_rlo, s_rhi);
                 u128_split(tg, s_tlo, s_thi);
             }
         }

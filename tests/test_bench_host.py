@@ -28,6 +28,13 @@ def test_full_geometry_launches_62_kernels(sms152):
     assert bench.ds_launches_per_step(_handle(FULL, 95000)) == 62
 
 
+def test_verification_rules_add_their_kernels(sms152):
+    # probabilistic: nucleus + accept-and-draw (as many as greedy); block: nucleus,
+    # residual masses, decisions (the counts the verify launch list shows)
+    assert bench.ds_launches_per_step(_handle(FULL, 95000), draft_mode=1, verify_mode=1) == 62
+    assert bench.ds_launches_per_step(_handle(FULL, 4096), draft_mode=1, verify_mode=2) == 63
+
+
 def test_one_split_at_batch_32(sms152):
     # 32 sequences leave one KV split per row tile and part: the fused kernel then
     # reads the attention's normalised output and only absorbs v (still one launch)
