@@ -354,6 +354,7 @@ def main():
     ap.add_argument("--fc-aux", type=int, default=0, help="--only fc: captured states (K = aux * hidden)")
     ap.add_argument("--roll-mode", choices=["greedy", "probabilistic"], default="greedy",
                     help="--only rollout: draft sampling (probabilistic: T 1.0, top_p 0.95)")
+    ap.add_argument("--roll-bs", type=int, default=1, help="--only rollout: sequences per call (1..32)")
     ap.add_argument("--format", choices=["bf16", "fp8", "nvfp4", "mxfp4"], default="bf16",
                     help="weight format of fc, q_b, o, gate, up, down (the weight-format sweep workloads)")
     ap.add_argument("--no-drift", action="store_true", help="--format fp8|nvfp4|mxfp4: skip the drift report")
@@ -745,12 +746,15 @@ def only_call(args, G, local):
     W = gen.make_weights(w, "cuda")
     I = gen.make_inputs(w, "cuda")
     ctx = I["ctx_list"][0]
-    ds = M.DSpark(g, W, max_bs=1, max_ctx=ctx)
+    rbs = args.roll_bs if args.only == "rollout" else 1
+    ds = M.DSpark(g, W, max_bs=rbs, max_ctx=ctx)
     x = torch.empty(1, g.block, g.hidden, dtype=torch.float32, device="cuda")
     h = torch.empty_like(x)
-    z = gen.draft_logits(1, g.block, g.vocab, 1, device="cuda")
+    z = gen.draft_logits(rbs, g.block, g.vocab, 1, device="cuda")
     ell = torch.empty_like(z)
-    tokens = torch.empty(1, g.block, dtype=torch.int32, device="cuda")
+    tokens = torch.empty(rbs, g.block, dtype=torch.int32, device="cuda")
+    gen_a = torch.Generator().manual_seed(7)
+    anchors = torch.randint(0, g.vocab, (rbs,), generator=gen_a, dtype=torch.int32).cuda() if rbs > 1 else I["anchor"]
     kv = ds.make_kv(I["kv_pools"], I["page_table"], I["ctx_len"], ctx)
     prob = args.only == "rollout" and args.roll_mode == "probabilistic"
     smp = M.Sample(M.PROBABILISTIC, M.PROBABILISTIC, 1.0, 0.95, 1, 0) if prob else M.Sample(M.GREEDY, M.GREEDY, 1.0,
@@ -758,7 +762,7 @@ def only_call(args, G, local):
 
     def call():
         if args.only == "rollout":
-            ds.markov_rollout(z, I["anchor"], smp, tokens, ell, 1)
+            ds.markov_rollout(z, anchors, smp, tokens, ell, rbs)
         else:
             ds.fuse_ctx(I["aux"], x, 1)
             ds.draft_block(x, kv, h, z, 1)
@@ -773,7 +777,7 @@ def only_call(args, G, local):
         b_.record()
     torch.cuda.synchronize()
     assert ds.check() == 0
-    print(json.dumps({"only": args.only, "avg_call_ms": statistics.mean(a_.elapsed_time(b_) for a_, b_ in evs)}))
+    print(json.dumps({"only": args.only, "bs": rbs, "avg_call_ms": statistics.mean(a_.elapsed_time(b_) for a_, b_ in evs)}))
 
 
 def only_append(args, G, local):

@@ -423,98 +423,130 @@ DS_DEVINL void ring_drain(RollRing &rg) {
         mbar_drain(&rg.full[c % kRollStages], (uint32_t)((c / kRollStages) & 1));
 }
 
-// Packed fp32 pairs: two independent IEEE fp32 FMAs (round to nearest) per
-// instruction, each lane bit-identical to fmaf.
-DS_DEVINL uint64_t pack_f2(uint32_t lo_bits, uint32_t hi_bits) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo_bits), "r"(hi_bits));
-    return r;
-}
-DS_DEVINL void unpack_f2(uint64_t v, float &lo, float &hi) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-DS_DEVINL void fma_f2(uint64_t &acc, uint64_t a, uint64_t b) {
-    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
-}
+// The chains: acc_v = fmaf(u_k, w2[k][v], acc_v) for k in order, per sequence
+// and vocabulary id (each an IEEE fp32 FMA, bit-identical to the oracle's fmaf
+// chain). u (w1[t_{i-1}] as fp32, the same for every thread) comes from shared
+// memory four k at a time (one 16-byte load per sequence), w2 as bf16 pairs.
+// A thread owns its primary pair for all NB sequences of the pass (p0, p1)
+// and, by EX: 0 nothing more; 1 one extra chain, a leftover pair of the CTA for
+// one sequence (s0[0], s1[0]: the leftover pairs' chains are spread one per
+// thread so that no warp does twice the work); 2 a leftover pair for all NB
+// sequences (s0, s1), when the leftovers are too many to spread.
+template <int NB>
+struct RollAcc {
+    float p0[NB], p1[NB], s0[NB], s1[NB];
+};
 
-// One chunk of the chains: for every row the bf16 pair of w2 is widened to two
-// fp32 values and each of the NB sequences takes one packed FMA (k in order).
-template <int NB, bool TWO>
-DS_DEVINL void roll_chunk(const uint32_t *w, int wpr, int rows, int k0, int o0, int o1, bool has0, bool has1,
-                          const uint64_t (*s_u)[256], uint64_t (&a0)[NB], uint64_t (&a1)[NB]) {
-#pragma unroll 4
-    for (int kk = 0; kk < rows; ++kk) {
-        const uint32_t w0 = has0 ? w[kk * wpr + o0] : 0u;
-        const uint64_t xy0 = pack_f2(w0 << 16, w0 & 0xFFFF0000u);
-        uint64_t xy1 = 0;
-        if (TWO) {
-            const uint32_t w1v = has1 ? w[kk * wpr + o1] : 0u;
-            xy1 = pack_f2(w1v << 16, w1v & 0xFFFF0000u);
-        }
+// rows k0 .. k0 + 3 of the chains (k0 a multiple of 4); wv0 / wv1: the w2 pairs
+template <int NB, int EX>
+DS_DEVINL void roll_rows4(const uint32_t (&wv0)[4], const uint32_t (&wv1)[4], int k0, const float (*s_uf)[256],
+                          int ex_seq, RollAcc<NB> &a) {
+    float4 u4[NB];
+#pragma unroll
+    for (int bb = 0; bb < NB; ++bb) u4[bb] = *(const float4 *)&s_uf[bb][k0];
+    float4 ue = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (EX == 1) ue = *(const float4 *)&s_uf[ex_seq][k0];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float x0 = __uint_as_float(wv0[j] << 16), y0 = __uint_as_float(wv0[j] & 0xFFFF0000u);
+        const float x1 = __uint_as_float(wv1[j] << 16), y1 = __uint_as_float(wv1[j] & 0xFFFF0000u);
 #pragma unroll
         for (int bb = 0; bb < NB; ++bb) {
-            const uint64_t uu = s_u[bb][k0 + kk];
-            fma_f2(a0[bb], uu, xy0);
-            if (TWO) fma_f2(a1[bb], uu, xy1);
+            const float u = j == 0 ? u4[bb].x : j == 1 ? u4[bb].y : j == 2 ? u4[bb].z : u4[bb].w;
+            a.p0[bb] = __fmaf_rn(u, x0, a.p0[bb]);
+            a.p1[bb] = __fmaf_rn(u, y0, a.p1[bb]);
+            if (EX == 2) {
+                a.s0[bb] = __fmaf_rn(u, x1, a.s0[bb]);
+                a.s1[bb] = __fmaf_rn(u, y1, a.s1[bb]);
+            }
+        }
+        if (EX == 1) {
+            const float u = j == 0 ? ue.x : j == 1 ? ue.y : j == 2 ? ue.z : ue.w;
+            a.s0[0] = __fmaf_rn(u, x1, a.s0[0]);
+            a.s1[0] = __fmaf_rn(u, y1, a.s1[0]);
         }
     }
 }
+// one row k of the chains (the tail of a chunk whose length is not a multiple of 4)
+template <int NB, int EX>
+DS_DEVINL void roll_row1(uint32_t wv0, uint32_t wv1, int k, const float (*s_uf)[256], int ex_seq, RollAcc<NB> &a) {
+    const float x0 = __uint_as_float(wv0 << 16), y0 = __uint_as_float(wv0 & 0xFFFF0000u);
+    const float x1 = __uint_as_float(wv1 << 16), y1 = __uint_as_float(wv1 & 0xFFFF0000u);
+#pragma unroll
+    for (int bb = 0; bb < NB; ++bb) {
+        const float u = s_uf[bb][k];
+        a.p0[bb] = __fmaf_rn(u, x0, a.p0[bb]);
+        a.p1[bb] = __fmaf_rn(u, y0, a.p1[bb]);
+        if (EX == 2) {
+            a.s0[bb] = __fmaf_rn(u, x1, a.s0[bb]);
+            a.s1[bb] = __fmaf_rn(u, y1, a.s1[bb]);
+        }
+    }
+    if (EX == 1) {
+        const float u = s_uf[ex_seq][k];
+        a.s0[0] = __fmaf_rn(u, x1, a.s0[0]);
+        a.s1[0] = __fmaf_rn(u, y1, a.s1[0]);
+    }
+}
 
-// ell_i for NB sequences over this CTA's pairs (thread t owns pairs lo + t and
-// lo + t + blockDim): w2 comes from the ring; the chain over k stays in order.
-// Each CTA max-reduces its greedy keys (or its maxima of ell / T) into amax[b].
-// A failed wait sets *s_fail; every thread still reaches the block reduction.
+// One streamed chunk of rows k0 .. k0 + rows - 1.
+template <int NB, int EX>
+DS_DEVINL void roll_chunk(const uint32_t *w, int wpr, int rows, int k0, int o0, int o1, bool has0, bool has1,
+                          const float (*s_uf)[256], int ex_seq, RollAcc<NB> &a) {
+    int kk = 0;
+    if ((k0 & 3) == 0) {
+#pragma unroll 2
+        for (; kk + 4 <= rows; kk += 4) {
+            uint32_t wv0[4], wv1[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                wv0[j] = has0 ? w[(kk + j) * wpr + o0] : 0u;
+                wv1[j] = (EX != 0 && has1) ? w[(kk + j) * wpr + o1] : 0u;
+            }
+            roll_rows4<NB, EX>(wv0, wv1, k0 + kk, s_uf, ex_seq, a);
+        }
+    }
+    for (; kk < rows; ++kk)
+        roll_row1<NB, EX>(has0 ? w[kk * wpr + o0] : 0u, (EX != 0 && has1) ? w[kk * wpr + o1] : 0u, k0 + kk, s_uf,
+                          ex_seq, a);
+}
+
 // Rows [0, kt) of the chains from tensor memory (primary pairs: this thread's
-// lane and columns) and the secondary rows in shared memory. Warp-collective.
-template <int NB, bool TWO>
-DS_DEVINL void roll_tmem_rows(uint32_t taddr, int kt, const uint32_t (*s_sec)[kRollSec], int t, bool has1,
-                              const uint64_t (*s_u)[256], uint64_t (&a0)[NB], uint64_t (&a1)[NB]) {
+// lane and columns) and the leftover pairs' rows in shared memory (column sp).
+// Warp-collective.
+template <int NB, int EX>
+DS_DEVINL void roll_tmem_rows(uint32_t taddr, int kt, const uint32_t (*s_sec)[kRollSec], int sp, bool has1,
+                              const float (*s_uf)[256], int ex_seq, RollAcc<NB> &a) {
     for (int k16 = 0; k16 < kt; k16 += 16) {
         uint32_t v[16];
         tmem_ld16u(taddr + (uint32_t)k16, v);
+        if (k16 + 16 <= kt) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const int k = k16 + j;
-            if (k < kt) {
-                const uint64_t xy0 = pack_f2(v[j] << 16, v[j] & 0xFFFF0000u);
-                uint64_t xy1 = 0;
-                if (TWO) {
-                    const uint32_t w1v = has1 ? s_sec[k][t] : 0u;
-                    xy1 = pack_f2(w1v << 16, w1v & 0xFFFF0000u);
-                }
+            for (int j4 = 0; j4 < 16; j4 += 4) {
+                uint32_t wv0[4], wv1[4];
 #pragma unroll
-                for (int bb = 0; bb < NB; ++bb) {
-                    const uint64_t uu = s_u[bb][k];
-                    fma_f2(a0[bb], uu, xy0);
-                    if (TWO) fma_f2(a1[bb], uu, xy1);
+                for (int j = 0; j < 4; ++j) {
+                    wv0[j] = v[j4 + j];
+                    wv1[j] = (EX != 0 && has1) ? s_sec[k16 + j4 + j][sp] : 0u;
                 }
+                roll_rows4<NB, EX>(wv0, wv1, k16 + j4, s_uf, ex_seq, a);
             }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                if (k16 + j < kt)
+                    roll_row1<NB, EX>(v[j], (EX != 0 && has1) ? s_sec[k16 + j][sp] : 0u, k16 + j, s_uf, ex_seq, a);
         }
     }
 }
 
-template <int NB>
-__device__ void rollout_logits(const RolloutParams &p, const CUtensorMap *tm, int i, int b0, int nb, int lo, int hi,
-                               RollRing &rg, uint32_t taddr, const uint32_t (*s_sec)[kRollSec],
-                               const uint64_t (*s_u)[256], unsigned long long *amax, unsigned long long *red,
-                               uint64_t pol, volatile int *s_fail) {
-    const int V = p.V, r = p.r;
-    uint64_t a0[NB], a1[NB];
-#pragma unroll
-    for (int bb = 0; bb < NB; ++bb) a0[bb] = a1[bb] = 0ull;
-    const int q0 = threadIdx.x, q1 = threadIdx.x + blockDim.x;
-    const bool has0 = lo + q0 < hi, has1 = lo + q1 < hi;
-    const bool two = __any_sync(0xffffffffu, has1);  // warp-uniform
-    const int lane = threadIdx.x & 31;
-    // word offsets of the thread's pairs in a stage (row 0)
-    const int o0 = (q0 / rg.box_w) * kRollKC * rg.box_w + q0 % rg.box_w;
-    const int o1 = (q1 / rg.box_w) * kRollKC * rg.box_w + q1 % rg.box_w;
-    if (rg.kt > 0) {
-        if (two)
-            roll_tmem_rows<NB, true>(taddr, rg.kt, s_sec, threadIdx.x, has1, s_u, a0, a1);
-        else
-            roll_tmem_rows<NB, false>(taddr, rg.kt, s_sec, threadIdx.x, has1, s_u, a0, a1);
-    }
+// The chains of one pass in a given EX mode.
+template <int NB, int EX>
+DS_DEVINL bool roll_pass(const RolloutParams &p, const CUtensorMap *tm, int lo, RollRing &rg, uint32_t taddr,
+                         const uint32_t (*s_sec)[kRollSec], const float (*s_uf)[256], int sp, int ex_seq, bool has0,
+                         bool has1, int o0, int o1, uint64_t pol, volatile int *s_fail, RollAcc<NB> &acc) {
+    const int r = p.r, lane = threadIdx.x & 31;
+    if (rg.kt > 0) roll_tmem_rows<NB, EX>(taddr, rg.kt, s_sec, sp, has1, s_uf, ex_seq, acc);
     bool failed = false;
     for (int ch = 0; ch < rg.nchunks; ++ch) {
         const long long c = rg.consumed;
@@ -530,45 +562,85 @@ __device__ void rollout_logits(const RolloutParams &p, const CUtensorMap *tm, in
         if (!failed) {
             const uint32_t *w = (const uint32_t *)(rg.stage + (size_t)s * rg.stage_bytes);
             const int k0 = rg.kt + ch * kRollKC, rows = min(kRollKC, r - k0);
-            if (two)
-                roll_chunk<NB, true>(w, rg.box_w, rows, k0, o0, o1, has0, has1, s_u, a0, a1);
-            else
-                roll_chunk<NB, false>(w, rg.box_w, rows, k0, o0, o1, has0, has1, s_u, a0, a1);
+            roll_chunk<NB, EX>(w, rg.box_w, rows, k0, o0, o1, has0, has1, s_uf, ex_seq, acc);
             rg.consumed = c + 1;
         }
         __syncwarp();
         if (lane == 0 && !failed) mbar_arrive(&rg.empty[s]);
     }
-    if (failed) *s_fail = 1;
+    return !failed;
+}
+
+template <int NB>
+__device__ void rollout_logits(const RolloutParams &p, const CUtensorMap *tm, int i, int b0, int nb, int lo, int hi,
+                               RollRing &rg, uint32_t taddr, const uint32_t (*s_sec)[kRollSec],
+                               const float (*s_uf)[256], unsigned long long *amax, unsigned long long *red,
+                               uint64_t pol, volatile int *s_fail) {
+    const int V = p.V;
+    RollAcc<NB> acc;
+#pragma unroll
+    for (int bb = 0; bb < NB; ++bb) acc.p0[bb] = acc.p1[bb] = acc.s0[bb] = acc.s1[bb] = 0.f;
+    const int nt = (int)blockDim.x;
+    const int q0 = threadIdx.x;
+    const bool has0 = lo + q0 < hi;
+    // the CTA's leftover pairs lo + nt + sp (sp < nsec): one chain per thread
+    // (pair sp = t / NB, sequence t % NB) when they fit, else pair t for all NB
+    const int nsec = max(0, hi - lo - nt);
+    const bool spread = NB > 1 && nsec * NB <= nt;
+    const int sp = spread ? (int)threadIdx.x / NB : (int)threadIdx.x;
+    const int ex_seq = spread ? (int)threadIdx.x % NB : 0;
+    const bool has1 = spread ? (int)threadIdx.x < nsec * NB : (int)threadIdx.x < nsec;
+    const int q1 = nt + sp;
+    const bool two = __any_sync(0xffffffffu, has1);  // warp-uniform
+    // word offsets of the thread's pairs in a stage (row 0)
+    const int o0 = (q0 / rg.box_w) * kRollKC * rg.box_w + q0 % rg.box_w;
+    const int o1 = (q1 / rg.box_w) * kRollKC * rg.box_w + q1 % rg.box_w;
+    bool ok;
+    if (!two)
+        ok = roll_pass<NB, 0>(p, tm, lo, rg, taddr, s_sec, s_uf, sp, ex_seq, has0, has1, o0, o1, pol, s_fail, acc);
+    else if (spread)
+        ok = roll_pass<NB, 1>(p, tm, lo, rg, taddr, s_sec, s_uf, sp, ex_seq, has0, has1, o0, o1, pol, s_fail, acc);
+    else
+        ok = roll_pass<NB, 2>(p, tm, lo, rg, taddr, s_sec, s_uf, sp, ex_seq, has0, has1, o0, o1, pol, s_fail, acc);
+    if (!ok) *s_fail = 1;
     unsigned long long best[NB];
 #pragma unroll
     for (int bb = 0; bb < NB; ++bb) best[bb] = 0;
     bool bad = false;
+    // one output pair pp for sequence bb with chain values d0, d1
+    auto emit = [&](int pp, int bb, float d0, float d1) -> unsigned long long {
+        const size_t off = ((size_t)(b0 + bb) * p.B + i) * V + 2 * pp;
+        const float2 z = *(const float2 *)(p.z + off);
+        const float l0 = __fadd_rn(z.x, d0), l1 = __fadd_rn(z.y, d1);
+        *(float2 *)(p.ell + off) = make_float2(l0, l1);
+        if (!isfinite(l0) || !isfinite(l1)) bad = true;
+        unsigned long long k0, k1;
+        if (p.draft_mode == DSPARK_GREEDY) {
+            k0 = argmax_key(l0, 2 * pp);
+            k1 = argmax_key(l1, 2 * pp + 1);
+        } else {
+            k0 = f2ord(__fdiv_rn(l0, p.T));
+            k1 = f2ord(__fdiv_rn(l1, p.T));
+        }
+        return max(k0, k1);
+    };
+    if (has0) {
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        const int pp = lo + (j ? q1 : q0);
-        if (pp >= hi) continue;
+        for (int bb = 0; bb < NB; ++bb)
+            if (bb < nb) best[bb] = max(best[bb], emit(lo + q0, bb, acc.p0[bb], acc.p1[bb]));
+    }
+    if (has1) {
+        if (spread) {
+            if (ex_seq < nb) {
+                const unsigned long long k = emit(lo + q1, ex_seq, acc.s0[0], acc.s1[0]);
 #pragma unroll
-        for (int bb = 0; bb < NB; ++bb) {
-            if (bb < nb) {
-                const int b = b0 + bb;
-                float d0, d1;
-                unpack_f2(j ? a1[bb] : a0[bb], d0, d1);
-                const size_t off = ((size_t)b * p.B + i) * V + 2 * pp;
-                const float2 z = *(const float2 *)(p.z + off);
-                const float l0 = __fadd_rn(z.x, d0), l1 = __fadd_rn(z.y, d1);
-                *(float2 *)(p.ell + off) = make_float2(l0, l1);
-                if (!isfinite(l0) || !isfinite(l1)) bad = true;
-                unsigned long long k0, k1;
-                if (p.draft_mode == DSPARK_GREEDY) {
-                    k0 = argmax_key(l0, 2 * pp);
-                    k1 = argmax_key(l1, 2 * pp + 1);
-                } else {
-                    k0 = f2ord(__fdiv_rn(l0, p.T));
-                    k1 = f2ord(__fdiv_rn(l1, p.T));
-                }
-                best[bb] = max(best[bb], max(k0, k1));
+                for (int bb = 0; bb < NB; ++bb)
+                    if (bb == ex_seq) best[bb] = max(best[bb], k);
             }
+        } else {
+#pragma unroll
+            for (int bb = 0; bb < NB; ++bb)
+                if (bb < nb) best[bb] = max(best[bb], emit(lo + q1, bb, acc.s0[bb], acc.s1[bb]));
         }
     }
     if (bad) set_error(p.err, DSPARK_ERR_BAD_INPUT);
@@ -593,7 +665,7 @@ __global__ void __launch_bounds__(kSampThreads, 1)
     rollout_kernel(const __grid_constant__ CUtensorMap tmW2, RolloutParams p) {
     __shared__ NucleusSmem sm;
     __shared__ DrawSmem dsm;
-    __shared__ __align__(16) uint64_t s_u[kRollChunk][256];  // (u, u) fp32 pairs of w1[t_{i-1}]
+    __shared__ __align__(16) float s_uf[kRollChunk][256];  // w1[t_{i-1}] as fp32, per sequence of the pass
     __shared__ __align__(8) uint64_t s_full[kRollStages], s_empty[kRollStages];
     __shared__ int s_prev[kMaxSampBs];
     __shared__ volatile int s_fail;
@@ -682,15 +754,15 @@ __global__ void __launch_bounds__(kSampThreads, 1)
             for (int idx = threadIdx.x; idx < kRollChunk * r; idx += blockDim.x) {
                 const int bb = idx / r, k = idx % r;
                 const float u = bb < nb ? __bfloat162float(p.w1[(size_t)s_prev[b0 + bb] * r + k]) : 0.f;
-                s_u[bb][k] = pack_f2(__float_as_uint(u), __float_as_uint(u));
+                s_uf[bb][k] = u;
             }
             __syncthreads();
             if (hi > lo) {
                 if (nb == 1)
-                    rollout_logits<1>(p, &tmW2, i, b0, 1, lo, hi, rg, taddr, s_sec, s_u,
+                    rollout_logits<1>(p, &tmW2, i, b0, 1, lo, hi, rg, taddr, s_sec, s_uf,
                                       sc + L.amax + (size_t)i * p.bs, sm.red, pol, &s_fail);
                 else
-                    rollout_logits<kRollChunk>(p, &tmW2, i, b0, nb, lo, hi, rg, taddr, s_sec, s_u,
+                    rollout_logits<kRollChunk>(p, &tmW2, i, b0, nb, lo, hi, rg, taddr, s_sec, s_uf,
                                                sc + L.amax + (size_t)i * p.bs, sm.red, pol, &s_fail);
             }
             __syncthreads();
