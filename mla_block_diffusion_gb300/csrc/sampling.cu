@@ -515,28 +515,33 @@ DS_DEVINL void roll_chunk(const uint32_t *w, int wpr, int rows, int k0, int o0, 
 // lane and columns) and the leftover pairs' rows in shared memory (column sp).
 // Warp-collective.
 template <int NB, int EX>
+DS_DEVINL void roll_tmem16(const uint32_t (&v)[16], int k16, int kt, const uint32_t (*s_sec)[kRollSec], int sp,
+                           bool has1, const float (*s_uf)[256], int ex_seq, RollAcc<NB> &a) {
+    if (k16 + 16 <= kt) {
+#pragma unroll
+        for (int j4 = 0; j4 < 16; j4 += 4) {
+            uint32_t wv0[4], wv1[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                wv0[j] = v[j4 + j];
+                wv1[j] = (EX != 0 && has1) ? s_sec[k16 + j4 + j][sp] : 0u;
+            }
+            roll_rows4<NB, EX>(wv0, wv1, k16 + j4, s_uf, ex_seq, a);
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            if (k16 + j < kt)
+                roll_row1<NB, EX>(v[j], (EX != 0 && has1) ? s_sec[k16 + j][sp] : 0u, k16 + j, s_uf, ex_seq, a);
+    }
+}
+template <int NB, int EX>
 DS_DEVINL void roll_tmem_rows(uint32_t taddr, int kt, const uint32_t (*s_sec)[kRollSec], int sp, bool has1,
                               const float (*s_uf)[256], int ex_seq, RollAcc<NB> &a) {
     for (int k16 = 0; k16 < kt; k16 += 16) {
         uint32_t v[16];
         tmem_ld16u(taddr + (uint32_t)k16, v);
-        if (k16 + 16 <= kt) {
-#pragma unroll
-            for (int j4 = 0; j4 < 16; j4 += 4) {
-                uint32_t wv0[4], wv1[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    wv0[j] = v[j4 + j];
-                    wv1[j] = (EX != 0 && has1) ? s_sec[k16 + j4 + j][sp] : 0u;
-                }
-                roll_rows4<NB, EX>(wv0, wv1, k16 + j4, s_uf, ex_seq, a);
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-                if (k16 + j < kt)
-                    roll_row1<NB, EX>(v[j], (EX != 0 && has1) ? s_sec[k16 + j][sp] : 0u, k16 + j, s_uf, ex_seq, a);
-        }
+        roll_tmem16<NB, EX>(v, k16, kt, s_sec, sp, has1, s_uf, ex_seq, a);
     }
 }
 
@@ -574,8 +579,8 @@ DS_DEVINL bool roll_pass(const RolloutParams &p, const CUtensorMap *tm, int lo, 
 template <int NB>
 __device__ void rollout_logits(const RolloutParams &p, const CUtensorMap *tm, int i, int b0, int nb, int lo, int hi,
                                RollRing &rg, uint32_t taddr, const uint32_t (*s_sec)[kRollSec],
-                               const float (*s_uf)[256], unsigned long long *amax, unsigned long long *red,
-                               uint64_t pol, volatile int *s_fail) {
+                               const float (*s_uf)[256], unsigned long long *amax,
+                               unsigned long long (*red8)[kRollWarps], uint64_t pol, volatile int *s_fail) {
     const int V = p.V;
     RollAcc<NB> acc;
 #pragma unroll
@@ -644,12 +649,19 @@ __device__ void rollout_logits(const RolloutParams &p, const CUtensorMap *tm, in
         }
     }
     if (bad) set_error(p.err, DSPARK_ERR_BAD_INPUT);
+    // every sequence's maximum over the CTA in one round: warp maxima, one barrier,
+    // then one thread per sequence (the caller's next barrier frees red8)
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
     for (int bb = 0; bb < NB; ++bb) {
-        if (bb < nb) {
-            const unsigned long long m = block_max_u64(best[bb], red);
-            if (threadIdx.x == 0) atomicMax(&amax[b0 + bb], m);
-        }
+        best[bb] = warp_max_u64(best[bb]);
+        if (lane == 0) red8[bb][warp] = best[bb];
+    }
+    __syncthreads();
+    if ((int)threadIdx.x < nb) {
+        unsigned long long m = 0;
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) m = max(m, red8[threadIdx.x][w]);
+        atomicMax(&amax[b0 + threadIdx.x], m);
     }
 }
 
@@ -666,6 +678,7 @@ __global__ void __launch_bounds__(kSampThreads, 1)
     __shared__ NucleusSmem sm;
     __shared__ DrawSmem dsm;
     __shared__ __align__(16) float s_uf[kRollChunk][256];  // w1[t_{i-1}] as fp32, per sequence of the pass
+    __shared__ unsigned long long s_red8[kRollChunk][kRollWarps];
     __shared__ __align__(8) uint64_t s_full[kRollStages], s_empty[kRollStages];
     __shared__ int s_prev[kMaxSampBs];
     __shared__ volatile int s_fail;
@@ -760,10 +773,10 @@ __global__ void __launch_bounds__(kSampThreads, 1)
             if (hi > lo) {
                 if (nb == 1)
                     rollout_logits<1>(p, &tmW2, i, b0, 1, lo, hi, rg, taddr, s_sec, s_uf,
-                                      sc + L.amax + (size_t)i * p.bs, sm.red, pol, &s_fail);
+                                      sc + L.amax + (size_t)i * p.bs, s_red8, pol, &s_fail);
                 else
                     rollout_logits<kRollChunk>(p, &tmW2, i, b0, nb, lo, hi, rg, taddr, s_sec, s_uf,
-                                               sc + L.amax + (size_t)i * p.bs, sm.red, pol, &s_fail);
+                                               sc + L.amax + (size_t)i * p.bs, s_red8, pol, &s_fail);
             }
             __syncthreads();
             ok = !s_fail;
