@@ -556,10 +556,6 @@ DS_DEVINL bool roll_pass(const RolloutParams &p, const CUtensorMap *tm, int lo, 
     for (int ch = 0; ch < rg.nchunks; ++ch) {
         const long long c = rg.consumed;
         const int s = (int)(c % kRollStages);
-        if (!failed && threadIdx.x == 0 && !ring_issue(rg, tm, lo, pol, s_fail)) {
-            set_error(p.err, DSPARK_ERR_TIMEOUT);
-            *s_fail = 1;
-        }
         if (!failed && !mbar_wait_bounded(&rg.full[s], (uint32_t)((c / kRollStages) & 1), s_fail)) {
             set_error(p.err, DSPARK_ERR_TIMEOUT);
             failed = true;
@@ -572,6 +568,12 @@ DS_DEVINL bool roll_pass(const RolloutParams &p, const CUtensorMap *tm, int lo, 
         }
         __syncwarp();
         if (lane == 0 && !failed) mbar_arrive(&rg.empty[s]);
+        // thread 0 refills after its own chunk: the stage it refills was released by
+        // every warp one chunk earlier, so the wait rarely holds this warp
+        if (!failed && threadIdx.x == 0 && !ring_issue(rg, tm, lo, pol, s_fail)) {
+            set_error(p.err, DSPARK_ERR_TIMEOUT);
+            *s_fail = 1;
+        }
     }
     return !failed;
 }
