@@ -708,6 +708,7 @@ dspark_status dspark_draft_block(dspark_handle_t *h, float *x, const dspark_kv_t
     ap.block = g.block;
     ap.splits = L.splits;
     ap.tok_per_split = L.tok_per_split;
+    ap.cps = L.cps;
     ap.scale_log2 = h->scale_log2;
     ap.o_lat = olat;
     ap.part_o = (float *)(w + L.part_o);

@@ -41,6 +41,7 @@ constexpr int kTcKeys = 64;      // keys per chunk (one page)
 constexpr int kTcStages = 2;     // KV chunk stages in shared memory
 constexpr int kTcPgAhead = 8;    // page numbers the producer reads ahead of their chunks
 constexpr float kTcRescaleLog2 = 8.f;
+constexpr int kTcMaxChunks = 32;  // chunks per CTA at most when the grid fills the GPU anyway
 
 template <int DQK, int DV>
 struct TcCfg {
@@ -141,6 +142,21 @@ __global__ void __launch_bounds__(192, 2)
     const int r0 = tile * kTcRows;
 
     pdl_trigger();
+    {
+        // a split past the end of this sequence's chunks: only its (max, sum) words
+        // (empty), for the split combine; nothing else is set up
+        int cx = p.ctx_len[b];
+        if (cx < 0 || cx > p.max_ctx) cx = 0;
+        if (split * p.cps > (cx + kTcKeys - 1) / kTcKeys) {
+            if (p.splits > 1 && part == 0 && threadIdx.x >= 64) {
+                pdl_wait();
+                const int rr = r0 + (int)threadIdx.x - 64;
+                if (rr < p.R)
+                    *(float2 *)(p.part_ml + (((size_t)b * p.splits + split) * p.R + rr) * 2) = make_float2(-INFINITY, 0.f);
+            }
+            return;
+        }
+    }
     if (threadIdx.x == 0) {
         for (int i = 0; i < kTcStages; ++i) {
             mbar_init(&kv_full[i], 1);
@@ -489,6 +505,11 @@ int attention_tc_splits(int R, int dv, int bs, int max_ctx, int num_sms, int *cp
     const int chunks = (max_ctx + kTcKeys - 1) / kTcKeys + 1;
     int s = num_sms / (tiles * parts * bs);
     if (s < 1) s = 1;
+    // When the unsplit grid already fills the GPU (many sequences), the contexts
+    // differ and each CTA would walk its own sequence's whole context: split so
+    // that no CTA takes more than kTcMaxChunks chunks (short sequences leave
+    // their upper splits empty; those CTAs exit at once).
+    if (tiles * parts * bs >= num_sms) s = max(s, (chunks + kTcMaxChunks - 1) / kTcMaxChunks);
     if (s > chunks) s = chunks;
     if (s > 20) s = 20;  // the fused split combine takes up to 20 splits
     *cps = (chunks + s - 1) / s;

@@ -22,6 +22,7 @@ struct AttnParams {
     const __nv_bfloat16 *blk_kv;    // [bs * block, DQK]
     int block;
     int splits, tok_per_split;      // KV split plan (tok_per_split a multiple of 64)
+    int cps;                        // tensor-core path: 64-token chunks per split (split s: chunks s cps ..)
     float scale_log2;               // softmax scale * log2(e)
     float *o_lat;                   // [bs, R, DV]
     float *part_o;                  // [bs, splits, R, DV]

@@ -676,7 +676,8 @@ constexpr int kCVParts = kCVThreads / kCVPairs;  // latent parts (8)
 __global__ void __launch_bounds__(kCVThreads) attn_combine_vabsorb_kernel(
     const float *__restrict__ part_o, const float *__restrict__ part_ml, int splits, int R,
     const float *__restrict__ o_lat, int M, int n_h, int block, int d_nope, int d_v, int kv_lora,
-    const __nv_bfloat16 *__restrict__ w_kvb, __nv_bfloat16 *__restrict__ out) {
+    const __nv_bfloat16 *__restrict__ w_kvb, __nv_bfloat16 *__restrict__ out, const int32_t *__restrict__ ctx_len,
+    int max_ctx, int cps) {
     pdl_trigger();
     extern __shared__ __align__(16) uint8_t smc[];
     const int wstride = kv_lora * 2 + 16;                              // bytes per staged v_b row
@@ -701,6 +702,11 @@ __global__ void __launch_bounds__(kCVThreads) attn_combine_vabsorb_kernel(
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
             if (mm < mr) {
                 const int m = m0 + mm, b = m / block, r = (m % block) * n_h + h;
+                // the splits that hold chunks of this sequence (the others wrote only
+                // an empty (max, sum) pair and no partial)
+                int cx = ctx_len[b];
+                if (cx < 0 || cx > max_ctx) cx = 0;
+                const int nsv = min(splits, ((cx + 63) / 64 + 1 + cps - 1) / cps);
                 const float *ml = part_ml + ((size_t)b * splits * R + r) * 2;
                 const float4 *src = (const float4 *)(part_o + ((size_t)b * splits * R + r) * kv_lora) + c4;
                 const size_t sstep = (size_t)R * kv_lora / 4;
@@ -708,17 +714,17 @@ __global__ void __launch_bounds__(kCVThreads) attn_combine_vabsorb_kernel(
                 float4 v[kCVMaxSplit];
 #pragma unroll
                 for (int s = 0; s < kCVMaxSplit; ++s) {
-                    w[s] = s < splits ? __ldcg((const float2 *)(ml + (size_t)s * R * 2)) : make_float2(0.f, 0.f);
-                    v[s] = s < splits ? __ldcg(src + s * sstep) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    w[s] = s < nsv ? __ldcg((const float2 *)(ml + (size_t)s * R * 2)) : make_float2(0.f, 0.f);
+                    v[s] = s < nsv ? __ldcg(src + s * sstep) : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
                 float mx = -INFINITY;
 #pragma unroll
                 for (int s = 0; s < kCVMaxSplit; ++s)
-                    if (s < splits && w[s].y > 0.f) mx = fmaxf(mx, w[s].x);
+                    if (s < nsv && w[s].y > 0.f) mx = fmaxf(mx, w[s].x);
                 float den = 0.f;
 #pragma unroll
                 for (int s = 0; s < kCVMaxSplit; ++s) {
-                    if (s < splits && w[s].y > 0.f) {
+                    if (s < nsv && w[s].y > 0.f) {
                         const float e = exp2f(w[s].x - mx);
                         den += e * w[s].y;
                         acc.x += e * v[s].x;
@@ -1128,7 +1134,8 @@ __global__ void attn_combine_kernel(const float *__restrict__ part_o, const floa
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 8
         for (int s = 0; s < splits; ++s) {
-            const float w = sml[s][1] > 0.f ? exp2f(sml[s][0] - M) : 0.f;
+            if (!(sml[s][1] > 0.f)) continue;  // an empty split wrote no partial
+            const float w = exp2f(sml[s][0] - M);
             const float4 v = __ldcg((const float4 *)(part_o + (base + (size_t)s * R) * DV + c));
             acc.x += w * v.x;
             acc.y += w * v.y;
@@ -1374,7 +1381,7 @@ cudaError_t launch_attn_combine_vabsorb(const AttnParams &p, int M, int n_h, int
     }
     return launch_pdl(attn_combine_vabsorb_kernel, dim3(n_h, (M + kCVRows - 1) / kCVRows), dim3(kCVThreads), smem,
                       st, p.part_o, p.part_ml, p.splits, p.R, p.o_lat, M, n_h, p.block, d_nope, d_v, kv_lora, w_kvb,
-                      out);
+                      out, p.ctx_len, p.max_ctx, p.cps > 0 ? p.cps : 1 << 20);
 }
 
 cudaError_t launch_attn_combine(const AttnParams &p, int bs, int dv, cudaStream_t st) {

@@ -55,6 +55,10 @@ def test_tiny_step_draft(M):
     (MIDLAT, 3, (1000, 77, 4097)),  # tensor-core attention: partial pages, a one-token last page, splits
     (MIDLAT, 1, (0,)),             # tensor-core attention: only the block's own latents
     (MIDLAT, 2, (64, 640)),        # tensor-core attention: contexts ending on page boundaries
+    # 26 sequences fill the GPU with unsplit CTAs, so the split plan caps the chunks per
+    # CTA: long contexts take two splits, short ones leave their second split empty
+    (MIDLAT, 26, (3000, 10, 1600, 0, 500, 2047, 64, 2900, 1535, 1537, 77, 3000, 128, 250, 1800, 999,
+                  2500, 5, 1400, 2222, 640, 1600, 300, 2800, 1, 1536)),
 ])
 def test_mid_draft(M, G, bs, ctx):
     w = workload(G, bs, ctx, seed=7)
