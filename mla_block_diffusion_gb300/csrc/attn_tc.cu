@@ -41,7 +41,7 @@ constexpr int kTcKeys = 64;      // keys per chunk (one page)
 constexpr int kTcStages = 2;     // KV chunk stages in shared memory
 constexpr int kTcPgAhead = 8;    // page numbers the producer reads ahead of their chunks
 constexpr float kTcRescaleLog2 = 8.f;
-constexpr int kTcMaxChunks = 32;  // chunks per CTA at most when the grid fills the GPU anyway
+constexpr int kTcMaxChunks = 48;  // chunks per CTA at most when the grid fills the GPU anyway
 
 template <int DQK, int DV>
 struct TcCfg {

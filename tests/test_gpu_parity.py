@@ -57,8 +57,8 @@ def test_tiny_step_draft(M):
     (MIDLAT, 2, (64, 640)),        # tensor-core attention: contexts ending on page boundaries
     # 26 sequences fill the GPU with unsplit CTAs, so the split plan caps the chunks per
     # CTA: long contexts take two splits, short ones leave their second split empty
-    (MIDLAT, 26, (3000, 10, 1600, 0, 500, 2047, 64, 2900, 1535, 1537, 77, 3000, 128, 250, 1800, 999,
-                  2500, 5, 1400, 2222, 640, 1600, 300, 2800, 1, 1536)),
+    (MIDLAT, 26, (4000, 10, 1600, 0, 500, 2047, 64, 3900, 1535, 2049, 77, 3100, 128, 250, 1800, 999,
+                  2500, 5, 1400, 2222, 640, 1600, 300, 2800, 1, 2048)),
 ])
 def test_mid_draft(M, G, bs, ctx):
     w = workload(G, bs, ctx, seed=7)
