@@ -246,8 +246,8 @@ Layout layout_for(const dspark_handle *h, int bs, int max_ctx) {
     L.scratch = take((sw1 > sw2 ? sw1 : sw2) * 8);
     // latent-cache append: up to block + 1 new tokens per sequence
     const size_t A = (size_t)(g.block + 1) * bs;
-    L.app_hn = take(A * g.hidden * 2);
-    L.app_kv = take(A * kvd * 4);
+    L.app_hn = take((size_t)g.n_layers * A * g.hidden * 2);
+    L.app_kv = take((size_t)g.n_layers * A * kvd * 4);
     L.total = off;
     return L;
 }
@@ -321,6 +321,52 @@ cudaError_t gemm(const dspark_handle *h, const CUtensorMap &A, const CUtensorMap
         case 64: return gemm_t<64>(A, a2, B, p, h->num_sms, st, pend);
         case 128: return gemm_t<128>(A, a2, B, p, h->num_sms, st, pend);
         default: return gemm_t<224>(A, a2, B, p, h->num_sms, st, pend);
+    }
+}
+
+template <int BN>
+cudaError_t gemm_layers_t(const GemmMaps &maps, const CUtensorMap &B, GemmParams p, int num_sms, cudaStream_t st) {
+    using C = GemmCfg<BN>;
+    static bool attr = false;
+    if (!attr) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(gemm_layers_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    gemm_grid(p, 4, num_sms, BN, nullptr);
+    p.pair_red = 0;
+    return launch_pdl(gemm_layers_kernel<BN>, dim3(p.grid), dim3(192), (size_t)C::kSmemBytes, st, B, p, maps);
+}
+
+// L matrices of n_out x K (maps.m[0..L)) against activation rows l * M .. of B:
+// out[l] = W_l x_l, [M][n_out] fp32 each, one after another.
+cudaError_t gemm_layers(const dspark_handle *h, const GemmMaps &maps, int L, const CUtensorMap &B, int n_out, int K,
+                        int M, float *out, void *ws, cudaStream_t st) {
+    GemmParams p;
+    memset(&p, 0, sizeof(p));
+    p.n_out = n_out;
+    p.K = K;
+    p.M = M;
+    p.epi = EPI_STORE;
+    p.out_f32 = out;
+    p.ldo = n_out;
+    p.KB = (K + 63) / 64;
+    p.tpl = (n_out + 127) / 128;
+    p.brows = M;
+    p.lay_stride = (long long)M * n_out;
+    p.tiles = L * p.tpl;
+    p.units = (long long)p.tiles * p.KB;
+    if (p.tiles > kMaxCounters) return cudaErrorInvalidValue;
+    p.counters = (int *)((char *)ws + kCtlCounters);
+    p.err = (int *)((char *)ws + kCtlErr);
+    p.partials = (float *)((char *)ws + kCtlBytes);
+    switch (bn_for(M)) {
+        case 16: return gemm_layers_t<16>(maps, B, p, h->num_sms, st);
+        case 32: return gemm_layers_t<32>(maps, B, p, h->num_sms, st);
+        case 64: return gemm_layers_t<64>(maps, B, p, h->num_sms, st);
+        case 128: return gemm_layers_t<128>(maps, B, p, h->num_sms, st);
+        default: return gemm_layers_t<224>(maps, B, p, h->num_sms, st);
     }
 }
 
@@ -871,20 +917,28 @@ dspark_status dspark_kv_append(dspark_handle_t *h, const float *x_new, int n_max
     const int kvd = g.kv_lora + g.d_rope;
     __nv_bfloat16 *hn = (__nv_bfloat16 *)(w + L.app_hn);
     float *kvo = (float *)(w + L.app_kv);
+    const int nl = g.n_layers;
     if (h->c_app_ws != ws || h->c_app_rows != A) {
-        if (!make_map(&h->b_app, hn, A, g.hidden, bn_for(A))) return DSPARK_ERR_CUDA;
+        if (!make_map(&h->b_app, hn, (uint64_t)nl * A, g.hidden, bn_for(A))) return DSPARK_ERR_CUDA;
         h->c_app_ws = ws;
         h->c_app_rows = A;
     }
     const int cap = kv->max_pages * g.page_size;
-    for (int l = 0; l < g.n_layers; ++l) {
-        const dspark_layer_weights_t &W = h->w.layers[l];
-        RUN(launch_rmsnorm(x_new, g.hidden, W.attn_norm, g.hidden, g.eps, hn, g.hidden, nullptr, 0, A, err, s));
-        RUN(gemm(h, h->kva[l], nullptr, h->b_app, kvd, g.hidden, A, EPI_STORE, kvo, nullptr, kvd, ws, s));
-        RUN(launch_kv_scatter(kvo, g.kv_lora, g.d_rope, W.kv_a_norm, g.eps, h->rope, n_new, n_max, kv->ctx_len,
-                              kv->page_table, kv->max_pages, g.page_size, kv->n_pages, cap,
-                              (__nv_bfloat16 *)kv->pools[l], bs, err, s));
+    // The layers' entries do not depend on each other: every layer's pre-norm in
+    // one launch, every layer's kv_a rows in one GEMM launch, one scatter.
+    AppendLayers al;
+    memset(&al, 0, sizeof(al));
+    for (int l = 0; l < nl; ++l) {
+        al.g_attn[l] = h->w.layers[l].attn_norm;
+        al.g_kv[l] = h->w.layers[l].kv_a_norm;
+        al.pool[l] = (__nv_bfloat16 *)kv->pools[l];
     }
+    RUN(launch_append_norm(x_new, g.hidden, al, nl, g.hidden, g.eps, hn, A, err, s));
+    static_assert(sizeof(GemmMaps) == sizeof(h->kva), "one map per layer");
+    RUN(gemm_layers(h, *reinterpret_cast<const GemmMaps *>(h->kva), nl, h->b_app, kvd, g.hidden, A, kvo, ws, s));
+    RUN(launch_kv_scatter_layers(kvo, (size_t)A * kvd, nl, al, g.kv_lora, g.d_rope, g.eps, h->rope, n_new, n_max,
+                                 kv->ctx_len, kv->page_table, kv->max_pages, g.page_size, kv->n_pages, cap, bs, err,
+                                 s));
     // the append is the one call that advances ctx_len (documented in the header)
     RUN(launch_ctx_advance(const_cast<int32_t *>(kv->ctx_len), n_new, n_max, cap, bs, err, s));
     return DSPARK_OK;

@@ -56,6 +56,12 @@ struct GemmParams {
     float gscale, gscale2;
     L2Prefetch pf;      // weights of a later kernel, pulled into L2 by the producer
     const __nv_bfloat16 *act;  // the activations [M, K] (read directly by the FP8 kernel)
+    // Several matrices in one launch (the layers' kv_a rows of the latent-cache
+    // append): tiles [l tpl, (l + 1) tpl) belong to matrix l, whose activations are
+    // rows l brows .. of the B map and whose output starts lay_stride floats after
+    // matrix l - 1's. tpl = 0: one matrix.
+    int tpl, brows;
+    long long lay_stride;
     // Pairwise reduction (every CTA's range covers at least one tile, so a split
     // tile has two contributors): CTA c + 1 takes the tile's last k-blocks first
     // thing, writes them to its slot 2(c + 1) and raises counters[tile]; CTA c,
@@ -196,13 +202,17 @@ __device__ __forceinline__ void gemm_reduce_tile(const GemmParams &p, int tile, 
         gemm_reduce_impl<BN, SCALED, U, false>(p, tile, c_lo, c_hi, et, n);
 }
 
-// Shared memory keeps one CTA per SM; the launch bound of two caps the
-// registers at 170 so that the next (small) kernel's warps fit in the register
-// files of the SM sub-partitions beside this CTA's and start early.
-template <int BN>
-__global__ void __launch_bounds__(192, 2)
-    gemm_swapab_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
-                       const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+// The weight maps of a several-matrix launch.
+struct GemmMaps {
+    CUtensorMap m[DSPARK_MAX_LAYERS];
+};
+
+// The kernel body; MULTI: tiles of several matrices (GemmParams::tpl), the A
+// maps from `maps`, no paired tiles and no pending output.
+template <int BN, bool MULTI>
+DS_DEVINL void gemm_swapab_body(const CUtensorMap *mA, const CUtensorMap *mA2, const CUtensorMap *mB,
+                                const GemmParams &p, const GemmMaps *maps) {
+    const CUtensorMap &tmA = *mA, &tmA2 = *mA2, &tmB = *mB;
     using C = GemmCfg<BN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -237,8 +247,10 @@ __global__ void __launch_bounds__(192, 2)
         fence_mbar_init();
     }
     if (threadIdx.x == 32) {
-        tma_prefetch_desc(&tmA);
-        tma_prefetch_desc(&tmA2);
+        if (!MULTI) {
+            tma_prefetch_desc(&tmA);
+            tma_prefetch_desc(&tmA2);
+        }
         tma_prefetch_desc(&tmB);
     }
     if (warp == 1) tmem_alloc(&s_tmem, C::kTmemCols);
@@ -263,7 +275,11 @@ __global__ void __launch_bounds__(192, 2)
                 mbar_arrive_expect_tx(&full[s], C::kStageBytes);
                 armed |= 1u << s;
                 uint8_t *a = sA + s * C::kABytes;
-                if (p.paired) {
+                if (MULTI) {
+                    const CUtensorMap *ml = &maps->m[tile / p.tpl];
+                    tma_load_2d_hint(a, ml, kb * 64, (tile % p.tpl) * 128, &full[s], pol);
+                    tma_load_2d_hint(a + 8192, ml, kb * 64, (tile % p.tpl) * 128 + 64, &full[s], pol);
+                } else if (p.paired) {
                     tma_load_2d_hint(a, &tmA, kb * 64, tile * 64, &full[s], pol);
                     tma_load_2d_hint(a + 8192, &tmA2, kb * 64, tile * 64, &full[s], pol);
                 } else {
@@ -274,7 +290,8 @@ __global__ void __launch_bounds__(192, 2)
             l2_prefetch_share(p.pf, (unsigned int)cta, (unsigned int)p.grid);
             pdl_wait();
             for (long long it = 0; it < pre; ++it)
-                tma_load_2d(sB + (int)it * C::kBBytes, &tmB, (int)((u0 + it) % p.KB) * 64, 0, &full[(int)it]);
+                tma_load_2d(sB + (int)it * C::kBBytes, &tmB, (int)((u0 + it) % p.KB) * 64,
+                            MULTI ? (int)((u0 + it) / p.KB / p.tpl) * p.brows : 0, &full[(int)it]);
             long long it = pre;
             for (long long u = u0 + pre; u < u1; ++u, ++it) {
                 const int s = (int)(it % C::kStages);
@@ -285,14 +302,18 @@ __global__ void __launch_bounds__(192, 2)
                 armed |= 1u << s;
                 armed_par = (armed_par & ~(1u << s)) | ((round & 1u) << s);
                 uint8_t *a = sA + s * C::kABytes;
-                if (p.paired) {
+                if (MULTI) {
+                    const CUtensorMap *ml = &maps->m[tile / p.tpl];
+                    tma_load_2d_hint(a, ml, kb * 64, (tile % p.tpl) * 128, &full[s], pol);
+                    tma_load_2d_hint(a + 8192, ml, kb * 64, (tile % p.tpl) * 128 + 64, &full[s], pol);
+                } else if (p.paired) {
                     tma_load_2d_hint(a, &tmA, kb * 64, tile * 64, &full[s], pol);
                     tma_load_2d_hint(a + 8192, &tmA2, kb * 64, tile * 64, &full[s], pol);
                 } else {
                     tma_load_2d_hint(a, &tmA, kb * 64, tile * 128, &full[s], pol);
                     tma_load_2d_hint(a + 8192, &tmA, kb * 64, tile * 128 + 64, &full[s], pol);
                 }
-                tma_load_2d(sB + s * C::kBBytes, &tmB, kb * 64, 0, &full[s]);
+                tma_load_2d(sB + s * C::kBBytes, &tmB, kb * 64, MULTI ? (tile / p.tpl) * p.brows : 0, &full[s]);
             }
         } else {
             pdl_wait();
@@ -390,6 +411,10 @@ __global__ void __launch_bounds__(192, 2)
             const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * BN);
             const int slot = (tile == (int)(u0 / p.KB)) ? 2 * cta : 2 * cta + 1;
             const bool final = whole || (pair_head && BN <= 32);
+            // the tile's own matrix (several-matrix launches): its output base and tile index
+            GemmParams pl = p;
+            const int tl = MULTI ? tile % p.tpl : tile;
+            if (MULTI) pl.out_f32 = p.out_f32 + (long long)(tile / p.tpl) * p.lay_stride;
 #pragma unroll
             for (int c0 = 0; c0 < BN; c0 += 16) {
                 float v[16];
@@ -415,11 +440,11 @@ __global__ void __launch_bounds__(192, 2)
                         }
                         named_bar_sync(1, 128);
                     } else {
-                        const int n = tile * 128 + row;
+                        const int n = tl * 128 + row;
                         if (n < p.n_out) {
 #pragma unroll
                             for (int j = 0; j < 16; ++j)
-                                if (c0 + j < p.M) gemm_store(p, n, c0 + j, v[j]);
+                                if (c0 + j < p.M) gemm_store(pl, n, c0 + j, v[j]);
                         }
                     }
                 } else {
@@ -451,7 +476,12 @@ __global__ void __launch_bounds__(192, 2)
                 named_bar_sync(1, 128);
                 if (s_last) {
                     __threadfence();
-                    gemm_reduce_tile<BN, false, 4>(p, tile, c_lo, c_hi, et, nch);
+                    if (MULTI) {
+                        const int n = tl * 128 + et;
+                        if (n < p.n_out) gemm_reduce_impl<BN, false, 4, false>(pl, tile, c_lo, c_hi, et, n);
+                    } else {
+                        gemm_reduce_tile<BN, false, 4>(p, tile, c_lo, c_hi, et, nch);
+                    }
                 }
             }
             u = seg_end;
@@ -472,6 +502,24 @@ __global__ void __launch_bounds__(192, 2)
         tc_fence_after();
         tmem_dealloc(tmem, C::kTmemCols);
     }
+}
+
+// Shared memory keeps one CTA per SM; the launch bound of two caps the
+// registers at 170 so that the next (small) kernel's warps fit in the register
+// files of the SM sub-partitions beside this CTA's and start early.
+template <int BN>
+__global__ void __launch_bounds__(192, 2)
+    gemm_swapab_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
+                       const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+    gemm_swapab_body<BN, false>(&tmA, &tmA2, &tmB, p, nullptr);
+}
+
+// Several matrices of the same shape against their own activation rows in one
+// launch (the layers of the latent-cache append).
+template <int BN>
+__global__ void __launch_bounds__(192, 2)
+    gemm_layers_kernel(const __grid_constant__ CUtensorMap tmB, const GemmParams p, const __grid_constant__ GemmMaps maps) {
+    gemm_swapab_body<BN, true>(&tmB, &tmB, &tmB, p, &maps);
 }
 
 }  // namespace ds

@@ -62,14 +62,24 @@ cudaError_t launch_v_absorb(const float *o_lat, int M, int n_h, int d_nope, int 
 bool attention_supported(int dqk, int dv);
 cudaError_t launch_attention(const AttnParams &p, int bs, int dqk, int dv, cudaStream_t st);
 cudaError_t launch_attn_combine(const AttnParams &p, int bs, int dv, cudaStream_t st);
-// Latent-cache append: rows b * n_max + j (j < n_new[b]) of kv [*, kv_lora + d_rope]
-// become [RMSNorm(c_kv) * g || RoPE(k_r, ctx_len[b] + j)] bf16 in the page pool;
-// then ctx_len[b] += n_new[b]. Positions at or beyond cap, invalid pages and
-// n_new outside [0, n_max] are reported (DSPARK_ERR_OOB) and not written.
-cudaError_t launch_kv_scatter(const float *kv, int kv_lora, int d_rope, const float *g_kv, float eps,
-                              const RopeTable &rt, const int32_t *n_new, int n_max, const int32_t *ctx_len,
-                              const int32_t *page_table, int max_pages, int page, int n_pages, int cap,
-                              __nv_bfloat16 *pool, int bs, int *err, cudaStream_t st);
+// Per-layer pointers of the latent-cache append (first n used).
+struct AppendLayers {
+    const float *g_attn[DSPARK_MAX_LAYERS];  // attention pre-norm gains
+    const float *g_kv[DSPARK_MAX_LAYERS];    // kv_a norm gains
+    __nv_bfloat16 *pool[DSPARK_MAX_LAYERS];  // page pools
+};
+// y[l][m] = RMSNorm(x[m]) * g_attn[l] (bf16, [L][M][H]) for every layer at once.
+cudaError_t launch_append_norm(const float *x, int ldx, const AppendLayers &al, int L, int H, float eps,
+                               __nv_bfloat16 *y, int M, int *err, cudaStream_t st);
+// Latent-cache append, every layer at once: rows b * n_max + j (j < n_new[b]) of
+// layer l's kv [*, kv_lora + d_rope] (at kv + l * kv_stride) become
+// [RMSNorm(c_kv) * g_kv[l] || RoPE(k_r, ctx_len[b] + j)] bf16 in pool[l].
+// Positions at or beyond cap, invalid pages and n_new outside [0, n_max] are
+// reported (DSPARK_ERR_OOB) and not written.
+cudaError_t launch_kv_scatter_layers(const float *kv, size_t kv_stride, int L, const AppendLayers &al, int kv_lora,
+                                     int d_rope, float eps, const RopeTable &rt, const int32_t *n_new, int n_max,
+                                     const int32_t *ctx_len, const int32_t *page_table, int max_pages, int page,
+                                     int n_pages, int cap, int bs, int *err, cudaStream_t st);
 cudaError_t launch_ctx_advance(int32_t *ctx_len, const int32_t *n_new, int n_max, int cap, int bs, int *err,
                                cudaStream_t st);
 // Tensor-core attention (latent 512 + rope 64): pool_map views one layer's page

@@ -1187,19 +1187,22 @@ __global__ void confidence_kernel(const float *__restrict__ h_out, int H, const 
 // block rows -- written at pos = ctx_len + j through the page table. One CTA per
 // (token slot, sequence); slots j >= n_new[b] write nothing.
 // ---------------------------------------------------------------------------
-__global__ void kv_scatter_kernel(const float *__restrict__ kv, int kv_lora, int d_rope,
-                                  const float *__restrict__ g_kv, float eps, RopeTable rt,
+__global__ void kv_scatter_kernel(const float *__restrict__ kv_all, size_t kv_stride, AppendLayers al, int kv_lora,
+                                  int d_rope, float eps, RopeTable rt,
                                   const int32_t *__restrict__ n_new, int n_max, const int32_t *__restrict__ ctx_len,
                                   const int32_t *__restrict__ page_table, int max_pages, int page, int n_pages, int cap,
-                                  __nv_bfloat16 *__restrict__ pool, int *err) {
+                                  int *err) {
     pdl_trigger();
     pdl_wait();
     __shared__ float red[33];
-    const int j = blockIdx.x, b = blockIdx.y;
+    const int j = blockIdx.x, b = blockIdx.y, l = blockIdx.z;  // token slot, sequence, layer
+    const float *kv = kv_all + (size_t)l * kv_stride;
+    const float *g_kv = al.g_kv[l];
+    __nv_bfloat16 *pool = al.pool[l];
     const int kvd = kv_lora + d_rope;
     const int n = n_new[b];
     if (n < 0 || n > n_max) {
-        if (threadIdx.x == 0 && j == 0) set_error(err, DSPARK_ERR_OOB);
+        if (threadIdx.x == 0 && j == 0 && l == 0) set_error(err, DSPARK_ERR_OOB);
         return;
     }
     if (j >= n) return;
@@ -1229,6 +1232,27 @@ __global__ void kv_scatter_kernel(const float *__restrict__ kv, int kv_lora, int
         dst[kv_lora + 2 * q] = __float2bfloat16(x0 * fc - x1 * fs);
         dst[kv_lora + 2 * q + 1] = __float2bfloat16(x0 * fs + x1 * fc);
     }
+}
+
+// The append's pre-norms: row m of x normalised once and scaled by every
+// layer's gain, y[l][m] = bf16(x[m] * rsqrt(mean x[m]^2 + eps) * g_attn[l]).
+// Grid (M, L).
+__global__ void __launch_bounds__(kNormThreads) append_norm_kernel(const float *__restrict__ x, int ldx,
+                                                                   AppendLayers al, int H, float eps,
+                                                                   __nv_bfloat16 *__restrict__ y, int M, int *err) {
+    pdl_trigger();
+    pdl_wait();
+    __shared__ float red[33];
+    const int m = blockIdx.x, l = blockIdx.y;
+    const float *xr = x + (size_t)m * ldx;
+    float ss = 0.f;
+    for (int i = threadIdx.x; i < H; i += blockDim.x) ss += xr[i] * xr[i];
+    ss = block_sum(ss, red);
+    if (!isfinite(ss) && threadIdx.x == 0 && l == 0) set_error(err, DSPARK_ERR_BAD_INPUT);
+    const float r = rsqrtf(ss / (float)H + eps);
+    const float *g = al.g_attn[l];
+    __nv_bfloat16 *yr = y + ((size_t)l * M + m) * H;
+    for (int i = threadIdx.x; i < H; i += blockDim.x) yr[i] = __float2bfloat16(xr[i] * r * g[i]);
 }
 
 // ctx_len[b] += n_new[b] once every layer's entries are written (a sequence whose
@@ -1389,12 +1413,17 @@ cudaError_t launch_attn_combine(const AttnParams &p, int bs, int dv, cudaStream_
                       p.o_lat);
 }
 
-cudaError_t launch_kv_scatter(const float *kv, int kv_lora, int d_rope, const float *g_kv, float eps,
-                              const RopeTable &rt, const int32_t *n_new, int n_max, const int32_t *ctx_len,
-                              const int32_t *page_table, int max_pages, int page, int n_pages, int cap,
-                              __nv_bfloat16 *pool, int bs, int *err, cudaStream_t st) {
-    return launch_pdl(kv_scatter_kernel, dim3(n_max, bs), dim3(128), 0, st, kv, kv_lora, d_rope, g_kv, eps, rt, n_new,
-                      n_max, ctx_len, page_table, max_pages, page, n_pages, cap, pool, err);
+cudaError_t launch_kv_scatter_layers(const float *kv, size_t kv_stride, int L, const AppendLayers &al, int kv_lora,
+                                     int d_rope, float eps, const RopeTable &rt, const int32_t *n_new, int n_max,
+                                     const int32_t *ctx_len, const int32_t *page_table, int max_pages, int page,
+                                     int n_pages, int cap, int bs, int *err, cudaStream_t st) {
+    return launch_pdl(kv_scatter_kernel, dim3(n_max, bs, L), dim3(128), 0, st, kv, kv_stride, al, kv_lora, d_rope, eps,
+                      rt, n_new, n_max, ctx_len, page_table, max_pages, page, n_pages, cap, err);
+}
+
+cudaError_t launch_append_norm(const float *x, int ldx, const AppendLayers &al, int L, int H, float eps,
+                               __nv_bfloat16 *y, int M, int *err, cudaStream_t st) {
+    return launch_pdl(append_norm_kernel, dim3(M, L), dim3(kNormThreads), 0, st, x, ldx, al, H, eps, y, M, err);
 }
 
 cudaError_t launch_ctx_advance(int32_t *ctx_len, const int32_t *n_new, int n_max, int cap, int bs, int *err,
