@@ -573,12 +573,16 @@ def main():
                  "bound": "hbm", "achieved": fc_achieved, "peak": hbm, "unit": "GB/s", "frac": fc_achieved / hbm,
                  "traffic": traffic, "algorithmic_bytes_per_launch": fc_bytes, "avg_launch_ms": fc_ms,
                  "peak_source": src,
-                 "why_this_launch": "the weight GEMMs are one kernel class (27 launches per step, about three "
-                                    "quarters of the serialised step; the lm_head the longest launch at about "
-                                    "355 us for 2.35 GB); the fc fusion is the one launch of that class the API "
-                                    "isolates (dspark_fuse_ctx), with the same kernel and tiles as the lm_head "
-                                    "and 514 MB of weights, larger than L2, so CUDA events time it alone; the "
-                                    "class's launches and shares: profiles/step_launches_*.md"}
+                 "why_this_launch": ("the weight GEMMs are one kernel class (27 launches per step, about three "
+                                     "quarters of the serialised step; the lm_head the longest launch at about "
+                                     "355 us for 2.35 GB); the fc fusion is the one launch of that class the API "
+                                     "isolates (dspark_fuse_ctx), with the same kernel and tiles as the lm_head "
+                                     "and 514 MB of weights, larger than L2, so CUDA events time it alone; the "
+                                     "class's launches and shares: profiles/step_launches_*.md")
+                 if args.format == "bf16" else
+                 ("the fc fusion is the one launch of the quantised GEMM kernel (21 launches per step: fc, q_b, o, "
+                  "gate/up, down) that the API isolates (dspark_fuse_ctx); q_a||kv_a and the lm_head stay bf16; "
+                  "the launches and shares: profiles/step_launches_*.md")}
     if roofline is None:
         roofline = gemm_line
     else:
