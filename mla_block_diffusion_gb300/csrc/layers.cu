@@ -1218,13 +1218,23 @@ __global__ void kv_scatter_kernel(const float *__restrict__ kv_all, size_t kv_st
         return;
     }
     const float *row = kv + ((size_t)b * n_max + j) * kvd;
+    const float4 *row4 = (const float4 *)row;  // kv_lora a multiple of 64, rows 16-byte aligned
     float ss = 0.f;
-    for (int i = threadIdx.x; i < kv_lora; i += blockDim.x) ss += row[i] * row[i];
+    for (int i = threadIdx.x; i < kv_lora / 4; i += blockDim.x) {
+        const float4 v = row4[i];
+        ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+    }
     ss = block_sum(ss, red);
     if (!isfinite(ss) && threadIdx.x == 0) set_error(err, DSPARK_ERR_BAD_INPUT);
     const float r = rsqrtf(ss / (float)kv_lora + eps);
     __nv_bfloat16 *dst = pool + ((size_t)pg * page + pos % page) * kvd;
-    for (int i = threadIdx.x; i < kv_lora; i += blockDim.x) dst[i] = __float2bfloat16(row[i] * r * g_kv[i]);
+    const float4 *g4 = (const float4 *)g_kv;
+    for (int i = threadIdx.x; i < kv_lora / 4; i += blockDim.x) {
+        const float4 v = row4[i], g = __ldg(g4 + i);
+        const __nv_bfloat162 a = __floats2bfloat162_rn(v.x * r * g.x, v.y * r * g.y);
+        const __nv_bfloat162 c = __floats2bfloat162_rn(v.z * r * g.z, v.w * r * g.w);
+        *(uint2 *)(dst + 4 * i) = make_uint2(*reinterpret_cast<const uint32_t *>(&a), *reinterpret_cast<const uint32_t *>(&c));
+    }
     for (int q = threadIdx.x; q < d_rope / 2; q += blockDim.x) {
         float fc, fs;
         rope_cs((double)pos, rt.inv_freq[q], fc, fs);
@@ -1241,18 +1251,26 @@ __global__ void __launch_bounds__(kNormThreads) append_norm_kernel(const float *
                                                                    AppendLayers al, int H, float eps,
                                                                    __nv_bfloat16 *__restrict__ y, int M, int *err) {
     pdl_trigger();
-    pdl_wait();
     __shared__ float red[33];
-    const int m = blockIdx.x, l = blockIdx.y;
-    const float *xr = x + (size_t)m * ldx;
+    const int m = blockIdx.x, l = blockIdx.y, n4 = H / 4;
+    const float4 *g4 = (const float4 *)al.g_attn[l];
+    pdl_wait();
+    const float4 *xr = (const float4 *)(x + (size_t)m * ldx);
     float ss = 0.f;
-    for (int i = threadIdx.x; i < H; i += blockDim.x) ss += xr[i] * xr[i];
+    for (int i = threadIdx.x; i < n4; i += blockDim.x) {
+        const float4 v = xr[i];
+        ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+    }
     ss = block_sum(ss, red);
     if (!isfinite(ss) && threadIdx.x == 0 && l == 0) set_error(err, DSPARK_ERR_BAD_INPUT);
     const float r = rsqrtf(ss / (float)H + eps);
-    const float *g = al.g_attn[l];
-    __nv_bfloat16 *yr = y + ((size_t)l * M + m) * H;
-    for (int i = threadIdx.x; i < H; i += blockDim.x) yr[i] = __float2bfloat16(xr[i] * r * g[i]);
+    uint2 *yr = (uint2 *)(y + ((size_t)l * M + m) * H);
+    for (int i = threadIdx.x; i < n4; i += blockDim.x) {
+        const float4 v = xr[i], g = __ldg(g4 + i);
+        const __nv_bfloat162 a = __floats2bfloat162_rn(v.x * r * g.x, v.y * r * g.y);
+        const __nv_bfloat162 c = __floats2bfloat162_rn(v.z * r * g.z, v.w * r * g.w);
+        yr[i] = make_uint2(*reinterpret_cast<const uint32_t *>(&a), *reinterpret_cast<const uint32_t *>(&c));
+    }
 }
 
 // ctx_len[b] += n_new[b] once every layer's entries are written (a sequence whose
