@@ -50,8 +50,9 @@ typedef enum {
     DSPARK_ERR_WORKSPACE = 6,     /* workspace pointer null or smaller than required */
     DSPARK_ERR_TIMEOUT = 16,      /* device: a bounded inter-CTA wait expired */
     DSPARK_ERR_BAD_INPUT = 17,    /* device: a logit or intermediate was not finite, an
-                                     activation entering an FP8/NVFP4/MXFP4 GEMM exceeded
-                                     65504, or an MXFP4 scale lies outside 2^-22 .. 2^13 */
+                                     activation entering an NVFP4/MXFP4 GEMM (or an FP8 GEMM
+                                     of more than 32 rows) exceeded 65504, or an MXFP4 scale
+                                     lies outside 2^-22 .. 2^13 */
     DSPARK_ERR_OOB = 18           /* device: page id, token id or ctx_len out of range */
 } dspark_status;
 
@@ -71,8 +72,10 @@ enum { DSPARK_GREEDY = 0, DSPARK_PROBABILISTIC = 1, DSPARK_BLOCK = 2 /* verify_m
  * (E4M3 per output row), NVFP4 (E2M1, E4M3 group-16 scales, global scale;
  * then hidden, q_lora, n_heads*d_v and inter multiples of 256) or MXFP4 (E2M1,
  * E8M0 power-of-two scales per 32 inputs; then those sizes multiples of 512).
- * With FP8, NVFP4 or MXFP4, block * bs <= 64 per call and the activations entering those GEMMs
- * stay within +-65504 (they are taken in f16; see DSPARK_ERR_BAD_INPUT).
+ * With FP8, NVFP4 or MXFP4, block * bs <= 64 per call. FP8 GEMMs of up to 32 rows take
+ * the bf16 activations exactly (as two E4M3 terms per row and 128-k chunk); NVFP4,
+ * MXFP4 and FP8 above 32 rows take them in f16, so they must stay within +-65504
+ * (see DSPARK_ERR_BAD_INPUT).
  */
 typedef struct {
     int hidden, n_aux, n_layers, n_heads;

@@ -1,11 +1,9 @@
-// Markov rollout and lossless verification for the DSpark step.
+// Markov rollout of the DSpark step (verification is in verify.cu).
 //
 // Model cards: a low-rank sequential Markov head drafts the 7 tokens of a
 // block ("Kimi-K3-DSpark-NVFP4", Original model card / Model Overview; Markov
-// rank 256, "Kimi K3 DSpark Q8_0 GGUF", Architecture metadata); the target
-// verifies them in one pass and the output distribution equals the target's
-// ("kimi-k3-dspark-gguf", intro); greedy or probabilistic draft sampling and
-// an argmax match at temperature 0 ("Kimi-K3-DSpark-NVFP4", Sampling options).
+// rank 256, "Kimi K3 DSpark Q8_0 GGUF", Architecture metadata); greedy or
+// probabilistic draft sampling ("Kimi-K3-DSpark-NVFP4", Sampling options).
 //
 // Every decision is made in exact integers on 2^32-scaled weights so that it
 // is reproducible bit for bit: for a logit row l at temperature T,
@@ -14,14 +12,14 @@
 // a 16-bit head, the degree-7 Taylor polynomial in Horner form with fused
 // multiply-adds, then scaling by 2^n). The top-p nucleus is the shortest run of
 // keys (E_v << 18 | (2^18 - 1 - v)) in descending order whose weight reaches
-// tau = max(1, floor(S * P32 / 2^32)); it is found here by an 8-bit radix
-// select over the grid. Draws use 24-bit uniforms from Philox4x32-10 (Salmon et
+// tau = max(1, floor(S * P32 / 2^32)); the rollout finds it over the grid by
+// histogram levels (grid_nucleus below). Draws use 24-bit uniforms from Philox4x32-10 (Salmon et
 // al., SC'11) keyed by the seed with counter (step, seq, pos, purpose) and pick
 // the smallest id whose running weight (ascending ids) exceeds
 // floor(total * W / 2^24).
 //
-// The rollout and the probabilistic verify run cooperatively (all CTAs
-// resident) and synchronise through a bounded grid barrier in the workspace.
+// The rollout runs cooperatively (all CTAs resident) and synchronises through a
+// bounded grid barrier in the workspace.
 #include "sampling_spec.cuh"
 
 #include <algorithm>
