@@ -421,10 +421,29 @@ DS_DEVINL void ring_drain(RollRing &rg) {
         mbar_drain(&rg.full[c % kRollStages], (uint32_t)((c / kRollStages) & 1));
 }
 
+// Two fp32 chains of bf16 products: lo += u * w.lo, hi += u * w.hi, where u is
+// the low (HI = false) or high half of u2. The bf16 operands widen exactly, so
+// each step is one IEEE fp32 FMA with a single rounding (identical to fmaf on
+// the widened values).
+template <bool HI>
+DS_DEVINL void fma_bf16x2(float &lo, float &hi, uint32_t u2, uint32_t w) {
+    if (HI)
+        asm("{\n\t.reg .b16 wl, wh, ul, uh;\n\tmov.b32 {wl, wh}, %2;\n\tmov.b32 {ul, uh}, %3;\n\t"
+            "fma.rn.f32.bf16 %0, uh, wl, %0;\n\tfma.rn.f32.bf16 %1, uh, wh, %1;\n\t}"
+            : "+f"(lo), "+f"(hi)
+            : "r"(w), "r"(u2));
+    else
+        asm("{\n\t.reg .b16 wl, wh, ul, uh;\n\tmov.b32 {wl, wh}, %2;\n\tmov.b32 {ul, uh}, %3;\n\t"
+            "fma.rn.f32.bf16 %0, ul, wl, %0;\n\tfma.rn.f32.bf16 %1, ul, wh, %1;\n\t}"
+            : "+f"(lo), "+f"(hi)
+            : "r"(w), "r"(u2));
+}
+
 // The chains: acc_v = fmaf(u_k, w2[k][v], acc_v) for k in order, per sequence
-// and vocabulary id (each an IEEE fp32 FMA, bit-identical to the oracle's fmaf
-// chain). u (w1[t_{i-1}] as fp32, the same for every thread) comes from shared
-// memory four k at a time (one 16-byte load per sequence), w2 as bf16 pairs.
+// and vocabulary id (each an IEEE fp32 FMA of bf16 operands, bit-identical to the
+// oracle's fmaf chain on the widened values). u (w1[t_{i-1}], bf16, the same for
+// every thread) comes from shared memory eight k at a time (one 16-byte load per
+// sequence); w2 stays in its bf16 pairs.
 // A thread owns its primary pair for all NB sequences of the pass (p0, p1)
 // and, by EX: 0 nothing more; 1 one extra chain, a leftover pair of the CTA for
 // one sequence (s0[0], s1[0]: the leftover pairs' chains are spread one per
@@ -435,77 +454,67 @@ struct RollAcc {
     float p0[NB], p1[NB], s0[NB], s1[NB];
 };
 
-// rows k0 .. k0 + 3 of the chains (k0 a multiple of 4); wv0 / wv1: the w2 pairs
+// rows k0 .. k0 + 7 of the chains (k0 a multiple of 8); wv0 / wv1: the w2 pairs
 template <int NB, int EX>
-DS_DEVINL void roll_rows4(const uint32_t (&wv0)[4], const uint32_t (&wv1)[4], int k0, const float (*s_uf)[256],
+DS_DEVINL void roll_rows8(const uint32_t (&wv0)[8], const uint32_t (&wv1)[8], int k0, const uint16_t (*s_ub)[256],
                           int ex_seq, RollAcc<NB> &a) {
-    float4 u4[NB];
+    uint4 uq[NB];
 #pragma unroll
-    for (int bb = 0; bb < NB; ++bb) u4[bb] = *(const float4 *)&s_uf[bb][k0];
-    float4 ue = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (EX == 1) ue = *(const float4 *)&s_uf[ex_seq][k0];
+    for (int bb = 0; bb < NB; ++bb) uq[bb] = *(const uint4 *)&s_ub[bb][k0];
+    uint4 ue = make_uint4(0u, 0u, 0u, 0u);
+    if (EX == 1) ue = *(const uint4 *)&s_ub[ex_seq][k0];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const float x0 = __uint_as_float(wv0[j] << 16), y0 = __uint_as_float(wv0[j] & 0xFFFF0000u);
-        const float x1 = __uint_as_float(wv1[j] << 16), y1 = __uint_as_float(wv1[j] & 0xFFFF0000u);
+    for (int j = 0; j < 8; ++j) {
 #pragma unroll
         for (int bb = 0; bb < NB; ++bb) {
-            const float u = j == 0 ? u4[bb].x : j == 1 ? u4[bb].y : j == 2 ? u4[bb].z : u4[bb].w;
-            a.p0[bb] = __fmaf_rn(u, x0, a.p0[bb]);
-            a.p1[bb] = __fmaf_rn(u, y0, a.p1[bb]);
-            if (EX == 2) {
-                a.s0[bb] = __fmaf_rn(u, x1, a.s0[bb]);
-                a.s1[bb] = __fmaf_rn(u, y1, a.s1[bb]);
+            const uint32_t u2 = (j >> 1) == 0 ? uq[bb].x : (j >> 1) == 1 ? uq[bb].y : (j >> 1) == 2 ? uq[bb].z : uq[bb].w;
+            if (j & 1) {
+                fma_bf16x2<true>(a.p0[bb], a.p1[bb], u2, wv0[j]);
+                if (EX == 2) fma_bf16x2<true>(a.s0[bb], a.s1[bb], u2, wv1[j]);
+            } else {
+                fma_bf16x2<false>(a.p0[bb], a.p1[bb], u2, wv0[j]);
+                if (EX == 2) fma_bf16x2<false>(a.s0[bb], a.s1[bb], u2, wv1[j]);
             }
         }
         if (EX == 1) {
-            const float u = j == 0 ? ue.x : j == 1 ? ue.y : j == 2 ? ue.z : ue.w;
-            a.s0[0] = __fmaf_rn(u, x1, a.s0[0]);
-            a.s1[0] = __fmaf_rn(u, y1, a.s1[0]);
+            const uint32_t u2 = (j >> 1) == 0 ? ue.x : (j >> 1) == 1 ? ue.y : (j >> 1) == 2 ? ue.z : ue.w;
+            if (j & 1)
+                fma_bf16x2<true>(a.s0[0], a.s1[0], u2, wv1[j]);
+            else
+                fma_bf16x2<false>(a.s0[0], a.s1[0], u2, wv1[j]);
         }
     }
 }
-// one row k of the chains (the tail of a chunk whose length is not a multiple of 4)
+// one row k of the chains (tails whose length is not a multiple of 8)
 template <int NB, int EX>
-DS_DEVINL void roll_row1(uint32_t wv0, uint32_t wv1, int k, const float (*s_uf)[256], int ex_seq, RollAcc<NB> &a) {
-    const float x0 = __uint_as_float(wv0 << 16), y0 = __uint_as_float(wv0 & 0xFFFF0000u);
-    const float x1 = __uint_as_float(wv1 << 16), y1 = __uint_as_float(wv1 & 0xFFFF0000u);
+DS_DEVINL void roll_row1(uint32_t wv0, uint32_t wv1, int k, const uint16_t (*s_ub)[256], int ex_seq, RollAcc<NB> &a) {
 #pragma unroll
     for (int bb = 0; bb < NB; ++bb) {
-        const float u = s_uf[bb][k];
-        a.p0[bb] = __fmaf_rn(u, x0, a.p0[bb]);
-        a.p1[bb] = __fmaf_rn(u, y0, a.p1[bb]);
-        if (EX == 2) {
-            a.s0[bb] = __fmaf_rn(u, x1, a.s0[bb]);
-            a.s1[bb] = __fmaf_rn(u, y1, a.s1[bb]);
-        }
+        const uint32_t u2 = s_ub[bb][k];
+        fma_bf16x2<false>(a.p0[bb], a.p1[bb], u2, wv0);
+        if (EX == 2) fma_bf16x2<false>(a.s0[bb], a.s1[bb], u2, wv1);
     }
-    if (EX == 1) {
-        const float u = s_uf[ex_seq][k];
-        a.s0[0] = __fmaf_rn(u, x1, a.s0[0]);
-        a.s1[0] = __fmaf_rn(u, y1, a.s1[0]);
-    }
+    if (EX == 1) fma_bf16x2<false>(a.s0[0], a.s1[0], (uint32_t)s_ub[ex_seq][k], wv1);
 }
 
 // One streamed chunk of rows k0 .. k0 + rows - 1.
 template <int NB, int EX>
 DS_DEVINL void roll_chunk(const uint32_t *w, int wpr, int rows, int k0, int o0, int o1, bool has0, bool has1,
-                          const float (*s_uf)[256], int ex_seq, RollAcc<NB> &a) {
+                          const uint16_t (*s_ub)[256], int ex_seq, RollAcc<NB> &a) {
     int kk = 0;
-    if ((k0 & 3) == 0) {
-#pragma unroll 2
-        for (; kk + 4 <= rows; kk += 4) {
-            uint32_t wv0[4], wv1[4];
+    if ((k0 & 7) == 0) {
+        for (; kk + 8 <= rows; kk += 8) {
+            uint32_t wv0[8], wv1[8];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < 8; ++j) {
                 wv0[j] = has0 ? w[(kk + j) * wpr + o0] : 0u;
                 wv1[j] = (EX != 0 && has1) ? w[(kk + j) * wpr + o1] : 0u;
             }
-            roll_rows4<NB, EX>(wv0, wv1, k0 + kk, s_uf, ex_seq, a);
+            roll_rows8<NB, EX>(wv0, wv1, k0 + kk, s_ub, ex_seq, a);
         }
     }
     for (; kk < rows; ++kk)
-        roll_row1<NB, EX>(has0 ? w[kk * wpr + o0] : 0u, (EX != 0 && has1) ? w[kk * wpr + o1] : 0u, k0 + kk, s_uf,
+        roll_row1<NB, EX>(has0 ? w[kk * wpr + o0] : 0u, (EX != 0 && has1) ? w[kk * wpr + o1] : 0u, k0 + kk, s_ub,
                           ex_seq, a);
 }
 
@@ -514,42 +523,42 @@ DS_DEVINL void roll_chunk(const uint32_t *w, int wpr, int rows, int k0, int o0, 
 // Warp-collective.
 template <int NB, int EX>
 DS_DEVINL void roll_tmem16(const uint32_t (&v)[16], int k16, int kt, const uint32_t (*s_sec)[kRollSec], int sp,
-                           bool has1, const float (*s_uf)[256], int ex_seq, RollAcc<NB> &a) {
+                           bool has1, const uint16_t (*s_ub)[256], int ex_seq, RollAcc<NB> &a) {
     if (k16 + 16 <= kt) {
 #pragma unroll
-        for (int j4 = 0; j4 < 16; j4 += 4) {
-            uint32_t wv0[4], wv1[4];
+        for (int j8 = 0; j8 < 16; j8 += 8) {
+            uint32_t wv0[8], wv1[8];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                wv0[j] = v[j4 + j];
-                wv1[j] = (EX != 0 && has1) ? s_sec[k16 + j4 + j][sp] : 0u;
+            for (int j = 0; j < 8; ++j) {
+                wv0[j] = v[j8 + j];
+                wv1[j] = (EX != 0 && has1) ? s_sec[k16 + j8 + j][sp] : 0u;
             }
-            roll_rows4<NB, EX>(wv0, wv1, k16 + j4, s_uf, ex_seq, a);
+            roll_rows8<NB, EX>(wv0, wv1, k16 + j8, s_ub, ex_seq, a);
         }
     } else {
 #pragma unroll
         for (int j = 0; j < 16; ++j)
             if (k16 + j < kt)
-                roll_row1<NB, EX>(v[j], (EX != 0 && has1) ? s_sec[k16 + j][sp] : 0u, k16 + j, s_uf, ex_seq, a);
+                roll_row1<NB, EX>(v[j], (EX != 0 && has1) ? s_sec[k16 + j][sp] : 0u, k16 + j, s_ub, ex_seq, a);
     }
 }
 template <int NB, int EX>
 DS_DEVINL void roll_tmem_rows(uint32_t taddr, int kt, const uint32_t (*s_sec)[kRollSec], int sp, bool has1,
-                              const float (*s_uf)[256], int ex_seq, RollAcc<NB> &a) {
+                              const uint16_t (*s_ub)[256], int ex_seq, RollAcc<NB> &a) {
     for (int k16 = 0; k16 < kt; k16 += 16) {
         uint32_t v[16];
         tmem_ld16u(taddr + (uint32_t)k16, v);
-        roll_tmem16<NB, EX>(v, k16, kt, s_sec, sp, has1, s_uf, ex_seq, a);
+        roll_tmem16<NB, EX>(v, k16, kt, s_sec, sp, has1, s_ub, ex_seq, a);
     }
 }
 
 // The chains of one pass in a given EX mode.
 template <int NB, int EX>
 DS_DEVINL bool roll_pass(const RolloutParams &p, const CUtensorMap *tm, int lo, RollRing &rg, uint32_t taddr,
-                         const uint32_t (*s_sec)[kRollSec], const float (*s_uf)[256], int sp, int ex_seq, bool has0,
+                         const uint32_t (*s_sec)[kRollSec], const uint16_t (*s_ub)[256], int sp, int ex_seq, bool has0,
                          bool has1, int o0, int o1, uint64_t pol, volatile int *s_fail, RollAcc<NB> &acc) {
     const int r = p.r, lane = threadIdx.x & 31;
-    if (rg.kt > 0) roll_tmem_rows<NB, EX>(taddr, rg.kt, s_sec, sp, has1, s_uf, ex_seq, acc);
+    if (rg.kt > 0) roll_tmem_rows<NB, EX>(taddr, rg.kt, s_sec, sp, has1, s_ub, ex_seq, acc);
     bool failed = false;
     for (int ch = 0; ch < rg.nchunks; ++ch) {
         const long long c = rg.consumed;
@@ -561,7 +570,7 @@ DS_DEVINL bool roll_pass(const RolloutParams &p, const CUtensorMap *tm, int lo, 
         if (!failed) {
             const uint32_t *w = (const uint32_t *)(rg.stage + (size_t)s * rg.stage_bytes);
             const int k0 = rg.kt + ch * kRollKC, rows = min(kRollKC, r - k0);
-            roll_chunk<NB, EX>(w, rg.box_w, rows, k0, o0, o1, has0, has1, s_uf, ex_seq, acc);
+            roll_chunk<NB, EX>(w, rg.box_w, rows, k0, o0, o1, has0, has1, s_ub, ex_seq, acc);
             rg.consumed = c + 1;
         }
         __syncwarp();
@@ -579,7 +588,7 @@ DS_DEVINL bool roll_pass(const RolloutParams &p, const CUtensorMap *tm, int lo, 
 template <int NB>
 __device__ void rollout_logits(const RolloutParams &p, const CUtensorMap *tm, int i, int b0, int nb, int lo, int hi,
                                RollRing &rg, uint32_t taddr, const uint32_t (*s_sec)[kRollSec],
-                               const float (*s_uf)[256], unsigned long long *amax,
+                               const uint16_t (*s_ub)[256], unsigned long long *amax,
                                unsigned long long (*red8)[kRollWarps], uint64_t pol, volatile int *s_fail) {
     const int V = p.V;
     RollAcc<NB> acc;
@@ -602,11 +611,11 @@ __device__ void rollout_logits(const RolloutParams &p, const CUtensorMap *tm, in
     const int o1 = (q1 / rg.box_w) * kRollKC * rg.box_w + q1 % rg.box_w;
     bool ok;
     if (!two)
-        ok = roll_pass<NB, 0>(p, tm, lo, rg, taddr, s_sec, s_uf, sp, ex_seq, has0, has1, o0, o1, pol, s_fail, acc);
+        ok = roll_pass<NB, 0>(p, tm, lo, rg, taddr, s_sec, s_ub, sp, ex_seq, has0, has1, o0, o1, pol, s_fail, acc);
     else if (spread)
-        ok = roll_pass<NB, 1>(p, tm, lo, rg, taddr, s_sec, s_uf, sp, ex_seq, has0, has1, o0, o1, pol, s_fail, acc);
+        ok = roll_pass<NB, 1>(p, tm, lo, rg, taddr, s_sec, s_ub, sp, ex_seq, has0, has1, o0, o1, pol, s_fail, acc);
     else
-        ok = roll_pass<NB, 2>(p, tm, lo, rg, taddr, s_sec, s_uf, sp, ex_seq, has0, has1, o0, o1, pol, s_fail, acc);
+        ok = roll_pass<NB, 2>(p, tm, lo, rg, taddr, s_sec, s_ub, sp, ex_seq, has0, has1, o0, o1, pol, s_fail, acc);
     if (!ok) *s_fail = 1;
     unsigned long long best[NB];
 #pragma unroll
@@ -677,7 +686,7 @@ __global__ void __launch_bounds__(kSampThreads, 1)
     rollout_kernel(const __grid_constant__ CUtensorMap tmW2, RolloutParams p) {
     __shared__ NucleusSmem sm;
     __shared__ DrawSmem dsm;
-    __shared__ __align__(16) float s_uf[kRollChunk][256];  // w1[t_{i-1}] as fp32, per sequence of the pass
+    __shared__ __align__(16) uint16_t s_ub[kRollChunk][256];  // w1[t_{i-1}] (bf16 bits), per sequence of the pass
     __shared__ unsigned long long s_red8[kRollChunk][kRollWarps];
     __shared__ __align__(8) uint64_t s_full[kRollStages], s_empty[kRollStages];
     __shared__ int s_prev[kMaxSampBs];
@@ -766,16 +775,15 @@ __global__ void __launch_bounds__(kSampThreads, 1)
             const int nb = min(kRollChunk, p.bs - b0);
             for (int idx = threadIdx.x; idx < kRollChunk * r; idx += blockDim.x) {
                 const int bb = idx / r, k = idx % r;
-                const float u = bb < nb ? __bfloat162float(p.w1[(size_t)s_prev[b0 + bb] * r + k]) : 0.f;
-                s_uf[bb][k] = u;
+                s_ub[bb][k] = bb < nb ? __bfloat16_as_ushort(p.w1[(size_t)s_prev[b0 + bb] * r + k]) : (uint16_t)0;
             }
             __syncthreads();
             if (hi > lo) {
                 if (nb == 1)
-                    rollout_logits<1>(p, &tmW2, i, b0, 1, lo, hi, rg, taddr, s_sec, s_uf,
+                    rollout_logits<1>(p, &tmW2, i, b0, 1, lo, hi, rg, taddr, s_sec, s_ub,
                                       sc + L.amax + (size_t)i * p.bs, s_red8, pol, &s_fail);
                 else
-                    rollout_logits<kRollChunk>(p, &tmW2, i, b0, nb, lo, hi, rg, taddr, s_sec, s_uf,
+                    rollout_logits<kRollChunk>(p, &tmW2, i, b0, nb, lo, hi, rg, taddr, s_sec, s_ub,
                                                sc + L.amax + (size_t)i * p.bs, s_red8, pol, &s_fail);
             }
             __syncthreads();
@@ -876,24 +884,6 @@ struct ResLayout {  // dynamic shared memory, bytes
         total = bars + kResSlots * 8;
     }
 };
-
-// Two fp32 chains of bf16 products: lo += u * w.lo, hi += u * w.hi, where u is
-// the low (HI = false) or high half of u2. The bf16 operands widen exactly, so
-// each step is one IEEE fp32 FMA with a single rounding (identical to fmaf on
-// the widened values).
-template <bool HI>
-DS_DEVINL void fma_bf16x2(float &lo, float &hi, uint32_t u2, uint32_t w) {
-    if (HI)
-        asm("{\n\t.reg .b16 wl, wh, ul, uh;\n\tmov.b32 {wl, wh}, %2;\n\tmov.b32 {ul, uh}, %3;\n\t"
-            "fma.rn.f32.bf16 %0, uh, wl, %0;\n\tfma.rn.f32.bf16 %1, uh, wh, %1;\n\t}"
-            : "+f"(lo), "+f"(hi)
-            : "r"(w), "r"(u2));
-    else
-        asm("{\n\t.reg .b16 wl, wh, ul, uh;\n\tmov.b32 {wl, wh}, %2;\n\tmov.b32 {ul, uh}, %3;\n\t"
-            "fma.rn.f32.bf16 %0, ul, wl, %0;\n\tfma.rn.f32.bf16 %1, ul, wh, %1;\n\t}"
-            : "+f"(lo), "+f"(hi)
-            : "r"(w), "r"(u2));
-}
 
 // Chains of this thread's pairs (four fp32 accumulators: primary lo/hi, secondary lo/hi).
 struct ResAcc {
