@@ -96,6 +96,7 @@ constexpr int kMaxLevels = 8;        // level 0 + at most 5 refinements of the 4
 constexpr int kMassSlices = 64;      // CTAs per block-verification row for the residual masses (2 per lane of a warp)
 constexpr size_t kStageMax = 200 * 1024;  // largest staging of the draw rows in shared memory
 constexpr int kStatWords = 4;
+constexpr int kNucBatch = 5;         // float4 loads in flight per thread in the row pass
 
 // Part [lo, hi) of cluster rank c over ids [r0, r1): whole quads from r0, the
 // last CTA to r1.
@@ -404,16 +405,27 @@ __global__ void __launch_bounds__(kVThreads, 1) nucleus_rows_kernel(VerifyParams
         }
         s_lt = tok >= 0 ? row[tok] : 0.f;
     }
-    // 1. y = l / T into shared memory, this CTA's max
+    // 1. y = l / T into shared memory, this CTA's max (the thread's float4 loads
+    // issued kNucBatch at a time, so the part costs one or two HBM round trips)
     const float *rp = row + lo;
     unsigned long long mx = 0;
     bool bad = false;
-    for (int j = 4 * t; j < n; j += 4 * kVThreads) {
-        const float4 l = __ldg((const float4 *)(rp + j));
-        const float y0 = div_T(l.x, T), y1 = div_T(l.y, T), y2 = div_T(l.z, T), y3 = div_T(l.w, T);
-        if (!isfinite(y0) || !isfinite(y1) || !isfinite(y2) || !isfinite(y3)) bad = true;
-        *(float4 *)(yv + j) = make_float4(y0, y1, y2, y3);
-        mx = max(mx, (unsigned long long)max(max(f2ord(y0), f2ord(y1)), max(f2ord(y2), f2ord(y3))));
+    for (int j0 = 4 * t; j0 < n; j0 += 4 * kVThreads * kNucBatch) {
+        float4 l[kNucBatch];
+#pragma unroll
+        for (int u = 0; u < kNucBatch; ++u) {
+            const int j = j0 + 4 * kVThreads * u;
+            l[u] = j < n ? __ldg((const float4 *)(rp + j)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < kNucBatch; ++u) {
+            const int j = j0 + 4 * kVThreads * u;
+            if (j >= n) break;
+            const float y0 = div_T(l[u].x, T), y1 = div_T(l[u].y, T), y2 = div_T(l[u].z, T), y3 = div_T(l[u].w, T);
+            if (!isfinite(y0) || !isfinite(y1) || !isfinite(y2) || !isfinite(y3)) bad = true;
+            *(float4 *)(yv + j) = make_float4(y0, y1, y2, y3);
+            mx = max(mx, (unsigned long long)max(max(f2ord(y0), f2ord(y1)), max(f2ord(y2), f2ord(y3))));
+        }
     }
     if (bad) set_error(p.err, DSPARK_ERR_BAD_INPUT);
     mx = block_max_u64(mx, red);
@@ -721,52 +733,6 @@ DS_DEVINL bool stage_rows(float *dst0, const float *row0, float *dst1, const flo
     return ok;
 }
 
-// A weighted pick by one CTA over ids [r0, r1): the smallest v whose running
-// weight base + sum_{r0 <= u <= v} weight(u) exceeds `target` (warp segments
-// summed with coalesced reads; the warp holding the target walks it
-// lane-contiguously). Writes v to *out (nothing when no weight reaches it).
-template <class WF>
-DS_DEVINL void cta_pick(WF weight, int r0, int r1, unsigned __int128 base, unsigned __int128 target, int32_t *out,
-                        DrawScan &ds_) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = (int)(blockDim.x >> 5);
-    const int n = r1 - r0;
-    const int segw = 32 * ((n + 32 * nw - 1) / (32 * nw));
-    const int s0 = r0 + warp * segw, s1 = min(r1, s0 + segw);
-    unsigned __int128 mine = 0;
-    for (int v = s0 + lane; v < s1; v += 32) mine += weight(v);
-    mine = warp_sum_u128(mine);
-    if (lane == 0) u128_split(mine, ds_.wlo[warp], ds_.whi[warp]);
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        unsigned __int128 acc = base;
-        for (int w = 0; w < nw; ++w) {
-            const unsigned __int128 x = u128_join(ds_.wlo[w], ds_.whi[w]);
-            u128_split(acc, ds_.wlo[w], ds_.whi[w]);
-            acc += x;
-        }
-    }
-    __syncthreads();
-    const unsigned __int128 start = u128_join(ds_.wlo[warp], ds_.whi[warp]);
-    if (s0 < s1 && start <= target && target < start + mine) {
-        const int per = (s1 - s0 + 31) / 32;
-        const int v0 = s0 + lane * per, v1 = min(s1, v0 + per);
-        unsigned __int128 run = 0;
-        for (int v = v0; v < v1; ++v) run += weight(v);
-        const unsigned __int128 incl = warp_incl_u128(run);
-        const unsigned __int128 st0 = start + incl - run;
-        if (v0 < v1 && st0 <= target && target < st0 + run) {
-            unsigned __int128 cum = st0;
-            for (int v = v0; v < v1; ++v) {
-                cum += weight(v);
-                if (cum > target) {
-                    *out = v;
-                    break;
-                }
-            }
-        }
-    }
-}
-
 // ---------------------------------------------------------------------------
 // Token-by-token probabilistic verification. Accept t_i iff
 // U * Eq_t * Sp < 2^32 * Ep_t * Sq (U 32-bit, purpose 2); on the first reject
@@ -780,34 +746,6 @@ DS_DEVINL void cta_pick(WF weight, int r0, int r1, unsigned __int128 base, unsig
 // ---------------------------------------------------------------------------
 constexpr int kDrawSlices = 128;
 
-// Warp 0: the number of accepted drafts of sequence b (B if all), and this
-// lane's drafted token (position = lane).
-DS_DEVINL int token_accepts(const VerifyParams &p, int b, int &t) {
-    const int a = threadIdx.x & 31, B = p.B, V = p.V, R = ver_rows_per_seq(p);
-    bool acc = false;
-    t = 0;
-    if (a < B) {
-        t = p.tokens[b * B + a];
-        if (t < 0 || t >= V) {
-            set_error(p.err, DSPARK_ERR_OOB);
-            t = 0;
-        }
-        const RowStats sp = row_stats(p, b * R + a);
-        unsigned long long eq = 1, Sq = 1;
-        if (!p.draft_greedy) {
-            const RowStats sq = row_stats(p, b * R + B + 1 + a);
-            eq = sq.et;
-            Sq = sq.Sn;
-        }
-        const uint32_t U = philox_word(p.seed, (uint32_t)b, p.step, (uint32_t)a, 2u);
-        const unsigned __int128 lhs = (unsigned __int128)U * eq * sp.Sn;
-        const unsigned __int128 rhs = ((unsigned __int128)sp.et << 32) * Sq;
-        acc = lhs < rhs;
-    }
-    const unsigned rej = __ballot_sync(0xffffffffu, a < B && !acc);
-    return rej ? __ffs((int)rej) - 1 : B;
-}
-
 // The draw's weight of id v after `a` accepts: the bonus row's nucleus weight
 // (a == B) or the residual max(0, Ep_v Sq - Eq_v Sp) at position a.
 struct TokenDraw {
@@ -815,46 +753,53 @@ struct TokenDraw {
     float T, mp, mq;
     unsigned long long ksp, Sp, ksq, Sq;
     int bonus, dg, t;
-    DS_DEVINL unsigned __int128 operator()(int v) const {
-        const unsigned long long Ep = weight_of(prow[v], T, mp);
+    // from id v's target logit lp and draft logit lq (lq unused for the bonus
+    // row and a greedy draft)
+    DS_DEVINL unsigned __int128 of(float lp, float lq, int v) const {
+        const unsigned long long Ep = weight_of(lp, T, mp);
         const unsigned long long ep = key_of(Ep, v) >= ksp ? Ep : 0ull;
         if (bonus) return ep;
         unsigned long long eq;
         if (dg) {
             eq = (v == t) ? 1ull : 0ull;
         } else {
-            const unsigned long long Eq = weight_of(qrow[v], T, mq);
+            const unsigned long long Eq = weight_of(lq, T, mq);
             eq = key_of(Eq, v) >= ksq ? Eq : 0ull;
         }
         const unsigned __int128 x = (unsigned __int128)ep * Sq, y = (unsigned __int128)eq * Sp;
         return x > y ? x - y : (unsigned __int128)0;
     }
 };
-DS_DEVINL TokenDraw token_draw(const VerifyParams &p, int b, int a) {
-    const int B = p.B, V = p.V, R = ver_rows_per_seq(p);
-    TokenDraw d;
-    d.bonus = a == B;
-    d.dg = p.draft_greedy;
-    d.T = p.T;
-    const int pi = d.bonus ? B : a;
-    d.prow = p.P + ((size_t)b * (B + 1) + pi) * V;
-    const RowStats sp = row_stats(p, b * R + pi);
-    d.mp = sp.m;
-    d.ksp = sp.kstar;
-    d.Sp = sp.Sn;
-    d.qrow = p.ell + ((size_t)b * B + (d.bonus ? 0 : a)) * V;
-    d.t = d.bonus ? 0 : min(max(p.tokens[b * B + a], 0), V - 1);
-    d.mq = 0.f;
-    d.ksq = 0;
-    d.Sq = 1;
-    if (!d.bonus && !d.dg) {
-        const RowStats sq = row_stats(p, b * R + B + 1 + a);
-        d.mq = sq.m;
-        d.ksq = sq.kstar;
-        d.Sq = sq.Sn;
+
+// The weights of the contiguous run of ids [v0, v1), their logits loaded eight
+// ids at a time (a run costs one L2 round trip per eight ids, not one per id).
+// With `out`, stops at the first id whose running total (from `base`) exceeds
+// `target` and writes it there.
+constexpr int kRunBatch = 8;
+DS_DEVINL unsigned __int128 run_weights(const TokenDraw &d, int v0, int v1, unsigned __int128 base,
+                                        unsigned __int128 target, int32_t *out) {
+    unsigned __int128 cum = base;
+    const bool q = !d.bonus && !d.dg;
+    for (int g = v0; g < v1; g += kRunBatch) {
+        float lp[kRunBatch], lq[kRunBatch];
+#pragma unroll
+        for (int j = 0; j < kRunBatch; ++j) {
+            lp[j] = g + j < v1 ? __ldg(d.prow + g + j) : 0.f;
+            lq[j] = (q && g + j < v1) ? __ldg(d.qrow + g + j) : 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < kRunBatch; ++j) {
+            if (g + j >= v1) break;
+            cum += d.of(lp[j], lq[j], g + j);
+            if (out && cum > target) {
+                *out = g + j;
+                return cum;
+            }
+        }
     }
-    return d;
+    return cum;
 }
+
 // Slice x of kDrawSlices over [0, V).
 DS_DEVINL void draw_slice(int V, int x, int &lo, int &hi) {
     lo = (int)((long long)V * x / kDrawSlices);
@@ -872,26 +817,73 @@ DS_DEVINL unsigned long long *draw_parts(const VerifyParams &p) {
 // No CTA waits for another.
 __global__ void __launch_bounds__(256) verify_token_draw_kernel(VerifyParams p) {
     __shared__ DrawScan dsm;
+    __shared__ TokenDraw s_d;
     __shared__ int s_a, s_last, s_slice;
     __shared__ unsigned long long s_blo, s_bhi, s_tlo, s_thi;
     pdl_trigger();
     pdl_wait();
-    const int b = blockIdx.y, B = p.B;
-    int t = 0;
-    if (threadIdx.x < 32) {
-        const int a = token_accepts(p, b, t);
-        if (threadIdx.x == 0) s_a = a;
+    const int b = blockIdx.y, B = p.B, V = p.V, R = ver_rows_per_seq(p);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // Warp 0, lane j = position j: the accept test of every position and the
+    // draw's parameters in one round of loads (target row j's statistics for
+    // j <= B, the draft row's for j < B); the first reject (or B) picks the lane
+    // whose statistics the draw takes.
+    int tj = 0, a = 0;
+    if (warp == 0) {
+        RowStats sp{}, sq{};
+        int raw = 0;
+        if (lane <= B) sp = row_stats(p, b * R + lane);
+        if (lane < B) {
+            raw = p.tokens[b * B + lane];
+            tj = raw;
+            if (raw < 0 || raw >= V) {
+                set_error(p.err, DSPARK_ERR_OOB);
+                tj = 0;
+            }
+            if (!p.draft_greedy) sq = row_stats(p, b * R + B + 1 + lane);
+        }
+        bool acc = false;
+        if (lane < B) {
+            const unsigned long long eq = p.draft_greedy ? 1ull : sq.et, Sq = p.draft_greedy ? 1ull : sq.Sn;
+            const uint32_t U = philox_word(p.seed, (uint32_t)b, p.step, (uint32_t)lane, 2u);
+            const unsigned __int128 lhs = (unsigned __int128)U * eq * sp.Sn;
+            const unsigned __int128 rhs = ((unsigned __int128)sp.et << 32) * Sq;
+            acc = lhs < rhs;
+        }
+        const unsigned rej = __ballot_sync(0xffffffffu, lane < B && !acc);
+        a = rej ? __ffs((int)rej) - 1 : B;
+        if (lane == a) {
+            TokenDraw d;
+            d.bonus = a == B;
+            d.dg = p.draft_greedy;
+            d.T = p.T;
+            d.prow = p.P + ((size_t)b * (B + 1) + a) * V;
+            d.mp = sp.m;
+            d.ksp = sp.kstar;
+            d.Sp = sp.Sn;
+            d.qrow = p.ell + ((size_t)b * B + (d.bonus ? 0 : a)) * V;
+            d.t = d.bonus ? 0 : min(max(raw, 0), V - 1);
+            const bool q = !d.bonus && !d.dg;
+            d.mq = q ? sq.m : 0.f;
+            d.ksq = q ? sq.kstar : 0ull;
+            d.Sq = q ? sq.Sn : 1ull;
+            s_d = d;
+            s_a = a;
+        }
     }
     __syncthreads();
-    const int a = s_a;
-    const TokenDraw d = token_draw(p, b, a);
+    const TokenDraw d = s_d;
+    a = s_a;
+    // this CTA's slice of the vocabulary as one contiguous run per thread
     int lo, hi;
-    draw_slice(p.V, blockIdx.x, lo, hi);
-    unsigned __int128 acc = 0;
-    for (int v = lo + threadIdx.x; v < hi; v += blockDim.x) acc += d(v);
-    acc = warp_sum_u128(acc);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (lane == 0) u128_split(acc, dsm.wlo[warp], dsm.whi[warp]);
+    draw_slice(V, blockIdx.x, lo, hi);
+    const int per = (hi - lo + (int)blockDim.x - 1) / (int)blockDim.x;
+    int v0 = min(hi, lo + (int)threadIdx.x * per), v1 = min(hi, v0 + per);
+    unsigned __int128 run = run_weights(d, v0, v1, 0, 0, nullptr);
+    {
+        const unsigned __int128 ws = warp_sum_u128(run);
+        if (lane == 0) u128_split(ws, dsm.wlo[warp], dsm.whi[warp]);
+    }
     __syncthreads();
     unsigned long long *parts = draw_parts(p) + (size_t)b * kDrawSlices * 2;
     if (threadIdx.x == 0) {
@@ -908,8 +900,8 @@ __global__ void __launch_bounds__(256) verify_token_draw_kernel(VerifyParams p) 
     __threadfence();
     if (threadIdx.x == 0) p.draw_count[b] = 0u;
     // the outputs
-    if (threadIdx.x < 32) {
-        if (lane < a) p.out_tokens[b * (B + 1) + lane] = t;
+    if (warp == 0) {
+        if (lane < a) p.out_tokens[b * (B + 1) + lane] = tj;
         if (lane > a && lane <= B) p.out_tokens[b * (B + 1) + lane] = -1;
         if (lane == 0) p.accept_len[b] = a;
     }
@@ -918,6 +910,7 @@ __global__ void __launch_bounds__(256) verify_token_draw_kernel(VerifyParams p) 
     unsigned __int128 x = 0;
     if (c < kDrawSlices) x = u128_join(ldcg_u64(parts + 2 * c), ldcg_u64(parts + 2 * c + 1));
     const unsigned __int128 inc = warp_incl_u128(x);
+    __syncthreads();  // the warp totals above are read
     if (lane == 31) u128_split(inc, dsm.wlo[warp], dsm.whi[warp]);
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -939,8 +932,28 @@ __global__ void __launch_bounds__(256) verify_token_draw_kernel(VerifyParams p) 
         u128_split(ex, s_blo, s_bhi);
     }
     __syncthreads();
-    draw_slice(p.V, s_slice, lo, hi);
-    cta_pick(d, lo, hi, u128_join(s_blo, s_bhi), tg, p.out_tokens + b * (B + 1) + a, dsm);
+    // the target's slice again as runs: the thread whose run holds the target walks it
+    draw_slice(V, s_slice, lo, hi);
+    const int per2 = (hi - lo + (int)blockDim.x - 1) / (int)blockDim.x;
+    v0 = min(hi, lo + (int)threadIdx.x * per2);
+    v1 = min(hi, v0 + per2);
+    run = run_weights(d, v0, v1, 0, 0, nullptr);
+    const unsigned __int128 rinc = warp_incl_u128(run);
+    __syncthreads();  // the slice prefixes above are read
+    if (lane == 31) u128_split(rinc, dsm.wlo[warp], dsm.whi[warp]);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned __int128 s0 = u128_join(s_blo, s_bhi);
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
+            const unsigned __int128 y = u128_join(dsm.wlo[w], dsm.whi[w]);
+            u128_split(s0, dsm.wlo[w], dsm.whi[w]);
+            s0 += y;
+        }
+    }
+    __syncthreads();
+    const unsigned __int128 start = u128_join(dsm.wlo[warp], dsm.whi[warp]) + rinc - run;
+    if (v0 < v1 && run > 0 && start <= tg && tg < start + run)
+        run_weights(d, v0, v1, start, tg, p.out_tokens + b * (B + 1) + a);
 }
 
 // ---------------------------------------------------------------------------
@@ -979,9 +992,11 @@ struct BlockRow {
     unsigned long long kstar, S;
     ExactDivisor div;
     int onehot;  // -1: a spec row; else the one token of a greedy draft
-    DS_DEVINL double prob(int v, float T) const {
+    DS_DEVINL double prob(int v, float T) const { return onehot >= 0 ? (v == onehot ? 1.0 : 0.0) : prob_l(row[v], v, T); }
+    // from id v's logit l, already loaded
+    DS_DEVINL double prob_l(float l, int v, float T) const {
         if (onehot >= 0) return v == onehot ? 1.0 : 0.0;
-        const unsigned long long E = weight_of(row[v], T, m);
+        const unsigned long long E = weight_of(l, T, m);
         const unsigned long long e = key_of(E, v) >= kstar ? E : 0ull;
         return e ? exact_div(e, div) : 0.0;
     }
@@ -994,6 +1009,15 @@ DS_DEVINL unsigned __int128 block_term(const BlockRow &rp, const BlockRow &rq, d
     if (a == 0.0) return 0;
     const double x = pi == 1.0 ? a : __dmul_rn(pi, a);
     const double c = rq.prob(v, T);
+    return fx80(c == 0.0 ? x : __dsub_rn(x, c));
+}
+// The same from the logits of id v in the two rows, already loaded.
+DS_DEVINL unsigned __int128 block_term_l(const BlockRow &rp, const BlockRow &rq, double pi, float T, int v, float lp,
+                                         float lq) {
+    const double a = rp.prob_l(lp, v, T);
+    if (a == 0.0) return 0;
+    const double x = pi == 1.0 ? a : __dmul_rn(pi, a);
+    const double c = rq.prob_l(lq, v, T);
     return fx80(c == 0.0 ? x : __dsub_rn(x, c));
 }
 
@@ -1032,6 +1056,7 @@ DS_DEVINL BlockRow block_rowq(const VerifyParams &p, int b, int i) {
     return r;
 }
 constexpr int kMaxBlockRows = 17;  // block <= 16, plus the bonus row
+constexpr int kMassBatch = 5;      // pairs of ids whose logits a thread loads at once
 
 // Warp 0: pi_0..pi_B of sequence b into pis[] (pi_0 = 1,
 // pi_k = min(pi_{k-1} p_{k-1}(t_k) / q_{k-1}(t_k), 1)); the per-position ratios
@@ -1085,9 +1110,28 @@ __global__ void __launch_bounds__(256) verify_block_mass_kernel(VerifyParams p) 
     const BlockRow rp = block_rowp(p, b, i), rq = block_rowq(p, b, i);
     const int np = p.V / 2;
     const int lo = (int)((long long)blockIdx.x * np / gridDim.x), hi = (int)((long long)(blockIdx.x + 1) * np / gridDim.x);
+    // the thread's pairs of ids, their logits loaded kMassBatch pairs at a time
     unsigned __int128 acc = 0;
-    for (int pp = lo + threadIdx.x; pp < hi; pp += blockDim.x)
-        acc += block_term(rp, rq, pi, p.T, 2 * pp) + block_term(rp, rq, pi, p.T, 2 * pp + 1);
+    const bool lq_ = rq.onehot < 0;
+    for (int p0 = lo + (int)threadIdx.x; p0 < hi; p0 += (int)blockDim.x * kMassBatch) {
+        float lp[2 * kMassBatch], lq[2 * kMassBatch];
+#pragma unroll
+        for (int u = 0; u < kMassBatch; ++u) {
+            const int pp = p0 + (int)blockDim.x * u;
+            const bool in = pp < hi;
+            lp[2 * u] = in ? __ldg(rp.row + 2 * pp) : 0.f;
+            lp[2 * u + 1] = in ? __ldg(rp.row + 2 * pp + 1) : 0.f;
+            lq[2 * u] = (in && lq_) ? __ldg(rq.row + 2 * pp) : 0.f;
+            lq[2 * u + 1] = (in && lq_) ? __ldg(rq.row + 2 * pp + 1) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < kMassBatch; ++u) {
+            const int pp = p0 + (int)blockDim.x * u;
+            if (pp >= hi) break;
+            acc += block_term_l(rp, rq, pi, p.T, 2 * pp, lp[2 * u], lq[2 * u]) +
+                   block_term_l(rp, rq, pi, p.T, 2 * pp + 1, lp[2 * u + 1], lq[2 * u + 1]);
+        }
+    }
     acc = warp_sum_u128(acc);
     if ((threadIdx.x & 31) == 0) u128_split(acc, rlo[threadIdx.x >> 5], rhi[threadIdx.x >> 5]);
     __syncthreads();
@@ -1112,6 +1156,7 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_block_final_kernel(Verify
     __shared__ double s_pis[kMaxBlockRows];
     __shared__ int s_tau, s_plain, s_slice;
     __shared__ unsigned long long s_rlo, s_rhi, s_tlo, s_thi;
+    __shared__ unsigned long long s_mlo[kMaxBlockRows], s_mhi[kMaxBlockRows];
     __shared__ __align__(8) uint64_t s_bar;
     __shared__ volatile int s_fail;
     pdl_trigger();
@@ -1120,16 +1165,25 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_block_final_kernel(Verify
     const int b = blockIdx.y, B = p.B, V = p.V;
     const uint32_t rank = cluster_rank();
     const unsigned long long *ms = block_masses(p);
-    if (threadIdx.x < 32) {
-        block_pis(p, b, s_pis);
-        // masses of positions 0..B-1 (lane i) and the decisions (one lane each)
-        const int i = threadIdx.x;
-        unsigned __int128 Si = 0;
-        if (i < B) {
-            const unsigned long long *src = ms + ((size_t)(b * B + i) * kMassSlices) * 2;
-            for (int c = 0; c < kMassSlices; ++c) Si += u128_join(src[2 * c], src[2 * c + 1]);
+    {
+        // warp 1 + i: the mass S_i of position i < B from its 64 slice partials
+        // (two per lane, one round of loads), beside warp 0's pi chain
+        const int w = (int)(threadIdx.x >> 5) - 1, lane = threadIdx.x & 31;
+        static_assert(kMassSlices == 64, "two slices per lane");
+        if (w >= 0 && w < B) {
+            const unsigned long long *src = ms + ((size_t)(b * B + w) * kMassSlices) * 2;
+            const unsigned __int128 x = u128_join(src[4 * lane], src[4 * lane + 1]) +
+                                        u128_join(src[4 * lane + 2], src[4 * lane + 3]);
+            const unsigned __int128 S = warp_sum_u128(x);
+            if (lane == 0) u128_split(S, s_mlo[w], s_mhi[w]);
         }
-        __syncwarp();
+    }
+    if (threadIdx.x < 32) block_pis(p, b, s_pis);
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        // the decisions (one lane each)
+        const int i = threadIdx.x;
+        const unsigned __int128 Si = i < B ? u128_join(s_mlo[i], s_mhi[i]) : (unsigned __int128)0;
         bool eta = false;
         if (i >= 1 && i <= B) {
             const double pi_i = s_pis[i];
@@ -1156,7 +1210,6 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_block_final_kernel(Verify
             // the residual draw's target and the mass slice that holds it: lane l
             // holds slices 2l and 2l + 1; an inclusive scan of the lane totals
             // finds the first slice whose running mass exceeds the target
-            static_assert(kMassSlices == 64, "two slices per lane");
             const uint32_t W = philox_word(p.seed, (uint32_t)b, p.step, (uint32_t)tau, 3u) >> 8;
             const unsigned __int128 tg = (St * (unsigned __int128)(W & 0xFFFFFFu)) >> 24;
             const unsigned long long *src = ms + ((size_t)(b * B + tau) * kMassSlices) * 2;
