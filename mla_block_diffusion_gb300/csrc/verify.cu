@@ -92,6 +92,7 @@ constexpr int kGroupsK = kBinsK / kSub;
 constexpr int kHistBins = kBinsK > kBins0 ? kBinsK : kBins0;
 constexpr int kMaxGroups = kHistBins / kSub;
 constexpr int kCandCap = kVThreads;  // keys of the crossing bin ranked in one CTA
+static_assert(kHistBins >= kCandCap, "a CTA lists its crossing-bin keys in the merged-histogram space");
 constexpr int kMaxLevels = 8;        // level 0 + at most 5 refinements of the 44-bit residual key
 constexpr int kMassSlices = 64;      // CTAs per block-verification row for the residual masses (2 per lane of a warp)
 constexpr size_t kStageMax = 200 * 1024;  // largest staging of the draw rows in shared memory
@@ -431,10 +432,12 @@ __global__ void __launch_bounds__(kVThreads, 1) nucleus_rows_kernel(VerifyParams
     mx = block_max_u64(mx, red);
     if (t == 0) s_cmax = mx;
     cluster_sync();
+    if (warp == 0) {
+        // lane r reads CTA r's maximum
+        const unsigned long long m = warp_max_u64(lane < kVCl ? ld_peer_u64(&s_cmax, (uint32_t)lane) : 0ull);
+        if (lane == 0) st.m = ord2f((uint32_t)m);
+    }
     if (t == 0) {
-        unsigned long long m = 0;
-        for (int r = 0; r < kVCl; ++r) m = max(m, ld_peer_u64(&s_cmax, (uint32_t)r));
-        st.m = ord2f((uint32_t)m);
         st.above = 0;
         st.done = 0;
         st.Sn = 0;
@@ -538,26 +541,30 @@ __global__ void __launch_bounds__(kVThreads, 1) nucleus_rows_kernel(VerifyParams
         __syncthreads();
         if (st.done) break;
         if (level == 0) {
-            // gather the crossing bin's keys into rank 0: count them here, reserve
-            // a range of rank 0's slots with one atomic, tell every CTA the count
+            // gather the crossing bin's keys into rank 0: list them here (in the
+            // merged-histogram space, free until the ranking), reserve a range of
+            // rank 0's slots with one atomic, tell every CTA the count, copy the list
             if (t == 0) s_lcnt = 0;
             __syncthreads();
+            unsigned long long *lst = mw;
             for (int j = t; j < n; j += kVThreads) {
                 const float e = yv[j];
-                if (e >= st.elo && e < st.ehi) atomicAdd(&s_lcnt, 1u);
+                if (!(e >= st.elo && e < st.ehi)) continue;
+                const uint32_t slot = atomicAdd(&s_lcnt, 1u);
+                if (slot < (uint32_t)kCandCap) lst[slot] = key_of(weight_bits(e), lo + j);
             }
             __syncthreads();
             if (t == 0) {
                 s_base = atom_add_peer_u32(&s_cnt, 0u, s_lcnt);
                 for (int r = 0; r < kVCl; ++r) st_peer_u32(&s_counts[rank], (uint32_t)r, s_lcnt);
-                s_lcnt = 0;
             }
             __syncthreads();
-            for (int j = t; j < n; j += kVThreads) {
-                const float e = yv[j];
-                if (!(e >= st.elo && e < st.ehi)) continue;
-                const uint32_t slot = s_base + atomicAdd(&s_lcnt, 1u);
-                if (slot < (uint32_t)kCandCap) st_peer_u64(cand + slot, 0u, key_of(weight_bits(e), lo + j));
+            {
+                const uint32_t nl = min(s_lcnt, (uint32_t)kCandCap);
+                for (uint32_t i = t; i < nl; i += kVThreads) {
+                    const uint32_t slot = s_base + i;
+                    if (slot < (uint32_t)kCandCap) st_peer_u64(cand + slot, 0u, lst[i]);
+                }
             }
             cluster_sync();  // G: every key is in rank 0, every count in every CTA
             uint32_t N = 0;
@@ -745,6 +752,7 @@ DS_DEVINL bool stage_rows(float *dst0, const float *row0, float *dst1, const flo
 // CTA per sequence picks inside the slice that holds the target.
 // ---------------------------------------------------------------------------
 constexpr int kDrawSlices = 128;
+constexpr int kDrawThreads = 1024;  // a run of one or two ids per thread at V = 163,840
 
 // The draw's weight of id v after `a` accepts: the bonus row's nucleus weight
 // (a == B) or the residual max(0, Ep_v Sq - Eq_v Sp) at position a.
@@ -815,10 +823,11 @@ DS_DEVINL unsigned long long *draw_parts(const VerifyParams &p) {
 // zero by that CTA) makes the decisions, writes the outputs, finds the slice
 // that holds the draw's target floor(total * W24 / 2^24) and picks inside it.
 // No CTA waits for another.
-__global__ void __launch_bounds__(256) verify_token_draw_kernel(VerifyParams p) {
+__global__ void __launch_bounds__(kDrawThreads, 1) verify_token_draw_kernel(VerifyParams p) {
     __shared__ DrawScan dsm;
     __shared__ TokenDraw s_d;
     __shared__ int s_a, s_last, s_slice;
+    __shared__ uint32_t s_W;
     __shared__ unsigned long long s_blo, s_bhi, s_tlo, s_thi;
     pdl_trigger();
     pdl_wait();
@@ -869,6 +878,8 @@ __global__ void __launch_bounds__(256) verify_token_draw_kernel(VerifyParams p) 
             d.Sq = q ? sq.Sn : 1ull;
             s_d = d;
             s_a = a;
+            // the draw's uniform, needed only by the last CTA: formed here, off its path
+            s_W = philox_word(p.seed, (uint32_t)b, p.step, (uint32_t)a, a == B ? 4u : 3u) >> 8;
         }
     }
     __syncthreads();
@@ -886,52 +897,63 @@ __global__ void __launch_bounds__(256) verify_token_draw_kernel(VerifyParams p) 
     }
     __syncthreads();
     unsigned long long *parts = draw_parts(p) + (size_t)b * kDrawSlices * 2;
-    if (threadIdx.x == 0) {
-        unsigned __int128 tot = 0;
-        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += u128_join(dsm.wlo[w], dsm.whi[w]);
-        parts[2 * blockIdx.x] = (unsigned long long)tot;
-        parts[2 * blockIdx.x + 1] = (unsigned long long)(tot >> 64);
-        __threadfence();
-        const unsigned old = atomicAdd(p.draw_count + b, 1u);
-        s_last = old == (unsigned)(kDrawSlices - 1);
+    if (warp == 0) {  // the CTA's total from the warp totals, then the count
+        const int nw = (int)(blockDim.x >> 5);
+        const unsigned __int128 tot =
+            warp_sum_u128(lane < nw ? u128_join(dsm.wlo[lane], dsm.whi[lane]) : (unsigned __int128)0);
+        if (lane == 0) {
+            parts[2 * blockIdx.x] = (unsigned long long)tot;
+            parts[2 * blockIdx.x + 1] = (unsigned long long)(tot >> 64);
+            __threadfence();
+            const unsigned old = atomicAdd(p.draw_count + b, 1u);
+            s_last = old == (unsigned)(kDrawSlices - 1);
+        }
     }
     __syncthreads();
     if (!s_last) return;
     __threadfence();
-    if (threadIdx.x == 0) p.draw_count[b] = 0u;
-    // the outputs
     if (warp == 0) {
+        if (lane == 0) p.draw_count[b] = 0u;
+        // the outputs
         if (lane < a) p.out_tokens[b * (B + 1) + lane] = tj;
         if (lane > a && lane <= B) p.out_tokens[b * (B + 1) + lane] = -1;
         if (lane == 0) p.accept_len[b] = a;
-    }
-    // the slice totals' exclusive prefix (thread c: slice c), the target and its slice
-    const int c = threadIdx.x;
-    unsigned __int128 x = 0;
-    if (c < kDrawSlices) x = u128_join(ldcg_u64(parts + 2 * c), ldcg_u64(parts + 2 * c + 1));
-    const unsigned __int128 inc = warp_incl_u128(x);
-    __syncthreads();  // the warp totals above are read
-    if (lane == 31) u128_split(inc, dsm.wlo[warp], dsm.whi[warp]);
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        unsigned __int128 s0 = 0;
-        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
-            const unsigned __int128 y = u128_join(dsm.wlo[w], dsm.whi[w]);
-            u128_split(s0, dsm.wlo[w], dsm.whi[w]);
-            s0 += y;
+        // the target and its slice: lane l holds slices 4l .. 4l + 3
+        static_assert(kDrawSlices == 128, "four slices per lane");
+        unsigned __int128 x[4], sum = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int c = 4 * lane + k;
+            x[k] = u128_join(ldcg_u64(parts + 2 * c), ldcg_u64(parts + 2 * c + 1));
+            sum += x[k];
         }
-        const uint32_t W = philox_word(p.seed, (uint32_t)b, p.step, (uint32_t)a, a == B ? 4u : 3u) >> 8;
-        u128_split((s0 * (unsigned __int128)(W & 0xFFFFFFu)) >> 24, s_tlo, s_thi);
-        s_slice = kDrawSlices - 1;
+        const unsigned __int128 incl = warp_incl_u128(sum);
+        const unsigned __int128 total = shfl_u128(incl, 31);
+        const unsigned __int128 tg = (total * (unsigned __int128)(s_W & 0xFFFFFFu)) >> 24;
+        unsigned __int128 ex = incl - sum;
+        int cand = -1;
+        unsigned __int128 before = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            if (cand < 0 && x[k] > 0 && ex <= tg && tg < ex + x[k]) {
+                cand = 4 * lane + k;
+                before = ex;
+            }
+            ex += x[k];
+        }
+        const unsigned hit = __ballot_sync(0xffffffffu, cand >= 0);
+        const int src = hit ? __ffs((int)hit) - 1 : 0;
+        const int c = __shfl_sync(0xffffffffu, cand, src);
+        const unsigned __int128 bf = shfl_u128(before, src);
+        if (lane == 0) {
+            s_slice = hit ? c : -1;  // no slice when the total weight is zero
+            u128_split(bf, s_blo, s_bhi);
+            u128_split(tg, s_tlo, s_thi);
+        }
     }
     __syncthreads();
+    if (s_slice < 0) return;
     const unsigned __int128 tg = u128_join(s_tlo, s_thi);
-    const unsigned __int128 ex = u128_join(dsm.wlo[warp], dsm.whi[warp]) + inc - x;
-    if (c < kDrawSlices && x > 0 && ex <= tg && tg < ex + x) {
-        s_slice = c;
-        u128_split(ex, s_blo, s_bhi);
-    }
-    __syncthreads();
     // the target's slice again as runs: the thread whose run holds the target walks it
     draw_slice(V, s_slice, lo, hi);
     const int per2 = (hi - lo + (int)blockDim.x - 1) / (int)blockDim.x;
@@ -939,19 +961,14 @@ __global__ void __launch_bounds__(256) verify_token_draw_kernel(VerifyParams p) 
     v1 = min(hi, v0 + per2);
     run = run_weights(d, v0, v1, 0, 0, nullptr);
     const unsigned __int128 rinc = warp_incl_u128(run);
-    __syncthreads();  // the slice prefixes above are read
     if (lane == 31) u128_split(rinc, dsm.wlo[warp], dsm.whi[warp]);
     __syncthreads();
-    if (threadIdx.x == 0) {
-        unsigned __int128 s0 = u128_join(s_blo, s_bhi);
-        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
-            const unsigned __int128 y = u128_join(dsm.wlo[w], dsm.whi[w]);
-            u128_split(s0, dsm.wlo[w], dsm.whi[w]);
-            s0 += y;
-        }
-    }
-    __syncthreads();
-    const unsigned __int128 start = u128_join(dsm.wlo[warp], dsm.whi[warp]) + rinc - run;
+    // every warp forms its own exclusive prefix from the warp totals
+    const int nw = (int)(blockDim.x >> 5);
+    const unsigned __int128 wt = lane < nw ? u128_join(dsm.wlo[lane], dsm.whi[lane]) : (unsigned __int128)0;
+    const unsigned __int128 winc = warp_incl_u128(wt);
+    const unsigned __int128 wex = shfl_u128(winc - wt, warp);
+    const unsigned __int128 start = u128_join(s_blo, s_bhi) + wex + rinc - run;
     if (v0 < v1 && run > 0 && start <= tg && tg < start + run)
         run_weights(d, v0, v1, start, tg, p.out_tokens + b * (B + 1) + a);
 }
@@ -1392,7 +1409,7 @@ cudaError_t launch_verify(VerifyParams p, int grid, cudaStream_t st) {
         return launch_pdl_cluster(verify_block_final_kernel, dim3(kVCl, p.bs), dim3(kVThreads),
                                   p.stage ? stage2 / 2 : 0, st, kVCl, p);
     }
-    return launch_pdl(verify_token_draw_kernel, dim3(kDrawSlices, p.bs), dim3(256), 0, st, p);
+    return launch_pdl(verify_token_draw_kernel, dim3(kDrawSlices, p.bs), dim3(kDrawThreads), 0, st, p);
 }
 
 }  // namespace ds
