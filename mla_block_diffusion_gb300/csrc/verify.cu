@@ -662,26 +662,25 @@ DS_DEVINL void cluster_pick(WF weight, int r0, int r1, long long W24, unsigned _
     mine = warp_sum_u128(mine);
     if (lane == 0) u128_split(mine, ds_.wlo[warp], ds_.whi[warp]);
     __syncthreads();
-    if (threadIdx.x == 0) {
-        unsigned __int128 acc = 0;
-        for (int w = 0; w < kVWarps; ++w) {
-            const unsigned __int128 x = u128_join(ds_.wlo[w], ds_.whi[w]);
-            u128_split(acc, ds_.wlo[w], ds_.whi[w]);
-            acc += x;
-        }
-        u128_split(acc, ds_.tlo, ds_.thi);
+    static_assert(kVWarps == 32, "one warp total per lane");
+    if (warp == 0) {  // the warps' exclusive prefixes and the CTA's total
+        const unsigned __int128 x = u128_join(ds_.wlo[lane], ds_.whi[lane]);
+        const unsigned __int128 inc = warp_incl_u128(x);
+        u128_split(inc - x, ds_.wlo[lane], ds_.whi[lane]);
+        if (lane == 31) u128_split(inc, ds_.tlo, ds_.thi);
     }
     cluster_sync();  // every CTA's total is in its shared memory
-    if (threadIdx.x == 0) {
-        unsigned __int128 before = 0, total = 0;
-        for (int r = 0; r < kVCl; ++r) {
-            const unsigned __int128 x = u128_join(ld_peer_u64(&ds_.tlo, (uint32_t)r), ld_peer_u64(&ds_.thi, (uint32_t)r));
-            if (r < (int)rank) before += x;
-            total += x;
+    if (warp == 0) {  // lane r reads CTA r's total
+        const unsigned __int128 x =
+            lane < kVCl ? u128_join(ld_peer_u64(&ds_.tlo, (uint32_t)lane), ld_peer_u64(&ds_.thi, (uint32_t)lane))
+                        : (unsigned __int128)0;
+        const unsigned __int128 inc = warp_incl_u128(x);
+        const unsigned __int128 before = shfl_u128(inc - x, (int)rank), total = shfl_u128(inc, 31);
+        if (lane == 0) {
+            const unsigned __int128 tg = W24 >= 0 ? (total * (unsigned __int128)(W24 & 0xFFFFFF)) >> 24 : target;
+            u128_split(base + before, ds_.blo, ds_.bhi);
+            u128_split(tg, ds_.glo, ds_.ghi);
         }
-        const unsigned __int128 tg = W24 >= 0 ? (total * (unsigned __int128)(W24 & 0xFFFFFF)) >> 24 : target;
-        u128_split(base + before, ds_.blo, ds_.bhi);
-        u128_split(tg, ds_.glo, ds_.ghi);
     }
     cluster_sync();  // peers have read this CTA's total
     const unsigned __int128 tg = u128_join(ds_.glo, ds_.ghi);
@@ -1080,7 +1079,7 @@ constexpr int kMassBatch = 5;      // pairs of ids whose logits a thread loads a
 // come from the rows' statistics (one lane each), the chain from lane 0.
 DS_DEVINL void block_pis(const VerifyParams &p, int b, double *pis) {
     const int lane = threadIdx.x & 31, B = p.B, R = ver_rows_per_seq(p);
-    double a = 0.0, c = 1.0;
+    double a = 0.0, c = 1.0, ratio = 0.0;
     if (lane < B) {
         const RowStats sp = row_stats(p, b * R + lane);
         a = sp.et ? __ddiv_rn((double)sp.et, (double)sp.Sn) : 0.0;
@@ -1088,15 +1087,18 @@ DS_DEVINL void block_pis(const VerifyParams &p, int b, double *pis) {
             const RowStats sq = row_stats(p, b * R + B + 1 + lane);
             c = sq.et ? __ddiv_rn((double)sq.et, (double)sq.Sn) : 0.0;
         }
+        // p_k(t_k) / q_k(t_k) does not depend on the chain: every lane divides at once
+        if (c != 0.0) ratio = __ddiv_rn(a, c);
     }
     double pi = 1.0;
     if (lane == 0) pis[0] = 1.0;
     for (int k = 1; k <= B; ++k) {
         const double ak = __shfl_sync(0xffffffffu, a, k - 1), ck = __shfl_sync(0xffffffffu, c, k - 1);
+        const double rk = __shfl_sync(0xffffffffu, ratio, k - 1);
         if (ck == 0.0) {
             pi = (ak > 0.0 && pi > 0.0) ? 1.0 : 0.0;
         } else {
-            const double x = __dmul_rn(pi, __ddiv_rn(ak, ck));
+            const double x = __dmul_rn(pi, rk);
             pi = x < 1.0 ? x : 1.0;
         }
         if (lane == 0) pis[k] = pi;
@@ -1112,6 +1114,7 @@ DS_DEVINL unsigned long long *block_masses(const VerifyParams &p) {
 __global__ void __launch_bounds__(256) verify_block_mass_kernel(VerifyParams p) {
     __shared__ double s_pis[kMaxBlockRows];
     __shared__ unsigned long long rlo[8], rhi[8];
+    __shared__ BlockRow s_rows[2];
     pdl_trigger();
     pdl_wait();
     const int b = blockIdx.y / p.B, i = blockIdx.y % p.B;
@@ -1121,10 +1124,14 @@ __global__ void __launch_bounds__(256) verify_block_mass_kernel(VerifyParams p) 
             if (t0 < 0 || t0 >= p.V) set_error(p.err, DSPARK_ERR_OOB);
         }
         block_pis(p, b, s_pis);
+    } else if (threadIdx.x == 32) {  // the rows' divisors, beside the pi chain
+        s_rows[0] = block_rowp(p, b, i);
+    } else if (threadIdx.x == 64) {
+        s_rows[1] = block_rowq(p, b, i);
     }
     __syncthreads();
     const double pi = s_pis[i];
-    const BlockRow rp = block_rowp(p, b, i), rq = block_rowq(p, b, i);
+    const BlockRow rp = s_rows[0], rq = s_rows[1];
     const int np = p.V / 2;
     const int lo = (int)((long long)blockIdx.x * np / gridDim.x), hi = (int)((long long)(blockIdx.x + 1) * np / gridDim.x);
     // the thread's pairs of ids, their logits loaded kMassBatch pairs at a time
@@ -1174,6 +1181,7 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_block_final_kernel(Verify
     __shared__ int s_tau, s_plain, s_slice;
     __shared__ unsigned long long s_rlo, s_rhi, s_tlo, s_thi;
     __shared__ unsigned long long s_mlo[kMaxBlockRows], s_mhi[kMaxBlockRows];
+    __shared__ BlockRow s_rp[kMaxBlockRows], s_rq[kMaxBlockRows];
     __shared__ __align__(8) uint64_t s_bar;
     __shared__ volatile int s_fail;
     pdl_trigger();
@@ -1193,6 +1201,16 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_block_final_kernel(Verify
                                         u128_join(src[4 * lane + 2], src[4 * lane + 3]);
             const unsigned __int128 S = warp_sum_u128(x);
             if (lane == 0) u128_split(S, s_mlo[w], s_mhi[w]);
+        }
+        // warps B + 1 .. 31 (lane 0): the target rows 0..B and the draft rows
+        // 0..B-1 with their divisors, whichever position the decisions pick
+        if (w >= B && lane == 0) {
+            for (int j = w - B; j < 2 * B + 1; j += 31 - B) {
+                if (j <= B)
+                    s_rp[j] = block_rowp(p, b, j);
+                else
+                    s_rq[j - B - 1] = block_rowq(p, b, j - B - 1);
+            }
         }
     }
     if (threadIdx.x < 32) block_pis(p, b, s_pis);
@@ -1273,7 +1291,7 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_block_final_kernel(Verify
     __syncthreads();
     const int tau = s_tau;
     int32_t *dst = p.out_tokens + b * (B + 1) + tau;
-    const BlockRow rp = block_rowp(p, b, tau);
+    const BlockRow rp = s_rp[tau];
     const float T = p.T;
     if (s_plain) {
         const uint32_t W = philox_word(p.seed, (uint32_t)b, p.step, (uint32_t)tau, tau == B ? 4u : 3u) >> 8;
@@ -1294,7 +1312,7 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_block_final_kernel(Verify
         };
         cluster_draw(wf, V, W, dst, dsm);
     } else {
-        const BlockRow rq = block_rowq(p, b, tau);
+        const BlockRow rq = s_rq[tau];
         const double pi = s_pis[tau];
         auto wf = [&](int v) -> unsigned __int128 { return block_term(rp, rq, pi, T, v); };
         const int np = V / 2, c = s_slice;
