@@ -1073,6 +1073,7 @@ DS_DEVINL BlockRow block_rowq(const VerifyParams &p, int b, int i) {
 }
 constexpr int kMaxBlockRows = 17;  // block <= 16, plus the bonus row
 constexpr int kMassBatch = 5;      // pairs of ids whose logits a thread loads at once
+constexpr int kMassThreads = 512;
 
 // Warp 0: pi_0..pi_B of sequence b into pis[] (pi_0 = 1,
 // pi_k = min(pi_{k-1} p_{k-1}(t_k) / q_{k-1}(t_k), 1)); the per-position ratios
@@ -1108,12 +1109,17 @@ DS_DEVINL void block_pis(const VerifyParams &p, int b, double *pis) {
 DS_DEVINL unsigned long long *block_masses(const VerifyParams &p) {
     return p.scratch + kStatWords * (size_t)p.bs * ver_rows_per_seq(p);
 }
+// pi_0..pi_B of every sequence as double bits ([b * kMaxBlockRows + k]), after the draw's slice totals.
+DS_DEVINL unsigned long long *block_pi_words(const VerifyParams &p) {
+    return p.scratch + kStatWords * (size_t)p.bs * (2 * p.B + 1) + (size_t)p.bs * p.B * kMassSlices * 2 +
+           (size_t)p.bs * kDrawSlices * 2;
+}
 
 // Residual masses S_i = sum_x max(pi_i p_i(x) - q_i(x), 0) for i < B: grid
 // (kMassSlices, bs * B), one vocabulary slice per CTA.
-__global__ void __launch_bounds__(256) verify_block_mass_kernel(VerifyParams p) {
+__global__ void __launch_bounds__(kMassThreads) verify_block_mass_kernel(VerifyParams p) {
     __shared__ double s_pis[kMaxBlockRows];
-    __shared__ unsigned long long rlo[8], rhi[8];
+    __shared__ unsigned long long rlo[kMassThreads / 32], rhi[kMassThreads / 32];
     __shared__ BlockRow s_rows[2];
     pdl_trigger();
     pdl_wait();
@@ -1124,6 +1130,11 @@ __global__ void __launch_bounds__(256) verify_block_mass_kernel(VerifyParams p) 
             if (t0 < 0 || t0 >= p.V) set_error(p.err, DSPARK_ERR_OOB);
         }
         block_pis(p, b, s_pis);
+        __syncwarp();
+        // one CTA per sequence keeps the chain for the decisions
+        if (blockIdx.x == 0 && i == 0 && (int)threadIdx.x <= p.B)
+            block_pi_words(p)[(size_t)b * kMaxBlockRows + threadIdx.x] =
+                (unsigned long long)__double_as_longlong(s_pis[threadIdx.x]);
     } else if (threadIdx.x == 32) {  // the rows' divisors, beside the pi chain
         s_rows[0] = block_rowp(p, b, i);
     } else if (threadIdx.x == 64) {
@@ -1213,7 +1224,9 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_block_final_kernel(Verify
             }
         }
     }
-    if (threadIdx.x < 32) block_pis(p, b, s_pis);
+    // the pi chain as the residual-mass kernel formed it
+    if ((int)threadIdx.x <= B)
+        s_pis[threadIdx.x] = __longlong_as_double((long long)block_pi_words(p)[(size_t)b * kMaxBlockRows + threadIdx.x]);
     __syncthreads();
     if (threadIdx.x < 32) {
         // the decisions (one lane each)
@@ -1387,7 +1400,8 @@ __global__ void verify_greedy_finalize(const int32_t *__restrict__ tokens, int b
 // ---------------------------------------------------------------------------
 size_t verify_scratch_words(int bs, int B, int grid) {
     (void)grid;
-    return kStatWords * (size_t)bs * (2 * B + 1) + (size_t)bs * B * kMassSlices * 2 + (size_t)bs * kDrawSlices * 2;
+    return kStatWords * (size_t)bs * (2 * B + 1) + (size_t)bs * B * kMassSlices * 2 + (size_t)bs * kDrawSlices * 2 +
+           (size_t)bs * kMaxBlockRows;
 }
 
 bool verify_setup(int V) {
@@ -1422,7 +1436,7 @@ cudaError_t launch_verify(VerifyParams p, int grid, cudaStream_t st) {
     const size_t stage2 = (size_t)2 * max_part(p.V) * 4;
     p.stage = stage2 <= kStageMax ? 1 : 0;
     if (p.verify_mode == DSPARK_BLOCK) {
-        e = launch_pdl(verify_block_mass_kernel, dim3(kMassSlices, p.bs * p.B), dim3(256), 0, st, p);
+        e = launch_pdl(verify_block_mass_kernel, dim3(kMassSlices, p.bs * p.B), dim3(kMassThreads), 0, st, p);
         if (e != cudaSuccess) return e;
         return launch_pdl_cluster(verify_block_final_kernel, dim3(kVCl, p.bs), dim3(kVThreads),
                                   p.stage ? stage2 / 2 : 0, st, kVCl, p);
