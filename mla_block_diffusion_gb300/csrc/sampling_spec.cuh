@@ -44,7 +44,12 @@ DS_DEVINL uint32_t philox_word(unsigned long long seed, uint32_t seq, uint32_t s
 // ---------------------------------------------------------------------------
 DS_DEVINL float exp_hat(float x) {
     if (!(x >= -23.0f)) return 0.0f;
-    const float n = rintf(__fmul_rn(x, 1.44269502162933349609375f));
+    // n = rint(x * log2(e)) (ties to even) by adding and removing 1.5 * 2^23: for
+    // |x * log2(e)| < 2^22 the sum rounds to an integer and its low bits hold n
+    // (the same integer as rintf, off the conversion pipe)
+    const float t = __fadd_rn(__fmul_rn(x, 1.44269502162933349609375f), 12582912.0f);
+    const float n = __fsub_rn(t, 12582912.0f);
+    const int ni = __float_as_int(t) - 0x4B400000;
     float r = __fmaf_rn(-n, 0.693145751953125f, x);
     r = __fmaf_rn(-n, 1.428606765330187045037746429443359375e-06f, r);
     float p = 1.98412701138295233249664306640625e-04f;
@@ -55,7 +60,7 @@ DS_DEVINL float exp_hat(float x) {
     p = __fmaf_rn(p, r, 0.5f);
     p = __fmaf_rn(p, r, 1.0f);
     p = __fmaf_rn(p, r, 1.0f);
-    return __fmul_rn(p, __int_as_float(((int)n + 127) << 23));
+    return __fmul_rn(p, __int_as_float((ni + 127) << 23));
 }
 
 // y = l / T, IEEE division (T == 1 gives l itself, bit for bit, without the division).
