@@ -776,11 +776,16 @@ dspark_status dspark_draft_block(dspark_handle_t *h, float *x, const dspark_kv_t
     GemmPending *const want_o = defer ? &pend_o : nullptr, *const want_x = defer ? &pend_x : nullptr;
     for (int l = 0; l < g.n_layers; ++l) {
         const dspark_layer_weights_t &W = h->w.layers[l];
+        // The block's first kernel releases the rest only after its dependency wait:
+        // the latent norms, q absorption, attention and combine read ctx_len, the page
+        // table and the pool before their own waits, and a cache append launched
+        // earlier may still be writing them until then.
+        const bool first = l == 0;
         if (defer)
             RUN(launch_rmsnorm_cluster(x, g.hidden, &pend_x, true, W.attn_norm, g.hidden, g.eps, hn, g.hidden, nullptr,
-                                       0, M, err, s));
+                                       0, M, err, s, first));
         else
-            RUN(launch_rmsnorm(x, g.hidden, W.attn_norm, g.hidden, g.eps, hn, g.hidden, nullptr, 0, M, err, s));
+            RUN(launch_rmsnorm(x, g.hidden, W.attn_norm, g.hidden, g.eps, hn, g.hidden, nullptr, 0, M, err, s, first));
         // q_b's weights stream into L2 while the latency-bound q_a || kv_a GEMM runs
         const L2Prefetch pf_qb = mat_prefetch(W.w_q_b, g.weight_format, (uint64_t)g.n_heads * qhd, g.q_lora);
         RUN(gemm(h, h->qkv_a[l], nullptr, h->b_hn, g.q_lora + kvd, g.hidden, M, EPI_STORE, qkv, nullptr,

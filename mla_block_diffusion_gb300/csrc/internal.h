@@ -30,8 +30,10 @@ struct AttnParams {
     int *err;
 };
 
+// late: release the dependent kernels only after this kernel's own dependency
+// wait (the first kernel of a draft block)
 cudaError_t launch_rmsnorm(const float *x, int ldx, const float *g, int H, float eps, __nv_bfloat16 *y, int ldy,
-                           float *y32, int ldy32, int M, int *err, cudaStream_t st);
+                           float *y32, int ldy32, int M, int *err, cudaStream_t st, bool late = false);
 cudaError_t launch_latent(const float *qkv, int ld, int q_lora, int kv_lora, int d_rope, const float *g_q,
                           const float *g_kv, float eps, const int32_t *ctx_len, int block, int max_ctx,
                           const RopeTable &rt, __nv_bfloat16 *cq, __nv_bfloat16 *blk_kv, int M, int *err,
@@ -47,7 +49,7 @@ cudaError_t launch_q_absorb(const float *q, int M, int n_h, int d_nope, int d_ro
 bool row_cluster_fits(int H);
 cudaError_t launch_rmsnorm_cluster(float *x, int ldx, const GemmPending *pend, bool add, const float *g, int H,
                                    float eps, __nv_bfloat16 *y, int ldy, float *y32, int ldy32, int M, int *err,
-                                   cudaStream_t st);
+                                   cudaStream_t st, bool late = false);
 cudaError_t launch_latent_cluster(const float *qkv, int ld, const GemmPending *pend, int q_lora, int kv_lora,
                                   int d_rope, const float *g_q, const float *g_kv, float eps, const int32_t *ctx_len,
                                   int block, int max_ctx, const RopeTable &rt, __nv_bfloat16 *cq,

@@ -41,15 +41,19 @@ __device__ float block_sum(float v, float *red) {
 // RMSNorm: y = x / sqrt(mean(x^2) + eps) * g, written as bf16 (GEMM operand)
 // and optionally fp32. One CTA per row; H a multiple of 4. The gains are read
 // before the wait on the producing kernel; the first 4 * blockDim float4 of the
-// row stay in registers between the two passes.
+// row stay in registers between the two passes. With `late` (the first kernel
+// of a draft block) the kernel releases its dependents only after its own
+// dependency wait: the block's later kernels read the context lengths, page
+// table and latent pool before their waits, and an earlier cache append may
+// still be writing them until that wait returns.
 // ---------------------------------------------------------------------------
 constexpr int kNormThreads = 512;
 
 __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const float *__restrict__ x, int ldx,
                                                                const float *__restrict__ g, int H, float eps,
                                                                __nv_bfloat16 *__restrict__ y, int ldy,
-                                                               float *__restrict__ y32, int ldy32, int *err) {
-    pdl_trigger();
+                                                               float *__restrict__ y32, int ldy32, int *err, int late) {
+    if (!late) pdl_trigger();
     __shared__ float red[33];
     const int m = blockIdx.x, n4 = H / 4;
     const float4 *xr = (const float4 *)(x + (size_t)m * ldx);
@@ -61,6 +65,7 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const float *__re
         gr[u] = i < n4 ? __ldg(g4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     pdl_wait();
+    if (late) pdl_trigger();
     float ss = 0.f;
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -252,8 +257,8 @@ DS_DEVINL float4 row_value(const float4 *row, const GemmPending &pend, const Pen
 // Grid (kRowCl, M); H a multiple of 4.
 __global__ void __launch_bounds__(kRowClThreads) rmsnorm_cluster_kernel(
     float *__restrict__ x, int ldx, GemmPending pend, int add, const float *__restrict__ g, int H, float eps,
-    __nv_bfloat16 *__restrict__ y, int ldy, float *__restrict__ y32, int ldy32, int *err) {
-    pdl_trigger();
+    __nv_bfloat16 *__restrict__ y, int ldy, float *__restrict__ y32, int ldy32, int *err, int late) {
+    if (!late) pdl_trigger();  // (late: as in rmsnorm_kernel)
     __shared__ float2 red[33];
     __shared__ float2 s_parts[kRowCl];
     __shared__ __align__(8) uint64_t s_bar;
@@ -274,6 +279,7 @@ __global__ void __launch_bounds__(kRowClThreads) rmsnorm_cluster_kernel(
     if (threadIdx.x == 0) s_fail = 0;
     cluster_sum_setup(&s_bar);
     pdl_wait();
+    if (late) pdl_trigger();
     float4 *xr = (float4 *)(x + (size_t)m * ldx);
     float4 v[kRowVals];
     float ss = 0.f;
@@ -1293,9 +1299,9 @@ __global__ void ctx_advance_kernel(int32_t *__restrict__ ctx_len, const int32_t 
 // Host-side launch wrappers
 // ---------------------------------------------------------------------------
 cudaError_t launch_rmsnorm(const float *x, int ldx, const float *g, int H, float eps, __nv_bfloat16 *y, int ldy,
-                           float *y32, int ldy32, int M, int *err, cudaStream_t st) {
+                           float *y32, int ldy32, int M, int *err, cudaStream_t st, bool late) {
     return launch_pdl(rmsnorm_kernel, dim3(M), dim3(kNormThreads), 0, st, x, ldx, g, H, eps, y, ldy, y32, ldy32,
-                      err);
+                      err, late ? 1 : 0);
 }
 
 cudaError_t launch_latent(const float *qkv, int ld, int q_lora, int kv_lora, int d_rope, const float *g_q,
@@ -1332,13 +1338,13 @@ bool row_cluster_fits(int H) {
 
 cudaError_t launch_rmsnorm_cluster(float *x, int ldx, const GemmPending *pend, bool add, const float *g, int H,
                                    float eps, __nv_bfloat16 *y, int ldy, float *y32, int ldy32, int M, int *err,
-                                   cudaStream_t st) {
+                                   cudaStream_t st, bool late) {
     if (!row_cluster_fits(H)) return cudaErrorInvalidValue;
     GemmPending pd;
     memset(&pd, 0, sizeof(pd));
     if (pend) pd = *pend;
     return launch_pdl_cluster(rmsnorm_cluster_kernel, dim3(kRowCl, M), dim3(kRowClThreads), 0, st, kRowCl, x, ldx,
-                              pd, add ? 1 : 0, g, H, eps, y, ldy, y32, ldy32, err);
+                              pd, add ? 1 : 0, g, H, eps, y, ldy, y32, ldy32, err, late ? 1 : 0);
 }
 
 cudaError_t launch_latent_cluster(const float *qkv, int ld, const GemmPending *pend, int q_lora, int kv_lora,
