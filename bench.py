@@ -158,6 +158,30 @@ def barrier(world):
         dist.barrier()
 
 
+def job_figures(ms_step: float, e2e_ms_step: float, world: int, bs: int, block: int) -> dict:
+    """Whole-job figures of N replicas from the per-step times (already the
+    maximum over ranks): every rank drafts bs blocks per step at once, so the job
+    spends ms_step / N per block and drafts block * bs * N tokens per step."""
+    return {"us_per_block": ms_step * 1e3 / world, "e2e_us_per_block": e2e_ms_step * 1e3 / world,
+            "drafted_tokens_per_s": block * bs * world / (ms_step * 1e-3)}
+
+
+def run_config(w, ctx_list, world: int, draft_mode: int, verify_mode: int, T: float, top_p: float, fmt: str,
+               total_bytes: int) -> dict:
+    """The JSON line's config: the workload and its replicas."""
+    G, bs = w.geom, w.bs
+    max_ctx = max(ctx_list)
+    return {"workload": w.name, "model": "DSpark drafter (Kimi-K3 geometry), random init",
+            "global_batch": bs * world, "blocks_per_step": bs * world,
+            "seq_len": max_ctx if bs == 1 else f"{min(ctx_list)}..{max_ctx} (mean {statistics.mean(ctx_list):.0f})",
+            "block": G.block, "draft": MODE_NAMES[draft_mode], "verify": MODE_NAMES[verify_mode],
+            "temperature": T if (draft_mode or verify_mode) else None,
+            "top_p": top_p if (draft_mode or verify_mode) else None, "weights": fmt,
+            "rope": "yarn-16 from 65536" if G.yarn_factor > 1 else "plain",
+            "parallelism": f"replicas{world}",
+            "l2": f"no flush: working set {total_bytes / 1e9:.2f} GB per step > 129 MB L2"}
+
+
 def max_over_ranks(x: float, world: int) -> float:
     if world == 1:
         return x
@@ -381,15 +405,7 @@ def main():
     max_ctx = max(ctx_list)
     bs = w.bs
     ab = algorithmic_bytes(G, ctx_list, bs=bs, fmt=args.format)
-    config = {"workload": w.name, "model": "DSpark drafter (Kimi-K3 geometry), random init",
-              "global_batch": bs * world, "blocks_per_step": bs * world,
-              "seq_len": max_ctx if bs == 1 else f"{min(ctx_list)}..{max_ctx} (mean {statistics.mean(ctx_list):.0f})",
-              "block": G.block, "draft": MODE_NAMES[draft_mode], "verify": MODE_NAMES[verify_mode],
-              "temperature": T if (draft_mode or verify_mode) else None,
-              "top_p": top_p if (draft_mode or verify_mode) else None, "weights": args.format,
-              "rope": "yarn-16 from 65536" if G.yarn_factor > 1 else "plain",
-              "parallelism": f"replicas{world}",
-              "l2": f"no flush: working set {ab['total'] / 1e9:.2f} GB per step > 129 MB L2"}
+    config = run_config(w, ctx_list, world, draft_mode, verify_mode, T, top_p, args.format, ab["total"])
 
     if args.only == "fc":
         return only_fc(args, G, world, rank, local)
@@ -621,18 +637,18 @@ def main():
     accept = acc.cpu().tolist()
 
     gpu_launches_per_step = ds_launches_per_step(ds, bs=bs, draft_mode=draft_mode, verify_mode=verify_mode)
-    us = ms * 1e3 / world  # whole job: every rank runs its own step
+    jf = job_figures(ms, e2e_ms, world, bs, G.block)  # whole job: every rank runs its own step
     line = {
-        "metric": METRIC, "value": us, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": ms, "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic", "config": config,
-        "drafted_tokens_per_s": G.block * bs * world / (ms * 1e-3),
+        "metric": METRIC, "value": jf["us_per_block"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic", "config": config,
+        "drafted_tokens_per_s": jf["drafted_tokens_per_s"],
         "hbm": {"algorithmic_bytes_per_step": ab["total"], "achieved_TBps": ab["total"] / (ms * 1e-3) / 1e12,
                 "frac_of_peak": ab["total"] / (ms * 1e-3) / 1e9 / hbm, "peak_GBps": hbm, "peak_source": src,
                 "frac_of_8TBps": ab["total"] / (ms * 1e-3) / 8e12},
         "roofline": roofline,
         "clocks": clocks,
-        "e2e": {"value": e2e_ms * 1e3 / world, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "e2e": {"value": jf["e2e_us_per_block"], "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": gpu_launches_per_step * args.steps,
         "accept_len": accept if bs <= 8 else {"histogram_0_to_7": np.bincount(np.asarray(accept), minlength=G.block + 1)
                                                                      .tolist()},
