@@ -21,7 +21,10 @@
  *    error word inside the workspace; read it with dspark_check().
  *  - Every pointer passed to a kernel must be 16-byte aligned.
  *  - A handle is used by one stream at a time; calls that share a workspace
- *    must be ordered on one stream.
+ *    must be ordered on one stream. Stream order is all the ordering needed:
+ *    the kernels overlap their neighbours' tails (programmatic dependent
+ *    launch), but each reads what an earlier call wrote (the cache append's
+ *    pages and ctx_len included) only after that call has completed.
  *  - The workspace is caller-allocated (dspark_workspace_bytes) and must be
  *    zero-filled once before its first use; the kernels keep its counters at
  *    zero afterwards. After dspark_check() reports DSPARK_ERR_TIMEOUT the
